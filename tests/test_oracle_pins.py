@@ -1,0 +1,532 @@
+"""Pins for the CPU oracle: values the pages print, closed forms, invariants
+and library cross-checks, chosen so that a plausible slip in the oracle (a
+dropped field, a wrong group index, a transposed operand, reciprocal instead
+of division, half-away rounding) fails at least one of them.
+
+Page citations: [cortiq] = docs.rs cortiq-engine 0.8.49 kv_cache.rs;
+[rswa] = franken_ocr 0.8.0 src/native_engine/rswa.rs.
+"""
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+from conftest import load_golden
+
+f32 = np.float32
+
+
+def bits_to_f32(b: int) -> np.float32:
+    return np.frombuffer(np.uint32(b).tobytes(), np.float32)[0]
+
+
+# ---------------------------------------------------------------- quantiser
+
+def test_ties_to_even_rswa_vector():
+    """[rswa] test int8_row_quantization_uses_ties_to_even, verbatim."""
+    g = load_golden("quant_ties_to_even.txt")
+    row = np.zeros(int(g["width"]), f32)
+    head = np.array(g["row_head"].split(), f32)
+    row[: head.size] = head
+    want = np.array(g["codes_head"].split(), np.int8)
+    q, s = oracle.quantize_row_i8(row)
+    assert np.array_equal(q[: want.size], want)
+    assert s.view(np.uint32) == int(g["scale_bits"], 16)
+
+
+@pytest.mark.parametrize("group", [32, 128])
+def test_ties_to_even_q8_2f_row(group):
+    """The same vector through the q8_2f quantiser ([cortiq] quant_row): absmax
+    127 puts the scale at 1.0, above the 1e-12 floor, so the tie rule alone
+    decides the codes (half away from zero would give 1, 2, 3, 4 ...)."""
+    g = load_golden("quant_ties_to_even.txt")
+    row = np.zeros(128, f32)
+    head = np.array(g["row_head"].split(), f32)
+    row[: head.size] = head
+    want = np.array(g["codes_head"].split(), np.int8)
+    q, s = oracle.quant_row(row, None, group)
+    assert np.array_equal(q[: want.size], want)
+    assert s[0].view(np.uint32) == int(g["scale_bits"], 16)
+
+
+def test_division_not_reciprocal_rswa_fixture():
+    """[rswa] test int8_row_quantization_divides_instead_of_multiplying_by_reciprocal."""
+    g = load_golden("quant_division.txt")
+    row = np.zeros(int(g["width"]), f32)
+    row[0] = bits_to_f32(int(g["x0_bits"], 16))
+    row[1] = bits_to_f32(int(g["x1_bits"], 16))
+    q, s = oracle.quantize_row_i8(row)
+    assert list(q[:2]) == [int(c) for c in g["codes"].split()]
+    recip = np.rint(row[1] * (f32(1.0) / s))  # the formula the page rules out
+    assert int(recip) == int(g["reciprocal_code1"])
+
+
+def test_division_not_reciprocal_q8_2f_scaled():
+    """The page fixture sits below the q8_2f 1e-12 scale floor, so it is scaled by
+    2^67 (exact in f32: every quotient and scale scales by the same power of two)
+    to bring it into the q8_2f quantiser's range; the codes must not change."""
+    g = load_golden("quant_division.txt")
+    row = np.zeros(128, f32)
+    row[0] = bits_to_f32(int(g["x0_bits"], 16))
+    row[1] = bits_to_f32(int(g["x1_bits"], 16))
+    scaled = (row * f32(2.0 ** 67)).astype(f32)
+    assert np.array_equal(scaled / f32(2.0 ** 67), row)  # the scaling is exact
+    for group in (32, 128):
+        q, s = oracle.quant_row(scaled, None, group)
+        assert list(q[:2]) == [int(c) for c in g["codes"].split()]
+        assert int(np.rint(scaled[1] * (f32(1.0) / s[0]))) == int(g["reciprocal_code1"])
+
+
+def test_quantiser_lcg_sweep_matches_numpy_f32():
+    """[rswa] test int8_row_quantization_matches_scalar_contract: 256 rows from the
+    page's LCG over magnitudes 2^-20..2^20 (row 0 all zero).  Expected codes come
+    from numpy's own f32 division and np.rint (IEEE round-half-even), an
+    implementation independent of the C oracle; both quantisers are checked."""
+    state = 0xD1B54A32D192ED03
+    mask = (1 << 64) - 1
+    for case in range(256):
+        mag = f32(2.0) ** f32((case % 41) - 20)
+        row = np.zeros(128, f32)
+        for i in range(128):
+            state = (state * 6364136223846793005 + 1442695040888963407) & mask
+            unit = f32((state >> 40) & 0xFFFFFFFF) / f32((1 << 24) - 1)
+            row[i] = (unit * f32(2.0) - f32(1.0)) * mag
+        if case == 0:
+            row[:] = 0.0
+        absmax = np.max(np.abs(row))
+        # rswa mirror: scale 1.0 for an all-zero row
+        sc = absmax / f32(127.0) if absmax > 0 else f32(1.0)
+        want = np.clip(np.rint(row / sc), -127, 127).astype(np.int8)
+        q, s = oracle.quantize_row_i8(row)
+        assert s.view(np.uint32) == f32(sc).view(np.uint32), case
+        assert np.array_equal(q, want), case
+        # q8_2f (cortiq): per 32-channel group, scale floored at 1e-12
+        q2, s2 = oracle.quant_row(row, None, 32)
+        for gi in range(4):
+            seg = row[gi * 32:(gi + 1) * 32]
+            sg = max(np.max(np.abs(seg)) / f32(127.0), f32(1e-12))
+            assert s2[gi].view(np.uint32) == f32(sg).view(np.uint32), (case, gi)
+            assert np.array_equal(q2[gi * 32:(gi + 1) * 32],
+                                  np.clip(np.rint(seg / f32(sg)), -127, 127).astype(np.int8))
+
+
+def test_quantiser_floor_and_zero_group():
+    """[cortiq] quant_row: scale = max(absmax/127, 1e-12); an all-zero group takes
+    the floor (not rswa's 1.0) and codes 0; a group below the floor quantises
+    against the floor."""
+    row = np.zeros(128, f32)
+    row[40] = 1e-14
+    row[64:96] = np.linspace(-3, 3, 32, dtype=f32)
+    q, s = oracle.quant_row(row, None, 32)
+    assert s[0] == f32(1e-12) and not q[:32].any()
+    assert s[1] == f32(1e-12)
+    assert q[40] == int(np.rint(f32(1e-14) / f32(1e-12)))
+    assert s[2] == f32(3.0) / f32(127.0)
+    assert q[64] == -127 and q[95] == 127
+
+
+def test_quantiser_col_division_and_half_scale_bound():
+    """The benchmark spec pin: dequantised rows reproduce the originals within scale/2 per
+    element; with a per-channel field the residual x/col is what is quantised."""
+    x = synthetic.normal((50, 128), 11) * synthetic.channel_sigma((128,), 12)
+    col = synthetic.channel_sigma((128,), 13)
+    for r in x:
+        q, s = oracle.quant_row(r, None, 32)
+        deq = q.astype(np.float64) * np.repeat(s, 32)
+        assert np.all(np.abs(deq - r) <= np.repeat(s, 32) / 2 * (1 + 1e-6))
+        q, s = oracle.quant_row(r, col, 32)
+        resid = (r / col).astype(f32)
+        deq = q.astype(np.float64) * np.repeat(s, 32)
+        assert np.all(np.abs(deq - resid) <= np.repeat(s, 32) / 2 * (1 + 1e-6))
+        # V-style: one group over the whole row
+        q, s = oracle.quant_row(r, col, 128)
+        assert s.size == 1
+        assert np.all(np.abs(q * np.float64(s[0]) - resid) <= s[0] / 2 * (1 + 1e-6))
+
+
+# ------------------------------------------------------------------- freeze
+
+def _integer_rows(n, hd, seed):
+    """Rows of integers whose every 32-channel group peaks at exactly 127, so the
+    pre-freeze q8 codes equal the values and the scale is 1.0 in every group."""
+    r = synthetic.rng(seed)
+    x = r.integers(-126, 127, size=(n, hd)).astype(f32)
+    for g0 in range(0, hd, 32):
+        x[np.arange(n), g0 + r.integers(0, 32, size=n)] = 127.0
+    return x
+
+
+def test_freeze_col_is_exact_channel_rms():
+    """[cortiq] freeze_cols: col[d] = max(sqrt(sum_p row^2 / n), 1e-6).  With
+    integer rows the f32 sum of squares is exact (< 2^24), /64 is exact, so col
+    must equal the correctly rounded sqrt of the exact integer mean square."""
+    hd = 128
+    x = _integer_rows(64, hd, 21)
+    c = oracle.OracleSeqCache(oracle.Q8, 1, hd, 80)
+    for p in range(64):
+        c.append(x[p][None], x[p][None])
+    assert not c.frozen and c.needs_freeze()
+    assert np.array_equal(c.kq[0, :64], x.astype(np.int8))
+    sumsq = (x.astype(np.int64) ** 2).sum(axis=0)
+    want = np.sqrt(sumsq.astype(np.float64) / 64.0).astype(f32)  # double rounding is safe for sqrt
+    c.freeze()
+    assert np.array_equal(c.kcol[0], want)
+    assert np.array_equal(c.vcol[0], want)
+
+
+def test_freeze_trigger_is_start_of_65th_append():
+    """[cortiq] append: the freeze runs at the START of an append once seq_len >=
+    KV_COL_WARMUP (64) and no field is set; after exactly 64 rows the cache is
+    still unfrozen, the 65th append freezes over the first 64 rows."""
+    hd, n_kv = 64, 2
+    sig = synthetic.channel_sigma((n_kv, hd), 31)
+    k = synthetic.outlier_rows(70, n_kv, hd, sig, 32)
+    v = synthetic.outlier_rows(70, n_kv, hd, sig, 33)
+    c = oracle.OracleSeqCache(oracle.Q8, n_kv, hd, 80)
+    for p in range(64):
+        c.append(k[p], v[p])
+    assert not c.frozen and np.all(c.kcol == 1.0)
+    c.append(k[64], v[64])
+    assert c.frozen and c.seq_len == 65
+    # the field is the RMS of the 64 dequantised rows, not of 65
+    ref = oracle.OracleSeqCache(oracle.Q8, n_kv, hd, 80)
+    for p in range(64):
+        ref.append(k[p], v[p])
+    deq = np.stack([[ref.row(h, p, False) for p in range(64)] for h in range(n_kv)])
+    rms = np.sqrt((deq.astype(np.float32) ** 2).astype(np.float64).mean(axis=1))
+    assert np.allclose(c.kcol, rms, rtol=1e-5)
+
+
+def test_freeze_requantised_rows_stay_within_compound_bound():
+    """Rows requantised at the freeze are re-read from their dequantised values, so
+    relative to the ORIGINAL input the error is bounded by s/2 + s'*col/2 (the
+    bound compounds); rows appended after the freeze are quantised once against
+    col and obey s'*col/2."""
+    hd = 128
+    sig = synthetic.channel_sigma((1, hd), 41)
+    k = synthetic.outlier_rows(100, 1, hd, sig, 42)
+    c = oracle.OracleSeqCache(oracle.Q8K, 1, hd, 128)
+    pre = oracle.OracleSeqCache(oracle.Q8K, 1, hd, 128)
+    for p in range(100):
+        c.append(k[p], k[p])
+        if p < 64:
+            pre.append(k[p], k[p])
+    col = c.kcol[0].astype(np.float64)
+    for p in range(100):
+        s_new = np.repeat(c.ks[0, p], 32).astype(np.float64)
+        err = np.abs(c.row(0, p, False) - k[p, 0])
+        if p < 64:
+            s_old = np.repeat(pre.ks[0, p], 32).astype(np.float64)
+            assert np.all(err <= s_old / 2 + s_new * col / 2 + 1e-5 * np.abs(k[p, 0]))
+        else:
+            assert np.all(err <= s_new * col / 2 * (1 + 1e-5) + 1e-6 * np.abs(k[p, 0]))
+
+
+def test_page_channel_structure_and_q8_grid_tolerance():
+    """[cortiq] test q8_attend_matches_f32_within_grid, with the page's hash rows
+    (even channels x4, odd x1/4), its query and its tolerances.  The frozen K
+    field must also follow the 16:1 even/odd channel RMS ratio."""
+    g = load_golden("q8_grid.txt")
+    heads, hd, P = int(g["heads"]), int(g["hd"]), int(g["positions"])
+
+    def synth(p, salt):
+        i = np.arange(heads * hd)
+        x = ((i * 31 + p * 17 + salt * 7 + 3) % 97).astype(f32) / f32(97.0) - f32(0.5)
+        return np.where(i % 2 == 0, x * f32(4.0), x * f32(0.25)).astype(f32).reshape(heads, hd)
+
+    fc = oracle.OracleSeqCache(oracle.F32, heads, hd, P)
+    qc = oracle.OracleSeqCache(oracle.Q8, heads, hd, P)
+    for p in range(P):
+        k, v = synth(p, 1), synth(p, 2)
+        fc.append(k, v)
+        qc.append(k, v)
+    assert qc.frozen
+    ratio = qc.kcol[:, 0::2].mean() / qc.kcol[:, 1::2].mean()
+    assert 12.0 < ratio < 20.0
+    q = (((np.arange(hd) * 13 + 5) % 89).astype(f32) / f32(89.0) - f32(0.5)).astype(f32)
+    scale = f32(1.0) / f32(math.sqrt(hd))
+    for kvh in range(heads):
+        of, pf = fc.attend_head(q, kvh, scale)
+        o8, p8 = qc.attend_head(q, kvh, scale)
+        m = max(np.max(np.abs(of)), 1e-6)
+        assert np.all(np.abs(of - o8) <= m * float(g["out_rel_tol"]) + float(g["out_abs_tol"]))
+        assert np.all(np.abs(pf - p8) < float(g["prob_tol"]))
+    assert qc.memory_bytes() * int(g["memory_factor"]) < fc.memory_bytes()
+
+
+# ------------------------------------------------------------ layout/memory
+
+def test_layout_and_memory_page_values():
+    """[cortiq] tests append_tracks_seq_len_and_layout and dead_head_stores_nothing."""
+    g = load_golden("cortiq_memory.txt")
+    H, hd = int(g["layout_heads"]), int(g["layout_hd"])
+    c = oracle.OracleSeqCache(oracle.F32, H, hd, 4)
+    k = np.arange(H * hd, dtype=f32).reshape(H, hd)
+    c.append(k, np.full((H, hd), 2.0, f32))
+    assert c.seq_len == 1 and c.head_rows[0] == 1
+    assert np.array_equal(c.k[1, 0], k[1])
+    assert c.memory_bytes() == int(g["layout_bytes"])
+    H, hd = int(g["dead_heads"]), int(g["dead_hd"])
+    c = oracle.OracleSeqCache(oracle.F32, H, hd, 4, alive=[1, 0])
+    for _ in range(2):
+        c.append(np.ones((H, hd), f32), np.full((H, hd), 2.0, f32))
+    assert c.seq_len == 2 and c.head_rows[0] == 2 and c.head_rows[1] == 0
+    assert c.memory_bytes() == int(g["dead_bytes"])
+
+
+@pytest.mark.parametrize("hd,lo,hi", [(128, 3.70, 3.72), (64, 3.65, 3.67)])
+def test_q8_memory_ratio(hd, lo, hi):
+    """[cortiq] KvMode doc: q8_2f is ~3.7x smaller than f32.  Per position per head:
+    f32 = 8*hd bytes; q8 = 2*hd codes + 4*(hd/32) K scales + 4 V scale."""
+    g = load_golden("cortiq_memory.txt")
+    n = 4096
+    fc = oracle.OracleSeqCache(oracle.F32, 1, hd, n)
+    qc = oracle.OracleSeqCache(oracle.Q8, 1, hd, n)
+    # memory_bytes only counts rows, so fill head_rows directly (no values needed)
+    fc.head_rows[0] = n
+    qc.head_rows[0] = n
+    ratio = fc.memory_bytes() / qc.memory_bytes()
+    assert lo < ratio < hi
+    assert abs(ratio - float(g["q8_ratio_approx"])) < 0.06
+
+
+# ---------------------------------------------------------------- attention
+
+def _softmax_ref(q, K, V, scale):
+    """Library cross-check: scipy's softmax over numpy f64 scores."""
+    from scipy.special import softmax
+
+    w = softmax(np.float64(scale) * (K @ q.astype(np.float64)))
+    return w @ V, w
+
+
+@pytest.mark.parametrize("mode", [oracle.F32, oracle.Q8, oracle.Q8K, oracle.Q8V])
+def test_attend_matches_scipy_on_dequantised_rows(mode):
+    hd, n_kv, hpk, L = 64, 2, 3, 90
+    sig = synthetic.channel_sigma((n_kv, hd), 51)
+    k = synthetic.outlier_rows(L, n_kv, hd, sig, 52)
+    v = synthetic.outlier_rows(L, n_kv, hd, sig, 53)
+    c = oracle.OracleSeqCache(mode, n_kv, hd, L)
+    c.append_rows(k, v)
+    q = synthetic.normal((n_kv * hpk, hd), 54)
+    scale = f32(1.0) / f32(math.sqrt(hd))
+    imp = np.zeros(L, np.float64)
+    out = c.decode(q, n_kv * hpk, scale, imp)
+    imp_ref = np.zeros(L)
+    for h in range(n_kv * hpk):
+        g = h // hpk
+        K, V = c.dequant(g, False), c.dequant(g, True)
+        o, w = _softmax_ref(q[h], K, V, scale)
+        assert np.allclose(out[h], o, rtol=1e-12, atol=1e-12)
+        imp_ref += w
+    assert np.allclose(imp, imp_ref, rtol=1e-12, atol=1e-15)
+    # weights sum to one per head -> imp sums to the number of live Q heads
+    assert abs(imp.sum() - n_kv * hpk) < 1e-9
+    if mode == oracle.F32:  # f32 rows are used as stored
+        assert np.array_equal(c.dequant(1, False), k[:, 1].astype(np.float64))
+
+
+def test_dead_group_zero_output_and_untouched_imp():
+    hd, n_kv, hpk, L = 32, 4, 2, 20
+    alive = [1, 0, 1, 0]
+    c = oracle.OracleSeqCache(oracle.Q8, n_kv, hd, L, alive=alive)
+    c.append_rows(synthetic.normal((L, n_kv, hd), 61), synthetic.normal((L, n_kv, hd), 62))
+    assert c.head_rows.tolist() == [L, 0, L, 0]
+    imp = np.full(L, 0.25)
+    out = c.decode(synthetic.normal((n_kv * hpk, hd), 63), n_kv * hpk, f32(0.125), imp)
+    assert not out[2:4].any() and not out[6:8].any()
+    assert abs(imp.sum() - (0.25 * L + 2 * hpk)) < 1e-9
+
+
+def test_grouped_equals_per_head_bitwise():
+    """[cortiq] test attend_group_equals_per_head_attend_bitexact (oracle side)."""
+    hd, n_kv, hpk, L = 32, 2, 3, 70
+    for mode in (oracle.F32, oracle.Q8):
+        c = oracle.OracleSeqCache(mode, n_kv, hd, L)
+        c.append_rows(synthetic.normal((L, n_kv, hd), 71), synthetic.normal((L, n_kv, hd), 72))
+        q = synthetic.normal((n_kv * hpk, hd), 73)
+        for g in range(n_kv):
+            imp = np.zeros(L)
+            out = c.attend_group(q[g * hpk:(g + 1) * hpk], g, f32(0.17), imp)
+            imp_ref = np.zeros(L)
+            for h in range(hpk):
+                o, p = c.attend_head(q[g * hpk + h], g, f32(0.17))
+                assert np.array_equal(out[h], o)
+                imp_ref += p
+            assert np.array_equal(imp, imp_ref)
+
+
+def test_closed_forms_single_key_and_equal_scores():
+    """1 key -> its V; equal scores -> the mean of the V rows (for any query)."""
+    c = oracle.OracleSeqCache(oracle.F32, 1, 16, 4)
+    c.append(np.eye(16, dtype=f32)[0][None], np.full((1, 16), 7.0, f32))
+    out, p = c.attend_head(np.arange(16, dtype=f32), 0, f32(0.25))
+    assert np.all(out == 7.0) and p.tolist() == [1.0]
+    c.append(np.eye(16, dtype=f32)[0][None], np.full((1, 16), 4.0, f32))
+    c2 = oracle.OracleSeqCache(oracle.F32, 1, 16, 4)
+    c2.append(np.eye(16, dtype=f32)[0][None], np.full((1, 16), 2.0, f32))
+    c2.append(np.eye(16, dtype=f32)[0][None], np.full((1, 16), 4.0, f32))
+    out, p = c2.attend_head(np.full(16, 3.0, f32), 0, f32(0.25))
+    assert np.allclose(out, 3.0, rtol=0, atol=1e-15) and np.allclose(p, 0.5)
+
+
+# ------------------------------------------------------------------- R-SWA
+
+H, HD, W = 10, 128, 128
+
+
+def _fill(seq, f):
+    out = np.zeros((H, seq, HD), f32)
+    for r in range(seq):
+        for d in range(HD):
+            out[:, r, d] = f(r, d)
+    return out
+
+
+def _token(f):
+    out = np.zeros((H, HD), f32)
+    for d in range(HD):
+        out[:, d] = f(d)
+    return out
+
+
+def _rswa_state(cap):
+    return (np.zeros((H, cap, HD), f32), np.zeros((H, cap, HD), f32),
+            np.zeros((H, W, HD), f32), np.zeros((H, W, HD), f32), np.zeros(2, np.int32))
+
+
+def test_rswa_page_closed_forms():
+    g = load_golden("rswa_closed_forms.txt")
+    assert (int(g["num_heads"]), int(g["head_dim"]), int(g["ring_window"])) == (H, HD, W)
+    scale = f32(1.0) / f32(math.sqrt(HD))
+    e0 = lambda r, d: 1.0 if d == 0 else 0.0
+    # single key
+    rk, rv, gk, gv, cur = _rswa_state(8)
+    rk[:, :1] = _fill(1, e0)
+    rv[:, :1] = 7.0
+    out = oracle.rswa_decode(_token(lambda d: 5.0 if d == 0 else 0.0), rk, rv, 1, gk, gv, 0, scale)
+    assert np.all(np.abs(out - float(g["single_key_value"])) < float(g["single_key_tol"]))
+    # equal scores
+    rk, rv, gk, gv, cur = _rswa_state(8)
+    rk[:, :2] = _fill(2, e0)
+    rv[:, :2] = _fill(2, lambda r, d: 2.0 if r == 0 else 4.0)
+    out = oracle.rswa_decode(_token(lambda d: 3.0 if d == 0 else 0.0), rk, rv, 2, gk, gv, 0, scale)
+    assert np.all(np.abs(out - float(g["equal_scores_value"])) < float(g["equal_scores_tol"]))
+    # write-then-attend (the query sees its own ring token)
+    rk, rv, gk, gv, cur = _rswa_state(8)
+    rk[:, :1] = _fill(1, lambda r, d: 1.0 if d == 1 else 0.0)
+    rv[:, :1] = 1.0
+    slot = oracle.rswa_write(gk, gv, _token(lambda d: 1.0 if d == 0 else 0.0),
+                             _token(lambda d: 5.0), True, cur)
+    assert slot == 0 and cur[0] == 1
+    out = oracle.rswa_decode(_token(lambda d: 10.0 if d == 0 else 0.0), rk, rv, 1, gk, gv, cur[0], scale)
+    approx = float(g["ring_entry_approx"])
+    assert np.all(np.abs(out - approx) < 1e-3) and np.all(out > 3.0)
+    w = math.exp(10.0 / math.sqrt(128.0))
+    assert np.all(np.abs(out - (w * 5 + 1) / (w + 1)) < float(g["ring_entry_tol"]))
+
+
+def test_rswa_online_fold_matches_two_pass():
+    """[rswa] test online_matches_naive_softmax: the streaming fold (f32, page
+    order) and the materialised two-pass definition agree within 1e-4."""
+    g = load_golden("rswa_closed_forms.txt")
+    m = 5
+    keys = _fill(m, lambda r, d: float(r + 1) if d == 0 else 0.0)[0]
+    vals = _fill(m, lambda r, d: r + d * 0.01)[0]
+    q = np.zeros(HD, f32)
+    q[0] = 0.5
+    scale = f32(1.0) / f32(math.sqrt(HD))
+    online = oracle.online_head(q, keys, vals, scale)
+    rk, rv, gk, gv, _ = _rswa_state(16)
+    rk[:, :m] = keys
+    rv[:, :m] = vals
+    two_pass = oracle.rswa_decode(np.tile(q, (H, 1)), rk, rv, m, gk, gv, 0, scale)[0]
+    assert abs(online[0] - two_pass[0]) < float(g["online_vs_naive_tol"])
+    assert np.max(np.abs(online - two_pass)) < 1e-5
+
+
+def test_rswa_cursor_sequence():
+    g = load_golden("ring_cursors.txt")
+    rk, rv, gk, gv, cur = _rswa_state(4)
+    for step in range(W):
+        slot = oracle.rswa_write(gk, gv, _token(lambda d: float(step)), _token(lambda d: 0.0), True, cur)
+        assert slot == step and cur[0] == step + 1
+        # write_decode_step doc: during warm-up ring_pos tracks ring_len (mod W)
+        assert cur[1] == (step + 1) % W
+    assert cur[1] == int(g["warm_ring_pos_after_w"])
+    slots, pos = [], []
+    for _ in range(2):
+        slots.append(oracle.rswa_write(gk, gv, _token(lambda d: 99.0), _token(lambda d: 99.0), True, cur))
+        pos.append(int(cur[1]))
+    assert slots == [int(s) for s in g["steady_slots"].split()]
+    assert pos == [int(s) for s in g["steady_ring_pos"].split()]
+    assert cur[0] == W and gk[0, 0, 0] == 99.0
+    for expect in list(range(2, W)) + [0, 1]:
+        assert oracle.rswa_write(gk, gv, _token(lambda d: 0.0), _token(lambda d: 0.0), True, cur) == expect
+    assert cur[1] == 2
+
+
+def test_rswa_errors():
+    rk, rv, gk, gv, cur = _rswa_state(4)
+    with pytest.raises(RuntimeError):
+        oracle.rswa_write(gk, gv, _token(lambda d: 1.0), _token(lambda d: 1.0), False, cur)
+    assert cur.tolist() == [0, 0]
+    with pytest.raises(RuntimeError):
+        oracle.rswa_decode(_token(lambda d: 1.0), rk, rv, None, gk, gv, 0, f32(0.1))
+    with pytest.raises(RuntimeError):
+        oracle.rswa_decode(_token(lambda d: 1.0), rk, rv, 0, gk, gv, 0, f32(0.1))
+
+
+def rope(x, pos, base=10000.0):
+    """Standard pairwise rotary embedding of the last axis at absolute position pos
+    (test harness only: the pages leave RoPE to the caller)."""
+    hd = x.shape[-1]
+    i = np.arange(hd // 2, dtype=np.float64)
+    th = pos * base ** (-2.0 * i / hd)
+    c, s = np.cos(th), np.sin(th)
+    a, b = x[..., 0::2].astype(np.float64), x[..., 1::2].astype(np.float64)
+    out = np.empty(x.shape, np.float64)
+    out[..., 0::2] = a * c - b * s
+    out[..., 1::2] = a * s + b * c
+    return out.astype(f32)
+
+
+def test_rswa_steady_state_is_prefix_plus_last_w_with_absolute_rope():
+    """R-SWA module doc: after the ring wraps, decode equals brute-force attention
+    over prefix ++ the last W generated rows (in logical order), with RoPE at
+    the TRUE absolute position.  A slot-indexed RoPE must fail (teeth)."""
+    m, steps = 37, 500
+    prefix_k = synthetic.normal((H, m, HD), 81)
+    prefix_v = synthetic.normal((H, m, HD), 82)
+    gen_k = synthetic.normal((steps, H, HD), 83)
+    gen_v = synthetic.normal((steps, H, HD), 84)
+    q_raw = synthetic.normal((H, HD), 85)
+    scale = f32(1.0) / f32(math.sqrt(HD))
+    pk = np.stack([rope(prefix_k[:, r], r) for r in range(m)], axis=1)
+    outs = {}
+    for variant in ("absolute", "slot"):
+        rk, rv, gk, gv, cur = _rswa_state(m)
+        rk[:] = pk
+        rv[:] = prefix_v
+        for t in range(steps):
+            slot_next = cur[0] if cur[0] < W else cur[1]
+            pos = m + t if variant == "absolute" else m + slot_next
+            oracle.rswa_write(gk, gv, rope(gen_k[t], pos), gen_v[t], True, cur)
+        assert cur.tolist() == [W, steps % W] == [128, 116]
+        qpos = m + steps - 1
+        outs[variant] = oracle.rswa_decode(rope(q_raw, qpos), rk, rv, m, gk, gv, cur[0], scale)
+    # brute force, logical order, absolute positions
+    from scipy.special import softmax
+
+    keep = range(steps - W, steps)
+    ref = np.zeros((H, HD))
+    for h in range(H):
+        K = np.concatenate([pk[h], np.stack([rope(gen_k[t, h], m + t) for t in keep])]).astype(np.float64)
+        V = np.concatenate([prefix_v[h], gen_v[list(keep), h]]).astype(np.float64)
+        w = softmax(np.float64(scale) * (K @ rope(q_raw, m + steps - 1)[h].astype(np.float64)))
+        ref[h] = w @ V
+    assert np.allclose(outs["absolute"], ref, rtol=1e-10, atol=1e-12)
+    assert np.max(np.abs(outs["slot"] - ref)) > 1e-3
