@@ -1,0 +1,224 @@
+/*
+ * kvd.h -- C ABI of the GB300 KV-cache decode-attention library.
+ *
+ * One process, one GPU (sm_103a).  Every device buffer is allocated by the
+ * caller (by any CUDA allocator) and passed in as a plain pointer;
+ * the library computes the sizes, never allocates device memory and keeps
+ * no global state.  Every call is asynchronous on the caller's CUDA stream
+ * (`stream` is a cudaStream_t passed as void*, NULL = legacy default
+ * stream) unless its comment says otherwise.
+ *
+ * Errors.  Every entry point returns a kvd_status.  Arguments are checked
+ * on the host BEFORE anything is launched or mutated: a call that returns
+ * an error other than KVD_ECUDA has changed neither the cache contents nor
+ * the host-mirrored cursors.  KVD_ECUDA reports a failed CUDA launch or
+ * copy (the stream is then in an unknown state).  Kernels never trap: an
+ * inconsistency they detect (a bound violated by corrupt metadata, a wait
+ * that timed out) sets a device error word that kvd_layer_device_error /
+ * rswa_device_error read back after the caller synchronises.
+ *
+ * Sources (page title, then the item on the page):
+ *   cortiq  = docs.rs cortiq-engine 0.8.49, src/cortiq_engine/kv_cache.rs
+ *   rswa    = franken_ocr 0.8.0, src/native_engine/rswa.rs
+ */
+#ifndef KVD_H
+#define KVD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KVD_API __attribute__((visibility("default")))
+#else
+#define KVD_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Storage mode of one layer (cortiq KvMode): KVD_F32 stores f32 K and V;
+ * KVD_Q8 (q8_2f) stores int8 K with one f32 scale per 32 channels and int8
+ * V with one f32 scale per row, both against per-channel fields frozen
+ * after 64 rows; KVD_Q8K quantises K only, KVD_Q8V V only. */
+typedef enum { KVD_F32 = 0, KVD_Q8 = 1, KVD_Q8K = 2, KVD_Q8V = 3 } kvd_mode;
+
+typedef enum {
+    KVD_OK = 0,
+    KVD_EINVAL = -1,    /* malformed argument (null pointer, bad size/shape) */
+    KVD_ECAPACITY = -2, /* a sequence or ring would exceed its capacity      */
+    KVD_ESTATE = -3,    /* call not valid in the current state (no prefill)  */
+    KVD_EEMPTY = -4,    /* empty attention key set                           */
+    KVD_ECUDA = -5,     /* a CUDA launch or copy failed                      */
+    KVD_EDEVICE = -6    /* the device error word was set by a kernel         */
+} kvd_status;
+
+/* Device buffers of one layer, indexed by these slots in the size array of
+ * kvd_layer_bytes and the pointer array of kvd_layer_init.  A slot whose
+ * size is 0 for the chosen mode takes a NULL pointer. */
+enum {
+    KVD_BUF_K = 0,    /* f32  K rows            (KVD_F32, KVD_Q8V)          */
+    KVD_BUF_V = 1,    /* f32  V rows            (KVD_F32, KVD_Q8K)          */
+    KVD_BUF_KQ = 2,   /* int8 K codes           (KVD_Q8, KVD_Q8K)           */
+    KVD_BUF_VQ = 3,   /* int8 V codes           (KVD_Q8, KVD_Q8V)           */
+    KVD_BUF_KS = 4,   /* f32  K scale per 32 ch (KVD_Q8, KVD_Q8K)           */
+    KVD_BUF_VS = 5,   /* f32  V scale per row   (KVD_Q8, KVD_Q8V)           */
+    KVD_BUF_KCOL = 6, /* f32  K channel field [n_seq][n_live][hd]           */
+    KVD_BUF_VCOL = 7, /* f32  V channel field [n_seq][n_live][hd]           */
+    KVD_BUF_META = 8, /* library metadata (row offsets, lengths, flags)    */
+    KVD_BUF_COUNT = 9
+};
+
+/* Layer descriptor.  Caller-allocated (host memory, plain bytes), filled by
+ * kvd_layer_init and then owned by the library until the caller frees it;
+ * its contents are private.  It mirrors on the host every length the
+ * kernels need, so no call reads device memory back. */
+typedef struct kvd_layer {
+    uint64_t opaque[48];
+} kvd_layer;
+
+/* Sizes of a layer's buffers (cortiq LayerKvCache: one contiguous region
+ * per live KV head per sequence, rows of head_dim values).
+ *   n_seq      sequences in the batch (each is its own conversation);
+ *   n_kv       KV heads; head_dim 64 or 128;
+ *   mode       kvd_mode;
+ *   capacity   host [n_seq], the most rows each sequence may ever hold
+ *              (rounded up to a multiple of 16 internally);
+ *   alive      host [n_kv], 0 = dead KV head (stores nothing, its query
+ *              heads produce zeros), NULL = all alive;
+ *   bytes_out  host [KVD_BUF_COUNT] device bytes per slot (0 = unused);
+ *   host_bytes_out  bytes of the host state block kvd_layer_init needs.
+ * Layout of every row buffer: sequence-major, then live head, then row:
+ * [seq][live head][row][...], sequence b occupying n_live * cap_b rows. */
+KVD_API kvd_status kvd_layer_bytes(int32_t n_seq, int32_t n_kv, int32_t head_dim, int32_t mode,
+                           const int64_t *capacity, const uint8_t *alive,
+                           int64_t *bytes_out, int64_t *host_bytes_out);
+
+/* Bind L to caller buffers (device pointers in dev_bufs[KVD_BUF_COUNT],
+ * each 256-byte aligned, sized by kvd_layer_bytes; host_state of
+ * host_bytes_out bytes) and clear every sequence: length 0, fields unset
+ * (stored as 1.0).  Enqueues the metadata upload and field reset on
+ * `stream`; host_state must stay alive and unmoved while L is in use. */
+KVD_API kvd_status kvd_layer_init(kvd_layer *L, int32_t n_seq, int32_t n_kv, int32_t head_dim,
+                          int32_t mode, const int64_t *capacity, const uint8_t *alive,
+                          void *const *dev_bufs, void *host_state, void *stream);
+
+/* cortiq clear: forget sequence `seq` (or every sequence, seq = -1): length
+ * 0, fields unset.  Row contents are left in place and never read again. */
+KVD_API kvd_status kvd_layer_reset(kvd_layer *L, int32_t seq, void *stream);
+
+/* Host-mirrored state: rows stored by sequence `seq`, and whether its
+ * channel fields are frozen.  Synchronous, reads no device memory. */
+KVD_API kvd_status kvd_layer_seq_len(const kvd_layer *L, int32_t seq, int64_t *len_out,
+                             int32_t *frozen_out);
+
+/* cortiq memory_bytes summed over the batch: f32 rows, scales and frozen
+ * fields at 4 bytes, int8 codes at 1 byte, for the rows currently stored. */
+KVD_API kvd_status kvd_layer_memory_bytes(const kvd_layer *L, int64_t *bytes_out);
+
+/* cortiq LayerKvCache::append (+ quant_row), batched over sequences.
+ *   k, v   device f32 [sum n_new][n_kv][head_dim]: the new rows of sequence
+ *          0, then of sequence 1, ...; dead heads' slices are ignored;
+ *   n_new  host [n_seq] rows appended per sequence, or NULL for one row
+ *          each (k, v then hold [n_seq][n_kv][head_dim]).
+ * Each row of a quantised component is divided by its channel field (1
+ * before the freeze) and coded per group: scale = max(absmax/127, 1e-12),
+ * code = clamp(round_half_even(r / scale), -127, 127), f32 IEEE throughout.
+ * Semantics are those of appending the rows one at a time: the freeze of
+ * kv_freeze_colfield runs before the first row appended while the sequence
+ * holds >= 64 rows with its fields unset.  KVD_ECAPACITY if any sequence
+ * would exceed its capacity (nothing is appended then). */
+KVD_API kvd_status kv_append(kvd_layer *L, const float *k, const float *v, const int32_t *n_new,
+                     void *stream);
+
+/* cortiq freeze_cols for every sequence that holds >= 64 rows and has no
+ * field yet (a no-op for the others and for KVD_F32): per live head and
+ * quantised component, dequantise the stored rows, col[d] = max(sqrt(
+ * sum_p row[p][d]^2 / n), 1e-6) in row order with IEEE rounding of every
+ * operation, then requantise every stored row against col.  Idempotent. */
+KVD_API kvd_status kv_freeze_colfield(kvd_layer *L, void *stream);
+
+/* Workspace bytes decode_attention needs for n_q query heads (with_imp != 0
+ * adds the score buffer the imp pass uses).  Depends only on the layer's
+ * shape and capacities, so one allocation serves every later call. */
+KVD_API kvd_status kvd_decode_workspace_bytes(const kvd_layer *L, int32_t n_q, int32_t with_imp,
+                                      int64_t *bytes_out);
+
+/* Single-token GQA decode attention over the layer (cortiq attend_group
+ * over every KV group): query head h reads KV head h / (n_q / n_kv);
+ *   out[b][h] = sum_p softmax_p(scale * <q[b][h], K^[p]>) V^[p]
+ * over the rows stored for sequence b, with K^ = code * scale * kcol, V^ =
+ * code * scale * vcol for quantised components.  Split over the SMs by
+ * position chunks (flash-decoding) and merged by log-sum-exp.
+ *   q    device f32 [n_seq][n_q][head_dim];  out device f32, same shape;
+ *   imp  device f32 or NULL: imp[imp_off(b) + p] += sum over live query
+ *        heads of their softmax weight on row p (cortiq accumulate_imp);
+ *        imp_off(b) = sum of the (16-rounded) capacities of the sequences
+ *        before b, so imp holds sum_b cap_b floats;
+ *   workspace  device, >= kvd_decode_workspace_bytes(L, n_q, imp != NULL).
+ * Dead groups and empty sequences give zeros and leave imp unchanged.
+ * n_q must be a multiple of n_kv with n_q / n_kv <= 16. */
+KVD_API kvd_status decode_attention(const float *q, const kvd_layer *L, int32_t n_q, float scale,
+                            float *out, float *imp, void *workspace, int64_t workspace_bytes,
+                            void *stream);
+
+/* Device error word of the layer (0 = clean), copied back synchronously;
+ * clear != 0 resets it.  Bit 0: a bounded wait timed out; bit 1: a kernel
+ * found metadata out of range and skipped the access. */
+KVD_API kvd_status kvd_layer_device_error(const kvd_layer *L, int32_t clear, uint32_t *word_out);
+
+/* ---- R-SWA (rswa module): retained prefix + W-slot ring, per stream ----
+ * Per stream s and head h the reference block is ref[s][h][0..ref_cap) and
+ * the ring ring[s][h][0..W), rows of head_dim f32 (head-major, as rswa
+ * RingCache keeps them).  Cursors live on the host, one int32 per stream:
+ * prefill_len (< 0 = no prefill recorded), ring_len, ring_pos. */
+
+/* rswa RingCache::record_prefill for stream `s`: copy k, v (device f32
+ * [H][seq][head_dim]) into the reference block and reset the stream's ring
+ * (ring_len = ring_pos = 0).  KVD_ECAPACITY if seq > ref_cap. */
+KVD_API kvd_status rswa_record_prefill(float *ref_k, float *ref_v, const float *k, const float *v,
+                               int32_t s, int32_t seq, int32_t B, int32_t H, int32_t head_dim,
+                               int64_t ref_cap, int32_t W, int32_t *prefill_len,
+                               int32_t *ring_len, int32_t *ring_pos, void *stream);
+
+/* rswa RingCache::write_decode_step for every stream at once: stream s
+ * writes its token (k, v device f32 [B][H][head_dim], already rotated at
+ * the true absolute position by the caller) into slot ring_len[s] while
+ * ring_len < W (then ring_len += 1, ring_pos = ring_len % W) and into slot
+ * ring_pos[s] afterwards (then ring_pos = (ring_pos + 1) % W).  Cursors are
+ * host arrays updated in place; slot_out (host [B] or NULL) gets each
+ * stream's slot.  KVD_ESTATE if any stream has no prefill (nothing written). */
+KVD_API kvd_status rswa_ring_write(float *ring_k, float *ring_v, const float *k, const float *v,
+                           const int32_t *prefill_len, int32_t *ring_len, int32_t *ring_pos,
+                           int32_t B, int32_t H, int32_t head_dim, int32_t W,
+                           int32_t *slot_out, void *stream);
+
+/* Workspace bytes rswa_decode needs. */
+KVD_API kvd_status rswa_decode_workspace_bytes(int32_t B, int32_t H, int32_t head_dim,
+                                       int64_t ref_cap, int32_t W, int64_t *bytes_out);
+
+/* rswa decode_attention for every stream: per (stream, head) softmax over
+ * reference rows [0, prefill_len) followed by ring rows [0, ring_len),
+ * no mask, scale `scale`; out device f32 [B][H * head_dim].  ring_pos is
+ * accepted for the cursor contract only (attention over the ring does not
+ * depend on the order of its slots).  KVD_ESTATE if a stream has no
+ * prefill, KVD_EEMPTY if one has no keys.  ws >= rswa_decode_workspace_bytes;
+ * its first 4 bytes are the device error word (rswa_device_error), which the
+ * caller zeroes once before the first call. */
+KVD_API kvd_status rswa_decode(const float *q, const float *ref_k, const float *ref_v,
+                       const float *ring_k, const float *ring_v, const int32_t *prefill_len,
+                       const int32_t *ring_len, const int32_t *ring_pos, int32_t B, int32_t H,
+                       int32_t head_dim, int64_t ref_cap, int32_t W, float scale, float *out,
+                       void *workspace, int64_t workspace_bytes, void *stream);
+
+/* Device error word kept in an R-SWA workspace (see kvd_layer_device_error). */
+KVD_API kvd_status rswa_device_error(const void *workspace, int32_t clear, uint32_t *word_out);
+
+/* Short English description of a status code (static storage). */
+KVD_API const char *kvd_status_string(int32_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVD_H */

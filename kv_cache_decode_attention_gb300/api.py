@@ -1,0 +1,268 @@
+"""Python binding over the C ABI: torch tensors in, raw device pointers out.
+
+Every computation runs in libkvd.so; this module only allocates the device
+buffers the library asks for (torch owns them), marshals pointers, shapes
+and the current CUDA stream, and raises on a non-OK status.
+
+Names follow the pages: ``LayerKvCache`` (cortiq kv_cache.rs, batched over
+sequences) with ``kv_append``, ``kv_freeze_colfield``, ``decode_attention``;
+``RingCache`` (franken_ocr rswa.rs, batched over streams) with
+``rswa_record_prefill``, ``rswa_ring_write`` (write_decode_step) and
+``rswa_decode``.
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+import math
+
+import numpy as np
+import torch
+
+from . import _abi
+from ._abi import F32, Q8, Q8K, Q8V  # noqa: F401
+
+MODE_NAMES = {"f32": F32, "q8": Q8, "q8_2f": Q8, "q8k": Q8K, "q8v": Q8V}
+
+
+def _stream(stream=None) -> C.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+def _ptr(t: torch.Tensor | None) -> C.c_void_p | None:
+    if t is None:
+        return None
+    return C.c_void_p(t.data_ptr())
+
+
+def _f32_cuda(t: torch.Tensor, name: str) -> torch.Tensor:
+    if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous()):
+        raise ValueError("%s must be a contiguous float32 CUDA tensor" % name)
+    return t
+
+
+def _np_ptr(a: np.ndarray) -> C.c_void_p:
+    return C.c_void_p(a.ctypes.data)
+
+
+class LayerKvCache:
+    """One layer's KV cache for a batch of sequences (device buffers owned here).
+
+    mode: 'f32' | 'q8' (q8_2f) | 'q8k' | 'q8v' or the integer kvd_mode.
+    capacity: rows per sequence (int or per-sequence sequence of ints).
+    alive: per-KV-head 0/1 mask (dead heads store nothing), default all alive.
+    """
+
+    def __init__(self, n_seq: int, n_kv: int, head_dim: int, mode, capacity, alive=None,
+                 device="cuda", stream=None):
+        self.mode = MODE_NAMES[mode] if isinstance(mode, str) else int(mode)
+        self.n_seq, self.n_kv, self.head_dim = int(n_seq), int(n_kv), int(head_dim)
+        cap = np.broadcast_to(np.asarray(capacity, np.int64), (self.n_seq,)).copy()
+        self.capacity = cap
+        self.alive = (np.ones(self.n_kv, np.uint8) if alive is None
+                      else np.ascontiguousarray(alive, dtype=np.uint8))
+        sizes = np.zeros(_abi.BUF_COUNT, np.int64)
+        host_bytes = C.c_int64(0)
+        _abi.call("kvd_layer_bytes", self.n_seq, self.n_kv, self.head_dim, self.mode,
+                  _np_ptr(cap), _np_ptr(self.alive), _np_ptr(sizes), C.byref(host_bytes))
+        self.buf_bytes = sizes
+        self.device = torch.device(device)
+        self.bufs = [torch.empty(int(n), dtype=torch.uint8, device=self.device) if n > 0 else None
+                     for n in sizes]
+        self._ptrs = (C.c_void_p * _abi.BUF_COUNT)(
+            *[b.data_ptr() if b is not None else None for b in self.bufs])
+        self._host = np.zeros(int(host_bytes.value) + 64, np.uint8)
+        self.L = _abi.kvd_layer()
+        _abi.call("kvd_layer_init", C.byref(self.L), self.n_seq, self.n_kv, self.head_dim,
+                  self.mode, _np_ptr(cap), _np_ptr(self.alive), self._ptrs,
+                  _np_ptr(self._host), _stream(stream))
+        self.n_live = int(self.alive.astype(bool).sum())
+        self.cap16 = (cap + 15) // 16 * 16
+        self.row_base = np.concatenate([[0], np.cumsum(self.cap16 * self.n_live)[:-1]]).astype(np.int64)
+        self.imp_base = np.concatenate([[0], np.cumsum(self.cap16)[:-1]]).astype(np.int64)
+        self.imp_len = int(self.cap16.sum())
+        self.live_heads = [h for h in range(self.n_kv) if self.alive[h]]
+
+    # ---- host-mirrored state -------------------------------------------
+    def seq_len(self, b: int) -> int:
+        n, f = C.c_int64(0), C.c_int32(0)
+        _abi.call("kvd_layer_seq_len", C.byref(self.L), int(b), C.byref(n), C.byref(f))
+        return int(n.value)
+
+    def frozen(self, b: int) -> bool:
+        n, f = C.c_int64(0), C.c_int32(0)
+        _abi.call("kvd_layer_seq_len", C.byref(self.L), int(b), C.byref(n), C.byref(f))
+        return bool(f.value)
+
+    def memory_bytes(self) -> int:
+        n = C.c_int64(0)
+        _abi.call("kvd_layer_memory_bytes", C.byref(self.L), C.byref(n))
+        return int(n.value)
+
+    def device_error(self, clear: bool = True) -> int:
+        w = C.c_uint32(0)
+        st = _abi.lib().kvd_layer_device_error(C.byref(self.L), int(clear), C.byref(w))
+        if st not in (_abi.OK, _abi.EDEVICE):
+            _abi.check("kvd_layer_device_error", st)
+        return int(w.value)
+
+    def reset(self, seq: int = -1, stream=None):
+        _abi.call("kvd_layer_reset", C.byref(self.L), int(seq), _stream(stream))
+
+    def workspace_bytes(self, n_q: int, with_imp: bool) -> int:
+        n = C.c_int64(0)
+        _abi.call("kvd_decode_workspace_bytes", C.byref(self.L), int(n_q), int(with_imp), C.byref(n))
+        return int(n.value)
+
+    # ---- views of the stored rows (for inspection and tests) ------------
+    def region(self, b: int, kv_head: int) -> tuple[int, int]:
+        """(first storage row, rows) of sequence b's live KV head `kv_head`."""
+        gl = self.live_heads.index(kv_head)
+        return int(self.row_base[b] + gl * self.cap16[b]), int(self.cap16[b])
+
+    def component(self, slot: int) -> torch.Tensor | None:
+        """Typed view of a row buffer: f32 [rows, hd], int8 [rows, hd], K scales
+        [rows, hd/32], V scales [rows], fields [n_seq, n_live, hd]."""
+        b = self.bufs[slot]
+        if b is None:
+            return None
+        hd = self.head_dim
+        if slot in (_abi.BUF_K, _abi.BUF_V):
+            return b.view(torch.float32)[: (b.numel() // 4) // hd * hd].view(-1, hd)
+        if slot in (_abi.BUF_KQ, _abi.BUF_VQ):
+            return b.view(torch.int8)[: b.numel() // hd * hd].view(-1, hd)
+        if slot == _abi.BUF_KS:
+            ng = hd // 32
+            return b.view(torch.float32)[: (b.numel() // 4) // ng * ng].view(-1, ng)
+        if slot == _abi.BUF_VS:
+            return b.view(torch.float32)
+        if slot in (_abi.BUF_KCOL, _abi.BUF_VCOL):
+            n = self.n_seq * self.n_live * hd
+            return b.view(torch.float32)[:n].view(self.n_seq, self.n_live, hd)
+        return b
+
+
+def kv_append(layer: LayerKvCache, k: torch.Tensor, v: torch.Tensor, n_new=None, stream=None):
+    """Append rows: k, v [sum n_new, n_kv, hd] (or [n_seq, n_kv, hd] with n_new None)."""
+    _f32_cuda(k, "k")
+    _f32_cuda(v, "v")
+    rows = k.numel() // (layer.n_kv * layer.head_dim)
+    if n_new is None:
+        if rows != layer.n_seq or v.numel() != k.numel():
+            raise ValueError("k/v must hold one row per sequence")
+        nn = None
+    else:
+        nn = np.ascontiguousarray(n_new, dtype=np.int32)
+        if nn.shape != (layer.n_seq,) or rows != int(nn.sum()) or v.numel() != k.numel():
+            raise ValueError("k/v rows must equal sum(n_new)")
+    _abi.call("kv_append", C.byref(layer.L), _ptr(k), _ptr(v),
+              None if nn is None else _np_ptr(nn), _stream(stream))
+
+
+def kv_freeze_colfield(layer: LayerKvCache, stream=None):
+    _abi.call("kv_freeze_colfield", C.byref(layer.L), _stream(stream))
+
+
+def decode_attention(q: torch.Tensor, cache: LayerKvCache, out: torch.Tensor | None = None,
+                     imp: torch.Tensor | None = None, scale: float | None = None,
+                     workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """q [n_seq, n_q, hd] -> out [n_seq, n_q, hd]; imp (float32 [imp_len]) accumulates."""
+    _f32_cuda(q, "q")
+    n_q = q.numel() // (cache.n_seq * cache.head_dim)
+    if q.numel() != cache.n_seq * n_q * cache.head_dim:
+        raise ValueError("q must be [n_seq, n_q, head_dim]")
+    if out is None:
+        out = torch.empty_like(q)
+    _f32_cuda(out, "out")
+    if imp is not None:
+        _f32_cuda(imp, "imp")
+        if imp.numel() < cache.imp_len:
+            raise ValueError("imp must hold %d floats" % cache.imp_len)
+    need = cache.workspace_bytes(n_q, imp is not None)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(cache.head_dim)
+    _abi.call("decode_attention", _ptr(q), C.byref(cache.L), int(n_q), C.c_float(scale),
+              _ptr(out), _ptr(imp), _ptr(workspace), int(workspace.numel()), _stream(stream))
+    return out
+
+
+class RingCache:
+    """R-SWA caches of B streams for one layer: reference block [B, H, ref_cap, hd]
+    plus a W-slot ring [B, H, W, hd], cursors on the host."""
+
+    def __init__(self, B: int, ref_cap: int, H: int = 10, head_dim: int = 128, W: int = 128,
+                 device="cuda"):
+        self.B, self.H, self.head_dim, self.W, self.ref_cap = B, H, head_dim, W, ref_cap
+        dev = torch.device(device)
+        self.ref_k = torch.zeros(B, H, ref_cap, head_dim, device=dev)
+        self.ref_v = torch.zeros(B, H, ref_cap, head_dim, device=dev)
+        self.ring_k = torch.zeros(B, H, W, head_dim, device=dev)
+        self.ring_v = torch.zeros(B, H, W, head_dim, device=dev)
+        self.prefill_len = np.full(B, -1, np.int32)
+        self.ring_len = np.zeros(B, np.int32)
+        self.ring_pos = np.zeros(B, np.int32)
+        n = C.c_int64(0)
+        _abi.call("rswa_decode_workspace_bytes", B, H, head_dim, ref_cap, W, C.byref(n))
+        self.workspace = torch.zeros(int(n.value), dtype=torch.uint8, device=dev)
+
+    def device_error(self, clear: bool = True) -> int:
+        w = C.c_uint32(0)
+        st = _abi.lib().rswa_device_error(_ptr(self.workspace), int(clear), C.byref(w))
+        if st not in (_abi.OK, _abi.EDEVICE):
+            _abi.check("rswa_device_error", st)
+        return int(w.value)
+
+
+def rswa_record_prefill(cache: RingCache, s: int, k: torch.Tensor, v: torch.Tensor, stream=None):
+    """Record stream s's prefill k, v [H, seq, hd] as its reference block."""
+    _f32_cuda(k, "k")
+    _f32_cuda(v, "v")
+    seq = k.numel() // (cache.H * cache.head_dim)
+    if k.numel() != cache.H * seq * cache.head_dim or v.numel() != k.numel():
+        raise ValueError("prefill k/v must be [H, seq, head_dim]")
+    _abi.call("rswa_record_prefill", _ptr(cache.ref_k), _ptr(cache.ref_v), _ptr(k), _ptr(v),
+              int(s), int(seq), cache.B, cache.H, cache.head_dim, cache.ref_cap, cache.W,
+              _np_ptr(cache.prefill_len), _np_ptr(cache.ring_len), _np_ptr(cache.ring_pos),
+              _stream(stream))
+
+
+def rswa_ring_write(cache: RingCache, k: torch.Tensor, v: torch.Tensor, stream=None) -> np.ndarray:
+    """write_decode_step for every stream: k, v [B, H, hd]; returns the slots written."""
+    _f32_cuda(k, "k")
+    _f32_cuda(v, "v")
+    if k.numel() != cache.B * cache.H * cache.head_dim or v.numel() != k.numel():
+        raise ValueError("k/v must be [B, H, head_dim]")
+    slots = np.zeros(cache.B, np.int32)
+    _abi.call("rswa_ring_write", _ptr(cache.ring_k), _ptr(cache.ring_v), _ptr(k), _ptr(v),
+              _np_ptr(cache.prefill_len), _np_ptr(cache.ring_len), _np_ptr(cache.ring_pos),
+              cache.B, cache.H, cache.head_dim, cache.W, _np_ptr(slots), _stream(stream))
+    return slots
+
+
+def rswa_decode(q: torch.Tensor, cache: RingCache, out: torch.Tensor | None = None,
+                scale: float | None = None, stream=None) -> torch.Tensor:
+    """q [B, H, hd] -> out [B, H * hd]: softmax over reference ++ ring per head."""
+    _f32_cuda(q, "q")
+    if q.numel() != cache.B * cache.H * cache.head_dim:
+        raise ValueError("q must be [B, H, head_dim]")
+    if out is None:
+        out = torch.empty(cache.B, cache.H * cache.head_dim, device=q.device)
+    _f32_cuda(out, "out")
+    if scale is None:
+        scale = 1.0 / math.sqrt(cache.head_dim)
+    _abi.call("rswa_decode", _ptr(q), _ptr(cache.ref_k), _ptr(cache.ref_v), _ptr(cache.ring_k),
+              _ptr(cache.ring_v), _np_ptr(cache.prefill_len), _np_ptr(cache.ring_len),
+              _np_ptr(cache.ring_pos), cache.B, cache.H, cache.head_dim, cache.ref_cap, cache.W,
+              C.c_float(scale), _ptr(out), _ptr(cache.workspace), int(cache.workspace.numel()),
+              _stream(stream))
+    return out
+
+
+def rswa_attention(cache: RingCache, q, k, v, stream=None) -> torch.Tensor:
+    """rswa attention(): write this step's K/V into every ring, then attend (the
+    query sees itself as the newest ring row)."""
+    rswa_ring_write(cache, k, v, stream)
+    return rswa_decode(q, cache, stream=stream)

@@ -1,0 +1,460 @@
+// kvd_decode.cu -- host entry points of the decode path: GQA decode attention
+// over a layer (cortiq attend_group for every group, batched over sequences)
+// and the R-SWA ring write / decode (rswa RingCache::write_decode_step,
+// decode_attention), plus their merge and imp kernels' launches.
+
+#include <algorithm>
+#include <cmath>
+#include <vector>
+
+#include "kvd_decode_kernels.cuh"
+
+namespace kvd {
+
+cudaError_t split_layer_f32(int, int, const SplitArgs &, const LayerSrc &, dim3, cudaStream_t);
+cudaError_t split_layer_q8(int, int, const SplitArgs &, const LayerSrc &, dim3, cudaStream_t);
+cudaError_t split_layer_q8k(int, int, const SplitArgs &, const LayerSrc &, dim3, cudaStream_t);
+cudaError_t split_layer_q8v(int, int, const SplitArgs &, const LayerSrc &, dim3, cudaStream_t);
+
+namespace {
+
+constexpr int kMinChunk = 256;           // rows; multiple of every tile height
+constexpr int64_t kTargetCtas = 152 * 8; // about four waves of two CTAs per SM
+
+int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+int64_t ceil_div(int64_t x, int64_t a) { return (x + a - 1) / a; }
+
+int hpk_bucket(int hpk) {
+    int b = 1;
+    while (b < hpk) b <<= 1;
+    return b;
+}
+
+// Rows per chunk: at least kMinChunk, large enough that the grid holds about
+// kTargetCtas chunks, a multiple of kMinChunk.
+int32_t pick_chunk(int64_t work_rows) {
+    const int64_t c = std::max<int64_t>(kMinChunk, ceil_div(work_rows, kTargetCtas));
+    return int32_t(round_up(c, kMinChunk));
+}
+
+struct DecodeWs {
+    int64_t pm, pl, pacc, ml, scores, total;
+    int32_t nc_max;
+};
+
+DecodeWs decode_ws(const Layer *l, int32_t n_q, bool imp) {
+    DecodeWs w;
+    const int hpk = n_q / l->n_kv;
+    w.nc_max = int32_t(std::max<int64_t>(1, ceil_div(l->max_cap, kMinChunk)));
+    const int64_t P = int64_t(l->n_seq) * std::max(1, l->n_live) * w.nc_max * hpk;
+    int64_t o = 0;
+    auto take = [&](int64_t bytes) {
+        const int64_t at = o;
+        o = round_up(o + bytes, 256);
+        return at;
+    };
+    w.pm = take(P * 4);
+    w.pl = take(P * 4);
+    w.pacc = take(P * l->hd * 4);
+    w.ml = take(int64_t(l->n_seq) * n_q * 2 * 4);
+    w.scores = imp ? take((l->total_rows + kRowAlign) * hpk * 4) : -1;
+    w.total = o;
+    return w;
+}
+
+struct RswaWs {
+    int64_t err, pm, pl, pacc, total;
+    int32_t nc_max;
+};
+
+RswaWs rswa_ws(int32_t B, int32_t H, int32_t hd, int64_t ref_cap, int32_t W) {
+    RswaWs w;
+    w.nc_max = int32_t(ceil_div(ref_cap, kMinChunk) + ceil_div(W, kMinChunk));
+    const int64_t P = int64_t(B) * H * w.nc_max;
+    int64_t o = 0;
+    auto take = [&](int64_t bytes) {
+        const int64_t at = o;
+        o = round_up(o + bytes, 256);
+        return at;
+    };
+    w.err = take(16);
+    w.pm = take(P * 4);
+    w.pl = take(P * 4);
+    w.pacc = take(P * hd * 4);
+    w.total = o;
+    return w;
+}
+
+// ------------------------------------------------------------------ imp
+
+struct ImpArgs {
+    const float *scores;  // [storage row][hpk] log2 scores
+    const float *ml;      // [n_seq][n_q][2]
+    float *imp;
+    const int64_t *row_base, *cap, *imp_base;
+    const int32_t *seq_len, *live;
+    int32_t n_q, hpk, n_live;
+};
+
+// imp[b][p] += sum over live groups (ascending) and their heads (ascending)
+// of 2^(s - M) / L: the softmax weight of every live query head on row p.
+__global__ void __launch_bounds__(256) imp_kernel(ImpArgs a) {
+    const int b = blockIdx.y;
+    const int p = blockIdx.x * 256 + threadIdx.x;
+    const int L = a.seq_len[b];
+    if (p >= L) return;
+    const int64_t cap = a.cap[b];
+    float add = 0.0f;
+    for (int gl = 0; gl < a.n_live; ++gl) {
+        const int g = a.live[gl];
+        const int64_t row = a.row_base[b] + gl * cap + p;
+        for (int hh = 0; hh < a.hpk; ++hh) {
+            const int h = g * a.hpk + hh;
+            const float M = a.ml[(int64_t(b) * a.n_q + h) * 2];
+            const float Ls = a.ml[(int64_t(b) * a.n_q + h) * 2 + 1];
+            add += exp2f(a.scores[row * a.hpk + hh] - M) / Ls;
+        }
+    }
+    a.imp[a.imp_base[b] + p] += add;
+}
+
+// ---------------------------------------------------------------- R-SWA copies
+
+struct RingWriteTable {
+    int32_t s0, n;
+    int32_t slot[kSlice];
+};
+
+// Stream s0 + i copies its token's H rows of K and V into ring slot slot[i].
+__global__ void ring_write_kernel(float *ring_k, float *ring_v, const float *k, const float *v,
+                                  int32_t H, int32_t hd, int32_t W, RingWriteTable t) {
+    const int i = blockIdx.y;
+    if (i >= t.n) return;
+    const int s = t.s0 + i;
+    const int64_t per = int64_t(H) * hd;
+    for (int64_t e = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; e < per;
+         e += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t h = e / hd, d = e % hd;
+        const int64_t dst = ((int64_t(s) * H + h) * W + t.slot[i]) * hd + d;
+        ring_k[dst] = k[int64_t(s) * per + e];
+        ring_v[dst] = v[int64_t(s) * per + e];
+    }
+}
+
+// Copy a [H][seq][hd] prefill into the reference block of stream s.
+__global__ void prefill_copy_kernel(float *ref_k, float *ref_v, const float *k, const float *v,
+                                    int32_t s, int32_t seq, int32_t H, int32_t hd,
+                                    int64_t ref_cap) {
+    const int64_t per_head = int64_t(seq) * hd;
+    const int64_t total = per_head * H;
+    for (int64_t e = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; e < total;
+         e += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t h = e / per_head, r = e % per_head;
+        const int64_t dst = (int64_t(s) * H + h) * ref_cap * hd + r;
+        ref_k[dst] = k[e];
+        ref_v[dst] = v[e];
+    }
+}
+
+template <int HD>
+cudaError_t launch_split_rswa(const SplitArgs &a, const RswaSrc &s, const RswaTable &t, dim3 grid,
+                              cudaStream_t st) {
+    using C = SplitCfg<HD, 1, false, false>;
+    auto kern = split_rswa_kernel<HD>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kThreads, C::SMEM, st>>>(a, s, t);
+    return cudaGetLastError();
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+}  // namespace kvd
+
+using namespace kvd;
+
+extern "C" kvd_status kvd_decode_workspace_bytes(const kvd_layer *L, int32_t n_q, int32_t with_imp,
+                                                 int64_t *bytes_out) {
+    const Layer *l = checked_layer(L);
+    if (l == nullptr || bytes_out == nullptr) return KVD_EINVAL;
+    if (n_q < l->n_kv || n_q % l->n_kv != 0 || n_q / l->n_kv > kMaxHpk) return KVD_EINVAL;
+    *bytes_out = decode_ws(l, n_q, with_imp != 0).total;
+    return KVD_OK;
+}
+
+extern "C" kvd_status decode_attention(const float *q, const kvd_layer *L, int32_t n_q, float scale,
+                                       float *out, float *imp, void *workspace,
+                                       int64_t workspace_bytes, void *stream) {
+    const Layer *l = checked_layer(L);
+    if (l == nullptr || q == nullptr || out == nullptr) return KVD_EINVAL;
+    if (n_q < l->n_kv || n_q % l->n_kv != 0 || n_q / l->n_kv > kMaxHpk) return KVD_EINVAL;
+    if (!std::isfinite(scale)) return KVD_EINVAL;
+    if (!aligned16(q) || !aligned16(out) || (imp && (reinterpret_cast<uintptr_t>(imp) & 3)))
+        return KVD_EINVAL;
+    const DecodeWs w = decode_ws(l, n_q, imp != nullptr);
+    if (workspace == nullptr || workspace_bytes < w.total ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255))
+        return KVD_EINVAL;
+    const int hpk = n_q / l->n_kv;
+    cudaStream_t st = as_stream(stream);
+    char *ws = static_cast<char *>(workspace);
+
+    int64_t work = 0, max_len = 0;
+    for (int b = 0; b < l->n_seq; ++b) {
+        work += l->h_seq_len[b] * int64_t(l->n_live);
+        max_len = std::max(max_len, l->h_seq_len[b]);
+    }
+    const int32_t chunk = pick_chunk(work);
+
+    SplitArgs a;
+    a.q = q;
+    a.n_q = n_q;
+    a.hpk = hpk;
+    a.qscale = scale * kLog2e;
+    a.chunk = chunk;
+    a.nc_max = w.nc_max;
+    a.n_grp = std::max(1, l->n_live);
+    a.pm = reinterpret_cast<float *>(ws + w.pm);
+    a.pl = reinterpret_cast<float *>(ws + w.pl);
+    a.pacc = reinterpret_cast<float *>(ws + w.pacc);
+    a.scores = imp ? reinterpret_cast<float *>(ws + w.scores) : nullptr;
+    a.err = l->d_err;
+
+    if (max_len > 0 && l->n_live > 0) {
+        LayerSrc s;
+        s.kf = static_cast<const float *>(l->buf[KVD_BUF_K]);
+        s.vf = static_cast<const float *>(l->buf[KVD_BUF_V]);
+        s.kq = static_cast<const int8_t *>(l->buf[KVD_BUF_KQ]);
+        s.vq = static_cast<const int8_t *>(l->buf[KVD_BUF_VQ]);
+        s.ks = static_cast<const float *>(l->buf[KVD_BUF_KS]);
+        s.vs = static_cast<const float *>(l->buf[KVD_BUF_VS]);
+        s.kcol = static_cast<const float *>(l->buf[KVD_BUF_KCOL]);
+        s.row_base = l->d_row_base;
+        s.cap = l->d_cap;
+        s.seq_len = l->d_seq_len;
+        s.live = l->d_live;
+        s.n_live = l->n_live;
+        dim3 grid(unsigned(ceil_div(max_len, chunk)), unsigned(l->n_live), unsigned(l->n_seq));
+        const int hb = hpk_bucket(hpk);
+        cudaError_t e;
+        switch (l->mode) {
+            case KVD_F32: e = split_layer_f32(l->hd, hb, a, s, grid, st); break;
+            case KVD_Q8: e = split_layer_q8(l->hd, hb, a, s, grid, st); break;
+            case KVD_Q8K: e = split_layer_q8k(l->hd, hb, a, s, grid, st); break;
+            default: e = split_layer_q8v(l->hd, hb, a, s, grid, st); break;
+        }
+        if (e != cudaSuccess) return KVD_ECUDA;
+    }
+
+    MergeArgs m;
+    m.pm = a.pm;
+    m.pl = a.pl;
+    m.pacc = a.pacc;
+    m.out = out;
+    m.ml = imp ? reinterpret_cast<float *>(ws + w.ml) : nullptr;
+    m.n_q = n_q;
+    m.hpk = hpk;
+    m.n_grp = a.n_grp;
+    m.nc_max = w.nc_max;
+    m.chunk = chunk;
+    MergeLayerSrc ms;
+    ms.seq_len = l->d_seq_len;
+    ms.slot = l->d_slot;
+    ms.vcol = static_cast<const float *>(l->buf[KVD_BUF_VCOL]);
+    ms.n_live = l->n_live;
+    dim3 mgrid(unsigned(n_q), unsigned(l->n_seq));
+    if (l->hd == 128) merge_layer_kernel<128><<<mgrid, 128, 0, st>>>(m, ms);
+    else merge_layer_kernel<64><<<mgrid, 64, 0, st>>>(m, ms);
+    if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
+
+    if (imp && max_len > 0 && l->n_live > 0) {
+        ImpArgs ia;
+        ia.scores = a.scores;
+        ia.ml = m.ml;
+        ia.imp = imp;
+        ia.row_base = l->d_row_base;
+        ia.cap = l->d_cap;
+        ia.imp_base = reinterpret_cast<const int64_t *>(
+            static_cast<const char *>(l->buf[KVD_BUF_META]) + l->ml.imp_base);
+        ia.seq_len = l->d_seq_len;
+        ia.live = l->d_live;
+        ia.n_q = n_q;
+        ia.hpk = hpk;
+        ia.n_live = l->n_live;
+        dim3 igrid(unsigned(ceil_div(max_len, 256)), unsigned(l->n_seq));
+        imp_kernel<<<igrid, 256, 0, st>>>(ia);
+        if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
+    }
+    return KVD_OK;
+}
+
+// ------------------------------------------------------------------ R-SWA
+
+extern "C" kvd_status rswa_record_prefill(float *ref_k, float *ref_v, const float *k,
+                                          const float *v, int32_t s, int32_t seq, int32_t B,
+                                          int32_t H, int32_t head_dim, int64_t ref_cap, int32_t W,
+                                          int32_t *prefill_len, int32_t *ring_len,
+                                          int32_t *ring_pos, void *stream) {
+    if (ref_k == nullptr || ref_v == nullptr || prefill_len == nullptr || ring_len == nullptr ||
+        ring_pos == nullptr)
+        return KVD_EINVAL;
+    if (B < 1 || s < 0 || s >= B || H < 1 || head_dim < 1 || W < 1 || ref_cap < 0 || seq < 0)
+        return KVD_EINVAL;
+    if (seq > ref_cap) return KVD_ECAPACITY;
+    if (seq > 0 && (k == nullptr || v == nullptr)) return KVD_EINVAL;
+    if (seq > 0) {
+        const int64_t total = int64_t(H) * seq * head_dim;
+        const unsigned blocks = unsigned(std::min<int64_t>(ceil_div(total, 256), 152 * 16));
+        prefill_copy_kernel<<<blocks, 256, 0, as_stream(stream)>>>(ref_k, ref_v, k, v, s, seq, H,
+                                                                   head_dim, ref_cap);
+        if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
+    }
+    prefill_len[s] = seq;
+    ring_len[s] = 0;
+    ring_pos[s] = 0;
+    return KVD_OK;
+}
+
+extern "C" kvd_status rswa_ring_write(float *ring_k, float *ring_v, const float *k, const float *v,
+                                      const int32_t *prefill_len, int32_t *ring_len,
+                                      int32_t *ring_pos, int32_t B, int32_t H, int32_t head_dim,
+                                      int32_t W, int32_t *slot_out, void *stream) {
+    if (ring_k == nullptr || ring_v == nullptr || k == nullptr || v == nullptr ||
+        prefill_len == nullptr || ring_len == nullptr || ring_pos == nullptr)
+        return KVD_EINVAL;
+    if (B < 1 || H < 1 || head_dim < 1 || W < 1) return KVD_EINVAL;
+    for (int s = 0; s < B; ++s) {
+        if (prefill_len[s] < 0) return KVD_ESTATE;
+        if (ring_len[s] < 0 || ring_len[s] > W || ring_pos[s] < 0 || ring_pos[s] >= W)
+            return KVD_EINVAL;
+    }
+    std::vector<int32_t> slot(B);
+    for (int s = 0; s < B; ++s) slot[s] = ring_len[s] < W ? ring_len[s] : ring_pos[s];
+    for (int32_t s0 = 0; s0 < B; s0 += kSlice) {
+        RingWriteTable t;
+        t.s0 = s0;
+        t.n = std::min(kSlice, B - s0);
+        for (int i = 0; i < t.n; ++i) t.slot[i] = slot[s0 + i];
+        const int64_t per = int64_t(H) * head_dim;
+        dim3 grid(unsigned(std::min<int64_t>(ceil_div(per, 256), 64)), unsigned(t.n));
+        ring_write_kernel<<<grid, 256, 0, as_stream(stream)>>>(ring_k, ring_v, k, v, H, head_dim, W,
+                                                              t);
+        if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
+    }
+    for (int s = 0; s < B; ++s) {
+        if (ring_len[s] < W) {
+            ring_len[s] += 1;
+            ring_pos[s] = ring_len[s] % W;
+        } else {
+            ring_pos[s] = (ring_pos[s] + 1) % W;
+        }
+        if (slot_out) slot_out[s] = slot[s];
+    }
+    return KVD_OK;
+}
+
+extern "C" kvd_status rswa_decode_workspace_bytes(int32_t B, int32_t H, int32_t head_dim,
+                                                  int64_t ref_cap, int32_t W, int64_t *bytes_out) {
+    if (bytes_out == nullptr || B < 1 || H < 1 || (head_dim != 64 && head_dim != 128) ||
+        ref_cap < 0 || W < 1)
+        return KVD_EINVAL;
+    *bytes_out = rswa_ws(B, H, head_dim, ref_cap, W).total;
+    return KVD_OK;
+}
+
+extern "C" kvd_status rswa_decode(const float *q, const float *ref_k, const float *ref_v,
+                                  const float *ring_k, const float *ring_v,
+                                  const int32_t *prefill_len, const int32_t *ring_len,
+                                  const int32_t *ring_pos, int32_t B, int32_t H, int32_t head_dim,
+                                  int64_t ref_cap, int32_t W, float scale, float *out,
+                                  void *workspace, int64_t workspace_bytes, void *stream) {
+    if (q == nullptr || ref_k == nullptr || ref_v == nullptr || ring_k == nullptr ||
+        ring_v == nullptr || prefill_len == nullptr || ring_len == nullptr || out == nullptr)
+        return KVD_EINVAL;
+    if (B < 1 || H < 1 || (head_dim != 64 && head_dim != 128) || ref_cap < 0 || W < 1)
+        return KVD_EINVAL;
+    // Bulk copies move whole 16-row groups: both regions must hold them.
+    if (ref_cap % kRowAlign != 0 || W % kRowAlign != 0) return KVD_EINVAL;
+    if (!std::isfinite(scale)) return KVD_EINVAL;
+    if (!aligned16(q) || !aligned16(out) || !aligned16(ref_k) || !aligned16(ref_v) ||
+        !aligned16(ring_k) || !aligned16(ring_v))
+        return KVD_EINVAL;
+    const RswaWs w = rswa_ws(B, H, head_dim, ref_cap, W);
+    if (workspace == nullptr || workspace_bytes < w.total ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255))
+        return KVD_EINVAL;
+    int64_t work = 0;
+    for (int s = 0; s < B; ++s) {
+        if (prefill_len[s] < 0) return KVD_ESTATE;
+        if (prefill_len[s] > ref_cap || ring_len[s] < 0 || ring_len[s] > W) return KVD_EINVAL;
+        if (ring_pos && (ring_pos[s] < 0 || ring_pos[s] >= W)) return KVD_EINVAL;
+        if (prefill_len[s] + ring_len[s] == 0) return KVD_EEMPTY;
+        work += int64_t(prefill_len[s] + ring_len[s]) * H;
+    }
+    const int32_t chunk = pick_chunk(work);
+    char *ws = static_cast<char *>(workspace);
+    cudaStream_t st = as_stream(stream);
+    SplitArgs a;
+    a.q = q;
+    a.n_q = H;
+    a.hpk = 1;
+    a.qscale = scale * kLog2e;
+    a.chunk = chunk;
+    a.nc_max = w.nc_max;
+    a.n_grp = H;
+    a.pm = reinterpret_cast<float *>(ws + w.pm);
+    a.pl = reinterpret_cast<float *>(ws + w.pl);
+    a.pacc = reinterpret_cast<float *>(ws + w.pacc);
+    a.scores = nullptr;
+    a.err = reinterpret_cast<uint32_t *>(ws + w.err);
+    RswaSrc src;
+    src.ref_k = ref_k;
+    src.ref_v = ref_v;
+    src.ring_k = ring_k;
+    src.ring_v = ring_v;
+    src.ref_cap = ref_cap;
+    src.W = W;
+    src.H = H;
+    MergeArgs m;
+    m.pm = a.pm;
+    m.pl = a.pl;
+    m.pacc = a.pacc;
+    m.out = out;
+    m.ml = nullptr;
+    m.n_q = H;
+    m.hpk = 1;
+    m.n_grp = H;
+    m.nc_max = w.nc_max;
+    m.chunk = chunk;
+    for (int32_t s0 = 0; s0 < B; s0 += kSlice) {
+        RswaTable t;
+        t.s0 = s0;
+        t.n = std::min(kSlice, B - s0);
+        int32_t max_nc = 0;
+        for (int i = 0; i < t.n; ++i) {
+            t.prefill_len[i] = prefill_len[s0 + i];
+            t.ring_len[i] = ring_len[s0 + i];
+            const int32_t nc = int32_t(ceil_div(t.prefill_len[i], chunk) + ceil_div(t.ring_len[i], chunk));
+            max_nc = std::max(max_nc, nc);
+        }
+        dim3 grid(unsigned(max_nc), unsigned(H), unsigned(t.n));
+        cudaError_t e = head_dim == 128 ? launch_split_rswa<128>(a, src, t, grid, st)
+                                        : launch_split_rswa<64>(a, src, t, grid, st);
+        if (e != cudaSuccess) return KVD_ECUDA;
+        dim3 mgrid(unsigned(H), unsigned(t.n));
+        if (head_dim == 128) merge_rswa_kernel<128><<<mgrid, 128, 0, st>>>(m, t);
+        else merge_rswa_kernel<64><<<mgrid, 64, 0, st>>>(m, t);
+        if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
+    }
+    return KVD_OK;
+}
+
+extern "C" kvd_status rswa_device_error(const void *workspace, int32_t clear, uint32_t *word_out) {
+    if (workspace == nullptr) return KVD_EINVAL;
+    uint32_t w = 0;
+    if (cudaMemcpy(&w, workspace, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return KVD_ECUDA;
+    if (clear && cudaMemset(const_cast<void *>(workspace), 0, 4) != cudaSuccess) return KVD_ECUDA;
+    if (word_out) *word_out = w;
+    return w ? KVD_EDEVICE : KVD_OK;
+}

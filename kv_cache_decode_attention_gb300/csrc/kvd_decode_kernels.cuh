@@ -1,0 +1,547 @@
+// kvd_decode_kernels.cuh -- split-KV decode attention kernels (templates).
+//
+// One CTA owns one chunk of consecutive cached rows of one (sequence, KV
+// group) and every query head of that group (GQA: each K and V row is read
+// once for all hpk heads, as cortiq attend_group reads it).  The chunk is
+// streamed through shared memory in tiles by 1-D bulk asynchronous copies
+// (TMA bulk engine, mbarrier completion) into a ring of kNSeg slots that
+// alternates K tiles (with their scales) and V tiles.  Per tile:
+//   score pass  lanes split the channels of a row; each lane forms partial
+//               dots for RB rows x HPK heads and one butterfly
+//               reduce-scatter over the warp leaves one complete score per
+//               lane (dequantisation fused in: int8 codes x per-32-channel
+//               scale, field and softmax scale folded into q once);
+//   softmax     running max per head, rescale of the running sum and
+//               accumulator by exp2(old - new) (the online recurrence of
+//               rswa fold, applied per tile);
+//   value pass  each warp walks rows, lanes own channels, accumulators in
+//               registers; V codes are weighted by exp * row scale.
+// The CTA writes its (max, sum, accumulator) partial per head; a second
+// kernel merges the chunks of a sequence by log-sum-exp and applies the V
+// field.  Scores are kept in the log2 domain (q is pre-scaled by log2(e)).
+#pragma once
+
+#include <math.h>
+
+#include "kvd_internal.cuh"
+
+namespace kvd {
+
+constexpr int kThreads = 128;
+constexpr int kWarps = kThreads / 32;
+constexpr int kNSeg = 4;
+constexpr float kLog2e = 1.4426950408889634f;
+
+constexpr int ce_max(int a, int b) { return a > b ? a : b; }
+constexpr int ce_min(int a, int b) { return a < b ? a : b; }
+constexpr int ce_log2(int x) { return x <= 1 ? 0 : 1 + ce_log2(x / 2); }
+constexpr int ce_round(int x, int a) { return (x + a - 1) / a * a; }
+
+// Tile geometry for a head dim and storage mode.
+template <int HD, bool KQ, bool VQ>
+struct TileCfg {
+    static constexpr int NG = HD / kKGroup;
+    static constexpr int CPL = HD / 32;  // channels per lane
+    static constexpr int KROW = KQ ? HD : 4 * HD;
+    static constexpr int VROW = VQ ? HD : 4 * HD;
+    static constexpr int TR = ce_min(256, 16384 / ce_max(KROW, VROW));  // rows per tile
+    static constexpr int KS_OFF = TR * KROW;
+    static constexpr int VS_OFF = KS_OFF + (KQ ? TR * NG * 4 : 0);
+    static constexpr int KSEG = VS_OFF + (VQ ? TR * 4 : 0);
+    static constexpr int VSEG = TR * VROW;
+    static constexpr int SLOT = ce_round(ce_max(KSEG, VSEG), 128);
+};
+
+template <int HD, int HPK, bool KQ, bool VQ>
+struct SplitCfg : TileCfg<HD, KQ, VQ> {
+    using T = TileCfg<HD, KQ, VQ>;
+    static constexpr int RPW = T::TR / kWarps;             // score rows per warp per tile
+    static constexpr int RB = ce_min(32 / HPK, RPW);       // rows per reduce batch
+    static constexpr int E = RB * HPK;                     // entries per reduce (<= 32)
+    static constexpr int LOGE = ce_log2(E);
+    static constexpr int SC_OFF = kNSeg * T::SLOT;         // scores/weights [TR][HPK]
+    static constexpr int MISC_OFF = SC_OFF + T::TR * HPK * 4;
+    // misc: kNSeg mbarriers, red[kWarps][HPK], mrun[HPK], alpha[HPK], flag
+    static constexpr int SMEM = MISC_OFF + kNSeg * 8 + (kWarps + 2) * HPK * 4 + 16;
+    static_assert(kWarps * HPK * HD * 4 <= kNSeg * T::SLOT, "accumulator reduction must fit");
+    static_assert((1 << LOGE) == E, "reduce entries must be a power of two");
+};
+
+// Arguments common to every split launch.
+struct SplitArgs {
+    const float *q;        // [.., n_q, HD] query rows
+    int32_t n_q, hpk;      // query heads per sequence/stream; heads per KV group
+    float qscale;          // softmax scale * log2(e)
+    int32_t chunk;         // rows per chunk (multiple of every tile height)
+    int32_t nc_max;        // chunk slots per (sequence, group) in the partials
+    int32_t n_grp;         // groups per sequence in the partials (live heads / R-SWA heads)
+    float *pm, *pl, *pacc; // partial max, sum, accumulator
+    float *scores;         // per-row log2 scores for the imp pass, or null
+    uint32_t *err;
+};
+
+// Where one CTA's chunk lives.
+struct ChunkInfo {
+    const char *k, *v, *ks, *vs;  // global address of the chunk's first row
+    int n;                        // rows in the chunk (>= 1)
+    int64_t pidx0;                // partial index of the group's head 0
+    const float *q;               // query of the group's head 0
+    const float *kcol;            // K field of the group, or null
+    int64_t score0;               // scores index of row 0, head 0 (or -1)
+};
+
+// Butterfly reduce-scatter of E partial sums held by every lane: after it,
+// lane l holds in v[0] the full warp sum of entry l >> (5 - LOGE).
+template <int E, int LOGE>
+__device__ __forceinline__ float reduce_scatter(float (&v)[E], int lane) {
+#pragma unroll
+    for (int s = 0; s < LOGE; ++s) {
+        const int off = 16 >> s;
+        const int half = (E >> s) >> 1;
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const float send = upper ? v[i] : v[i + half];
+            const float keep = upper ? v[i + half] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+    }
+#pragma unroll
+    for (int s = LOGE; s < 5; ++s) v[0] += __shfl_xor_sync(0xffffffffu, v[0], 16 >> s);
+    return v[0];
+}
+
+// Load CPL consecutive channels of a row (lane's share) as f32.
+template <int CPL, bool Q>
+__device__ __forceinline__ void load_lane(const char *row, int lane, float (&x)[CPL]) {
+    if (Q) {
+        if (CPL == 4) {
+            const uint32_t w = reinterpret_cast<const uint32_t *>(row)[lane];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) x[j] = float(int8_t((w >> (8 * j)) & 0xffu));
+        } else {
+            const uint32_t w = reinterpret_cast<const uint16_t *>(row)[lane];
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) x[j] = float(int8_t((w >> (8 * j)) & 0xffu));
+        }
+    } else {
+        if (CPL == 4) {
+            const float4 f = reinterpret_cast<const float4 *>(row)[lane];
+            x[0] = f.x;
+            x[1] = f.y;
+            x[2] = f.z;
+            x[3] = f.w;
+        } else {
+            const float2 f = reinterpret_cast<const float2 *>(row)[lane];
+            x[0] = f.x;
+            x[1] = f.y;
+        }
+    }
+}
+
+template <int HD, int HPK, bool KQ, bool VQ>
+__device__ __forceinline__ void issue_segment(const ChunkInfo &ci, char *smem, uint64_t *bar,
+                                              int j) {
+    using C = SplitCfg<HD, HPK, KQ, VQ>;
+    const int slot = j % kNSeg;
+    const int t = j >> 1;
+    const int row0 = t * C::TR;
+    const int nt = min(C::TR, ci.n - row0);
+    const int rows = (nt + kRowAlign - 1) / kRowAlign * kRowAlign;
+    char *dst = smem + slot * C::SLOT;
+    if ((j & 1) == 0) {
+        uint32_t bytes = uint32_t(rows) * C::KROW;
+        if (KQ) bytes += uint32_t(rows) * C::NG * 4;
+        if (VQ) bytes += uint32_t(rows) * 4;
+        mbar_arrive_expect_tx(&bar[slot], bytes);
+        bulk_g2s(dst, ci.k + int64_t(row0) * C::KROW, uint32_t(rows) * C::KROW, &bar[slot]);
+        if (KQ)
+            bulk_g2s(dst + C::KS_OFF, ci.ks + int64_t(row0) * C::NG * 4, uint32_t(rows) * C::NG * 4,
+                     &bar[slot]);
+        if (VQ)
+            bulk_g2s(dst + C::VS_OFF, ci.vs + int64_t(row0) * 4, uint32_t(rows) * 4, &bar[slot]);
+    } else {
+        const uint32_t bytes = uint32_t(rows) * C::VROW;
+        mbar_arrive_expect_tx(&bar[slot], bytes);
+        bulk_g2s(dst, ci.v + int64_t(row0) * C::VROW, bytes, &bar[slot]);
+    }
+}
+
+template <int HD, int HPK, bool KQ, bool VQ>
+__device__ void split_body(const ChunkInfo &ci, const SplitArgs &a, char *smem) {
+    using C = SplitCfg<HD, HPK, KQ, VQ>;
+    constexpr int CPL = C::CPL, TR = C::TR;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    float *sc = reinterpret_cast<float *>(smem + C::SC_OFF);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + C::MISC_OFF);
+    float *red = reinterpret_cast<float *>(bar + kNSeg);
+    float *mrun = red + kWarps * HPK;
+    float *alpha = mrun + HPK;
+
+    const int n = ci.n;
+    const int ntiles = (n + TR - 1) / TR;
+    const int nseg = 2 * ntiles;
+
+    if (tid == 0) {
+        for (int s = 0; s < kNSeg; ++s) mbar_init(&bar[s], 1);
+        fence_mbar_init();
+    }
+    if (tid < HPK) mrun[tid] = -INFINITY;
+    __syncthreads();
+    if (tid == 0)
+        for (int j = 0; j < min(kNSeg, nseg); ++j) issue_segment<HD, HPK, KQ, VQ>(ci, smem, bar, j);
+
+    // Query of every head of the group for this lane's channels, with the
+    // K field and the softmax scale (in log2 units) folded in.
+    float qr[HPK][CPL];
+#pragma unroll
+    for (int h = 0; h < HPK; ++h) {
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+            float x = 0.0f;
+            if (h < a.hpk) {
+                x = ci.q[h * HD + lane * CPL + j];
+                if (KQ) x *= ci.kcol[lane * CPL + j];
+                x *= a.qscale;
+            }
+            qr[h][j] = x;
+        }
+    }
+    float acc[HPK][CPL];
+#pragma unroll
+    for (int h = 0; h < HPK; ++h)
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) acc[h][j] = 0.0f;
+    float lsum = 0.0f;  // this thread's share of the running sum of head tid % HPK
+    bool ok = true;
+
+    for (int t = 0; t < ntiles && ok; ++t) {
+        const int row0 = t * TR;
+        const int nt = min(TR, n - row0);
+        // ---------------------------------------------------- K tile
+        int j = 2 * t;
+        int slot = j % kNSeg;
+        // Every thread waits; the give-up decision is made block-wide so that
+        // no thread leaves the loop while others sit in a barrier.
+        if (__syncthreads_or(!mbar_wait_bounded(&bar[slot], (j / kNSeg) & 1))) {
+            ok = false;
+            break;
+        }
+        const char *kseg = smem + slot * C::SLOT;
+#pragma unroll 1
+        for (int bt = 0; bt < C::RPW / C::RB; ++bt) {
+            const int rbase = warp * C::RPW + bt * C::RB;
+            float v[C::E];
+#pragma unroll
+            for (int r = 0; r < C::RB; ++r) {
+                float x[CPL];
+                load_lane<CPL, KQ>(kseg + (rbase + r) * C::KROW, lane, x);
+                float gs = 1.0f;
+                if (KQ)
+                    gs = reinterpret_cast<const float *>(kseg + C::KS_OFF)[(rbase + r) * C::NG +
+                                                                           (lane * CPL) / kKGroup];
+#pragma unroll
+                for (int h = 0; h < HPK; ++h) {
+                    float p = 0.0f;
+#pragma unroll
+                    for (int jj = 0; jj < CPL; ++jj) p = fmaf(qr[h][jj], x[jj], p);
+                    v[r * HPK + h] = KQ ? p * gs : p;
+                }
+            }
+            const float s = reduce_scatter<C::E, C::LOGE>(v, lane);
+            if ((lane & ((32 >> C::LOGE) - 1)) == 0) {
+                const int e = lane >> (5 - C::LOGE);
+                const int r = rbase + e / HPK, h = e % HPK;
+                const float sv = r < nt ? s : -INFINITY;
+                sc[r * HPK + h] = sv;
+                if (a.scores != nullptr && r < nt && h < a.hpk)
+                    a.scores[ci.score0 + int64_t(row0 + r) * a.hpk + h] = sv;
+            }
+        }
+        __syncthreads();
+        // ------------------------------------------- tile max per head
+        {
+            const int h = tid % HPK;
+            float mx = -INFINITY;
+            for (int r = tid / HPK; r < nt; r += kThreads / HPK) mx = fmaxf(mx, sc[r * HPK + h]);
+#pragma unroll
+            for (int off = HPK; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            if (lane < HPK) red[warp * HPK + lane] = mx;
+        }
+        __syncthreads();
+        if (tid < HPK) {
+            float mx = red[tid];
+#pragma unroll
+            for (int w = 1; w < kWarps; ++w) mx = fmaxf(mx, red[w * HPK + tid]);
+            const float mo = mrun[tid];
+            const float mn = fmaxf(mo, mx);
+            alpha[tid] = (mo == -INFINITY) ? 0.0f : exp2f(mo - mn);
+            mrun[tid] = mn;
+        }
+        __syncthreads();
+        // --------------------- weights exp2(s - max) (x V row scale), sums
+        {
+            const int h = tid % HPK;
+            const float mn = mrun[h];
+            lsum *= alpha[h];
+            const float *vsr = reinterpret_cast<const float *>(kseg + C::VS_OFF);
+            for (int r = tid / HPK; r < nt; r += kThreads / HPK) {
+                const float e = exp2f(sc[r * HPK + h] - mn);
+                lsum += e;
+                sc[r * HPK + h] = VQ ? e * vsr[r] : e;
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < HPK; ++h) {
+            const float al = alpha[h];
+#pragma unroll
+            for (int jj = 0; jj < CPL; ++jj) acc[h][jj] *= al;
+        }
+        __syncthreads();  // K slot drained, weights visible
+        if (tid == 0 && j + kNSeg < nseg) issue_segment<HD, HPK, KQ, VQ>(ci, smem, bar, j + kNSeg);
+        // ---------------------------------------------------- V tile
+        j = 2 * t + 1;
+        slot = j % kNSeg;
+        if (__syncthreads_or(!mbar_wait_bounded(&bar[slot], (j / kNSeg) & 1))) {
+            ok = false;
+            break;
+        }
+        const char *vseg = smem + slot * C::SLOT;
+        for (int r = warp; r < nt; r += kWarps) {
+            float x[CPL];
+            load_lane<CPL, VQ>(vseg + r * C::VROW, lane, x);
+            float w[HPK];
+            if (HPK % 4 == 0) {
+#pragma unroll
+                for (int h = 0; h < HPK; h += 4) {
+                    const float4 w4 = *reinterpret_cast<const float4 *>(&sc[r * HPK + h]);
+                    w[h] = w4.x;
+                    w[h + 1] = w4.y;
+                    w[h + 2] = w4.z;
+                    w[h + 3] = w4.w;
+                }
+            } else {
+#pragma unroll
+                for (int h = 0; h < HPK; ++h) w[h] = sc[r * HPK + h];
+            }
+#pragma unroll
+            for (int h = 0; h < HPK; ++h)
+#pragma unroll
+                for (int jj = 0; jj < CPL; ++jj) acc[h][jj] = fmaf(w[h], x[jj], acc[h][jj]);
+        }
+        __syncthreads();  // V slot drained
+        if (tid == 0 && j + kNSeg < nseg) issue_segment<HD, HPK, KQ, VQ>(ci, smem, bar, j + kNSeg);
+    }
+
+    if (!ok) {  // block-uniform (decided by __syncthreads_or above)
+        // A copy never completed: record it, give the copies still in flight a
+        // bounded chance to land (so none writes into a successor CTA's
+        // shared memory), and leave without a partial.
+        if (tid == 0) {
+            set_error(a.err, kErrTimeout);
+            for (int s = 0; s < kNSeg; ++s) (void)mbar_wait_bounded(&bar[s], 0, 100000000ull);
+            for (int s = 0; s < kNSeg; ++s) (void)mbar_wait_bounded(&bar[s], 1, 100000000ull);
+        }
+        return;
+    }
+
+    // ------------------------------------------------------ partial out
+    {
+        const int h = tid % HPK;
+        float l = lsum;
+#pragma unroll
+        for (int off = HPK; off < 32; off <<= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+        if (lane < HPK) red[warp * HPK + lane] = l;
+    }
+    float *accs = reinterpret_cast<float *>(smem);  // [kWarps][HPK][HD], reuses the slots
+#pragma unroll
+    for (int h = 0; h < HPK; ++h)
+#pragma unroll
+        for (int jj = 0; jj < CPL; ++jj) accs[(warp * HPK + h) * HD + lane * CPL + jj] = acc[h][jj];
+    __syncthreads();
+    if (tid < a.hpk && tid < HPK) {
+        float l = red[tid];
+#pragma unroll
+        for (int w = 1; w < kWarps; ++w) l += red[w * HPK + tid];
+        a.pm[ci.pidx0 + tid] = mrun[tid];
+        a.pl[ci.pidx0 + tid] = l;
+    }
+    for (int i = tid; i < a.hpk * HD; i += kThreads) {
+        const int h = i / HD, d = i % HD;
+        float s = accs[h * HD + d];
+#pragma unroll
+        for (int w = 1; w < kWarps; ++w) s += accs[(w * HPK + h) * HD + d];
+        a.pacc[(ci.pidx0 + h) * HD + d] = s;
+    }
+}
+
+// ---------------------------------------------------------------- layer
+
+struct LayerSrc {
+    const float *kf, *vf;
+    const int8_t *kq, *vq;
+    const float *ks, *vs, *kcol;
+    const int64_t *row_base, *cap;
+    const int32_t *seq_len, *live;
+    int32_t n_live;
+};
+
+template <int HD, int HPK, bool KQ, bool VQ>
+__global__ void __launch_bounds__(kThreads, 2) split_layer_kernel(SplitArgs a, LayerSrc src) {
+    extern __shared__ __align__(128) char smem[];
+    const int b = blockIdx.z, gl = blockIdx.y, c = blockIdx.x;
+    const int L = src.seq_len[b];
+    const int64_t r0 = int64_t(c) * a.chunk;
+    if (r0 >= L) return;
+    const int64_t cap = src.cap[b];
+    if (L > cap) {
+        if (threadIdx.x == 0) set_error(a.err, kErrBounds);
+        return;
+    }
+    const int64_t row = src.row_base[b] + int64_t(gl) * cap + r0;
+    ChunkInfo ci;
+    ci.k = KQ ? reinterpret_cast<const char *>(src.kq + row * HD)
+              : reinterpret_cast<const char *>(src.kf + row * HD);
+    ci.v = VQ ? reinterpret_cast<const char *>(src.vq + row * HD)
+              : reinterpret_cast<const char *>(src.vf + row * HD);
+    ci.ks = KQ ? reinterpret_cast<const char *>(src.ks + row * (HD / kKGroup)) : nullptr;
+    ci.vs = VQ ? reinterpret_cast<const char *>(src.vs + row) : nullptr;
+    ci.n = int(a.chunk < L - r0 ? int64_t(a.chunk) : L - r0);
+    ci.pidx0 = ((int64_t(b) * a.n_grp + gl) * a.nc_max + c) * a.hpk;
+    const int g = src.live[gl];
+    ci.q = a.q + (int64_t(b) * a.n_q + int64_t(g) * a.hpk) * HD;
+    ci.kcol = KQ ? src.kcol + (int64_t(b) * src.n_live + gl) * HD : nullptr;
+    ci.score0 = row * a.hpk;
+    split_body<HD, HPK, KQ, VQ>(ci, a, smem);
+}
+
+// ---------------------------------------------------------------- R-SWA
+
+struct RswaTable {
+    int32_t s0, n;                // first stream of the launch, streams in it
+    int32_t prefill_len[kSlice];  // reference rows per stream
+    int32_t ring_len[kSlice];     // ring rows per stream
+};
+
+struct RswaSrc {
+    const float *ref_k, *ref_v, *ring_k, *ring_v;
+    int64_t ref_cap;
+    int32_t W, H;
+};
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 2) split_rswa_kernel(SplitArgs a, RswaSrc src,
+                                                                 RswaTable tb) {
+    extern __shared__ __align__(128) char smem[];
+    const int si = blockIdx.z, h = blockIdx.y, c = blockIdx.x;
+    if (si >= tb.n) return;
+    const int s = tb.s0 + si;
+    const int pl = tb.prefill_len[si], rl = tb.ring_len[si];
+    const int ncp = (pl + a.chunk - 1) / a.chunk;
+    const int ncr = (rl + a.chunk - 1) / a.chunk;
+    ChunkInfo ci;
+    const int64_t head = int64_t(s) * src.H + h;
+    if (c < ncp) {
+        const int64_t row = head * src.ref_cap + int64_t(c) * a.chunk;
+        ci.k = reinterpret_cast<const char *>(src.ref_k + row * HD);
+        ci.v = reinterpret_cast<const char *>(src.ref_v + row * HD);
+        ci.n = min(a.chunk, pl - c * a.chunk);
+    } else if (c - ncp < ncr) {
+        const int cr = c - ncp;
+        const int64_t row = head * src.W + int64_t(cr) * a.chunk;
+        ci.k = reinterpret_cast<const char *>(src.ring_k + row * HD);
+        ci.v = reinterpret_cast<const char *>(src.ring_v + row * HD);
+        ci.n = min(a.chunk, rl - cr * a.chunk);
+    } else {
+        return;
+    }
+    ci.ks = ci.vs = nullptr;
+    ci.pidx0 = (head * a.nc_max + c) * 1;
+    ci.q = a.q + head * HD;
+    ci.kcol = nullptr;
+    ci.score0 = -1;
+    split_body<HD, 1, false, false>(ci, a, smem);
+}
+
+// ---------------------------------------------------------------- merge
+
+struct MergeArgs {
+    const float *pm, *pl, *pacc;
+    float *out;     // [.., n_q, HD]
+    float *ml;      // (max, sum) per (sequence, query head) for the imp pass, or null
+    int32_t n_q, hpk, n_grp, nc_max, chunk;
+};
+
+// Log-sum-exp merge of the chunk partials of one (sequence, query head):
+// out[d] = field[d] * sum_c acc_c[d] 2^(m_c - M) / sum_c l_c 2^(m_c - M).
+template <int HD>
+__device__ void merge_body(const MergeArgs &a, int b, int h, int grp, int nc, const float *vcol) {
+    const int d = threadIdx.x;
+    float *o = a.out + (int64_t(b) * a.n_q + h) * HD;
+    if (grp < 0 || nc == 0) {
+        o[d] = 0.0f;
+        if (a.ml && d == 0) {
+            a.ml[(int64_t(b) * a.n_q + h) * 2] = -INFINITY;
+            a.ml[(int64_t(b) * a.n_q + h) * 2 + 1] = 0.0f;
+        }
+        return;
+    }
+    const int hh = h % a.hpk;
+    const int64_t p0 = (int64_t(b) * a.n_grp + grp) * a.nc_max * a.hpk + hh;
+    float M = -INFINITY;
+    for (int c = 0; c < nc; ++c) M = fmaxf(M, a.pm[p0 + int64_t(c) * a.hpk]);
+    float Ls = 0.0f, s = 0.0f;
+    for (int c = 0; c < nc; ++c) {
+        const int64_t p = p0 + int64_t(c) * a.hpk;
+        const float f = exp2f(a.pm[p] - M);
+        Ls = fmaf(a.pl[p], f, Ls);
+        s = fmaf(a.pacc[p * HD + d], f, s);
+    }
+    float r = s / Ls;
+    if (vcol) r *= vcol[d];
+    o[d] = r;
+    if (a.ml && d == 0) {
+        a.ml[(int64_t(b) * a.n_q + h) * 2] = M;
+        a.ml[(int64_t(b) * a.n_q + h) * 2 + 1] = Ls;
+    }
+}
+
+struct MergeLayerSrc {
+    const int32_t *seq_len, *slot;
+    const float *vcol;  // [n_seq][n_live][HD] or null
+    int32_t n_live;
+};
+
+template <int HD>
+__global__ void __launch_bounds__(HD) merge_layer_kernel(MergeArgs a, MergeLayerSrc src) {
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int L = src.seq_len[b];
+    const int grp = src.slot[h / a.hpk];
+    const int nc = (L + a.chunk - 1) / a.chunk;
+    const float *vcol = (src.vcol && grp >= 0) ? src.vcol + (int64_t(b) * src.n_live + grp) * HD : nullptr;
+    merge_body<HD>(a, b, h, grp, nc, vcol);
+}
+
+template <int HD>
+__global__ void __launch_bounds__(HD) merge_rswa_kernel(MergeArgs a, RswaTable tb) {
+    const int h = blockIdx.x, si = blockIdx.y;
+    if (si >= tb.n) return;
+    const int s = tb.s0 + si;
+    const int nc = (tb.prefill_len[si] + a.chunk - 1) / a.chunk +
+                   (tb.ring_len[si] + a.chunk - 1) / a.chunk;
+    merge_body<HD>(a, s, h, h, nc, nullptr);
+}
+
+// Host launcher for one instance (instantiated per storage mode in its own unit).
+template <int HD, int HPK, bool KQ, bool VQ>
+cudaError_t launch_split_layer_impl(const SplitArgs &a, const LayerSrc &s, dim3 grid,
+                                    cudaStream_t st) {
+    using C = SplitCfg<HD, HPK, KQ, VQ>;
+    auto kern = split_layer_kernel<HD, HPK, KQ, VQ>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kThreads, C::SMEM, st>>>(a, s);
+    return cudaGetLastError();
+}
+
+}  // namespace kvd

@@ -1,0 +1,139 @@
+// kvd_internal.cuh -- private declarations shared by the library's .cu files.
+//
+// Layer metadata, the device error word, and the sm_100-family PTX helpers
+// used by the kernels: mbarrier waits with a time limit, and 1-D bulk
+// asynchronous global->shared copies (the TMA bulk-copy engine).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvd.h"
+
+namespace kvd {
+
+constexpr int kColWarmup = 64;  // cortiq KV_COL_WARMUP: rows before the fields freeze
+constexpr int kKGroup = 32;     // cortiq KV_K_GROUP: K channels per scale
+constexpr int kRowAlign = 16;   // per-sequence capacity is rounded to this many rows
+constexpr int kMaxHpk = 16;     // query heads per KV head handled by the kernels
+constexpr int kSlice = 256;     // sequences/streams described per launch (kernel params)
+
+// Device error-word bits.
+constexpr uint32_t kErrTimeout = 1u;
+constexpr uint32_t kErrBounds = 2u;
+
+inline bool quant_k(int mode) { return mode == KVD_Q8 || mode == KVD_Q8K; }
+inline bool quant_v(int mode) { return mode == KVD_Q8 || mode == KVD_Q8V; }
+
+// Device metadata block (KVD_BUF_META), laid out by layer_meta_layout().
+struct MetaLayout {
+    int64_t row_base;  // int64[n_seq]   first storage row of sequence b
+    int64_t cap;       // int64[n_seq]   rows per live head of sequence b
+    int64_t imp_base;  // int64[n_seq]   first imp entry of sequence b
+    int64_t seq_len;   // int32[n_seq]   rows stored
+    int64_t frozen;    // int32[n_seq]   1 once the fields are set
+    int64_t live;      // int32[n_kv]    live slot -> KV head
+    int64_t slot;      // int32[n_kv]    KV head -> live slot (-1 = dead)
+    int64_t err;       // uint32          device error word
+    int64_t total;     // bytes
+};
+
+// Private view of kvd_layer.
+struct Layer {
+    int32_t magic;
+    int32_t mode, n_seq, n_kv, hd, n_live, ng;
+    int32_t pad0;
+    int64_t total_rows;  // sum_b n_live * cap_b
+    int64_t imp_len;     // sum_b cap_b
+    int64_t max_cap;     // max_b cap_b
+    void *buf[KVD_BUF_COUNT];
+    MetaLayout ml;
+    // host state block
+    int64_t *h_cap, *h_row_base, *h_imp_base, *h_seq_len;
+    int32_t *h_frozen, *h_live, *h_slot;
+    uint8_t *h_alive;
+    // device pointers into the metadata block
+    int64_t *d_row_base, *d_cap;
+    int32_t *d_seq_len, *d_frozen, *d_live, *d_slot;
+    uint32_t *d_err;
+};
+static_assert(sizeof(Layer) <= sizeof(kvd_layer), "kvd_layer too small");
+constexpr int32_t kLayerMagic = 0x4b564431;  // "KVD1"
+
+inline Layer *as_layer(kvd_layer *L) { return reinterpret_cast<Layer *>(L); }
+inline const Layer *as_layer(const kvd_layer *L) { return reinterpret_cast<const Layer *>(L); }
+const Layer *checked_layer(const kvd_layer *L);
+Layer *checked_layer(kvd_layer *L);
+
+inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// ---------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+                     smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for phase `parity` of `bar` to complete, giving up after `limit_ns`
+// nanoseconds of wall time.  Returns false on time-out (the caller records
+// kErrTimeout and unwinds; no trap).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  uint64_t limit_ns = 2000000000ull) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// 1-D bulk asynchronous copy global -> shared (cp.async.bulk), completing
+// `bytes` of transaction count on `bar`.  dst, src and bytes must be
+// multiples of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
+                                         uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void set_error(uint32_t *err, uint32_t bit) {
+    if (err) atomicOr(err, bit);
+}
+
+}  // namespace kvd

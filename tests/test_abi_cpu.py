@@ -1,0 +1,128 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports every
+entry point include/kvd.h declares, and its host validation returns the
+documented status codes before touching the device (no device buffer is ever
+dereferenced here: every call below fails validation or only computes sizes)."""
+
+import ctypes as C
+import os
+
+import numpy as np
+import pytest
+
+from conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def abi():
+    from kv_cache_decode_attention_gb300 import _abi
+    from kv_cache_decode_attention_gb300.build import build
+
+    build()
+    return _abi
+
+
+def test_library_exports_every_declared_symbol(abi):
+    names = abi.declared_symbols()
+    assert len(names) >= 16
+    L = abi.lib()
+    for n in names:
+        assert hasattr(L, n), n
+    # and the binding declares exactly those
+    assert set(abi._SIGS) == set(names)
+
+
+def test_header_has_no_torch_types():
+    text = open(os.path.join(ROOT, "include", "kvd.h")).read()
+    for bad in ("torch", "at::", "Tensor", "c10"):
+        assert bad not in text
+
+
+def _bytes(abi, n_seq, n_kv, hd, mode, cap, alive=None):
+    cap = np.ascontiguousarray(cap, np.int64)
+    out = np.zeros(abi.BUF_COUNT, np.int64)
+    hb = C.c_int64(0)
+    al = None if alive is None else C.c_void_p(np.ascontiguousarray(alive, np.uint8).ctypes.data)
+    st = abi.lib().kvd_layer_bytes(n_seq, n_kv, hd, mode, C.c_void_p(cap.ctypes.data), al,
+                                   C.c_void_p(out.ctypes.data), C.byref(hb))
+    return st, out, hb.value
+
+
+def test_layer_bytes_layout(abi):
+    # q8 (K and V int8), hd 128, 2 sequences of 100 (-> 112) and 16 rows, 8 heads, 2 dead
+    alive = np.array([1, 1, 0, 1, 1, 1, 0, 1], np.uint8)
+    st, out, hb = _bytes(abi, 2, 8, 128, abi.Q8, [100, 16], alive)
+    assert st == abi.OK
+    rows = (112 + 16) * 6 + 16  # live rows + spare rows
+    r256 = lambda x: (x + 255) // 256 * 256
+    assert out[abi.BUF_KQ] == r256(rows * 128) and out[abi.BUF_VQ] == r256(rows * 128)
+    assert out[abi.BUF_KS] == r256(rows * 4 * 4) and out[abi.BUF_VS] == r256(rows * 4)
+    assert out[abi.BUF_K] == 0 and out[abi.BUF_V] == 0
+    assert out[abi.BUF_KCOL] == r256(2 * 6 * 128 * 4)
+    assert out[abi.BUF_META] > 0 and hb > 0
+    st, out, _ = _bytes(abi, 1, 2, 64, abi.F32, [256])
+    assert out[abi.BUF_K] == r256((256 * 2 + 16) * 64 * 4) and out[abi.BUF_KQ] == 0
+    st, out, _ = _bytes(abi, 1, 2, 64, abi.Q8K, [256])
+    assert out[abi.BUF_KQ] > 0 and out[abi.BUF_V] > 0 and out[abi.BUF_VQ] == 0 and out[abi.BUF_VCOL] == 0
+
+
+@pytest.mark.parametrize("args", [
+    (0, 8, 128, 1, [10]),     # no sequences
+    (1, 0, 128, 1, [10]),     # no heads
+    (1, 8, 96, 1, [10]),      # unsupported head_dim
+    (1, 8, 128, 7, [10]),     # bad mode
+    (1, 8, 128, 1, [-1]),     # negative capacity
+])
+def test_layer_bytes_rejects(abi, args):
+    st, _, _ = _bytes(abi, *args)
+    assert st == abi.EINVAL
+
+
+def test_rswa_host_validation_before_any_launch(abi):
+    L = abi.lib()
+    B, H, hd, W = 2, 10, 128, 128
+    pl = np.array([-1, 5], np.int32)
+    rl = np.zeros(B, np.int32)
+    rp = np.zeros(B, np.int32)
+    fake = C.c_void_p(1 << 20)  # never dereferenced: validation fails first
+    p = lambda a: C.c_void_p(a.ctypes.data)
+    # a stream without prefill: ESTATE and the cursors stay untouched
+    st = L.rswa_ring_write(fake, fake, fake, fake, p(pl), p(rl), p(rp), B, H, hd, W, None, None)
+    assert st == abi.ESTATE and rl.tolist() == [0, 0] and rp.tolist() == [0, 0]
+    n = C.c_int64(0)
+    assert L.rswa_decode_workspace_bytes(B, H, hd, 32640, W, C.byref(n)) == abi.OK and n.value > 0
+    ws = C.c_void_p(1 << 21)
+    st = L.rswa_decode(fake, fake, fake, fake, fake, p(pl), p(rl), p(rp), B, H, hd, 32640, W,
+                       C.c_float(0.088), fake, ws, n.value, None)
+    assert st == abi.ESTATE
+    pl[:] = [0, 5]
+    st = L.rswa_decode(fake, fake, fake, fake, fake, p(pl), p(rl), p(rp), B, H, hd, 32640, W,
+                       C.c_float(0.088), fake, ws, n.value, None)
+    assert st == abi.EEMPTY  # stream 0: no keys
+    # capacity: a prefill longer than the reference block
+    st = L.rswa_record_prefill(fake, fake, fake, fake, 0, 33000, B, H, hd, 32640, W, p(pl), p(rl),
+                               p(rp), None)
+    assert st == abi.ECAPACITY and pl.tolist() == [0, 5]
+    # ragged region sizes are refused (bulk copies move 16-row groups)
+    pl[:] = [3, 5]
+    st = L.rswa_decode(fake, fake, fake, fake, fake, p(pl), p(rl), p(rp), B, H, hd, 1000, 100,
+                       C.c_float(0.088), fake, ws, n.value, None)
+    assert st == abi.EINVAL
+
+
+def test_layer_calls_reject_uninitialised_descriptor(abi):
+    L = abi.lib()
+    lay = abi.kvd_layer()  # zeroed: not initialised
+    n = C.c_int64(0)
+    assert L.kvd_decode_workspace_bytes(C.byref(lay), 8, 0, C.byref(n)) == abi.EINVAL
+    assert L.kv_append(C.byref(lay), C.c_void_p(16), C.c_void_p(16), None, None) == abi.EINVAL
+    assert L.kv_freeze_colfield(C.byref(lay), None) == abi.EINVAL
+    assert L.kvd_status_string(abi.ECAPACITY) == b"capacity exceeded"
+
+
+def test_api_fails_loudly_without_library(tmp_path, monkeypatch):
+    from kv_cache_decode_attention_gb300 import _abi
+
+    monkeypatch.setattr(_abi, "_lib", None)
+    monkeypatch.setattr(_abi, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        _abi.lib()

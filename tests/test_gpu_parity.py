@@ -1,0 +1,287 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle, element by
+element, on seeded inputs that span several tiles, several chunks and ragged
+tails, plus the edge cases (empty and one-row sequences, exactly 64 rows, dead
+groups, every storage mode, head_dim 64 and 128, 1..16 query heads per group).
+"""
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+from helpers import (OUT_TOL, assert_imp_close, assert_storage_bitexact, gpu_append_bulk,
+                     gpu_append_stepwise, oracle_caches, out_error, seq_rows)
+
+pytestmark = pytest.mark.gpu
+
+MODES = {"f32": oracle.F32, "q8": oracle.Q8, "q8k": oracle.Q8K, "q8v": oracle.Q8V}
+
+
+@pytest.fixture(scope="module")
+def torch():
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    return torch
+
+
+@pytest.fixture(scope="module")
+def kvd(torch):
+    import kv_cache_decode_attention_gb300 as kvd
+    from kv_cache_decode_attention_gb300.build import build
+
+    build()
+    return kvd
+
+
+def _layer(kvd, mode, lengths, n_kv, hd, alive, cap_extra=0):
+    cap = [max(int(L) + cap_extra, 1) for L in lengths]
+    return kvd.LayerKvCache(len(lengths), n_kv, hd, mode, cap, alive=alive)
+
+
+@pytest.mark.parametrize("mode", list(MODES))
+@pytest.mark.parametrize("hd", [128, 64])
+@pytest.mark.parametrize("how", ["stepwise", "bulk"])
+def test_append_and_freeze_bitexact(torch, kvd, mode, hd, how):
+    lengths = [0, 1, 63, 64, 65, 130, 300]
+    n_kv, alive = 4, np.array([1, 0, 1, 1], np.uint8)
+    ks, vs = seq_rows(lengths, n_kv, hd, seed=5)
+    layer = _layer(kvd, MODES[mode], lengths, n_kv, hd, alive, cap_extra=7)
+    # canary: unwritten storage holds NaN bit patterns, never read as data
+    for b in layer.bufs[:6]:
+        if b is not None:
+            b.fill_(0xFF)
+    if how == "stepwise":
+        gpu_append_stepwise(layer, ks, vs, torch)
+    else:
+        gpu_append_bulk(layer, ks, vs, torch, pieces=(0.3, 0.75, 1.0))
+    torch.cuda.synchronize()
+    ocs = oracle_caches(MODES[mode], lengths, n_kv, hd, alive, ks, vs, cap=max(lengths) + 8)
+    assert_storage_bitexact(layer, ocs, torch)
+    assert layer.memory_bytes() == sum(o.memory_bytes() for o in ocs)
+    assert layer.device_error() == 0
+
+
+def test_explicit_freeze_is_idempotent_and_matches_oracle(torch, kvd):
+    lengths = [64, 70, 10]
+    n_kv, hd = 2, 128
+    ks, vs = seq_rows(lengths, n_kv, hd, seed=6)
+    layer = _layer(kvd, oracle.Q8, lengths, n_kv, hd, None, cap_extra=4)
+    gpu_append_bulk(layer, ks, vs, torch)
+    assert [layer.frozen(b) for b in range(3)] == [False, True, False]
+    kvd.kv_freeze_colfield(layer)
+    kvd.kv_freeze_colfield(layer)
+    torch.cuda.synchronize()
+    ocs = oracle_caches(oracle.Q8, lengths, n_kv, hd, None, ks, vs, cap=80)
+    for oc in ocs:
+        oc.freeze_if_due()
+    assert [layer.frozen(b) for b in range(3)] == [True, True, False]
+    assert_storage_bitexact(layer, ocs, torch)
+
+
+def _decode_case(torch, kvd, mode, hd, hpk, lengths, alive, seed, with_imp=True):
+    n_kv = len(alive)
+    n_q = n_kv * hpk
+    ks, vs = seq_rows(lengths, n_kv, hd, seed=seed)
+    layer = _layer(kvd, mode, lengths, n_kv, hd, alive, cap_extra=3)
+    for b in layer.bufs[:6]:
+        if b is not None:
+            b.fill_(0xFF)
+    gpu_append_bulk(layer, ks, vs, torch, pieces=(0.5, 1.0))
+    q = synthetic.normal((len(lengths), n_q, hd), seed + 77)
+    imp0 = synthetic.rng(seed + 78).uniform(0.0, 2.0, layer.imp_len).astype(np.float32)
+    qd = torch.from_numpy(q).cuda()
+    imp = torch.from_numpy(imp0).cuda() if with_imp else None
+    scale = 1.0 / math.sqrt(hd)
+    out = kvd.decode_attention(qd, layer, imp=imp, scale=scale)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    out = out.cpu().numpy()
+    ocs = oracle_caches(mode, lengths, n_kv, hd, alive, ks, vs, cap=max(lengths) + 4)
+    assert_storage_bitexact(layer, ocs, torch)
+    ref = np.zeros((len(lengths), n_q, hd))
+    live_mask = np.zeros((len(lengths), n_q), bool)
+    imp_ref = imp0.astype(np.float64).copy()
+    for b, oc in enumerate(ocs):
+        ib = int(layer.imp_base[b])
+        seg = imp_ref[ib:ib + max(lengths[b], 1)].copy() if lengths[b] else None
+        ref[b] = oc.decode(q[b], n_q, np.float32(scale), seg)
+        if seg is not None:
+            imp_ref[ib:ib + lengths[b]] = seg[:lengths[b]]
+        for h in range(n_q):
+            live_mask[b, h] = bool(alive[h // hpk]) and lengths[b] > 0
+    # dead groups and empty sequences: exact zeros
+    assert np.all(out[~live_mask] == 0.0)
+    err = out_error(out, ref, live_mask)
+    assert err <= OUT_TOL, err
+    if with_imp:
+        got = imp.cpu().numpy()
+        for b in range(len(lengths)):
+            ib = int(layer.imp_base[b])
+            assert_imp_close(got[ib:ib + lengths[b]], imp_ref[ib:ib + lengths[b]])
+        # rows beyond each sequence are untouched
+        untouched = np.ones(layer.imp_len, bool)
+        for b in range(len(lengths)):
+            ib = int(layer.imp_base[b])
+            untouched[ib:ib + lengths[b]] = False
+        assert np.array_equal(got[untouched], imp0[untouched])
+    return err
+
+
+@pytest.mark.parametrize("mode", list(MODES))
+@pytest.mark.parametrize("hpk", [1, 3, 4, 16])
+def test_decode_parity_hd128(torch, kvd, mode, hpk):
+    _decode_case(torch, kvd, MODES[mode], 128, hpk, [0, 1, 64, 300, 777, 1030],
+                 np.array([1, 1, 0, 1], np.uint8), seed=11 + hpk)
+
+
+@pytest.mark.parametrize("mode", list(MODES))
+@pytest.mark.parametrize("hpk", [2, 8])
+def test_decode_parity_hd64(torch, kvd, mode, hpk):
+    _decode_case(torch, kvd, MODES[mode], 64, hpk, [5, 257, 600], np.array([0, 1, 1], np.uint8),
+                 seed=21 + hpk)
+
+
+def test_tiny_f32_gqa_config(torch, kvd):
+    """Tiny f32 GQA decode: 1 sequence, 4 Q / 2 KV heads, head_dim 64, 256 rows,
+    K, V, q ~ N(0,1) from seed 0, scale 1/sqrt(64), output [4 x 64] plus imp[256]."""
+    n_kv, hd, hpk, L = 2, 64, 2, 256
+    k = synthetic.normal((L, n_kv, hd), 0)
+    v = synthetic.normal((L, n_kv, hd), 1)
+    q = synthetic.normal((1, n_kv * hpk, hd), 2)
+    layer = kvd.LayerKvCache(1, n_kv, hd, "f32", L)
+    kvd.kv_append(layer, torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda(), [L])
+    imp = torch.zeros(layer.imp_len, device="cuda")
+    out = kvd.decode_attention(torch.from_numpy(q).cuda(), layer, imp=imp, scale=0.125)
+    torch.cuda.synchronize()
+    oc = oracle.OracleSeqCache(oracle.F32, n_kv, hd, L)
+    oc.append_rows(k, v)
+    imp_ref = np.zeros(L)
+    ref = oc.decode(q[0], n_kv * hpk, np.float32(0.125), imp_ref)
+    assert out_error(out.cpu().numpy()[0], ref) <= OUT_TOL
+    got = imp.cpu().numpy()[:L]
+    assert_imp_close(got, imp_ref)
+    assert abs(got.sum() - n_kv * hpk) < 1e-3  # every head's weights sum to one
+
+
+def test_all_groups_dead_and_capacity_errors(torch, kvd):
+    layer = kvd.LayerKvCache(2, 2, 128, "q8", [8, 8], alive=[0, 0])
+    k = torch.randn(2, 2, 128, device="cuda")
+    for _ in range(3):
+        kvd.kv_append(layer, k, k)
+    out = kvd.decode_attention(torch.randn(2, 4, 128, device="cuda"), layer)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(out).item() == 0
+    assert layer.memory_bytes() == 0 and layer.seq_len(0) == 3
+    # capacity (8 rounds up to 16 rows): a bulk append that would overflow
+    # sequence 1 changes nothing, not even sequence 0's length
+    with pytest.raises(kvd.KvdError) as e:
+        kvd.kv_append(layer, torch.randn(15, 2, 128, device="cuda"),
+                      torch.randn(15, 2, 128, device="cuda"), [1, 14])
+    assert e.value.status == -2
+    assert layer.seq_len(0) == 3 and layer.seq_len(1) == 3
+    with pytest.raises(kvd.KvdError):  # 3 query heads for 2 KV heads
+        kvd.decode_attention(torch.randn(2, 3, 128, device="cuda"), layer)
+
+
+# ------------------------------------------------------------------- R-SWA
+
+def rope(x, pos, base=10000.0):
+    hd = x.shape[-1]
+    i = np.arange(hd // 2, dtype=np.float64)
+    th = pos * base ** (-2.0 * i / hd)
+    c, s = np.cos(th), np.sin(th)
+    a, b = x[..., 0::2].astype(np.float64), x[..., 1::2].astype(np.float64)
+    out = np.empty(x.shape, np.float64)
+    out[..., 0::2] = a * c - b * s
+    out[..., 1::2] = a * s + b * c
+    return out.astype(np.float32)
+
+
+def test_rswa_ring_and_decode_parity(torch, kvd):
+    """Three streams with different reference lengths (one empty); 300 decode steps
+    wrap the ring (K rotated at the true absolute position by the harness); the
+    device ring, its cursors and every decode step's output match the oracle."""
+    B, H, hd, W, ref_cap = 3, 10, 128, 128, 1024
+    prefill = [37, 0, 700]
+    cache = kvd.RingCache(B, ref_cap, H, hd, W)
+    o_ref_k = np.zeros((B, H, ref_cap, hd), np.float32)
+    o_ref_v = np.zeros_like(o_ref_k)
+    o_ring_k = np.zeros((B, H, W, hd), np.float32)
+    o_ring_v = np.zeros_like(o_ring_k)
+    cursors = [np.zeros(2, np.int32) for _ in range(B)]
+    for s in range(B):
+        m = prefill[s]
+        k = np.stack([rope(synthetic.normal((H, hd), 100 * s + r), r) for r in range(m)], axis=1) \
+            if m else np.zeros((H, 0, hd), np.float32)
+        v = synthetic.normal((H, m, hd), 100 * s + 99)
+        kvd.rswa_record_prefill(cache, s, torch.from_numpy(np.ascontiguousarray(k)).cuda(),
+                                torch.from_numpy(v).cuda())
+        o_ref_k[s, :, :m] = k
+        o_ref_v[s, :, :m] = v
+    scale = np.float32(1.0 / math.sqrt(hd))
+    worst = 0.0
+    for t in range(300):
+        kt = np.stack([rope(synthetic.normal((H, hd), 5000 + 7 * t + s), prefill[s] + t) for s in range(B)])
+        vt = synthetic.normal((B, H, hd), 9000 + t)
+        qt = np.stack([rope(synthetic.normal((H, hd), 13000 + 7 * t + s), prefill[s] + t) for s in range(B)])
+        slots = kvd.rswa_ring_write(cache, torch.from_numpy(kt).cuda(), torch.from_numpy(vt).cuda())
+        for s in range(B):
+            assert slots[s] == oracle.rswa_write(o_ring_k[s], o_ring_v[s], kt[s], vt[s], True, cursors[s])
+            assert cache.ring_len[s] == cursors[s][0] and cache.ring_pos[s] == cursors[s][1]
+        if t in (0, 1, 127, 128, 200, 299):
+            out = kvd.rswa_decode(torch.from_numpy(qt).cuda(), cache).cpu().numpy()
+            for s in range(B):
+                ref = oracle.rswa_decode(qt[s], o_ref_k[s], o_ref_v[s], prefill[s], o_ring_k[s],
+                                         o_ring_v[s], cursors[s][0], scale)
+                err = out_error(out[s].reshape(H, hd), ref)
+                worst = max(worst, err)
+                assert err <= OUT_TOL, (t, s, err)
+    assert cursors[0].tolist() == [128, 300 % 128]
+    assert np.array_equal(cache.ring_k.cpu().numpy(), o_ring_k)
+    assert np.array_equal(cache.ring_v.cpu().numpy(), o_ring_v)
+    assert cache.device_error() == 0
+
+
+def test_rswa_page_closed_form_on_gpu(torch, kvd):
+    """rswa attention_entry_writes_then_attends: out = (e^{10/sqrt(128)} 5 + 1) /
+    (e^{10/sqrt(128)} + 1) ~ 3.831 for every element."""
+    H, hd = 10, 128
+    cache = kvd.RingCache(1, 16, H, hd, 128)
+    k = torch.zeros(H, 1, hd, device="cuda")
+    k[:, :, 1] = 1.0
+    kvd.rswa_record_prefill(cache, 0, k, torch.ones(H, 1, hd, device="cuda"))
+    q = torch.zeros(1, H, hd, device="cuda")
+    q[..., 0] = 10.0
+    kt = torch.zeros(1, H, hd, device="cuda")
+    kt[..., 0] = 1.0
+    out = kvd.rswa_attention(cache, q, kt, torch.full((1, H, hd), 5.0, device="cuda"))
+    w = math.exp(10.0 / math.sqrt(128.0))
+    assert torch.allclose(out, torch.full_like(out, (w * 5 + 1) / (w + 1)), atol=1e-4)
+    assert cache.ring_len[0] == 1
+
+
+def test_rswa_errors_do_not_mutate(torch, kvd):
+    cache = kvd.RingCache(2, 32, 10, 128, 128)
+    t = torch.ones(2, 10, 128, device="cuda")
+    with pytest.raises(kvd.KvdError) as e:
+        kvd.rswa_ring_write(cache, t, t)
+    assert e.value.status == -3
+    assert cache.ring_len.tolist() == [0, 0] and cache.ring_pos.tolist() == [0, 0]
+    with pytest.raises(kvd.KvdError) as e:
+        kvd.rswa_decode(t, cache)
+    assert e.value.status == -3
+    kvd.rswa_record_prefill(cache, 0, torch.ones(10, 4, 128, device="cuda"),
+                            torch.ones(10, 4, 128, device="cuda"))
+    kvd.rswa_record_prefill(cache, 1, torch.ones(10, 0, 128, device="cuda"),
+                            torch.ones(10, 0, 128, device="cuda"))
+    with pytest.raises(kvd.KvdError) as e:  # stream 1 has no keys at all
+        kvd.rswa_decode(t, cache)
+    assert e.value.status == -4
+    with pytest.raises(kvd.KvdError) as e:
+        kvd.rswa_record_prefill(cache, 0, torch.ones(10, 40, 128, device="cuda"),
+                                torch.ones(10, 40, 128, device="cuda"))
+    assert e.value.status == -2 and cache.prefill_len.tolist() == [4, 0]
