@@ -1,0 +1,413 @@
+#!/usr/bin/env python
+"""Decode-attention benchmark on GB300: KV GB/s (fraction of the HBM roofline)
+and decode queries/s.
+
+Default workload: q8_2f GQA decode, 32 sequences x 4096 cached rows, 32 query
+/ 8 KV heads, head_dim 128, the cache built one row at a time through
+kv_append (freeze and requantisation at row 64).  One step = the whole hot
+path for one decode token: kv_append of one new K/V row per sequence
+(quantised against the frozen fields) + decode_attention over every cached
+row with the attention-mass (imp) accumulation.  The timed region holds
+exactly --steps steps between a barrier + device synchronisation on each side;
+--warmup steps run untimed first.  Two cache replicas alternate step by step
+so that every step streams HBM, not L2 (2 x 289 MB > 129 MB of L2).
+
+Under torchrun each rank times its own replica on its own GPU (independent
+sequences: weak scaling, no data-path collective); rank 0 prints one JSON line
+with the whole-job value.  `--impl reference` times the CPU oracle instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attention KV GB/s (fraction of GB300 HBM peak) and queries/sec, 1 GPU"
+L2_BYTES = 129 * 1024 * 1024
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the GPU works."""
+
+    def __init__(self, index: int, period_ms: int = 20):
+        self.index, self.period_ms = index, period_ms
+        self.samples, self.proc, self.thread = [], None, None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + CLOCK_FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def mark(self):
+        return time.time()
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0: float, t1: float):
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        if not inside:  # a short timed region: take the samples nearest to it
+            inside = [p for (t, p) in sorted(self.samples, key=lambda s: abs(s[0] - (t0 + t1) / 2))[:3]]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[1]) for p in inside if num(p[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4) if p[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(inside[0][2]), "samples": len(inside), "reasons": reasons}
+
+
+# --------------------------------------------------------------- reference
+
+def oracle_sample_gbs(wl, n_seq_sample: int, min_seconds: float, max_reps: int | None = None):
+    """Time the CPU oracle (single thread) decoding `n_seq_sample` sequences of
+    the workload (every query head, every cached row, f64 two-pass softmax)."""
+    import oracle
+    import torch
+
+    from kv_cache_decode_attention_gb300 import workloads as W
+
+    caches, qs = [], []
+    q_all = wl.query(10_000).cpu().numpy()
+    for b in range(n_seq_sample):
+        k, v = wl.rows(b)
+        k, v = k.cpu().numpy(), v.cpu().numpy()
+        oc = oracle.OracleSeqCache(wl.mode, wl.n_kv, wl.hd, int(wl.lengths[b]), alive=wl.alive)
+        oc.append_rows(k, v)
+        caches.append(oc)
+        qs.append(q_all[b])
+        del k, v
+        torch.cuda.empty_cache()
+    n_live = int(wl.alive.sum())
+    bytes_per = W.decode_bytes(wl.mode, n_live, wl.hd, wl.n_q, wl.lengths[:n_seq_sample], True,
+                               n_seq_sample)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        for b, oc in enumerate(caches):
+            imp = np.zeros(oc.cap)
+            oc.decode(qs[b], wl.n_q, np.float32(wl.scale), imp)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or (max_reps is not None and reps >= max_reps):
+            break
+    per_rep = el / reps
+    return bytes_per / per_rep / 1e9, per_rep, bytes_per
+
+
+def run_reference(args, rank):
+    """--impl reference: the CPU oracle as it stands, on the host cores, each
+    step a bounded sample (one sequence, every head and cached row) of the
+    workload; rank 0 only."""
+    if rank != 0:
+        return
+    import torch
+
+    from kv_cache_decode_attention_gb300 import workloads as W
+
+    if not torch.cuda.is_available():
+        print(json.dumps({"impl": "reference", "unavailable": "needs the GPU box to build the workload"}))
+        return
+    wl = build_workload(args.workload, replicas=1)[0]
+    # warm-up and timed steps: one oracle decode of the sampled sequence each
+    gbs_w, _, _ = oracle_sample_gbs(wl, 1, 0.0, max_reps=max(1, args.warmup))
+    t0 = time.perf_counter()
+    gbs, per, nbytes = oracle_sample_gbs(wl, 1, 0.0, max_reps=args.steps)
+    el = time.perf_counter() - t0
+    sample = "1 of %d sequences (all %d query heads, %d rows), f64 two-pass softmax" % (
+        wl.n_seq, wl.n_q, int(wl.lengths[0]))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(per * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "sample": sample},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "queries_per_s": round(1.0 / per, 4),
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def build_workload(name: str, replicas: int):
+    from kv_cache_decode_attention_gb300 import workloads as W
+
+    builders = {"q8_gqa": W.q8_gqa, "long_q8": W.long_q8, "tiny_f32": W.tiny_f32}
+    if name not in builders:
+        raise SystemExit("unknown workload %s" % name)
+    return [builders[name]() for _ in range(replicas)]
+
+
+def run_gpu(args, rank, world):
+    import torch
+
+    import kv_cache_decode_attention_gb300 as kvd
+    from kv_cache_decode_attention_gb300 import workloads as W
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    probe = build_workload(args.workload, 1)
+    wl0 = probe[0]
+    n_live = int(wl0.alive.sum())
+    ws_bytes_each = W.decode_bytes(wl0.mode, n_live, wl0.hd, wl0.n_q, wl0.lengths, True, wl0.n_seq)
+    R = max(1, min(8, math.ceil(4 * L2_BYTES / ws_bytes_each)))
+    wls = probe + build_workload(args.workload, R - 1)
+    n_steps = args.warmup + args.steps
+    extra = int(wl0.layer.capacity[0] - wl0.lengths[0])
+    if math.ceil(2 * n_steps / R) > extra:
+        raise SystemExit("too many steps for the cache capacity (%d rows spare)" % extra)
+
+    # per-replica buffers, all resident before timing
+    imps = [torch.zeros(w.layer.imp_len, device=dev) for w in wls]
+    outs = [torch.empty(w.n_seq, w.n_q, w.hd, device=dev) for w in wls]
+    ws = torch.empty(max(w.layer.workspace_bytes(w.n_q, True) for w in wls), dtype=torch.uint8, device=dev)
+    qs = [wl0.query(i, dev) for i in range(8)]
+    news = [wl0.new_rows(i, dev) for i in range(8)]
+    stream = torch.cuda.current_stream()
+
+    def step(i, with_events=None):
+        w = wls[i % R]
+        k, v = news[i % 8]
+        kvd.kv_append(w.layer, k, v)
+        if with_events is not None:
+            with_events[0].record(stream)
+        kvd.decode_attention(qs[i % 8], w.layer, out=outs[i % R], imp=imps[i % R], scale=w.scale,
+                             workspace=ws)
+        if with_events is not None:
+            with_events[1].record(stream)
+
+    def lengths_now():
+        return [np.array([w.layer.seq_len(b) for b in range(w.n_seq)], np.int64) for w in wls]
+
+    # ---- warm-up
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+
+    # ---- timed region
+    bytes_total = 0
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    lens_before = lengths_now()
+    sampler = ClockSampler(dev.index)
+    with sampler:
+        time.sleep(0.3)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        c0 = time.time()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.profiler.start()  # profilers started with capture off record only this range
+        t0.record(stream)
+        for j in range(args.steps):
+            step(args.warmup + j, ev[j])
+        t1.record(stream)
+        torch.cuda.synchronize()
+        torch.cuda.profiler.stop()
+        if dist is not None:
+            dist.barrier()
+        c1 = time.time()
+        time.sleep(0.1)
+    elapsed_ms = t0.elapsed_time(t1)
+    # algorithmic bytes of exactly the timed steps (lengths known on the host)
+    lens = [l.copy() for l in lens_before]
+    for j in range(args.steps):
+        r = (args.warmup + j) % R
+        w = wls[r]
+        bytes_total += W.append_bytes(w.mode, n_live, w.hd, w.n_seq)
+        lens[r] += 1
+        bytes_total += W.decode_bytes(w.mode, n_live, w.hd, w.n_q, lens[r], True, w.n_seq)
+    dec_ms = [a.elapsed_time(b) for a, b in ev]
+    if dist is not None:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_per_step = elapsed_ms / args.steps
+    gbs = bytes_total / (elapsed_ms * 1e-3) / 1e9 * world
+
+    # ---- dominant kernel: the decode call without imp, timed alone (same
+    #      workload and launch configuration, CUDA events on the launching stream)
+    nrep = max(20, args.steps)
+    dev_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nrep)]
+    for j in range(nrep):
+        w = wls[j % R]
+        dev_ev[j][0].record(stream)
+        kvd.decode_attention(qs[j % 8], w.layer, out=outs[j % R], imp=None, scale=w.scale, workspace=ws)
+        dev_ev[j][1].record(stream)
+    torch.cuda.synchronize()
+    k_ms = statistics.mean(a.elapsed_time(b) for a, b in dev_ev)
+    lens_now = lengths_now()
+    kbytes = statistics.mean(
+        W.decode_bytes(wls[j % R].mode, n_live, wl0.hd, wl0.n_q, lens_now[j % R], False, wl0.n_seq)
+        for j in range(nrep))
+    peak, peak_kind = peaks()
+    achieved = kbytes / (k_ms * 1e-3) / 1e9
+
+    # ---- end to end through the public API with host buffers
+    pin_q = [qs[i].cpu().pin_memory() for i in range(8)]
+    pin_k = [news[i][0].cpu().pin_memory() for i in range(8)]
+    pin_v = [news[i][1].cpu().pin_memory() for i in range(8)]
+    pin_out = torch.empty(wl0.n_seq, wl0.n_q, wl0.hd).pin_memory()
+    dq = torch.empty_like(qs[0])
+    dk, dv = torch.empty_like(news[0][0]), torch.empty_like(news[0][1])
+    e2e_steps = args.steps
+    if math.ceil(2 * (n_steps + e2e_steps) / R) > extra:
+        e2e_steps = 0
+    e2e = None
+    if e2e_steps:
+        torch.cuda.synchronize()
+        lens_b = lengths_now()
+        a0 = time.perf_counter()
+        for j in range(e2e_steps):
+            i = n_steps + j
+            w = wls[i % R]
+            dq.copy_(pin_q[i % 8], non_blocking=True)
+            dk.copy_(pin_k[i % 8], non_blocking=True)
+            dv.copy_(pin_v[i % 8], non_blocking=True)
+            kvd.kv_append(w.layer, dk, dv)
+            kvd.decode_attention(dq, w.layer, out=outs[i % R], imp=imps[i % R], scale=w.scale, workspace=ws)
+            pin_out.copy_(outs[i % R], non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+        a1 = time.perf_counter()
+        eb = 0
+        lens_e = [l.copy() for l in lens_b]
+        for j in range(e2e_steps):
+            r = (n_steps + j) % R
+            w = wls[r]
+            lens_e[r] += 1
+            eb += W.append_bytes(w.mode, n_live, w.hd, w.n_seq)
+            eb += W.decode_bytes(w.mode, n_live, w.hd, w.n_q, lens_e[r], True, w.n_seq)
+        e2e = {"value": round(eb / (a1 - a0) / 1e9 * world, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": int(dq.numel() * 4 + dk.numel() * 4 + dv.numel() * 4),
+               "d2h_bytes_per_step": int(pin_out.numel() * 4)}
+    for w in wls:
+        err = w.layer.device_error()
+        if err:
+            raise SystemExit("device error word set: %d" % err)
+
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline and world >= 1:
+        v, per, nb = oracle_sample_gbs(wl0, 1, args.cpu_seconds)
+        cpu = {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": "1 of %d sequences (all %d query heads x %d rows) decoded in f64, "
+                         "%.1f s" % (wl0.n_seq, wl0.n_q, int(wl0.lengths[0]), args.cpu_seconds)}
+    clocks = sampler.summary(c0, c1)
+    line = {
+        "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": wl0.name, "mode": "q8_2f", "n_seq": wl0.n_seq,
+                   "cached_rows": int(wl0.lengths[0]), "n_q": wl0.n_q, "n_kv": wl0.n_kv,
+                   "head_dim": wl0.hd, "step": "kv_append 1 row/seq + decode_attention with imp",
+                   "replicas": R, "l2": "inputs larger than L2 (%d rotated cache replicas)" % R,
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "fraction_of_peak": round(gbs / world / peak, 4),
+        "queries_per_s": round(wl0.n_seq * world / (ms_per_step * 1e-3), 1),
+        "roofline": {"bound": "hbm", "kernel": "decode_attention (split + merge, imp off)",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "peak_kind": peak_kind, "ms_per_launch": round(k_ms, 5),
+                     "bytes_per_launch": int(kbytes)},
+        "decode_ms_in_step": round(statistics.mean(dec_ms), 5),
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps * 4,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="q8_gqa", choices=["q8_gqa", "long_q8", "tiny_f32"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1 and args.impl != "reference":
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+    from __graft_entry__ import build
+
+    if args.impl == "reference":
+        if rank == 0:
+            build()
+        run_reference(args, rank)
+        return
+    build()
+    run_gpu(args, rank, world)
+
+
+if __name__ == "__main__":
+    main()
