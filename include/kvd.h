@@ -162,6 +162,27 @@ KVD_API kvd_status decode_attention(const float *q, const kvd_layer *L, int32_t 
                             float *out, float *imp, void *workspace, int64_t workspace_bytes,
                             void *stream);
 
+/* decode_attention for callers that cannot allocate device memory (the pages
+ * have no counterpart: this is a deployment variant).  Some callers cannot
+ * call cudaMalloc on their decode path -- an inference runtime that hands out
+ * device memory from a fixed, pre-planned arena, a plug-in inside a host
+ * application that owns every allocation, code that must not take
+ * cudaMalloc's implicit device-wide synchronisation while serving -- so this
+ * call takes no workspace: its scratch (the per-chunk partial results) lives
+ * in a 16 MiB array compiled into the library, which every GPU that loads the
+ * library holds until the process exits.  It allocates nothing and computes
+ * the same outputs as decode_attention with imp = NULL.
+ *   Limit: n_seq * n_live * chunks * (n_q / n_kv) * (2 + head_dim) * 4 bytes
+ *   (each region rounded up to 256) must fit in 16 MiB, where chunks is the
+ *   longest sequence divided by the rows per chunk the call picks (>= 256);
+ *   a larger call returns KVD_ECAPACITY and launches nothing.
+ *   The first call on each device looks up the array's device address (with
+ *   that device current); make it before any stream capture.  Calls share
+ *   the array: two calls whose kernels overlap on the GPU race and must be
+ *   serialised by the caller. */
+KVD_API kvd_status decode_attention_static(const float *q, const kvd_layer *L, int32_t n_q,
+                                           float scale, float *out, void *stream);
+
 /* Device error word of the layer (0 = clean), copied back synchronously;
  * clear != 0 resets it.  Bit 0: a bounded wait timed out; bit 1: a kernel
  * found metadata out of range and skipped the access. */

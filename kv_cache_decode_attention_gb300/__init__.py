@@ -11,6 +11,7 @@ from .api import (  # noqa: F401
     LayerKvCache,
     RingCache,
     decode_attention,
+    decode_attention_static,
     kv_append,
     kv_freeze_colfield,
     rswa_attention,

@@ -189,6 +189,27 @@ def decode_attention(q: torch.Tensor, cache: LayerKvCache, out: torch.Tensor | N
     return out
 
 
+def decode_attention_static(q: torch.Tensor, cache: LayerKvCache, out: torch.Tensor | None = None,
+                            scale: float | None = None, stream=None) -> torch.Tensor:
+    """decode_attention without imp and without a workspace, for callers that
+    cannot allocate device memory on their decode path: the library's own
+    16 MiB scratch array holds the partial results.  Raises KvdError with
+    status -2 when the call needs more scratch than that.  Calls that overlap
+    on the GPU share the array and must be serialised."""
+    _f32_cuda(q, "q")
+    n_q = q.numel() // (cache.n_seq * cache.head_dim)
+    if q.numel() != cache.n_seq * n_q * cache.head_dim:
+        raise ValueError("q must be [n_seq, n_q, head_dim]")
+    if out is None:
+        out = torch.empty_like(q)
+    _f32_cuda(out, "out")
+    if scale is None:
+        scale = 1.0 / math.sqrt(cache.head_dim)
+    _abi.call("decode_attention_static", _ptr(q), C.byref(cache.L), int(n_q), C.c_float(scale),
+              _ptr(out), _stream(stream))
+    return out
+
+
 class RingCache:
     """R-SWA caches of B streams for one layer: reference block [B, H, ref_cap, hd]
     plus a W-slot ring [B, H, W, hd], cursors on the host."""
