@@ -74,7 +74,7 @@ enum {
  * its contents are private.  It mirrors on the host every length the
  * kernels need, so no call reads device memory back. */
 typedef struct kvd_layer {
-    uint64_t opaque[48];
+    uint64_t opaque[128];
 } kvd_layer;
 
 /* Sizes of a layer's buffers (cortiq LayerKvCache: one contiguous region

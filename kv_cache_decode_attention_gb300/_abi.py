@@ -22,7 +22,7 @@ BUF_K, BUF_V, BUF_KQ, BUF_VQ, BUF_KS, BUF_VS, BUF_KCOL, BUF_VCOL, BUF_META, BUF_
 
 
 class kvd_layer(C.Structure):
-    _fields_ = [("opaque", C.c_uint64 * 48)]
+    _fields_ = [("opaque", C.c_uint64 * 128)]
 
 
 class KvdError(RuntimeError):

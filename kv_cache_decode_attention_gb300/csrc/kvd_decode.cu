@@ -7,7 +7,9 @@
 #include <cmath>
 #include <vector>
 
-#include "kvd_decode_kernels.cuh"
+#include <cstring>
+
+#include "kvd_split_mma.cuh"
 
 namespace kvd {
 
@@ -15,6 +17,8 @@ cudaError_t split_layer_f32(int, int, const SplitArgs &, const LayerSrc &, dim3,
 cudaError_t split_layer_q8(int, int, const SplitArgs &, const LayerSrc &, dim3, cudaStream_t);
 cudaError_t split_layer_q8k(int, int, const SplitArgs &, const LayerSrc &, dim3, cudaStream_t);
 cudaError_t split_layer_q8v(int, int, const SplitArgs &, const LayerSrc &, dim3, cudaStream_t);
+cudaError_t split_layer_q8_mma(int, const SplitArgs &, const LayerSrc &, const MmaMaps &, dim3,
+                               cudaStream_t);
 
 namespace {
 
@@ -238,7 +242,14 @@ extern "C" kvd_status decode_attention(const float *q, const kvd_layer *L, int32
         dim3 grid(unsigned(ceil_div(max_len, chunk)), unsigned(l->n_live), unsigned(l->n_seq));
         const int hb = hpk_bucket(hpk);
         cudaError_t e;
-        switch (l->mode) {
+        const bool mma = l->mode == KVD_Q8 && l->hd == 128 && l->have_tmap_kq && l->have_tmap_vq;
+        MmaMaps maps;
+        if (mma) {
+            std::memcpy(&maps.kq, l->tmap_kq, sizeof(maps.kq));
+            std::memcpy(&maps.vq, l->tmap_vq, sizeof(maps.vq));
+        }
+        switch (mma ? -1 : l->mode) {
+            case -1: e = split_layer_q8_mma(hb, a, s, maps, grid, st); break;
             case KVD_F32: e = split_layer_f32(l->hd, hb, a, s, grid, st); break;
             case KVD_Q8: e = split_layer_q8(l->hd, hb, a, s, grid, st); break;
             case KVD_Q8K: e = split_layer_q8k(l->hd, hb, a, s, grid, st); break;

@@ -5,8 +5,12 @@
 // are a straight slice, dead heads store nothing).  The library computes
 // where each region lives; the caller allocates the buffers.
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "kvd_internal.cuh"
@@ -98,6 +102,37 @@ void slot_bytes(const Shape &s, int64_t *out) {
 
 int64_t host_block_bytes(int32_t n_seq, int32_t n_kv) {
     return 8 * 4 * int64_t(n_seq) + 4 * int64_t(n_seq) + 8 * int64_t(n_kv) + round_up(n_kv, 8);
+}
+
+// TMA descriptor of an int8 code buffer: 2-D [rows][hd] bytes, row pitch hd,
+// boxes of 128 rows x 128 bytes landing in shared memory with the 128-byte
+// swizzle (16-byte chunk c of row r stored at chunk c ^ (r % 8)); rows past
+// the end read as zeros.  Returns false if the driver entry point is missing
+// or refuses the descriptor (the caller then uses the plain bulk-copy kernel).
+bool encode_code_map(void *base, int64_t rows, int hd, unsigned char *out) {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    std::call_once(once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (encode == nullptr || hd != 128) return false;
+    alignas(64) CUtensorMap m;
+    const cuuint64_t dims[2] = {cuuint64_t(hd), cuuint64_t(rows)};
+    const cuuint64_t strides[1] = {cuuint64_t(hd)};
+    const cuuint32_t box[2] = {128u, 128u};
+    const cuuint32_t estr[2] = {1u, 1u};
+    if (encode(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    static_assert(sizeof(CUtensorMap) == 128, "tensor map size");
+    std::memcpy(out, &m, sizeof(m));
+    return true;
 }
 
 __global__ void fill_f32_kernel(float *p, int64_t n, float v) {
@@ -241,6 +276,11 @@ extern "C" kvd_status kvd_layer_init(kvd_layer *L, int32_t n_seq, int32_t n_kv, 
         }
         if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
     }
+    const int64_t code_rows = s.total_rows + kRowAlign;
+    if (l.buf[KVD_BUF_KQ])
+        l.have_tmap_kq = encode_code_map(l.buf[KVD_BUF_KQ], code_rows, head_dim, l.tmap_kq) ? 1 : 0;
+    if (l.buf[KVD_BUF_VQ])
+        l.have_tmap_vq = encode_code_map(l.buf[KVD_BUF_VQ], code_rows, head_dim, l.tmap_vq) ? 1 : 0;
     std::memcpy(L, &l, sizeof(l));
     return KVD_OK;
 }
