@@ -39,7 +39,7 @@ struct AppendArgs {
 };
 
 constexpr int kAppendWarps = 4;
-constexpr int kItemsPerWarp = 4;
+constexpr int kItemsPerWarp = 1;
 
 // Quantise one row held by a warp, CPL consecutive channels per lane, against
 // the field `col` (1.0 before the freeze), with groups of `group` channels

@@ -1,32 +1,37 @@
 // kvd_split_mma.cuh -- split-KV decode over the q8_2f cache (int8 K and V,
-// head_dim 128) on the tensor cores.
+// head_dim 128) on the tensor cores (warp-level mma.sync, f16 in, f32 out).
 //
-// Why: with int8 rows, the CUDA-core kernel spends ~84 instructions per
-// cached row on int8->f32 conversions, hpk x 128 FMAs per pass and the warp
-// reductions; at GQA fan-out 4..16 that is issue-bound far below the HBM
-// roofline.  Here both contractions go through mma.sync, and the only
-// per-element CUDA-core work left is a 4-instruction int8->f16 conversion of
-// the K codes.
+// Why: with int8 rows the CUDA-core kernel spends ~84 instructions per cached
+// row (int8->f32 conversions, hpk x 128 FMAs per pass, warp reductions) and is
+// issue-bound far below the HBM roofline at GQA fan-out 4..16.  Here both
+// contractions run as f16 MMAs with f32 accumulation; the CUDA cores only turn
+// each int8 code into an exact f16 once (a byte splice and one HSUB2 per pair),
+// shared by every query head of the group.  (The legacy int8 mma.sync path is
+// far slower than f16 on this GPU, so the codes go through f16.)
 //
-// Score (per tile of 128 rows, each warp 32 rows = two m16 blocks):
-//   S[row][h] = 2^-E_h * sum_g ks[row][g] * (K_g f16) . (q_g t1 + q_g t2)
-//   K codes are exact in f16; q * kcol * scale * log2(e) * 2^E_h is split
-//   into two f16 terms t1 + t2 (22 significant bits; E_h puts each head's
-//   largest term near 2^14); m16n8k16 MMAs accumulate in f32 per 32-channel
-//   group so the group scale ks[row][g] applies after.  The channel order
-//   inside a k16 step is permuted consistently in A and B so that one lane's
-//   four consecutive int8 codes feed its fragment directly.
-// Softmax: online over tiles, running max per head, in the log2 domain.
-// Value (the same tile): w = 2^(S - max) * vs[row] is quantised to a 24-bit
-//   unsigned fixed point relative to the tile's largest vs (exact byte digits
-//   w = d0 + 256 d1 + 65536 d2, relative error <= 2^-24 of the largest
-//   weight); m16n8k32 u8 x s8 MMAs with int32 accumulation give
-//   sum_p d_j[h][p] V[p][c] exactly; the three digit sums are combined in
-//   f32 once per tile and folded into the running accumulator.  Warps split
-//   the 128 channels (32 each), so no cross-warp reduction is needed.
-// Data movement: K and V code tiles arrive by TMA tensor copies with the
-// 128-byte swizzle (conflict-free ldmatrix), scales by 1-D bulk copies, into
-// a ring of kMmaSlots slots alternating K and V segments.
+// Per tile of 128 cached rows:
+//   scores  warps split the rows (32 each, two m16 blocks):
+//           S[row][h] = 2^-E_h * sum_g ks[row][g] * K_g . (t1_h + t2_h)_g
+//           K codes are exact in f16; q * kcol * scale * log2(e) * 2^E_h is
+//           split into two f16 terms t1 + t2 (22 significant bits, E_h puts the
+//           head's largest term near 2^14); m16n8k16 MMAs accumulate each
+//           32-channel group in f32 so its scale ks[row][g] applies after.  The
+//           channel order inside a k16 step is permuted identically in A and B
+//           so a lane's four consecutive codes feed its fragment directly.
+//           The per-warp maximum of each head is reduced in registers.
+//   softmax online over tiles in the log2 domain (running max per head; every
+//           thread derives the same maxima from the per-warp values).
+//   weights w = 2^(S - max) * vs[row] * 2^Ew (Ew puts the tile's largest V
+//           scale near 2^14) split into two f16 terms, written to shared
+//           memory as the A operand [term][k16 step][head][position].
+//   values  warps split the 128 channels (32 each); V codes become the f16 B
+//           operand straight from ldmatrix.trans; m16n8k16 MMAs with M = the
+//           group's heads accumulate into f32 registers across all tiles (the
+//           accumulator is rescaled by the softmax correction and the change
+//           of Ew between tiles).
+// K and V code tiles arrive by TMA tensor copies with the 128-byte swizzle
+// (conflict-free ldmatrix); scales by 1-D bulk copies; a ring of kMmaSlots
+// slots alternates K and V segments.
 #pragma once
 
 #include <cuda.h>
@@ -37,25 +42,25 @@
 namespace kvd {
 
 constexpr int kMmaTR = 128;        // rows per tile
-constexpr int kMmaSlots = 4;       // ring slots (K, V alternate)
+constexpr int kMmaSlots = 3;       // ring slots (K, V alternate)
 constexpr int kMmaTile = 16384;    // bytes of one 128 x 128 code tile
 constexpr int kMmaKsOff = 16384;   // K scales within a K segment
 constexpr int kMmaVsOff = 18432;   // V scales within a K segment
 constexpr int kMmaSlot = 19456;    // bytes per slot (multiple of 1024)
+constexpr int kMmaAw = 2 * 8 * 16 * 32;  // weights [term][k16 step][16 heads][16 f16]
 
 template <int HPK>
 struct MmaCfg {
-    static constexpr int HPKP = HPK < 4 ? 4 : HPK;   // heads padded for the layouts
+    static constexpr int HPKP = HPK < 4 ? 4 : HPK;          // heads padded for the layouts
     static constexpr int NT = HPKP / 8 > 0 ? HPKP / 8 : 1;  // score n8 tiles
-    static constexpr int MT = (3 * HPKP + 15) / 16;  // PV m16 tiles (3 digits x heads)
-    static constexpr int MROWS = 16 * MT;
-    static constexpr int S_OFF = kMmaSlots * kMmaSlot;           // scores [TR][HPKP] f32
-    static constexpr int A_OFF = S_OFF + kMmaTR * HPKP * 4;      // digits [8][MROWS][16]
-    static constexpr int MISC_OFF = A_OFF + 8 * MROWS * 16;
-    // misc: bars[kMmaSlots], red[kWarps][HPKP], mrun[HPKP], alpha[HPKP], vred[kWarps], u
-    static constexpr int SMEM = MISC_OFF + kMmaSlots * 8 + (kWarps + 2) * HPKP * 4 + kWarps * 4 + 16;
+    static constexpr int S_OFF = kMmaSlots * kMmaSlot;       // scores [TR][HPKP] f32
+    static constexpr int AW_OFF = S_OFF + kMmaTR * HPKP * 4;
+    static constexpr int MISC_OFF = AW_OFF + kMmaAw;
+    // misc: bars[kMmaSlots], red[kWarps][HPKP], vred[kWarps]
+    static constexpr int SMEM = MISC_OFF + kMmaSlots * 8 + kWarps * HPKP * 4 + kWarps * 4;
     static constexpr int SMEM_ALLOC = SMEM + 1024;  // room to align the base to 1024
-    static_assert(kWarps * HPKP * 128 * 4 <= kMmaSlots * kMmaSlot, "acc staging must fit");
+    static constexpr int MIN_CTAS = HPK >= 16 ? 2 : 3;
+    static_assert(kMmaTR * HPKP * 4 >= HPKP * 128 * 4, "q staging reuses the score area");
 };
 
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
@@ -89,32 +94,27 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// D += A(16x32 u8, row) * B(32x8 s8, col), s32 accumulate.
-__device__ __forceinline__ void mma_u8s8(int (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k32.row.col.s32.u8.s8.s32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
-        " {%8, %9}, {%0, %1, %2, %3};"
-        : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// Four int8 codes -> two exact f16 pairs (codes 0,1 and codes 2,3): bias the
-// bytes to unsigned, splice them under the f16 exponent of 1024, subtract 1152.
-__device__ __forceinline__ void codes_to_f16(uint32_t w, uint32_t &lo, uint32_t &hi) {
-    const uint32_t u = w ^ 0x80808080u;
-    const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);
-    const uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);
+// Exact f16 of two int8 codes picked from a word: bias to unsigned, splice each
+// byte under the f16 exponent of 1024 (giving 1024 + code + 128), subtract 1152.
+// sel picks the two bytes (0x4140: bytes 0,1; 0x4342: 2,3; 0x4240: 0,2; 0x4341: 1,3).
+template <uint32_t SEL>
+__device__ __forceinline__ uint32_t codes_f16x2(uint32_t biased) {
+    const uint32_t a = __byte_perm(biased, 0x64646464u, SEL);
     const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
     const __half2 x = __hsub2(*reinterpret_cast<const __half2 *>(&a), bias);
-    const __half2 y = __hsub2(*reinterpret_cast<const __half2 *>(&b), bias);
-    lo = *reinterpret_cast<const uint32_t *>(&x);
-    hi = *reinterpret_cast<const uint32_t *>(&y);
+    return *reinterpret_cast<const uint32_t *>(&x);
 }
 
 __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
     const __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// exponent e with x in [2^(e-1), 2^e), x > 0
+__device__ __forceinline__ int exponent_of(float x) {
+    int e;
+    frexpf(x, &e);
+    return e;
 }
 
 struct MmaMaps {
@@ -142,25 +142,30 @@ __device__ __forceinline__ void mma_issue(const ChunkInfo &ci, const CUtensorMap
     }
 }
 
+// Byte offset of weight (term, position p, head h) in the A operand area: 16 x
+// 16 f16 blocks per (term, k16 step), the two 8-position halves of a head's
+// row swapped on heads 4..7 and 12..15 so ldmatrix rows hit distinct banks.
+__device__ __forceinline__ int aw_offset(int term, int p, int h) {
+    const int ks = p >> 4, k = p & 15;
+    return ((term * 8 + ks) * 16 + h) * 32 + (((k >> 3) ^ ((h >> 2) & 1)) << 4) + (k & 7) * 2;
+}
+
 // One CTA: one chunk of ci.n rows starting at storage row `row_base` of one
 // (sequence, live group).  Writes the partial (max, sum, acc) of each head.
 template <int HPK>
 __device__ void split_mma_body(const ChunkInfo &ci, int64_t row_base, const SplitArgs &a,
                                const CUtensorMap *kmap, const CUtensorMap *vmap, char *smem_raw) {
     using C = MmaCfg<HPK>;
-    constexpr int HPKP = C::HPKP, NT = C::NT, MT = C::MT, MROWS = C::MROWS;
+    constexpr int HPKP = C::HPKP, NT = C::NT;
     char *sm = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                         ~uintptr_t(1023));
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int gl4 = lane >> 2, t4 = lane & 3;
     float *S = reinterpret_cast<float *>(sm + C::S_OFF);
-    char *A = sm + C::A_OFF;
+    char *Aw = sm + C::AW_OFF;
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + C::MISC_OFF);
     float *red = reinterpret_cast<float *>(bar + kMmaSlots);
-    float *mrun = red + kWarps * HPKP;
-    float *alpha = mrun + HPKP;
-    float *vred = alpha + HPKP;
-    float *ushared = vred + kWarps;
+    float *vred = red + kWarps * HPKP;
 
     const int n = ci.n;
     const int ntiles = (n + kMmaTR - 1) / kMmaTR;
@@ -170,16 +175,13 @@ __device__ void split_mma_body(const ChunkInfo &ci, int64_t row_base, const Spli
         for (int s = 0; s < kMmaSlots; ++s) mbar_init(&bar[s], 1);
         fence_mbar_init();
     }
-    if (tid < HPKP) mrun[tid] = -INFINITY;
     __syncthreads();
     if (tid == 0)
         for (int j = 0; j < min(kMmaSlots, nseg); ++j) mma_issue<HPK>(ci, kmap, vmap, row_base, sm, bar, j);
 
-    // ---- query terms: q * kcol * scale * log2e * 2^E_h = t1 + t2 (f16)
-    // staging [HPKP][128] in the score area (exactly that size, free until the
-    // first tile's scores)
+    // ---- query terms: q * kcol * scale * log2e * 2^E_h = t1 + t2 (f16),
+    //      staged through the score area
     float *qf = S;
-    static_assert(kMmaTR == 128, "the score area doubles as the q staging area");
     for (int i = tid; i < HPKP * 128; i += kThreads) {
         const int h = i >> 7, d = i & 127;
         qf[i] = h < a.hpk ? ci.q[h * 128 + d] * ci.kcol[d] * a.qscale : 0.0f;
@@ -188,58 +190,53 @@ __device__ void split_mma_body(const ChunkInfo &ci, int64_t row_base, const Spli
     if (tid < HPKP) {
         float mx = 0.0f;
         for (int d = 0; d < 128; ++d) mx = fmaxf(mx, fabsf(qf[tid * 128 + d]));
-        int e2 = 0;
-        if (mx > 0.0f) {
-            int ex;
-            frexpf(mx, &ex);  // mx in [2^(ex-1), 2^ex)
-            e2 = 14 - ex;
-        }
-        alpha[tid] = float(e2);  // exponent scratch, overwritten in the tile loop
+        red[tid] = mx > 0.0f ? float(14 - exponent_of(mx)) : 0.0f;
     }
     __syncthreads();
-    // B fragments: [group][k16 step][n-tile][term][2]
-    uint32_t bq[4][2][NT][2][2];
-    float qexp[NT][2];  // 2^-E of the heads this lane's score columns hold
+    uint32_t bq[4][2][NT][2][2];  // [group][k16 step][n-tile][term][reg]
+    float qexp[NT][2];            // 2^-E of the heads in this lane's score columns
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
             const int h = nt * 8 + 2 * t4 + c;
-            qexp[nt][c] = h < HPKP ? exp2f(-alpha[h]) : 0.0f;
+            qexp[nt][c] = h < HPKP ? exp2f(-red[h]) : 0.0f;
         }
         const int hb = nt * 8 + gl4;  // the B column this lane feeds
-        const float sc = hb < HPKP ? exp2f(alpha[hb]) : 0.0f;
+        const float sc = hb < HPKP ? exp2f(red[hb]) : 0.0f;
 #pragma unroll
         for (int g = 0; g < 4; ++g)
 #pragma unroll
             for (int ks = 0; ks < 2; ++ks) {
                 const int c0 = 32 * g + 16 * ks + 4 * t4;
-                float x[4];
+                float x[4], r[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) x[i] = hb < HPKP ? qf[hb * 128 + c0 + i] * sc : 0.0f;
-                float r[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) r[i] = x[i] - __half2float(__float2half_rn(x[i]));
+                for (int i = 0; i < 4; ++i) {
+                    x[i] = hb < HPKP ? qf[hb * 128 + c0 + i] * sc : 0.0f;
+                    r[i] = x[i] - __half2float(__float2half_rn(x[i]));
+                }
                 bq[g][ks][nt][0][0] = pack_half2(x[0], x[1]);
                 bq[g][ks][nt][0][1] = pack_half2(x[2], x[3]);
                 bq[g][ks][nt][1][0] = pack_half2(r[0], r[1]);
                 bq[g][ks][nt][1][1] = pack_half2(r[2], r[3]);
             }
     }
-    __syncthreads();  // qf staging read before the scores overwrite it
+    __syncthreads();  // staging read before the scores overwrite it
 
-    // PV accumulators: this lane's heads x 8 channels (2 blocks x 4)
-    constexpr int NH = HPKP >= 16 ? 2 : 1;  // heads per lane after the digit combine
-    float acc[NH][8];
-#pragma unroll
-    for (int i = 0; i < NH; ++i)
-#pragma unroll
-        for (int c = 0; c < 8; ++c) acc[i][c] = 0.0f;
+    // running state (every thread derives the same maxima from red)
+    const int hw = tid % HPKP;  // head whose weights this thread writes
+    float m_w = -INFINITY, m_a = -INFINITY, m_b = -INFINITY;  // heads hw, gl4, gl4 + 8
     float lsum = 0.0f;
+    int ew_prev = 0;
+    float acc[4][4];  // [n-tile: block 0 even, 0 odd, 1 even, 1 odd][frag]
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[i][c] = 0.0f;
     bool ok = true;
+    const uint32_t aw_base = smem_addr(Aw);
 
-    const uint32_t A_base = smem_addr(A);
-    for (int t = 0; t < ntiles && ok; ++t) {
+    for (int t = 0; t < ntiles; ++t) {
         const int row0 = t * kMmaTR;
         const int nt_rows = min(kMmaTR, n - row0);
         int j = 2 * t;
@@ -248,11 +245,17 @@ __device__ void split_mma_body(const ChunkInfo &ci, int64_t row_base, const Spli
             ok = false;
             break;
         }
+        // the previous tile's V slot is drained (every thread passed the barrier)
+        if (tid == 0 && t > 0 && j - 1 + kMmaSlots < nseg)
+            mma_issue<HPK>(ci, kmap, vmap, row_base, sm, bar, j - 1 + kMmaSlots);
         const char *kseg = sm + slot * kMmaSlot;
         const uint32_t kbase = smem_addr(kseg);
         const float *ks_s = reinterpret_cast<const float *>(kseg + kMmaKsOff);
         const float *vs_s = reinterpret_cast<const float *>(kseg + kMmaVsOff);
         // ------------------------------------------------ scores (f16 MMA)
+        float wmax[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) wmax[nt][0] = wmax[nt][1] = -INFINITY;
 #pragma unroll
         for (int mb = 0; mb < 2; ++mb) {
             const int r0 = warp * 32 + mb * 16;
@@ -272,36 +275,37 @@ __device__ void split_mma_body(const ChunkInfo &ci, int64_t row_base, const Spli
                 const int chunk = 2 * g + (mi >> 1);
                 uint32_t w[4];
                 ldsm_x4(kbase + lrow * 128 + ((chunk ^ (lrow & 7)) << 4), w);
-                uint32_t a00, a02, a01, a03, a10, a12, a11, a13;
-                codes_to_f16(w[0], a00, a02);  // row gl4,   channels 4t..4t+3 (k step 0)
-                codes_to_f16(w[1], a01, a03);  // row gl4+8
-                codes_to_f16(w[2], a10, a12);  // row gl4,   k step 1
-                codes_to_f16(w[3], a11, a13);  // row gl4+8
-                float dg[NT][4];
+                // row gl4 / gl4 + 8, channels 4t..4t+3 of k16 step 0 and 1
+                const uint32_t u0 = w[0] ^ 0x80808080u, u1 = w[1] ^ 0x80808080u;
+                const uint32_t u2 = w[2] ^ 0x80808080u, u3 = w[3] ^ 0x80808080u;
+                const uint32_t a00 = codes_f16x2<0x4140>(u0), a02 = codes_f16x2<0x4342>(u0);
+                const uint32_t a01 = codes_f16x2<0x4140>(u1), a03 = codes_f16x2<0x4342>(u1);
+                const uint32_t a10 = codes_f16x2<0x4140>(u2), a12 = codes_f16x2<0x4342>(u2);
+                const uint32_t a11 = codes_f16x2<0x4140>(u3), a13 = codes_f16x2<0x4342>(u3);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) dg[nt][i] = 0.0f;
+                    float dg[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
                     for (int tm = 0; tm < 2; ++tm) {
-                        mma_f16(dg[nt], a00, a01, a02, a03, bq[g][0][nt][tm][0], bq[g][0][nt][tm][1]);
-                        mma_f16(dg[nt], a10, a11, a12, a13, bq[g][1][nt][tm][0], bq[g][1][nt][tm][1]);
+                        mma_f16(dg, a00, a01, a02, a03, bq[g][0][nt][tm][0], bq[g][0][nt][tm][1]);
+                        mma_f16(dg, a10, a11, a12, a13, bq[g][1][nt][tm][0], bq[g][1][nt][tm][1]);
                     }
-                    sacc[nt][0] = fmaf(kA[g], dg[nt][0], sacc[nt][0]);
-                    sacc[nt][1] = fmaf(kA[g], dg[nt][1], sacc[nt][1]);
-                    sacc[nt][2] = fmaf(kB[g], dg[nt][2], sacc[nt][2]);
-                    sacc[nt][3] = fmaf(kB[g], dg[nt][3], sacc[nt][3]);
+                    sacc[nt][0] = fmaf(kA[g], dg[0], sacc[nt][0]);
+                    sacc[nt][1] = fmaf(kA[g], dg[1], sacc[nt][1]);
+                    sacc[nt][2] = fmaf(kB[g], dg[2], sacc[nt][2]);
+                    sacc[nt][3] = fmaf(kB[g], dg[3], sacc[nt][3]);
                 }
             }
+            const int ra = r0 + gl4, rb = r0 + gl4 + 8;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     const int h = nt * 8 + 2 * t4 + c;
+                    const float sa = ra < nt_rows ? sacc[nt][c] * qexp[nt][c] : -INFINITY;
+                    const float sb = rb < nt_rows ? sacc[nt][2 + c] * qexp[nt][c] : -INFINITY;
+                    wmax[nt][c] = fmaxf(wmax[nt][c], fmaxf(sa, sb));
                     if (h < HPKP) {
-                        const int ra = r0 + gl4, rb = r0 + gl4 + 8;
-                        const float sa = ra < nt_rows ? sacc[nt][c] * qexp[nt][c] : -INFINITY;
-                        const float sb = rb < nt_rows ? sacc[nt][2 + c] * qexp[nt][c] : -INFINITY;
                         S[ra * HPKP + h] = sa;
                         S[rb * HPKP + h] = sb;
                         if (a.scores != nullptr && h < a.hpk) {
@@ -312,7 +316,18 @@ __device__ void split_mma_body(const ChunkInfo &ci, int64_t row_base, const Spli
                 }
             }
         }
-        // largest V row scale of the tile (rows < nt_rows)
+        // per-warp maxima of every head and of the V row scales
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                float m = wmax[nt][c];
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+                const int h = nt * 8 + 2 * t4 + c;
+                if (gl4 == 0 && h < HPKP) red[warp * HPKP + h] = m;
+            }
         {
             float v = tid < nt_rows ? vs_s[tid] : 0.0f;
 #pragma unroll
@@ -320,156 +335,105 @@ __device__ void split_mma_body(const ChunkInfo &ci, int64_t row_base, const Spli
             if (lane == 0) vred[warp] = v;
         }
         __syncthreads();
-        // ------------------------------------------------ tile max, rescale
-        {
-            const int h = tid % HPKP;
-            float mx = -INFINITY;
-            for (int r = tid / HPKP; r < nt_rows; r += kThreads / HPKP) mx = fmaxf(mx, S[r * HPKP + h]);
+        // -------------------------- new maxima (identical in every thread)
+        float vmax = vred[0];
 #pragma unroll
-            for (int off = HPKP; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-            if (lane < HPKP) red[warp * HPKP + lane] = mx;
+        for (int w = 1; w < kWarps; ++w) vmax = fmaxf(vmax, vred[w]);
+        const int ew = vmax > 0.0f ? 14 - exponent_of(vmax) : 0;
+        const float wscale = exp2f(float(ew));
+        auto tile_max = [&](int h) {
+            float m = red[h];
+#pragma unroll
+            for (int w = 1; w < kWarps; ++w) m = fmaxf(m, red[w * HPKP + h]);
+            return m;
+        };
+        auto correction = [](float mo, float mn) { return mo == -INFINITY ? 0.0f : exp2f(mo - mn); };
+        const float mw_new = fmaxf(m_w, tile_max(hw));
+        const float al_w = correction(m_w, mw_new);
+        m_w = mw_new;
+        float al_a = 0.0f, al_b = 0.0f;
+        if (gl4 < HPKP) {
+            const float mn = fmaxf(m_a, tile_max(gl4));
+            al_a = correction(m_a, mn);
+            m_a = mn;
         }
-        __syncthreads();
-        if (tid < HPKP) {
-            float mx = red[tid];
-#pragma unroll
-            for (int w = 1; w < kWarps; ++w) mx = fmaxf(mx, red[w * HPKP + tid]);
-            const float mo = mrun[tid];
-            const float mn = fmaxf(mo, mx);
-            alpha[tid] = (mo == -INFINITY) ? 0.0f : exp2f(mo - mn);
-            mrun[tid] = mn;
+        if (gl4 + 8 < HPKP) {
+            const float mn = fmaxf(m_b, tile_max(gl4 + 8));
+            al_b = correction(m_b, mn);
+            m_b = mn;
         }
-        if (tid == 0) {
-            float vm = vred[0];
-#pragma unroll
-            for (int w = 1; w < kWarps; ++w) vm = fmaxf(vm, vred[w]);
-            ushared[0] = vm > 0.0f ? vm * (1.0f / 16777215.0f) : 1.0f;
-        }
-        __syncthreads();
-        // ------------------------------- weights -> 24-bit unsigned digits
-        {
-            const int h = tid % HPKP;
-            const float mn = mrun[h];
-            const float inv_u = 1.0f / ushared[0];
-            lsum *= alpha[h];
-            for (int qd = tid / HPKP; qd < 32; qd += kThreads / HPKP) {
-                const int kb = qd >> 3, half = (qd >> 2) & 1, tq = qd & 3;
-                const int pbase = 32 * kb + 16 * half + 2 * tq;
-                uint32_t qv[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int p = pbase + (i & 1) + 8 * (i >> 1);
-                    float wv = 0.0f;
-                    if (h < a.hpk && p < nt_rows) {
-                        const float e = exp2f(S[p * HPKP + h] - mn);
-                        lsum += e;
-                        wv = e * vs_s[p] * inv_u;
-                    }
-                    qv[i] = min(__float2uint_rn(wv), 0xFFFFFFu);
+        // ---------------------------------- weights -> f16 terms in shared
+        lsum *= al_w;
+        for (int pp = tid / HPKP; pp < kMmaTR / 2; pp += kThreads / HPKP) {
+            const int p = 2 * pp;
+            float w0 = 0.0f, w1 = 0.0f;
+            if (hw < a.hpk) {
+                if (p < nt_rows) {
+                    const float e = exp2f(S[p * HPKP + hw] - m_w);
+                    lsum += e;
+                    w0 = e * vs_s[p] * wscale;
                 }
-                const uint32_t lo0 = __byte_perm(qv[0], qv[1], 0x0040);
-                const uint32_t hi0 = __byte_perm(qv[2], qv[3], 0x0040);
-                const uint32_t lo1 = __byte_perm(qv[0], qv[1], 0x0051);
-                const uint32_t hi1 = __byte_perm(qv[2], qv[3], 0x0051);
-                const uint32_t lo2 = __byte_perm(qv[0], qv[1], 0x0062);
-                const uint32_t hi2 = __byte_perm(qv[2], qv[3], 0x0062);
-                const int kc = 2 * kb + half;
-                char *dst = A + (kc * MROWS) * 16 + 4 * tq;
-                *reinterpret_cast<uint32_t *>(dst + (0 * HPKP + h) * 16) = __byte_perm(lo0, hi0, 0x5410);
-                *reinterpret_cast<uint32_t *>(dst + (1 * HPKP + h) * 16) = __byte_perm(lo1, hi1, 0x5410);
-                *reinterpret_cast<uint32_t *>(dst + (2 * HPKP + h) * 16) = __byte_perm(lo2, hi2, 0x5410);
+                if (p + 1 < nt_rows) {
+                    const float e = exp2f(S[(p + 1) * HPKP + hw] - m_w);
+                    lsum += e;
+                    w1 = e * vs_s[p + 1] * wscale;
+                }
             }
+            const float r0 = w0 - __half2float(__float2half_rn(w0));
+            const float r1 = w1 - __half2float(__float2half_rn(w1));
+            *reinterpret_cast<uint32_t *>(Aw + aw_offset(0, p, hw)) = pack_half2(w0, w1);
+            *reinterpret_cast<uint32_t *>(Aw + aw_offset(1, p, hw)) = pack_half2(r0, r1);
         }
-        __syncthreads();  // digits visible; K slot drained
+        __syncthreads();  // weights visible; K slot drained
         if (tid == 0 && j + kMmaSlots < nseg) mma_issue<HPK>(ci, kmap, vmap, row_base, sm, bar, j + kMmaSlots);
-        // ------------------------------------------------ P.V (u8 x s8 MMA)
+        // ------------------------------------------------ P.V (f16 MMA)
         j = 2 * t + 1;
         slot = j % kMmaSlots;
         if (__syncthreads_or(!mbar_wait_bounded(&bar[slot], (j / kMmaSlots) & 1))) {
             ok = false;
             break;
         }
-        const uint32_t vbase = smem_addr(sm + slot * kMmaSlot);
-        int dv[MT][4][4];
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) dv[mt][q4][i] = 0;
-#pragma unroll
-        for (int kb = 0; kb < 4; ++kb) {
-            uint32_t af[MT][4];
-            {
-                const int mi = lane >> 3, rr = lane & 7;
-#pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                    const int m = 16 * mt + rr + 8 * (mi & 1);
-                    const int kc = 2 * kb + (mi >> 1);
-                    ldsm_x4(A_base + (kc * MROWS + m) * 16, af[mt]);
-                }
-            }
-#pragma unroll
-            for (int cb = 0; cb < 2; ++cb) {
-                const int cc = 2 * warp + cb;  // 16-channel chunk of the row
-                const int pos = 32 * kb + 8 * (lane >> 3) + (lane & 7);
-                uint32_t x[4];
-                ldsm_x4_t(vbase + pos * 128 + ((cc ^ (pos & 7)) << 4), x);
-                const uint32_t be0 = __byte_perm(x[0], x[1], 0x6420);
-                const uint32_t be1 = __byte_perm(x[2], x[3], 0x6420);
-                const uint32_t bo0 = __byte_perm(x[0], x[1], 0x7531);
-                const uint32_t bo1 = __byte_perm(x[2], x[3], 0x7531);
-#pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                    mma_u8s8(dv[mt][2 * cb], af[mt], be0, be1);
-                    mma_u8s8(dv[mt][2 * cb + 1], af[mt], bo0, bo1);
-                }
-            }
-        }
-        // digits -> f32, fold into the running accumulator:
-        // acc = acc * alpha + u * (d0 + 256 d1 + 65536 d2)
         {
-            const float u = ushared[0];
-            if (HPKP == 4) {
-                // rows: g<4 -> (digit 0, head g) and (digit 2, head g); g>=4 -> digit 1 of head g-4
+            // acc holds sum * 2^ew: rescale by the softmax correction and the
+            // change of weight exponent
+            const float fa = al_a * exp2f(float(ew - ew_prev));
+            const float fb = al_b * exp2f(float(ew - ew_prev));
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4)
+            for (int i = 0; i < 4; ++i) {
+                acc[i][0] *= fa;
+                acc[i][1] *= fa;
+                acc[i][2] *= fb;
+                acc[i][3] *= fb;
+            }
+            ew_prev = ew;
+        }
+        const uint32_t vbase = smem_addr(sm + slot * kMmaSlot);
+        const int mi = lane >> 3, rr = lane & 7;
+#pragma unroll 2
+        for (int ks = 0; ks < 8; ++ks) {
+            // V: matrices (positions +0..7, +8..15) x (channel chunks 2w, 2w + 1)
+            const int pos = 16 * ks + 8 * (mi & 1) + rr;
+            const int cc = 2 * warp + (mi >> 1);
+            uint32_t x[4];
+            ldsm_x4_t(vbase + pos * 128 + ((cc ^ (pos & 7)) << 4), x);
+            uint32_t b[4][2];  // [n-tile][reg]
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        const int d1 = __shfl_xor_sync(0xffffffffu, dv[0][q4][c], 16);
-                        if (gl4 < 4) {
-                            const int lo = d1 * 256 + dv[0][q4][c];
-                            const float val = fmaf(float(dv[0][q4][2 + c]), 65536.0f, float(lo));
-                            const int ch = (q4 >> 1) * 4 + 2 * c + (q4 & 1);
-                            acc[0][ch] = fmaf(acc[0][ch], alpha[gl4], u * val);
-                        }
-                    }
-            } else if (HPKP == 8) {
+            for (int blk = 0; blk < 2; ++blk) {
+                const uint32_t lo = x[2 * blk] ^ 0x80808080u, hi = x[2 * blk + 1] ^ 0x80808080u;
+                b[2 * blk][0] = codes_f16x2<0x4240>(lo);
+                b[2 * blk][1] = codes_f16x2<0x4240>(hi);
+                b[2 * blk + 1][0] = codes_f16x2<0x4341>(lo);
+                b[2 * blk + 1][1] = codes_f16x2<0x4341>(hi);
+            }
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4)
+            for (int term = 0; term < 2; ++term) {
+                const int m = rr + 8 * (mi & 1), ch = mi >> 1;
+                uint32_t af[4];
+                ldsm_x4(aw_base + ((term * 8 + ks) * 16 + m) * 32 + ((ch ^ ((m >> 2) & 1)) << 4), af);
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        const int lo = dv[0][q4][2 + c] * 256 + dv[0][q4][c];
-                        const float val = fmaf(float(dv[1][q4][c]), 65536.0f, float(lo));
-                        const int ch = (q4 >> 1) * 4 + 2 * c + (q4 & 1);
-                        acc[0][ch] = fmaf(acc[0][ch], alpha[gl4], u * val);
-                    }
-            } else {
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4)
-#pragma unroll
-                        for (int c = 0; c < 2; ++c) {
-                            const int lo = dv[1][q4][2 * hh + c] * 256 + dv[0][q4][2 * hh + c];
-                            const float val = fmaf(float(dv[2][q4][2 * hh + c]), 65536.0f, float(lo));
-                            const int ch = (q4 >> 1) * 4 + 2 * c + (q4 & 1);
-                            acc[hh][ch] = fmaf(acc[hh][ch], alpha[gl4 + 8 * hh], u * val);
-                        }
+                for (int q = 0; q < 4; ++q) mma_f16(acc[q], af[0], af[1], af[2], af[3], b[q][0], b[q][1]);
             }
         }
-        __syncthreads();  // V slot drained, alpha/u no longer needed
-        if (tid == 0 && j + kMmaSlots < nseg) mma_issue<HPK>(ci, kmap, vmap, row_base, sm, bar, j + kMmaSlots);
     }
 
     if (!ok) {
@@ -483,10 +447,10 @@ __device__ void split_mma_body(const ChunkInfo &ci, int64_t row_base, const Spli
 
     // ------------------------------------------------------------ partials
     {
-        const int h = tid % HPKP;
         float l = lsum;
 #pragma unroll
         for (int off = HPKP; off < 32; off <<= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+        __syncthreads();  // every warp is past its last read of red
         if (lane < HPKP) red[warp * HPKP + lane] = l;
     }
     __syncthreads();
@@ -494,26 +458,31 @@ __device__ void split_mma_body(const ChunkInfo &ci, int64_t row_base, const Spli
         float l = red[tid];
 #pragma unroll
         for (int w = 1; w < kWarps; ++w) l += red[w * HPKP + tid];
-        a.pm[ci.pidx0 + tid] = mrun[tid];
+        a.pm[ci.pidx0 + tid] = m_w;  // hw == tid here
         a.pl[ci.pidx0 + tid] = l;
     }
-    // lane (gl4, t4) of warp w holds channels 32w + 16cb + 4t4 + {0..3} of
-    // head gl4 (+8 for the second head when HPKP == 16)
+    // lane (gl4, t4) of warp w holds heads gl4 and gl4 + 8 at channels
+    // 32w + 16 blk + 4 t4 + {0, 2} (even tile) and + {1, 3} (odd tile)
+    const float unscale = exp2f(-float(ew_prev));
 #pragma unroll
-    for (int hh = 0; hh < NH; ++hh) {
+    for (int hh = 0; hh < 2; ++hh) {
         const int h = gl4 + 8 * hh;
-        const bool mine = (HPKP == 4 ? gl4 < 4 : true) && h < a.hpk;
-        if (mine) {
-            float *dst = a.pacc + (ci.pidx0 + h) * 128 + 32 * warp + 4 * t4;
-            *reinterpret_cast<float4 *>(dst) = make_float4(acc[hh][0], acc[hh][1], acc[hh][2], acc[hh][3]);
-            *reinterpret_cast<float4 *>(dst + 16) =
-                make_float4(acc[hh][4], acc[hh][5], acc[hh][6], acc[hh][7]);
+        if (h < a.hpk) {
+#pragma unroll
+            for (int blk = 0; blk < 2; ++blk) {
+                float *dst = a.pacc + (ci.pidx0 + h) * 128 + 32 * warp + 16 * blk + 4 * t4;
+                const float *e = acc[2 * blk];
+                const float *o = acc[2 * blk + 1];
+                *reinterpret_cast<float4 *>(dst) =
+                    make_float4(e[2 * hh] * unscale, o[2 * hh] * unscale, e[2 * hh + 1] * unscale,
+                                o[2 * hh + 1] * unscale);
+            }
         }
     }
 }
 
 template <int HPK>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, MmaCfg<HPK>::MIN_CTAS)
     split_mma_kernel(SplitArgs a, LayerSrc src, const __grid_constant__ MmaMaps maps) {
     extern __shared__ __align__(128) char smem[];
     const int b = blockIdx.z, gl = blockIdx.y, c = blockIdx.x;
