@@ -197,11 +197,10 @@ def run_gpu(args, rank, world):
     import kv_cache_decode_attention_gb300 as kvd
     from kv_cache_decode_attention_gb300 import workloads as W
 
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    from kv_cache_decode_attention_gb300 import replicas
+
+    dev = torch.device("cuda", replicas.rank_info().local_rank)
     torch.cuda.set_device(dev)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
 
     probe = build_workload(args.workload, 1)
     wl0 = probe[0]
@@ -249,8 +248,7 @@ def run_gpu(args, rank, world):
     sampler = ClockSampler(dev.index)
     with sampler:
         time.sleep(0.3)
-        if dist is not None:
-            dist.barrier()
+        replicas.barrier()
         torch.cuda.synchronize()
         c0 = time.time()
         t0 = torch.cuda.Event(enable_timing=True)
@@ -262,8 +260,7 @@ def run_gpu(args, rank, world):
         t1.record(stream)
         torch.cuda.synchronize()
         torch.cuda.profiler.stop()
-        if dist is not None:
-            dist.barrier()
+        replicas.barrier()
         c1 = time.time()
         time.sleep(0.1)
     elapsed_ms = t0.elapsed_time(t1)
@@ -276,12 +273,9 @@ def run_gpu(args, rank, world):
         lens[r] += 1
         bytes_total += W.decode_bytes(w.mode, n_live, w.hd, w.n_q, lens[r], True, w.n_seq)
     dec_ms = [a.elapsed_time(b) for a, b in ev]
-    if dist is not None:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = replicas.max_over_ranks(elapsed_ms)  # every rank ran its own replica
     ms_per_step = elapsed_ms / args.steps
-    gbs = bytes_total / (elapsed_ms * 1e-3) / 1e9 * world
+    gbs = replicas.whole_job_rate(bytes_total, elapsed_ms * 1e-3, world) / 1e9
 
     # ---- dominant kernel: the decode call without imp, timed alone (same
     #      workload and launch configuration, CUDA events on the launching stream)
@@ -390,13 +384,15 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
+    from kv_cache_decode_attention_gb300.replicas import rank_info
+
+    info = rank_info()
+    world, rank = info.world, info.rank
     if world > 1 and args.impl != "reference":
         import torch
         import torch.distributed as dist
 
-        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.cuda.set_device(info.local_rank)
         dist.init_process_group("nccl")
     from __graft_entry__ import build
 

@@ -83,6 +83,7 @@ class LayerKvCache:
         self.imp_base = np.concatenate([[0], np.cumsum(self.cap16)[:-1]]).astype(np.int64)
         self.imp_len = int(self.cap16.sum())
         self.live_heads = [h for h in range(self.n_kv) if self.alive[h]]
+        self._ws_bytes = {}
 
     # ---- host-mirrored state -------------------------------------------
     def seq_len(self, b: int) -> int:
@@ -111,9 +112,13 @@ class LayerKvCache:
         _abi.call("kvd_layer_reset", C.byref(self.L), int(seq), _stream(stream))
 
     def workspace_bytes(self, n_q: int, with_imp: bool) -> int:
-        n = C.c_int64(0)
-        _abi.call("kvd_decode_workspace_bytes", C.byref(self.L), int(n_q), int(with_imp), C.byref(n))
-        return int(n.value)
+        key = (int(n_q), bool(with_imp))
+        got = self._ws_bytes.get(key)
+        if got is None:  # depends only on the layer's shape: ask the library once
+            n = C.c_int64(0)
+            _abi.call("kvd_decode_workspace_bytes", C.byref(self.L), key[0], int(key[1]), C.byref(n))
+            got = self._ws_bytes[key] = int(n.value)
+        return got
 
     # ---- views of the stored rows (for inspection and tests) ------------
     def region(self, b: int, kv_head: int) -> tuple[int, int]:

@@ -23,6 +23,7 @@ cudaError_t split_layer_q8_mma(int, const SplitArgs &, const LayerSrc &, const M
 namespace {
 
 constexpr int kMinChunk = 256;           // rows; multiple of every tile height
+constexpr int kMaxChunk = 2048;          // rows; bounds one CTA's f32 accumulation chain
 constexpr int64_t kTargetCtas = 152 * 8; // about four waves of two CTAs per SM
 
 int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
@@ -34,11 +35,14 @@ int hpk_bucket(int hpk) {
     return b;
 }
 
-// Rows per chunk: at least kMinChunk, large enough that the grid holds about
-// kTargetCtas chunks, a multiple of kMinChunk.
+// Rows per chunk: a multiple of kMinChunk, large enough that the grid holds
+// about kTargetCtas chunks, but at most kMaxChunk.  The cap keeps each CTA's
+// sequential f32 accumulation short (its rounding grows like the square root
+// of the rows summed, and long diffuse softmaxes shrink the output), at the
+// cost of more partials, which are ~0.2% of the bytes.
 int32_t pick_chunk(int64_t work_rows) {
     const int64_t c = std::max<int64_t>(kMinChunk, ceil_div(work_rows, kTargetCtas));
-    return int32_t(round_up(c, kMinChunk));
+    return int32_t(std::min<int64_t>(kMaxChunk, round_up(c, kMinChunk)));
 }
 
 struct DecodeWs {
@@ -92,7 +96,7 @@ RswaWs rswa_ws(int32_t B, int32_t H, int32_t hd, int64_t ref_cap, int32_t W) {
 // ------------------------------------------------------------------ imp
 
 struct ImpArgs {
-    const float *scores;  // [storage row][hpk] log2 scores
+    const float *scores;  // per (sequence, live group): [hpk][cap] log2 scores
     const float *ml;      // [n_seq][n_q][2]
     float *imp;
     const int64_t *row_base, *cap, *imp_base;
@@ -102,22 +106,32 @@ struct ImpArgs {
 
 // imp[b][p] += sum over live groups (ascending) and their heads (ascending)
 // of 2^(s - M) / L: the softmax weight of every live query head on row p.
-__global__ void __launch_bounds__(256) imp_kernel(ImpArgs a) {
+// Each block first stages the (max, 1/sum) of sequence b's heads in shared
+// memory; threads then own rows and read their scores coalesced.
+constexpr int kImpThreads = 256;
+
+__global__ void __launch_bounds__(kImpThreads) imp_kernel(ImpArgs a) {
+    extern __shared__ float mlinv[];  // [n_q][2]: max, 1/sum
     const int b = blockIdx.y;
-    const int p = blockIdx.x * 256 + threadIdx.x;
     const int L = a.seq_len[b];
+    const int p0 = blockIdx.x * kImpThreads;
+    if (p0 >= L) return;
+    for (int i = threadIdx.x; i < a.n_q; i += kImpThreads) {
+        const float M = a.ml[(int64_t(b) * a.n_q + i) * 2];
+        const float Ls = a.ml[(int64_t(b) * a.n_q + i) * 2 + 1];
+        mlinv[2 * i] = M;
+        mlinv[2 * i + 1] = Ls > 0.0f ? 1.0f / Ls : 0.0f;
+    }
+    __syncthreads();
+    const int p = p0 + threadIdx.x;
     if (p >= L) return;
     const int64_t cap = a.cap[b];
     float add = 0.0f;
     for (int gl = 0; gl < a.n_live; ++gl) {
         const int g = a.live[gl];
-        const int64_t row = a.row_base[b] + gl * cap + p;
-        for (int hh = 0; hh < a.hpk; ++hh) {
-            const int h = g * a.hpk + hh;
-            const float M = a.ml[(int64_t(b) * a.n_q + h) * 2];
-            const float Ls = a.ml[(int64_t(b) * a.n_q + h) * 2 + 1];
-            add += exp2f(a.scores[row * a.hpk + hh] - M) / Ls;
-        }
+        const float *sg = a.scores + (a.row_base[b] + gl * cap) * a.hpk + p;
+        const float *mg = mlinv + 2 * g * a.hpk;
+        for (int hh = 0; hh < a.hpk; ++hh) add += exp2f(sg[hh * cap] - mg[2 * hh]) * mg[2 * hh + 1];
     }
     a.imp[a.imp_base[b] + p] += add;
 }
@@ -293,8 +307,13 @@ extern "C" kvd_status decode_attention(const float *q, const kvd_layer *L, int32
         ia.n_q = n_q;
         ia.hpk = hpk;
         ia.n_live = l->n_live;
-        dim3 igrid(unsigned(ceil_div(max_len, 256)), unsigned(l->n_seq));
-        imp_kernel<<<igrid, 256, 0, st>>>(ia);
+        dim3 igrid(unsigned(ceil_div(max_len, kImpThreads)), unsigned(l->n_seq));
+        const size_t ml_bytes = size_t(n_q) * 2 * sizeof(float);
+        if (ml_bytes > 48 * 1024 &&
+            cudaFuncSetAttribute(imp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(ml_bytes)) != cudaSuccess)
+            return KVD_ECUDA;
+        imp_kernel<<<igrid, kImpThreads, ml_bytes, st>>>(ia);
         if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
     }
     return KVD_OK;

@@ -87,7 +87,8 @@ struct ChunkInfo {
     int64_t pidx0;                // partial index of the group's head 0
     const float *q;               // query of the group's head 0
     const float *kcol;            // K field of the group, or null
-    int64_t score0;               // scores index of row 0, head 0 (or -1)
+    int64_t score0;               // scores index of the chunk's row 0, head 0 (or -1)
+    int64_t score_ld;             // scores stride between heads (rows of the region)
 };
 
 // Butterfly reduce-scatter of E partial sums held by every lane: after it,
@@ -255,7 +256,7 @@ __device__ void split_body(const ChunkInfo &ci, const SplitArgs &a, char *smem) 
                 const float sv = r < nt ? s : -INFINITY;
                 sc[r * HPK + h] = sv;
                 if (a.scores != nullptr && r < nt && h < a.hpk)
-                    a.scores[ci.score0 + int64_t(row0 + r) * a.hpk + h] = sv;
+                    a.scores[ci.score0 + h * ci.score_ld + row0 + r] = sv;
             }
         }
         __syncthreads();
@@ -291,12 +292,6 @@ __device__ void split_body(const ChunkInfo &ci, const SplitArgs &a, char *smem) 
                 sc[r * HPK + h] = VQ ? e * vsr[r] : e;
             }
         }
-#pragma unroll
-        for (int h = 0; h < HPK; ++h) {
-            const float al = alpha[h];
-#pragma unroll
-            for (int jj = 0; jj < CPL; ++jj) acc[h][jj] *= al;
-        }
         __syncthreads();  // K slot drained, weights visible
         if (tid == 0 && j + kNSeg < nseg) issue_segment<HD, HPK, KQ, VQ>(ci, smem, bar, j + kNSeg);
         // ---------------------------------------------------- V tile
@@ -307,6 +302,13 @@ __device__ void split_body(const ChunkInfo &ci, const SplitArgs &a, char *smem) 
             break;
         }
         const char *vseg = smem + slot * C::SLOT;
+        // this tile's rows accumulate into fresh registers, folded into the
+        // running (rescaled) sum once per tile: short rounding chains
+        float tacc[HPK][CPL];
+#pragma unroll
+        for (int h = 0; h < HPK; ++h)
+#pragma unroll
+            for (int jj = 0; jj < CPL; ++jj) tacc[h][jj] = 0.0f;
         for (int r = warp; r < nt; r += kWarps) {
             float x[CPL];
             load_lane<CPL, VQ>(vseg + r * C::VROW, lane, x);
@@ -327,7 +329,13 @@ __device__ void split_body(const ChunkInfo &ci, const SplitArgs &a, char *smem) 
 #pragma unroll
             for (int h = 0; h < HPK; ++h)
 #pragma unroll
-                for (int jj = 0; jj < CPL; ++jj) acc[h][jj] = fmaf(w[h], x[jj], acc[h][jj]);
+                for (int jj = 0; jj < CPL; ++jj) tacc[h][jj] = fmaf(w[h], x[jj], tacc[h][jj]);
+        }
+#pragma unroll
+        for (int h = 0; h < HPK; ++h) {
+            const float al = alpha[h];
+#pragma unroll
+            for (int jj = 0; jj < CPL; ++jj) acc[h][jj] = fmaf(acc[h][jj], al, tacc[h][jj]);
         }
         __syncthreads();  // V slot drained
         if (tid == 0 && j + kNSeg < nseg) issue_segment<HD, HPK, KQ, VQ>(ci, smem, bar, j + kNSeg);
@@ -411,7 +419,9 @@ __global__ void __launch_bounds__(kThreads, 2) split_layer_kernel(SplitArgs a, L
     const int g = src.live[gl];
     ci.q = a.q + (int64_t(b) * a.n_q + int64_t(g) * a.hpk) * HD;
     ci.kcol = KQ ? src.kcol + (int64_t(b) * src.n_live + gl) * HD : nullptr;
-    ci.score0 = row * a.hpk;
+    // scores region of (b, gl): [hpk][cap] starting at its first storage row * hpk
+    ci.score0 = (src.row_base[b] + int64_t(gl) * cap) * a.hpk + r0;
+    ci.score_ld = cap;
     split_body<HD, HPK, KQ, VQ>(ci, a, smem);
 }
 
@@ -460,6 +470,7 @@ __global__ void __launch_bounds__(kThreads, 2) split_rswa_kernel(SplitArgs a, Rs
     ci.q = a.q + head * HD;
     ci.kcol = nullptr;
     ci.score0 = -1;
+    ci.score_ld = 0;
     split_body<HD, 1, false, false>(ci, a, smem);
 }
 

@@ -53,14 +53,13 @@ template <int HPK>
 struct MmaCfg {
     static constexpr int HPKP = HPK < 4 ? 4 : HPK;          // heads padded for the layouts
     static constexpr int NT = HPKP / 8 > 0 ? HPKP / 8 : 1;  // score n8 tiles
-    static constexpr int S_OFF = kMmaSlots * kMmaSlot;       // scores [TR][HPKP] f32
-    static constexpr int AW_OFF = S_OFF + kMmaTR * HPKP * 4;
+    static constexpr int S_OFF = kMmaSlots * kMmaSlot;       // q staging [HPKP][128] f32
+    static constexpr int AW_OFF = S_OFF + HPKP * 128 * 4;
     static constexpr int MISC_OFF = AW_OFF + kMmaAw;
     // misc: bars[kMmaSlots], red[kWarps][HPKP], vred[kWarps]
     static constexpr int SMEM = MISC_OFF + kMmaSlots * 8 + kWarps * HPKP * 4 + kWarps * 4;
     static constexpr int SMEM_ALLOC = SMEM + 1024;  // room to align the base to 1024
     static constexpr int MIN_CTAS = HPK >= 16 ? 2 : 3;
-    static_assert(kMmaTR * HPKP * 4 >= HPKP * 128 * 4, "q staging reuses the score area");
 };
 
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
@@ -157,11 +156,12 @@ __device__ void split_mma_body(const ChunkInfo &ci, int64_t row_base, const Spli
                                const CUtensorMap *kmap, const CUtensorMap *vmap, char *smem_raw) {
     using C = MmaCfg<HPK>;
     constexpr int HPKP = C::HPKP, NT = C::NT;
-    char *sm = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                        ~uintptr_t(1023));
+    // align to 1024 by offsetting the shared array itself, so every derived
+    // pointer stays a known shared-memory pointer (plain LDS/STS)
+    char *sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int gl4 = lane >> 2, t4 = lane & 3;
-    float *S = reinterpret_cast<float *>(sm + C::S_OFF);
+    const int mi = lane >> 3, rr = lane & 7;  // ldmatrix: matrix index, row in matrix
     char *Aw = sm + C::AW_OFF;
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + C::MISC_OFF);
     float *red = reinterpret_cast<float *>(bar + kMmaSlots);
@@ -180,8 +180,8 @@ __device__ void split_mma_body(const ChunkInfo &ci, int64_t row_base, const Spli
         for (int j = 0; j < min(kMmaSlots, nseg); ++j) mma_issue<HPK>(ci, kmap, vmap, row_base, sm, bar, j);
 
     // ---- query terms: q * kcol * scale * log2e * 2^E_h = t1 + t2 (f16),
-    //      staged through the score area
-    float *qf = S;
+    //      staged through the staging area
+    float *qf = reinterpret_cast<float *>(sm + C::S_OFF);
     for (int i = tid; i < HPKP * 128; i += kThreads) {
         const int h = i >> 7, d = i & 127;
         qf[i] = h < a.hpk ? ci.q[h * 128 + d] * ci.kcol[d] * a.qscale : 0.0f;
@@ -221,12 +221,44 @@ __device__ void split_mma_body(const ChunkInfo &ci, int64_t row_base, const Spli
                 bq[g][ks][nt][1][1] = pack_half2(r[2], r[3]);
             }
     }
-    __syncthreads();  // staging read before the scores overwrite it
+    __syncthreads();  // staging read before anything reuses it
 
-    // running state (every thread derives the same maxima from red)
-    const int hw = tid % HPKP;  // head whose weights this thread writes
-    float m_w = -INFINITY, m_a = -INFINITY, m_b = -INFINITY;  // heads hw, gl4, gl4 + 8
-    float lsum = 0.0f;
+    // Lane-constant shared-memory offsets.  K tile (ldmatrix, scores): row
+    // warp*32 + mb*16 + rr + 8*(mi&1), 16-byte chunk 2g + (mi>>1), swizzled by
+    // the row's low 3 bits (= rr).  V tile (ldmatrix.trans): position 16ks +
+    // 8*(mi&1) + rr, chunk 2*warp + (mi>>1).  Weights: head row rr + 8*(mi&1),
+    // half mi>>1, swapped on heads 4..7 / 12..15.
+    const uint32_t k_lane = uint32_t(warp * 32 + rr + 8 * (mi & 1)) * 128;
+    uint32_t k_chunk[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) k_chunk[g] = uint32_t(((2 * g + (mi >> 1)) ^ rr) << 4);
+    const uint32_t v_lane = uint32_t(8 * (mi & 1) + rr) * 128 + uint32_t(((2 * warp + (mi >> 1)) ^ rr) << 4);
+    const int am = rr + 8 * (mi & 1);
+    const uint32_t aw_lane = uint32_t(am * 32 + (((mi >> 1) ^ ((am >> 2) & 1)) << 4));
+    const uint32_t aw_base = smem_addr(Aw) + aw_lane;
+    // where this lane writes the weight terms of its score values: head h =
+    // nt*8 + 2*t4 + c, position warp*32 + mb*16 + gl4 + 8*rw (k16 step warp*2 + mb)
+    int wofs[2][NT][2][2];
+#pragma unroll
+    for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+#pragma unroll
+                for (int rw = 0; rw < 2; ++rw) {
+                    const int h = nt * 8 + 2 * t4 + c;
+                    wofs[mb][nt][c][rw] =
+                        ((warp * 2 + mb) * 16 + h) * 32 + ((rw ^ ((h >> 2) & 1)) << 4) + gl4 * 2;
+                }
+
+    // running state: maxima and sums of this lane's score-column heads
+    // (nt*8 + 2*t4 + c) and maxima of its P.V heads (gl4, gl4 + 8); every lane
+    // derives identical maxima from the per-warp values in red
+    float mcol[NT][2], lcol[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) mcol[nt][0] = mcol[nt][1] = -INFINITY, lcol[nt][0] = lcol[nt][1] = 0.0f;
+    float m_a = -INFINITY, m_b = -INFINITY;
     int ew_prev = 0;
     float acc[4][4];  // [n-tile: block 0 even, 0 odd, 1 even, 1 odd][frag]
 #pragma unroll
@@ -234,7 +266,6 @@ __device__ void split_mma_body(const ChunkInfo &ci, int64_t row_base, const Spli
 #pragma unroll
         for (int c = 0; c < 4; ++c) acc[i][c] = 0.0f;
     bool ok = true;
-    const uint32_t aw_base = smem_addr(Aw);
 
     for (int t = 0; t < ntiles; ++t) {
         const int row0 = t * kMmaTR;
@@ -249,13 +280,11 @@ __device__ void split_mma_body(const ChunkInfo &ci, int64_t row_base, const Spli
         if (tid == 0 && t > 0 && j - 1 + kMmaSlots < nseg)
             mma_issue<HPK>(ci, kmap, vmap, row_base, sm, bar, j - 1 + kMmaSlots);
         const char *kseg = sm + slot * kMmaSlot;
-        const uint32_t kbase = smem_addr(kseg);
+        const uint32_t kaddr = smem_addr(kseg) + k_lane;
         const float *ks_s = reinterpret_cast<const float *>(kseg + kMmaKsOff);
         const float *vs_s = reinterpret_cast<const float *>(kseg + kMmaVsOff);
         // ------------------------------------------------ scores (f16 MMA)
-        float wmax[NT][2];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) wmax[nt][0] = wmax[nt][1] = -INFINITY;
+        float sreg[2][NT][2][2];  // [m block][n-tile][column][row gl4 / gl4 + 8]
 #pragma unroll
         for (int mb = 0; mb < 2; ++mb) {
             const int r0 = warp * 32 + mb * 16;
@@ -268,13 +297,10 @@ __device__ void split_mma_body(const ChunkInfo &ci, int64_t row_base, const Spli
             const float4 ksB = *reinterpret_cast<const float4 *>(&ks_s[(r0 + gl4 + 8) * 4]);
             const float kA[4] = {ksA.x, ksA.y, ksA.z, ksA.w};
             const float kB[4] = {ksB.x, ksB.y, ksB.z, ksB.w};
-            const int mi = lane >> 3, rr = lane & 7;
-            const int lrow = r0 + rr + 8 * (mi & 1);
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
-                const int chunk = 2 * g + (mi >> 1);
                 uint32_t w[4];
-                ldsm_x4(kbase + lrow * 128 + ((chunk ^ (lrow & 7)) << 4), w);
+                ldsm_x4(kaddr + mb * 2048 + k_chunk[g], w);
                 // row gl4 / gl4 + 8, channels 4t..4t+3 of k16 step 0 and 1
                 const uint32_t u0 = w[0] ^ 0x80808080u, u1 = w[1] ^ 0x80808080u;
                 const uint32_t u2 = w[2] ^ 0x80808080u, u3 = w[3] ^ 0x80808080u;
@@ -298,22 +324,24 @@ __device__ void split_mma_body(const ChunkInfo &ci, int64_t row_base, const Spli
             }
             const int ra = r0 + gl4, rb = r0 + gl4 + 8;
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
-                    const int h = nt * 8 + 2 * t4 + c;
-                    const float sa = ra < nt_rows ? sacc[nt][c] * qexp[nt][c] : -INFINITY;
-                    const float sb = rb < nt_rows ? sacc[nt][2 + c] * qexp[nt][c] : -INFINITY;
-                    wmax[nt][c] = fmaxf(wmax[nt][c], fmaxf(sa, sb));
-                    if (h < HPKP) {
-                        S[ra * HPKP + h] = sa;
-                        S[rb * HPKP + h] = sb;
-                        if (a.scores != nullptr && h < a.hpk) {
-                            if (ra < nt_rows) a.scores[ci.score0 + int64_t(row0 + ra) * a.hpk + h] = sa;
-                            if (rb < nt_rows) a.scores[ci.score0 + int64_t(row0 + rb) * a.hpk + h] = sb;
+                    sreg[mb][nt][c][0] = ra < nt_rows ? sacc[nt][c] * qexp[nt][c] : -INFINITY;
+                    sreg[mb][nt][c][1] = rb < nt_rows ? sacc[nt][2 + c] * qexp[nt][c] : -INFINITY;
+                }
+            if (a.scores != nullptr) {
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        const int h = nt * 8 + 2 * t4 + c;
+                        if (h < a.hpk) {
+                            float *sp = a.scores + ci.score0 + h * ci.score_ld + row0;
+                            if (ra < nt_rows) sp[ra] = sreg[mb][nt][c][0];
+                            if (rb < nt_rows) sp[rb] = sreg[mb][nt][c][1];
                         }
                     }
-                }
             }
         }
         // per-warp maxima of every head and of the V row scales
@@ -321,7 +349,8 @@ __device__ void split_mma_body(const ChunkInfo &ci, int64_t row_base, const Spli
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
-                float m = wmax[nt][c];
+                float m = fmaxf(fmaxf(sreg[0][nt][c][0], sreg[0][nt][c][1]),
+                                fmaxf(sreg[1][nt][c][0], sreg[1][nt][c][1]));
                 m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
                 m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
                 m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
@@ -341,49 +370,56 @@ __device__ void split_mma_body(const ChunkInfo &ci, int64_t row_base, const Spli
         for (int w = 1; w < kWarps; ++w) vmax = fmaxf(vmax, vred[w]);
         const int ew = vmax > 0.0f ? 14 - exponent_of(vmax) : 0;
         const float wscale = exp2f(float(ew));
+        // Heads past HPKP (padding lanes) read a clamped head: harmless, and
+        // it keeps every lane on the same path.  Tile maxima are finite (each
+        // tile has a valid row), so exp2(old - new) is 0 on the first tile.
         auto tile_max = [&](int h) {
+            h = min(h, HPKP - 1);
             float m = red[h];
 #pragma unroll
             for (int w = 1; w < kWarps; ++w) m = fmaxf(m, red[w * HPKP + h]);
             return m;
         };
-        auto correction = [](float mo, float mn) { return mo == -INFINITY ? 0.0f : exp2f(mo - mn); };
-        const float mw_new = fmaxf(m_w, tile_max(hw));
-        const float al_w = correction(m_w, mw_new);
-        m_w = mw_new;
-        float al_a = 0.0f, al_b = 0.0f;
-        if (gl4 < HPKP) {
-            const float mn = fmaxf(m_a, tile_max(gl4));
-            al_a = correction(m_a, mn);
-            m_a = mn;
-        }
-        if (gl4 + 8 < HPKP) {
-            const float mn = fmaxf(m_b, tile_max(gl4 + 8));
-            al_b = correction(m_b, mn);
-            m_b = mn;
-        }
-        // ---------------------------------- weights -> f16 terms in shared
-        lsum *= al_w;
-        for (int pp = tid / HPKP; pp < kMmaTR / 2; pp += kThreads / HPKP) {
-            const int p = 2 * pp;
-            float w0 = 0.0f, w1 = 0.0f;
-            if (hw < a.hpk) {
-                if (p < nt_rows) {
-                    const float e = exp2f(S[p * HPKP + hw] - m_w);
-                    lsum += e;
-                    w0 = e * vs_s[p] * wscale;
-                }
-                if (p + 1 < nt_rows) {
-                    const float e = exp2f(S[(p + 1) * HPKP + hw] - m_w);
-                    lsum += e;
-                    w1 = e * vs_s[p + 1] * wscale;
-                }
+        const float mna = fmaxf(m_a, tile_max(gl4));
+        const float al_a = exp2f(m_a - mna);
+        m_a = mna;
+        const float mnb = fmaxf(m_b, tile_max(gl4 + 8));
+        const float al_b = exp2f(m_b - mnb);
+        m_b = mnb;
+        // ------------------- weights from the score registers -> f16 terms
+        float vsw[2][2];  // V row scale * 2^ew of this lane's rows (0 past the tile)
+#pragma unroll
+        for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
+            for (int rw = 0; rw < 2; ++rw) {
+                const int p = warp * 32 + mb * 16 + gl4 + 8 * rw;
+                vsw[mb][rw] = p < nt_rows ? vs_s[p] * wscale : 0.0f;
             }
-            const float r0 = w0 - __half2float(__float2half_rn(w0));
-            const float r1 = w1 - __half2float(__float2half_rn(w1));
-            *reinterpret_cast<uint32_t *>(Aw + aw_offset(0, p, hw)) = pack_half2(w0, w1);
-            *reinterpret_cast<uint32_t *>(Aw + aw_offset(1, p, hw)) = pack_half2(r0, r1);
-        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                // padding columns (heads >= HPKP when HPKP is 4) compute like
+                // the others and write weight rows the value pass never reads
+                const int h = nt * 8 + 2 * t4 + c;
+                const float mn = fmaxf(mcol[nt][c], tile_max(h));
+                lcol[nt][c] *= exp2f(mcol[nt][c] - mn);
+                mcol[nt][c] = mn;
+                const float live = h < a.hpk ? 1.0f : 0.0f;
+#pragma unroll
+                for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
+                    for (int rw = 0; rw < 2; ++rw) {
+                        // rows past the tile hold -inf scores: e = 0
+                        const float e = live * exp2f(sreg[mb][nt][c][rw] - mn);
+                        lcol[nt][c] += e;
+                        const float w = e * vsw[mb][rw];
+                        const __half t1 = __float2half_rn(w);
+                        const __half t2 = __float2half_rn(w - __half2float(t1));
+                        *reinterpret_cast<__half *>(Aw + wofs[mb][nt][c][rw]) = t1;
+                        *reinterpret_cast<__half *>(Aw + 8 * 16 * 32 + wofs[mb][nt][c][rw]) = t2;
+                    }
+            }
         __syncthreads();  // weights visible; K slot drained
         if (tid == 0 && j + kMmaSlots < nseg) mma_issue<HPK>(ci, kmap, vmap, row_base, sm, bar, j + kMmaSlots);
         // ------------------------------------------------ P.V (f16 MMA)
@@ -393,29 +429,20 @@ __device__ void split_mma_body(const ChunkInfo &ci, int64_t row_base, const Spli
             ok = false;
             break;
         }
-        {
-            // acc holds sum * 2^ew: rescale by the softmax correction and the
-            // change of weight exponent
-            const float fa = al_a * exp2f(float(ew - ew_prev));
-            const float fb = al_b * exp2f(float(ew - ew_prev));
+        // This tile's P.V goes into fresh MMA accumulators (16 chained MMAs
+        // each); it is folded into the running sum with IEEE FMAs below, so the
+        // tensor cores' accumulation rounding never compounds across tiles.
+        float dacc[4][4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                acc[i][0] *= fa;
-                acc[i][1] *= fa;
-                acc[i][2] *= fb;
-                acc[i][3] *= fb;
-            }
-            ew_prev = ew;
-        }
-        const uint32_t vbase = smem_addr(sm + slot * kMmaSlot);
-        const int mi = lane >> 3, rr = lane & 7;
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) dacc[i][c] = 0.0f;
+        const uint32_t vaddr = smem_addr(sm + slot * kMmaSlot) + v_lane;
 #pragma unroll 2
         for (int ks = 0; ks < 8; ++ks) {
             // V: matrices (positions +0..7, +8..15) x (channel chunks 2w, 2w + 1)
-            const int pos = 16 * ks + 8 * (mi & 1) + rr;
-            const int cc = 2 * warp + (mi >> 1);
             uint32_t x[4];
-            ldsm_x4_t(vbase + pos * 128 + ((cc ^ (pos & 7)) << 4), x);
+            ldsm_x4_t(vaddr + ks * 2048, x);
             uint32_t b[4][2];  // [n-tile][reg]
 #pragma unroll
             for (int blk = 0; blk < 2; ++blk) {
@@ -427,12 +454,25 @@ __device__ void split_mma_body(const ChunkInfo &ci, int64_t row_base, const Spli
             }
 #pragma unroll
             for (int term = 0; term < 2; ++term) {
-                const int m = rr + 8 * (mi & 1), ch = mi >> 1;
                 uint32_t af[4];
-                ldsm_x4(aw_base + ((term * 8 + ks) * 16 + m) * 32 + ((ch ^ ((m >> 2) & 1)) << 4), af);
+                ldsm_x4(aw_base + (term * 8 + ks) * 512, af);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) mma_f16(acc[q], af[0], af[1], af[2], af[3], b[q][0], b[q][1]);
+                for (int q = 0; q < 4; ++q) mma_f16(dacc[q], af[0], af[1], af[2], af[3], b[q][0], b[q][1]);
             }
+        }
+        {
+            // acc holds sum * 2^ew: rescale by the softmax correction and the
+            // change of weight exponent, then add this tile
+            const float fa = al_a * exp2f(float(ew - ew_prev));
+            const float fb = al_b * exp2f(float(ew - ew_prev));
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc[i][0] = fmaf(acc[i][0], fa, dacc[i][0]);
+                acc[i][1] = fmaf(acc[i][1], fa, dacc[i][1]);
+                acc[i][2] = fmaf(acc[i][2], fb, dacc[i][2]);
+                acc[i][3] = fmaf(acc[i][3], fb, dacc[i][3]);
+            }
+            ew_prev = ew;
         }
     }
 
@@ -446,20 +486,40 @@ __device__ void split_mma_body(const ChunkInfo &ci, int64_t row_base, const Spli
     }
 
     // ------------------------------------------------------------ partials
-    {
-        float l = lsum;
+    // sums: reduce each column head over the lanes sharing it, then the warps
 #pragma unroll
-        for (int off = HPKP; off < 32; off <<= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-        __syncthreads();  // every warp is past its last read of red
-        if (lane < HPKP) red[warp * HPKP + lane] = l;
-    }
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            float l = lcol[nt][c];
+            l += __shfl_xor_sync(0xffffffffu, l, 4);
+            l += __shfl_xor_sync(0xffffffffu, l, 8);
+            l += __shfl_xor_sync(0xffffffffu, l, 16);
+            lcol[nt][c] = l;
+        }
+    __syncthreads();  // every warp is past its last read of red
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const int h = nt * 8 + 2 * t4 + c;
+            if (gl4 == 0 && h < HPKP) red[warp * HPKP + h] = lcol[nt][c];
+        }
     __syncthreads();
-    if (tid < a.hpk) {
-        float l = red[tid];
+    if (warp == 0 && gl4 == 0) {
 #pragma unroll
-        for (int w = 1; w < kWarps; ++w) l += red[w * HPKP + tid];
-        a.pm[ci.pidx0 + tid] = m_w;  // hw == tid here
-        a.pl[ci.pidx0 + tid] = l;
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int h = nt * 8 + 2 * t4 + c;
+                if (h < a.hpk) {
+                    float l = red[h];
+#pragma unroll
+                    for (int w = 1; w < kWarps; ++w) l += red[w * HPKP + h];
+                    a.pm[ci.pidx0 + h] = mcol[nt][c];
+                    a.pl[ci.pidx0 + h] = l;
+                }
+            }
     }
     // lane (gl4, t4) of warp w holds heads gl4 and gl4 + 8 at channels
     // 32w + 16 blk + 4 t4 + {0, 2} (even tile) and + {1, 3} (odd tile)
@@ -505,7 +565,8 @@ __global__ void __launch_bounds__(kThreads, MmaCfg<HPK>::MIN_CTAS)
     const int g = src.live[gl];
     ci.q = a.q + (int64_t(b) * a.n_q + int64_t(g) * a.hpk) * 128;
     ci.kcol = src.kcol + (int64_t(b) * src.n_live + gl) * 128;
-    ci.score0 = row * a.hpk;
+    ci.score0 = (src.row_base[b] + int64_t(gl) * cap) * a.hpk + r0;
+    ci.score_ld = cap;
     split_mma_body<HPK>(ci, row, a, &maps.kq, &maps.vq, smem);
 }
 

@@ -61,6 +61,7 @@ void *static_scratch() {
 }
 
 constexpr int kMinChunkRows = 256;
+constexpr int kMaxChunkRows = 2048;
 constexpr int64_t kCtaTarget = 152 * 8;
 
 int64_t up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
@@ -85,8 +86,9 @@ extern "C" kvd_status decode_attention_static(const float *q, const kvd_layer *L
         work += l->h_seq_len[b] * int64_t(l->n_live);
         max_len = std::max(max_len, l->h_seq_len[b]);
     }
-    const int32_t chunk =
-        int32_t(up(std::max<int64_t>(kMinChunkRows, cdiv(work, kCtaTarget)), kMinChunkRows));
+    // the same chunking as decode_attention
+    const int32_t chunk = int32_t(std::min<int64_t>(
+        kMaxChunkRows, up(std::max<int64_t>(kMinChunkRows, cdiv(work, kCtaTarget)), kMinChunkRows)));
     const int32_t nc = int32_t(std::max<int64_t>(1, cdiv(max_len, chunk)));
     const int32_t n_grp = std::max(1, l->n_live);
     // Partials of this call: (max, sum, accumulator[hd]) per head per chunk.

@@ -1,0 +1,188 @@
+"""Full-size parity: the benchmark's own workloads (built by the same builders,
+decoded by the same calls and launch configuration as bench.py), checked on
+sampled sequences that the CPU oracle recomputes from the regenerated inputs.
+
+Every oracle input is regenerated from the workload's seeds (never read back
+from the device); the device's stored codes, scales, fields and ring rows are
+compared bit for bit with the oracle's, outputs within 2e-5 of the output RMS,
+imp within 1e-5 relative.
+"""
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from helpers import OUT_TOL, assert_imp_close, out_error
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env():
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    import kv_cache_decode_attention_gb300 as kvd
+    from kv_cache_decode_attention_gb300 import workloads as W
+    from kv_cache_decode_attention_gb300.build import build
+
+    build()
+    return torch, kvd, W
+
+
+def _oracle_seq(wl, b, heads=None):
+    """Oracle cache of sequence b (all KV heads, or the listed ones) from the
+    regenerated rows."""
+    k, v = wl.rows(b)
+    k, v = k.cpu().numpy(), v.cpu().numpy()
+    if heads is None:
+        oc = oracle.OracleSeqCache(wl.mode, wl.n_kv, wl.hd, int(wl.lengths[b]), alive=wl.alive)
+        oc.append_rows(k, v)
+        return oc, None
+    kk = np.ascontiguousarray(k[:, heads])
+    vv = np.ascontiguousarray(v[:, heads])
+    oc = oracle.OracleSeqCache(wl.mode, len(heads), wl.hd, int(wl.lengths[b]))
+    oc.append_rows(kk, vv)
+    return oc, heads
+
+
+def _check_storage(kvd, wl, b, oc, heads):
+    from kv_cache_decode_attention_gb300 import _abi
+
+    L = int(wl.lengths[b])
+    # the oracle cache holds either every KV head (index = head) or just the
+    # listed heads (index = position in the list)
+    pairs = ([(h, h) for h in range(wl.n_kv) if wl.alive[h]] if heads is None
+             else [(h, i) for i, h in enumerate(heads)])
+    for h, oh in pairs:
+        r0, _ = wl.layer.region(b, h)
+        gl = wl.layer.live_heads.index(h)
+        if oc.kq is not None:
+            kq = wl.layer.component(_abi.BUF_KQ)[r0:r0 + L].cpu().numpy()
+            ks = wl.layer.component(_abi.BUF_KS)[r0:r0 + L].cpu().numpy()
+            assert np.array_equal(kq, oc.kq[oh, :L]), (b, h)
+            assert np.array_equal(ks.view(np.uint32), oc.ks[oh, :L].view(np.uint32)), (b, h)
+            col = wl.layer.component(_abi.BUF_KCOL)[b, gl].cpu().numpy()
+            assert np.array_equal(col.view(np.uint32), oc.kcol[oh].view(np.uint32)), (b, h)
+        else:
+            kf = wl.layer.component(_abi.BUF_K)[r0:r0 + L].cpu().numpy()
+            assert np.array_equal(kf.view(np.uint32), oc.k[oh, :L].view(np.uint32)), (b, h)
+        if oc.vq is not None:
+            vq = wl.layer.component(_abi.BUF_VQ)[r0:r0 + L].cpu().numpy()
+            vs = wl.layer.component(_abi.BUF_VS)[r0:r0 + L].cpu().numpy()
+            assert np.array_equal(vq, oc.vq[oh, :L]), (b, h)
+            assert np.array_equal(vs.view(np.uint32), oc.vs[oh, :L].view(np.uint32)), (b, h)
+            col = wl.layer.component(_abi.BUF_VCOL)[b, gl].cpu().numpy()
+            assert np.array_equal(col.view(np.uint32), oc.vcol[oh].view(np.uint32)), (b, h)
+        else:
+            vf = wl.layer.component(_abi.BUF_V)[r0:r0 + L].cpu().numpy()
+            assert np.array_equal(vf.view(np.uint32), oc.v[oh, :L].view(np.uint32)), (b, h)
+
+
+def _decode_and_check(torch, kvd, wl, samples, heads_per_sample=None, with_imp=True, errors=None):
+    q = wl.query(0)
+    imp = torch.zeros(wl.layer.imp_len, device="cuda") if with_imp else None
+    ws = torch.empty(wl.layer.workspace_bytes(wl.n_q, with_imp), dtype=torch.uint8, device="cuda")
+    out = kvd.decode_attention(q, wl.layer, imp=imp, scale=wl.scale, workspace=ws)
+    torch.cuda.synchronize()
+    assert wl.layer.device_error() == 0
+    out = out.cpu().numpy()
+    qh = q.cpu().numpy()
+    got_imp = imp.cpu().numpy() if with_imp else None
+    for b in samples:
+        heads = heads_per_sample
+        oc, hs = _oracle_seq(wl, b, heads)
+        _check_storage(kvd, wl, b, oc, hs)
+        L = int(wl.lengths[b])
+        if hs is None:
+            imp_ref = np.zeros(max(L, 1))
+            ref = oc.decode(qh[b], wl.n_q, np.float32(wl.scale), imp_ref)
+            live = np.array([bool(wl.alive[h // wl.hpk]) for h in range(wl.n_q)])
+            assert np.all(out[b][~live] == 0.0)
+            err = out_error(out[b], ref, live)
+            if errors is not None:
+                errors.append((wl.name, b, int(wl.lengths[b]), err))
+            else:
+                assert err <= OUT_TOL, (b, err)
+            if with_imp:
+                ib = int(wl.layer.imp_base[b])
+                assert_imp_close(got_imp[ib:ib + L], imp_ref[:L])
+        else:
+            qg = np.concatenate([qh[b, g * wl.hpk:(g + 1) * wl.hpk] for g in hs])
+            ref = oc.decode(qg, len(hs) * wl.hpk, np.float32(wl.scale))
+            gq = np.concatenate([out[b, g * wl.hpk:(g + 1) * wl.hpk] for g in hs])
+            err = out_error(gq, ref)
+            assert err <= OUT_TOL, (b, err)
+
+
+def test_q8_gqa_full_size(env):
+    """32 seq x 4096 rows, 32 Q / 8 KV heads, q8_2f built one row at a time."""
+    torch, kvd, W = env
+    wl = W.q8_gqa(extra_cap=64)
+    _decode_and_check(torch, kvd, wl, samples=[0, 17, 31])
+    del wl
+    torch.cuda.empty_cache()
+
+
+def test_long_q8_full_size(env):
+    """4 seq x 131072 rows, 64 Q / 4 KV heads (16 per group): one sampled group."""
+    torch, kvd, W = env
+    wl = W.long_q8(extra_cap=64)
+    _decode_and_check(torch, kvd, wl, samples=[2], heads_per_sample=[1], with_imp=False)
+    del wl
+    torch.cuda.empty_cache()
+
+
+def test_ragged_full_size(env):
+    """256 seq, L ~ U{1..16384}, four layers (f32, q8, q8k, q8v), 2 of 8 KV heads
+    dead per layer: shortest, longest, and sequences around the freeze point."""
+    torch, kvd, W = env
+    layers = W.ragged(extra_cap=16)
+    L = layers[0].lengths
+    order = np.argsort(L)
+    picks = {int(order[0]), int(order[-1]), int(np.argmin(np.abs(L - 64))),
+             int(np.argmin(np.abs(L - 100))), int(order[len(order) // 2])}
+    errors = []
+    for wl in layers:
+        _decode_and_check(torch, kvd, wl, samples=sorted(picks), errors=errors)
+    print("ragged output errors (layer, sequence, rows, max err / rms):", errors)
+    bad = [e for e in errors if e[3] > OUT_TOL]
+    assert not bad, bad
+    del layers
+    torch.cuda.empty_cache()
+
+
+def test_rswa_steady_full_size(env):
+    """16 streams, 10 heads, prefix 32640 rows, ring after 500 steps: ring bytes
+    bit-exact and outputs of two sampled streams against the oracle (which
+    replays the 500 ring writes itself)."""
+    torch, kvd, W = env
+    wl = W.rswa_steady()
+    c = wl.cache
+    assert c.ring_len.tolist() == [128] * c.B and c.ring_pos.tolist() == [500 % 128] * c.B
+    q = wl.query(0)
+    out = kvd.rswa_decode(q, c).cpu().numpy()
+    assert c.device_error() == 0
+    qh = q.cpu().numpy()
+    scale = np.float32(1.0 / math.sqrt(128))
+    ring_k = np.zeros((c.B, c.H, c.W, c.head_dim), np.float32)
+    ring_v = np.zeros_like(ring_k)
+    cursors = [np.zeros(2, np.int32) for _ in range(c.B)]
+    for t in range(wl.steps):
+        k, v = wl.step_rows(t)
+        k, v = k.cpu().numpy(), v.cpu().numpy()
+        for s in range(c.B):
+            oracle.rswa_write(ring_k[s], ring_v[s], k[s], v[s], True, cursors[s])
+    assert np.array_equal(c.ring_k.cpu().numpy(), ring_k)
+    assert np.array_equal(c.ring_v.cpu().numpy(), ring_v)
+    for s in (3, 15):
+        pk, pv = wl.prefill_rows(s)
+        pk, pv = pk.cpu().numpy(), pv.cpu().numpy()
+        ref = oracle.rswa_decode(qh[s], pk, pv, wl.prefill, ring_k[s], ring_v[s], cursors[s][0], scale)
+        err = out_error(out[s].reshape(c.H, c.head_dim), ref)
+        assert err <= OUT_TOL, (s, err)
+    del wl, c
+    torch.cuda.empty_cache()
