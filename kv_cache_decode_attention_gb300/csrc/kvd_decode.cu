@@ -17,8 +17,9 @@ cudaError_t split_layer_f32(int, int, const SplitArgs &, const LayerSrc &, dim3,
 cudaError_t split_layer_q8(int, int, const SplitArgs &, const LayerSrc &, dim3, cudaStream_t);
 cudaError_t split_layer_q8k(int, int, const SplitArgs &, const LayerSrc &, dim3, cudaStream_t);
 cudaError_t split_layer_q8v(int, int, const SplitArgs &, const LayerSrc &, dim3, cudaStream_t);
-cudaError_t split_layer_q8_mma(int, const SplitArgs &, const LayerSrc &, const MmaMaps &, dim3,
-                               cudaStream_t);
+cudaError_t split_layer_q8_warp(int, const WarpArgs &, const LayerSrc &, const MmaMaps &,
+                                cudaStream_t);
+int64_t split_q8_warp_workers(int);
 
 namespace {
 
@@ -46,15 +47,43 @@ int32_t pick_chunk(int64_t work_rows) {
 }
 
 struct DecodeWs {
-    int64_t pm, pl, pacc, ml, scores, total;
+    int64_t pm, pl, pacc, ml, scores, total;  // byte offsets; total < 0 if unknown
+    int64_t slots;                            // tensor-core path partial slots
     int32_t nc_max;
 };
+
+// The q8_2f cache with head_dim 128 runs on the tensor-core kernel when its
+// TMA descriptors exist.
+bool warp_path(const Layer *l) {
+    return l->mode == KVD_Q8 && l->hd == 128 && l->have_tmap_kq && l->have_tmap_vq;
+}
+
+int warp_nt(int hpk) { return hpk > 8 ? 2 : 1; }
+
+// Partial slots the tensor-core kernel may write: every unit's blocks at full
+// capacity plus one per worker (each worker start splits at most one block).
+int64_t warp_slots(const Layer *l, int hpk) {
+    int64_t nb = 0;
+    for (int b = 0; b < l->n_seq; ++b)
+        nb += int64_t(l->n_live) * ceil_div(ceil_div(l->h_cap[b], kWR), kBlockTiles);
+    const int64_t g = split_q8_warp_workers(warp_nt(hpk));
+    return g > 0 ? nb + g : -1;
+}
 
 DecodeWs decode_ws(const Layer *l, int32_t n_q, bool imp) {
     DecodeWs w;
     const int hpk = n_q / l->n_kv;
     w.nc_max = int32_t(std::max<int64_t>(1, ceil_div(l->max_cap, kMinChunk)));
-    const int64_t P = int64_t(l->n_seq) * std::max(1, l->n_live) * w.nc_max * hpk;
+    int64_t P = int64_t(l->n_seq) * std::max(1, l->n_live) * w.nc_max * hpk;
+    w.slots = 0;
+    if (warp_path(l)) {
+        w.slots = warp_slots(l, hpk);
+        if (w.slots < 0) {
+            w.total = -1;
+            return w;
+        }
+        P = std::max(P, w.slots * hpk);
+    }
     int64_t o = 0;
     auto take = [&](int64_t bytes) {
         const int64_t at = o;
@@ -91,6 +120,87 @@ RswaWs rswa_ws(int32_t B, int32_t H, int32_t hd, int64_t ref_cap, int32_t W) {
     w.pacc = take(P * hd * 4);
     w.total = o;
     return w;
+}
+
+// ------------------------------------------------------------- run merge
+
+struct RunMergeArgs {
+    const float *pm, *pl, *pacc;  // run partials [slot][hpk] (+ [128])
+    float *out;                   // [n_seq][n_q][128]
+    float *ml;                    // (max, sum) per (sequence, query head) for imp, or null
+    int32_t n_q, hpk;
+    int64_t T;                    // tiles of all units in the split launch
+    int32_t G;                    // workers of the split launch
+};
+
+// Log-sum-exp merge of the run partials of one (sequence, query head) written
+// by the tensor-core kernel: out[d] = field[d] * sum_r acc_r[d] 2^(m_r - M) /
+// sum_r l_r 2^(m_r - M).  The runs of block j of unit u occupy the slots
+// NB(u) + j + c for the workers c holding its first through its last tile.
+__global__ void __launch_bounds__(128) merge_runs_kernel(RunMergeArgs a, MergeLayerSrc src) {
+    __shared__ int64_t part[2][4];
+    const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
+    const int L = src.seq_len[b];
+    const int grp = src.slot[h / a.hpk];
+    float *o = a.out + (int64_t(b) * a.n_q + h) * 128;
+    float *mlp = a.ml ? a.ml + (int64_t(b) * a.n_q + h) * 2 : nullptr;
+    if (grp < 0 || L <= 0) {
+        o[d] = 0.0f;
+        if (mlp && d == 0) {
+            mlp[0] = -INFINITY;
+            mlp[1] = 0.0f;
+        }
+        return;
+    }
+    // tiles and blocks of the sequences before b
+    int64_t tp = 0, bp = 0;
+    for (int i = d; i < b; i += 128) {
+        const int64_t ti = (int64_t(src.seq_len[i]) + kWR - 1) / kWR;
+        tp += ti;
+        bp += (ti + kBlockTiles - 1) / kBlockTiles;
+    }
+    for (int off = 16; off > 0; off >>= 1) {
+        tp += __shfl_xor_sync(0xffffffffu, tp, off);
+        bp += __shfl_xor_sync(0xffffffffu, bp, off);
+    }
+    if ((d & 31) == 0) {
+        part[0][d >> 5] = tp;
+        part[1][d >> 5] = bp;
+    }
+    __syncthreads();
+    tp = (part[0][0] + part[0][1] + part[0][2] + part[0][3]) * src.n_live;
+    bp = (part[1][0] + part[1][1] + part[1][2] + part[1][3]) * src.n_live;
+    const int64_t Tb = (int64_t(L) + kWR - 1) / kWR, nb = (Tb + kBlockTiles - 1) / kBlockTiles;
+    const int64_t Pu = tp + grp * Tb, NBu = bp + grp * nb;
+    const int hh = h % a.hpk;
+    auto started = [&](int64_t x) {  // workers whose range starts at or before tile x
+        const int64_t c = ((x + 1) * a.G + a.T - 1) / a.T;
+        return c < a.G ? c : int64_t(a.G);
+    };
+    float M = -INFINITY;
+    for (int64_t j = 0; j < nb; ++j) {
+        const int64_t x0 = Pu + j * kBlockTiles, x1 = min(Pu + Tb, x0 + kBlockTiles);
+        const int64_t s1 = NBu + j + started(x1 - 1) - 1;
+        for (int64_t sl = NBu + j + started(x0) - 1; sl <= s1; ++sl) M = fmaxf(M, a.pm[sl * a.hpk + hh]);
+    }
+    float Ls = 0.0f, acc = 0.0f;
+    for (int64_t j = 0; j < nb; ++j) {
+        const int64_t x0 = Pu + j * kBlockTiles, x1 = min(Pu + Tb, x0 + kBlockTiles);
+        const int64_t s1 = NBu + j + started(x1 - 1) - 1;
+        for (int64_t sl = NBu + j + started(x0) - 1; sl <= s1; ++sl) {
+            const int64_t p = sl * a.hpk + hh;
+            const float f = exp2f(a.pm[p] - M);
+            Ls = fmaf(a.pl[p], f, Ls);
+            acc = fmaf(a.pacc[p * 128 + d], f, acc);
+        }
+    }
+    float r = acc / Ls;
+    if (src.vcol) r *= src.vcol[(int64_t(b) * src.n_live + grp) * 128 + d];
+    o[d] = r;
+    if (mlp && d == 0) {
+        mlp[0] = M;
+        mlp[1] = Ls;
+    }
 }
 
 // ------------------------------------------------------------------ imp
@@ -197,7 +307,9 @@ extern "C" kvd_status kvd_decode_workspace_bytes(const kvd_layer *L, int32_t n_q
     const Layer *l = checked_layer(L);
     if (l == nullptr || bytes_out == nullptr) return KVD_EINVAL;
     if (n_q < l->n_kv || n_q % l->n_kv != 0 || n_q / l->n_kv > kMaxHpk) return KVD_EINVAL;
-    *bytes_out = decode_ws(l, n_q, with_imp != 0).total;
+    const int64_t total = decode_ws(l, n_q, with_imp != 0).total;
+    if (total < 0) return KVD_ECUDA;
+    *bytes_out = total;
     return KVD_OK;
 }
 
@@ -211,6 +323,7 @@ extern "C" kvd_status decode_attention(const float *q, const kvd_layer *L, int32
     if (!aligned16(q) || !aligned16(out) || (imp && (reinterpret_cast<uintptr_t>(imp) & 3)))
         return KVD_EINVAL;
     const DecodeWs w = decode_ws(l, n_q, imp != nullptr);
+    if (w.total < 0) return KVD_ECUDA;
     if (workspace == nullptr || workspace_bytes < w.total ||
         (reinterpret_cast<uintptr_t>(workspace) & 255))
         return KVD_EINVAL;
@@ -239,64 +352,90 @@ extern "C" kvd_status decode_attention(const float *q, const kvd_layer *L, int32
     a.scores = imp ? reinterpret_cast<float *>(ws + w.scores) : nullptr;
     a.err = l->d_err;
 
-    if (max_len > 0 && l->n_live > 0) {
-        LayerSrc s;
-        s.kf = static_cast<const float *>(l->buf[KVD_BUF_K]);
-        s.vf = static_cast<const float *>(l->buf[KVD_BUF_V]);
-        s.kq = static_cast<const int8_t *>(l->buf[KVD_BUF_KQ]);
-        s.vq = static_cast<const int8_t *>(l->buf[KVD_BUF_VQ]);
-        s.ks = static_cast<const float *>(l->buf[KVD_BUF_KS]);
-        s.vs = static_cast<const float *>(l->buf[KVD_BUF_VS]);
-        s.kcol = static_cast<const float *>(l->buf[KVD_BUF_KCOL]);
-        s.row_base = l->d_row_base;
-        s.cap = l->d_cap;
-        s.seq_len = l->d_seq_len;
-        s.live = l->d_live;
-        s.n_live = l->n_live;
-        dim3 grid(unsigned(ceil_div(max_len, chunk)), unsigned(l->n_live), unsigned(l->n_seq));
-        const int hb = hpk_bucket(hpk);
-        cudaError_t e;
-        const bool mma = l->mode == KVD_Q8 && l->hd == 128 && l->have_tmap_kq && l->have_tmap_vq;
-        MmaMaps maps;
-        if (mma) {
-            std::memcpy(&maps.kq, l->tmap_kq, sizeof(maps.kq));
-            std::memcpy(&maps.vq, l->tmap_vq, sizeof(maps.vq));
-        }
-        switch (mma ? -1 : l->mode) {
-            case -1: e = split_layer_q8_mma(hb, a, s, maps, grid, st); break;
-            case KVD_F32: e = split_layer_f32(l->hd, hb, a, s, grid, st); break;
-            case KVD_Q8: e = split_layer_q8(l->hd, hb, a, s, grid, st); break;
-            case KVD_Q8K: e = split_layer_q8k(l->hd, hb, a, s, grid, st); break;
-            default: e = split_layer_q8v(l->hd, hb, a, s, grid, st); break;
-        }
-        if (e != cudaSuccess) return KVD_ECUDA;
-    }
-
-    MergeArgs m;
-    m.pm = a.pm;
-    m.pl = a.pl;
-    m.pacc = a.pacc;
-    m.out = out;
-    m.ml = imp ? reinterpret_cast<float *>(ws + w.ml) : nullptr;
-    m.n_q = n_q;
-    m.hpk = hpk;
-    m.n_grp = a.n_grp;
-    m.nc_max = w.nc_max;
-    m.chunk = chunk;
+    LayerSrc s;
+    s.kf = static_cast<const float *>(l->buf[KVD_BUF_K]);
+    s.vf = static_cast<const float *>(l->buf[KVD_BUF_V]);
+    s.kq = static_cast<const int8_t *>(l->buf[KVD_BUF_KQ]);
+    s.vq = static_cast<const int8_t *>(l->buf[KVD_BUF_VQ]);
+    s.ks = static_cast<const float *>(l->buf[KVD_BUF_KS]);
+    s.vs = static_cast<const float *>(l->buf[KVD_BUF_VS]);
+    s.kcol = static_cast<const float *>(l->buf[KVD_BUF_KCOL]);
+    s.row_base = l->d_row_base;
+    s.cap = l->d_cap;
+    s.seq_len = l->d_seq_len;
+    s.live = l->d_live;
+    s.n_live = l->n_live;
     MergeLayerSrc ms;
     ms.seq_len = l->d_seq_len;
     ms.slot = l->d_slot;
     ms.vcol = static_cast<const float *>(l->buf[KVD_BUF_VCOL]);
     ms.n_live = l->n_live;
-    dim3 mgrid(unsigned(n_q), unsigned(l->n_seq));
-    if (l->hd == 128) merge_layer_kernel<128><<<mgrid, 128, 0, st>>>(m, ms);
-    else merge_layer_kernel<64><<<mgrid, 64, 0, st>>>(m, ms);
-    if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
+    float *ml = imp ? reinterpret_cast<float *>(ws + w.ml) : nullptr;
+
+    if (warp_path(l)) {
+        // tensor-core kernel over balanced tile ranges, then the run merge
+        int64_t T = 0;
+        for (int b = 0; b < l->n_seq; ++b) T += int64_t(l->n_live) * ceil_div(l->h_seq_len[b], kWR);
+        const int nt = warp_nt(hpk);
+        const int64_t workers = split_q8_warp_workers(nt);
+        if (workers <= 0) return KVD_ECUDA;
+        WarpArgs wa;
+        wa.a = a;
+        wa.T = T;
+        wa.G = int32_t(std::min(T, workers));
+        wa.n_seq = l->n_seq;
+        if (T > 0) {
+            MmaMaps maps;
+            std::memcpy(&maps.kq, l->tmap_kq, sizeof(maps.kq));
+            std::memcpy(&maps.vq, l->tmap_vq, sizeof(maps.vq));
+            if (split_layer_q8_warp(nt, wa, s, maps, st) != cudaSuccess) return KVD_ECUDA;
+        }
+        RunMergeArgs rm;
+        rm.pm = a.pm;
+        rm.pl = a.pl;
+        rm.pacc = a.pacc;
+        rm.out = out;
+        rm.ml = ml;
+        rm.n_q = n_q;
+        rm.hpk = hpk;
+        rm.T = T;
+        rm.G = wa.G;
+        merge_runs_kernel<<<dim3(unsigned(n_q), unsigned(l->n_seq)), 128, 0, st>>>(rm, ms);
+        if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
+    } else {
+        if (max_len > 0 && l->n_live > 0) {
+            dim3 grid(unsigned(ceil_div(max_len, chunk)), unsigned(l->n_live), unsigned(l->n_seq));
+            const int hb = hpk_bucket(hpk);
+            cudaError_t e;
+            switch (l->mode) {
+                case KVD_F32: e = split_layer_f32(l->hd, hb, a, s, grid, st); break;
+                case KVD_Q8: e = split_layer_q8(l->hd, hb, a, s, grid, st); break;
+                case KVD_Q8K: e = split_layer_q8k(l->hd, hb, a, s, grid, st); break;
+                default: e = split_layer_q8v(l->hd, hb, a, s, grid, st); break;
+            }
+            if (e != cudaSuccess) return KVD_ECUDA;
+        }
+        MergeArgs m;
+        m.pm = a.pm;
+        m.pl = a.pl;
+        m.pacc = a.pacc;
+        m.out = out;
+        m.ml = ml;
+        m.n_q = n_q;
+        m.hpk = hpk;
+        m.n_grp = a.n_grp;
+        m.nc_max = w.nc_max;
+        m.chunk = chunk;
+        dim3 mgrid(unsigned(n_q), unsigned(l->n_seq));
+        if (l->hd == 128) merge_layer_kernel<128><<<mgrid, 128, 0, st>>>(m, ms);
+        else merge_layer_kernel<64><<<mgrid, 64, 0, st>>>(m, ms);
+        if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
+    }
 
     if (imp && max_len > 0 && l->n_live > 0) {
         ImpArgs ia;
         ia.scores = a.scores;
-        ia.ml = m.ml;
+        ia.ml = ml;
         ia.imp = imp;
         ia.row_base = l->d_row_base;
         ia.cap = l->d_cap;

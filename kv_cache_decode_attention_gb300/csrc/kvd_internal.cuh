@@ -57,7 +57,7 @@ struct Layer {
     int32_t *d_seq_len, *d_frozen, *d_live, *d_slot;
     uint32_t *d_err;
     // TMA tensor maps (CUtensorMap, 128 bytes each) of the int8 K and V code
-    // buffers, 2-D [rows][head_dim] with 128-byte swizzled [128 x 128] boxes;
+    // buffers, 2-D [rows][head_dim] with 128-byte swizzled [32 x 128] boxes;
     // have_tmap = 0 when they are not built (head_dim 64 or no int8 buffer).
     int32_t have_tmap_kq, have_tmap_vq;
     unsigned char tmap_kq[128], tmap_vq[128];

@@ -105,7 +105,7 @@ int64_t host_block_bytes(int32_t n_seq, int32_t n_kv) {
 }
 
 // TMA descriptor of an int8 code buffer: 2-D [rows][hd] bytes, row pitch hd,
-// boxes of 128 rows x 128 bytes landing in shared memory with the 128-byte
+// boxes of 32 rows x 128 bytes landing in shared memory with the 128-byte
 // swizzle (16-byte chunk c of row r stored at chunk c ^ (r % 8)); rows past
 // the end read as zeros.  Returns false if the driver entry point is missing
 // or refuses the descriptor (the caller then uses the plain bulk-copy kernel).
@@ -124,7 +124,7 @@ bool encode_code_map(void *base, int64_t rows, int hd, unsigned char *out) {
     alignas(64) CUtensorMap m;
     const cuuint64_t dims[2] = {cuuint64_t(hd), cuuint64_t(rows)};
     const cuuint64_t strides[1] = {cuuint64_t(hd)};
-    const cuuint32_t box[2] = {128u, 128u};
+    const cuuint32_t box[2] = {128u, 32u};
     const cuuint32_t estr[2] = {1u, 1u};
     if (encode(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

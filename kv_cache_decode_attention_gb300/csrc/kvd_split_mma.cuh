@@ -1,37 +1,51 @@
 // kvd_split_mma.cuh -- split-KV decode over the q8_2f cache (int8 K and V,
 // head_dim 128) on the tensor cores (warp-level mma.sync, f16 in, f32 out).
 //
-// Why: with int8 rows the CUDA-core kernel spends ~84 instructions per cached
-// row (int8->f32 conversions, hpk x 128 FMAs per pass, warp reductions) and is
-// issue-bound far below the HBM roofline at GQA fan-out 4..16.  Here both
-// contractions run as f16 MMAs with f32 accumulation; the CUDA cores only turn
-// each int8 code into an exact f16 once (a byte splice and one HSUB2 per pair),
-// shared by every query head of the group.  (The legacy int8 mma.sync path is
-// far slower than f16 on this GPU, so the codes go through f16.)
+// Why tensor cores: with int8 rows a CUDA-core kernel spends ~84 instructions
+// per cached row (int8->f32 conversions, hpk x 128 FMAs per pass, warp
+// reductions) and is issue-bound far below the HBM roofline at GQA fan-out
+// 4..16.  Here both contractions run as f16 MMAs with f32 accumulation; the
+// CUDA cores only turn each int8 code into an exact f16 once (a byte splice
+// and one HSUB2 per pair), shared by every query head of the group.  (The
+// legacy int8 mma.sync path is far slower than f16 on this GPU, so the codes
+// go through f16.)
 //
-// Per tile of 128 cached rows:
-//   scores  warps split the rows (32 each, two m16 blocks):
-//           S[row][h] = 2^-E_h * sum_g ks[row][g] * K_g . (t1_h + t2_h)_g
+// Work split: a persistent grid of one-warp CTAs.  The cached rows of all
+// (sequence, live group) units are cut into tiles of 32 rows and laid end to
+// end; worker c owns the contiguous tile range [c T / G, (c+1) T / G), so
+// every warp streams the same number of tiles whatever the length mix.  A
+// worker keeps one online-softmax state per run -- a stretch of its range
+// inside one unit and one block of kBlockTiles tiles -- and writes the run's
+// (max, sum, accumulator) per head as one partial; a second kernel merges a
+// unit's partials by log-sum-exp.  Partial slots need no table: the run of
+// worker c starting in block j of unit u sits at slot NB(u) + j + c, where
+// NB(u) counts the blocks of the units before u.  (Runs start at block starts
+// and worker starts; moving to the next run start adds one to j or to c, so
+// slots are distinct, and the merge finds a block's runs as the slot range
+// from the worker holding its first tile to the one holding its last.)
+//
+// Each warp owns a ring of kStages stages (K codes, V codes, K scales, V
+// scales of one tile) filled by TMA: 2-D tensor copies with the 128-byte
+// swizzle for the codes (conflict-free ldmatrix), 1-D bulk copies for the
+// scales, one mbarrier per stage.  Per tile:
+//   scores  S[row][h] = 2^-E_h sum_g ks[row][g] K_g . (t1_h + t2_h)_g with
+//           M = the tile's rows (two m16 blocks), N = heads, K = channels.
 //           K codes are exact in f16; q * kcol * scale * log2(e) * 2^E_h is
-//           split into two f16 terms t1 + t2 (22 significant bits, E_h puts the
-//           head's largest term near 2^14); m16n8k16 MMAs accumulate each
-//           32-channel group in f32 so its scale ks[row][g] applies after.  The
-//           channel order inside a k16 step is permuted identically in A and B
-//           so a lane's four consecutive codes feed its fragment directly.
-//           The per-warp maximum of each head is reduced in registers.
-//   softmax online over tiles in the log2 domain (running max per head; every
-//           thread derives the same maxima from the per-warp values).
+//           split into two f16 terms t1 + t2 (22 significant bits, E_h puts
+//           the head's largest term near 2^14) whose MMAs chain into one f32
+//           accumulator per 32-channel group, so ks[row][g] applies after.
+//           Inside a k16 step the channel order is permuted identically in A
+//           and B so a lane's four consecutive codes feed its fragment.
+//   softmax online per warp in the log2 domain (running max per head).
 //   weights w = 2^(S - max) * vs[row] * 2^Ew (Ew puts the tile's largest V
-//           scale near 2^14) split into two f16 terms, written to shared
-//           memory as the A operand [term][k16 step][head][position].
-//   values  warps split the 128 channels (32 each); V codes become the f16 B
-//           operand straight from ldmatrix.trans; m16n8k16 MMAs with M = the
-//           group's heads accumulate into f32 registers across all tiles (the
-//           accumulator is rescaled by the softmax correction and the change
-//           of Ew between tiles).
-// K and V code tiles arrive by TMA tensor copies with the 128-byte swizzle
-// (conflict-free ldmatrix); scales by 1-D bulk copies; a ring of kMmaSlots
-// slots alternates K and V segments.
+//           scale near 2^14), split into two f16 terms and written
+//           transposed ([row][head]) to a 1 KB per-warp buffer.
+//   values  out^T = V^T P^T: M = channels (eight m16 blocks, even channels of
+//           a 16-channel chunk in rows 0..7, odd ones in rows 8..15, straight
+//           from ldmatrix.trans of the V tile), N = heads, K = the tile's
+//           rows; the two weight terms chain into fresh f32 accumulators that
+//           are folded into the running sum with one IEEE FMA per element
+//           (rescaled by the softmax correction and the change of Ew).
 #pragma once
 
 #include <cuda.h>
@@ -41,25 +55,25 @@
 
 namespace kvd {
 
-constexpr int kMmaTR = 128;        // rows per tile
-constexpr int kMmaSlots = 3;       // ring slots (K, V alternate)
-constexpr int kMmaTile = 16384;    // bytes of one 128 x 128 code tile
-constexpr int kMmaKsOff = 16384;   // K scales within a K segment
-constexpr int kMmaVsOff = 18432;   // V scales within a K segment
-constexpr int kMmaSlot = 19456;    // bytes per slot (multiple of 1024)
-constexpr int kMmaAw = 2 * 8 * 16 * 32;  // weights [term][k16 step][16 heads][16 f16]
+constexpr int kWR = 32;             // rows per tile
+constexpr int kBlockTiles = 128;    // tiles per partial block (4096 rows)
+constexpr int kStages = 2;          // ring stages per warp
+constexpr int kStK = 0;             // K codes [32][128], 128-byte swizzled
+constexpr int kStV = 4096;          // V codes [32][128], 128-byte swizzled
+constexpr int kStKs = 8192;         // K scales [32][4] f32
+constexpr int kStVs = 8704;         // V scales [32] f32
+constexpr int kStageBytes = 9216;   // multiple of 1024 (swizzle atom)
+constexpr uint32_t kStageTx = 4096 + 4096 + 512 + 128;
 
-template <int HPK>
-struct MmaCfg {
-    static constexpr int HPKP = HPK < 4 ? 4 : HPK;          // heads padded for the layouts
-    static constexpr int NT = HPKP / 8 > 0 ? HPKP / 8 : 1;  // score n8 tiles
-    static constexpr int S_OFF = kMmaSlots * kMmaSlot;       // q staging [HPKP][128] f32
-    static constexpr int AW_OFF = S_OFF + HPKP * 128 * 4;
-    static constexpr int MISC_OFF = AW_OFF + kMmaAw;
-    // misc: bars[kMmaSlots], red[kWarps][HPKP], vred[kWarps]
-    static constexpr int SMEM = MISC_OFF + kMmaSlots * 8 + kWarps * HPKP * 4 + kWarps * 4;
+// NT: score/value n8 tiles of heads (1 for hpk <= 8, 2 for hpk <= 16).
+template <int NT>
+struct WarpCfg {
+    static constexpr int P_OFF = kStages * kStageBytes;  // P^T [term][NT][32 rows][8 heads] f16
+    static constexpr int Q_OFF = P_OFF + 2 * NT * 512;   // q fragments when NT == 2
+    static constexpr int Q_BYTES = NT == 1 ? 0 : 4 * 2 * NT * 2 * 32 * 8;
+    static constexpr int BAR_OFF = Q_OFF + Q_BYTES;
+    static constexpr int SMEM = BAR_OFF + kStages * 8;
     static constexpr int SMEM_ALLOC = SMEM + 1024;  // room to align the base to 1024
-    static constexpr int MIN_CTAS = HPK >= 16 ? 2 : 3;
 };
 
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
@@ -69,6 +83,12 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
         : "memory");
+}
+
+// Order this thread's earlier generic-proxy accesses of shared memory before
+// later async-proxy (TMA) writes to it.
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
@@ -81,6 +101,10 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                  : "r"(addr));
+}
+
+__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
 // D += A(16x16 f16, row) * B(16x8 f16, col), f32 accumulate.
@@ -109,476 +133,537 @@ __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-// exponent e with x in [2^(e-1), 2^e), x > 0
-__device__ __forceinline__ int exponent_of(float x) {
-    int e;
-    frexpf(x, &e);
-    return e;
+// 2^x by the hardware approximation (relative error a few ulp; results below
+// the smallest normal flush to zero, which no weight here needs).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
+
+// e with x in [2^(e-1), 2^e) for a positive normal x.
+__device__ __forceinline__ int exponent_of(float x) {
+    return int((__float_as_uint(x) >> 23) & 0xffu) - 126;
+}
+
+// 2^e for -126 <= e <= 127.
+__device__ __forceinline__ float pow2i(int e) { return __uint_as_float(uint32_t(e + 127) << 23); }
 
 struct MmaMaps {
     CUtensorMap kq, vq;
 };
 
-template <int HPK>
-__device__ __forceinline__ void mma_issue(const ChunkInfo &ci, const CUtensorMap *kmap,
-                                          const CUtensorMap *vmap, int64_t row_base, char *sm,
-                                          uint64_t *bar, int j) {
-    const int slot = j % kMmaSlots;
-    const int t = j >> 1;
-    const int row0 = t * kMmaTR;
-    const int nt = min(kMmaTR, ci.n - row0);
-    const int rows = (nt + kRowAlign - 1) / kRowAlign * kRowAlign;
-    char *dst = sm + slot * kMmaSlot;
-    if ((j & 1) == 0) {
-        mbar_arrive_expect_tx(&bar[slot], uint32_t(kMmaTile + rows * 16 + rows * 4));
-        tma_load_2d(dst, kmap, 0, int(row_base + row0), &bar[slot]);
-        bulk_g2s(dst + kMmaKsOff, ci.ks + int64_t(row0) * 16, uint32_t(rows) * 16, &bar[slot]);
-        bulk_g2s(dst + kMmaVsOff, ci.vs + int64_t(row0) * 4, uint32_t(rows) * 4, &bar[slot]);
-    } else {
-        mbar_arrive_expect_tx(&bar[slot], uint32_t(kMmaTile));
-        tma_load_2d(dst, vmap, 0, int(row_base + row0), &bar[slot]);
+struct WarpArgs {
+    SplitArgs a;
+    int64_t T;      // tiles of all units
+    int32_t G;      // workers (grid size), 1 <= G <= T
+    int32_t n_seq;
+};
+
+// Number of workers whose range starts at or before global tile x.
+__device__ __forceinline__ int64_t workers_started(int64_t x, int64_t T, int64_t G) {
+    const int64_t c = ((x + 1) * G + T - 1) / T;
+    return c < G ? c : G;
+}
+
+// Position of one tile in the unit order (sequence-major, live group, tile).
+struct TileCursor {
+    int b, gl, tl;   // sequence, live group, tile within the unit
+    int Tb, Lb;      // tiles and rows of sequence b
+    int64_t cap;     // region rows of sequence b
+    int64_t rbase;   // storage row of the unit's row 0
+    int64_t bq;      // partial blocks of the units of sequences before b
+};
+
+__device__ __forceinline__ int blocks_of(int tiles) { return (tiles + kBlockTiles - 1) / kBlockTiles; }
+
+// Load sequence b's shape into the cursor; false (and an error bit) if its
+// length exceeds its capacity.
+__device__ __forceinline__ bool cursor_seq(TileCursor &c, const LayerSrc &src, uint32_t *err) {
+    c.cap = src.cap[c.b];
+    c.rbase = src.row_base[c.b];
+    if (int64_t(c.Lb) > c.cap) {
+        set_error(err, kErrBounds);
+        return false;
     }
+    return true;
 }
 
-// Byte offset of weight (term, position p, head h) in the A operand area: 16 x
-// 16 f16 blocks per (term, k16 step), the two 8-position halves of a head's
-// row swapped on heads 4..7 and 12..15 so ldmatrix rows hit distinct banks.
-__device__ __forceinline__ int aw_offset(int term, int p, int h) {
-    const int ks = p >> 4, k = p & 15;
-    return ((term * 8 + ks) * 16 + h) * 32 + (((k >> 3) ^ ((h >> 2) & 1)) << 4) + (k & 7) * 2;
+// Advance to the next tile in the global order; false past the last sequence.
+__device__ __forceinline__ bool cursor_next(TileCursor &c, const LayerSrc &src, int n_seq,
+                                            uint32_t *err) {
+    if (++c.tl < c.Tb) return true;
+    c.tl = 0;
+    if (++c.gl < src.n_live) {
+        c.rbase += c.cap;
+        return true;
+    }
+    c.gl = 0;
+    c.bq += int64_t(src.n_live) * blocks_of(c.Tb);
+    for (;;) {
+        if (++c.b >= n_seq) return false;
+        c.Lb = src.seq_len[c.b];
+        c.Tb = (c.Lb + kWR - 1) / kWR;
+        if (c.Tb > 0) break;
+    }
+    return cursor_seq(c, src, err);
 }
 
-// One CTA: one chunk of ci.n rows starting at storage row `row_base` of one
-// (sequence, live group).  Writes the partial (max, sum, acc) of each head.
-template <int HPK>
-__device__ void split_mma_body(const ChunkInfo &ci, int64_t row_base, const SplitArgs &a,
-                               const CUtensorMap *kmap, const CUtensorMap *vmap, char *smem_raw) {
-    using C = MmaCfg<HPK>;
-    constexpr int HPKP = C::HPKP, NT = C::NT;
-    // align to 1024 by offsetting the shared array itself, so every derived
-    // pointer stays a known shared-memory pointer (plain LDS/STS)
-    char *sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+// Find global tile x: a warp-wide scan of the sequences' tile counts.
+__device__ inline bool cursor_locate(TileCursor &c, int64_t x, const LayerSrc &src, int n_seq, int lane,
+                              uint32_t *err) {
+    int64_t tp = 0, bq = 0;  // tiles and blocks of the sequences before `base`
+    for (int base = 0; base < n_seq; base += 32) {
+        const int i = base + lane;
+        const int L = i < n_seq ? src.seq_len[i] : 0;
+        const int Tb = (L + kWR - 1) / kWR;
+        int64_t ut = int64_t(src.n_live) * Tb, ub = int64_t(src.n_live) * blocks_of(Tb);
+        // inclusive prefix over the lanes
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int64_t t = __shfl_up_sync(0xffffffffu, ut, off);
+            const int64_t bb = __shfl_up_sync(0xffffffffu, ub, off);
+            if (lane >= off) ut += t, ub += bb;
+        }
+        const int64_t tot_t = __shfl_sync(0xffffffffu, ut, 31);
+        const int64_t tot_b = __shfl_sync(0xffffffffu, ub, 31);
+        if (tp + tot_t > x) {
+            // first lane whose inclusive prefix passes x
+            const unsigned m = __ballot_sync(0xffffffffu, tp + ut > x);
+            const int src_lane = __ffs(m) - 1;
+            const int64_t ex_t = __shfl_sync(0xffffffffu, ut, src_lane) -
+                                 int64_t(src.n_live) * __shfl_sync(0xffffffffu, Tb, src_lane);
+            const int64_t ex_b = __shfl_sync(0xffffffffu, ub, src_lane) -
+                                 int64_t(src.n_live) * blocks_of(__shfl_sync(0xffffffffu, Tb, src_lane));
+            c.b = base + src_lane;
+            c.Lb = __shfl_sync(0xffffffffu, L, src_lane);
+            c.Tb = __shfl_sync(0xffffffffu, Tb, src_lane);
+            c.bq = bq + ex_b;
+            const int64_t r = x - (tp + ex_t);
+            c.gl = int(r / c.Tb);
+            c.tl = int(r % c.Tb);
+            if (!cursor_seq(c, src, err)) return false;
+            c.rbase += int64_t(c.gl) * c.cap;
+            return true;
+        }
+        tp += tot_t;
+        bq += tot_b;
+    }
+    set_error(err, kErrBounds);
+    return false;
+}
+
+__device__ __forceinline__ void issue_tile(const TileCursor &c, const CUtensorMap *kmap,
+                                           const CUtensorMap *vmap, const LayerSrc &src, char *stage,
+                                           uint64_t *bar) {
+    const int64_t row = c.rbase + int64_t(c.tl) * kWR;
+    mbar_arrive_expect_tx(bar, kStageTx);
+    tma_load_2d(stage + kStK, kmap, 0, int(row), bar);
+    tma_load_2d(stage + kStV, vmap, 0, int(row), bar);
+    bulk_g2s(stage + kStKs, src.ks + row * 4, 512, bar);
+    bulk_g2s(stage + kStVs, src.vs + row, 128, bar);
+}
+
+template <int NT>
+__global__ void __launch_bounds__(32) split_warp_kernel(WarpArgs wa, LayerSrc src,
+                                                        const __grid_constant__ MmaMaps maps) {
+    using C = WarpCfg<NT>;
+    extern __shared__ __align__(128) char smem_raw[];
+    const SplitArgs &a = wa.a;
+    const int lane = threadIdx.x;
     const int gl4 = lane >> 2, t4 = lane & 3;
     const int mi = lane >> 3, rr = lane & 7;  // ldmatrix: matrix index, row in matrix
-    char *Aw = sm + C::AW_OFF;
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + C::MISC_OFF);
-    float *red = reinterpret_cast<float *>(bar + kMmaSlots);
-    float *vred = red + kWarps * HPKP;
+    // align to 1024 by offsetting the shared array itself, so every derived
+    // pointer stays a known shared-memory pointer
+    char *sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + C::BAR_OFF);
+    const int64_t T = wa.T, G = wa.G, c = blockIdx.x;
+    const int64_t x_begin = c * T / G, x_end = (c + 1) * T / G;
+    if (x_begin >= x_end) return;
 
-    const int n = ci.n;
-    const int ntiles = (n + kMmaTR - 1) / kMmaTR;
-    const int nseg = 2 * ntiles;
+    TileCursor cur;
+    if (!cursor_locate(cur, x_begin, src, wa.n_seq, lane, a.err)) return;
+    TileCursor prod = cur;
 
-    if (tid == 0) {
-        for (int s = 0; s < kMmaSlots; ++s) mbar_init(&bar[s], 1);
+    if (lane == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(&bar[s], 1);
         fence_mbar_init();
     }
-    __syncthreads();
-    if (tid == 0)
-        for (int j = 0; j < min(kMmaSlots, nseg); ++j) mma_issue<HPK>(ci, kmap, vmap, row_base, sm, bar, j);
-
-    // ---- query terms: q * kcol * scale * log2e * 2^E_h = t1 + t2 (f16),
-    //      staged through the staging area
-    float *qf = reinterpret_cast<float *>(sm + C::S_OFF);
-    for (int i = tid; i < HPKP * 128; i += kThreads) {
-        const int h = i >> 7, d = i & 127;
-        qf[i] = h < a.hpk ? ci.q[h * 128 + d] * ci.kcol[d] * a.qscale : 0.0f;
-    }
-    __syncthreads();
-    if (tid < HPKP) {
-        float mx = 0.0f;
-        for (int d = 0; d < 128; ++d) mx = fmaxf(mx, fabsf(qf[tid * 128 + d]));
-        red[tid] = mx > 0.0f ? float(14 - exponent_of(mx)) : 0.0f;
-    }
-    __syncthreads();
-    uint32_t bq[4][2][NT][2][2];  // [group][k16 step][n-tile][term][reg]
-    float qexp[NT][2];            // 2^-E of the heads in this lane's score columns
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            const int h = nt * 8 + 2 * t4 + c;
-            qexp[nt][c] = h < HPKP ? exp2f(-red[h]) : 0.0f;
+    __syncwarp();
+    int64_t issued = 0;  // tiles issued so far (tile i goes to stage i % kStages)
+    bool prod_ok = true;
+    {
+        const int64_t first = x_end - x_begin < kStages ? x_end - x_begin : int64_t(kStages);
+        for (int64_t i = 0; i < first && prod_ok; ++i) {
+            if (lane == 0) issue_tile(prod, &maps.kq, &maps.vq, src, sm + (i % kStages) * kStageBytes,
+                                      &bar[i % kStages]);
+            ++issued;
+            if (x_begin + issued < x_end) prod_ok = cursor_next(prod, src, wa.n_seq, a.err);
         }
-        const int hb = nt * 8 + gl4;  // the B column this lane feeds
-        const float sc = hb < HPKP ? exp2f(red[hb]) : 0.0f;
-#pragma unroll
-        for (int g = 0; g < 4; ++g)
-#pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {
-                const int c0 = 32 * g + 16 * ks + 4 * t4;
-                float x[4], r[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    x[i] = hb < HPKP ? qf[hb * 128 + c0 + i] * sc : 0.0f;
-                    r[i] = x[i] - __half2float(__float2half_rn(x[i]));
-                }
-                bq[g][ks][nt][0][0] = pack_half2(x[0], x[1]);
-                bq[g][ks][nt][0][1] = pack_half2(x[2], x[3]);
-                bq[g][ks][nt][1][0] = pack_half2(r[0], r[1]);
-                bq[g][ks][nt][1][1] = pack_half2(r[2], r[3]);
-            }
     }
-    __syncthreads();  // staging read before anything reuses it
 
-    // Lane-constant shared-memory offsets.  K tile (ldmatrix, scores): row
-    // warp*32 + mb*16 + rr + 8*(mi&1), 16-byte chunk 2g + (mi>>1), swizzled by
-    // the row's low 3 bits (= rr).  V tile (ldmatrix.trans): position 16ks +
-    // 8*(mi&1) + rr, chunk 2*warp + (mi>>1).  Weights: head row rr + 8*(mi&1),
-    // half mi>>1, swapped on heads 4..7 / 12..15.
-    const uint32_t k_lane = uint32_t(warp * 32 + rr + 8 * (mi & 1)) * 128;
+    // Lane-constant shared-memory offsets.  K tile (ldmatrix): row
+    // mb*16 + rr + 8*(mi&1), 16-byte chunk 2g + (mi>>1), swizzled by the row's
+    // low 3 bits (= rr).  V tile (ldmatrix.trans): row 8*mi + rr, chunk cc.
+    const uint32_t k_lane = uint32_t(rr + 8 * (mi & 1)) * 128;
     uint32_t k_chunk[4];
 #pragma unroll
     for (int g = 0; g < 4; ++g) k_chunk[g] = uint32_t(((2 * g + (mi >> 1)) ^ rr) << 4);
-    const uint32_t v_lane = uint32_t(8 * (mi & 1) + rr) * 128 + uint32_t(((2 * warp + (mi >> 1)) ^ rr) << 4);
-    const int am = rr + 8 * (mi & 1);
-    const uint32_t aw_lane = uint32_t(am * 32 + (((mi >> 1) ^ ((am >> 2) & 1)) << 4));
-    const uint32_t aw_base = smem_addr(Aw) + aw_lane;
-    // where this lane writes the weight terms of its score values: head h =
-    // nt*8 + 2*t4 + c, position warp*32 + mb*16 + gl4 + 8*rw (k16 step warp*2 + mb)
-    int wofs[2][NT][2][2];
-#pragma unroll
-    for (int mb = 0; mb < 2; ++mb)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int c = 0; c < 2; ++c)
-#pragma unroll
-                for (int rw = 0; rw < 2; ++rw) {
-                    const int h = nt * 8 + 2 * t4 + c;
-                    wofs[mb][nt][c][rw] =
-                        ((warp * 2 + mb) * 16 + h) * 32 + ((rw ^ ((h >> 2) & 1)) << 4) + gl4 * 2;
-                }
+    const uint32_t v_lane = uint32_t(8 * mi + rr) * 128;
+    const uint32_t p_base = smem_addr(sm + C::P_OFF);
+    const uint32_t p_ld = p_base + uint32_t(8 * mi + rr) * 16;  // ldmatrix.trans rows of P^T
+    const uint32_t p_st = p_base + uint32_t(t4) * 4;              // + row * 16
 
-    // running state: maxima and sums of this lane's score-column heads
-    // (nt*8 + 2*t4 + c) and maxima of its P.V heads (gl4, gl4 + 8); every lane
-    // derives identical maxima from the per-warp values in red
-    float mcol[NT][2], lcol[NT][2];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) mcol[nt][0] = mcol[nt][1] = -INFINITY, lcol[nt][0] = lcol[nt][1] = 0.0f;
-    float m_a = -INFINITY, m_b = -INFINITY;
-    int ew_prev = 0;
-    float acc[4][4];  // [n-tile: block 0 even, 0 odd, 1 even, 1 odd][frag]
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) acc[i][c] = 0.0f;
+    uint32_t bq[NT == 1 ? 4 : 1][2][NT][2][2];  // q fragments [group][k16][n-tile][term][reg]
+    uint2 *qs = reinterpret_cast<uint2 *>(sm + C::Q_OFF);  // same, in shared memory (NT == 2)
+    float qexp[NT][2];
+    int q_b = -1, q_gl = -1;
+
+    int64_t x = x_begin, i = 0;  // global tile, worker-local tile count
     bool ok = true;
-
-    for (int t = 0; t < ntiles; ++t) {
-        const int row0 = t * kMmaTR;
-        const int nt_rows = min(kMmaTR, n - row0);
-        int j = 2 * t;
-        int slot = j % kMmaSlots;
-        if (__syncthreads_or(!mbar_wait_bounded(&bar[slot], (j / kMmaSlots) & 1))) {
-            ok = false;
-            break;
-        }
-        // the previous tile's V slot is drained (every thread passed the barrier)
-        if (tid == 0 && t > 0 && j - 1 + kMmaSlots < nseg)
-            mma_issue<HPK>(ci, kmap, vmap, row_base, sm, bar, j - 1 + kMmaSlots);
-        const char *kseg = sm + slot * kMmaSlot;
-        const uint32_t kaddr = smem_addr(kseg) + k_lane;
-        const float *ks_s = reinterpret_cast<const float *>(kseg + kMmaKsOff);
-        const float *vs_s = reinterpret_cast<const float *>(kseg + kMmaVsOff);
-        // ------------------------------------------------ scores (f16 MMA)
-        float sreg[2][NT][2][2];  // [m block][n-tile][column][row gl4 / gl4 + 8]
+    while (x < x_end) {
+        // ------------------------------------------------ run set-up
+        int64_t run_len = x_end - x;
+        if (run_len > cur.Tb - cur.tl) run_len = cur.Tb - cur.tl;
+        if (run_len > kBlockTiles - cur.tl % kBlockTiles) run_len = kBlockTiles - cur.tl % kBlockTiles;
+        const int64_t slot = cur.bq + int64_t(cur.gl) * blocks_of(cur.Tb) + cur.tl / kBlockTiles + c;
+        if (cur.b != q_b || cur.gl != q_gl) {
+            // q * kcol * scale * log2e * 2^E_h = t1 + t2 (f16) for the heads
+            // this lane feeds as B columns (nt*8 + gl4), channels
+            // 16*chunk + 4*t4 .. + 3 of every chunk
+            q_b = cur.b;
+            q_gl = cur.gl;
+            const int g = src.live[cur.gl];
+            const float *qg = a.q + (int64_t(cur.b) * a.n_q + int64_t(g) * a.hpk) * 128;
+            const float *kc = src.kcol + (int64_t(cur.b) * src.n_live + cur.gl) * 128;
 #pragma unroll
-        for (int mb = 0; mb < 2; ++mb) {
-            const int r0 = warp * 32 + mb * 16;
-            float sacc[NT][4];
+            for (int nt = 0; nt < NT; ++nt) {
+                const int hb = nt * 8 + gl4;
+                float xq[8][4];
+                float mx = 0.0f;
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
+                for (int ch = 0; ch < 8; ++ch) {
+                    const int d = 16 * ch + 4 * t4;
+                    float4 qv = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    if (hb < a.hpk) qv = *reinterpret_cast<const float4 *>(qg + hb * 128 + d);
+                    const float4 kv = *reinterpret_cast<const float4 *>(kc + d);
+                    xq[ch][0] = qv.x * kv.x * a.qscale;
+                    xq[ch][1] = qv.y * kv.y * a.qscale;
+                    xq[ch][2] = qv.z * kv.z * a.qscale;
+                    xq[ch][3] = qv.w * kv.w * a.qscale;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) sacc[nt][i] = 0.0f;
-            const float4 ksA = *reinterpret_cast<const float4 *>(&ks_s[(r0 + gl4) * 4]);
-            const float4 ksB = *reinterpret_cast<const float4 *>(&ks_s[(r0 + gl4 + 8) * 4]);
-            const float kA[4] = {ksA.x, ksA.y, ksA.z, ksA.w};
-            const float kB[4] = {ksB.x, ksB.y, ksB.z, ksB.w};
+                    for (int j = 0; j < 4; ++j) mx = fmaxf(mx, fabsf(xq[ch][j]));
+                }
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                const int E = mx > 0.0f ? min(14 - exponent_of(mx), 100) : 0;
+                const float sc = pow2i(E);
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                uint32_t w[4];
-                ldsm_x4(kaddr + mb * 2048 + k_chunk[g], w);
-                // row gl4 / gl4 + 8, channels 4t..4t+3 of k16 step 0 and 1
-                const uint32_t u0 = w[0] ^ 0x80808080u, u1 = w[1] ^ 0x80808080u;
-                const uint32_t u2 = w[2] ^ 0x80808080u, u3 = w[3] ^ 0x80808080u;
-                const uint32_t a00 = codes_f16x2<0x4140>(u0), a02 = codes_f16x2<0x4342>(u0);
-                const uint32_t a01 = codes_f16x2<0x4140>(u1), a03 = codes_f16x2<0x4342>(u1);
-                const uint32_t a10 = codes_f16x2<0x4140>(u2), a12 = codes_f16x2<0x4342>(u2);
-                const uint32_t a11 = codes_f16x2<0x4140>(u3), a13 = codes_f16x2<0x4342>(u3);
+                for (int ch = 0; ch < 8; ++ch) {
+                    float hi[4], lo[4];
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    float dg[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-                    for (int tm = 0; tm < 2; ++tm) {
-                        mma_f16(dg, a00, a01, a02, a03, bq[g][0][nt][tm][0], bq[g][0][nt][tm][1]);
-                        mma_f16(dg, a10, a11, a12, a13, bq[g][1][nt][tm][0], bq[g][1][nt][tm][1]);
+                    for (int j = 0; j < 4; ++j) {
+                        hi[j] = xq[ch][j] * sc;
+                        lo[j] = hi[j] - __half2float(__float2half_rn(hi[j]));
                     }
-                    sacc[nt][0] = fmaf(kA[g], dg[0], sacc[nt][0]);
-                    sacc[nt][1] = fmaf(kA[g], dg[1], sacc[nt][1]);
-                    sacc[nt][2] = fmaf(kB[g], dg[2], sacc[nt][2]);
-                    sacc[nt][3] = fmaf(kB[g], dg[3], sacc[nt][3]);
+                    const uint32_t r00 = pack_half2(hi[0], hi[1]), r01 = pack_half2(hi[2], hi[3]);
+                    const uint32_t r10 = pack_half2(lo[0], lo[1]), r11 = pack_half2(lo[2], lo[3]);
+                    if constexpr (NT == 1) {
+                        bq[ch >> 1][ch & 1][nt][0][0] = r00;
+                        bq[ch >> 1][ch & 1][nt][0][1] = r01;
+                        bq[ch >> 1][ch & 1][nt][1][0] = r10;
+                        bq[ch >> 1][ch & 1][nt][1][1] = r11;
+                    } else {
+                        qs[((ch * NT + nt) * 2 + 0) * 32 + lane] = make_uint2(r00, r01);
+                        qs[((ch * NT + nt) * 2 + 1) * 32 + lane] = make_uint2(r10, r11);
+                    }
                 }
+                // 2^-E of the heads in this lane's score columns (nt*8 + 2*t4 + cc),
+                // held by the lanes feeding those heads (gl4 = 2*t4 + cc)
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc)
+                    qexp[nt][cc] = pow2i(-__shfl_sync(0xffffffffu, E, (2 * t4 + cc) * 4));
             }
-            const int ra = r0 + gl4, rb = r0 + gl4 + 8;
+            __syncwarp();
+        }
+        float m[NT][2], l[NT][2];
+        float acc[8][NT][4];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
+        for (int nt = 0; nt < NT; ++nt) {
+            m[nt][0] = m[nt][1] = -INFINITY;
+            l[nt][0] = l[nt][1] = 0.0f;
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    sreg[mb][nt][c][0] = ra < nt_rows ? sacc[nt][c] * qexp[nt][c] : -INFINITY;
-                    sreg[mb][nt][c][1] = rb < nt_rows ? sacc[nt][2 + c] * qexp[nt][c] : -INFINITY;
-                }
-            if (a.scores != nullptr) {
+            for (int cc = 0; cc < 8; ++cc)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[cc][nt][j] = 0.0f;
+        }
+        int ew_prev = 0;
+
+        for (int64_t k = 0; k < run_len; ++k, ++i, ++x) {
+            const int stg = int(i % kStages);
+            char *st = sm + stg * kStageBytes;
+            if (__any_sync(0xffffffffu, !mbar_wait_bounded(&bar[stg], uint32_t(i / kStages) & 1u))) {
+                ok = false;
+                break;
+            }
+            const int n_valid = min(kWR, cur.Lb - cur.tl * kWR);
+            const uint32_t kaddr = smem_addr(st + kStK) + k_lane;
+            const float *ks_s = reinterpret_cast<const float *>(st + kStKs);
+            const float *vs_s = reinterpret_cast<const float *>(st + kStVs);
+
+            // ------------------------------------------------ scores
+            float sreg[2][NT][2][2];  // [m block][n-tile][column][row gl4 / gl4 + 8]
+#pragma unroll
+            for (int mb = 0; mb < 2; ++mb) {
+                float sacc[NT][4];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        const int h = nt * 8 + 2 * t4 + c;
+                    for (int j = 0; j < 4; ++j) sacc[nt][j] = 0.0f;
+                const float4 ksA = *reinterpret_cast<const float4 *>(&ks_s[(mb * 16 + gl4) * 4]);
+                const float4 ksB = *reinterpret_cast<const float4 *>(&ks_s[(mb * 16 + gl4 + 8) * 4]);
+                const float kA[4] = {ksA.x, ksA.y, ksA.z, ksA.w};
+                const float kB[4] = {ksB.x, ksB.y, ksB.z, ksB.w};
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    uint32_t w[4];
+                    ldsm_x4(kaddr + mb * 2048 + k_chunk[g], w);
+                    const uint32_t u0 = w[0] ^ 0x80808080u, u1 = w[1] ^ 0x80808080u;
+                    const uint32_t u2 = w[2] ^ 0x80808080u, u3 = w[3] ^ 0x80808080u;
+                    const uint32_t a00 = codes_f16x2<0x4140>(u0), a02 = codes_f16x2<0x4342>(u0);
+                    const uint32_t a01 = codes_f16x2<0x4140>(u1), a03 = codes_f16x2<0x4342>(u1);
+                    const uint32_t a10 = codes_f16x2<0x4140>(u2), a12 = codes_f16x2<0x4342>(u2);
+                    const uint32_t a11 = codes_f16x2<0x4140>(u3), a13 = codes_f16x2<0x4342>(u3);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        float dg[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                        for (int tm = 0; tm < 2; ++tm) {
+                            uint32_t b0, b1, b2, b3;
+                            if constexpr (NT == 1) {
+                                b0 = bq[g][0][nt][tm][0];
+                                b1 = bq[g][0][nt][tm][1];
+                                b2 = bq[g][1][nt][tm][0];
+                                b3 = bq[g][1][nt][tm][1];
+                            } else {
+                                const uint2 q0 = qs[(((2 * g) * NT + nt) * 2 + tm) * 32 + lane];
+                                const uint2 q1 = qs[(((2 * g + 1) * NT + nt) * 2 + tm) * 32 + lane];
+                                b0 = q0.x;
+                                b1 = q0.y;
+                                b2 = q1.x;
+                                b3 = q1.y;
+                            }
+                            mma_f16(dg, a00, a01, a02, a03, b0, b1);
+                            mma_f16(dg, a10, a11, a12, a13, b2, b3);
+                        }
+                        sacc[nt][0] = fmaf(kA[g], dg[0], sacc[nt][0]);
+                        sacc[nt][1] = fmaf(kA[g], dg[1], sacc[nt][1]);
+                        sacc[nt][2] = fmaf(kB[g], dg[2], sacc[nt][2]);
+                        sacc[nt][3] = fmaf(kB[g], dg[3], sacc[nt][3]);
+                    }
+                }
+                const int ra = mb * 16 + gl4, rb = ra + 8;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int cc = 0; cc < 2; ++cc) {
+                        sreg[mb][nt][cc][0] = ra < n_valid ? sacc[nt][cc] * qexp[nt][cc] : -INFINITY;
+                        sreg[mb][nt][cc][1] = rb < n_valid ? sacc[nt][2 + cc] * qexp[nt][cc] : -INFINITY;
+                    }
+            }
+            if (a.scores != nullptr) {
+                // per-row log2 scores for the imp pass: [hpk][cap] per unit
+                float *sp = a.scores + cur.rbase * a.hpk + int64_t(cur.tl) * kWR;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int cc = 0; cc < 2; ++cc) {
+                        const int h = nt * 8 + 2 * t4 + cc;
                         if (h < a.hpk) {
-                            float *sp = a.scores + ci.score0 + h * ci.score_ld + row0;
-                            if (ra < nt_rows) sp[ra] = sreg[mb][nt][c][0];
-                            if (rb < nt_rows) sp[rb] = sreg[mb][nt][c][1];
+                            float *sh = sp + int64_t(h) * cur.cap;
+#pragma unroll
+                            for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
+                                for (int rw = 0; rw < 2; ++rw) {
+                                    const int r = mb * 16 + gl4 + 8 * rw;
+                                    if (r < n_valid) sh[r] = sreg[mb][nt][cc][rw];
+                                }
                         }
                     }
             }
-        }
-        // per-warp maxima of every head and of the V row scales
+
+            // ------------------------------------------------ softmax
+            float vsr[2][2];
+            float vmax = 0.0f;
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+            for (int mb = 0; mb < 2; ++mb)
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                float m = fmaxf(fmaxf(sreg[0][nt][c][0], sreg[0][nt][c][1]),
-                                fmaxf(sreg[1][nt][c][0], sreg[1][nt][c][1]));
-                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
-                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-                const int h = nt * 8 + 2 * t4 + c;
-                if (gl4 == 0 && h < HPKP) red[warp * HPKP + h] = m;
-            }
-        {
-            float v = tid < nt_rows ? vs_s[tid] : 0.0f;
+                for (int rw = 0; rw < 2; ++rw) {
+                    const int r = mb * 16 + gl4 + 8 * rw;
+                    vsr[mb][rw] = r < n_valid ? vs_s[r] : 0.0f;
+                    vmax = fmaxf(vmax, vsr[mb][rw]);
+                }
+            vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 4));
+            vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 8));
+            vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 16));
+            const int ew = vmax > 0.0f ? min(14 - exponent_of(vmax), 100) : 0;
+            const float wsc = pow2i(ew);
+            const float dew = float(ew - ew_prev);
+            ew_prev = ew;
+            float fa[NT][2];
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-            if (lane == 0) vred[warp] = v;
-        }
-        __syncthreads();
-        // -------------------------- new maxima (identical in every thread)
-        float vmax = vred[0];
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int w = 1; w < kWarps; ++w) vmax = fmaxf(vmax, vred[w]);
-        const int ew = vmax > 0.0f ? 14 - exponent_of(vmax) : 0;
-        const float wscale = exp2f(float(ew));
-        // Heads past HPKP (padding lanes) read a clamped head: harmless, and
-        // it keeps every lane on the same path.  Tile maxima are finite (each
-        // tile has a valid row), so exp2(old - new) is 0 on the first tile.
-        auto tile_max = [&](int h) {
-            h = min(h, HPKP - 1);
-            float m = red[h];
+                for (int cc = 0; cc < 2; ++cc) {
+                    float tmx = fmaxf(fmaxf(sreg[0][nt][cc][0], sreg[0][nt][cc][1]),
+                                      fmaxf(sreg[1][nt][cc][0], sreg[1][nt][cc][1]));
+                    tmx = fmaxf(tmx, __shfl_xor_sync(0xffffffffu, tmx, 4));
+                    tmx = fmaxf(tmx, __shfl_xor_sync(0xffffffffu, tmx, 8));
+                    tmx = fmaxf(tmx, __shfl_xor_sync(0xffffffffu, tmx, 16));
+                    const float mn = fmaxf(m[nt][cc], tmx);
+                    // m is -inf before the first tile: both factors are then 0
+                    fa[nt][cc] = fast_exp2(m[nt][cc] - mn + dew);
+                    l[nt][cc] *= fast_exp2(m[nt][cc] - mn);
+                    m[nt][cc] = mn;
+                }
 #pragma unroll
-            for (int w = 1; w < kWarps; ++w) m = fmaxf(m, red[w * HPKP + h]);
-            return m;
-        };
-        const float mna = fmaxf(m_a, tile_max(gl4));
-        const float al_a = exp2f(m_a - mna);
-        m_a = mna;
-        const float mnb = fmaxf(m_b, tile_max(gl4 + 8));
-        const float al_b = exp2f(m_b - mnb);
-        m_b = mnb;
-        // ------------------- weights from the score registers -> f16 terms
-        float vsw[2][2];  // V row scale * 2^ew of this lane's rows (0 past the tile)
-#pragma unroll
-        for (int mb = 0; mb < 2; ++mb)
-#pragma unroll
-            for (int rw = 0; rw < 2; ++rw) {
-                const int p = warp * 32 + mb * 16 + gl4 + 8 * rw;
-                vsw[mb][rw] = p < nt_rows ? vs_s[p] * wscale : 0.0f;
-            }
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                // padding columns (heads >= HPKP when HPKP is 4) compute like
-                // the others and write weight rows the value pass never reads
-                const int h = nt * 8 + 2 * t4 + c;
-                const float mn = fmaxf(mcol[nt][c], tile_max(h));
-                lcol[nt][c] *= exp2f(mcol[nt][c] - mn);
-                mcol[nt][c] = mn;
-                const float live = h < a.hpk ? 1.0f : 0.0f;
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int mb = 0; mb < 2; ++mb)
 #pragma unroll
                     for (int rw = 0; rw < 2; ++rw) {
-                        // rows past the tile hold -inf scores: e = 0
-                        const float e = live * exp2f(sreg[mb][nt][c][rw] - mn);
-                        lcol[nt][c] += e;
-                        const float w = e * vsw[mb][rw];
-                        const __half t1 = __float2half_rn(w);
-                        const __half t2 = __float2half_rn(w - __half2float(t1));
-                        *reinterpret_cast<__half *>(Aw + wofs[mb][nt][c][rw]) = t1;
-                        *reinterpret_cast<__half *>(Aw + 8 * 16 * 32 + wofs[mb][nt][c][rw]) = t2;
+                        // rows past the tile hold -inf scores and a zero scale
+                        const float e0 = fast_exp2(sreg[mb][nt][0][rw] - m[nt][0]);
+                        const float e1 = fast_exp2(sreg[mb][nt][1][rw] - m[nt][1]);
+                        l[nt][0] += e0;
+                        l[nt][1] += e1;
+                        const float vw = vsr[mb][rw] * wsc;
+                        const float w0 = e0 * vw, w1 = e1 * vw;
+                        const uint32_t t1 = pack_half2(w0, w1);
+                        const float2 back = __half22float2(*reinterpret_cast<const __half2 *>(&t1));
+                        const uint32_t t2 = pack_half2(w0 - back.x, w1 - back.y);
+                        const uint32_t row = uint32_t(mb * 16 + gl4 + 8 * rw) * 16;
+                        sts32(p_st + uint32_t(nt) * 512 + row, t1);
+                        sts32(p_st + uint32_t(NT + nt) * 512 + row, t2);
                     }
-            }
-        __syncthreads();  // weights visible; K slot drained
-        if (tid == 0 && j + kMmaSlots < nseg) mma_issue<HPK>(ci, kmap, vmap, row_base, sm, bar, j + kMmaSlots);
-        // ------------------------------------------------ P.V (f16 MMA)
-        j = 2 * t + 1;
-        slot = j % kMmaSlots;
-        if (__syncthreads_or(!mbar_wait_bounded(&bar[slot], (j / kMmaSlots) & 1))) {
-            ok = false;
-            break;
-        }
-        // This tile's P.V goes into fresh MMA accumulators (16 chained MMAs
-        // each); it is folded into the running sum with IEEE FMAs below, so the
-        // tensor cores' accumulation rounding never compounds across tiles.
-        float dacc[4][4];
+            __syncwarp();
+            uint32_t bp[2][NT][4];  // P^T fragments [term][n-tile][b0/b1 of k16 step 0, 1]
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+            for (int tm = 0; tm < 2; ++tm)
 #pragma unroll
-            for (int c = 0; c < 4; ++c) dacc[i][c] = 0.0f;
-        const uint32_t vaddr = smem_addr(sm + slot * kMmaSlot) + v_lane;
-#pragma unroll 2
-        for (int ks = 0; ks < 8; ++ks) {
-            // V: matrices (positions +0..7, +8..15) x (channel chunks 2w, 2w + 1)
-            uint32_t x[4];
-            ldsm_x4_t(vaddr + ks * 2048, x);
-            uint32_t b[4][2];  // [n-tile][reg]
-#pragma unroll
-            for (int blk = 0; blk < 2; ++blk) {
-                const uint32_t lo = x[2 * blk] ^ 0x80808080u, hi = x[2 * blk + 1] ^ 0x80808080u;
-                b[2 * blk][0] = codes_f16x2<0x4240>(lo);
-                b[2 * blk][1] = codes_f16x2<0x4240>(hi);
-                b[2 * blk + 1][0] = codes_f16x2<0x4341>(lo);
-                b[2 * blk + 1][1] = codes_f16x2<0x4341>(hi);
-            }
-#pragma unroll
-            for (int term = 0; term < 2; ++term) {
-                uint32_t af[4];
-                ldsm_x4(aw_base + (term * 8 + ks) * 512, af);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) mma_f16(dacc[q], af[0], af[1], af[2], af[3], b[q][0], b[q][1]);
-            }
-        }
-        {
-            // acc holds sum * 2^ew: rescale by the softmax correction and the
-            // change of weight exponent, then add this tile
-            const float fa = al_a * exp2f(float(ew - ew_prev));
-            const float fb = al_b * exp2f(float(ew - ew_prev));
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                acc[i][0] = fmaf(acc[i][0], fa, dacc[i][0]);
-                acc[i][1] = fmaf(acc[i][1], fa, dacc[i][1]);
-                acc[i][2] = fmaf(acc[i][2], fb, dacc[i][2]);
-                acc[i][3] = fmaf(acc[i][3], fb, dacc[i][3]);
-            }
-            ew_prev = ew;
-        }
-    }
+                for (int nt = 0; nt < NT; ++nt) ldsm_x4_t(p_ld + uint32_t(tm * NT + nt) * 512, bp[tm][nt]);
 
-    if (!ok) {
-        if (tid == 0) {
-            set_error(a.err, kErrTimeout);
-            for (int s = 0; s < kMmaSlots; ++s) (void)mbar_wait_bounded(&bar[s], 0, 100000000ull);
-            for (int s = 0; s < kMmaSlots; ++s) (void)mbar_wait_bounded(&bar[s], 1, 100000000ull);
+            // ------------------------------------------------ values
+            const uint32_t vaddr = smem_addr(st + kStV) + v_lane;
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) {
+                uint32_t xv[4];
+                ldsm_x4_t(vaddr + (uint32_t((cc ^ rr)) << 4), xv);
+                uint32_t af[2][4];
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                    const uint32_t lo = xv[2 * kk] ^ 0x80808080u, hi = xv[2 * kk + 1] ^ 0x80808080u;
+                    af[kk][0] = codes_f16x2<0x4240>(lo);
+                    af[kk][1] = codes_f16x2<0x4341>(lo);
+                    af[kk][2] = codes_f16x2<0x4240>(hi);
+                    af[kk][3] = codes_f16x2<0x4341>(hi);
+                }
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+                        for (int tm = 0; tm < 2; ++tm)
+                            mma_f16(d, af[kk][0], af[kk][1], af[kk][2], af[kk][3], bp[tm][nt][2 * kk],
+                                    bp[tm][nt][2 * kk + 1]);
+                    acc[cc][nt][0] = fmaf(acc[cc][nt][0], fa[nt][0], d[0]);
+                    acc[cc][nt][1] = fmaf(acc[cc][nt][1], fa[nt][1], d[1]);
+                    acc[cc][nt][2] = fmaf(acc[cc][nt][2], fa[nt][0], d[2]);
+                    acc[cc][nt][3] = fmaf(acc[cc][nt][3], fa[nt][1], d[3]);
+                }
+            }
+            __syncwarp();  // every lane is done with this stage and the P^T buffer
+            // refill this stage with the tile kStages ahead
+            if (x_begin + issued < x_end && prod_ok) {
+                if (lane == 0) {
+                    fence_proxy_async();
+                    issue_tile(prod, &maps.kq, &maps.vq, src, st, &bar[stg]);
+                }
+                ++issued;
+                if (x_begin + issued < x_end) prod_ok = cursor_next(prod, src, wa.n_seq, a.err);
+            }
+            if (x + 1 < x_end && !cursor_next(cur, src, wa.n_seq, a.err)) {
+                ok = false;
+                ++i;
+                break;
+            }
         }
-        return;
-    }
+        if (!ok) break;
 
-    // ------------------------------------------------------------ partials
-    // sums: reduce each column head over the lanes sharing it, then the warps
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            float l = lcol[nt][c];
-            l += __shfl_xor_sync(0xffffffffu, l, 4);
-            l += __shfl_xor_sync(0xffffffffu, l, 8);
-            l += __shfl_xor_sync(0xffffffffu, l, 16);
-            lcol[nt][c] = l;
-        }
-    __syncthreads();  // every warp is past its last read of red
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            const int h = nt * 8 + 2 * t4 + c;
-            if (gl4 == 0 && h < HPKP) red[warp * HPKP + h] = lcol[nt][c];
-        }
-    __syncthreads();
-    if (warp == 0 && gl4 == 0) {
+        // ------------------------------------------------ run partial
+        const int64_t p0 = slot * a.hpk;
+        const float unscale = pow2i(-ew_prev);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const int h = nt * 8 + 2 * t4 + c;
+            for (int cc = 0; cc < 2; ++cc) {
+                float lv = l[nt][cc];
+                lv += __shfl_xor_sync(0xffffffffu, lv, 4);
+                lv += __shfl_xor_sync(0xffffffffu, lv, 8);
+                lv += __shfl_xor_sync(0xffffffffu, lv, 16);
+                const int h = nt * 8 + 2 * t4 + cc;
                 if (h < a.hpk) {
-                    float l = red[h];
+                    if (gl4 == 0) {
+                        a.pm[p0 + h] = m[nt][cc];
+                        a.pl[p0 + h] = lv;
+                    }
+                    float *dst = a.pacc + (p0 + h) * 128 + 2 * gl4;
 #pragma unroll
-                    for (int w = 1; w < kWarps; ++w) l += red[w * HPKP + h];
-                    a.pm[ci.pidx0 + h] = mcol[nt][c];
-                    a.pl[ci.pidx0 + h] = l;
+                    for (int ch = 0; ch < 8; ++ch)
+                        *reinterpret_cast<float2 *>(dst + 16 * ch) =
+                            make_float2(acc[ch][nt][cc] * unscale, acc[ch][nt][2 + cc] * unscale);
                 }
             }
     }
-    // lane (gl4, t4) of warp w holds heads gl4 and gl4 + 8 at channels
-    // 32w + 16 blk + 4 t4 + {0, 2} (even tile) and + {1, 3} (odd tile)
-    const float unscale = exp2f(-float(ew_prev));
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-        const int h = gl4 + 8 * hh;
-        if (h < a.hpk) {
-#pragma unroll
-            for (int blk = 0; blk < 2; ++blk) {
-                float *dst = a.pacc + (ci.pidx0 + h) * 128 + 32 * warp + 16 * blk + 4 * t4;
-                const float *e = acc[2 * blk];
-                const float *o = acc[2 * blk + 1];
-                *reinterpret_cast<float4 *>(dst) =
-                    make_float4(e[2 * hh] * unscale, o[2 * hh] * unscale, e[2 * hh + 1] * unscale,
-                                o[2 * hh + 1] * unscale);
-            }
+
+    if (!ok) {
+        // A copy never completed (or the sequences changed under the launch):
+        // record it and give the copies still in flight a bounded chance to
+        // land, so none writes into a successor CTA's shared memory.
+        if (lane == 0) {
+            set_error(a.err, kErrTimeout);
+            for (int64_t j = i; j < issued; ++j)
+                (void)mbar_wait_bounded(&bar[j % kStages], uint32_t(j / kStages) & 1u, 100000000ull);
         }
     }
 }
 
-template <int HPK>
-__global__ void __launch_bounds__(kThreads, MmaCfg<HPK>::MIN_CTAS)
-    split_mma_kernel(SplitArgs a, LayerSrc src, const __grid_constant__ MmaMaps maps) {
-    extern __shared__ __align__(128) char smem[];
-    const int b = blockIdx.z, gl = blockIdx.y, c = blockIdx.x;
-    const int L = src.seq_len[b];
-    const int64_t r0 = int64_t(c) * a.chunk;
-    if (r0 >= L) return;
-    const int64_t cap = src.cap[b];
-    if (L > cap) {
-        if (threadIdx.x == 0) set_error(a.err, kErrBounds);
-        return;
-    }
-    const int64_t row = src.row_base[b] + int64_t(gl) * cap + r0;
-    ChunkInfo ci;
-    ci.k = nullptr;
-    ci.v = nullptr;
-    ci.ks = reinterpret_cast<const char *>(src.ks + row * 4);
-    ci.vs = reinterpret_cast<const char *>(src.vs + row);
-    ci.n = int(a.chunk < L - r0 ? int64_t(a.chunk) : L - r0);
-    ci.pidx0 = ((int64_t(b) * a.n_grp + gl) * a.nc_max + c) * a.hpk;
-    const int g = src.live[gl];
-    ci.q = a.q + (int64_t(b) * a.n_q + int64_t(g) * a.hpk) * 128;
-    ci.kcol = src.kcol + (int64_t(b) * src.n_live + gl) * 128;
-    ci.score0 = (src.row_base[b] + int64_t(gl) * cap) * a.hpk + r0;
-    ci.score_ld = cap;
-    split_mma_body<HPK>(ci, row, a, &maps.kq, &maps.vq, smem);
-}
-
-template <int HPK>
-cudaError_t launch_split_mma(const SplitArgs &a, const LayerSrc &s, const MmaMaps &maps, dim3 grid,
-                             cudaStream_t st) {
-    using C = MmaCfg<HPK>;
-    auto kern = split_mma_kernel<HPK>;
+template <int NT>
+cudaError_t launch_split_warp(const WarpArgs &wa, const LayerSrc &s, const MmaMaps &maps,
+                              cudaStream_t st) {
+    using C = WarpCfg<NT>;
+    auto kern = split_warp_kernel<NT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, C::SMEM_ALLOC, st>>>(a, s, maps);
+    kern<<<unsigned(wa.G), 32, C::SMEM_ALLOC, st>>>(wa, s, maps);
     return cudaGetLastError();
+}
+
+// Workers of one launch on the current device: SMs x resident CTAs per SM.
+template <int NT>
+int64_t split_warp_workers() {
+    int dev = 0, sms = 0, occ = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    auto kern = split_warp_kernel<NT>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             WarpCfg<NT>::SMEM_ALLOC) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 32, WarpCfg<NT>::SMEM_ALLOC) !=
+            cudaSuccess)
+        return 0;
+    return int64_t(sms) * occ;
 }
 
 }  // namespace kvd

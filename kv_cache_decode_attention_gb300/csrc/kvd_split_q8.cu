@@ -2,6 +2,8 @@
 // (K quantised: true, V quantised: true), one instance per head dim and
 // query-heads-per-group bucket.  Kept in its own unit so the four storage
 // modes compile in parallel.
+#include <mutex>
+
 #include "kvd_split_mma.cuh"
 
 namespace kvd {
@@ -17,16 +19,25 @@ cudaError_t split_layer_q8(int hd, int hpk_bucket, const SplitArgs &a, const Lay
     return cudaErrorInvalidValue;
 }
 
-cudaError_t split_layer_q8_mma(int hpk_bucket, const SplitArgs &a, const LayerSrc &s,
-                               const MmaMaps &maps, dim3 grid, cudaStream_t st) {
-    switch (hpk_bucket) {
-        case 1: return launch_split_mma<1>(a, s, maps, grid, st);
-        case 2: return launch_split_mma<2>(a, s, maps, grid, st);
-        case 4: return launch_split_mma<4>(a, s, maps, grid, st);
-        case 8: return launch_split_mma<8>(a, s, maps, grid, st);
-        case 16: return launch_split_mma<16>(a, s, maps, grid, st);
-        default: return cudaErrorInvalidValue;
-    }
+cudaError_t split_layer_q8_warp(int nt, const WarpArgs &wa, const LayerSrc &s, const MmaMaps &maps,
+                                cudaStream_t st) {
+    if (nt == 1) return launch_split_warp<1>(wa, s, maps, st);
+    if (nt == 2) return launch_split_warp<2>(wa, s, maps, st);
+    return cudaErrorInvalidValue;
+}
+
+// Workers (resident one-warp CTAs) of the tensor-core kernel on the current
+// device, cached per device; 0 if the query fails.
+int64_t split_q8_warp_workers(int nt) {
+    constexpr int kMaxDev = 64;
+    static std::mutex mu;
+    static int64_t cache[kMaxDev][2] = {};
+    int dev = 0;
+    if (nt < 1 || nt > 2 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    int64_t &w = cache[dev][nt - 1];
+    if (w == 0) w = nt == 1 ? split_warp_workers<1>() : split_warp_workers<2>();
+    return w;
 }
 
 }  // namespace kvd
