@@ -47,7 +47,7 @@ int32_t pick_chunk(int64_t work_rows) {
 }
 
 struct DecodeWs {
-    int64_t pm, pl, pacc, ml, scores, total;  // byte offsets; total < 0 if unknown
+    int64_t pm, pl, pacc, ml, scores, units, total;  // byte offsets; total < 0 if unknown
     int64_t slots;                            // tensor-core path partial slots
     int32_t nc_max;
 };
@@ -95,6 +95,7 @@ DecodeWs decode_ws(const Layer *l, int32_t n_q, bool imp) {
     w.pacc = take(P * l->hd * 4);
     w.ml = take(int64_t(l->n_seq) * n_q * 2 * 4);
     w.scores = imp ? take((l->total_rows + kRowAlign) * hpk * 4) : -1;
+    w.units = take(int64_t(l->n_seq) * std::max(1, l->n_live) * 2 * 8);
     w.total = o;
     return w;
 }
@@ -126,20 +127,25 @@ RswaWs rswa_ws(int32_t B, int32_t H, int32_t hd, int64_t ref_cap, int32_t W) {
 
 struct RunMergeArgs {
     const float *pm, *pl, *pacc;  // run partials [slot][hpk] (+ [128])
+    const int64_t *unit_slots;    // [n_seq * n_live][2]: first and last run slot of each unit
     float *out;                   // [n_seq][n_q][128]
     float *ml;                    // (max, sum) per (sequence, query head) for imp, or null
     int32_t n_q, hpk;
-    int64_t T;                    // tiles of all units in the split launch
-    int32_t G;                    // workers of the split launch
 };
 
 // Log-sum-exp merge of the run partials of one (sequence, query head) written
 // by the tensor-core kernel: out[d] = field[d] * sum_r acc_r[d] 2^(m_r - M) /
-// sum_r l_r 2^(m_r - M).  The runs of block j of unit u occupy the slots
-// NB(u) + j + c for the workers c holding its first through its last tile.
+// sum_r l_r 2^(m_r - M).  A unit's runs fill the slot range between the
+// first and last run slots the split kernel recorded for it, with empty
+// markers (max -inf) in skipped slots.  The four warps take every fourth
+// slot in one pass with a running maximum, lanes own four channels each, and
+// the warps' sums are rescaled to the common maximum and added in a fixed
+// order.
 __global__ void __launch_bounds__(128) merge_runs_kernel(RunMergeArgs a, MergeLayerSrc src) {
-    __shared__ int64_t part[2][4];
-    const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
+    __shared__ float wmax[4], wsum[4];
+    __shared__ __align__(16) float wacc[4][128];
+    const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;  // d: output channel
+    const int warp = d >> 5, lane = d & 31;
     const int L = src.seq_len[b];
     const int grp = src.slot[h / a.hpk];
     float *o = a.out + (int64_t(b) * a.n_q + h) * 128;
@@ -152,53 +158,51 @@ __global__ void __launch_bounds__(128) merge_runs_kernel(RunMergeArgs a, MergeLa
         }
         return;
     }
-    // tiles and blocks of the sequences before b
-    int64_t tp = 0, bp = 0;
-    for (int i = d; i < b; i += 128) {
-        const int64_t ti = (int64_t(src.seq_len[i]) + kWR - 1) / kWR;
-        tp += ti;
-        bp += (ti + kBlockTiles - 1) / kBlockTiles;
-    }
-    for (int off = 16; off > 0; off >>= 1) {
-        tp += __shfl_xor_sync(0xffffffffu, tp, off);
-        bp += __shfl_xor_sync(0xffffffffu, bp, off);
-    }
-    if ((d & 31) == 0) {
-        part[0][d >> 5] = tp;
-        part[1][d >> 5] = bp;
-    }
-    __syncthreads();
-    tp = (part[0][0] + part[0][1] + part[0][2] + part[0][3]) * src.n_live;
-    bp = (part[1][0] + part[1][1] + part[1][2] + part[1][3]) * src.n_live;
-    const int64_t Tb = (int64_t(L) + kWR - 1) / kWR, nb = (Tb + kBlockTiles - 1) / kBlockTiles;
-    const int64_t Pu = tp + grp * Tb, NBu = bp + grp * nb;
+    const float vc = src.vcol ? src.vcol[(int64_t(b) * src.n_live + grp) * 128 + d] : 1.0f;
+    const int64_t unit = int64_t(b) * src.n_live + grp;
+    const int64_t first = a.unit_slots[2 * unit], last = a.unit_slots[2 * unit + 1];
     const int hh = h % a.hpk;
-    auto started = [&](int64_t x) {  // workers whose range starts at or before tile x
-        const int64_t c = ((x + 1) * a.G + a.T - 1) / a.T;
-        return c < a.G ? c : int64_t(a.G);
-    };
-    float M = -INFINITY;
-    for (int64_t j = 0; j < nb; ++j) {
-        const int64_t x0 = Pu + j * kBlockTiles, x1 = min(Pu + Tb, x0 + kBlockTiles);
-        const int64_t s1 = NBu + j + started(x1 - 1) - 1;
-        for (int64_t sl = NBu + j + started(x0) - 1; sl <= s1; ++sl) M = fmaxf(M, a.pm[sl * a.hpk + hh]);
-    }
-    float Ls = 0.0f, acc = 0.0f;
-    for (int64_t j = 0; j < nb; ++j) {
-        const int64_t x0 = Pu + j * kBlockTiles, x1 = min(Pu + Tb, x0 + kBlockTiles);
-        const int64_t s1 = NBu + j + started(x1 - 1) - 1;
-        for (int64_t sl = NBu + j + started(x0) - 1; sl <= s1; ++sl) {
-            const int64_t p = sl * a.hpk + hh;
-            const float f = exp2f(a.pm[p] - M);
-            Ls = fmaf(a.pl[p], f, Ls);
-            acc = fmaf(a.pacc[p * 128 + d], f, acc);
+    const float *pmh = a.pm + hh, *plh = a.pl + hh, *pah = a.pacc + int64_t(hh) * 128 + 4 * lane;
+    // one pass per warp with a running maximum (every lane sees the same m)
+    float M = -INFINITY, Ls = 0.0f;
+    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll 4
+    for (int64_t sl = first + warp; sl <= last; sl += 4) {
+        const float m = pmh[sl * a.hpk];
+        const float pl = plh[sl * a.hpk];
+        const float4 v = *reinterpret_cast<const float4 *>(pah + sl * a.hpk * 128);
+        if (m == -INFINITY) continue;  // empty marker
+        if (m > M) {
+            const float r = exp2f(M - m);  // 0 while M is -inf
+            Ls *= r;
+            acc.x *= r;
+            acc.y *= r;
+            acc.z *= r;
+            acc.w *= r;
+            M = m;
         }
+        const float f = exp2f(m - M);
+        Ls = fmaf(pl, f, Ls);
+        acc.x = fmaf(v.x, f, acc.x);
+        acc.y = fmaf(v.y, f, acc.y);
+        acc.z = fmaf(v.z, f, acc.z);
+        acc.w = fmaf(v.w, f, acc.w);
     }
-    float r = acc / Ls;
-    if (src.vcol) r *= src.vcol[(int64_t(b) * src.n_live + grp) * 128 + d];
-    o[d] = r;
+    if (lane == 0) wmax[warp] = M;
+    __syncthreads();
+    const float Mall = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
+    const float fw = exp2f(M - Mall);  // 0 for a warp that saw no run
+    acc.x *= fw;
+    acc.y *= fw;
+    acc.z *= fw;
+    acc.w *= fw;
+    *reinterpret_cast<float4 *>(&wacc[warp][4 * lane]) = acc;
+    if (lane == 0) wsum[warp] = Ls * fw;
+    __syncthreads();
+    Ls = (wsum[0] + wsum[1]) + (wsum[2] + wsum[3]);
+    o[d] = ((wacc[0][d] + wacc[1][d]) + (wacc[2][d] + wacc[3][d])) / Ls * vc;
     if (mlp && d == 0) {
-        mlp[0] = M;
+        mlp[0] = Mall;
         mlp[1] = Ls;
     }
 }
@@ -214,36 +218,55 @@ struct ImpArgs {
     int32_t n_q, hpk, n_live;
 };
 
-// imp[b][p] += sum over live groups (ascending) and their heads (ascending)
-// of 2^(s - M) / L: the softmax weight of every live query head on row p.
-// Each block first stages the (max, 1/sum) of sequence b's heads in shared
-// memory; threads then own rows and read their scores coalesced.
+// imp[b][p] += sum over the live heads of sequence b of 2^(s - M) / L: the
+// softmax weight of every live query head on row p.  A block owns 256 rows of
+// one sequence: it stages the (max, 1/sum) of the sequence's live heads in
+// shared memory (in live order, head i = gl * hpk + hh), then its threads
+// split as 64 row quads x 4 head classes (i mod 4), each quad read as one
+// 16-byte load per head (a unit's scores start on a 16-row boundary and its
+// capacity is a multiple of 16 rows).  The four classes' sums are added in
+// a fixed order.
 constexpr int kImpThreads = 256;
+constexpr int kImpRows = 256;   // rows per block
+constexpr int kImpClasses = 4;  // head classes per row quad
 
 __global__ void __launch_bounds__(kImpThreads) imp_kernel(ImpArgs a) {
-    extern __shared__ float mlinv[];  // [n_q][2]: max, 1/sum
-    const int b = blockIdx.y;
+    extern __shared__ float mlinv[];  // [n_live * hpk][2]: max, 1/sum
+    __shared__ __align__(16) float part[kImpClasses][kImpRows];
+    const int b = blockIdx.y, t = threadIdx.x;
     const int L = a.seq_len[b];
-    const int p0 = blockIdx.x * kImpThreads;
+    const int p0 = blockIdx.x * kImpRows;
     if (p0 >= L) return;
-    for (int i = threadIdx.x; i < a.n_q; i += kImpThreads) {
-        const float M = a.ml[(int64_t(b) * a.n_q + i) * 2];
-        const float Ls = a.ml[(int64_t(b) * a.n_q + i) * 2 + 1];
+    const int nh = a.n_live * a.hpk;
+    const int64_t cap = a.cap[b];
+    for (int i = t; i < nh; i += kImpThreads) {
+        const int h = a.live[i / a.hpk] * a.hpk + i % a.hpk;
+        const float M = a.ml[(int64_t(b) * a.n_q + h) * 2];
+        const float Ls = a.ml[(int64_t(b) * a.n_q + h) * 2 + 1];
         mlinv[2 * i] = M;
         mlinv[2 * i + 1] = Ls > 0.0f ? 1.0f / Ls : 0.0f;
     }
     __syncthreads();
-    const int p = p0 + threadIdx.x;
-    if (p >= L) return;
-    const int64_t cap = a.cap[b];
-    float add = 0.0f;
-    for (int gl = 0; gl < a.n_live; ++gl) {
-        const int g = a.live[gl];
-        const float *sg = a.scores + (a.row_base[b] + gl * cap) * a.hpk + p;
-        const float *mg = mlinv + 2 * g * a.hpk;
-        for (int hh = 0; hh < a.hpk; ++hh) add += exp2f(sg[hh * cap] - mg[2 * hh]) * mg[2 * hh + 1];
+    const int quad = t % (kImpRows / 4), cls = t / (kImpRows / 4);
+    const int p = p0 + 4 * quad;
+    float add[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (p < L) {
+        // the scores of live head i start at row_base * hpk + i * cap
+        const float *sb = a.scores + a.row_base[b] * a.hpk + p;
+#pragma unroll 4
+        for (int i = cls; i < nh; i += kImpClasses) {
+            const float4 sv = *reinterpret_cast<const float4 *>(sb + int64_t(i) * cap);
+            const float M = mlinv[2 * i], il = mlinv[2 * i + 1];
+            add[0] += exp2f(sv.x - M) * il;
+            add[1] += exp2f(sv.y - M) * il;
+            add[2] += exp2f(sv.z - M) * il;
+            add[3] += exp2f(sv.w - M) * il;
+        }
     }
-    a.imp[a.imp_base[b] + p] += add;
+    *reinterpret_cast<float4 *>(&part[cls][4 * quad]) = make_float4(add[0], add[1], add[2], add[3]);
+    __syncthreads();
+    const int r = p0 + t;
+    if (r < L) a.imp[a.imp_base[b] + r] += (part[0][t] + part[1][t]) + (part[2][t] + part[3][t]);
 }
 
 // ---------------------------------------------------------------- R-SWA copies
@@ -384,6 +407,7 @@ extern "C" kvd_status decode_attention(const float *q, const kvd_layer *L, int32
         wa.T = T;
         wa.G = int32_t(std::min(T, workers));
         wa.n_seq = l->n_seq;
+        wa.unit_slots = reinterpret_cast<int64_t *>(ws + w.units);
         if (T > 0) {
             MmaMaps maps;
             std::memcpy(&maps.kq, l->tmap_kq, sizeof(maps.kq));
@@ -398,8 +422,7 @@ extern "C" kvd_status decode_attention(const float *q, const kvd_layer *L, int32
         rm.ml = ml;
         rm.n_q = n_q;
         rm.hpk = hpk;
-        rm.T = T;
-        rm.G = wa.G;
+        rm.unit_slots = wa.unit_slots;
         merge_runs_kernel<<<dim3(unsigned(n_q), unsigned(l->n_seq)), 128, 0, st>>>(rm, ms);
         if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
     } else {
@@ -446,9 +469,9 @@ extern "C" kvd_status decode_attention(const float *q, const kvd_layer *L, int32
         ia.n_q = n_q;
         ia.hpk = hpk;
         ia.n_live = l->n_live;
-        dim3 igrid(unsigned(ceil_div(max_len, kImpThreads)), unsigned(l->n_seq));
-        const size_t ml_bytes = size_t(n_q) * 2 * sizeof(float);
-        if (ml_bytes > 48 * 1024 &&
+        dim3 igrid(unsigned(ceil_div(max_len, kImpRows)), unsigned(l->n_seq));
+        const size_t ml_bytes = size_t(std::max(1, l->n_live * hpk)) * 2 * sizeof(float);
+        if (ml_bytes > 40 * 1024 &&
             cudaFuncSetAttribute(imp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(ml_bytes)) != cudaSuccess)
             return KVD_ECUDA;

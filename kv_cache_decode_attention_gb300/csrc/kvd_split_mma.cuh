@@ -21,8 +21,10 @@
 // worker c starting in block j of unit u sits at slot NB(u) + j + c, where
 // NB(u) counts the blocks of the units before u.  (Runs start at block starts
 // and worker starts; moving to the next run start adds one to j or to c, so
-// slots are distinct, and the merge finds a block's runs as the slot range
-// from the worker holding its first tile to the one holding its last.)
+// slots are distinct.  Where a worker starts exactly on a block start both
+// grow and one slot is skipped; that worker marks it empty, so a unit's runs
+// and markers fill the slot range from its first run to its last, which the
+// workers holding those runs record for the merge.)
 //
 // Each warp owns a ring of kStages stages (K codes, V codes, K scales, V
 // scales of one tile) filled by TMA: 2-D tensor copies with the 128-byte
@@ -155,8 +157,9 @@ struct MmaMaps {
 
 struct WarpArgs {
     SplitArgs a;
-    int64_t T;      // tiles of all units
-    int32_t G;      // workers (grid size), 1 <= G <= T
+    int64_t *unit_slots;  // [n_seq * n_live][2]: slot of each unit's first and last run
+    int64_t T;            // tiles of all units
+    int32_t G;            // workers (grid size), 1 <= G <= T
     int32_t n_seq;
 };
 
@@ -284,6 +287,16 @@ __global__ void __launch_bounds__(32) split_warp_kernel(WarpArgs wa, LayerSrc sr
     TileCursor cur;
     if (!cursor_locate(cur, x_begin, src, wa.n_seq, lane, a.err)) return;
     TileCursor prod = cur;
+    if (cur.tl % kBlockTiles == 0) {
+        // This worker starts on a block start: the slot just below its first
+        // run belongs to no run.  Mark it empty (max -inf) so that every unit's
+        // runs fill a contiguous slot range.
+        const int64_t gap = cur.bq + int64_t(cur.gl) * blocks_of(cur.Tb) + cur.tl / kBlockTiles + c - 1;
+        if (gap >= 0 && lane < a.hpk) {
+            a.pm[gap * a.hpk + lane] = -INFINITY;
+            a.pl[gap * a.hpk + lane] = 0.0f;
+        }
+    }
 
     if (lane == 0) {
         for (int s = 0; s < kStages; ++s) mbar_init(&bar[s], 1);
@@ -327,6 +340,9 @@ __global__ void __launch_bounds__(32) split_warp_kernel(WarpArgs wa, LayerSrc sr
         if (run_len > cur.Tb - cur.tl) run_len = cur.Tb - cur.tl;
         if (run_len > kBlockTiles - cur.tl % kBlockTiles) run_len = kBlockTiles - cur.tl % kBlockTiles;
         const int64_t slot = cur.bq + int64_t(cur.gl) * blocks_of(cur.Tb) + cur.tl / kBlockTiles + c;
+        const int64_t unit = int64_t(cur.b) * src.n_live + cur.gl;
+        const bool unit_end = cur.tl + run_len == cur.Tb;
+        if (cur.tl == 0 && lane == 0) wa.unit_slots[2 * unit] = slot;
         if (cur.b != q_b || cur.gl != q_gl) {
             // q * kcol * scale * log2e * 2^E_h = t1 + t2 (f16) for the heads
             // this lane feeds as B columns (nt*8 + gl4), channels
@@ -602,6 +618,7 @@ __global__ void __launch_bounds__(32) split_warp_kernel(WarpArgs wa, LayerSrc sr
         if (!ok) break;
 
         // ------------------------------------------------ run partial
+        if (unit_end && lane == 0) wa.unit_slots[2 * unit + 1] = slot;
         const int64_t p0 = slot * a.hpk;
         const float unscale = pow2i(-ew_prev);
 #pragma unroll
