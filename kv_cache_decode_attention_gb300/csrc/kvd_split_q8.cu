@@ -4,7 +4,7 @@
 // modes compile in parallel.
 #include <mutex>
 
-#include "kvd_split_mma.cuh"
+#include "kvd_split_h16.cuh"
 
 namespace kvd {
 
@@ -19,15 +19,17 @@ cudaError_t split_layer_q8(int hd, int hpk_bucket, const SplitArgs &a, const Lay
     return cudaErrorInvalidValue;
 }
 
+// Tensor-core kernels for the q8_2f cache: heads in N for groups of up to 8
+// query heads, heads in M for groups of 9..16 (nt = 1, 2).
 cudaError_t split_layer_q8_warp(int nt, const WarpArgs &wa, const LayerSrc &s, const MmaMaps &maps,
                                 cudaStream_t st) {
     if (nt == 1) return launch_split_warp<1>(wa, s, maps, st);
-    if (nt == 2) return launch_split_warp<2>(wa, s, maps, st);
+    if (nt == 2) return launch_split_h16(wa, s, maps, st);
     return cudaErrorInvalidValue;
 }
 
-// Workers (resident one-warp CTAs) of the tensor-core kernel on the current
-// device, cached per device; 0 if the query fails.
+// Workers (resident one-warp CTAs) of that kernel on the current device,
+// cached per device; 0 if the query fails.
 int64_t split_q8_warp_workers(int nt) {
     constexpr int kMaxDev = 64;
     static std::mutex mu;
@@ -36,7 +38,7 @@ int64_t split_q8_warp_workers(int nt) {
     if (nt < 1 || nt > 2 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
     std::lock_guard<std::mutex> lock(mu);
     int64_t &w = cache[dev][nt - 1];
-    if (w == 0) w = nt == 1 ? split_warp_workers<1>() : split_warp_workers<2>();
+    if (w == 0) w = nt == 1 ? split_warp_workers<1>() : split_h16_workers();
     return w;
 }
 
