@@ -17,9 +17,9 @@ cudaError_t split_layer_f32(int, int, const SplitArgs &, const LayerSrc &, dim3,
 cudaError_t split_layer_q8(int, int, const SplitArgs &, const LayerSrc &, dim3, cudaStream_t);
 cudaError_t split_layer_q8k(int, int, const SplitArgs &, const LayerSrc &, dim3, cudaStream_t);
 cudaError_t split_layer_q8v(int, int, const SplitArgs &, const LayerSrc &, dim3, cudaStream_t);
-cudaError_t split_layer_q8_warp(int, const WarpArgs &, const LayerSrc &, const MmaMaps &,
-                                cudaStream_t);
-int64_t split_q8_warp_workers(int);
+int q8_tc_variant(int);
+cudaError_t split_layer_q8_tc(int, const WarpArgs &, const LayerSrc &, const MmaMaps &, cudaStream_t);
+int64_t split_q8_tc_workers(int);
 
 namespace {
 
@@ -58,15 +58,13 @@ bool warp_path(const Layer *l) {
     return l->mode == KVD_Q8 && l->hd == 128 && l->have_tmap_kq && l->have_tmap_vq;
 }
 
-int warp_nt(int hpk) { return hpk > 8 ? 2 : 1; }
-
 // Partial slots the tensor-core kernel may write: every unit's blocks at full
 // capacity plus one per worker (each worker start splits at most one block).
 int64_t warp_slots(const Layer *l, int hpk) {
     int64_t nb = 0;
     for (int b = 0; b < l->n_seq; ++b)
         nb += int64_t(l->n_live) * ceil_div(ceil_div(l->h_cap[b], kWR), kBlockTiles);
-    const int64_t g = split_q8_warp_workers(warp_nt(hpk));
+    const int64_t g = split_q8_tc_workers(q8_tc_variant(hpk));
     return g > 0 ? nb + g : -1;
 }
 
@@ -399,8 +397,8 @@ extern "C" kvd_status decode_attention(const float *q, const kvd_layer *L, int32
         // tensor-core kernel over balanced tile ranges, then the run merge
         int64_t T = 0;
         for (int b = 0; b < l->n_seq; ++b) T += int64_t(l->n_live) * ceil_div(l->h_seq_len[b], kWR);
-        const int nt = warp_nt(hpk);
-        const int64_t workers = split_q8_warp_workers(nt);
+        const int variant = q8_tc_variant(hpk);
+        const int64_t workers = split_q8_tc_workers(variant);
         if (workers <= 0) return KVD_ECUDA;
         WarpArgs wa;
         wa.a = a;
@@ -412,7 +410,7 @@ extern "C" kvd_status decode_attention(const float *q, const kvd_layer *L, int32
             MmaMaps maps;
             std::memcpy(&maps.kq, l->tmap_kq, sizeof(maps.kq));
             std::memcpy(&maps.vq, l->tmap_vq, sizeof(maps.vq));
-            if (split_layer_q8_warp(nt, wa, s, maps, st) != cudaSuccess) return KVD_ECUDA;
+            if (split_layer_q8_tc(variant, wa, s, maps, st) != cudaSuccess) return KVD_ECUDA;
         }
         RunMergeArgs rm;
         rm.pm = a.pm;

@@ -280,13 +280,17 @@ __global__ void __launch_bounds__(32, 8) split_h16_kernel(WarpArgs wa, LayerSrc 
             // (the t4 lanes of any gl4 cover all 32 rows: every lane has the same vmax)
             const int ew = vmax > 0.0f ? min(14 - exponent_of(vmax), 100) : 0;
             const float wsc = pow2i(ew);
-            const float dew = float(ew - ew_prev);
+            // the change of Ew is an exact power of two (the approximate exp2
+            // is not exact even at integers, and these factors compound over a run)
+            const float dsc = ldexpf(1.0f, ew - ew_prev);
             ew_prev = ew;
             const float mna = fmaxf(ma, ta), mnb = fmaxf(mb, tb);
-            // m is -inf before the first tile: both factors are then 0
-            const float fa_a = fast_exp2(ma - mna + dew), fa_b = fast_exp2(mb - mnb + dew);
-            la *= fast_exp2(ma - mna);
-            lb *= fast_exp2(mb - mnb);
+            // exactly 1 while the maximum holds; 0 before the first tile (m = -inf)
+            const float ala = mna == ma ? 1.0f : fast_exp2(ma - mna);
+            const float alb = mnb == mb ? 1.0f : fast_exp2(mb - mnb);
+            const float fa_a = ala * dsc, fa_b = alb * dsc;
+            la *= ala;
+            lb *= alb;
             ma = mna;
             mb = mnb;
             // weights -> f16 terms in the A layout of the value MMA: k16 step

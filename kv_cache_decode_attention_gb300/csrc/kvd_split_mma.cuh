@@ -58,7 +58,7 @@
 namespace kvd {
 
 constexpr int kWR = 32;             // rows per tile
-constexpr int kBlockTiles = 128;    // tiles per partial block (4096 rows)
+constexpr int kBlockTiles = 64;     // tiles per partial block (2048 rows; bounds one f32 fold chain)
 constexpr int kStages = 2;          // ring stages per warp
 constexpr int kStK = 0;             // K codes [32][128], 128-byte swizzled
 constexpr int kStV = 4096;          // V codes [32][128], 128-byte swizzled
@@ -67,13 +67,14 @@ constexpr int kStVs = 8704;         // V scales [32] f32
 constexpr int kStageBytes = 9216;   // multiple of 1024 (swizzle atom)
 constexpr uint32_t kStageTx = 4096 + 4096 + 512 + 128;
 
-// NT: score/value n8 tiles of heads (1 for hpk <= 8, 2 for hpk <= 16).
-template <int NT>
+// PACK: groups of at most 4 query heads put both query terms (and both
+// weight terms) side by side in the 8 columns of one n8 tile; larger groups
+// (up to 8 heads) use the 8 columns for heads and chain the two terms.
+template <bool PACK>
 struct WarpCfg {
-    static constexpr int P_OFF = kStages * kStageBytes;  // P^T [term][NT][32 rows][8 heads] f16
-    static constexpr int Q_OFF = P_OFF + 2 * NT * 512;   // q fragments when NT == 2
-    static constexpr int Q_BYTES = NT == 1 ? 0 : 4 * 2 * NT * 2 * 32 * 8;
-    static constexpr int BAR_OFF = Q_OFF + Q_BYTES;
+    static constexpr int P_OFF = kStages * kStageBytes;   // P^T [term][32 rows][8 columns] f16
+    static constexpr int P_BYTES = PACK ? 512 : 1024;
+    static constexpr int BAR_OFF = P_OFF + P_BYTES;
     static constexpr int SMEM = BAR_OFF + kStages * 8;
     static constexpr int SMEM_ALLOC = SMEM + 1024;  // room to align the base to 1024
 };
@@ -268,10 +269,10 @@ __device__ __forceinline__ void issue_tile(const TileCursor &c, const CUtensorMa
     bulk_g2s(stage + kStVs, src.vs + row, 128, bar);
 }
 
-template <int NT>
+template <bool PACK>
 __global__ void __launch_bounds__(32) split_warp_kernel(WarpArgs wa, LayerSrc src,
                                                         const __grid_constant__ MmaMaps maps) {
-    using C = WarpCfg<NT>;
+    using C = WarpCfg<PACK>;
     extern __shared__ __align__(128) char smem_raw[];
     const SplitArgs &a = wa.a;
     const int lane = threadIdx.x;
@@ -328,9 +329,17 @@ __global__ void __launch_bounds__(32) split_warp_kernel(WarpArgs wa, LayerSrc sr
     const uint32_t p_ld = p_base + uint32_t(8 * mi + rr) * 16;  // ldmatrix.trans rows of P^T
     const uint32_t p_st = p_base + uint32_t(t4) * 4;              // + row * 16
 
-    uint32_t bq[NT == 1 ? 4 : 1][2][NT][2][2];  // q fragments [group][k16][n-tile][term][reg]
-    uint2 *qs = reinterpret_cast<uint2 *>(sm + C::Q_OFF);  // same, in shared memory (NT == 2)
-    float qexp[NT][2];
+    // Score columns.  PACK: column n holds term n / 4 of head n % 4, so this
+    // lane's columns 2*t4, 2*t4 + 1 are heads hc0 = (2*t4) % 4 and hc0 + 1
+    // (the t1 part when t4 < 2, the t2 part otherwise); after the two parts
+    // are added, lanes t4 and t4 ^ 2 hold the same scores.  Otherwise columns
+    // are heads 2*t4, 2*t4 + 1.
+    const int hc0 = PACK ? (2 * t4) & 3 : 2 * t4;
+    const bool owner = !PACK || t4 < 2;  // writes scores and partials of its heads
+    // B fragments of the query [chunk][term or -][reg]: the column this lane
+    // feeds is gl4 (PACK: term gl4 / 4 of head gl4 % 4; else head gl4)
+    uint32_t bq[8][PACK ? 1 : 2][2];
+    float qexp[2];
     int q_b = -1, q_gl = -1;
 
     int64_t x = x_begin, i = 0;  // global tile, worker-local tile count
@@ -345,75 +354,64 @@ __global__ void __launch_bounds__(32) split_warp_kernel(WarpArgs wa, LayerSrc sr
         const bool unit_end = cur.tl + run_len == cur.Tb;
         if (cur.tl == 0 && lane == 0) wa.unit_slots[2 * unit] = slot;
         if (cur.b != q_b || cur.gl != q_gl) {
-            // q * kcol * scale * log2e * 2^E_h = t1 + t2 (f16) for the heads
-            // this lane feeds as B columns (nt*8 + gl4), channels
+            // q * kcol * scale * log2e * 2^E_h = t1 + t2 (f16), channels
             // 16*chunk + 4*t4 .. + 3 of every chunk
             q_b = cur.b;
             q_gl = cur.gl;
             const int g = src.live[cur.gl];
             const float *qg = a.q + (int64_t(cur.b) * a.n_q + int64_t(g) * a.hpk) * 128;
             const float *kc = src.kcol + (int64_t(cur.b) * src.n_live + cur.gl) * 128;
+            const int hb = PACK ? gl4 & 3 : gl4;
+            float xq[8][4];
+            float mx = 0.0f;
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                const int hb = nt * 8 + gl4;
-                float xq[8][4];
-                float mx = 0.0f;
+            for (int ch = 0; ch < 8; ++ch) {
+                const int d = 16 * ch + 4 * t4;
+                float4 qv = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                if (hb < a.hpk) qv = *reinterpret_cast<const float4 *>(qg + hb * 128 + d);
+                const float4 kv = *reinterpret_cast<const float4 *>(kc + d);
+                xq[ch][0] = qv.x * kv.x * a.qscale;
+                xq[ch][1] = qv.y * kv.y * a.qscale;
+                xq[ch][2] = qv.z * kv.z * a.qscale;
+                xq[ch][3] = qv.w * kv.w * a.qscale;
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    const int d = 16 * ch + 4 * t4;
-                    float4 qv = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                    if (hb < a.hpk) qv = *reinterpret_cast<const float4 *>(qg + hb * 128 + d);
-                    const float4 kv = *reinterpret_cast<const float4 *>(kc + d);
-                    xq[ch][0] = qv.x * kv.x * a.qscale;
-                    xq[ch][1] = qv.y * kv.y * a.qscale;
-                    xq[ch][2] = qv.z * kv.z * a.qscale;
-                    xq[ch][3] = qv.w * kv.w * a.qscale;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) mx = fmaxf(mx, fabsf(xq[ch][j]));
-                }
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                const int E = mx > 0.0f ? min(14 - exponent_of(mx), 100) : 0;
-                const float sc = pow2i(E);
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    float hi[4], lo[4];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        hi[j] = xq[ch][j] * sc;
-                        lo[j] = hi[j] - __half2float(__float2half_rn(hi[j]));
-                    }
-                    const uint32_t r00 = pack_half2(hi[0], hi[1]), r01 = pack_half2(hi[2], hi[3]);
-                    const uint32_t r10 = pack_half2(lo[0], lo[1]), r11 = pack_half2(lo[2], lo[3]);
-                    if constexpr (NT == 1) {
-                        bq[ch >> 1][ch & 1][nt][0][0] = r00;
-                        bq[ch >> 1][ch & 1][nt][0][1] = r01;
-                        bq[ch >> 1][ch & 1][nt][1][0] = r10;
-                        bq[ch >> 1][ch & 1][nt][1][1] = r11;
-                    } else {
-                        qs[((ch * NT + nt) * 2 + 0) * 32 + lane] = make_uint2(r00, r01);
-                        qs[((ch * NT + nt) * 2 + 1) * 32 + lane] = make_uint2(r10, r11);
-                    }
-                }
-                // 2^-E of the heads in this lane's score columns (nt*8 + 2*t4 + cc),
-                // held by the lanes feeding those heads (gl4 = 2*t4 + cc)
-#pragma unroll
-                for (int cc = 0; cc < 2; ++cc)
-                    qexp[nt][cc] = pow2i(-__shfl_sync(0xffffffffu, E, (2 * t4 + cc) * 4));
+                for (int j = 0; j < 4; ++j) mx = fmaxf(mx, fabsf(xq[ch][j]));
             }
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const int E = mx > 0.0f ? min(14 - exponent_of(mx), 100) : 0;
+            const float sc = pow2i(E);
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+                float hi[4], lo[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    hi[j] = xq[ch][j] * sc;
+                    lo[j] = hi[j] - __half2float(__float2half_rn(hi[j]));
+                }
+                if constexpr (PACK) {
+                    const bool t2 = gl4 >= 4;
+                    bq[ch][0][0] = t2 ? pack_half2(lo[0], lo[1]) : pack_half2(hi[0], hi[1]);
+                    bq[ch][0][1] = t2 ? pack_half2(lo[2], lo[3]) : pack_half2(hi[2], hi[3]);
+                } else {
+                    bq[ch][0][0] = pack_half2(hi[0], hi[1]);
+                    bq[ch][0][1] = pack_half2(hi[2], hi[3]);
+                    bq[ch][PACK ? 0 : 1][0] = pack_half2(lo[0], lo[1]);
+                    bq[ch][PACK ? 0 : 1][1] = pack_half2(lo[2], lo[3]);
+                }
+            }
+            // 2^-E of the heads of this lane's score columns, held by the
+            // lanes feeding them (gl4 = head)
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) qexp[cc] = pow2i(-__shfl_sync(0xffffffffu, E, (hc0 + cc) * 4));
             __syncwarp();
         }
-        float m[NT][2], l[NT][2];
-        float acc[8][NT][4];
+        float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.0f, 0.0f};
+        float acc[8][4];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            m[nt][0] = m[nt][1] = -INFINITY;
-            l[nt][0] = l[nt][1] = 0.0f;
+        for (int cc = 0; cc < 8; ++cc)
 #pragma unroll
-            for (int cc = 0; cc < 8; ++cc)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) acc[cc][nt][j] = 0.0f;
-        }
+            for (int j = 0; j < 4; ++j) acc[cc][j] = 0.0f;
         int ew_prev = 0;
 
         for (int64_t k = 0; k < run_len; ++k, ++i, ++x) {
@@ -429,14 +427,10 @@ __global__ void __launch_bounds__(32) split_warp_kernel(WarpArgs wa, LayerSrc sr
             const float *vs_s = reinterpret_cast<const float *>(st + kStVs);
 
             // ------------------------------------------------ scores
-            float sreg[2][NT][2][2];  // [m block][n-tile][column][row gl4 / gl4 + 8]
+            float sreg[2][2][2];  // [m block][column][row gl4 / gl4 + 8]
 #pragma unroll
             for (int mb = 0; mb < 2; ++mb) {
-                float sacc[NT][4];
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) sacc[nt][j] = 0.0f;
+                float sacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
                 const float4 ksA = *reinterpret_cast<const float4 *>(&ks_s[(mb * 16 + gl4) * 4]);
                 const float4 ksB = *reinterpret_cast<const float4 *>(&ks_s[(mb * 16 + gl4 + 8) * 4]);
                 const float kA[4] = {ksA.x, ksA.y, ksA.z, ksA.w};
@@ -451,62 +445,46 @@ __global__ void __launch_bounds__(32) split_warp_kernel(WarpArgs wa, LayerSrc sr
                     const uint32_t a01 = codes_f16x2<0x4140>(u1), a03 = codes_f16x2<0x4342>(u1);
                     const uint32_t a10 = codes_f16x2<0x4140>(u2), a12 = codes_f16x2<0x4342>(u2);
                     const uint32_t a11 = codes_f16x2<0x4140>(u3), a13 = codes_f16x2<0x4342>(u3);
+                    float dg[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        float dg[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-                        for (int tm = 0; tm < 2; ++tm) {
-                            uint32_t b0, b1, b2, b3;
-                            if constexpr (NT == 1) {
-                                b0 = bq[g][0][nt][tm][0];
-                                b1 = bq[g][0][nt][tm][1];
-                                b2 = bq[g][1][nt][tm][0];
-                                b3 = bq[g][1][nt][tm][1];
-                            } else {
-                                const uint2 q0 = qs[(((2 * g) * NT + nt) * 2 + tm) * 32 + lane];
-                                const uint2 q1 = qs[(((2 * g + 1) * NT + nt) * 2 + tm) * 32 + lane];
-                                b0 = q0.x;
-                                b1 = q0.y;
-                                b2 = q1.x;
-                                b3 = q1.y;
-                            }
-                            mma_f16(dg, a00, a01, a02, a03, b0, b1);
-                            mma_f16(dg, a10, a11, a12, a13, b2, b3);
-                        }
-                        sacc[nt][0] = fmaf(kA[g], dg[0], sacc[nt][0]);
-                        sacc[nt][1] = fmaf(kA[g], dg[1], sacc[nt][1]);
-                        sacc[nt][2] = fmaf(kB[g], dg[2], sacc[nt][2]);
-                        sacc[nt][3] = fmaf(kB[g], dg[3], sacc[nt][3]);
+                    for (int tm = 0; tm < (PACK ? 1 : 2); ++tm) {
+                        mma_f16(dg, a00, a01, a02, a03, bq[2 * g][tm][0], bq[2 * g][tm][1]);
+                        mma_f16(dg, a10, a11, a12, a13, bq[2 * g + 1][tm][0], bq[2 * g + 1][tm][1]);
                     }
+                    sacc[0] = fmaf(kA[g], dg[0], sacc[0]);
+                    sacc[1] = fmaf(kA[g], dg[1], sacc[1]);
+                    sacc[2] = fmaf(kB[g], dg[2], sacc[2]);
+                    sacc[3] = fmaf(kB[g], dg[3], sacc[3]);
+                }
+                if constexpr (PACK) {
+                    // add the other term's part (columns 2*t4 ^ 4)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) sacc[j] += __shfl_xor_sync(0xffffffffu, sacc[j], 2);
                 }
                 const int ra = mb * 16 + gl4, rb = ra + 8;
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        sreg[mb][nt][cc][0] = ra < n_valid ? sacc[nt][cc] * qexp[nt][cc] : -INFINITY;
-                        sreg[mb][nt][cc][1] = rb < n_valid ? sacc[nt][2 + cc] * qexp[nt][cc] : -INFINITY;
-                    }
+                for (int cc = 0; cc < 2; ++cc) {
+                    sreg[mb][cc][0] = ra < n_valid ? sacc[cc] * qexp[cc] : -INFINITY;
+                    sreg[mb][cc][1] = rb < n_valid ? sacc[2 + cc] * qexp[cc] : -INFINITY;
+                }
             }
-            if (a.scores != nullptr) {
+            if (a.scores != nullptr && owner) {
                 // per-row log2 scores for the imp pass: [hpk][cap] per unit
                 float *sp = a.scores + cur.rbase * a.hpk + int64_t(cur.tl) * kWR;
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int h = hc0 + cc;
+                    if (h < a.hpk) {
+                        float *sh = sp + int64_t(h) * cur.cap;
 #pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        const int h = nt * 8 + 2 * t4 + cc;
-                        if (h < a.hpk) {
-                            float *sh = sp + int64_t(h) * cur.cap;
+                        for (int mb = 0; mb < 2; ++mb)
 #pragma unroll
-                            for (int mb = 0; mb < 2; ++mb)
-#pragma unroll
-                                for (int rw = 0; rw < 2; ++rw) {
-                                    const int r = mb * 16 + gl4 + 8 * rw;
-                                    if (r < n_valid) sh[r] = sreg[mb][nt][cc][rw];
-                                }
-                        }
+                            for (int rw = 0; rw < 2; ++rw) {
+                                const int r = mb * 16 + gl4 + 8 * rw;
+                                if (r < n_valid) sh[r] = sreg[mb][cc][rw];
+                            }
                     }
+                }
             }
 
             // ------------------------------------------------ softmax
@@ -525,50 +503,50 @@ __global__ void __launch_bounds__(32) split_warp_kernel(WarpArgs wa, LayerSrc sr
             vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 16));
             const int ew = vmax > 0.0f ? min(14 - exponent_of(vmax), 100) : 0;
             const float wsc = pow2i(ew);
-            const float dew = float(ew - ew_prev);
+            // the change of Ew is an exact power of two (the approximate exp2
+            // is not exact even at integers, and these factors compound over a run)
+            const float dsc = ldexpf(1.0f, ew - ew_prev);
             ew_prev = ew;
-            float fa[NT][2];
+            float fa[2];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
+            for (int cc = 0; cc < 2; ++cc) {
+                float tmx = fmaxf(fmaxf(sreg[0][cc][0], sreg[0][cc][1]), fmaxf(sreg[1][cc][0], sreg[1][cc][1]));
+                tmx = fmaxf(tmx, __shfl_xor_sync(0xffffffffu, tmx, 4));
+                tmx = fmaxf(tmx, __shfl_xor_sync(0xffffffffu, tmx, 8));
+                tmx = fmaxf(tmx, __shfl_xor_sync(0xffffffffu, tmx, 16));
+                const float mn = fmaxf(m[cc], tmx);
+                // exactly 1 while the maximum holds; 0 before the first tile (m = -inf)
+                const float al = mn == m[cc] ? 1.0f : fast_exp2(m[cc] - mn);
+                fa[cc] = al * dsc;
+                l[cc] *= al;
+                m[cc] = mn;
+            }
 #pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    float tmx = fmaxf(fmaxf(sreg[0][nt][cc][0], sreg[0][nt][cc][1]),
-                                      fmaxf(sreg[1][nt][cc][0], sreg[1][nt][cc][1]));
-                    tmx = fmaxf(tmx, __shfl_xor_sync(0xffffffffu, tmx, 4));
-                    tmx = fmaxf(tmx, __shfl_xor_sync(0xffffffffu, tmx, 8));
-                    tmx = fmaxf(tmx, __shfl_xor_sync(0xffffffffu, tmx, 16));
-                    const float mn = fmaxf(m[nt][cc], tmx);
-                    // m is -inf before the first tile: both factors are then 0
-                    fa[nt][cc] = fast_exp2(m[nt][cc] - mn + dew);
-                    l[nt][cc] *= fast_exp2(m[nt][cc] - mn);
-                    m[nt][cc] = mn;
-                }
+            for (int mb = 0; mb < 2; ++mb)
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int mb = 0; mb < 2; ++mb)
-#pragma unroll
-                    for (int rw = 0; rw < 2; ++rw) {
-                        // rows past the tile hold -inf scores and a zero scale
-                        const float e0 = fast_exp2(sreg[mb][nt][0][rw] - m[nt][0]);
-                        const float e1 = fast_exp2(sreg[mb][nt][1][rw] - m[nt][1]);
-                        l[nt][0] += e0;
-                        l[nt][1] += e1;
-                        const float vw = vsr[mb][rw] * wsc;
-                        const float w0 = e0 * vw, w1 = e1 * vw;
-                        const uint32_t t1 = pack_half2(w0, w1);
-                        const float2 back = __half22float2(*reinterpret_cast<const __half2 *>(&t1));
-                        const uint32_t t2 = pack_half2(w0 - back.x, w1 - back.y);
-                        const uint32_t row = uint32_t(mb * 16 + gl4 + 8 * rw) * 16;
-                        sts32(p_st + uint32_t(nt) * 512 + row, t1);
-                        sts32(p_st + uint32_t(NT + nt) * 512 + row, t2);
+                for (int rw = 0; rw < 2; ++rw) {
+                    // rows past the tile hold -inf scores and a zero scale
+                    const float e0 = fast_exp2(sreg[mb][0][rw] - m[0]);
+                    const float e1 = fast_exp2(sreg[mb][1][rw] - m[1]);
+                    l[0] += e0;
+                    l[1] += e1;
+                    const float vw = vsr[mb][rw] * wsc;
+                    const float w0 = e0 * vw, w1 = e1 * vw;
+                    const uint32_t t1 = pack_half2(w0, w1);
+                    const float2 back = __half22float2(*reinterpret_cast<const __half2 *>(&t1));
+                    const uint32_t t2 = pack_half2(w0 - back.x, w1 - back.y);
+                    const uint32_t row = uint32_t(mb * 16 + gl4 + 8 * rw) * 16;
+                    if constexpr (PACK) {
+                        sts32(p_st + row, t4 < 2 ? t1 : t2);  // column 2*t4: term t4 / 2
+                    } else {
+                        sts32(p_st + row, t1);
+                        sts32(p_st + 512 + row, t2);
                     }
+                }
             __syncwarp();
-            uint32_t bp[2][NT][4];  // P^T fragments [term][n-tile][b0/b1 of k16 step 0, 1]
+            uint32_t bp[PACK ? 1 : 2][4];  // P^T fragments [term][b0/b1 of k16 step 0, 1]
 #pragma unroll
-            for (int tm = 0; tm < 2; ++tm)
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) ldsm_x4_t(p_ld + uint32_t(tm * NT + nt) * 512, bp[tm][nt]);
+            for (int tm = 0; tm < (PACK ? 1 : 2); ++tm) ldsm_x4_t(p_ld + uint32_t(tm) * 512, bp[tm]);
 
             // ------------------------------------------------ values
             const uint32_t vaddr = smem_addr(st + kStV) + v_lane;
@@ -585,20 +563,16 @@ __global__ void __launch_bounds__(32) split_warp_kernel(WarpArgs wa, LayerSrc sr
                     af[kk][2] = codes_f16x2<0x4240>(hi);
                     af[kk][3] = codes_f16x2<0x4341>(hi);
                 }
+                float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                for (int kk = 0; kk < 2; ++kk)
 #pragma unroll
-                    for (int kk = 0; kk < 2; ++kk)
-#pragma unroll
-                        for (int tm = 0; tm < 2; ++tm)
-                            mma_f16(d, af[kk][0], af[kk][1], af[kk][2], af[kk][3], bp[tm][nt][2 * kk],
-                                    bp[tm][nt][2 * kk + 1]);
-                    acc[cc][nt][0] = fmaf(acc[cc][nt][0], fa[nt][0], d[0]);
-                    acc[cc][nt][1] = fmaf(acc[cc][nt][1], fa[nt][1], d[1]);
-                    acc[cc][nt][2] = fmaf(acc[cc][nt][2], fa[nt][0], d[2]);
-                    acc[cc][nt][3] = fmaf(acc[cc][nt][3], fa[nt][1], d[3]);
-                }
+                    for (int tm = 0; tm < (PACK ? 1 : 2); ++tm)
+                        mma_f16(d, af[kk][0], af[kk][1], af[kk][2], af[kk][3], bp[tm][2 * kk], bp[tm][2 * kk + 1]);
+                acc[cc][0] = fmaf(acc[cc][0], fa[0], d[0]);
+                acc[cc][1] = fmaf(acc[cc][1], fa[1], d[1]);
+                acc[cc][2] = fmaf(acc[cc][2], fa[0], d[2]);
+                acc[cc][3] = fmaf(acc[cc][3], fa[1], d[3]);
             }
             __syncwarp();  // every lane is done with this stage and the P^T buffer
             // refill this stage with the tile kStages ahead
@@ -622,27 +596,32 @@ __global__ void __launch_bounds__(32) split_warp_kernel(WarpArgs wa, LayerSrc sr
         if (unit_end && lane == 0) wa.unit_slots[2 * unit + 1] = slot;
         const int64_t p0 = slot * a.hpk;
         const float unscale = pow2i(-ew_prev);
+        if constexpr (PACK) {
+            // add the t2 columns' sums (lanes t4 ^ 2) to the t1 columns'
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+            for (int cc = 0; cc < 8; ++cc)
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                float lv = l[nt][cc];
-                lv += __shfl_xor_sync(0xffffffffu, lv, 4);
-                lv += __shfl_xor_sync(0xffffffffu, lv, 8);
-                lv += __shfl_xor_sync(0xffffffffu, lv, 16);
-                const int h = nt * 8 + 2 * t4 + cc;
-                if (h < a.hpk) {
-                    if (gl4 == 0) {
-                        a.pm[p0 + h] = m[nt][cc];
-                        a.pl[p0 + h] = lv;
-                    }
-                    float *dst = a.pacc + (p0 + h) * 128 + 2 * gl4;
+                for (int j = 0; j < 4; ++j) acc[cc][j] += __shfl_xor_sync(0xffffffffu, acc[cc][j], 2);
+        }
 #pragma unroll
-                    for (int ch = 0; ch < 8; ++ch)
-                        *reinterpret_cast<float2 *>(dst + 16 * ch) =
-                            make_float2(acc[ch][nt][cc] * unscale, acc[ch][nt][2 + cc] * unscale);
+        for (int cc = 0; cc < 2; ++cc) {
+            float lv = l[cc];
+            lv += __shfl_xor_sync(0xffffffffu, lv, 4);
+            lv += __shfl_xor_sync(0xffffffffu, lv, 8);
+            lv += __shfl_xor_sync(0xffffffffu, lv, 16);
+            const int h = hc0 + cc;
+            if (owner && h < a.hpk) {
+                if (gl4 == 0) {
+                    a.pm[p0 + h] = m[cc];
+                    a.pl[p0 + h] = lv;
                 }
+                float *dst = a.pacc + (p0 + h) * 128 + 2 * gl4;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch)
+                    *reinterpret_cast<float2 *>(dst + 16 * ch) =
+                        make_float2(acc[ch][cc] * unscale, acc[ch][2 + cc] * unscale);
             }
+        }
     }
 
     if (!ok) {
@@ -657,11 +636,11 @@ __global__ void __launch_bounds__(32) split_warp_kernel(WarpArgs wa, LayerSrc sr
     }
 }
 
-template <int NT>
+template <bool PACK>
 cudaError_t launch_split_warp(const WarpArgs &wa, const LayerSrc &s, const MmaMaps &maps,
                               cudaStream_t st) {
-    using C = WarpCfg<NT>;
-    auto kern = split_warp_kernel<NT>;
+    using C = WarpCfg<PACK>;
+    auto kern = split_warp_kernel<PACK>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     kern<<<unsigned(wa.G), 32, C::SMEM_ALLOC, st>>>(wa, s, maps);
@@ -669,16 +648,16 @@ cudaError_t launch_split_warp(const WarpArgs &wa, const LayerSrc &s, const MmaMa
 }
 
 // Workers of one launch on the current device: SMs x resident CTAs per SM.
-template <int NT>
+template <bool PACK>
 int64_t split_warp_workers() {
     int dev = 0, sms = 0, occ = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return 0;
-    auto kern = split_warp_kernel<NT>;
+    auto kern = split_warp_kernel<PACK>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             WarpCfg<NT>::SMEM_ALLOC) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 32, WarpCfg<NT>::SMEM_ALLOC) !=
+                             WarpCfg<PACK>::SMEM_ALLOC) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 32, WarpCfg<PACK>::SMEM_ALLOC) !=
             cudaSuccess)
         return 0;
     return int64_t(sms) * occ;

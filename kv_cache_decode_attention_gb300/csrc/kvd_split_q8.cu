@@ -19,26 +19,35 @@ cudaError_t split_layer_q8(int hd, int hpk_bucket, const SplitArgs &a, const Lay
     return cudaErrorInvalidValue;
 }
 
-// Tensor-core kernels for the q8_2f cache: heads in N for groups of up to 8
-// query heads, heads in M for groups of 9..16 (nt = 1, 2).
-cudaError_t split_layer_q8_warp(int nt, const WarpArgs &wa, const LayerSrc &s, const MmaMaps &maps,
-                                cudaStream_t st) {
-    if (nt == 1) return launch_split_warp<1>(wa, s, maps, st);
-    if (nt == 2) return launch_split_h16(wa, s, maps, st);
-    return cudaErrorInvalidValue;
+// Tensor-core kernels for the q8_2f cache by query heads per group:
+// variant 0 = up to 4 (terms packed in the columns), 1 = up to 8 (heads in
+// the columns), 2 = up to 16 (heads in the MMA rows).
+int q8_tc_variant(int hpk) { return hpk <= 4 ? 0 : hpk <= 8 ? 1 : 2; }
+
+cudaError_t split_layer_q8_tc(int variant, const WarpArgs &wa, const LayerSrc &s, const MmaMaps &maps,
+                              cudaStream_t st) {
+    switch (variant) {
+        case 0: return launch_split_warp<true>(wa, s, maps, st);
+        case 1: return launch_split_warp<false>(wa, s, maps, st);
+        case 2: return launch_split_h16(wa, s, maps, st);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
-// Workers (resident one-warp CTAs) of that kernel on the current device,
+// Workers (resident one-warp CTAs) of a variant on the current device,
 // cached per device; 0 if the query fails.
-int64_t split_q8_warp_workers(int nt) {
+int64_t split_q8_tc_workers(int variant) {
     constexpr int kMaxDev = 64;
     static std::mutex mu;
-    static int64_t cache[kMaxDev][2] = {};
+    static int64_t cache[kMaxDev][3] = {};
     int dev = 0;
-    if (nt < 1 || nt > 2 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+    if (variant < 0 || variant > 2 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
     std::lock_guard<std::mutex> lock(mu);
-    int64_t &w = cache[dev][nt - 1];
-    if (w == 0) w = nt == 1 ? split_warp_workers<1>() : split_h16_workers();
+    int64_t &w = cache[dev][variant];
+    if (w == 0) {
+        w = variant == 0 ? split_warp_workers<true>() : variant == 1 ? split_warp_workers<false>()
+                                                                     : split_h16_workers();
+    }
     return w;
 }
 
