@@ -41,6 +41,36 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one decode call
+# without imp -- the split kernel plus the run merge -- from one ncu capture of
+# this benchmark's roofline loop (command and figures in
+# profiles/decode_q8_gqa_traffic.md), valid while the kernel sources hash to
+# the captured version; reported as null otherwise.
+TRAFFIC = {
+    "q8_gqa": {"sources_sha256": "2f1a4308b45871f8ea0154ba1e530ec71f328a4b12250996987612e48659c224",
+               "bytes": 300522880},
+}
+
+
+def kernel_sources_sha256() -> str:
+    import hashlib
+
+    csrc = os.path.join(ROOT, "kv_cache_decode_attention_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload: str):
+    t = TRAFFIC.get(workload)
+    if not t or t["bytes"] is None or t["sources_sha256"] != kernel_sources_sha256():
+        return None
+    return t["bytes"]
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -281,12 +311,14 @@ def run_gpu(args, rank, world):
     #      workload and launch configuration, CUDA events on the launching stream)
     nrep = max(20, args.steps)
     dev_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nrep)]
+    torch.cuda.profiler.start()  # second profiled range: the decode calls of the roofline
     for j in range(nrep):
         w = wls[j % R]
         dev_ev[j][0].record(stream)
         kvd.decode_attention(qs[j % 8], w.layer, out=outs[j % R], imp=None, scale=w.scale, workspace=ws)
         dev_ev[j][1].record(stream)
     torch.cuda.synchronize()
+    torch.cuda.profiler.stop()
     k_ms = statistics.mean(a.elapsed_time(b) for a, b in dev_ev)
     lens_now = lengths_now()
     kbytes = statistics.mean(
@@ -360,7 +392,7 @@ def run_gpu(args, rank, world):
         "queries_per_s": round(wl0.n_seq * world / (ms_per_step * 1e-3), 1),
         "roofline": {"bound": "hbm", "kernel": "decode_attention (split + merge, imp off)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "frac": round(achieved / peak, 4), "traffic": measured_traffic(wl0.name),
                      "peak_kind": peak_kind, "ms_per_launch": round(k_ms, 5),
                      "bytes_per_launch": int(kbytes)},
         "decode_ms_in_step": round(statistics.mean(dec_ms), 5),

@@ -135,60 +135,75 @@ struct RunMergeArgs {
 // by the tensor-core kernel: out[d] = field[d] * sum_r acc_r[d] 2^(m_r - M) /
 // sum_r l_r 2^(m_r - M).  A unit's runs fill the slot range between the
 // first and last run slots the split kernel recorded for it, with empty
-// markers (max -inf) in skipped slots.  The four warps take every fourth
-// slot in one pass with a running maximum, lanes own four channels each, and
-// the warps' sums are rescaled to the common maximum and added in a fixed
-// order.
-__global__ void __launch_bounds__(128) merge_runs_kernel(RunMergeArgs a, MergeLayerSrc src) {
-    __shared__ float wmax[4], wsum[4];
-    __shared__ __align__(16) float wacc[4][128];
-    const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;  // d: output channel
-    const int warp = d >> 5, lane = d & 31;
+// markers (max -inf) in skipped slots.  Eight warps take every eighth slot,
+// loading four slots' (max, sum, accumulator) before using any (long units
+// have a hundred or more runs, so the loads must overlap); each keeps a
+// running maximum, lanes own four channels, and the warps' sums are rescaled
+// to the common maximum and added in a fixed order.
+constexpr int kMergeWarps = 8;
+constexpr int kMergeBatch = 4;
+
+__global__ void __launch_bounds__(32 * kMergeWarps) merge_runs_kernel(RunMergeArgs a, MergeLayerSrc src) {
+    __shared__ float wmax[kMergeWarps], wsum[kMergeWarps];
+    __shared__ __align__(16) float wacc[kMergeWarps][128];
+    const int h = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
+    const int warp = t >> 5, lane = t & 31;
     const int L = src.seq_len[b];
     const int grp = src.slot[h / a.hpk];
     float *o = a.out + (int64_t(b) * a.n_q + h) * 128;
     float *mlp = a.ml ? a.ml + (int64_t(b) * a.n_q + h) * 2 : nullptr;
     if (grp < 0 || L <= 0) {
-        o[d] = 0.0f;
-        if (mlp && d == 0) {
+        if (t < 128) o[t] = 0.0f;
+        if (mlp && t == 0) {
             mlp[0] = -INFINITY;
             mlp[1] = 0.0f;
         }
         return;
     }
-    const float vc = src.vcol ? src.vcol[(int64_t(b) * src.n_live + grp) * 128 + d] : 1.0f;
     const int64_t unit = int64_t(b) * src.n_live + grp;
     const int64_t first = a.unit_slots[2 * unit], last = a.unit_slots[2 * unit + 1];
     const int hh = h % a.hpk;
     const float *pmh = a.pm + hh, *plh = a.pl + hh, *pah = a.pacc + int64_t(hh) * 128 + 4 * lane;
-    // one pass per warp with a running maximum (every lane sees the same m)
     float M = -INFINITY, Ls = 0.0f;
     float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-#pragma unroll 4
-    for (int64_t sl = first + warp; sl <= last; sl += 4) {
-        const float m = pmh[sl * a.hpk];
-        const float pl = plh[sl * a.hpk];
-        const float4 v = *reinterpret_cast<const float4 *>(pah + sl * a.hpk * 128);
-        if (m == -INFINITY) continue;  // empty marker
-        if (m > M) {
-            const float r = exp2f(M - m);  // 0 while M is -inf
-            Ls *= r;
-            acc.x *= r;
-            acc.y *= r;
-            acc.z *= r;
-            acc.w *= r;
-            M = m;
+    for (int64_t s0 = first + warp; s0 <= last; s0 += kMergeWarps * kMergeBatch) {
+        float m[kMergeBatch], pl[kMergeBatch];
+        float4 v[kMergeBatch];
+#pragma unroll
+        for (int k = 0; k < kMergeBatch; ++k) {
+            const int64_t sl = s0 + int64_t(k) * kMergeWarps;
+            m[k] = -INFINITY;
+            if (sl <= last) {
+                m[k] = pmh[sl * a.hpk];
+                pl[k] = plh[sl * a.hpk];
+                v[k] = *reinterpret_cast<const float4 *>(pah + sl * a.hpk * 128);
+            }
         }
-        const float f = exp2f(m - M);
-        Ls = fmaf(pl, f, Ls);
-        acc.x = fmaf(v.x, f, acc.x);
-        acc.y = fmaf(v.y, f, acc.y);
-        acc.z = fmaf(v.z, f, acc.z);
-        acc.w = fmaf(v.w, f, acc.w);
+#pragma unroll
+        for (int k = 0; k < kMergeBatch; ++k) {
+            if (m[k] == -INFINITY) continue;  // past the range, or an empty marker
+            if (m[k] > M) {
+                const float r = exp2f(M - m[k]);  // 0 while M is -inf
+                Ls *= r;
+                acc.x *= r;
+                acc.y *= r;
+                acc.z *= r;
+                acc.w *= r;
+                M = m[k];
+            }
+            const float f = exp2f(m[k] - M);
+            Ls = fmaf(pl[k], f, Ls);
+            acc.x = fmaf(v[k].x, f, acc.x);
+            acc.y = fmaf(v[k].y, f, acc.y);
+            acc.z = fmaf(v[k].z, f, acc.z);
+            acc.w = fmaf(v[k].w, f, acc.w);
+        }
     }
     if (lane == 0) wmax[warp] = M;
     __syncthreads();
-    const float Mall = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
+    float Mall = wmax[0];
+#pragma unroll
+    for (int w = 1; w < kMergeWarps; ++w) Mall = fmaxf(Mall, wmax[w]);
     const float fw = exp2f(M - Mall);  // 0 for a warp that saw no run
     acc.x *= fw;
     acc.y *= fw;
@@ -197,11 +212,19 @@ __global__ void __launch_bounds__(128) merge_runs_kernel(RunMergeArgs a, MergeLa
     *reinterpret_cast<float4 *>(&wacc[warp][4 * lane]) = acc;
     if (lane == 0) wsum[warp] = Ls * fw;
     __syncthreads();
-    Ls = (wsum[0] + wsum[1]) + (wsum[2] + wsum[3]);
-    o[d] = ((wacc[0][d] + wacc[1][d]) + (wacc[2][d] + wacc[3][d])) / Ls * vc;
-    if (mlp && d == 0) {
-        mlp[0] = Mall;
-        mlp[1] = Ls;
+    if (t < 128) {
+        float sum = 0.0f, r = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kMergeWarps; ++w) {
+            sum += wsum[w];
+            r += wacc[w][t];
+        }
+        const float vc = src.vcol ? src.vcol[(int64_t(b) * src.n_live + grp) * 128 + t] : 1.0f;
+        o[t] = r / sum * vc;
+        if (mlp && t == 0) {
+            mlp[0] = Mall;
+            mlp[1] = sum;
+        }
     }
 }
 
@@ -219,14 +242,15 @@ struct ImpArgs {
 // imp[b][p] += sum over the live heads of sequence b of 2^(s - M) / L: the
 // softmax weight of every live query head on row p.  A block owns 256 rows of
 // one sequence: it stages the (max, 1/sum) of the sequence's live heads in
-// shared memory (in live order, head i = gl * hpk + hh), then its threads
-// split as 64 row quads x 4 head classes (i mod 4), each quad read as one
-// 16-byte load per head (a unit's scores start on a 16-row boundary and its
-// capacity is a multiple of 16 rows).  The four classes' sums are added in
-// a fixed order.
+// shared memory (in live order, head i = gl * hpk + hh) while its threads, 64
+// row quads x 4 head classes (i mod 4), already load their scores (one
+// 16-byte load per head: a unit's scores start on a 16-row boundary and its
+// capacity is a multiple of 16 rows) and the old imp values, so those loads
+// overlap.  The four classes' sums are added in a fixed order.
 constexpr int kImpThreads = 256;
 constexpr int kImpRows = 256;   // rows per block
 constexpr int kImpClasses = 4;  // head classes per row quad
+constexpr int kImpBatch = 8;    // score loads in flight per thread
 
 __global__ void __launch_bounds__(kImpThreads) imp_kernel(ImpArgs a) {
     extern __shared__ float mlinv[];  // [n_live * hpk][2]: max, 1/sum
@@ -244,27 +268,41 @@ __global__ void __launch_bounds__(kImpThreads) imp_kernel(ImpArgs a) {
         mlinv[2 * i] = M;
         mlinv[2 * i + 1] = Ls > 0.0f ? 1.0f / Ls : 0.0f;
     }
-    __syncthreads();
     const int quad = t % (kImpRows / 4), cls = t / (kImpRows / 4);
     const int p = p0 + 4 * quad;
+    const int r = p0 + t;
+    float *dst = a.imp + a.imp_base[b] + r;
+    const float old = r < L ? *dst : 0.0f;
+    // the scores of live head i start at row_base * hpk + i * cap
+    const float *sb = a.scores + a.row_base[b] * a.hpk + p;
     float add[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    if (p < L) {
-        // the scores of live head i start at row_base * hpk + i * cap
-        const float *sb = a.scores + a.row_base[b] * a.hpk + p;
-#pragma unroll 4
-        for (int i = cls; i < nh; i += kImpClasses) {
-            const float4 sv = *reinterpret_cast<const float4 *>(sb + int64_t(i) * cap);
-            const float M = mlinv[2 * i], il = mlinv[2 * i + 1];
-            add[0] += exp2f(sv.x - M) * il;
-            add[1] += exp2f(sv.y - M) * il;
-            add[2] += exp2f(sv.z - M) * il;
-            add[3] += exp2f(sv.w - M) * il;
+    float4 sv[kImpBatch];
+    auto load = [&](int i0) {
+#pragma unroll
+        for (int k = 0; k < kImpBatch; ++k) {
+            const int i = i0 + k * kImpClasses;
+            if (p < L && i < nh) sv[k] = *reinterpret_cast<const float4 *>(sb + int64_t(i) * cap);
+        }
+    };
+    load(cls);        // the first batch is in flight across the barrier
+    __syncthreads();  // the staged maxima and sums are visible
+    for (int i0 = cls; i0 < nh; i0 += kImpClasses * kImpBatch) {
+        if (i0 != cls) load(i0);
+#pragma unroll
+        for (int k = 0; k < kImpBatch; ++k) {
+            const int i = i0 + k * kImpClasses;
+            if (p < L && i < nh) {
+                const float M = mlinv[2 * i], il = mlinv[2 * i + 1];
+                add[0] += exp2f(sv[k].x - M) * il;
+                add[1] += exp2f(sv[k].y - M) * il;
+                add[2] += exp2f(sv[k].z - M) * il;
+                add[3] += exp2f(sv[k].w - M) * il;
+            }
         }
     }
     *reinterpret_cast<float4 *>(&part[cls][4 * quad]) = make_float4(add[0], add[1], add[2], add[3]);
     __syncthreads();
-    const int r = p0 + t;
-    if (r < L) a.imp[a.imp_base[b] + r] += (part[0][t] + part[1][t]) + (part[2][t] + part[3][t]);
+    if (r < L) *dst = old + ((part[0][t] + part[1][t]) + (part[2][t] + part[3][t]));
 }
 
 // ---------------------------------------------------------------- R-SWA copies
@@ -421,7 +459,7 @@ extern "C" kvd_status decode_attention(const float *q, const kvd_layer *L, int32
         rm.n_q = n_q;
         rm.hpk = hpk;
         rm.unit_slots = wa.unit_slots;
-        merge_runs_kernel<<<dim3(unsigned(n_q), unsigned(l->n_seq)), 128, 0, st>>>(rm, ms);
+        merge_runs_kernel<<<dim3(unsigned(n_q), unsigned(l->n_seq)), 32 * kMergeWarps, 0, st>>>(rm, ms);
         if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
     } else {
         if (max_len > 0 && l->n_live > 0) {
