@@ -349,6 +349,67 @@ int kvo_attend_group(const kvo_cache *c, const float *q_group, int kv_head, int 
     return n;
 }
 
+/* cortiq attend_group_upto with its three options, for every stored row
+ * (upto = all), in f64:
+ *   - only rows [first, stored) are scored, first clamped to stored - 1 (the
+ *     earliest visible position; sliding-window layers pass stored - window);
+ *     earlier rows have probability 0 and their imp entries are untouched;
+ *   - softcap > 0: every computed score (scale * <q, K^_p>) becomes
+ *     softcap * tanh(score / softcap) before the softmax (Gemma-2 logit
+ *     soft-capping); a sink is not a score and is not capped;
+ *   - sinks (NULL = none): one logit per head joins the softmax maximum and
+ *     adds exp(sink - max) to the denominator; it has no value row (the same
+ *     as appending a value-less column).
+ * out = sum_p w_p V^_p with w_p = exp(s_p - m) / (sum_q exp(s_q - m) +
+ * [exp(z - m)]), m = max(max_p s_p, [z]); imp[p] += w_p over the heads.  A
+ * dead or empty group yields zeros and leaves imp untouched. */
+int kvo_attend_group_ex(const kvo_cache *c, const float *q_group, int kv_head, int nheads,
+                        float scale, int first, float softcap, const float *sinks,
+                        double *out, double *imp)
+{
+    int hd = c->hd, stored = c->head_rows[kv_head];
+    if (stored == 0) {
+        for (int i = 0; i < nheads * hd; ++i) out[i] = 0.0;
+        return 0;
+    }
+    if (first > stored - 1) first = stored - 1;
+    if (first < 0) first = 0;
+    int span = stored - first;
+    double *s = (double *)malloc(sizeof(double) * (size_t)span);
+    double *r = (double *)malloc(sizeof(double) * (size_t)hd);
+    for (int h = 0; h < nheads; ++h) {
+        const float *q = q_group + (size_t)h * hd;
+        double *o = out + (size_t)h * hd;
+        double m = -INFINITY;
+        for (int p = first; p < stored; ++p) {
+            kvo_row(c, kv_head, p, 0, r);
+            double dot = 0.0;
+            for (int d = 0; d < hd; ++d) dot += (double)q[d] * r[d];
+            double v = (double)scale * dot;
+            if (softcap > 0.0f) v = (double)softcap * tanh(v / (double)softcap);
+            s[p - first] = v;
+            if (v > m) m = v;
+        }
+        if (sinks && (double)sinks[h] > m) m = (double)sinks[h];
+        double z = 0.0;
+        for (int i = 0; i < span; ++i) {
+            s[i] = exp(s[i] - m);
+            z += s[i];
+        }
+        if (sinks) z += exp((double)sinks[h] - m);
+        for (int d = 0; d < hd; ++d) o[d] = 0.0;
+        for (int p = first; p < stored; ++p) {
+            double w = s[p - first] / z;
+            if (imp) imp[p] += w;
+            kvo_row(c, kv_head, p, 1, r);
+            for (int d = 0; d < hd; ++d) o[d] += w * r[d];
+        }
+    }
+    free(r);
+    free(s);
+    return stored;
+}
+
 /* cortiq memory_bytes restricted to the stored K/V state: every f32
  * (rows, scales, fields) counts 4 bytes, every int8 code 1 byte. */
 long long kvo_memory_bytes(const kvo_cache *c)

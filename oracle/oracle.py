@@ -64,6 +64,8 @@ def lib():
             L.kvo_row.restype = None
             L.kvo_attend_head.argtypes = [C.POINTER(_Cache), vp, i32, f32, vp, vp]
             L.kvo_attend_group.argtypes = [C.POINTER(_Cache), vp, i32, i32, f32, vp, vp]
+            L.kvo_attend_group_ex.argtypes = [C.POINTER(_Cache), vp, i32, i32, f32, i32, f32, vp, vp,
+                                              vp]
             L.kvo_memory_bytes.argtypes = [C.POINTER(_Cache)]
             L.kvo_memory_bytes.restype = C.c_longlong
             L.kvo_rswa_write.argtypes = [i32, i32, i32, vp, vp, vp, vp, i32, vp, vp]
@@ -195,6 +197,36 @@ class OracleSeqCache:
             assert imp.dtype == np.float64 and imp.flags.c_contiguous
         lib().kvo_attend_group(C.byref(self._s), _p(q_group), kv_head, nheads, scale,
                                _p(out), _p(imp))
+        return out
+
+    def attend_group_ex(self, q_group, kv_head: int, scale: float, first: int = 0,
+                        softcap: float = 0.0, sinks=None, imp=None):
+        """attend_group with a first visible row, logit soft-capping and learned
+        sink logits (one per head of the group, or None)."""
+        q_group = np.ascontiguousarray(q_group, dtype=np.float32)
+        nheads = q_group.size // self.hd
+        out = np.zeros((nheads, self.hd), np.float64)
+        if imp is not None:
+            assert imp.dtype == np.float64 and imp.flags.c_contiguous
+        sk = None if sinks is None else np.ascontiguousarray(sinks, dtype=np.float32)
+        assert sk is None or sk.size == nheads
+        lib().kvo_attend_group_ex(C.byref(self._s), _p(q_group), kv_head, nheads, scale, int(first),
+                                  float(softcap), _p(sk), _p(out), _p(imp))
+        return out
+
+    def decode_ex(self, q, n_q: int, scale: float, window: int = 0, softcap: float = 0.0,
+                  sinks=None, imp=None):
+        """decode with a sliding window (first = stored - window when stored >
+        window; 0 = no window), soft-capping and per-query-head sinks [n_q]."""
+        hpk = n_q // self.n_kv
+        q = np.ascontiguousarray(q, dtype=np.float32).reshape(n_q, self.hd)
+        out = np.zeros((n_q, self.hd), np.float64)
+        for g in range(self.n_kv):
+            stored = int(self.head_rows[g])
+            first = stored - window if window > 0 and stored > window else 0
+            sk = None if sinks is None else np.asarray(sinks, np.float32)[g * hpk:(g + 1) * hpk]
+            out[g * hpk:(g + 1) * hpk] = self.attend_group_ex(q[g * hpk:(g + 1) * hpk], g, scale, first,
+                                                              softcap, sk, imp)
         return out
 
     def decode(self, q, n_q: int, scale: float, imp=None):

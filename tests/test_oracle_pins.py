@@ -373,6 +373,126 @@ def test_closed_forms_single_key_and_equal_scores():
     assert np.allclose(out, 3.0, rtol=0, atol=1e-15) and np.allclose(p, 0.5)
 
 
+# ------------------------------------------- window / softcap / sinks options
+
+def _ex_cache(mode=oracle.F32, L=40, hd=32, n_kv=2, seed=81):
+    c = oracle.OracleSeqCache(mode, n_kv, hd, L)
+    c.append_rows(synthetic.normal((L, n_kv, hd), seed), synthetic.normal((L, n_kv, hd), seed + 1))
+    return c
+
+
+def test_ex_defaults_equal_attend_group():
+    """first = 0, no cap, no sinks is [cortiq] attend_group itself, bit for bit."""
+    for mode in (oracle.F32, oracle.Q8):
+        c = _ex_cache(mode)
+        q = synthetic.normal((3, 32), 91)
+        i1, i2 = np.zeros(40), np.zeros(40)
+        a = c.attend_group(q, 1, f32(0.2), i1)
+        b = c.attend_group_ex(q, 1, f32(0.2), 0, 0.0, None, i2)
+        assert np.array_equal(a, b) and np.array_equal(i1, i2)
+
+
+def test_sink_single_row_closed_form():
+    """[cortiq] attend_group_upto: one stored row and a sink z: the row gets
+    e^s / (e^s + e^z) of the mass, the sink's share has no value row."""
+    c = oracle.OracleSeqCache(oracle.F32, 1, 8, 2)
+    k = np.array([[[0.5, -1.0, 0.25, 2.0, 0.0, 1.0, -0.5, 0.75]]], f32)
+    v = np.array([[[1.0, 2.0, 3.0, 4.0, 5.0, 6.0, 7.0, 8.0]]], f32)
+    c.append_rows(k, v)
+    q = np.array([[1.0, 0.5, -2.0, 0.25, 3.0, -1.0, 0.5, 1.0]], f32)
+    sc, z = f32(0.35), f32(-0.8)
+    s = float(sc) * float(np.dot(q[0].astype(np.float64), k[0, 0].astype(np.float64)))
+    share = math.exp(s) / (math.exp(s) + math.exp(float(z)))
+    imp = np.zeros(2)
+    out = c.attend_group_ex(q, 0, sc, 0, 0.0, np.array([z]), imp)
+    assert np.allclose(out[0], share * v[0, 0].astype(np.float64), rtol=1e-14, atol=0)
+    assert abs(imp[0] - share) < 1e-15 and imp[1] == 0.0
+
+
+def test_sink_scales_output_by_visible_mass():
+    """A sink only adds to the denominator: out_sink = out_plain * (visible
+    mass), and that mass is what imp receives; a sink far below every score
+    changes nothing."""
+    c = _ex_cache(oracle.Q8, L=50, seed=95)
+    q = synthetic.normal((4, 32), 96)
+    plain = c.attend_group_ex(q, 0, f32(0.3))
+    sinks = np.array([0.5, -2.0, 3.0, 0.0], f32)
+    for h in range(4):
+        imp = np.zeros(50)
+        o = c.attend_group_ex(q[h:h + 1], 0, f32(0.3), 0, 0.0, sinks[h:h + 1], imp)
+        mass = imp.sum()
+        assert 0.0 < mass < 1.0
+        assert np.allclose(o[0], plain[h] * mass, rtol=1e-12, atol=1e-15)
+    far = c.attend_group_ex(q, 0, f32(0.3), 0, 0.0, np.full(4, -1e4, f32))
+    assert np.array_equal(far, plain)
+
+
+def test_window_equals_the_visible_suffix():
+    """[cortiq] attend_group_upto: rows before `first` get probability 0, so the
+    result equals attending a cache that holds only rows [first, stored); their
+    imp entries are untouched."""
+    L, f, hd = 40, 13, 32
+    k = synthetic.normal((L, 2, hd), 97)
+    v = synthetic.normal((L, 2, hd), 98)
+    full = oracle.OracleSeqCache(oracle.F32, 2, hd, L)
+    full.append_rows(k, v)
+    tail = oracle.OracleSeqCache(oracle.F32, 2, hd, L)
+    tail.append_rows(np.ascontiguousarray(k[f:]), np.ascontiguousarray(v[f:]))
+    q = synthetic.normal((3, hd), 99)
+    imp = np.full(L, 0.5)
+    imp_t = np.zeros(L)
+    out = full.attend_group_ex(q, 1, f32(0.25), f, 0.0, None, imp)
+    ref = tail.attend_group(q, 1, f32(0.25), imp_t)
+    assert np.allclose(out, ref, rtol=1e-13, atol=1e-15)
+    assert np.all(imp[:f] == 0.5)
+    assert np.allclose(imp[f:] - 0.5, imp_t[:L - f], rtol=1e-12, atol=1e-15)
+
+
+def test_window_clamps_to_the_last_row():
+    """first >= stored is clamped to stored - 1: the last row alone, weight 1."""
+    c = _ex_cache(oracle.F32, L=10, hd=32)
+    q = synthetic.normal((2, 32), 100)
+    imp = np.zeros(10)
+    out = c.attend_group_ex(q, 0, f32(0.5), 25, 0.0, None, imp)
+    last = c.dequant(0, True)[9]
+    assert np.allclose(out, np.stack([last, last]), rtol=0, atol=1e-15)
+    assert imp[:9].sum() == 0.0 and abs(imp[9] - 2.0) < 1e-15
+
+
+def test_softcap_two_rows_closed_form():
+    """The cap applies to the scaled score: with two rows the weight ratio is
+    exp(c tanh(s1 / c) - c tanh(s2 / c)), s = scale * <q, k>."""
+    c = oracle.OracleSeqCache(oracle.F32, 1, 4, 2)
+    k = np.array([[[2.0, 0.0, 1.0, 0.0]], [[-1.0, 3.0, 0.0, 0.5]]], f32)
+    c.append_rows(k, np.ones((2, 1, 4), f32))
+    q = np.array([[1.5, -0.5, 2.0, 1.0]], f32)
+    sc, cap = f32(0.9), 1.25
+    s = [float(sc) * float(np.dot(q[0].astype(np.float64), k[i, 0].astype(np.float64))) for i in range(2)]
+    imp = np.zeros(2)
+    c.attend_group_ex(q, 0, sc, 0, cap, None, imp)
+    want = math.exp(cap * math.tanh(s[0] / cap) - cap * math.tanh(s[1] / cap))
+    assert abs(imp[0] / imp[1] - want) < 1e-12 * want
+
+
+def test_softcap_limits_and_bound():
+    """Gemma-2 soft-capping: a huge cap is the plain softmax; a small cap keeps
+    every score inside (-c, c), so no two weights differ by more than e^(2c),
+    which the uncapped scores here exceed by far."""
+    c = _ex_cache(oracle.F32, L=30, hd=32, seed=101)
+    q = (synthetic.normal((2, 32), 102) * 8.0).astype(f32)
+    plain_imp, big_imp = np.zeros(30), np.zeros(30)
+    plain = c.attend_group_ex(q, 1, f32(0.4), 0, 0.0, None, plain_imp)
+    big = c.attend_group_ex(q, 1, f32(0.4), 0, 1e7, None, big_imp)
+    assert np.allclose(big, plain, rtol=1e-9, atol=1e-12)
+    cap = 0.75
+    for h in range(2):
+        imp_c, imp_p = np.zeros(30), np.zeros(30)
+        c.attend_group_ex(q[h:h + 1], 1, f32(0.4), 0, cap, None, imp_c)
+        c.attend_group_ex(q[h:h + 1], 1, f32(0.4), 0, 0.0, None, imp_p)
+        assert imp_c.max() / imp_c.min() <= math.exp(2 * cap) * (1 + 1e-12)
+        assert imp_p.max() / imp_p.min() > math.exp(2 * cap) * 10
+
+
 # ------------------------------------------------------------------- R-SWA
 
 H, HD, W = 10, 128, 128
