@@ -162,6 +162,28 @@ KVD_API kvd_status decode_attention(const float *q, const kvd_layer *L, int32_t 
                             float *out, float *imp, void *workspace, int64_t workspace_bytes,
                             void *stream);
 
+/* decode_attention with the options of cortiq attend_group_upto (docs.rs
+ * cortiq-engine 0.8.49, kv_cache.rs, attend_group / attend_group_upto):
+ *   window   >= 0; 0 = every stored row.  Otherwise sequence b (L_b rows)
+ *            sees rows [first_b, L_b) with first_b = L_b - window when L_b >
+ *            window, else 0 -- the page's `first` as sliding-window layers
+ *            pass it; earlier rows get probability 0 and their imp entries
+ *            are left unchanged;
+ *   softcap  >= 0, finite; > 0 replaces every computed score s = scale *
+ *            <q, K^> by softcap * tanh(s / softcap) before the softmax
+ *            (logit soft-capping; the sink is not capped);
+ *   sinks    device f32 [n_q] or NULL: a learned sink logit per query head
+ *            that joins the softmax maximum and adds exp(sink - max) to its
+ *            denominator, with no value row (so the rows' weights, out and
+ *            imp shrink by the sink's share).
+ * Every other argument, the workspace size and the errors are those of
+ * decode_attention, which is this call with window 0, softcap 0 and no
+ * sinks.  Returns KVD_EINVAL for a negative window, a negative or
+ * non-finite softcap, or a misaligned sinks pointer. */
+KVD_API kvd_status decode_attention_ex(const float *q, const kvd_layer *L, int32_t n_q, float scale,
+                               int64_t window, float softcap, const float *sinks, float *out,
+                               float *imp, void *workspace, int64_t workspace_bytes, void *stream);
+
 /* decode_attention for callers that cannot allocate device memory (the pages
  * have no counterpart: this is a deployment variant).  Some callers cannot
  * call cudaMalloc on their decode path -- an inference runtime that hands out

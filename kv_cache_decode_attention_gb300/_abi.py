@@ -44,6 +44,7 @@ _SIGS = {
     "kv_freeze_colfield": [_P(kvd_layer), _vp],
     "kvd_decode_workspace_bytes": [_P(kvd_layer), _i32, _i32, _P(_i64)],
     "decode_attention": [_vp, _P(kvd_layer), _i32, _f32, _vp, _vp, _vp, _i64, _vp],
+    "decode_attention_ex": [_vp, _P(kvd_layer), _i32, _f32, _i64, _f32, _vp, _vp, _vp, _vp, _i64, _vp],
     "decode_attention_static": [_vp, _P(kvd_layer), _i32, _f32, _vp, _vp],
     "kvd_layer_device_error": [_P(kvd_layer), _i32, _P(C.c_uint32)],
     "rswa_record_prefill": [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i64, _i32,

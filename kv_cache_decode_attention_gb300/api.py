@@ -171,8 +171,13 @@ def kv_freeze_colfield(layer: LayerKvCache, stream=None):
 
 def decode_attention(q: torch.Tensor, cache: LayerKvCache, out: torch.Tensor | None = None,
                      imp: torch.Tensor | None = None, scale: float | None = None,
-                     workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """q [n_seq, n_q, hd] -> out [n_seq, n_q, hd]; imp (float32 [imp_len]) accumulates."""
+                     workspace: torch.Tensor | None = None, stream=None, window: int = 0,
+                     softcap: float = 0.0, sinks: torch.Tensor | None = None) -> torch.Tensor:
+    """q [n_seq, n_q, hd] -> out [n_seq, n_q, hd]; imp (float32 [imp_len]) accumulates.
+
+    window > 0 keeps each sequence's last `window` rows; softcap > 0 caps the
+    scores as softcap * tanh(s / softcap); sinks (float32 [n_q]) adds one
+    learned sink logit per query head to the softmax (decode_attention_ex)."""
     _f32_cuda(q, "q")
     n_q = q.numel() // (cache.n_seq * cache.head_dim)
     if q.numel() != cache.n_seq * n_q * cache.head_dim:
@@ -189,8 +194,17 @@ def decode_attention(q: torch.Tensor, cache: LayerKvCache, out: torch.Tensor | N
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     if scale is None:
         scale = 1.0 / math.sqrt(cache.head_dim)
-    _abi.call("decode_attention", _ptr(q), C.byref(cache.L), int(n_q), C.c_float(scale),
-              _ptr(out), _ptr(imp), _ptr(workspace), int(workspace.numel()), _stream(stream))
+    if window or softcap or sinks is not None:
+        if sinks is not None:
+            _f32_cuda(sinks, "sinks")
+            if sinks.numel() != n_q:
+                raise ValueError("sinks must hold one logit per query head (%d)" % n_q)
+        _abi.call("decode_attention_ex", _ptr(q), C.byref(cache.L), int(n_q), C.c_float(scale),
+                  int(window), C.c_float(softcap), _ptr(sinks), _ptr(out), _ptr(imp), _ptr(workspace),
+                  int(workspace.numel()), _stream(stream))
+    else:
+        _abi.call("decode_attention", _ptr(q), C.byref(cache.L), int(n_q), C.c_float(scale),
+                  _ptr(out), _ptr(imp), _ptr(workspace), int(workspace.numel()), _stream(stream))
     return out
 
 

@@ -128,6 +128,7 @@ struct RunMergeArgs {
     const int64_t *unit_slots;    // [n_seq * n_live][2]: first and last run slot of each unit
     float *out;                   // [n_seq][n_q][128]
     float *ml;                    // (max, sum) per (sequence, query head) for imp, or null
+    const float *sinks;           // learned sink logit per query head [n_q], or null
     int32_t n_q, hpk;
 };
 
@@ -203,7 +204,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_runs_kernel(RunMergeAr
     __syncthreads();
     float Mall = wmax[0];
 #pragma unroll
-    for (int w = 1; w < kMergeWarps; ++w) Mall = fmaxf(Mall, wmax[w]);
+    for (int w = 1; w < kMergeWarps; ++w) Mall = fmaxf(Mall, wmax[w]);  // finite: L >= 1
     const float fw = exp2f(M - Mall);  // 0 for a warp that saw no run
     acc.x *= fw;
     acc.y *= fw;
@@ -218,6 +219,14 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_runs_kernel(RunMergeAr
         for (int w = 0; w < kMergeWarps; ++w) {
             sum += wsum[w];
             r += wacc[w][t];
+        }
+        if (a.sinks) {
+            // a learned sink joins the maximum and the sum; it has no value row
+            const float z = a.sinks[h] * kLog2e;
+            const float Mf = fmaxf(Mall, z), f = exp2f(Mall - Mf);
+            sum = fmaf(sum, f, exp2f(z - Mf));
+            r *= f;
+            Mall = Mf;
         }
         const float vc = src.vcol ? src.vcol[(int64_t(b) * src.n_live + grp) * 128 + t] : 1.0f;
         o[t] = r / sum * vc;
@@ -236,6 +245,7 @@ struct ImpArgs {
     float *imp;
     const int64_t *row_base, *cap, *imp_base;
     const int32_t *seq_len, *live;
+    int64_t window;  // sliding window in rows (0 = none): rows before the first visible one are untouched
     int32_t n_q, hpk, n_live;
 };
 
@@ -257,7 +267,9 @@ __global__ void __launch_bounds__(kImpThreads) imp_kernel(ImpArgs a) {
     __shared__ __align__(16) float part[kImpClasses][kImpRows];
     const int b = blockIdx.y, t = threadIdx.x;
     const int L = a.seq_len[b];
-    const int p0 = blockIdx.x * kImpRows;
+    // blocks cover the visible rows, from the first one rounded down to 16
+    const int first = int(first_visible(L, a.window));
+    const int p0 = first / kRowAlign * kRowAlign + blockIdx.x * kImpRows;
     if (p0 >= L) return;
     const int nh = a.n_live * a.hpk;
     const int64_t cap = a.cap[b];
@@ -271,8 +283,9 @@ __global__ void __launch_bounds__(kImpThreads) imp_kernel(ImpArgs a) {
     const int quad = t % (kImpRows / 4), cls = t / (kImpRows / 4);
     const int p = p0 + 4 * quad;
     const int r = p0 + t;
+    const bool mine = r < L && r >= first;
     float *dst = a.imp + a.imp_base[b] + r;
-    const float old = r < L ? *dst : 0.0f;
+    const float old = mine ? *dst : 0.0f;
     // the scores of live head i start at row_base * hpk + i * cap
     const float *sb = a.scores + a.row_base[b] * a.hpk + p;
     float add[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -302,7 +315,7 @@ __global__ void __launch_bounds__(kImpThreads) imp_kernel(ImpArgs a) {
     }
     *reinterpret_cast<float4 *>(&part[cls][4 * quad]) = make_float4(add[0], add[1], add[2], add[3]);
     __syncthreads();
-    if (r < L) *dst = old + ((part[0][t] + part[1][t]) + (part[2][t] + part[3][t]));
+    if (mine) *dst = old + ((part[0][t] + part[1][t]) + (part[2][t] + part[3][t]));
 }
 
 // ---------------------------------------------------------------- R-SWA copies
@@ -375,11 +388,21 @@ extern "C" kvd_status kvd_decode_workspace_bytes(const kvd_layer *L, int32_t n_q
 extern "C" kvd_status decode_attention(const float *q, const kvd_layer *L, int32_t n_q, float scale,
                                        float *out, float *imp, void *workspace,
                                        int64_t workspace_bytes, void *stream) {
+    return decode_attention_ex(q, L, n_q, scale, 0, 0.0f, nullptr, out, imp, workspace, workspace_bytes,
+                               stream);
+}
+
+extern "C" kvd_status decode_attention_ex(const float *q, const kvd_layer *L, int32_t n_q, float scale,
+                                          int64_t window, float softcap, const float *sinks, float *out,
+                                          float *imp, void *workspace, int64_t workspace_bytes,
+                                          void *stream) {
     const Layer *l = checked_layer(L);
     if (l == nullptr || q == nullptr || out == nullptr) return KVD_EINVAL;
     if (n_q < l->n_kv || n_q % l->n_kv != 0 || n_q / l->n_kv > kMaxHpk) return KVD_EINVAL;
     if (!std::isfinite(scale)) return KVD_EINVAL;
-    if (!aligned16(q) || !aligned16(out) || (imp && (reinterpret_cast<uintptr_t>(imp) & 3)))
+    if (window < 0 || !std::isfinite(softcap) || softcap < 0.0f) return KVD_EINVAL;
+    if (!aligned16(q) || !aligned16(out) || (imp && (reinterpret_cast<uintptr_t>(imp) & 3)) ||
+        (sinks && (reinterpret_cast<uintptr_t>(sinks) & 3)))
         return KVD_EINVAL;
     const DecodeWs w = decode_ws(l, n_q, imp != nullptr);
     if (w.total < 0) return KVD_ECUDA;
@@ -390,10 +413,13 @@ extern "C" kvd_status decode_attention(const float *q, const kvd_layer *L, int32
     cudaStream_t st = as_stream(stream);
     char *ws = static_cast<char *>(workspace);
 
+    // rows from each sequence's first visible row rounded down to kRowAlign
     int64_t work = 0, max_len = 0;
     for (int b = 0; b < l->n_seq; ++b) {
-        work += l->h_seq_len[b] * int64_t(l->n_live);
-        max_len = std::max(max_len, l->h_seq_len[b]);
+        const int64_t Lb = l->h_seq_len[b];
+        const int64_t vis = Lb - first_visible(Lb, window) / kRowAlign * kRowAlign;
+        work += vis * int64_t(l->n_live);
+        max_len = std::max(max_len, vis);
     }
     const int32_t chunk = pick_chunk(work);
 
@@ -410,6 +436,8 @@ extern "C" kvd_status decode_attention(const float *q, const kvd_layer *L, int32
     a.pacc = reinterpret_cast<float *>(ws + w.pacc);
     a.scores = imp ? reinterpret_cast<float *>(ws + w.scores) : nullptr;
     a.err = l->d_err;
+    a.window = window;
+    a.softcap2 = softcap * kLog2e;
 
     LayerSrc s;
     s.kf = static_cast<const float *>(l->buf[KVD_BUF_K]);
@@ -434,7 +462,7 @@ extern "C" kvd_status decode_attention(const float *q, const kvd_layer *L, int32
     if (warp_path(l)) {
         // tensor-core kernel over balanced tile ranges, then the run merge
         int64_t T = 0;
-        for (int b = 0; b < l->n_seq; ++b) T += int64_t(l->n_live) * ceil_div(l->h_seq_len[b], kWR);
+        for (int b = 0; b < l->n_seq; ++b) T += int64_t(l->n_live) * tiles_of(l->h_seq_len[b], window);
         const int variant = q8_tc_variant(hpk);
         const int64_t workers = split_q8_tc_workers(variant);
         if (workers <= 0) return KVD_ECUDA;
@@ -459,6 +487,7 @@ extern "C" kvd_status decode_attention(const float *q, const kvd_layer *L, int32
         rm.n_q = n_q;
         rm.hpk = hpk;
         rm.unit_slots = wa.unit_slots;
+        rm.sinks = sinks;
         merge_runs_kernel<<<dim3(unsigned(n_q), unsigned(l->n_seq)), 32 * kMergeWarps, 0, st>>>(rm, ms);
         if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
     } else {
@@ -485,6 +514,8 @@ extern "C" kvd_status decode_attention(const float *q, const kvd_layer *L, int32
         m.n_grp = a.n_grp;
         m.nc_max = w.nc_max;
         m.chunk = chunk;
+        m.sinks = sinks;
+        m.window = window;
         dim3 mgrid(unsigned(n_q), unsigned(l->n_seq));
         if (l->hd == 128) merge_layer_kernel<128><<<mgrid, 128, 0, st>>>(m, ms);
         else merge_layer_kernel<64><<<mgrid, 64, 0, st>>>(m, ms);
@@ -505,6 +536,7 @@ extern "C" kvd_status decode_attention(const float *q, const kvd_layer *L, int32
         ia.n_q = n_q;
         ia.hpk = hpk;
         ia.n_live = l->n_live;
+        ia.window = window;
         dim3 igrid(unsigned(ceil_div(max_len, kImpRows)), unsigned(l->n_seq));
         const size_t ml_bytes = size_t(std::max(1, l->n_live * hpk)) * 2 * sizeof(float);
         if (ml_bytes > 40 * 1024 &&

@@ -67,6 +67,17 @@ struct SplitCfg : TileCfg<HD, KQ, VQ> {
     static_assert((1 << LOGE) == E, "reduce entries must be a power of two");
 };
 
+// First visible row of a sequence holding L rows under a sliding window of
+// `window` rows (0 = no window): cortiq attend_group_upto's `first` when the
+// caller passes stored - window.  Always <= L - 1 for L >= 1.
+__host__ __device__ __forceinline__ int64_t first_visible(int64_t L, int64_t window) {
+    return window > 0 && L > window ? L - window : 0;
+}
+
+// Softcap in the log2 domain: scores s2 = s * log2(e) are capped as
+// c2 * tanh(s2 / c2) with c2 = softcap * log2(e), the same as capping s.
+__device__ __forceinline__ float softcap_log2(float s2, float c2) { return c2 * tanhf(s2 / c2); }
+
 // Arguments common to every split launch.
 struct SplitArgs {
     const float *q;        // [.., n_q, HD] query rows
@@ -78,12 +89,15 @@ struct SplitArgs {
     float *pm, *pl, *pacc; // partial max, sum, accumulator
     float *scores;         // per-row log2 scores for the imp pass, or null
     uint32_t *err;
+    int64_t window = 0;      // sliding window in rows (0 = none)
+    float softcap2 = 0.0f;   // softcap * log2(e) (0 = none)
 };
 
 // Where one CTA's chunk lives.
 struct ChunkInfo {
     const char *k, *v, *ks, *vs;  // global address of the chunk's first row
     int n;                        // rows in the chunk (>= 1)
+    int lo;                       // rows of the chunk before the first visible one
     int64_t pidx0;                // partial index of the group's head 0
     const float *q;               // query of the group's head 0
     const float *kcol;            // K field of the group, or null
@@ -253,9 +267,10 @@ __device__ void split_body(const ChunkInfo &ci, const SplitArgs &a, char *smem) 
             if ((lane & ((32 >> C::LOGE) - 1)) == 0) {
                 const int e = lane >> (5 - C::LOGE);
                 const int r = rbase + e / HPK, h = e % HPK;
-                const float sv = r < nt ? s : -INFINITY;
+                const bool vis = r < nt && row0 + r >= ci.lo;
+                const float sv = vis ? (a.softcap2 > 0.0f ? softcap_log2(s, a.softcap2) : s) : -INFINITY;
                 sc[r * HPK + h] = sv;
-                if (a.scores != nullptr && r < nt && h < a.hpk)
+                if (a.scores != nullptr && vis && h < a.hpk)
                     a.scores[ci.score0 + h * ci.score_ld + row0 + r] = sv;
             }
         }
@@ -399,7 +414,11 @@ __global__ void __launch_bounds__(kThreads, 2) split_layer_kernel(SplitArgs a, L
     extern __shared__ __align__(128) char smem[];
     const int b = blockIdx.z, gl = blockIdx.y, c = blockIdx.x;
     const int L = src.seq_len[b];
-    const int64_t r0 = int64_t(c) * a.chunk;
+    // chunks start at the first visible row rounded down to kRowAlign (the
+    // bulk copies' alignment); the rows before it are masked in chunk 0
+    const int64_t first = first_visible(L, a.window);
+    const int64_t f0 = first / kRowAlign * kRowAlign;
+    const int64_t r0 = f0 + int64_t(c) * a.chunk;
     if (r0 >= L) return;
     const int64_t cap = src.cap[b];
     if (L > cap) {
@@ -408,6 +427,7 @@ __global__ void __launch_bounds__(kThreads, 2) split_layer_kernel(SplitArgs a, L
     }
     const int64_t row = src.row_base[b] + int64_t(gl) * cap + r0;
     ChunkInfo ci;
+    ci.lo = int(first - r0 > 0 ? first - r0 : 0);
     ci.k = KQ ? reinterpret_cast<const char *>(src.kq + row * HD)
               : reinterpret_cast<const char *>(src.kf + row * HD);
     ci.v = VQ ? reinterpret_cast<const char *>(src.vq + row * HD)
@@ -466,6 +486,7 @@ __global__ void __launch_bounds__(kThreads, 2) split_rswa_kernel(SplitArgs a, Rs
         return;
     }
     ci.ks = ci.vs = nullptr;
+    ci.lo = 0;
     ci.pidx0 = (head * a.nc_max + c) * 1;
     ci.q = a.q + head * HD;
     ci.kcol = nullptr;
@@ -480,6 +501,8 @@ struct MergeArgs {
     const float *pm, *pl, *pacc;
     float *out;     // [.., n_q, HD]
     float *ml;      // (max, sum) per (sequence, query head) for the imp pass, or null
+    const float *sinks = nullptr;  // learned sink logit per query head [n_q], or null
+    int64_t window = 0;            // sliding window in rows (0 = none)
     int32_t n_q, hpk, n_grp, nc_max, chunk;
 };
 
@@ -499,9 +522,11 @@ __device__ void merge_body(const MergeArgs &a, int b, int h, int grp, int nc, co
     }
     const int hh = h % a.hpk;
     const int64_t p0 = (int64_t(b) * a.n_grp + grp) * a.nc_max * a.hpk + hh;
-    float M = -INFINITY;
+    // a learned sink joins the maximum and the sum; it has no value row
+    const float z = a.sinks ? a.sinks[h] * kLog2e : -INFINITY;
+    float M = z;
     for (int c = 0; c < nc; ++c) M = fmaxf(M, a.pm[p0 + int64_t(c) * a.hpk]);
-    float Ls = 0.0f, s = 0.0f;
+    float Ls = a.sinks ? exp2f(z - M) : 0.0f, s = 0.0f;
     for (int c = 0; c < nc; ++c) {
         const int64_t p = p0 + int64_t(c) * a.hpk;
         const float f = exp2f(a.pm[p] - M);
@@ -528,7 +553,9 @@ __global__ void __launch_bounds__(HD) merge_layer_kernel(MergeArgs a, MergeLayer
     const int h = blockIdx.x, b = blockIdx.y;
     const int L = src.seq_len[b];
     const int grp = src.slot[h / a.hpk];
-    const int nc = (L + a.chunk - 1) / a.chunk;
+    // chunks start at the first visible row rounded down to kRowAlign
+    const int f0 = int(first_visible(L, a.window) / kRowAlign * kRowAlign);
+    const int nc = (L - f0 + a.chunk - 1) / a.chunk;
     const float *vcol = (src.vcol && grp >= 0) ? src.vcol + (int64_t(b) * src.n_live + grp) * HD : nullptr;
     merge_body<HD>(a, b, h, grp, nc, vcol);
 }

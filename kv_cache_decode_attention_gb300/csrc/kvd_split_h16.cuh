@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(32, 8) split_h16_kernel(WarpArgs wa, LayerSrc 
     if (x_begin >= x_end) return;
 
     TileCursor cur;
-    if (!cursor_locate(cur, x_begin, src, wa.n_seq, lane, a.err)) return;
+    if (!cursor_locate(cur, x_begin, src, wa.n_seq, a.window, lane, a.err)) return;
     TileCursor prod = cur;
     if (cur.tl % kBlockTiles == 0) {
         // the slot just below this worker's first run belongs to no run
@@ -70,7 +70,7 @@ __global__ void __launch_bounds__(32, 8) split_h16_kernel(WarpArgs wa, LayerSrc 
             if (lane == 0) issue_tile(prod, &maps.kq, &maps.vq, src, sm + (i % kStages) * kStageBytes,
                                       &bar[i % kStages]);
             ++issued;
-            if (x_begin + issued < x_end) prod_ok = cursor_next(prod, src, wa.n_seq, a.err);
+            if (x_begin + issued < x_end) prod_ok = cursor_next(prod, src, wa.n_seq, a.window, a.err);
         }
     }
 
@@ -181,7 +181,9 @@ __global__ void __launch_bounds__(32, 8) split_h16_kernel(WarpArgs wa, LayerSrc 
                 ok = false;
                 break;
             }
-            const int n_valid = min(kWR, cur.Lb - cur.tl * kWR);
+            const int row0 = cur.f0 + cur.tl * kWR;  // unit row of the tile's row 0
+            const int n_valid = min(kWR, cur.Lb - row0);
+            const int r_lo = cur.lo - row0;  // rows before it are outside the window
             const uint32_t kbase = smem_addr(st + kStK);
             const float *ks_s = reinterpret_cast<const float *>(st + kStKs);
             const float *vs_s = reinterpret_cast<const float *>(st + kStVs);
@@ -231,15 +233,20 @@ __global__ void __launch_bounds__(32, 8) split_h16_kernel(WarpArgs wa, LayerSrc 
                         sacc[3] = fmaf(ks1[g], dg[gg][3], sacc[3]);
                     }
                 }
-                const bool v0 = r0 < n_valid, v1 = r0 + 1 < n_valid;
-                sreg[nt][0] = v0 ? sacc[0] * qexp_a : -INFINITY;
-                sreg[nt][1] = v1 ? sacc[1] * qexp_a : -INFINITY;
-                sreg[nt][2] = v0 ? sacc[2] * qexp_b : -INFINITY;
-                sreg[nt][3] = v1 ? sacc[3] * qexp_b : -INFINITY;
+                const bool v0 = r0 >= r_lo && r0 < n_valid, v1 = r0 + 1 >= r_lo && r0 + 1 < n_valid;
+                float x[4] = {sacc[0] * qexp_a, sacc[1] * qexp_a, sacc[2] * qexp_b, sacc[3] * qexp_b};
+                if (a.softcap2 > 0.0f) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) x[j] = softcap_log2(x[j], a.softcap2);
+                }
+                sreg[nt][0] = v0 ? x[0] : -INFINITY;
+                sreg[nt][1] = v1 ? x[1] : -INFINITY;
+                sreg[nt][2] = v0 ? x[2] : -INFINITY;
+                sreg[nt][3] = v1 ? x[3] : -INFINITY;
             }
             if (a.scores != nullptr) {
                 // per-row log2 scores for the imp pass: [hpk][cap] per unit
-                float *sp = a.scores + cur.rbase * a.hpk + int64_t(cur.tl) * kWR;
+                float *sp = a.scores + cur.rbase * a.hpk + row0;
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     const int h = hh ? hb : ha;
@@ -248,11 +255,13 @@ __global__ void __launch_bounds__(32, 8) split_h16_kernel(WarpArgs wa, LayerSrc 
 #pragma unroll
                         for (int nt = 0; nt < 4; ++nt) {
                             const int r0 = nt * 8 + 2 * t4;
-                            if (r0 + 1 < n_valid)
+                            if (r0 >= r_lo && r0 + 1 < n_valid) {
                                 *reinterpret_cast<float2 *>(sh + r0) =
                                     make_float2(sreg[nt][2 * hh], sreg[nt][2 * hh + 1]);
-                            else if (r0 < n_valid)
-                                sh[r0] = sreg[nt][2 * hh];
+                            } else {
+                                if (r0 >= r_lo && r0 < n_valid) sh[r0] = sreg[nt][2 * hh];
+                                if (r0 + 1 >= r_lo && r0 + 1 < n_valid) sh[r0 + 1] = sreg[nt][2 * hh + 1];
+                            }
                         }
                     }
                 }
@@ -265,8 +274,8 @@ __global__ void __launch_bounds__(32, 8) split_h16_kernel(WarpArgs wa, LayerSrc 
             for (int nt = 0; nt < 4; ++nt) {
                 const int r0 = nt * 8 + 2 * t4;
                 const float2 vv = *reinterpret_cast<const float2 *>(&vs_s[r0]);
-                vsr[nt][0] = r0 < n_valid ? vv.x : 0.0f;
-                vsr[nt][1] = r0 + 1 < n_valid ? vv.y : 0.0f;
+                vsr[nt][0] = r0 >= r_lo && r0 < n_valid ? vv.x : 0.0f;
+                vsr[nt][1] = r0 + 1 >= r_lo && r0 + 1 < n_valid ? vv.y : 0.0f;
                 vmax = fmaxf(vmax, fmaxf(vsr[nt][0], vsr[nt][1]));
                 ta = fmaxf(ta, fmaxf(sreg[nt][0], sreg[nt][1]));
                 tb = fmaxf(tb, fmaxf(sreg[nt][2], sreg[nt][3]));
@@ -354,9 +363,9 @@ __global__ void __launch_bounds__(32, 8) split_h16_kernel(WarpArgs wa, LayerSrc 
                     issue_tile(prod, &maps.kq, &maps.vq, src, st, &bar[stg]);
                 }
                 ++issued;
-                if (x_begin + issued < x_end) prod_ok = cursor_next(prod, src, wa.n_seq, a.err);
+                if (x_begin + issued < x_end) prod_ok = cursor_next(prod, src, wa.n_seq, a.window, a.err);
             }
-            if (x + 1 < x_end && !cursor_next(cur, src, wa.n_seq, a.err)) {
+            if (x + 1 < x_end && !cursor_next(cur, src, wa.n_seq, a.window, a.err)) {
                 ok = false;
                 ++i;
                 break;

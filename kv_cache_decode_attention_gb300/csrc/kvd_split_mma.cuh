@@ -172,9 +172,11 @@ __device__ __forceinline__ int64_t workers_started(int64_t x, int64_t T, int64_t
 }
 
 // Position of one tile in the unit order (sequence-major, live group, tile).
+// A unit's tiles start at its first visible row rounded down to a tile (f0).
 struct TileCursor {
     int b, gl, tl;   // sequence, live group, tile within the unit
     int Tb, Lb;      // tiles and rows of sequence b
+    int f0, lo;      // row of tile 0, first visible row
     int64_t cap;     // region rows of sequence b
     int64_t rbase;   // storage row of the unit's row 0
     int64_t bq;      // partial blocks of the units of sequences before b
@@ -182,11 +184,20 @@ struct TileCursor {
 
 __device__ __forceinline__ int blocks_of(int tiles) { return (tiles + kBlockTiles - 1) / kBlockTiles; }
 
+// Tiles of a sequence of L rows under a sliding window (0 = none).
+__host__ __device__ __forceinline__ int64_t tiles_of(int64_t L, int64_t window) {
+    const int64_t f0 = first_visible(L, window) / kWR * kWR;
+    return (L - f0 + kWR - 1) / kWR;
+}
+
 // Load sequence b's shape into the cursor; false (and an error bit) if its
 // length exceeds its capacity.
-__device__ __forceinline__ bool cursor_seq(TileCursor &c, const LayerSrc &src, uint32_t *err) {
+__device__ __forceinline__ bool cursor_seq(TileCursor &c, const LayerSrc &src, int64_t window,
+                                           uint32_t *err) {
     c.cap = src.cap[c.b];
     c.rbase = src.row_base[c.b];
+    c.lo = int(first_visible(c.Lb, window));
+    c.f0 = c.lo / kWR * kWR;
     if (int64_t(c.Lb) > c.cap) {
         set_error(err, kErrBounds);
         return false;
@@ -195,7 +206,7 @@ __device__ __forceinline__ bool cursor_seq(TileCursor &c, const LayerSrc &src, u
 }
 
 // Advance to the next tile in the global order; false past the last sequence.
-__device__ __forceinline__ bool cursor_next(TileCursor &c, const LayerSrc &src, int n_seq,
+__device__ __forceinline__ bool cursor_next(TileCursor &c, const LayerSrc &src, int n_seq, int64_t window,
                                             uint32_t *err) {
     if (++c.tl < c.Tb) return true;
     c.tl = 0;
@@ -208,20 +219,20 @@ __device__ __forceinline__ bool cursor_next(TileCursor &c, const LayerSrc &src, 
     for (;;) {
         if (++c.b >= n_seq) return false;
         c.Lb = src.seq_len[c.b];
-        c.Tb = (c.Lb + kWR - 1) / kWR;
+        c.Tb = int(tiles_of(c.Lb, window));
         if (c.Tb > 0) break;
     }
-    return cursor_seq(c, src, err);
+    return cursor_seq(c, src, window, err);
 }
 
 // Find global tile x: a warp-wide scan of the sequences' tile counts.
-__device__ inline bool cursor_locate(TileCursor &c, int64_t x, const LayerSrc &src, int n_seq, int lane,
-                              uint32_t *err) {
+__device__ inline bool cursor_locate(TileCursor &c, int64_t x, const LayerSrc &src, int n_seq, int64_t window,
+                                     int lane, uint32_t *err) {
     int64_t tp = 0, bq = 0;  // tiles and blocks of the sequences before `base`
     for (int base = 0; base < n_seq; base += 32) {
         const int i = base + lane;
         const int L = i < n_seq ? src.seq_len[i] : 0;
-        const int Tb = (L + kWR - 1) / kWR;
+        const int Tb = int(tiles_of(L, window));
         int64_t ut = int64_t(src.n_live) * Tb, ub = int64_t(src.n_live) * blocks_of(Tb);
         // inclusive prefix over the lanes
 #pragma unroll
@@ -247,7 +258,7 @@ __device__ inline bool cursor_locate(TileCursor &c, int64_t x, const LayerSrc &s
             const int64_t r = x - (tp + ex_t);
             c.gl = int(r / c.Tb);
             c.tl = int(r % c.Tb);
-            if (!cursor_seq(c, src, err)) return false;
+            if (!cursor_seq(c, src, window, err)) return false;
             c.rbase += int64_t(c.gl) * c.cap;
             return true;
         }
@@ -261,7 +272,7 @@ __device__ inline bool cursor_locate(TileCursor &c, int64_t x, const LayerSrc &s
 __device__ __forceinline__ void issue_tile(const TileCursor &c, const CUtensorMap *kmap,
                                            const CUtensorMap *vmap, const LayerSrc &src, char *stage,
                                            uint64_t *bar) {
-    const int64_t row = c.rbase + int64_t(c.tl) * kWR;
+    const int64_t row = c.rbase + c.f0 + int64_t(c.tl) * kWR;
     mbar_arrive_expect_tx(bar, kStageTx);
     tma_load_2d(stage + kStK, kmap, 0, int(row), bar);
     tma_load_2d(stage + kStV, vmap, 0, int(row), bar);
@@ -270,7 +281,7 @@ __device__ __forceinline__ void issue_tile(const TileCursor &c, const CUtensorMa
 }
 
 template <bool PACK>
-__global__ void __launch_bounds__(32) split_warp_kernel(WarpArgs wa, LayerSrc src,
+__global__ void __launch_bounds__(32, 12) split_warp_kernel(WarpArgs wa, LayerSrc src,
                                                         const __grid_constant__ MmaMaps maps) {
     using C = WarpCfg<PACK>;
     extern __shared__ __align__(128) char smem_raw[];
@@ -287,7 +298,7 @@ __global__ void __launch_bounds__(32) split_warp_kernel(WarpArgs wa, LayerSrc sr
     if (x_begin >= x_end) return;
 
     TileCursor cur;
-    if (!cursor_locate(cur, x_begin, src, wa.n_seq, lane, a.err)) return;
+    if (!cursor_locate(cur, x_begin, src, wa.n_seq, a.window, lane, a.err)) return;
     TileCursor prod = cur;
     if (cur.tl % kBlockTiles == 0) {
         // This worker starts on a block start: the slot just below its first
@@ -313,7 +324,7 @@ __global__ void __launch_bounds__(32) split_warp_kernel(WarpArgs wa, LayerSrc sr
             if (lane == 0) issue_tile(prod, &maps.kq, &maps.vq, src, sm + (i % kStages) * kStageBytes,
                                       &bar[i % kStages]);
             ++issued;
-            if (x_begin + issued < x_end) prod_ok = cursor_next(prod, src, wa.n_seq, a.err);
+            if (x_begin + issued < x_end) prod_ok = cursor_next(prod, src, wa.n_seq, a.window, a.err);
         }
     }
 
@@ -421,7 +432,9 @@ __global__ void __launch_bounds__(32) split_warp_kernel(WarpArgs wa, LayerSrc sr
                 ok = false;
                 break;
             }
-            const int n_valid = min(kWR, cur.Lb - cur.tl * kWR);
+            const int row0 = cur.f0 + cur.tl * kWR;  // unit row of the tile's row 0
+            const int n_valid = min(kWR, cur.Lb - row0);
+            const int r_lo = cur.lo - row0;  // rows before it are outside the window
             const uint32_t kaddr = smem_addr(st + kStK) + k_lane;
             const float *ks_s = reinterpret_cast<const float *>(st + kStKs);
             const float *vs_s = reinterpret_cast<const float *>(st + kStVs);
@@ -462,15 +475,21 @@ __global__ void __launch_bounds__(32) split_warp_kernel(WarpArgs wa, LayerSrc sr
                     for (int j = 0; j < 4; ++j) sacc[j] += __shfl_xor_sync(0xffffffffu, sacc[j], 2);
                 }
                 const int ra = mb * 16 + gl4, rb = ra + 8;
+                const bool va = ra >= r_lo && ra < n_valid, vb = rb >= r_lo && rb < n_valid;
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
-                    sreg[mb][cc][0] = ra < n_valid ? sacc[cc] * qexp[cc] : -INFINITY;
-                    sreg[mb][cc][1] = rb < n_valid ? sacc[2 + cc] * qexp[cc] : -INFINITY;
+                    float x0 = sacc[cc] * qexp[cc], x1 = sacc[2 + cc] * qexp[cc];
+                    if (a.softcap2 > 0.0f) {
+                        x0 = softcap_log2(x0, a.softcap2);
+                        x1 = softcap_log2(x1, a.softcap2);
+                    }
+                    sreg[mb][cc][0] = va ? x0 : -INFINITY;
+                    sreg[mb][cc][1] = vb ? x1 : -INFINITY;
                 }
             }
             if (a.scores != nullptr && owner) {
                 // per-row log2 scores for the imp pass: [hpk][cap] per unit
-                float *sp = a.scores + cur.rbase * a.hpk + int64_t(cur.tl) * kWR;
+                float *sp = a.scores + cur.rbase * a.hpk + row0;
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
                     const int h = hc0 + cc;
@@ -481,7 +500,7 @@ __global__ void __launch_bounds__(32) split_warp_kernel(WarpArgs wa, LayerSrc sr
 #pragma unroll
                             for (int rw = 0; rw < 2; ++rw) {
                                 const int r = mb * 16 + gl4 + 8 * rw;
-                                if (r < n_valid) sh[r] = sreg[mb][cc][rw];
+                                if (r >= r_lo && r < n_valid) sh[r] = sreg[mb][cc][rw];
                             }
                     }
                 }
@@ -495,7 +514,7 @@ __global__ void __launch_bounds__(32) split_warp_kernel(WarpArgs wa, LayerSrc sr
 #pragma unroll
                 for (int rw = 0; rw < 2; ++rw) {
                     const int r = mb * 16 + gl4 + 8 * rw;
-                    vsr[mb][rw] = r < n_valid ? vs_s[r] : 0.0f;
+                    vsr[mb][rw] = r >= r_lo && r < n_valid ? vs_s[r] : 0.0f;
                     vmax = fmaxf(vmax, vsr[mb][rw]);
                 }
             vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 4));
@@ -582,9 +601,9 @@ __global__ void __launch_bounds__(32) split_warp_kernel(WarpArgs wa, LayerSrc sr
                     issue_tile(prod, &maps.kq, &maps.vq, src, st, &bar[stg]);
                 }
                 ++issued;
-                if (x_begin + issued < x_end) prod_ok = cursor_next(prod, src, wa.n_seq, a.err);
+                if (x_begin + issued < x_end) prod_ok = cursor_next(prod, src, wa.n_seq, a.window, a.err);
             }
-            if (x + 1 < x_end && !cursor_next(cur, src, wa.n_seq, a.err)) {
+            if (x + 1 < x_end && !cursor_next(cur, src, wa.n_seq, a.window, a.err)) {
                 ok = false;
                 ++i;
                 break;

@@ -82,7 +82,7 @@ def test_explicit_freeze_is_idempotent_and_matches_oracle(torch, kvd):
     assert_storage_bitexact(layer, ocs, torch)
 
 
-def _decode_case(torch, kvd, mode, hd, hpk, lengths, alive, seed, with_imp=True):
+def _decode_case(torch, kvd, mode, hd, hpk, lengths, alive, seed, with_imp=True, opts=None):
     n_kv = len(alive)
     n_q = n_kv * hpk
     ks, vs = seq_rows(lengths, n_kv, hd, seed=seed)
@@ -96,7 +96,12 @@ def _decode_case(torch, kvd, mode, hd, hpk, lengths, alive, seed, with_imp=True)
     qd = torch.from_numpy(q).cuda()
     imp = torch.from_numpy(imp0).cuda() if with_imp else None
     scale = 1.0 / math.sqrt(hd)
-    out = kvd.decode_attention(qd, layer, imp=imp, scale=scale)
+    opts = dict(opts or {})
+    sinks = opts.get("sinks")
+    gpu_opts = dict(opts)
+    if sinks is not None:
+        gpu_opts["sinks"] = torch.from_numpy(np.asarray(sinks, np.float32)).cuda()
+    out = kvd.decode_attention(qd, layer, imp=imp, scale=scale, **gpu_opts)
     torch.cuda.synchronize()
     assert layer.device_error() == 0
     out = out.cpu().numpy()
@@ -108,7 +113,11 @@ def _decode_case(torch, kvd, mode, hd, hpk, lengths, alive, seed, with_imp=True)
     for b, oc in enumerate(ocs):
         ib = int(layer.imp_base[b])
         seg = imp_ref[ib:ib + max(lengths[b], 1)].copy() if lengths[b] else None
-        ref[b] = oc.decode(q[b], n_q, np.float32(scale), seg)
+        if opts:
+            ref[b] = oc.decode_ex(q[b], n_q, np.float32(scale), opts.get("window", 0),
+                                  opts.get("softcap", 0.0), sinks, seg)
+        else:
+            ref[b] = oc.decode(q[b], n_q, np.float32(scale), seg)
         if seg is not None:
             imp_ref[ib:ib + lengths[b]] = seg[:lengths[b]]
         for h in range(n_q):
@@ -143,6 +152,39 @@ def test_decode_parity_hd128(torch, kvd, mode, hpk):
 def test_decode_parity_hd64(torch, kvd, mode, hpk):
     _decode_case(torch, kvd, MODES[mode], 64, hpk, [5, 257, 600], np.array([0, 1, 1], np.uint8),
                  seed=21 + hpk)
+
+
+_OPTS = {
+    "window": {"window": 75},
+    "softcap": {"softcap": 1.5},
+    "sinks": {"sinks": True},
+    "all": {"window": 250, "softcap": 4.0, "sinks": True},
+}
+
+
+@pytest.mark.parametrize("mode", list(MODES))
+@pytest.mark.parametrize("hpk", [4, 16])
+@pytest.mark.parametrize("opt", list(_OPTS))
+def test_decode_options_parity(torch, kvd, mode, hpk, opt):
+    """[cortiq] attend_group_upto's window (first = stored - window), logit
+    soft-capping and learned sinks, against the oracle: outputs, imp (rows
+    before the window untouched), every storage mode, heads in N and in M."""
+    opts = dict(_OPTS[opt])
+    n_q = 4 * hpk
+    if opts.pop("sinks", None):
+        opts["sinks"] = (synthetic.normal((n_q,), 500 + hpk) * 2.0).astype(np.float32)
+    _decode_case(torch, kvd, MODES[mode], 128, hpk, [0, 1, 64, 300, 777, 1030],
+                 np.array([1, 1, 0, 1], np.uint8), seed=31 + hpk, opts=opts)
+
+
+def test_decode_options_errors(torch, kvd):
+    layer = _layer(kvd, oracle.Q8, [40], 2, 128, None, cap_extra=8)
+    q = torch.zeros(1, 4, 128, device="cuda")
+    for bad in ({"window": -1}, {"softcap": -1.0}, {"softcap": float("nan")}):
+        with pytest.raises(kvd.KvdError):
+            kvd.decode_attention(q, layer, **bad)
+    with pytest.raises(ValueError):
+        kvd.decode_attention(q, layer, sinks=torch.zeros(3, device="cuda"))
 
 
 def test_tiny_f32_gqa_config(torch, kvd):
