@@ -182,7 +182,8 @@ __device__ __forceinline__ void issue_segment(const ChunkInfo &ci, char *smem, u
     }
 }
 
-template <int HD, int HPK, bool KQ, bool VQ>
+// OPT: the call has a window or a softcap (compiled out of the common path).
+template <int HD, int HPK, bool KQ, bool VQ, bool OPT>
 __device__ void split_body(const ChunkInfo &ci, const SplitArgs &a, char *smem) {
     using C = SplitCfg<HD, HPK, KQ, VQ>;
     constexpr int CPL = C::CPL, TR = C::TR;
@@ -267,8 +268,9 @@ __device__ void split_body(const ChunkInfo &ci, const SplitArgs &a, char *smem) 
             if ((lane & ((32 >> C::LOGE) - 1)) == 0) {
                 const int e = lane >> (5 - C::LOGE);
                 const int r = rbase + e / HPK, h = e % HPK;
-                const bool vis = r < nt && row0 + r >= ci.lo;
-                const float sv = vis ? (a.softcap2 > 0.0f ? softcap_log2(s, a.softcap2) : s) : -INFINITY;
+                const bool vis = r < nt && (!OPT || row0 + r >= ci.lo);
+                const float sv =
+                    vis ? (OPT && a.softcap2 > 0.0f ? softcap_log2(s, a.softcap2) : s) : -INFINITY;
                 sc[r * HPK + h] = sv;
                 if (a.scores != nullptr && vis && h < a.hpk)
                     a.scores[ci.score0 + h * ci.score_ld + row0 + r] = sv;
@@ -409,7 +411,7 @@ struct LayerSrc {
     int32_t n_live;
 };
 
-template <int HD, int HPK, bool KQ, bool VQ>
+template <int HD, int HPK, bool KQ, bool VQ, bool OPT>
 __global__ void __launch_bounds__(kThreads, 2) split_layer_kernel(SplitArgs a, LayerSrc src) {
     extern __shared__ __align__(128) char smem[];
     const int b = blockIdx.z, gl = blockIdx.y, c = blockIdx.x;
@@ -442,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 2) split_layer_kernel(SplitArgs a, L
     // scores region of (b, gl): [hpk][cap] starting at its first storage row * hpk
     ci.score0 = (src.row_base[b] + int64_t(gl) * cap) * a.hpk + r0;
     ci.score_ld = cap;
-    split_body<HD, HPK, KQ, VQ>(ci, a, smem);
+    split_body<HD, HPK, KQ, VQ, OPT>(ci, a, smem);
 }
 
 // ---------------------------------------------------------------- R-SWA
@@ -492,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 2) split_rswa_kernel(SplitArgs a, Rs
     ci.kcol = nullptr;
     ci.score0 = -1;
     ci.score_ld = 0;
-    split_body<HD, 1, false, false>(ci, a, smem);
+    split_body<HD, 1, false, false, false>(ci, a, smem);
 }
 
 // ---------------------------------------------------------------- merge
@@ -575,7 +577,8 @@ template <int HD, int HPK, bool KQ, bool VQ>
 cudaError_t launch_split_layer_impl(const SplitArgs &a, const LayerSrc &s, dim3 grid,
                                     cudaStream_t st) {
     using C = SplitCfg<HD, HPK, KQ, VQ>;
-    auto kern = split_layer_kernel<HD, HPK, KQ, VQ>;
+    auto kern = (a.window > 0 || a.softcap2 > 0.0f) ? split_layer_kernel<HD, HPK, KQ, VQ, true>
+                                                     : split_layer_kernel<HD, HPK, KQ, VQ, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, C::SMEM, st>>>(a, s);

@@ -32,6 +32,8 @@ struct H16Cfg {
     static constexpr int SMEM_ALLOC = SMEM + 1024;  // room to align the base to 1024
 };
 
+// OPT: the call has a window or a softcap (compiled out of the common path).
+template <bool OPT>
 __global__ void __launch_bounds__(32, 8) split_h16_kernel(WarpArgs wa, LayerSrc src,
                                                             const __grid_constant__ MmaMaps maps) {
     using C = H16Cfg;
@@ -233,16 +235,26 @@ __global__ void __launch_bounds__(32, 8) split_h16_kernel(WarpArgs wa, LayerSrc 
                         sacc[3] = fmaf(ks1[g], dg[gg][3], sacc[3]);
                     }
                 }
-                const bool v0 = r0 >= r_lo && r0 < n_valid, v1 = r0 + 1 >= r_lo && r0 + 1 < n_valid;
-                float x[4] = {sacc[0] * qexp_a, sacc[1] * qexp_a, sacc[2] * qexp_b, sacc[3] * qexp_b};
-                if (a.softcap2 > 0.0f) {
+                sreg[nt][0] = sacc[0] * qexp_a;
+                sreg[nt][1] = sacc[1] * qexp_a;
+                sreg[nt][2] = sacc[2] * qexp_b;
+                sreg[nt][3] = sacc[3] * qexp_b;
+                if (OPT && a.softcap2 > 0.0f) {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) x[j] = softcap_log2(x[j], a.softcap2);
+                    for (int j = 0; j < 4; ++j) sreg[nt][j] = softcap_log2(sreg[nt][j], a.softcap2);
                 }
-                sreg[nt][0] = v0 ? x[0] : -INFINITY;
-                sreg[nt][1] = v1 ? x[1] : -INFINITY;
-                sreg[nt][2] = v0 ? x[2] : -INFINITY;
-                sreg[nt][3] = v1 ? x[3] : -INFINITY;
+            }
+            // rows outside [r_lo, n_valid) (a partial last tile, or rows before
+            // the window in the first one) drop out; full tiles skip the masks
+            const bool full = (!OPT || r_lo <= 0) && n_valid == kWR;
+            if (!full) {
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt) {
+                    const int r0 = nt * 8 + 2 * t4;
+                    const bool v0 = r0 >= r_lo && r0 < n_valid, v1 = r0 + 1 >= r_lo && r0 + 1 < n_valid;
+                    if (!v0) sreg[nt][0] = sreg[nt][2] = -INFINITY;
+                    if (!v1) sreg[nt][1] = sreg[nt][3] = -INFINITY;
+                }
             }
             if (a.scores != nullptr) {
                 // per-row log2 scores for the imp pass: [hpk][cap] per unit
@@ -274,8 +286,12 @@ __global__ void __launch_bounds__(32, 8) split_h16_kernel(WarpArgs wa, LayerSrc 
             for (int nt = 0; nt < 4; ++nt) {
                 const int r0 = nt * 8 + 2 * t4;
                 const float2 vv = *reinterpret_cast<const float2 *>(&vs_s[r0]);
-                vsr[nt][0] = r0 >= r_lo && r0 < n_valid ? vv.x : 0.0f;
-                vsr[nt][1] = r0 + 1 >= r_lo && r0 + 1 < n_valid ? vv.y : 0.0f;
+                vsr[nt][0] = vv.x;
+                vsr[nt][1] = vv.y;
+                if (!full) {
+                    if (!(r0 >= r_lo && r0 < n_valid)) vsr[nt][0] = 0.0f;
+                    if (!(r0 + 1 >= r_lo && r0 + 1 < n_valid)) vsr[nt][1] = 0.0f;
+                }
                 vmax = fmaxf(vmax, fmaxf(vsr[nt][0], vsr[nt][1]));
                 ta = fmaxf(ta, fmaxf(sreg[nt][0], sreg[nt][1]));
                 tb = fmaxf(tb, fmaxf(sreg[nt][2], sreg[nt][3]));
@@ -410,10 +426,10 @@ __global__ void __launch_bounds__(32, 8) split_h16_kernel(WarpArgs wa, LayerSrc 
 
 inline cudaError_t launch_split_h16(const WarpArgs &wa, const LayerSrc &s, const MmaMaps &maps,
                                     cudaStream_t st) {
-    cudaError_t e =
-        cudaFuncSetAttribute(split_h16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, H16Cfg::SMEM_ALLOC);
+    auto kern = (wa.a.window > 0 || wa.a.softcap2 > 0.0f) ? split_h16_kernel<true> : split_h16_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, H16Cfg::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    split_h16_kernel<<<unsigned(wa.G), 32, H16Cfg::SMEM_ALLOC, st>>>(wa, s, maps);
+    kern<<<unsigned(wa.G), 32, H16Cfg::SMEM_ALLOC, st>>>(wa, s, maps);
     return cudaGetLastError();
 }
 
@@ -422,10 +438,10 @@ inline int64_t split_h16_workers() {
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return 0;
-    if (cudaFuncSetAttribute(split_h16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, H16Cfg::SMEM_ALLOC) !=
+    auto kern = split_h16_kernel<false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, H16Cfg::SMEM_ALLOC) !=
             cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, split_h16_kernel, 32, H16Cfg::SMEM_ALLOC) !=
-            cudaSuccess)
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 32, H16Cfg::SMEM_ALLOC) != cudaSuccess)
         return 0;
     return int64_t(sms) * occ;
 }

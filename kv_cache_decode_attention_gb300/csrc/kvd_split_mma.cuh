@@ -280,7 +280,8 @@ __device__ __forceinline__ void issue_tile(const TileCursor &c, const CUtensorMa
     bulk_g2s(stage + kStVs, src.vs + row, 128, bar);
 }
 
-template <bool PACK>
+// OPT: the call has a window or a softcap (compiled out of the common path).
+template <bool PACK, bool OPT>
 __global__ void __launch_bounds__(32, 12) split_warp_kernel(WarpArgs wa, LayerSrc src,
                                                         const __grid_constant__ MmaMaps maps) {
     using C = WarpCfg<PACK>;
@@ -474,18 +475,28 @@ __global__ void __launch_bounds__(32, 12) split_warp_kernel(WarpArgs wa, LayerSr
 #pragma unroll
                     for (int j = 0; j < 4; ++j) sacc[j] += __shfl_xor_sync(0xffffffffu, sacc[j], 2);
                 }
-                const int ra = mb * 16 + gl4, rb = ra + 8;
-                const bool va = ra >= r_lo && ra < n_valid, vb = rb >= r_lo && rb < n_valid;
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
                     float x0 = sacc[cc] * qexp[cc], x1 = sacc[2 + cc] * qexp[cc];
-                    if (a.softcap2 > 0.0f) {
+                    if (OPT && a.softcap2 > 0.0f) {
                         x0 = softcap_log2(x0, a.softcap2);
                         x1 = softcap_log2(x1, a.softcap2);
                     }
-                    sreg[mb][cc][0] = va ? x0 : -INFINITY;
-                    sreg[mb][cc][1] = vb ? x1 : -INFINITY;
+                    sreg[mb][cc][0] = x0;
+                    sreg[mb][cc][1] = x1;
                 }
+            }
+            // rows outside [r_lo, n_valid) (a partial last tile, or rows before
+            // the window in the first one) drop out; full tiles skip the masks
+            const bool full = (!OPT || r_lo <= 0) && n_valid == kWR;
+            if (!full) {
+#pragma unroll
+                for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
+                    for (int rw = 0; rw < 2; ++rw) {
+                        const int r = mb * 16 + gl4 + 8 * rw;
+                        if (!(r >= r_lo && r < n_valid)) sreg[mb][0][rw] = sreg[mb][1][rw] = -INFINITY;
+                    }
             }
             if (a.scores != nullptr && owner) {
                 // per-row log2 scores for the imp pass: [hpk][cap] per unit
@@ -514,7 +525,7 @@ __global__ void __launch_bounds__(32, 12) split_warp_kernel(WarpArgs wa, LayerSr
 #pragma unroll
                 for (int rw = 0; rw < 2; ++rw) {
                     const int r = mb * 16 + gl4 + 8 * rw;
-                    vsr[mb][rw] = r >= r_lo && r < n_valid ? vs_s[r] : 0.0f;
+                    vsr[mb][rw] = full || (r >= r_lo && r < n_valid) ? vs_s[r] : 0.0f;
                     vmax = fmaxf(vmax, vsr[mb][rw]);
                 }
             vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 4));
@@ -659,7 +670,8 @@ template <bool PACK>
 cudaError_t launch_split_warp(const WarpArgs &wa, const LayerSrc &s, const MmaMaps &maps,
                               cudaStream_t st) {
     using C = WarpCfg<PACK>;
-    auto kern = split_warp_kernel<PACK>;
+    auto kern = (wa.a.window > 0 || wa.a.softcap2 > 0.0f) ? split_warp_kernel<PACK, true>
+                                                           : split_warp_kernel<PACK, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     kern<<<unsigned(wa.G), 32, C::SMEM_ALLOC, st>>>(wa, s, maps);
@@ -673,7 +685,7 @@ int64_t split_warp_workers() {
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return 0;
-    auto kern = split_warp_kernel<PACK>;
+    auto kern = split_warp_kernel<PACK, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              WarpCfg<PACK>::SMEM_ALLOC) != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 32, WarpCfg<PACK>::SMEM_ALLOC) !=
