@@ -32,8 +32,9 @@ struct H16Cfg {
     static constexpr int SMEM_ALLOC = SMEM + 1024;  // room to align the base to 1024
 };
 
-// OPT: the call has a window or a softcap (compiled out of the common path).
-template <bool OPT>
+// OPT: the call has a window or a softcap; IMP: the call accumulates imp
+// (per-row scores are stored).  Both are compiled out of the common path.
+template <bool OPT, bool IMP>
 __global__ void __launch_bounds__(32, 8) split_h16_kernel(WarpArgs wa, LayerSrc src,
                                                             const __grid_constant__ MmaMaps maps) {
     using C = H16Cfg;
@@ -256,7 +257,7 @@ __global__ void __launch_bounds__(32, 8) split_h16_kernel(WarpArgs wa, LayerSrc 
                     if (!v1) sreg[nt][1] = sreg[nt][3] = -INFINITY;
                 }
             }
-            if (a.scores != nullptr) {
+            if (IMP) {
                 // per-row log2 scores for the imp pass: [hpk][cap] per unit
                 float *sp = a.scores + cur.rbase * a.hpk + row0;
 #pragma unroll
@@ -307,7 +308,7 @@ __global__ void __launch_bounds__(32, 8) split_h16_kernel(WarpArgs wa, LayerSrc 
             const float wsc = pow2i(ew);
             // the change of Ew is an exact power of two (the approximate exp2
             // is not exact even at integers, and these factors compound over a run)
-            const float dsc = ldexpf(1.0f, ew - ew_prev);
+            const float dsc = pow2_wide(ew - ew_prev);
             ew_prev = ew;
             const float mna = fmaxf(ma, ta), mnb = fmaxf(mb, tb);
             // exactly 1 while the maximum holds; 0 before the first tile (m = -inf)
@@ -426,7 +427,9 @@ __global__ void __launch_bounds__(32, 8) split_h16_kernel(WarpArgs wa, LayerSrc 
 
 inline cudaError_t launch_split_h16(const WarpArgs &wa, const LayerSrc &s, const MmaMaps &maps,
                                     cudaStream_t st) {
-    auto kern = (wa.a.window > 0 || wa.a.softcap2 > 0.0f) ? split_h16_kernel<true> : split_h16_kernel<false>;
+    const bool opt = wa.a.window > 0 || wa.a.softcap2 > 0.0f, imp = wa.a.scores != nullptr;
+    auto kern = opt ? (imp ? split_h16_kernel<true, true> : split_h16_kernel<true, false>)
+                    : (imp ? split_h16_kernel<false, true> : split_h16_kernel<false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, H16Cfg::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     kern<<<unsigned(wa.G), 32, H16Cfg::SMEM_ALLOC, st>>>(wa, s, maps);
@@ -438,7 +441,7 @@ inline int64_t split_h16_workers() {
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return 0;
-    auto kern = split_h16_kernel<false>;
+    auto kern = split_h16_kernel<false, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, H16Cfg::SMEM_ALLOC) !=
             cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 32, H16Cfg::SMEM_ALLOC) != cudaSuccess)

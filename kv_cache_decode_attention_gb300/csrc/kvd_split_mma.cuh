@@ -153,6 +153,13 @@ __device__ __forceinline__ int exponent_of(float x) {
 // 2^e for -126 <= e <= 127.
 __device__ __forceinline__ float pow2i(int e) { return __uint_as_float(uint32_t(e + 127) << 23); }
 
+// 2^d for |d| <= 252 as the product of two normal powers of two: exact, and
+// rounded like ldexpf(1, d) where the result leaves the normal range.
+__device__ __forceinline__ float pow2_wide(int d) {
+    const int d1 = d >> 1;
+    return pow2i(d1) * pow2i(d - d1);
+}
+
 struct MmaMaps {
     CUtensorMap kq, vq;
 };
@@ -280,8 +287,9 @@ __device__ __forceinline__ void issue_tile(const TileCursor &c, const CUtensorMa
     bulk_g2s(stage + kStVs, src.vs + row, 128, bar);
 }
 
-// OPT: the call has a window or a softcap (compiled out of the common path).
-template <bool PACK, bool OPT>
+// OPT: the call has a window or a softcap; IMP: the call accumulates imp
+// (per-row scores are stored).  Both are compiled out of the common path.
+template <bool PACK, bool OPT, bool IMP>
 __global__ void __launch_bounds__(32, 12) split_warp_kernel(WarpArgs wa, LayerSrc src,
                                                         const __grid_constant__ MmaMaps maps) {
     using C = WarpCfg<PACK>;
@@ -498,7 +506,7 @@ __global__ void __launch_bounds__(32, 12) split_warp_kernel(WarpArgs wa, LayerSr
                         if (!(r >= r_lo && r < n_valid)) sreg[mb][0][rw] = sreg[mb][1][rw] = -INFINITY;
                     }
             }
-            if (a.scores != nullptr && owner) {
+            if (IMP && owner) {
                 // per-row log2 scores for the imp pass: [hpk][cap] per unit
                 float *sp = a.scores + cur.rbase * a.hpk + row0;
 #pragma unroll
@@ -535,7 +543,7 @@ __global__ void __launch_bounds__(32, 12) split_warp_kernel(WarpArgs wa, LayerSr
             const float wsc = pow2i(ew);
             // the change of Ew is an exact power of two (the approximate exp2
             // is not exact even at integers, and these factors compound over a run)
-            const float dsc = ldexpf(1.0f, ew - ew_prev);
+            const float dsc = pow2_wide(ew - ew_prev);
             ew_prev = ew;
             float fa[2];
 #pragma unroll
@@ -670,8 +678,9 @@ template <bool PACK>
 cudaError_t launch_split_warp(const WarpArgs &wa, const LayerSrc &s, const MmaMaps &maps,
                               cudaStream_t st) {
     using C = WarpCfg<PACK>;
-    auto kern = (wa.a.window > 0 || wa.a.softcap2 > 0.0f) ? split_warp_kernel<PACK, true>
-                                                           : split_warp_kernel<PACK, false>;
+    const bool opt = wa.a.window > 0 || wa.a.softcap2 > 0.0f, imp = wa.a.scores != nullptr;
+    auto kern = opt ? (imp ? split_warp_kernel<PACK, true, true> : split_warp_kernel<PACK, true, false>)
+                    : (imp ? split_warp_kernel<PACK, false, true> : split_warp_kernel<PACK, false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     kern<<<unsigned(wa.G), 32, C::SMEM_ALLOC, st>>>(wa, s, maps);
@@ -685,7 +694,7 @@ int64_t split_warp_workers() {
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return 0;
-    auto kern = split_warp_kernel<PACK, false>;
+    auto kern = split_warp_kernel<PACK, false, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              WarpCfg<PACK>::SMEM_ALLOC) != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 32, WarpCfg<PACK>::SMEM_ALLOC) !=
