@@ -23,6 +23,8 @@ from .oracle import (  # noqa: F401
     quant_row,
     quantize_row_i8,
     rswa_decode,
+    rswa_decode_i8,
+    rswa_mirror,
     rswa_write,
     online_head,
 )

@@ -14,7 +14,8 @@
  *              freeze_cols, append, attend, attend_group_upto, memory_bytes)
  *   [rswa]    docs.rs franken_ocr 0.8.0, src/native_engine/rswa.rs
  *             (module doc, quantize_row_i8, RingCache::write_decode_step,
- *              decode_dims, decode_attention_scalar_head, fold)
+ *              decode_dims, decode_attention_scalar_head, decode_attention_int8,
+ *              fold)
  *
  * Precision.  The quantiser is fixed by the pages to f32 arithmetic, so it
  * is written in f32 with every operation separately rounded (build with
@@ -496,6 +497,71 @@ int kvo_rswa_decode(int H, int hd, const float *q, const float *ref_k, const flo
         softmax_attend(&rc, rswa_row, prefill_len + ring_len, hd, q + (size_t)h * hd, scale,
                        out + (size_t)h * hd, NULL);
     }
+    return 0;
+}
+
+/* rswa decode_attention_int8 for one stream, over the int8 mirror only:
+ * per head, q is quantised per row (quantize_row_i8, giving codes and
+ * qscale); each key row's score is the exact integer dot of the codes
+ * times qscale times the row's K scale times `scale`; softmax over the
+ * reference rows followed by the ring rows; the output is the softmax-
+ * weighted sum of the dequantised V rows (code times the row's V scale).
+ * Codes [H][rows][hd], scales [H][rows] for rows = ref_cap (reference) and
+ * W (ring).  The integer dot is exact (its bound is 127 * 127 * hd); the
+ * products and the softmax are evaluated in f64.  Returns 0, -3 with no
+ * prefill (prefill_len < 0), -4 for an empty key set. */
+int kvo_rswa_decode_i8(int H, int hd, const float *q, const int8_t *ref_k8, const float *ref_ks,
+                       const int8_t *ref_v8, const float *ref_vs, long long ref_cap,
+                       int prefill_len, const int8_t *ring_k8, const float *ring_ks,
+                       const int8_t *ring_v8, const float *ring_vs, int W, int ring_len,
+                       float scale, double *out)
+{
+    if (prefill_len < 0) return -3;
+    const int n = prefill_len + ring_len;
+    if (n == 0) return -4;
+    int8_t *qc = (int8_t *)malloc((size_t)hd);
+    double *w = (double *)malloc(sizeof(double) * (size_t)n);
+    for (int h = 0; h < H; ++h) {
+        const float qscale = kvo_quantize_row_i8(q + (size_t)h * hd, hd, qc);
+        double m = -INFINITY;
+        for (int p = 0; p < n; ++p) {
+            const int8_t *k;
+            float ks;
+            if (p < prefill_len) {
+                k = ref_k8 + ((size_t)h * (size_t)ref_cap + (size_t)p) * (size_t)hd;
+                ks = ref_ks[(size_t)h * (size_t)ref_cap + (size_t)p];
+            } else {
+                k = ring_k8 + ((size_t)h * (size_t)W + (size_t)(p - prefill_len)) * (size_t)hd;
+                ks = ring_ks[(size_t)h * (size_t)W + (size_t)(p - prefill_len)];
+            }
+            long long dot = 0;
+            for (int d = 0; d < hd; ++d) dot += (long long)qc[d] * (long long)k[d];
+            w[p] = (double)dot * (double)qscale * (double)ks * (double)scale;
+            if (w[p] > m) m = w[p];
+        }
+        double den = 0.0;
+        for (int p = 0; p < n; ++p) {
+            w[p] = exp(w[p] - m);
+            den += w[p];
+        }
+        double *o = out + (size_t)h * hd;
+        for (int d = 0; d < hd; ++d) o[d] = 0.0;
+        for (int p = 0; p < n; ++p) {
+            const int8_t *v;
+            float vs;
+            if (p < prefill_len) {
+                v = ref_v8 + ((size_t)h * (size_t)ref_cap + (size_t)p) * (size_t)hd;
+                vs = ref_vs[(size_t)h * (size_t)ref_cap + (size_t)p];
+            } else {
+                v = ring_v8 + ((size_t)h * (size_t)W + (size_t)(p - prefill_len)) * (size_t)hd;
+                vs = ring_vs[(size_t)h * (size_t)W + (size_t)(p - prefill_len)];
+            }
+            for (int d = 0; d < hd; ++d) o[d] += w[p] * (double)vs * (double)v[d];
+        }
+        for (int d = 0; d < hd; ++d) o[d] /= den;
+    }
+    free(w);
+    free(qc);
     return 0;
 }
 

@@ -71,6 +71,8 @@ def lib():
             L.kvo_rswa_write.argtypes = [i32, i32, i32, vp, vp, vp, vp, i32, vp, vp]
             L.kvo_rswa_decode.argtypes = [i32, i32, vp, vp, vp, C.c_longlong, i32, vp, vp,
                                           i32, i32, f32, vp]
+            L.kvo_rswa_decode_i8.argtypes = [i32, i32, vp, vp, vp, vp, vp, C.c_longlong, i32, vp, vp,
+                                             vp, vp, i32, i32, f32, vp]
             L.kvo_online_head.argtypes = [i32, i32, vp, vp, vp, f32, vp]
             L.kvo_online_head.restype = None
             _lib = L
@@ -269,6 +271,41 @@ def rswa_decode(q, ref_k, ref_v, prefill_len, ring_k, ring_v, ring_len, scale):
     rc = lib().kvo_rswa_decode(H, hd, _p(q), _p(ref_k), _p(ref_v), ref_cap,
                                -1 if prefill_len is None else int(prefill_len),
                                _p(ring_k), _p(ring_v), W, int(ring_len), scale, _p(out))
+    if rc == -3:
+        raise RuntimeError("rswa decode before prefill")
+    if rc == -4:
+        raise RuntimeError("rswa empty attention key set")
+    return out
+
+
+def rswa_mirror(rows):
+    """rswa int8 mirror of f32 rows [..., hd]: quantize_row_i8 on every row.
+    Returns (codes int8 [..., hd], scales f32 [...])."""
+    rows = np.ascontiguousarray(rows, dtype=np.float32)
+    flat = rows.reshape(-1, rows.shape[-1])
+    codes = np.zeros(flat.shape, np.int8)
+    scales = np.zeros(flat.shape[0], np.float32)
+    for i in range(flat.shape[0]):
+        codes[i], scales[i] = quantize_row_i8(flat[i])
+    return codes.reshape(rows.shape), scales.reshape(rows.shape[:-1])
+
+
+def rswa_decode_i8(q, ref_k8, ref_ks, ref_v8, ref_vs, prefill_len, ring_k8, ring_ks, ring_v8,
+                   ring_vs, ring_len, scale):
+    """rswa decode_attention_int8 for one stream over its int8 mirror: codes
+    [H, rows, hd] int8 and scales [H, rows] f32 (rows = ref_cap, W), q [H, hd] f32.
+    Returns out [H, hd] f64; raises on no-prefill / empty key set."""
+    H, ref_cap, hd = ref_k8.shape
+    W = ring_k8.shape[1]
+    q = np.ascontiguousarray(q, dtype=np.float32)
+    arrs = [np.ascontiguousarray(a, dtype=t) for a, t in
+            ((ref_k8, np.int8), (ref_ks, np.float32), (ref_v8, np.int8), (ref_vs, np.float32),
+             (ring_k8, np.int8), (ring_ks, np.float32), (ring_v8, np.int8), (ring_vs, np.float32))]
+    out = np.zeros((H, hd), np.float64)
+    rc = lib().kvo_rswa_decode_i8(H, hd, _p(q), _p(arrs[0]), _p(arrs[1]), _p(arrs[2]), _p(arrs[3]),
+                                  ref_cap, -1 if prefill_len is None else int(prefill_len),
+                                  _p(arrs[4]), _p(arrs[5]), _p(arrs[6]), _p(arrs[7]), W,
+                                  int(ring_len), scale, _p(out))
     if rc == -3:
         raise RuntimeError("rswa decode before prefill")
     if rc == -4:

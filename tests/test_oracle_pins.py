@@ -650,3 +650,146 @@ def test_rswa_steady_state_is_prefix_plus_last_w_with_absolute_rope():
         ref[h] = w @ V
     assert np.allclose(outs["absolute"], ref, rtol=1e-10, atol=1e-12)
     assert np.max(np.abs(outs["slot"] - ref)) > 1e-3
+
+
+# ------------------------------------------------- R-SWA int8 mirror (NEXT-2)
+
+def _mirror(rk, rv, gk, gv):
+    """The int8 mirror of the four f32 regions, one quantize_row_i8 per row."""
+    rk8, rks = oracle.rswa_mirror(rk)
+    rv8, rvs = oracle.rswa_mirror(rv)
+    gk8, gks = oracle.rswa_mirror(gk)
+    gv8, gvs = oracle.rswa_mirror(gv)
+    return rk8, rks, rv8, rvs, gk8, gks, gv8, gvs
+
+
+def _decode_i8(q, mir, pl, rl, scale):
+    rk8, rks, rv8, rvs, gk8, gks, gv8, gvs = mir
+    return oracle.rswa_decode_i8(q, rk8, rks, rv8, rvs, pl, gk8, gks, gv8, gvs, rl, scale)
+
+
+def test_rswa_i8_lossless_rows_equal_the_f32_decode():
+    """[rswa] decode_attention_int8: rows whose absmax is 127 and whose other
+    entries are small integers quantise losslessly (scale 1, codes = values),
+    so the int8 decode must equal the f32 definition (rswa_decode) over the
+    same rows, reference and ring alike, up to f64 rounding."""
+    rng = np.random.default_rng(11)
+    m, n_ring = 9, 5
+
+    def rows(shape):
+        x = rng.integers(-3, 4, size=shape).astype(f32)
+        x[..., 0] = 127.0
+        return x
+
+    rk, rv, gk, gv, cur = _rswa_state(16)
+    rk[:, :m], rv[:, :m] = rows((H, m, HD)), rows((H, m, HD))
+    for _ in range(n_ring):
+        oracle.rswa_write(gk, gv, rows((H, HD)), rows((H, HD)), True, cur)
+    q = rows((H, HD))
+    q[:, 0] = -127.0  # the anchor may sit at either sign
+    mir = _mirror(rk, rv, gk, gv)
+    for codes, scales, src, n in ((mir[0], mir[1], rk, m), (mir[4], mir[5], gk, n_ring)):
+        assert np.all(scales[:, :n] == f32(1.0))
+        assert np.array_equal(codes[:, :n].astype(f32), src[:, :n])
+    scale = f32(1e-3)
+    got = _decode_i8(q, mir, m, cur[0], scale)
+    ref = oracle.rswa_decode(q, rk, rv, m, gk, gv, cur[0], scale)
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-12)
+    # the scores carry real spread (not a one-hot or uniform softmax)
+    assert np.ptp(ref) > 1.0
+
+
+def test_rswa_i8_dot_reaches_the_page_bound():
+    """[rswa] quantize_row_i8: q = 1 and K = +-2 quantise to codes +-127 on all
+    128 channels, so the i32 dot is exactly +-127*127*128 (the page's bound).
+    Two keys with V rows 3 and -1 give out = -1 + 4 sigmoid(delta) with
+    delta = 2 dot qscale kscale scale; solving for the dot recovers the bound."""
+    g = load_golden("rswa_i8.txt")
+    bound = int(g["qk_bound"])
+    assert bound == 127 * 127 * int(g["head_dim"])
+    rk, rv, gk, gv, _ = _rswa_state(16)
+    rk[:, 0], rk[:, 1] = 2.0, -2.0
+    rv[:, 0], rv[:, 1] = 3.0, -1.0
+    q = np.ones((H, HD), f32)
+    mir = _mirror(rk, rv, gk, gv)
+    assert np.all(mir[0][:, 0] == 127) and np.all(mir[0][:, 1] == -127)
+    scale = f32(1.0 / 4096.0)
+    out = _decode_i8(q, mir, 2, 0, scale)
+    qscale = float(f32(1.0) / f32(127.0))
+    kscale = float(f32(2.0) / f32(127.0))
+    v0 = 127.0 * float(f32(3.0) / f32(127.0))
+    v1 = -127.0 * float(f32(1.0) / f32(127.0))
+    sig = (out - v1) / (v0 - v1)
+    delta = np.log(sig / (1.0 - sig))
+    dot = delta / (2.0 * qscale * kscale * float(scale))
+    assert np.all(np.abs(dot - bound) < 1e-3)
+
+
+def test_rswa_i8_single_key_returns_the_dequantised_row():
+    """One key: the softmax weight is 1, so out = V codes * V scale exactly, and
+    round-to-nearest keeps it within half a step (plus the division's rounding)
+    of the f32 row."""
+    rk, rv, gk, gv, _ = _rswa_state(16)
+    rk[:, 0] = synthetic.normal((H, HD), 91)
+    rv[:, 0] = synthetic.normal((H, HD), 92)
+    q = synthetic.normal((H, HD), 93)
+    mir = _mirror(rk, rv, gk, gv)
+    out = _decode_i8(q, mir, 1, 0, f32(0.1))
+    deq = mir[2][:, 0].astype(np.float64) * mir[3][:, 0, None].astype(np.float64)
+    assert np.array_equal(out, deq)
+    step = mir[3][:, 0, None].astype(np.float64)
+    assert np.all(np.abs(deq - rv[:, 0]) <= step * (0.5 + 1e-6))
+
+
+def test_rswa_i8_zero_query_averages_reference_and_ring():
+    """A zero query quantises to codes 0 with scale 1.0 (the page's zero-row
+    rule), every score is 0, and the output is the plain mean of the
+    dequantised V rows over the reference rows and the ring rows."""
+    g = load_golden("rswa_i8.txt")
+    q0, s0 = oracle.quantize_row_i8(np.zeros(HD, f32))
+    assert np.all(q0 == 0) and s0 == f32(float(g["zero_row_scale"]))
+    rk, rv, gk, gv, cur = _rswa_state(16)
+    rk[:, :4] = synthetic.normal((H, 4, HD), 94)
+    rv[:, :4] = synthetic.normal((H, 4, HD), 95)
+    for t in range(3):
+        oracle.rswa_write(gk, gv, synthetic.normal((H, HD), 96 + t), synthetic.normal((H, HD), 99 + t),
+                          True, cur)
+    mir = _mirror(rk, rv, gk, gv)
+    out = _decode_i8(np.zeros((H, HD), f32), mir, 4, cur[0], f32(0.3))
+    deq_ref = mir[2][:, :4].astype(np.float64) * mir[3][:, :4, None]
+    deq_ring = mir[6][:, :3].astype(np.float64) * mir[7][:, :3, None]
+    mean = np.concatenate([deq_ref, deq_ring], axis=1).mean(axis=1)
+    assert np.allclose(out, mean, rtol=1e-12, atol=1e-12)
+
+
+def test_rswa_i8_errors():
+    rk, rv, gk, gv, _ = _rswa_state(4)
+    mir = _mirror(rk, rv, gk, gv)
+    with pytest.raises(RuntimeError):
+        _decode_i8(np.ones((H, HD), f32), mir, None, 0, f32(0.1))
+    with pytest.raises(RuntimeError):
+        _decode_i8(np.ones((H, HD), f32), mir, 0, 0, f32(0.1))
+
+
+def test_rswa_i8_ring_rows_use_their_own_scales():
+    """Two ring keys of magnitudes 2 and -4 both quantise to codes +-127 and
+    differ only in their row scales (2/127, 4/127); with q = 1 the scores are
+    +-127*127*128 * qscale * kscale_r * scale, a closed form that fails if a
+    ring row reads another row's scale."""
+    rk, rv, gk, gv, cur = _rswa_state(16)
+    k_rows = [np.full((H, HD), 2.0, f32), np.full((H, HD), -4.0, f32)]
+    v_rows = [np.full((H, HD), 3.0, f32), np.full((H, HD), -1.0, f32)]
+    for kr, vr in zip(k_rows, v_rows):
+        oracle.rswa_write(gk, gv, kr, vr, True, cur)
+    mir = _mirror(rk, rv, gk, gv)
+    assert np.all(mir[4][:, 0] == 127) and np.all(mir[4][:, 1] == -127)
+    scale = f32(1.0 / 2048.0)
+    out = _decode_i8(np.ones((H, HD), f32), mir, 0, cur[0], scale)
+    qs = float(f32(1.0) / f32(127.0))
+    s0 = 2064512 * qs * float(f32(2.0) / f32(127.0)) * float(scale)
+    s1 = -2064512 * qs * float(f32(4.0) / f32(127.0)) * float(scale)
+    v0 = 127.0 * float(f32(3.0) / f32(127.0))
+    v1 = -127.0 * float(f32(1.0) / f32(127.0))
+    m = max(s0, s1)
+    w0, w1 = math.exp(s0 - m), math.exp(s1 - m)
+    assert np.allclose(out, (w0 * v0 + w1 * v1) / (w0 + w1), rtol=1e-12, atol=1e-12)
