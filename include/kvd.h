@@ -254,6 +254,56 @@ KVD_API kvd_status rswa_decode(const float *q, const float *ref_k, const float *
                        int32_t head_dim, int64_t ref_cap, int32_t W, float scale, float *out,
                        void *workspace, int64_t workspace_bytes, void *stream);
 
+/* ---- R-SWA int8 mirror (rswa Int8Kv, quantize_row_i8,
+ * decode_attention_int8) ----
+ * A per-row symmetric int8 copy of the four f32 regions, kept beside them
+ * (the f32 regions stay the source of truth).  Codes have the regions'
+ * shapes, [B][H][ref_cap][head_dim] and [B][H][W][head_dim]; each row has
+ * one f32 scale, [B][H][ref_cap] and [B][H][W].  A row's scale is
+ * max|x| / 127 (1.0 for an all-zero row) and its codes are
+ * clamp(round_half_even(x / scale), -127, 127), IEEE f32 division.  All
+ * eight are device pointers owned by the caller, 16-byte aligned. */
+typedef struct {
+    int8_t *ref_k, *ref_v;
+    float *ref_ks, *ref_vs;
+    int8_t *ring_k, *ring_v;
+    float *ring_ks, *ring_vs;
+} rswa_i8_mirror;
+
+/* rswa_record_prefill plus the int8 mirror of the copied rows (rswa
+ * RingCache::record_prefill with the int8 lever on: the whole reference block
+ * is mirrored once).  head_dim 64 or 128; k, v, ref_k, ref_v 16-byte aligned.
+ * Same cursor update and errors as rswa_record_prefill. */
+KVD_API kvd_status rswa_record_prefill_i8(float *ref_k, float *ref_v, const rswa_i8_mirror *m,
+                                          const float *k, const float *v, int32_t s, int32_t seq,
+                                          int32_t B, int32_t H, int32_t head_dim, int64_t ref_cap,
+                                          int32_t W, int32_t *prefill_len, int32_t *ring_len,
+                                          int32_t *ring_pos, void *stream);
+
+/* rswa_ring_write plus the int8 mirror of each freshly written ring row at the
+ * same slot (rswa write_decode_step with the int8 lever on).  head_dim 64 or
+ * 128; k, v, ring_k, ring_v 16-byte aligned.  Same cursor update, slot_out
+ * and errors as rswa_ring_write. */
+KVD_API kvd_status rswa_ring_write_i8(float *ring_k, float *ring_v, const rswa_i8_mirror *m,
+                                      const float *k, const float *v, const int32_t *prefill_len,
+                                      int32_t *ring_len, int32_t *ring_pos, int32_t B, int32_t H,
+                                      int32_t head_dim, int32_t W, int32_t *slot_out,
+                                      void *stream);
+
+/* rswa decode_attention_int8 for every stream, reading the int8 mirror only:
+ * per (stream, head) the query row is quantised like a cache row (codes and
+ * qscale); each key's score is the exact integer dot of the codes times
+ * qscale times the key row's K scale times `scale`; softmax over reference
+ * rows [0, prefill_len) followed by ring rows [0, ring_len); V rows are
+ * dequantised per row (code times the row's V scale).  out device f32
+ * [B][H * head_dim].  Same cursor contract, workspace
+ * (rswa_decode_workspace_bytes), alignment rules and errors as rswa_decode. */
+KVD_API kvd_status rswa_decode_i8(const float *q, const rswa_i8_mirror *m,
+                                  const int32_t *prefill_len, const int32_t *ring_len,
+                                  const int32_t *ring_pos, int32_t B, int32_t H, int32_t head_dim,
+                                  int64_t ref_cap, int32_t W, float scale, float *out,
+                                  void *workspace, int64_t workspace_bytes, void *stream);
+
 /* Device error word kept in an R-SWA workspace (see kvd_layer_device_error). */
 KVD_API kvd_status rswa_device_error(const void *workspace, int32_t clear, uint32_t *word_out);
 

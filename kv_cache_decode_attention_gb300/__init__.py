@@ -16,6 +16,7 @@ from .api import (  # noqa: F401
     kv_freeze_colfield,
     rswa_attention,
     rswa_decode,
+    rswa_decode_i8,
     rswa_record_prefill,
     rswa_ring_write,
 )

@@ -25,6 +25,12 @@ class kvd_layer(C.Structure):
     _fields_ = [("opaque", C.c_uint64 * 128)]
 
 
+class rswa_i8_mirror(C.Structure):
+    _fields_ = [("ref_k", C.c_void_p), ("ref_v", C.c_void_p), ("ref_ks", C.c_void_p),
+                ("ref_vs", C.c_void_p), ("ring_k", C.c_void_p), ("ring_v", C.c_void_p),
+                ("ring_ks", C.c_void_p), ("ring_vs", C.c_void_p)]
+
+
 class KvdError(RuntimeError):
     def __init__(self, fn: str, status: int, msg: str):
         super().__init__("%s failed: %s (%d)" % (fn, msg, status))
@@ -53,6 +59,12 @@ _SIGS = {
     "rswa_decode_workspace_bytes": [_i32, _i32, _i32, _i64, _i32, _P(_i64)],
     "rswa_decode": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, _i32, _f32,
                     _vp, _vp, _i64, _vp],
+    "rswa_record_prefill_i8": [_vp, _vp, _P(rswa_i8_mirror), _vp, _vp, _i32, _i32, _i32, _i32, _i32,
+                               _i64, _i32, _vp, _vp, _vp, _vp],
+    "rswa_ring_write_i8": [_vp, _vp, _P(rswa_i8_mirror), _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
+                           _i32, _vp, _vp],
+    "rswa_decode_i8": [_vp, _P(rswa_i8_mirror), _vp, _vp, _vp, _i32, _i32, _i32, _i64, _i32, _f32, _vp,
+                       _vp, _i64, _vp],
     "rswa_device_error": [_vp, _i32, _P(C.c_uint32)],
     "kvd_status_string": [_i32],
 }

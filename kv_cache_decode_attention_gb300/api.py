@@ -231,16 +231,32 @@ def decode_attention_static(q: torch.Tensor, cache: LayerKvCache, out: torch.Ten
 
 class RingCache:
     """R-SWA caches of B streams for one layer: reference block [B, H, ref_cap, hd]
-    plus a W-slot ring [B, H, W, hd], cursors on the host."""
+    plus a W-slot ring [B, H, W, hd], cursors on the host.  With int8=True an
+    int8 mirror (rswa Int8Kv: codes of the same shapes, one f32 scale per row)
+    is kept beside the f32 regions and written by the same calls."""
 
     def __init__(self, B: int, ref_cap: int, H: int = 10, head_dim: int = 128, W: int = 128,
-                 device="cuda"):
+                 device="cuda", int8: bool = False):
         self.B, self.H, self.head_dim, self.W, self.ref_cap = B, H, head_dim, W, ref_cap
         dev = torch.device(device)
         self.ref_k = torch.zeros(B, H, ref_cap, head_dim, device=dev)
         self.ref_v = torch.zeros(B, H, ref_cap, head_dim, device=dev)
         self.ring_k = torch.zeros(B, H, W, head_dim, device=dev)
         self.ring_v = torch.zeros(B, H, W, head_dim, device=dev)
+        self.mirror = None
+        if int8:
+            i8 = dict(dtype=torch.int8, device=dev)
+            self.ref_k8 = torch.zeros(B, H, ref_cap, head_dim, **i8)
+            self.ref_v8 = torch.zeros(B, H, ref_cap, head_dim, **i8)
+            self.ring_k8 = torch.zeros(B, H, W, head_dim, **i8)
+            self.ring_v8 = torch.zeros(B, H, W, head_dim, **i8)
+            self.ref_ks = torch.zeros(B, H, ref_cap, device=dev)
+            self.ref_vs = torch.zeros(B, H, ref_cap, device=dev)
+            self.ring_ks = torch.zeros(B, H, W, device=dev)
+            self.ring_vs = torch.zeros(B, H, W, device=dev)
+            self.mirror = _abi.rswa_i8_mirror(
+                _ptr(self.ref_k8), _ptr(self.ref_v8), _ptr(self.ref_ks), _ptr(self.ref_vs),
+                _ptr(self.ring_k8), _ptr(self.ring_v8), _ptr(self.ring_ks), _ptr(self.ring_vs))
         self.prefill_len = np.full(B, -1, np.int32)
         self.ring_len = np.zeros(B, np.int32)
         self.ring_pos = np.zeros(B, np.int32)
@@ -263,10 +279,14 @@ def rswa_record_prefill(cache: RingCache, s: int, k: torch.Tensor, v: torch.Tens
     seq = k.numel() // (cache.H * cache.head_dim)
     if k.numel() != cache.H * seq * cache.head_dim or v.numel() != k.numel():
         raise ValueError("prefill k/v must be [H, seq, head_dim]")
-    _abi.call("rswa_record_prefill", _ptr(cache.ref_k), _ptr(cache.ref_v), _ptr(k), _ptr(v),
-              int(s), int(seq), cache.B, cache.H, cache.head_dim, cache.ref_cap, cache.W,
-              _np_ptr(cache.prefill_len), _np_ptr(cache.ring_len), _np_ptr(cache.ring_pos),
-              _stream(stream))
+    args = (int(s), int(seq), cache.B, cache.H, cache.head_dim, cache.ref_cap, cache.W,
+            _np_ptr(cache.prefill_len), _np_ptr(cache.ring_len), _np_ptr(cache.ring_pos),
+            _stream(stream))
+    if cache.mirror is not None:
+        _abi.call("rswa_record_prefill_i8", _ptr(cache.ref_k), _ptr(cache.ref_v), C.byref(cache.mirror),
+                  _ptr(k), _ptr(v), *args)
+    else:
+        _abi.call("rswa_record_prefill", _ptr(cache.ref_k), _ptr(cache.ref_v), _ptr(k), _ptr(v), *args)
 
 
 def rswa_ring_write(cache: RingCache, k: torch.Tensor, v: torch.Tensor, stream=None) -> np.ndarray:
@@ -276,9 +296,14 @@ def rswa_ring_write(cache: RingCache, k: torch.Tensor, v: torch.Tensor, stream=N
     if k.numel() != cache.B * cache.H * cache.head_dim or v.numel() != k.numel():
         raise ValueError("k/v must be [B, H, head_dim]")
     slots = np.zeros(cache.B, np.int32)
-    _abi.call("rswa_ring_write", _ptr(cache.ring_k), _ptr(cache.ring_v), _ptr(k), _ptr(v),
-              _np_ptr(cache.prefill_len), _np_ptr(cache.ring_len), _np_ptr(cache.ring_pos),
-              cache.B, cache.H, cache.head_dim, cache.W, _np_ptr(slots), _stream(stream))
+    args = (_ptr(k), _ptr(v), _np_ptr(cache.prefill_len), _np_ptr(cache.ring_len),
+            _np_ptr(cache.ring_pos), cache.B, cache.H, cache.head_dim, cache.W, _np_ptr(slots),
+            _stream(stream))
+    if cache.mirror is not None:
+        _abi.call("rswa_ring_write_i8", _ptr(cache.ring_k), _ptr(cache.ring_v), C.byref(cache.mirror),
+                  *args)
+    else:
+        _abi.call("rswa_ring_write", _ptr(cache.ring_k), _ptr(cache.ring_v), *args)
     return slots
 
 
@@ -298,6 +323,27 @@ def rswa_decode(q: torch.Tensor, cache: RingCache, out: torch.Tensor | None = No
               _np_ptr(cache.ring_pos), cache.B, cache.H, cache.head_dim, cache.ref_cap, cache.W,
               C.c_float(scale), _ptr(out), _ptr(cache.workspace), int(cache.workspace.numel()),
               _stream(stream))
+    return out
+
+
+def rswa_decode_i8(q: torch.Tensor, cache: RingCache, out: torch.Tensor | None = None,
+                   scale: float | None = None, stream=None) -> torch.Tensor:
+    """rswa decode_attention_int8: q [B, H, hd] -> out [B, H * hd] over the int8
+    mirror (the cache must have been built with int8=True)."""
+    if cache.mirror is None:
+        raise ValueError("rswa_decode_i8 needs a RingCache built with int8=True")
+    _f32_cuda(q, "q")
+    if q.numel() != cache.B * cache.H * cache.head_dim:
+        raise ValueError("q must be [B, H, head_dim]")
+    if out is None:
+        out = torch.empty(cache.B, cache.H * cache.head_dim, device=q.device)
+    _f32_cuda(out, "out")
+    if scale is None:
+        scale = 1.0 / math.sqrt(cache.head_dim)
+    _abi.call("rswa_decode_i8", _ptr(q), C.byref(cache.mirror), _np_ptr(cache.prefill_len),
+              _np_ptr(cache.ring_len), _np_ptr(cache.ring_pos), cache.B, cache.H, cache.head_dim,
+              cache.ref_cap, cache.W, C.c_float(scale), _ptr(out), _ptr(cache.workspace),
+              int(cache.workspace.numel()), _stream(stream))
     return out
 
 

@@ -356,11 +356,74 @@ __global__ void prefill_copy_kernel(float *ref_k, float *ref_v, const float *k, 
     }
 }
 
+// rswa quantize_row_i8 of one HD-value row by one warp (lane = CPL
+// consecutive values): codes and the row scale, with the f32 row copied to
+// `copy` on the way.
 template <int HD>
+__device__ __forceinline__ void quant_row_i8_warp(const float *x, float *copy, int8_t *codes,
+                                                  float *scale, int lane) {
+    constexpr int CPL = HD / 32;
+    float v[CPL];
+    if (CPL == 4) {
+        const float4 f = reinterpret_cast<const float4 *>(x)[lane];
+        reinterpret_cast<float4 *>(copy)[lane] = f;
+        v[0] = f.x, v[1] = f.y, v[2] = f.z, v[3] = f.w;
+    } else {
+        const float2 f = reinterpret_cast<const float2 *>(x)[lane];
+        reinterpret_cast<float2 *>(copy)[lane] = f;
+        v[0] = f.x, v[1] = f.y;
+    }
+    float mx = 0.0f;
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) mx = fmaxf(mx, fabsf(v[j]));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    const float sc = mx > 0.0f ? __fdiv_rn(mx, 127.0f) : 1.0f;
+    uint32_t w = 0;
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) w |= (uint32_t(quant_code_i8(v[j], sc)) & 0xffu) << (8 * j);
+    if (CPL == 4) reinterpret_cast<uint32_t *>(codes)[lane] = w;
+    else reinterpret_cast<uint16_t *>(codes)[lane] = uint16_t(w);
+    if (lane == 0) *scale = sc;
+}
+
+// record_prefill with the int8 mirror: one warp per (head, row) of stream s
+// copies the K and V rows and writes their codes and scales.
+template <int HD>
+__global__ void prefill_i8_kernel(float *ref_k, float *ref_v, rswa_i8_mirror m, const float *k,
+                                  const float *v, int32_t s, int32_t seq, int32_t H, int64_t ref_cap) {
+    const int lane = threadIdx.x & 31;
+    const int64_t rows = int64_t(H) * seq;
+    for (int64_t w = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5; w < rows;
+         w += (int64_t(gridDim.x) * blockDim.x) >> 5) {
+        const int64_t h = w / seq, r = w % seq;
+        const int64_t dst = (int64_t(s) * H + h) * ref_cap + r;
+        quant_row_i8_warp<HD>(k + w * HD, ref_k + dst * HD, m.ref_k + dst * HD, m.ref_ks + dst, lane);
+        quant_row_i8_warp<HD>(v + w * HD, ref_v + dst * HD, m.ref_v + dst * HD, m.ref_vs + dst, lane);
+    }
+}
+
+// write_decode_step with the int8 mirror: one warp per (stream, head).
+template <int HD>
+__global__ void ring_write_i8_kernel(float *ring_k, float *ring_v, rswa_i8_mirror m, const float *k,
+                                     const float *v, int32_t H, int32_t W, RingWriteTable t) {
+    const int lane = threadIdx.x & 31;
+    const int64_t rows = int64_t(t.n) * H;
+    for (int64_t w = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5; w < rows;
+         w += (int64_t(gridDim.x) * blockDim.x) >> 5) {
+        const int i = int(w / H), h = int(w % H);
+        const int64_t src = (int64_t(t.s0 + i) * H + h) * HD;
+        const int64_t dst = (int64_t(t.s0 + i) * H + h) * W + t.slot[i];
+        quant_row_i8_warp<HD>(k + src, ring_k + dst * HD, m.ring_k + dst * HD, m.ring_ks + dst, lane);
+        quant_row_i8_warp<HD>(v + src, ring_v + dst * HD, m.ring_v + dst * HD, m.ring_vs + dst, lane);
+    }
+}
+
+template <int HD, bool I8>
 cudaError_t launch_split_rswa(const SplitArgs &a, const RswaSrc &s, const RswaTable &t, dim3 grid,
                               cudaStream_t st) {
-    using C = SplitCfg<HD, 1, false, false>;
-    auto kern = split_rswa_kernel<HD>;
+    using C = SplitCfg<HD, 1, I8, I8, I8>;
+    auto kern = split_rswa_kernel<HD, I8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, C::SMEM, st>>>(a, s, t);
@@ -551,11 +614,18 @@ extern "C" kvd_status decode_attention_ex(const float *q, const kvd_layer *L, in
 
 // ------------------------------------------------------------------ R-SWA
 
-extern "C" kvd_status rswa_record_prefill(float *ref_k, float *ref_v, const float *k,
-                                          const float *v, int32_t s, int32_t seq, int32_t B,
-                                          int32_t H, int32_t head_dim, int64_t ref_cap, int32_t W,
-                                          int32_t *prefill_len, int32_t *ring_len,
-                                          int32_t *ring_pos, void *stream) {
+// The eight mirror pointers are present and 16-byte aligned.
+static bool mirror_ok(const rswa_i8_mirror *m) {
+    return m != nullptr && aligned16(m->ref_k) && aligned16(m->ref_v) && aligned16(m->ref_ks) &&
+           aligned16(m->ref_vs) && aligned16(m->ring_k) && aligned16(m->ring_v) &&
+           aligned16(m->ring_ks) && aligned16(m->ring_vs) && m->ref_k && m->ref_v && m->ref_ks &&
+           m->ref_vs && m->ring_k && m->ring_v && m->ring_ks && m->ring_vs;
+}
+
+static kvd_status record_prefill(float *ref_k, float *ref_v, const rswa_i8_mirror *m, const float *k,
+                          const float *v, int32_t s, int32_t seq, int32_t B, int32_t H,
+                          int32_t head_dim, int64_t ref_cap, int32_t W, int32_t *prefill_len,
+                          int32_t *ring_len, int32_t *ring_pos, void *stream) {
     if (ref_k == nullptr || ref_v == nullptr || prefill_len == nullptr || ring_len == nullptr ||
         ring_pos == nullptr)
         return KVD_EINVAL;
@@ -563,11 +633,26 @@ extern "C" kvd_status rswa_record_prefill(float *ref_k, float *ref_v, const floa
         return KVD_EINVAL;
     if (seq > ref_cap) return KVD_ECAPACITY;
     if (seq > 0 && (k == nullptr || v == nullptr)) return KVD_EINVAL;
+    if (m != nullptr) {
+        if (!mirror_ok(m) || (head_dim != 64 && head_dim != 128) || !aligned16(ref_k) ||
+            !aligned16(ref_v) || (seq > 0 && (!aligned16(k) || !aligned16(v))))
+            return KVD_EINVAL;
+    }
     if (seq > 0) {
-        const int64_t total = int64_t(H) * seq * head_dim;
-        const unsigned blocks = unsigned(std::min<int64_t>(ceil_div(total, 256), 152 * 16));
-        prefill_copy_kernel<<<blocks, 256, 0, as_stream(stream)>>>(ref_k, ref_v, k, v, s, seq, H,
-                                                                   head_dim, ref_cap);
+        cudaStream_t st = as_stream(stream);
+        if (m != nullptr) {
+            const int64_t warps = int64_t(H) * seq;
+            const unsigned blocks = unsigned(std::min<int64_t>(ceil_div(warps, 8), 152 * 16));
+            if (head_dim == 128)
+                prefill_i8_kernel<128><<<blocks, 256, 0, st>>>(ref_k, ref_v, *m, k, v, s, seq, H, ref_cap);
+            else
+                prefill_i8_kernel<64><<<blocks, 256, 0, st>>>(ref_k, ref_v, *m, k, v, s, seq, H, ref_cap);
+        } else {
+            const int64_t total = int64_t(H) * seq * head_dim;
+            const unsigned blocks = unsigned(std::min<int64_t>(ceil_div(total, 256), 152 * 16));
+            prefill_copy_kernel<<<blocks, 256, 0, st>>>(ref_k, ref_v, k, v, s, seq, H, head_dim,
+                                                        ref_cap);
+        }
         if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
     }
     prefill_len[s] = seq;
@@ -576,14 +661,36 @@ extern "C" kvd_status rswa_record_prefill(float *ref_k, float *ref_v, const floa
     return KVD_OK;
 }
 
-extern "C" kvd_status rswa_ring_write(float *ring_k, float *ring_v, const float *k, const float *v,
-                                      const int32_t *prefill_len, int32_t *ring_len,
-                                      int32_t *ring_pos, int32_t B, int32_t H, int32_t head_dim,
-                                      int32_t W, int32_t *slot_out, void *stream) {
+extern "C" kvd_status rswa_record_prefill(float *ref_k, float *ref_v, const float *k,
+                                          const float *v, int32_t s, int32_t seq, int32_t B,
+                                          int32_t H, int32_t head_dim, int64_t ref_cap, int32_t W,
+                                          int32_t *prefill_len, int32_t *ring_len,
+                                          int32_t *ring_pos, void *stream) {
+    return record_prefill(ref_k, ref_v, nullptr, k, v, s, seq, B, H, head_dim, ref_cap, W,
+                          prefill_len, ring_len, ring_pos, stream);
+}
+
+extern "C" kvd_status rswa_record_prefill_i8(float *ref_k, float *ref_v, const rswa_i8_mirror *m,
+                                             const float *k, const float *v, int32_t s, int32_t seq,
+                                             int32_t B, int32_t H, int32_t head_dim, int64_t ref_cap,
+                                             int32_t W, int32_t *prefill_len, int32_t *ring_len,
+                                             int32_t *ring_pos, void *stream) {
+    if (m == nullptr) return KVD_EINVAL;
+    return record_prefill(ref_k, ref_v, m, k, v, s, seq, B, H, head_dim, ref_cap, W, prefill_len,
+                          ring_len, ring_pos, stream);
+}
+
+static kvd_status ring_write(float *ring_k, float *ring_v, const rswa_i8_mirror *m, const float *k,
+                      const float *v, const int32_t *prefill_len, int32_t *ring_len,
+                      int32_t *ring_pos, int32_t B, int32_t H, int32_t head_dim, int32_t W,
+                      int32_t *slot_out, void *stream) {
     if (ring_k == nullptr || ring_v == nullptr || k == nullptr || v == nullptr ||
         prefill_len == nullptr || ring_len == nullptr || ring_pos == nullptr)
         return KVD_EINVAL;
     if (B < 1 || H < 1 || head_dim < 1 || W < 1) return KVD_EINVAL;
+    if (m != nullptr && (!mirror_ok(m) || (head_dim != 64 && head_dim != 128) || !aligned16(k) ||
+                         !aligned16(v) || !aligned16(ring_k) || !aligned16(ring_v)))
+        return KVD_EINVAL;
     for (int s = 0; s < B; ++s) {
         if (prefill_len[s] < 0) return KVD_ESTATE;
         if (ring_len[s] < 0 || ring_len[s] > W || ring_pos[s] < 0 || ring_pos[s] >= W)
@@ -596,10 +703,20 @@ extern "C" kvd_status rswa_ring_write(float *ring_k, float *ring_v, const float 
         t.s0 = s0;
         t.n = std::min(kSlice, B - s0);
         for (int i = 0; i < t.n; ++i) t.slot[i] = slot[s0 + i];
-        const int64_t per = int64_t(H) * head_dim;
-        dim3 grid(unsigned(std::min<int64_t>(ceil_div(per, 256), 64)), unsigned(t.n));
-        ring_write_kernel<<<grid, 256, 0, as_stream(stream)>>>(ring_k, ring_v, k, v, H, head_dim, W,
-                                                              t);
+        if (m != nullptr) {
+            const unsigned blocks = unsigned(ceil_div(int64_t(t.n) * H, 8));
+            if (head_dim == 128)
+                ring_write_i8_kernel<128><<<blocks, 256, 0, as_stream(stream)>>>(ring_k, ring_v, *m, k, v,
+                                                                                H, W, t);
+            else
+                ring_write_i8_kernel<64><<<blocks, 256, 0, as_stream(stream)>>>(ring_k, ring_v, *m, k, v,
+                                                                               H, W, t);
+        } else {
+            const int64_t per = int64_t(H) * head_dim;
+            dim3 grid(unsigned(std::min<int64_t>(ceil_div(per, 256), 64)), unsigned(t.n));
+            ring_write_kernel<<<grid, 256, 0, as_stream(stream)>>>(ring_k, ring_v, k, v, H, head_dim,
+                                                                  W, t);
+        }
         if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
     }
     for (int s = 0; s < B; ++s) {
@@ -614,6 +731,24 @@ extern "C" kvd_status rswa_ring_write(float *ring_k, float *ring_v, const float 
     return KVD_OK;
 }
 
+extern "C" kvd_status rswa_ring_write(float *ring_k, float *ring_v, const float *k, const float *v,
+                                      const int32_t *prefill_len, int32_t *ring_len,
+                                      int32_t *ring_pos, int32_t B, int32_t H, int32_t head_dim,
+                                      int32_t W, int32_t *slot_out, void *stream) {
+    return ring_write(ring_k, ring_v, nullptr, k, v, prefill_len, ring_len, ring_pos, B, H, head_dim,
+                      W, slot_out, stream);
+}
+
+extern "C" kvd_status rswa_ring_write_i8(float *ring_k, float *ring_v, const rswa_i8_mirror *m,
+                                         const float *k, const float *v, const int32_t *prefill_len,
+                                         int32_t *ring_len, int32_t *ring_pos, int32_t B, int32_t H,
+                                         int32_t head_dim, int32_t W, int32_t *slot_out,
+                                         void *stream) {
+    if (m == nullptr) return KVD_EINVAL;
+    return ring_write(ring_k, ring_v, m, k, v, prefill_len, ring_len, ring_pos, B, H, head_dim, W,
+                      slot_out, stream);
+}
+
 extern "C" kvd_status rswa_decode_workspace_bytes(int32_t B, int32_t H, int32_t head_dim,
                                                   int64_t ref_cap, int32_t W, int64_t *bytes_out) {
     if (bytes_out == nullptr || B < 1 || H < 1 || (head_dim != 64 && head_dim != 128) ||
@@ -623,23 +758,21 @@ extern "C" kvd_status rswa_decode_workspace_bytes(int32_t B, int32_t H, int32_t 
     return KVD_OK;
 }
 
-extern "C" kvd_status rswa_decode(const float *q, const float *ref_k, const float *ref_v,
-                                  const float *ring_k, const float *ring_v,
-                                  const int32_t *prefill_len, const int32_t *ring_len,
-                                  const int32_t *ring_pos, int32_t B, int32_t H, int32_t head_dim,
-                                  int64_t ref_cap, int32_t W, float scale, float *out,
-                                  void *workspace, int64_t workspace_bytes, void *stream) {
-    if (q == nullptr || ref_k == nullptr || ref_v == nullptr || ring_k == nullptr ||
-        ring_v == nullptr || prefill_len == nullptr || ring_len == nullptr || out == nullptr)
+// rswa decode over the f32 regions (I8 false) or the int8 mirror (I8 true);
+// src holds the pointers of the one that is read, already checked.
+template <bool I8>
+static kvd_status rswa_decode_impl(const float *q, const RswaSrc &src_in, const int32_t *prefill_len,
+                            const int32_t *ring_len, const int32_t *ring_pos, int32_t B, int32_t H,
+                            int32_t head_dim, int64_t ref_cap, int32_t W, float scale, float *out,
+                            void *workspace, int64_t workspace_bytes, void *stream) {
+    if (q == nullptr || prefill_len == nullptr || ring_len == nullptr || out == nullptr)
         return KVD_EINVAL;
     if (B < 1 || H < 1 || (head_dim != 64 && head_dim != 128) || ref_cap < 0 || W < 1)
         return KVD_EINVAL;
     // Bulk copies move whole 16-row groups: both regions must hold them.
     if (ref_cap % kRowAlign != 0 || W % kRowAlign != 0) return KVD_EINVAL;
     if (!std::isfinite(scale)) return KVD_EINVAL;
-    if (!aligned16(q) || !aligned16(out) || !aligned16(ref_k) || !aligned16(ref_v) ||
-        !aligned16(ring_k) || !aligned16(ring_v))
-        return KVD_EINVAL;
+    if (!aligned16(q) || !aligned16(out)) return KVD_EINVAL;
     const RswaWs w = rswa_ws(B, H, head_dim, ref_cap, W);
     if (workspace == nullptr || workspace_bytes < w.total ||
         (reinterpret_cast<uintptr_t>(workspace) & 255))
@@ -668,11 +801,7 @@ extern "C" kvd_status rswa_decode(const float *q, const float *ref_k, const floa
     a.pacc = reinterpret_cast<float *>(ws + w.pacc);
     a.scores = nullptr;
     a.err = reinterpret_cast<uint32_t *>(ws + w.err);
-    RswaSrc src;
-    src.ref_k = ref_k;
-    src.ref_v = ref_v;
-    src.ring_k = ring_k;
-    src.ring_v = ring_v;
+    RswaSrc src = src_in;
     src.ref_cap = ref_cap;
     src.W = W;
     src.H = H;
@@ -699,8 +828,8 @@ extern "C" kvd_status rswa_decode(const float *q, const float *ref_k, const floa
             max_nc = std::max(max_nc, nc);
         }
         dim3 grid(unsigned(max_nc), unsigned(H), unsigned(t.n));
-        cudaError_t e = head_dim == 128 ? launch_split_rswa<128>(a, src, t, grid, st)
-                                        : launch_split_rswa<64>(a, src, t, grid, st);
+        cudaError_t e = head_dim == 128 ? launch_split_rswa<128, I8>(a, src, t, grid, st)
+                                        : launch_split_rswa<64, I8>(a, src, t, grid, st);
         if (e != cudaSuccess) return KVD_ECUDA;
         dim3 mgrid(unsigned(H), unsigned(t.n));
         if (head_dim == 128) merge_rswa_kernel<128><<<mgrid, 128, 0, st>>>(m, t);
@@ -708,6 +837,43 @@ extern "C" kvd_status rswa_decode(const float *q, const float *ref_k, const floa
         if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
     }
     return KVD_OK;
+}
+
+extern "C" kvd_status rswa_decode(const float *q, const float *ref_k, const float *ref_v,
+                                  const float *ring_k, const float *ring_v,
+                                  const int32_t *prefill_len, const int32_t *ring_len,
+                                  const int32_t *ring_pos, int32_t B, int32_t H, int32_t head_dim,
+                                  int64_t ref_cap, int32_t W, float scale, float *out,
+                                  void *workspace, int64_t workspace_bytes, void *stream) {
+    if (ref_k == nullptr || ref_v == nullptr || ring_k == nullptr || ring_v == nullptr ||
+        !aligned16(ref_k) || !aligned16(ref_v) || !aligned16(ring_k) || !aligned16(ring_v))
+        return KVD_EINVAL;
+    RswaSrc src{};
+    src.ref_k = ref_k;
+    src.ref_v = ref_v;
+    src.ring_k = ring_k;
+    src.ring_v = ring_v;
+    return rswa_decode_impl<false>(q, src, prefill_len, ring_len, ring_pos, B, H, head_dim, ref_cap, W,
+                                   scale, out, workspace, workspace_bytes, stream);
+}
+
+extern "C" kvd_status rswa_decode_i8(const float *q, const rswa_i8_mirror *m,
+                                     const int32_t *prefill_len, const int32_t *ring_len,
+                                     const int32_t *ring_pos, int32_t B, int32_t H, int32_t head_dim,
+                                     int64_t ref_cap, int32_t W, float scale, float *out,
+                                     void *workspace, int64_t workspace_bytes, void *stream) {
+    if (!mirror_ok(m)) return KVD_EINVAL;
+    RswaSrc src{};
+    src.ref_k8 = m->ref_k;
+    src.ref_v8 = m->ref_v;
+    src.ring_k8 = m->ring_k;
+    src.ring_v8 = m->ring_v;
+    src.ref_ks = m->ref_ks;
+    src.ref_vs = m->ref_vs;
+    src.ring_ks = m->ring_ks;
+    src.ring_vs = m->ring_vs;
+    return rswa_decode_impl<true>(q, src, prefill_len, ring_len, ring_pos, B, H, head_dim, ref_cap, W,
+                                  scale, out, workspace, workspace_bytes, stream);
 }
 
 extern "C" kvd_status rswa_device_error(const void *workspace, int32_t clear, uint32_t *word_out) {

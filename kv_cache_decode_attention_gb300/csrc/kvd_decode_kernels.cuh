@@ -37,24 +37,26 @@ constexpr int ce_min(int a, int b) { return a < b ? a : b; }
 constexpr int ce_log2(int x) { return x <= 1 ? 0 : 1 + ce_log2(x / 2); }
 constexpr int ce_round(int x, int a) { return (x + a - 1) / a * a; }
 
-// Tile geometry for a head dim and storage mode.
-template <int HD, bool KQ, bool VQ>
+// Tile geometry for a head dim and storage mode.  KI8: int8 K codes with
+// one scale per row (the R-SWA int8 mirror) instead of one per 32 channels.
+template <int HD, bool KQ, bool VQ, bool KI8 = false>
 struct TileCfg {
     static constexpr int NG = HD / kKGroup;
+    static constexpr int NKS = KI8 ? 1 : NG;  // K scales per row
     static constexpr int CPL = HD / 32;  // channels per lane
     static constexpr int KROW = KQ ? HD : 4 * HD;
     static constexpr int VROW = VQ ? HD : 4 * HD;
     static constexpr int TR = ce_min(256, 16384 / ce_max(KROW, VROW));  // rows per tile
     static constexpr int KS_OFF = TR * KROW;
-    static constexpr int VS_OFF = KS_OFF + (KQ ? TR * NG * 4 : 0);
+    static constexpr int VS_OFF = KS_OFF + (KQ ? TR * NKS * 4 : 0);
     static constexpr int KSEG = VS_OFF + (VQ ? TR * 4 : 0);
     static constexpr int VSEG = TR * VROW;
     static constexpr int SLOT = ce_round(ce_max(KSEG, VSEG), 128);
 };
 
-template <int HD, int HPK, bool KQ, bool VQ>
-struct SplitCfg : TileCfg<HD, KQ, VQ> {
-    using T = TileCfg<HD, KQ, VQ>;
+template <int HD, int HPK, bool KQ, bool VQ, bool KI8 = false>
+struct SplitCfg : TileCfg<HD, KQ, VQ, KI8> {
+    using T = TileCfg<HD, KQ, VQ, KI8>;
     static constexpr int RPW = T::TR / kWarps;             // score rows per warp per tile
     static constexpr int RB = ce_min(32 / HPK, RPW);       // rows per reduce batch
     static constexpr int E = RB * HPK;                     // entries per reduce (<= 32)
@@ -154,10 +156,10 @@ __device__ __forceinline__ void load_lane(const char *row, int lane, float (&x)[
     }
 }
 
-template <int HD, int HPK, bool KQ, bool VQ>
+template <int HD, int HPK, bool KQ, bool VQ, bool KI8>
 __device__ __forceinline__ void issue_segment(const ChunkInfo &ci, char *smem, uint64_t *bar,
                                               int j) {
-    using C = SplitCfg<HD, HPK, KQ, VQ>;
+    using C = SplitCfg<HD, HPK, KQ, VQ, KI8>;
     const int slot = j % kNSeg;
     const int t = j >> 1;
     const int row0 = t * C::TR;
@@ -166,12 +168,12 @@ __device__ __forceinline__ void issue_segment(const ChunkInfo &ci, char *smem, u
     char *dst = smem + slot * C::SLOT;
     if ((j & 1) == 0) {
         uint32_t bytes = uint32_t(rows) * C::KROW;
-        if (KQ) bytes += uint32_t(rows) * C::NG * 4;
+        if (KQ) bytes += uint32_t(rows) * C::NKS * 4;
         if (VQ) bytes += uint32_t(rows) * 4;
         mbar_arrive_expect_tx(&bar[slot], bytes);
         bulk_g2s(dst, ci.k + int64_t(row0) * C::KROW, uint32_t(rows) * C::KROW, &bar[slot]);
         if (KQ)
-            bulk_g2s(dst + C::KS_OFF, ci.ks + int64_t(row0) * C::NG * 4, uint32_t(rows) * C::NG * 4,
+            bulk_g2s(dst + C::KS_OFF, ci.ks + int64_t(row0) * C::NKS * 4, uint32_t(rows) * C::NKS * 4,
                      &bar[slot]);
         if (VQ)
             bulk_g2s(dst + C::VS_OFF, ci.vs + int64_t(row0) * 4, uint32_t(rows) * 4, &bar[slot]);
@@ -182,10 +184,21 @@ __device__ __forceinline__ void issue_segment(const ChunkInfo &ci, char *smem, u
     }
 }
 
+// Quantise one f32 value against a row scale as rswa quantize_row_i8 does:
+// IEEE division, round half to even, clamp to [-127, 127].
+__device__ __forceinline__ int quant_code_i8(float x, float sc) {
+    const float t = rintf(__fdiv_rn(x, sc));
+    return int(fminf(fmaxf(t, -127.0f), 127.0f));
+}
+
 // OPT: the call has a window or a softcap (compiled out of the common path).
-template <int HD, int HPK, bool KQ, bool VQ, bool OPT>
+// KI8: the R-SWA int8 mirror (one query head, int8 K with one scale per row):
+// the query is quantised per head like a cache row and the QK dot is the
+// exact integer dot of the codes, scaled by qscale * kscale[row] after.
+template <int HD, int HPK, bool KQ, bool VQ, bool OPT, bool KI8 = false>
 __device__ void split_body(const ChunkInfo &ci, const SplitArgs &a, char *smem) {
-    using C = SplitCfg<HD, HPK, KQ, VQ>;
+    using C = SplitCfg<HD, HPK, KQ, VQ, KI8>;
+    static_assert(!KI8 || (KQ && HPK == 1), "the int8 mirror has int8 K and one head per group");
     constexpr int CPL = C::CPL, TR = C::TR;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     float *sc = reinterpret_cast<float *>(smem + C::SC_OFF);
@@ -205,17 +218,33 @@ __device__ void split_body(const ChunkInfo &ci, const SplitArgs &a, char *smem) 
     if (tid < HPK) mrun[tid] = -INFINITY;
     __syncthreads();
     if (tid == 0)
-        for (int j = 0; j < min(kNSeg, nseg); ++j) issue_segment<HD, HPK, KQ, VQ>(ci, smem, bar, j);
+        for (int j = 0; j < min(kNSeg, nseg); ++j) issue_segment<HD, HPK, KQ, VQ, KI8>(ci, smem, bar, j);
 
     // Query of every head of the group for this lane's channels, with the
     // K field and the softmax scale (in log2 units) folded in.
     float qr[HPK][CPL];
+    uint32_t qi = 0;     // KI8: this lane's query codes, packed bytes
+    float qfac = 0.0f;   // KI8: qscale * softmax scale * log2(e)
+    if (KI8) {
+        float x[CPL], mx = 0.0f;
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+            x[j] = ci.q[lane * CPL + j];
+            mx = fmaxf(mx, fabsf(x[j]));
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        const float sq = mx > 0.0f ? __fdiv_rn(mx, 127.0f) : 1.0f;
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) qi |= (uint32_t(quant_code_i8(x[j], sq)) & 0xffu) << (8 * j);
+        qfac = sq * a.qscale;
+    }
 #pragma unroll
     for (int h = 0; h < HPK; ++h) {
 #pragma unroll
         for (int j = 0; j < CPL; ++j) {
             float x = 0.0f;
-            if (h < a.hpk) {
+            if (!KI8 && h < a.hpk) {
                 x = ci.q[h * HD + lane * CPL + j];
                 if (KQ) x *= ci.kcol[lane * CPL + j];
                 x *= a.qscale;
@@ -250,6 +279,15 @@ __device__ void split_body(const ChunkInfo &ci, const SplitArgs &a, char *smem) 
             float v[C::E];
 #pragma unroll
             for (int r = 0; r < C::RB; ++r) {
+                if (KI8) {
+                    // exact: |partial| <= 4 * 127 * 127 and every sum of the
+                    // reduction stays an integer below 2^24
+                    const char *kr = kseg + (rbase + r) * C::KROW;
+                    const uint32_t kw = CPL == 4 ? reinterpret_cast<const uint32_t *>(kr)[lane]
+                                                 : uint32_t(reinterpret_cast<const uint16_t *>(kr)[lane]);
+                    v[r] = float(__dp4a(int(qi), int(kw), 0));
+                    continue;
+                }
                 float x[CPL];
                 load_lane<CPL, KQ>(kseg + (rbase + r) * C::KROW, lane, x);
                 float gs = 1.0f;
@@ -264,10 +302,11 @@ __device__ void split_body(const ChunkInfo &ci, const SplitArgs &a, char *smem) 
                     v[r * HPK + h] = KQ ? p * gs : p;
                 }
             }
-            const float s = reduce_scatter<C::E, C::LOGE>(v, lane);
+            float s = reduce_scatter<C::E, C::LOGE>(v, lane);
             if ((lane & ((32 >> C::LOGE) - 1)) == 0) {
                 const int e = lane >> (5 - C::LOGE);
                 const int r = rbase + e / HPK, h = e % HPK;
+                if (KI8) s = s * reinterpret_cast<const float *>(kseg + C::KS_OFF)[r] * qfac;
                 const bool vis = r < nt && (!OPT || row0 + r >= ci.lo);
                 const float sv =
                     vis ? (OPT && a.softcap2 > 0.0f ? softcap_log2(s, a.softcap2) : s) : -INFINITY;
@@ -310,7 +349,7 @@ __device__ void split_body(const ChunkInfo &ci, const SplitArgs &a, char *smem) 
             }
         }
         __syncthreads();  // K slot drained, weights visible
-        if (tid == 0 && j + kNSeg < nseg) issue_segment<HD, HPK, KQ, VQ>(ci, smem, bar, j + kNSeg);
+        if (tid == 0 && j + kNSeg < nseg) issue_segment<HD, HPK, KQ, VQ, KI8>(ci, smem, bar, j + kNSeg);
         // ---------------------------------------------------- V tile
         j = 2 * t + 1;
         slot = j % kNSeg;
@@ -355,7 +394,7 @@ __device__ void split_body(const ChunkInfo &ci, const SplitArgs &a, char *smem) 
             for (int jj = 0; jj < CPL; ++jj) acc[h][jj] = fmaf(acc[h][jj], al, tacc[h][jj]);
         }
         __syncthreads();  // V slot drained
-        if (tid == 0 && j + kNSeg < nseg) issue_segment<HD, HPK, KQ, VQ>(ci, smem, bar, j + kNSeg);
+        if (tid == 0 && j + kNSeg < nseg) issue_segment<HD, HPK, KQ, VQ, KI8>(ci, smem, bar, j + kNSeg);
     }
 
     if (!ok) {  // block-uniform (decided by __syncthreads_or above)
@@ -372,7 +411,6 @@ __device__ void split_body(const ChunkInfo &ci, const SplitArgs &a, char *smem) 
 
     // ------------------------------------------------------ partial out
     {
-        const int h = tid % HPK;
         float l = lsum;
 #pragma unroll
         for (int off = HPK; off < 32; off <<= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
@@ -456,12 +494,16 @@ struct RswaTable {
 };
 
 struct RswaSrc {
-    const float *ref_k, *ref_v, *ring_k, *ring_v;
+    const float *ref_k, *ref_v, *ring_k, *ring_v;      // f32 regions
+    const int8_t *ref_k8, *ref_v8, *ring_k8, *ring_v8;  // int8 mirror codes
+    const float *ref_ks, *ref_vs, *ring_ks, *ring_vs;   // int8 mirror row scales
     int64_t ref_cap;
     int32_t W, H;
 };
 
-template <int HD>
+// I8: read the int8 mirror (rswa decode_attention_int8) instead of the f32
+// regions (decode_attention_scalar_head).
+template <int HD, bool I8>
 __global__ void __launch_bounds__(kThreads, 2) split_rswa_kernel(SplitArgs a, RswaSrc src,
                                                                  RswaTable tb) {
     extern __shared__ __align__(128) char smem[];
@@ -473,28 +515,42 @@ __global__ void __launch_bounds__(kThreads, 2) split_rswa_kernel(SplitArgs a, Rs
     const int ncr = (rl + a.chunk - 1) / a.chunk;
     ChunkInfo ci;
     const int64_t head = int64_t(s) * src.H + h;
+    ci.ks = ci.vs = nullptr;
     if (c < ncp) {
         const int64_t row = head * src.ref_cap + int64_t(c) * a.chunk;
-        ci.k = reinterpret_cast<const char *>(src.ref_k + row * HD);
-        ci.v = reinterpret_cast<const char *>(src.ref_v + row * HD);
+        if (I8) {
+            ci.k = reinterpret_cast<const char *>(src.ref_k8 + row * HD);
+            ci.v = reinterpret_cast<const char *>(src.ref_v8 + row * HD);
+            ci.ks = reinterpret_cast<const char *>(src.ref_ks + row);
+            ci.vs = reinterpret_cast<const char *>(src.ref_vs + row);
+        } else {
+            ci.k = reinterpret_cast<const char *>(src.ref_k + row * HD);
+            ci.v = reinterpret_cast<const char *>(src.ref_v + row * HD);
+        }
         ci.n = min(a.chunk, pl - c * a.chunk);
     } else if (c - ncp < ncr) {
         const int cr = c - ncp;
         const int64_t row = head * src.W + int64_t(cr) * a.chunk;
-        ci.k = reinterpret_cast<const char *>(src.ring_k + row * HD);
-        ci.v = reinterpret_cast<const char *>(src.ring_v + row * HD);
+        if (I8) {
+            ci.k = reinterpret_cast<const char *>(src.ring_k8 + row * HD);
+            ci.v = reinterpret_cast<const char *>(src.ring_v8 + row * HD);
+            ci.ks = reinterpret_cast<const char *>(src.ring_ks + row);
+            ci.vs = reinterpret_cast<const char *>(src.ring_vs + row);
+        } else {
+            ci.k = reinterpret_cast<const char *>(src.ring_k + row * HD);
+            ci.v = reinterpret_cast<const char *>(src.ring_v + row * HD);
+        }
         ci.n = min(a.chunk, rl - cr * a.chunk);
     } else {
         return;
     }
-    ci.ks = ci.vs = nullptr;
     ci.lo = 0;
     ci.pidx0 = (head * a.nc_max + c) * 1;
     ci.q = a.q + head * HD;
     ci.kcol = nullptr;
     ci.score0 = -1;
     ci.score_ld = 0;
-    split_body<HD, 1, false, false, false>(ci, a, smem);
+    split_body<HD, 1, I8, I8, false, I8>(ci, a, smem);
 }
 
 // ---------------------------------------------------------------- merge

@@ -171,8 +171,8 @@ class RswaWorkload:
         return synthetic.torch_normal((self.cache.B, self.H, self.hd), self.seed * 7919 + t, device)
 
 
-def rswa_steady(device="cuda", B=16, prefill=32640, steps=500, seed=3):
-    cache = api.RingCache(B, prefill, 10, 128, 128, device=device)
+def rswa_steady(device="cuda", B=16, prefill=32640, steps=500, seed=3, int8=False):
+    cache = api.RingCache(B, prefill, 10, 128, 128, device=device, int8=int8)
     wl = RswaWorkload(cache, seed, prefill, steps)
     for s in range(B):
         k, v = wl.prefill_rows(s, device)
@@ -220,3 +220,9 @@ def append_bytes(mode, n_live, hd, n_seq) -> int:
 
 def rswa_bytes(B, H, hd, lengths) -> int:
     return int(np.sum(lengths)) * H * hd * 8 + 2 * B * H * hd * 4
+
+
+def rswa_i8_bytes(B, H, hd, lengths) -> int:
+    """Algorithmic bytes of one int8-mirror decode: every row's K and V codes and
+    their two row scales, plus the f32 query and output."""
+    return int(np.sum(lengths)) * H * (2 * hd + 8) + 2 * B * H * hd * 4

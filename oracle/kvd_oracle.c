@@ -134,6 +134,14 @@ float kvo_quantize_row_i8(const float *x, int n, int8_t *q)
     return sc;
 }
 
+/* quantize_row_i8 on n_rows consecutive rows of n values (the int8 mirror
+ * of a whole region): codes [n_rows][n], scales [n_rows]. */
+void kvo_quantize_rows_i8(const float *x, long long n_rows, int n, int8_t *q, float *scales)
+{
+    for (long long r = 0; r < n_rows; ++r)
+        scales[r] = kvo_quantize_row_i8(x + (size_t)r * (size_t)n, n, q + (size_t)r * (size_t)n);
+}
+
 /* ---- storage addressing ------------------------------------------------ */
 
 static size_t row_off(const kvo_cache *c, int h, int p)

@@ -56,6 +56,8 @@ def lib():
             L.kvo_quant_row.restype = None
             L.kvo_quantize_row_i8.argtypes = [vp, i32, vp]
             L.kvo_quantize_row_i8.restype = f32
+            L.kvo_quantize_rows_i8.argtypes = [vp, C.c_longlong, i32, vp, vp]
+            L.kvo_quantize_rows_i8.restype = None
             L.kvo_needs_freeze.argtypes = [C.POINTER(_Cache)]
             L.kvo_freeze.argtypes = [C.POINTER(_Cache)]
             L.kvo_freeze.restype = None
@@ -282,12 +284,13 @@ def rswa_mirror(rows):
     """rswa int8 mirror of f32 rows [..., hd]: quantize_row_i8 on every row.
     Returns (codes int8 [..., hd], scales f32 [...])."""
     rows = np.ascontiguousarray(rows, dtype=np.float32)
-    flat = rows.reshape(-1, rows.shape[-1])
-    codes = np.zeros(flat.shape, np.int8)
-    scales = np.zeros(flat.shape[0], np.float32)
-    for i in range(flat.shape[0]):
-        codes[i], scales[i] = quantize_row_i8(flat[i])
-    return codes.reshape(rows.shape), scales.reshape(rows.shape[:-1])
+    n = rows.shape[-1]
+    n_rows = rows.size // n if n else 0
+    codes = np.zeros(rows.shape, np.int8)
+    scales = np.zeros(rows.shape[:-1], np.float32)
+    if n_rows:
+        lib().kvo_quantize_rows_i8(_p(rows), n_rows, n, _p(codes), _p(scales))
+    return codes, scales
 
 
 def rswa_decode_i8(q, ref_k8, ref_ks, ref_v8, ref_vs, prefill_len, ring_k8, ring_ks, ring_v8,

@@ -186,3 +186,44 @@ def test_rswa_steady_full_size(env):
         assert err <= OUT_TOL, (s, err)
     del wl, c
     torch.cuda.empty_cache()
+
+
+def test_rswa_i8_steady_full_size(env):
+    """The same workload with the int8 mirror (about 1.4 GB of codes and scales
+    read per decode): the ring mirror bit-exact, the reference mirror of two
+    sampled streams bit-exact, and their decode_attention_int8 outputs against
+    the oracle."""
+    torch, kvd, W = env
+    wl = W.rswa_steady(int8=True)
+    c = wl.cache
+    q = wl.query(0)
+    out = kvd.rswa_decode_i8(q, c).cpu().numpy()
+    assert c.device_error() == 0
+    qh = q.cpu().numpy()
+    scale = np.float32(1.0 / math.sqrt(128))
+    ring_k = np.zeros((c.B, c.H, c.W, c.head_dim), np.float32)
+    ring_v = np.zeros_like(ring_k)
+    cursors = [np.zeros(2, np.int32) for _ in range(c.B)]
+    for t in range(wl.steps):
+        k, v = wl.step_rows(t)
+        k, v = k.cpu().numpy(), v.cpu().numpy()
+        for s in range(c.B):
+            oracle.rswa_write(ring_k[s], ring_v[s], k[s], v[s], True, cursors[s])
+    gk8, gks = oracle.rswa_mirror(ring_k)
+    gv8, gvs = oracle.rswa_mirror(ring_v)
+    assert np.array_equal(c.ring_k8.cpu().numpy(), gk8)
+    assert np.array_equal(c.ring_v8.cpu().numpy(), gv8)
+    assert np.array_equal(c.ring_ks.cpu().numpy().view(np.uint32), gks.view(np.uint32))
+    assert np.array_equal(c.ring_vs.cpu().numpy().view(np.uint32), gvs.view(np.uint32))
+    for s in (3, 15):
+        pk, pv = wl.prefill_rows(s)
+        rk8, rks = oracle.rswa_mirror(pk.cpu().numpy())
+        rv8, rvs = oracle.rswa_mirror(pv.cpu().numpy())
+        assert np.array_equal(c.ref_k8[s].cpu().numpy(), rk8)
+        assert np.array_equal(c.ref_vs[s].cpu().numpy().view(np.uint32), rvs.view(np.uint32))
+        ref = oracle.rswa_decode_i8(qh[s], rk8, rks, rv8, rvs, wl.prefill, gk8[s], gks[s], gv8[s], gvs[s],
+                                    cursors[s][0], scale)
+        err = out_error(out[s].reshape(c.H, c.head_dim), ref)
+        assert err <= OUT_TOL, (s, err)
+    del wl, c
+    torch.cuda.empty_cache()

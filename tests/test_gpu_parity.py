@@ -327,3 +327,143 @@ def test_rswa_errors_do_not_mutate(torch, kvd):
         kvd.rswa_record_prefill(cache, 0, torch.ones(10, 40, 128, device="cuda"),
                                 torch.ones(10, 40, 128, device="cuda"))
     assert e.value.status == -2 and cache.prefill_len.tolist() == [4, 0]
+
+
+# ------------------------------------------------- R-SWA int8 mirror (NEXT-2)
+
+def _mirror_of(ref_k, ref_v, ring_k, ring_v):
+    rk8, rks = oracle.rswa_mirror(ref_k)
+    rv8, rvs = oracle.rswa_mirror(ref_v)
+    gk8, gks = oracle.rswa_mirror(ring_k)
+    gv8, gvs = oracle.rswa_mirror(ring_v)
+    return rk8, rks, rv8, rvs, gk8, gks, gv8, gvs
+
+
+@pytest.mark.parametrize("hd,H", [(128, 10), (64, 4)])
+def test_rswa_i8_mirror_and_decode_parity(torch, kvd, hd, H):
+    """Three streams (reference 37, 0 and 700 rows), 150 decode steps that wrap
+    the ring: the int8 mirror (codes and row scales) is bit-exact with the
+    oracle's quantize_row_i8 of the f32 rows, the f32 regions are still written,
+    and decode_attention_int8 outputs match the oracle at several steps."""
+    B, W, ref_cap = 3, 128, 1024
+    prefill = [37, 0, 700]
+    cache = kvd.RingCache(B, ref_cap, H, hd, W, int8=True)
+    o_ref_k = np.zeros((B, H, ref_cap, hd), np.float32)
+    o_ref_v = np.zeros_like(o_ref_k)
+    o_ring_k = np.zeros((B, H, W, hd), np.float32)
+    o_ring_v = np.zeros_like(o_ring_k)
+    cursors = [np.zeros(2, np.int32) for _ in range(B)]
+    for s in range(B):
+        m = prefill[s]
+        k = synthetic.normal((H, m, hd), 300 * s + 1)
+        v = synthetic.normal((H, m, hd), 300 * s + 2) * np.float32(3.0)
+        kvd.rswa_record_prefill(cache, s, torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda())
+        o_ref_k[s, :, :m] = k
+        o_ref_v[s, :, :m] = v
+        if m:
+            ck, sk = oracle.rswa_mirror(k)
+            cv, sv = oracle.rswa_mirror(v)
+            assert np.array_equal(cache.ref_k8[s, :, :m].cpu().numpy(), ck)
+            assert np.array_equal(cache.ref_ks[s, :, :m].cpu().numpy().view(np.uint32), sk.view(np.uint32))
+            assert np.array_equal(cache.ref_v8[s, :, :m].cpu().numpy(), cv)
+            assert np.array_equal(cache.ref_vs[s, :, :m].cpu().numpy().view(np.uint32), sv.view(np.uint32))
+    assert np.array_equal(cache.ref_k.cpu().numpy(), o_ref_k)
+    scale = np.float32(1.0 / math.sqrt(hd))
+    for t in range(150):
+        kt = synthetic.normal((B, H, hd), 7000 + t)
+        vt = synthetic.normal((B, H, hd), 8000 + t)
+        qt = synthetic.normal((B, H, hd), 9000 + t)
+        slots = kvd.rswa_ring_write(cache, torch.from_numpy(kt).cuda(), torch.from_numpy(vt).cuda())
+        for s in range(B):
+            assert slots[s] == oracle.rswa_write(o_ring_k[s], o_ring_v[s], kt[s], vt[s], True, cursors[s])
+            assert cache.ring_len[s] == cursors[s][0] and cache.ring_pos[s] == cursors[s][1]
+        if t in (0, 1, 127, 128, 149):
+            out = kvd.rswa_decode_i8(torch.from_numpy(qt).cuda(), cache).cpu().numpy()
+            for s in range(B):
+                mir = _mirror_of(o_ref_k[s], o_ref_v[s], o_ring_k[s], o_ring_v[s])
+                ref = oracle.rswa_decode_i8(qt[s], mir[0], mir[1], mir[2], mir[3], prefill[s], mir[4],
+                                            mir[5], mir[6], mir[7], cursors[s][0], scale)
+                err = out_error(out[s].reshape(H, hd), ref)
+                assert err <= OUT_TOL, (t, s, err)
+    assert np.array_equal(cache.ring_k.cpu().numpy(), o_ring_k)
+    assert np.array_equal(cache.ring_v.cpu().numpy(), o_ring_v)
+    gk8, gks = oracle.rswa_mirror(o_ring_k)
+    gv8, gvs = oracle.rswa_mirror(o_ring_v)
+    assert np.array_equal(cache.ring_k8.cpu().numpy(), gk8)
+    assert np.array_equal(cache.ring_v8.cpu().numpy(), gv8)
+    assert np.array_equal(cache.ring_ks.cpu().numpy().view(np.uint32), gks.view(np.uint32))
+    assert np.array_equal(cache.ring_vs.cpu().numpy().view(np.uint32), gvs.view(np.uint32))
+    assert cache.device_error() == 0
+
+
+def _bits(b):
+    return np.frombuffer(np.uint32(b).tobytes(), np.float32)[0]
+
+
+def test_rswa_i8_quantiser_edge_rows_on_gpu(torch, kvd):
+    """The page's worked rows through the device quantiser: ties to even, the
+    division-not-reciprocal fixture, an all-zero row (scale 1.0), and rows whose
+    magnitude sweeps 2^-20 .. 2^20 (the page's LCG contract) are bit-exact with
+    the oracle and the printed codes."""
+    from conftest import load_golden
+
+    H, hd = 10, 128
+    ties = load_golden("quant_ties_to_even.txt")
+    div = load_golden("quant_division.txt")
+    rows = np.zeros((H, 48, hd), np.float32)
+    rows[0, 0, :9] = [float(x) for x in ties["row_head"].split()]
+    rows[0, 1, 0], rows[0, 1, 1] = _bits(int(div["x0_bits"], 16)), _bits(int(div["x1_bits"], 16))
+    state = 0xD1B54A32D192ED03
+    for i in range(2, 43):
+        mag = np.float32(2.0) ** np.float32(i - 2 - 20)
+        for d in range(hd):
+            state = (state * 6364136223846793005 + 1442695040888963407) & (2 ** 64 - 1)
+            unit = np.float32((state >> 40) & 0xFFFFFFFF) / np.float32((1 << 24) - 1)
+            rows[1 + i % (H - 1), i, d] = (unit * np.float32(2.0) - np.float32(1.0)) * mag
+    cache = kvd.RingCache(1, 48, H, hd, 128, int8=True)
+    t = torch.from_numpy(rows).cuda()
+    kvd.rswa_record_prefill(cache, 0, t, t)
+    codes = cache.ref_k8[0].cpu().numpy()
+    scales = cache.ref_ks[0].cpu().numpy()
+    assert codes[0, 0, :9].tolist() == [int(x) for x in ties["codes_head"].split()]
+    assert scales[0, 0].view(np.uint32) == int(ties["scale_bits"], 16)
+    assert codes[0, 1, :2].tolist() == [int(x) for x in div["codes"].split()]
+    assert scales[0, 47] == np.float32(1.0) and not codes[0, 47].any()  # an all-zero row
+    ck, sk = oracle.rswa_mirror(rows)
+    assert np.array_equal(codes, ck)
+    assert np.array_equal(scales.view(np.uint32), sk.view(np.uint32))
+    assert np.array_equal(cache.ref_v8[0].cpu().numpy(), ck)
+
+
+def test_rswa_i8_errors(torch, kvd):
+    plain = kvd.RingCache(1, 32, 10, 128, 128)
+    t = torch.ones(1, 10, 128, device="cuda")
+    with pytest.raises(ValueError):
+        kvd.rswa_decode_i8(t, plain)
+    cache = kvd.RingCache(2, 32, 10, 128, 128, int8=True)
+    t2 = torch.ones(2, 10, 128, device="cuda")
+    with pytest.raises(kvd.KvdError) as e:
+        kvd.rswa_decode_i8(t2, cache)
+    assert e.value.status == -3
+    with pytest.raises(kvd.KvdError) as e:
+        kvd.rswa_ring_write(cache, t2, t2)
+    assert e.value.status == -3 and cache.ring_len.tolist() == [0, 0]
+    kvd.rswa_record_prefill(cache, 0, torch.ones(10, 4, 128, device="cuda"),
+                            torch.ones(10, 4, 128, device="cuda"))
+    kvd.rswa_record_prefill(cache, 1, torch.ones(10, 0, 128, device="cuda"),
+                            torch.ones(10, 0, 128, device="cuda"))
+    with pytest.raises(kvd.KvdError) as e:  # stream 1 has no keys at all
+        kvd.rswa_decode_i8(t2, cache)
+    assert e.value.status == -4
+    # the mirror writers take head_dim 64 or 128 only, and a mirror is required
+    import ctypes as C
+
+    lib = kvd.lib()
+    x = torch.ones(10, 4, 96, device="cuda")
+    pl, rl, rp = (np.array(a, np.int32) for a in (cache.prefill_len, cache.ring_len, cache.ring_pos))
+    args = (C.c_void_p(x.data_ptr()), C.c_void_p(x.data_ptr()), 0, 4, 2, 10, 96, 32, 128,
+            pl.ctypes.data_as(C.c_void_p), rl.ctypes.data_as(C.c_void_p), rp.ctypes.data_as(C.c_void_p), None)
+    ref = (C.c_void_p(cache.ref_k.data_ptr()), C.c_void_p(cache.ref_v.data_ptr()))
+    assert lib.rswa_record_prefill_i8(*ref, C.byref(cache.mirror), *args) == -1
+    assert lib.rswa_record_prefill_i8(*ref, None, *args) == -1
+    assert pl.tolist() == [4, 0]
