@@ -12,6 +12,12 @@ exactly --steps steps between a barrier + device synchronisation on each side;
 --warmup steps run untimed first.  Two cache replicas alternate step by step
 so that every step streams HBM, not L2 (2 x 289 MB > 129 MB of L2).
 
+Other workloads (--workload): long_q8 (4 sequences x 131072 rows, 64 query /
+4 KV heads), tiny_f32, and the R-SWA decode of franken_ocr's rswa module
+(16 streams x 10 heads, a 32640-row reference block + a full 128-slot ring):
+rswa reads the f32 regions, rswa_i8 the int8 mirror; one step = the ring
+write of one token per stream (mirror included) + the decode of every stream.
+
 Under torchrun each rank times its own replica on its own GPU (independent
 sequences: weak scaling, no data-path collective); rank 0 prints one JSON line
 with the whole-job value.  `--impl reference` times the CPU oracle instead.
@@ -174,6 +180,60 @@ def oracle_sample_gbs(wl, n_seq_sample: int, min_seconds: float, max_reps: int |
     return bytes_per / per_rep / 1e9, per_rep, bytes_per
 
 
+class RswaOracleSample:
+    """One stream of an R-SWA workload rebuilt on the host from the workload's
+    generators (its reference rows and the ring rows of its 500 writes), ready
+    for the CPU oracle's decode (f32 regions, or their int8 mirror)."""
+
+    def __init__(self, wl, int8: bool, s: int = 0):
+        import oracle
+
+        c = wl.cache
+        self.int8, self.H, self.hd = int8, c.H, c.head_dim
+        pk, pv = wl.prefill_rows(s)
+        self.ref_k, self.ref_v = pk.cpu().numpy(), pv.cpu().numpy()
+        self.ring_k = np.zeros((c.H, c.W, c.head_dim), np.float32)
+        self.ring_v = np.zeros_like(self.ring_k)
+        cur = np.zeros(2, np.int32)
+        for t in range(wl.steps):
+            k, v = wl.step_rows(t)
+            oracle.rswa_write(self.ring_k, self.ring_v, k[s].cpu().numpy(), v[s].cpu().numpy(), True, cur)
+        self.prefill, self.ring_len = wl.prefill, int(cur[0])
+        self.q = wl.query(10_000)[s].cpu().numpy()
+        if int8:
+            self.mir = [oracle.rswa_mirror(x) for x in (self.ref_k, self.ref_v, self.ring_k, self.ring_v)]
+        self.rows = self.prefill + self.ring_len
+        from kv_cache_decode_attention_gb300 import workloads as W
+
+        self.bytes = (W.rswa_i8_bytes if int8 else W.rswa_bytes)(1, c.H, c.head_dim, [self.rows])
+
+    def decode(self):
+        import oracle
+
+        scale = np.float32(1.0 / math.sqrt(self.hd))
+        if self.int8:
+            (rk, rks), (rv, rvs), (gk, gks), (gv, gvs) = self.mir
+            return oracle.rswa_decode_i8(self.q, rk, rks, rv, rvs, self.prefill, gk, gks, gv, gvs,
+                                         self.ring_len, scale)
+        return oracle.rswa_decode(self.q, self.ref_k, self.ref_v, self.prefill, self.ring_k, self.ring_v,
+                                  self.ring_len, scale)
+
+    def gbs(self, min_seconds: float, max_reps: int | None = None):
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            self.decode()
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= min_seconds or (max_reps is not None and reps >= max_reps):
+                break
+        per = el / reps
+        return self.bytes / per / 1e9, per
+
+    def describe(self, wl):
+        return "1 of %d streams (all %d heads, %d rows), %s, f64 softmax" % (
+            wl.cache.B, self.H, self.rows, "int8 mirror" if self.int8 else "f32 regions")
+
+
 def run_reference(args, rank):
     """--impl reference: the CPU oracle as it stands, on the host cores, each
     step a bounded sample (one sequence, every head and cached row) of the
@@ -187,20 +247,26 @@ def run_reference(args, rank):
     if not torch.cuda.is_available():
         print(json.dumps({"impl": "reference", "unavailable": "needs the GPU box to build the workload"}))
         return
-    wl = build_workload(args.workload, replicas=1)[0]
-    # warm-up and timed steps: one oracle decode of the sampled sequence each
-    gbs_w, _, _ = oracle_sample_gbs(wl, 1, 0.0, max_reps=max(1, args.warmup))
-    t0 = time.perf_counter()
-    gbs, per, nbytes = oracle_sample_gbs(wl, 1, 0.0, max_reps=args.steps)
-    el = time.perf_counter() - t0
-    sample = "1 of %d sequences (all %d query heads, %d rows), f64 two-pass softmax" % (
-        wl.n_seq, wl.n_q, int(wl.lengths[0]))
+    if args.workload in RSWA_WORKLOADS:
+        wl = W.rswa_steady(B=args.rswa_streams, int8=args.workload == "rswa_i8")
+        smp = RswaOracleSample(wl, args.workload == "rswa_i8")
+        smp.gbs(0.0, max_reps=max(1, args.warmup))
+        gbs, per = smp.gbs(0.0, max_reps=args.steps)
+        sample, name = smp.describe(wl), args.workload + "_steady"
+    else:
+        wl = build_workload(args.workload, replicas=1)[0]
+        # warm-up and timed steps: one oracle decode of the sampled sequence each
+        gbs_w, _, _ = oracle_sample_gbs(wl, 1, 0.0, max_reps=max(1, args.warmup))
+        gbs, per, nbytes = oracle_sample_gbs(wl, 1, 0.0, max_reps=args.steps)
+        sample = "1 of %d sequences (all %d query heads, %d rows), f64 two-pass softmax" % (
+            wl.n_seq, wl.n_q, int(wl.lengths[0]))
+        name = wl.name
     line = {
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(per * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "sample": sample},
+        "config": {"workload": name, "sample": sample},
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -211,6 +277,139 @@ def run_reference(args, rank):
 
 
 # ------------------------------------------------------------------ GPU arm
+
+RSWA_WORKLOADS = ("rswa", "rswa_i8")
+
+
+def run_gpu_rswa(args, rank, world):
+    """The R-SWA workloads: 16 streams in steady state (reference 32640 rows +
+    a full ring), one step = rswa ring write of one token per stream + decode
+    of every stream (f32 regions or the int8 mirror)."""
+    import torch
+
+    import kv_cache_decode_attention_gb300 as kvd
+    from kv_cache_decode_attention_gb300 import replicas
+    from kv_cache_decode_attention_gb300 import workloads as W
+
+    int8 = args.workload == "rswa_i8"
+    dev = torch.device("cuda", replicas.rank_info().local_rank)
+    torch.cuda.set_device(dev)
+    wl = W.rswa_steady(B=args.rswa_streams, int8=int8)
+    c = wl.cache
+    decode = kvd.rswa_decode_i8 if int8 else kvd.rswa_decode
+    B, H, hd = c.B, c.H, c.head_dim
+    lengths = c.prefill_len + c.ring_len  # steady state: constant over the steps
+    dec_bytes = (W.rswa_i8_bytes if int8 else W.rswa_bytes)(B, H, hd, lengths)
+    # ring write: read k, v; write the f32 rows (+ codes and scales with the mirror)
+    wr_bytes = B * H * hd * 4 * 4 + (B * H * (2 * hd + 8) if int8 else 0)
+    qs = [wl.query(i, dev) for i in range(8)]
+    news = [wl.step_rows(wl.steps + i, dev) for i in range(8)]
+    out = torch.empty(B, H * hd, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i, with_events=None):
+        k, v = news[i % 8]
+        kvd.rswa_ring_write(c, k, v)
+        if with_events is not None:
+            with_events[0].record(stream)
+        decode(qs[i % 8], c, out=out)
+        if with_events is not None:
+            with_events[1].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sampler = ClockSampler(dev.index)
+    with sampler:
+        time.sleep(0.3)
+        replicas.barrier()
+        torch.cuda.synchronize()
+        c0 = time.time()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.profiler.start()
+        t0.record(stream)
+        for j in range(args.steps):
+            step(args.warmup + j, ev[j])
+        t1.record(stream)
+        torch.cuda.synchronize()
+        torch.cuda.profiler.stop()
+        replicas.barrier()
+        c1 = time.time()
+        time.sleep(0.1)
+    elapsed_ms = replicas.max_over_ranks(t0.elapsed_time(t1))
+    ms_per_step = elapsed_ms / args.steps
+    gbs = replicas.whole_job_rate((dec_bytes + wr_bytes) * args.steps, elapsed_ms * 1e-3, world) / 1e9
+    dec_ms = [a.elapsed_time(b) for a, b in ev]
+
+    nrep = max(20, args.steps)
+    dev_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nrep)]
+    torch.cuda.profiler.start()
+    for j in range(nrep):
+        dev_ev[j][0].record(stream)
+        decode(qs[j % 8], c, out=out)
+        dev_ev[j][1].record(stream)
+    torch.cuda.synchronize()
+    torch.cuda.profiler.stop()
+    k_ms = statistics.mean(a.elapsed_time(b) for a, b in dev_ev)
+    peak, peak_kind = peaks()
+    achieved = dec_bytes / (k_ms * 1e-3) / 1e9
+
+    pin_q = [qs[i].cpu().pin_memory() for i in range(8)]
+    pin_k = [news[i][0].cpu().pin_memory() for i in range(8)]
+    pin_v = [news[i][1].cpu().pin_memory() for i in range(8)]
+    pin_out = torch.empty(B, H * hd).pin_memory()
+    dq, dk, dv = torch.empty_like(qs[0]), torch.empty_like(news[0][0]), torch.empty_like(news[0][1])
+    torch.cuda.synchronize()
+    a0 = time.perf_counter()
+    for j in range(args.steps):
+        dq.copy_(pin_q[j % 8], non_blocking=True)
+        dk.copy_(pin_k[j % 8], non_blocking=True)
+        dv.copy_(pin_v[j % 8], non_blocking=True)
+        kvd.rswa_ring_write(c, dk, dv)
+        decode(dq, c, out=out)
+        pin_out.copy_(out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    a1 = time.perf_counter()
+    e2e = {"value": round((dec_bytes + wr_bytes) * args.steps / (a1 - a0) / 1e9 * world, 2), "unit": "GB/s",
+           "h2d_bytes_per_step": int((dq.numel() + dk.numel() + dv.numel()) * 4),
+           "d2h_bytes_per_step": int(pin_out.numel() * 4)}
+    if c.device_error():
+        raise SystemExit("device error word set")
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline:
+        smp = RswaOracleSample(wl, int8)
+        v, per = smp.gbs(args.cpu_seconds)
+        cpu = {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": smp.describe(wl) + ", %.1f s" % args.cpu_seconds}
+    line = {
+        "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "i8" if int8 else "f32", "data": "synthetic",
+        "config": {"workload": args.workload + "_steady", "streams": B, "heads": H, "head_dim": hd,
+                   "reference_rows": int(wl.prefill), "ring_rows": int(c.W),
+                   "step": "rswa ring write 1 token/stream + decode of every stream",
+                   "l2": "inputs larger than L2 (%.2f GB read per decode)" % (dec_bytes / 1e9),
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "fraction_of_peak": round(gbs / world / peak, 4),
+        "queries_per_s": round(B * world / (ms_per_step * 1e-3), 1),
+        "roofline": {"bound": "hbm", "kernel": "rswa decode (split + merge)",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": measured_traffic(args.workload),
+                     "peak_kind": peak_kind, "ms_per_launch": round(k_ms, 5),
+                     "bytes_per_launch": int(dec_bytes)},
+        "decode_ms_in_step": round(statistics.mean(dec_ms), 5),
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps * 3,
+        "clocks": sampler.summary(c0, c1),
+    }
+    print(json.dumps(line), flush=True)
+
 
 def build_workload(name: str, replicas: int):
     from kv_cache_decode_attention_gb300 import workloads as W
@@ -410,8 +609,11 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", default="q8_gqa", choices=["q8_gqa", "long_q8", "tiny_f32"])
+    ap.add_argument("--workload", default="q8_gqa",
+                    choices=["q8_gqa", "long_q8", "tiny_f32", *RSWA_WORKLOADS])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--rswa-streams", type=int, default=16,
+                    help="streams of the R-SWA workloads (16 = the measured configuration)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -434,7 +636,10 @@ def main():
         run_reference(args, rank)
         return
     build()
-    run_gpu(args, rank, world)
+    if args.workload in RSWA_WORKLOADS:
+        run_gpu_rswa(args, rank, world)
+    else:
+        run_gpu(args, rank, world)
 
 
 if __name__ == "__main__":

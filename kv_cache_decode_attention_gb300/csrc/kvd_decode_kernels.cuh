@@ -128,10 +128,22 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[E], int lane) {
     return v[0];
 }
 
-// Load CPL consecutive channels of a row (lane's share) as f32.
-template <int CPL, bool Q>
+// Load CPL consecutive channels of a row (lane's share) as f32.  PERM: int8
+// codes convert by byte permutes and float subtracts (full-rate pipes)
+// rather than int-to-float conversions (a quarter-rate pipe); the value pass
+// uses it, where each code feeds few FMAs.
+template <int CPL, bool Q, bool PERM = false>
 __device__ __forceinline__ void load_lane(const char *row, int lane, float (&x)[CPL]) {
-    if (Q) {
+    if (Q && PERM) {
+        // code + 128 (the byte XOR 0x80) as the low mantissa byte of 2^23:
+        // the float 2^23 + 128 + code, exact; one subtract leaves the code
+        const uint32_t w = (CPL == 4 ? reinterpret_cast<const uint32_t *>(row)[lane]
+                                     : uint32_t(reinterpret_cast<const uint16_t *>(row)[lane])) ^
+                           0x80808080u;
+#pragma unroll
+        for (int j = 0; j < CPL; ++j)
+            x[j] = __uint_as_float(__byte_perm(w, 0x4b000000u, 0x7650u | uint32_t(j))) - 8388736.0f;
+    } else if (Q) {
         if (CPL == 4) {
             const uint32_t w = reinterpret_cast<const uint32_t *>(row)[lane];
 #pragma unroll
@@ -367,7 +379,7 @@ __device__ void split_body(const ChunkInfo &ci, const SplitArgs &a, char *smem) 
             for (int jj = 0; jj < CPL; ++jj) tacc[h][jj] = 0.0f;
         for (int r = warp; r < nt; r += kWarps) {
             float x[CPL];
-            load_lane<CPL, VQ>(vseg + r * C::VROW, lane, x);
+            load_lane<CPL, VQ, true>(vseg + r * C::VROW, lane, x);
             float w[HPK];
             if (HPK % 4 == 0) {
 #pragma unroll
