@@ -11,7 +11,8 @@
  * Sources restated here (page title, then the item on that page):
  *   [cortiq]  docs.rs cortiq-engine 0.8.49, src/cortiq_engine/kv_cache.rs
  *             (KvMode, KV_COL_WARMUP, KV_K_GROUP, LayerKvCache::quant_row,
- *              freeze_cols, append, attend, attend_group_upto, memory_bytes)
+ *              freeze_cols, append, attend, attend_group_upto, memory_bytes,
+ *              evict_born, KvCache::evict)
  *   [rswa]    docs.rs franken_ocr 0.8.0, src/native_engine/rswa.rs
  *             (module doc, quantize_row_i8, RingCache::write_decode_step,
  *              decode_dims, decode_attention_scalar_head, decode_attention_int8,
@@ -446,6 +447,91 @@ long long kvo_memory_bytes(const kvo_cache *c)
 }
 
 /* ---- R-SWA ------------------------------------------------------------- */
+
+/* ---- cortiq LayerKvCache::evict_born ------------------------------------ */
+
+typedef struct {
+    float imp;
+    int pos;
+} born_item;
+
+/* Highest accumulated mass first; equal mass keeps the lower position first
+ * (the page orders the middle positions with a stable sort of the ascending
+ * list, so this total order gives the same sequence; NaN mass is outside
+ * the contract). */
+static int born_cmp(const void *a, const void *b)
+{
+    const born_item *x = (const born_item *)a, *y = (const born_item *)b;
+    if (x->imp > y->imp) return -1;
+    if (x->imp < y->imp) return 1;
+    return (x->pos > y->pos) - (x->pos < y->pos);
+}
+
+static void gather_rows(void *base, size_t row_bytes, const int *kept, int n)
+{
+    /* kept ascends and kept[j] >= j, so copying j = 0, 1, ... in order never
+     * reads a row that an earlier step overwrote */
+    char *b = (char *)base;
+    for (int j = 0; j < n; ++j)
+        if (kept[j] != j) memmove(b + (size_t)j * row_bytes, b + (size_t)kept[j] * row_bytes, row_bytes);
+}
+
+/* cortiq evict_born for one sequence, with imp its accumulated mass per
+ * stored row: when more than keep_last rows are stored, keep the first
+ * min(sink, keep_last) rows (attention sinks), the last min(recent,
+ * keep_last - sinks) rows, and fill the rest of the budget with the middle
+ * rows of highest mass; then gather the kept rows, in row order, in every
+ * storage of every live head independently (f32 K and V, int8 codes with
+ * their scales) and in imp.  Returns the rows kept, -1 for a negative
+ * argument. */
+int kvo_evict_born(kvo_cache *c, float *imp, int keep_last, int sink, int recent)
+{
+    if (keep_last < 0 || sink < 0 || recent < 0) return -1;
+    const int stored = c->seq_len;
+    if (stored <= keep_last) return stored;
+    const int sink_n = sink < keep_last ? sink : keep_last;
+    const int recent_n = recent < keep_last - sink_n ? recent : keep_last - sink_n;
+    unsigned char *keep = (unsigned char *)calloc((size_t)stored, 1);
+    for (int p = 0; p < sink_n; ++p) keep[p] = 1;
+    for (int p = stored - recent_n; p < stored; ++p) keep[p] = 1;
+    int budget = keep_last - sink_n - recent_n;
+    born_item *order = (born_item *)malloc(sizeof(born_item) * (size_t)stored);
+    int m = 0;
+    for (int p = 0; p < stored; ++p)
+        if (!keep[p]) {
+            order[m].imp = imp[p];
+            order[m].pos = p;
+            ++m;
+        }
+    qsort(order, (size_t)m, sizeof(born_item), born_cmp);
+    for (int i = 0; i < m && budget > 0; ++i, --budget) keep[order[i].pos] = 1;
+    int *kept = (int *)malloc(sizeof(int) * (size_t)stored);
+    int n = 0;
+    for (int p = 0; p < stored; ++p)
+        if (keep[p]) kept[n++] = p;
+    const int hd = c->hd, ng = n_groups(hd);
+    for (int h = 0; h < c->n_kv; ++h) {
+        if (!c->alive[h]) continue;
+        const size_t base = (size_t)h * (size_t)c->cap;
+        if (c->k) gather_rows(c->k + base * hd, sizeof(float) * (size_t)hd, kept, n);
+        if (c->v) gather_rows(c->v + base * hd, sizeof(float) * (size_t)hd, kept, n);
+        if (c->kq) {
+            gather_rows(c->kq + base * hd, (size_t)hd, kept, n);
+            gather_rows(c->ks + base * ng, sizeof(float) * (size_t)ng, kept, n);
+        }
+        if (c->vq) {
+            gather_rows(c->vq + base * hd, (size_t)hd, kept, n);
+            gather_rows(c->vs + base, sizeof(float), kept, n);
+        }
+        c->head_rows[h] = n;
+    }
+    gather_rows(imp, sizeof(float), kept, n);
+    c->seq_len = n;
+    free(kept);
+    free(order);
+    free(keep);
+    return n;
+}
 
 /* rswa write_decode_step for one stream: warm-up appends at ring_len and
  * sets ring_pos = ring_len % W; steady state overwrites ring_pos and

@@ -68,6 +68,7 @@ def lib():
             L.kvo_attend_group.argtypes = [C.POINTER(_Cache), vp, i32, i32, f32, vp, vp]
             L.kvo_attend_group_ex.argtypes = [C.POINTER(_Cache), vp, i32, i32, f32, i32, f32, vp, vp,
                                               vp]
+            L.kvo_evict_born.argtypes = [C.POINTER(_Cache), vp, i32, i32, i32]
             L.kvo_memory_bytes.argtypes = [C.POINTER(_Cache)]
             L.kvo_memory_bytes.restype = C.c_longlong
             L.kvo_rswa_write.argtypes = [i32, i32, i32, vp, vp, vp, vp, i32, vp, vp]
@@ -245,6 +246,16 @@ class OracleSeqCache:
 
     def memory_bytes(self) -> int:
         return int(lib().kvo_memory_bytes(C.byref(self._s)))
+
+    def evict_born(self, keep_last: int, sink: int, recent: int, imp: np.ndarray) -> int:
+        """cortiq evict_born: keep sinks + recents + the middle rows of highest
+        mass, gathered in row order; imp (f32 [cap], this sequence's mass per
+        row) is gathered in place.  Returns the rows kept."""
+        assert imp.dtype == np.float32 and imp.flags.c_contiguous and imp.shape[0] >= self.seq_len
+        n = lib().kvo_evict_born(C.byref(self._s), _p(imp), keep_last, sink, recent)
+        if n < 0:
+            raise ValueError("evict_born: negative argument")
+        return n
 
 
 def rswa_write(ring_k, ring_v, k, v, prefill_recorded: bool, cursors):

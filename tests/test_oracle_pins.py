@@ -793,3 +793,112 @@ def test_rswa_i8_ring_rows_use_their_own_scales():
     m = max(s0, s1)
     w0, w1 = math.exp(s0 - m), math.exp(s1 - m)
     assert np.allclose(out, (w0 * v0 + w1 * v1) / (w0 + w1), rtol=1e-12, atol=1e-12)
+
+
+# --------------------------------------------------- Born eviction (NEXT-3)
+
+def _ramp_cache(mode, n_kv, hd, rows, seed=0, alive=None):
+    c = oracle.OracleSeqCache(mode, n_kv, hd, rows + 8, alive=alive)
+    rng = np.random.default_rng(seed)
+    for _ in range(rows):
+        c.append(rng.normal(size=(n_kv, hd)).astype(f32), rng.normal(size=(n_kv, hd)).astype(f32))
+        c.freeze_if_due()
+    return c
+
+
+def _snapshot(c):
+    return {n: None if getattr(c, n) is None else getattr(c, n).copy() for n in ("k", "v", "kq", "ks", "vq", "vs")}
+
+
+def test_born_page_example_keeps_sink_mass_and_recents():
+    """[cortiq] born_eviction_keeps_high_mass_position, through KvCache::evict's
+    recent = max(keep_last / 2, 1)."""
+    g = load_golden("born_eviction.txt")
+    n, keep = int(g["positions"]), int(g["keep_last"])
+    c = oracle.OracleSeqCache(oracle.F32, 1, 2, 16)
+    for pos in range(n):
+        c.append(np.full((1, 2), pos, f32), np.full((1, 2), pos + 100.0, f32))
+    imp = np.full(16, f32(float(g["light_mass"])), f32)
+    imp[int(g["heavy_position"])] = f32(float(g["heavy_mass"]))
+    kept = c.evict_born(keep, int(g["sink"]), max(keep // 2, 1), imp)
+    expect = [float(x) for x in g["kept_keys"].split()]
+    assert kept == keep == c.seq_len and c.head_rows[0] == keep
+    assert c.k[0, :keep, 0].tolist() == expect
+    assert c.v[0, :keep, 0].tolist() == [x + 100.0 for x in expect]
+    assert imp[:keep].tolist() == [float(imp_v) for imp_v in
+                                   np.array([0.05, 5.0, 0.05, 0.05], f32)]
+
+
+@pytest.mark.parametrize("mode", [oracle.Q8K, oracle.Q8V])
+def test_born_mixed_modes_gather_every_storage(mode):
+    """[cortiq] born_eviction_mixed_modes_stay_consistent: K and V live in
+    different storages in q8k / q8v; both are gathered, memory shrinks below
+    half, and the kept V rows are the heavy tail's."""
+    g = load_golden("born_eviction.txt")
+    n = int(g["mixed_appends"])
+    c = oracle.OracleSeqCache(mode, 1, 4, n)
+    for p in range(n):
+        c.append(np.full((1, 4), p * 0.01, f32), np.full((1, 4), float(p), f32))
+        c.freeze_if_due()
+    imp = np.arange(n, dtype=f32)
+    before = c.memory_bytes()
+    keep = int(g["mixed_keep"])
+    assert c.evict_born(keep, int(g["mixed_sink"]), int(g["mixed_recent"]), imp) == keep
+    assert c.head_rows[0] == keep and c.memory_bytes() < before / 2
+    out = c.attend_group(np.ones((1, 4), f32), 0, f32(1.0))
+    assert out[0, 0] > float(g["mixed_out_min"])
+    # sinks 0..3, the 8 heaviest middle rows 64..71, the recents 72..79
+    assert imp[:keep].tolist() == list(range(4)) + list(range(64, 80))
+
+
+def test_born_is_a_no_op_at_or_under_budget():
+    c = _ramp_cache(oracle.Q8, 2, 64, 70, seed=1)
+    snap, imp = _snapshot(c), np.arange(78, dtype=f32)
+    assert c.evict_born(70, 4, 8, imp.copy()) == 70 and c.evict_born(100, 4, 8, imp) == 70
+    for k, v in snap.items():
+        assert v is None or np.array_equal(getattr(c, k), v)
+
+
+@pytest.mark.parametrize("mode", [oracle.F32, oracle.Q8, oracle.Q8K, oracle.Q8V])
+def test_born_gathers_kept_rows_of_every_storage(mode):
+    """Equal mass everywhere: ties keep the lowest middle positions (the page's
+    stable sort), so the kept set is [0, s) + [s, s + budget) + the recents;
+    every storage of every live head (a dead head stores nothing) holds the
+    pre-eviction rows at those positions, in order, and imp follows them."""
+    c = _ramp_cache(mode, 3, 64, 150, seed=2, alive=[1, 0, 1])
+    snap = _snapshot(c)
+    imp = np.full(158, 0.25, f32)
+    imp[150:] = 99.0  # beyond the stored rows: never read
+    keep, sink, recent = 40, 3, 10
+    assert c.evict_born(keep, sink, recent, imp) == keep
+    kept = list(range(sink)) + list(range(sink, sink + keep - sink - recent)) + list(range(140, 150))
+    assert len(kept) == keep and np.all(imp[:keep] == f32(0.25))
+    for name, before in snap.items():
+        if before is None:
+            continue
+        for h in (0, 2):
+            assert np.array_equal(getattr(c, name)[h, :keep], before[h, kept]), (name, h)
+    assert c.head_rows.tolist() == [keep, 0, keep]
+
+
+def test_born_mass_order_and_clamps():
+    """Increasing mass keeps the sinks and the last rows; sink >= keep_last
+    keeps the first keep_last rows only; sink + recent > keep_last clamps the
+    recents; the middle picks follow the mass, not the position."""
+    def run(keep, sink, recent, imp_fn, n=60):
+        c = oracle.OracleSeqCache(oracle.F32, 1, 32, n + 4)
+        for p in range(n):
+            c.append(np.full((1, 32), p, f32), np.full((1, 32), p, f32))
+        imp = np.array([imp_fn(p) for p in range(n + 4)], f32)
+        c.evict_born(keep, sink, recent, imp)
+        return c.k[0, :keep, 0].astype(int).tolist()
+
+    assert run(12, 2, 3, lambda p: p) == [0, 1] + list(range(50, 60))
+    assert run(12, 20, 3, lambda p: p) == list(range(12))
+    assert run(12, 5, 30, lambda p: p) == list(range(5)) + list(range(53, 60))
+    # mass peaks at positions 30, 10, 20 (in that order of mass), budget 3
+    peaks = {30: 9.0, 10: 8.0, 20: 7.0, 40: 1.0}
+    assert run(8, 2, 3, lambda p: peaks.get(p, 0.0)) == [0, 1, 10, 20, 30, 57, 58, 59]
+    # a tie at the threshold goes to the lower position
+    ties = {25: 5.0, 15: 3.0, 35: 3.0, 45: 3.0}
+    assert run(7, 2, 3, lambda p: ties.get(p, 0.0)) == [0, 1, 15, 25, 57, 58, 59]
