@@ -138,6 +138,27 @@ KVD_API kvd_status kv_append(kvd_layer *L, const float *k, const float *v, const
  * operation, then requantise every stored row against col.  Idempotent. */
 KVD_API kvd_status kv_freeze_colfield(kvd_layer *L, void *stream);
 
+/* Workspace bytes kv_evict_born needs for a given keep_last. */
+KVD_API kvd_status kv_evict_workspace_bytes(const kvd_layer *L, int64_t keep_last, int64_t *bytes_out);
+
+/* cortiq LayerKvCache::evict_born for every sequence of the layer holding
+ * more than keep_last rows (the others are left alone): keep its first
+ * min(sink, keep_last) rows (attention sinks), its last min(recent,
+ * keep_last - sinks) rows, and fill the rest of the keep_last budget with
+ * the middle rows of highest accumulated mass imp (equal mass: the lower
+ * row first); the kept rows move, in row order, to rows 0 .. keep_last - 1
+ * of every storage of every live head independently (f32 K / V, int8 codes
+ * and their scales), imp moves with them, and the sequence's length
+ * becomes keep_last.  Frozen fields are kept.  cortiq KvCache::evict under
+ * EvictionPolicy::Born { sink } passes recent = max(keep_last / 2, 1).
+ *   imp        device f32, the buffer decode_attention accumulates
+ *              (imp_off(b) + p); masses must be finite;
+ *   workspace  device, 256-byte aligned, >= kv_evict_workspace_bytes.
+ * KVD_EINVAL for a negative keep_last, sink or recent. */
+KVD_API kvd_status kv_evict_born(kvd_layer *L, float *imp, int64_t keep_last, int32_t sink,
+                                 int32_t recent, void *workspace, int64_t workspace_bytes,
+                                 void *stream);
+
 /* Workspace bytes decode_attention needs for n_q query heads (with_imp != 0
  * adds the score buffer the imp pass uses).  Depends only on the layer's
  * shape and capacities, so one allocation serves every later call. */

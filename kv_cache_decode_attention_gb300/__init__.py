@@ -13,6 +13,7 @@ from .api import (  # noqa: F401
     decode_attention,
     decode_attention_static,
     kv_append,
+    kv_evict_born,
     kv_freeze_colfield,
     rswa_attention,
     rswa_decode,

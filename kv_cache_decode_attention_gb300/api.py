@@ -169,6 +169,25 @@ def kv_freeze_colfield(layer: LayerKvCache, stream=None):
     _abi.call("kv_freeze_colfield", C.byref(layer.L), _stream(stream))
 
 
+def kv_evict_born(layer: LayerKvCache, imp: torch.Tensor, keep_last: int, sink: int = 4,
+                  recent: int | None = None, workspace: torch.Tensor | None = None, stream=None):
+    """cortiq evict_born on every sequence holding more than keep_last rows: keep the
+    sinks, the recents and the middle rows of highest mass in imp (the buffer
+    decode_attention accumulates), gathered in row order in every storage.  With
+    recent=None it is cortiq KvCache::evict's Born rule, recent = max(keep_last // 2, 1)."""
+    _f32_cuda(imp, "imp")
+    if imp.numel() < layer.imp_len:
+        raise ValueError("imp must hold %d floats" % layer.imp_len)
+    if recent is None:
+        recent = max(int(keep_last) // 2, 1)
+    n = C.c_int64(0)
+    _abi.call("kv_evict_workspace_bytes", C.byref(layer.L), int(keep_last), C.byref(n))
+    if workspace is None:
+        workspace = torch.empty(max(int(n.value), 256), dtype=torch.uint8, device=imp.device)
+    _abi.call("kv_evict_born", C.byref(layer.L), _ptr(imp), int(keep_last), int(sink), int(recent),
+              _ptr(workspace), int(workspace.numel()), _stream(stream))
+
+
 def decode_attention(q: torch.Tensor, cache: LayerKvCache, out: torch.Tensor | None = None,
                      imp: torch.Tensor | None = None, scale: float | None = None,
                      workspace: torch.Tensor | None = None, stream=None, window: int = 0,

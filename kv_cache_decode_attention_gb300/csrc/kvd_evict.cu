@@ -1,0 +1,315 @@
+// kvd_evict.cu -- mass-based (Born) eviction on the device (cortiq
+// LayerKvCache::evict_born, applied by KvCache::evict under
+// EvictionPolicy::Born), batched over the sequences of a layer.
+//
+// Per sequence holding more than keep_last rows:
+//   select  one CTA: the middle rows [sinks, stored - recents) compete for
+//           the budget keep_last - sinks - recents by accumulated mass.  An
+//           exact radix select over order-preserving 32-bit keys of the
+//           masses finds the budget-th largest key T; every row above T is
+//           kept and, of the rows equal to T, the lowest positions (the
+//           order of the page's stable sort).  Two ordered block scans turn
+//           the keep flags into the ascending list of kept rows, and the
+//           CTA gathers imp along it.
+//   gather  one CTA per (live head, storage): the kept rows move down to
+//           positions 0 .. keep_last - 1 of every storage independently (f32
+//           K / V, int8 codes, their scales).  Kept positions ascend and
+//           kept[j] >= j, so walking tiles of j in order, loading a whole
+//           tile before storing it, never reads a row an earlier store
+//           overwrote: the move is in place, with no staging copy.
+// The device length becomes keep_last in the select kernel; the host mirror
+// is updated by the entry point.
+
+#include <algorithm>
+#include <vector>
+
+#include "kvd_internal.cuh"
+
+namespace kvd {
+namespace {
+
+constexpr int kSelectThreads = 1024;
+constexpr int kGatherThreads = 256;
+constexpr int kGatherUnits = 8;  // 16-byte (or smaller) units per thread per tile
+
+struct BornTable {
+    int32_t n;
+    int32_t seq[kSlice];       // sequence of entry i
+    int32_t stored[kSlice];    // its rows before the eviction
+    int64_t imp_base[kSlice];  // its first imp entry
+};
+
+struct BornArgs {
+    float *imp;
+    int32_t *idx;  // [kSlice][keep_last] kept rows of each table entry
+    int32_t *seq_len;
+    uint32_t *err;
+    int32_t keep_last, sink_n, recent;
+};
+
+// Order-preserving key of a float: larger float -> larger unsigned key,
+// -0 and +0 equal (as the page's comparison treats them).
+__device__ __forceinline__ uint32_t mass_key(float x) {
+    uint32_t u = __float_as_uint(x);
+    if (u == 0x80000000u) u = 0;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Exclusive prefix count of `flag` over the block in thread order, and the
+// block total.  `warp_sums` holds kSelectThreads / 32 ints of shared memory.
+__device__ __forceinline__ int block_excl_count(bool flag, int *warp_sums, int &total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const unsigned m = __ballot_sync(0xffffffffu, flag);
+    const int in_warp = __popc(m & ((1u << lane) - 1u));
+    __syncthreads();  // warp_sums free (a previous call has read it)
+    if (lane == 0) warp_sums[warp] = __popc(m);
+    __syncthreads();
+    if (warp == 0) {
+        const int v = lane < kSelectThreads / 32 ? warp_sums[lane] : 0;
+        int incl = v;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += t;
+        }
+        if (lane < kSelectThreads / 32) warp_sums[lane] = incl - v;  // exclusive
+        if (lane == 31) warp_sums[kSelectThreads / 32] = incl;
+    }
+    __syncthreads();
+    total = warp_sums[kSelectThreads / 32];
+    return warp_sums[warp] + in_warp;
+}
+
+__global__ void __launch_bounds__(kSelectThreads) born_select_kernel(BornArgs a, BornTable t) {
+    __shared__ uint32_t hist[256];
+    __shared__ int warp_sums[kSelectThreads / 32 + 1];
+    __shared__ uint32_t sel_digit;
+    __shared__ int sel_need;
+    const int i = blockIdx.x, tid = threadIdx.x;
+    if (i >= t.n) return;
+    const int b = t.seq[i], stored = t.stored[i];
+    const int keep_last = a.keep_last, sink_n = a.sink_n;
+    const int recent_n = min(a.recent, keep_last - sink_n);
+    const int hi = stored - recent_n;  // middle rows: [sink_n, hi)
+    const int budget = keep_last - sink_n - recent_n;
+    float *imp = a.imp + t.imp_base[i];
+    int32_t *idx = a.idx + int64_t(i) * keep_last;
+
+    // ---- radix select of the budget-th largest key among the middle rows
+    uint32_t prefix = 0, mask = 0;
+    int need = budget;
+    if (budget > 0) {
+        for (int shift = 24; shift >= 0; shift -= 8) {
+            for (int d = tid; d < 256; d += kSelectThreads) hist[d] = 0;
+            __syncthreads();
+            for (int p = sink_n + tid; p < hi; p += kSelectThreads) {
+                const uint32_t k = mass_key(imp[p]);
+                if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1u);
+            }
+            __syncthreads();
+            if (tid == 0) {
+                int cum = 0, d = 255;
+                for (; d > 0; --d) {
+                    if (cum + int(hist[d]) >= need) break;
+                    cum += int(hist[d]);
+                }
+                sel_digit = uint32_t(d);
+                sel_need = need - cum;
+            }
+            __syncthreads();
+            prefix |= sel_digit << shift;
+            mask |= 255u << shift;
+            need = sel_need;
+        }
+    }
+    // prefix = the threshold key; `need` rows equal to it are kept, lowest first
+
+    // ---- keep flags -> ascending list of kept rows
+    int eq_carry = 0, out_carry = 0;
+    for (int p0 = 0; p0 < stored; p0 += kSelectThreads) {
+        const int p = p0 + tid;
+        bool mid_gt = false, mid_eq = false;
+        if (budget > 0 && p >= sink_n && p < hi) {
+            const uint32_t k = mass_key(imp[p]);
+            mid_gt = k > prefix;
+            mid_eq = k == prefix;
+        }
+        int eq_total;
+        const int eq_rank = eq_carry + block_excl_count(mid_eq, warp_sums, eq_total);
+        eq_carry += eq_total;
+        const bool keep = p < stored && (p < sink_n || p >= hi || mid_gt || (mid_eq && eq_rank < need));
+        int out_total;
+        const int pos = out_carry + block_excl_count(keep, warp_sums, out_total);
+        out_carry += out_total;
+        if (keep && pos < keep_last) idx[pos] = p;
+    }
+    __syncthreads();
+    if (out_carry != keep_last) {
+        // cannot happen for finite masses: report it, and make the list the
+        // identity so that the gather leaves every row where it is
+        if (tid == 0) set_error(a.err, kErrBounds);
+        for (int j = tid; j < keep_last; j += kSelectThreads) idx[j] = j;
+        return;
+    }
+
+    // ---- imp follows its rows (in place, tiles in order)
+    for (int j0 = sink_n; j0 < keep_last; j0 += kSelectThreads) {
+        const int j = j0 + tid;
+        float v = 0.0f;
+        if (j < keep_last) v = imp[idx[j]];
+        __syncthreads();
+        if (j < keep_last) imp[j] = v;
+        __syncthreads();
+    }
+    if (tid == 0) a.seq_len[b] = keep_last;
+}
+
+struct GatherStorage {
+    char *base;         // the storage buffer
+    int32_t row_bytes;  // bytes per row (a multiple of 4)
+};
+
+struct GatherArgs {
+    GatherStorage st[4];
+    int32_t n_st;
+    const int32_t *idx;
+    const int64_t *row_base, *cap;
+    uint32_t *err;
+    int32_t keep_last, sink_n;
+};
+
+// Move the kept rows of one region (rows of `upr` units of type U) down to
+// positions sink_n .. keep_last - 1, tile by tile in order.  A kept row
+// outside [0, cap) (corrupt metadata) is reported and skipped.
+template <typename U>
+__device__ void gather_region(U *region, int upr, const int32_t *kept, int sink_n, int keep_last,
+                              int64_t cap, uint32_t *err) {
+    const int tile_rows = max(1, kGatherThreads * kGatherUnits / upr);
+    for (int j0 = sink_n; j0 < keep_last; j0 += tile_rows) {
+        const int rows = min(tile_rows, keep_last - j0);
+        // a tile whose last row stays in place stays entirely (kept ascends, kept[j] >= j)
+        if (kept[j0 + rows - 1] == j0 + rows - 1) continue;
+        U r[kGatherUnits];
+        const int units = rows * upr;
+#pragma unroll
+        for (int k = 0; k < kGatherUnits; ++k) {
+            const int e = threadIdx.x + k * kGatherThreads;
+            if (e < units) {
+                const int32_t src = kept[j0 + e / upr];
+                if (src >= 0 && src < cap) r[k] = region[int64_t(src) * upr + e % upr];
+                else set_error(err, kErrBounds);
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < kGatherUnits; ++k) {
+            const int e = threadIdx.x + k * kGatherThreads;
+            if (e < units) region[int64_t(j0 + e / upr) * upr + e % upr] = r[k];
+        }
+        __syncthreads();
+    }
+}
+
+__global__ void __launch_bounds__(kGatherThreads) born_gather_kernel(GatherArgs a, BornTable t) {
+    const int i = blockIdx.y;
+    if (i >= t.n) return;
+    const int s = blockIdx.x % a.n_st, gl = blockIdx.x / a.n_st;
+    const int b = t.seq[i];
+    const GatherStorage g = a.st[s];
+    const int64_t row0 = a.row_base[b] + int64_t(gl) * a.cap[b];
+    char *region = g.base + row0 * g.row_bytes;
+    const int32_t *kept = a.idx + int64_t(i) * a.keep_last;
+    const int64_t cap = a.cap[b];
+    if (g.row_bytes % 16 == 0)
+        gather_region(reinterpret_cast<uint4 *>(region), g.row_bytes / 16, kept, a.sink_n, a.keep_last, cap, a.err);
+    else if (g.row_bytes % 8 == 0)
+        gather_region(reinterpret_cast<uint2 *>(region), g.row_bytes / 8, kept, a.sink_n, a.keep_last, cap, a.err);
+    else
+        gather_region(reinterpret_cast<uint32_t *>(region), g.row_bytes / 4, kept, a.sink_n, a.keep_last, cap,
+                      a.err);
+}
+
+int64_t evict_ws_bytes(const Layer *l, int64_t keep_last) {
+    return (int64_t(std::min(kSlice, l->n_seq)) * keep_last * 4 + 255) / 256 * 256;
+}
+
+}  // namespace
+}  // namespace kvd
+
+using namespace kvd;
+
+extern "C" kvd_status kv_evict_workspace_bytes(const kvd_layer *L, int64_t keep_last, int64_t *bytes_out) {
+    const Layer *l = checked_layer(L);
+    if (l == nullptr || bytes_out == nullptr || keep_last < 0 || keep_last > (int64_t(1) << 31) - 1)
+        return KVD_EINVAL;
+    *bytes_out = evict_ws_bytes(l, keep_last);
+    return KVD_OK;
+}
+
+extern "C" kvd_status kv_evict_born(kvd_layer *L, float *imp, int64_t keep_last, int32_t sink,
+                                    int32_t recent, void *workspace, int64_t workspace_bytes,
+                                    void *stream) {
+    Layer *l = checked_layer(L);
+    if (l == nullptr || imp == nullptr || (reinterpret_cast<uintptr_t>(imp) & 3)) return KVD_EINVAL;
+    if (keep_last < 0 || keep_last > (int64_t(1) << 31) - 1 || sink < 0 || recent < 0) return KVD_EINVAL;
+    const int64_t need = evict_ws_bytes(l, keep_last);
+    if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
+        return KVD_EINVAL;
+    std::vector<int32_t> todo;
+    for (int b = 0; b < l->n_seq; ++b)
+        if (l->h_seq_len[b] > keep_last) todo.push_back(b);
+    if (todo.empty()) return KVD_OK;
+    cudaStream_t st = as_stream(stream);
+    BornArgs a;
+    a.imp = imp;
+    a.idx = static_cast<int32_t *>(workspace);
+    a.seq_len = l->d_seq_len;
+    a.err = l->d_err;
+    a.keep_last = int32_t(keep_last);
+    a.sink_n = int32_t(std::min<int64_t>(sink, keep_last));
+    a.recent = recent;
+    GatherArgs g;
+    g.n_st = 0;
+    auto add = [&](int slot, int32_t row_bytes) {
+        if (l->buf[slot] != nullptr) g.st[g.n_st++] = GatherStorage{static_cast<char *>(l->buf[slot]), row_bytes};
+    };
+    const bool qk = l->mode == KVD_Q8 || l->mode == KVD_Q8K;
+    const bool qv = l->mode == KVD_Q8 || l->mode == KVD_Q8V;
+    if (qk) {
+        add(KVD_BUF_KQ, l->hd);
+        add(KVD_BUF_KS, (l->hd / 32) * 4);
+    } else {
+        add(KVD_BUF_K, l->hd * 4);
+    }
+    if (qv) {
+        add(KVD_BUF_VQ, l->hd);
+        add(KVD_BUF_VS, 4);
+    } else {
+        add(KVD_BUF_V, l->hd * 4);
+    }
+    g.idx = a.idx;
+    g.err = l->d_err;
+    g.row_base = l->d_row_base;
+    g.cap = l->d_cap;
+    g.keep_last = a.keep_last;
+    g.sink_n = a.sink_n;
+    for (size_t s0 = 0; s0 < todo.size(); s0 += kSlice) {
+        BornTable t;
+        t.n = int32_t(std::min<size_t>(kSlice, todo.size() - s0));
+        for (int i = 0; i < t.n; ++i) {
+            const int b = todo[s0 + i];
+            t.seq[i] = b;
+            t.stored[i] = int32_t(l->h_seq_len[b]);
+            t.imp_base[i] = l->h_imp_base[b];
+        }
+        born_select_kernel<<<unsigned(t.n), kSelectThreads, 0, st>>>(a, t);
+        if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
+        if (l->n_live > 0 && g.n_st > 0 && keep_last > a.sink_n) {
+            dim3 grid(unsigned(l->n_live * g.n_st), unsigned(t.n));
+            born_gather_kernel<<<grid, kGatherThreads, 0, st>>>(g, t);
+            if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
+        }
+    }
+    for (int b : todo) l->h_seq_len[b] = keep_last;
+    return KVD_OK;
+}

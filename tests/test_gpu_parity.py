@@ -467,3 +467,111 @@ def test_rswa_i8_errors(torch, kvd):
     assert lib.rswa_record_prefill_i8(*ref, C.byref(cache.mirror), *args) == -1
     assert lib.rswa_record_prefill_i8(*ref, None, *args) == -1
     assert pl.tolist() == [4, 0]
+
+
+# --------------------------------------------------- Born eviction (NEXT-3)
+
+def _mass(lengths, imp_base, imp_len, seed):
+    """Seeded masses with many exact ties (small integers / 8), the same array
+    for the device buffer and every oracle sequence."""
+    rng = np.random.default_rng(seed)
+    full = np.zeros(imp_len, np.float32)
+    per = []
+    for b, L in enumerate(lengths):
+        m = (rng.integers(0, 12, size=int(L)) / 8.0).astype(np.float32)
+        full[imp_base[b]:imp_base[b] + int(L)] = m
+        per.append(m)
+    return full, per
+
+
+@pytest.mark.parametrize("mode", list(MODES))
+@pytest.mark.parametrize("hd", [128, 64])
+def test_born_eviction_parity(torch, kvd, mode, hd):
+    """Sequences above, at and below the budget, a dead head, many tied masses:
+    after kv_evict_born every storage, imp and the lengths equal the oracle's
+    evict_born bit for bit; decode over the evicted cache and over rows appended
+    afterwards matches the oracle."""
+    lengths = [700, 150, 151, 40, 2300]
+    n_kv, alive, extra = 4, [1, 1, 0, 1], 40
+    keep, sink, recent = 150, 4, 60
+    ks, vs = seq_rows(lengths, n_kv, hd, seed=61)
+    layer = _layer(kvd, MODES[mode], lengths, n_kv, hd, alive, cap_extra=extra)
+    gpu_append_bulk(layer, ks, vs, torch, pieces=(0.5, 1.0))
+    ocs = oracle_caches(MODES[mode], lengths, n_kv, hd, alive, ks, vs, cap=max(lengths) + extra)
+    for oc in ocs:
+        oc.freeze_if_due()
+    full, per = _mass(lengths, layer.imp_base, layer.imp_len, seed=62)
+    imp = torch.from_numpy(full.copy()).cuda()
+    kvd.kv_evict_born(layer, imp, keep, sink, recent)
+    got_imp = imp.cpu().numpy()
+    for b, oc in enumerate(ocs):
+        o_imp = np.zeros(oc.cap, np.float32)
+        o_imp[:lengths[b]] = per[b]
+        assert oc.evict_born(keep, sink, recent, o_imp) == min(lengths[b], keep)
+        n = oc.seq_len
+        assert np.array_equal(got_imp[layer.imp_base[b]:layer.imp_base[b] + n].view(np.uint32),
+                              o_imp[:n].view(np.uint32)), b
+    assert_storage_bitexact(layer, ocs, torch)
+    assert layer.device_error() == 0
+    n_q = n_kv * 2
+    scale = np.float32(1.0 / math.sqrt(hd))
+    for step in range(2):
+        q = synthetic.normal((len(lengths), n_q, hd), 63 + step)
+        out = kvd.decode_attention(torch.from_numpy(q).cuda(), layer, scale=float(scale)).cpu().numpy()
+        for b, oc in enumerate(ocs):
+            ref = oc.decode(q[b], n_q, scale)
+            live = np.repeat(np.array(alive, bool), 2)
+            assert out_error(out[b], ref, live) <= OUT_TOL, (step, b)
+        # rows appended after the eviction land behind the kept rows
+        k_new = synthetic.normal((len(lengths), n_kv, hd), 64 + step)
+        v_new = synthetic.normal((len(lengths), n_kv, hd), 65 + step)
+        kvd.kv_append(layer, torch.from_numpy(k_new).cuda(), torch.from_numpy(v_new).cuda())
+        for b, oc in enumerate(ocs):
+            oc.append(k_new[b], v_new[b])
+            oc.freeze_if_due()
+    assert_storage_bitexact(layer, ocs, torch)
+
+
+def test_born_page_example_on_gpu(torch, kvd):
+    """cortiq born_eviction_keeps_high_mass_position: kept keys 0, 3, 6, 7."""
+    from conftest import load_golden
+
+    g = load_golden("born_eviction.txt")
+    hd = 64
+    layer = _layer(kvd, MODES["f32"], [8], 1, hd, [1], cap_extra=8)
+    k = np.repeat(np.arange(8, dtype=np.float32)[:, None, None], hd, axis=2)
+    kvd.kv_append(layer, torch.from_numpy(k).cuda(), torch.from_numpy(k + 100).cuda(), np.array([8], np.int32))
+    imp = torch.full((layer.imp_len,), float(g["light_mass"]), device="cuda")
+    imp[int(g["heavy_position"])] = float(g["heavy_mass"])
+    kvd.kv_evict_born(layer, imp, int(g["keep_last"]), sink=int(g["sink"]))  # recent = max(4 // 2, 1)
+    keys = layer.component(kvd._abi.BUF_K)[:4, 0].cpu().numpy().tolist()
+    assert keys == [float(x) for x in g["kept_keys"].split()]
+    assert layer.seq_len(0) == 4 and layer.device_error() == 0
+
+
+def test_born_edges_and_errors(torch, kvd):
+    """keep_last 0 empties a sequence (fields stay frozen), a budget at or above
+    every length is a no-op, sink >= keep_last keeps the first rows, and a
+    negative argument is refused before anything changes."""
+    lengths = [90, 30]
+    ks, vs = seq_rows(lengths, 2, 128, seed=71)
+    layer = _layer(kvd, MODES["q8"], lengths, 2, 128, None, cap_extra=16)
+    gpu_append_bulk(layer, ks, vs, torch)
+    ocs = oracle_caches(MODES["q8"], lengths, 2, 128, None, ks, vs, cap=106)
+    for oc in ocs:
+        oc.freeze_if_due()
+    imp = torch.zeros(layer.imp_len, device="cuda")
+    with pytest.raises(kvd.KvdError) as e:
+        kvd.kv_evict_born(layer, imp, 10, sink=-1, recent=2)
+    assert e.value.status == -1 and layer.seq_len(0) == 90
+    kvd.kv_evict_born(layer, imp, 100, 4, 8)  # nobody above the budget
+    assert_storage_bitexact(layer, ocs, torch)
+    kvd.kv_evict_born(layer, imp, 50, 60, 8)  # sinks take the whole budget
+    for b, oc in enumerate(ocs):
+        o_imp = np.zeros(oc.cap, np.float32)
+        oc.evict_born(50, 60, 8, o_imp)
+    assert layer.seq_len(0) == 50 and layer.seq_len(1) == 30
+    assert_storage_bitexact(layer, ocs, torch)
+    kvd.kv_evict_born(layer, imp, 0, 4, 8)
+    assert layer.seq_len(0) == 0 and layer.seq_len(1) == 0 and layer.frozen(0)
+    assert layer.device_error() == 0
