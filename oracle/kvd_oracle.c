@@ -12,7 +12,7 @@
  *   [cortiq]  docs.rs cortiq-engine 0.8.49, src/cortiq_engine/kv_cache.rs
  *             (KvMode, KV_COL_WARMUP, KV_K_GROUP, LayerKvCache::quant_row,
  *              freeze_cols, append, attend, attend_group_upto, memory_bytes,
- *              evict_born, KvCache::evict)
+ *              evict_born, KvCache::evict, truncate_last)
  *   [rswa]    docs.rs franken_ocr 0.8.0, src/native_engine/rswa.rs
  *             (module doc, quantize_row_i8, RingCache::write_decode_step,
  *              decode_dims, decode_attention_scalar_head, decode_attention_int8,
@@ -526,10 +526,31 @@ int kvo_evict_born(kvo_cache *c, float *imp, int keep_last, int sink, int recent
         c->head_rows[h] = n;
     }
     gather_rows(imp, sizeof(float), kept, n);
+    /* the page truncates imp to the kept rows and each later append pushes a
+     * zero; in this flat buffer the dropped rows' entries are cleared */
+    for (int p = n; p < stored; ++p) imp[p] = 0.0f;
     c->seq_len = n;
     free(kept);
     free(order);
     free(keep);
+    return n;
+}
+
+/* cortiq LayerKvCache::truncate_last: drop the last min(n_drop, stored)
+ * rows of every storage and of imp (speculative-decode reject).  The rows'
+ * bytes stay where they are (nothing reads past the length); their imp
+ * entries are cleared so that rows appended later start from zero mass, as
+ * each appended row does on the page.  Returns the new length. */
+int kvo_truncate_last(kvo_cache *c, float *imp, int n_drop)
+{
+    if (n_drop < 0) return -1;
+    const int d = n_drop < c->seq_len ? n_drop : c->seq_len;
+    const int n = c->seq_len - d;
+    for (int h = 0; h < c->n_kv; ++h)
+        if (c->alive[h]) c->head_rows[h] = n;
+    if (imp)
+        for (int p = n; p < c->seq_len; ++p) imp[p] = 0.0f;
+    c->seq_len = n;
     return n;
 }
 

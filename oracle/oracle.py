@@ -69,6 +69,7 @@ def lib():
             L.kvo_attend_group_ex.argtypes = [C.POINTER(_Cache), vp, i32, i32, f32, i32, f32, vp, vp,
                                               vp]
             L.kvo_evict_born.argtypes = [C.POINTER(_Cache), vp, i32, i32, i32]
+            L.kvo_truncate_last.argtypes = [C.POINTER(_Cache), vp, i32]
             L.kvo_memory_bytes.argtypes = [C.POINTER(_Cache)]
             L.kvo_memory_bytes.restype = C.c_longlong
             L.kvo_rswa_write.argtypes = [i32, i32, i32, vp, vp, vp, vp, i32, vp, vp]
@@ -246,6 +247,15 @@ class OracleSeqCache:
 
     def memory_bytes(self) -> int:
         return int(lib().kvo_memory_bytes(C.byref(self._s)))
+
+    def truncate_last(self, n_drop: int, imp: np.ndarray | None = None) -> int:
+        """cortiq truncate_last: drop the last n_drop rows (imp entries cleared)."""
+        if imp is not None:
+            assert imp.dtype == np.float32 and imp.flags.c_contiguous and imp.shape[0] >= self.seq_len
+        n = lib().kvo_truncate_last(C.byref(self._s), _p(imp), n_drop)
+        if n < 0:
+            raise ValueError("truncate_last: negative count")
+        return n
 
     def evict_born(self, keep_last: int, sink: int, recent: int, imp: np.ndarray) -> int:
         """cortiq evict_born: keep sinks + recents + the middle rows of highest

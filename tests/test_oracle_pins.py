@@ -873,6 +873,7 @@ def test_born_gathers_kept_rows_of_every_storage(mode):
     assert c.evict_born(keep, sink, recent, imp) == keep
     kept = list(range(sink)) + list(range(sink, sink + keep - sink - recent)) + list(range(140, 150))
     assert len(kept) == keep and np.all(imp[:keep] == f32(0.25))
+    assert np.all(imp[keep:150] == 0.0) and np.all(imp[150:] == f32(99.0))  # dropped rows cleared
     for name, before in snap.items():
         if before is None:
             continue
@@ -902,3 +903,22 @@ def test_born_mass_order_and_clamps():
     # a tie at the threshold goes to the lower position
     ties = {25: 5.0, 15: 3.0, 35: 3.0, 45: 3.0}
     assert run(7, 2, 3, lambda p: ties.get(p, 0.0)) == [0, 1, 15, 25, 57, 58, 59]
+
+
+def test_truncate_last_page_example_and_resume():
+    """[cortiq] truncate_rolls_back_speculative_positions; then an append lands at
+    the freed position, its mass starts from zero, and dropping more rows than
+    are stored empties the sequence."""
+    g = load_golden("born_eviction.txt")
+    c = oracle.OracleSeqCache(oracle.F32, 2, 4, 16)
+    for pos in range(int(g["trunc_appends"])):
+        c.append(np.full((2, 4), pos, f32), np.full((2, 4), pos, f32))
+    imp = np.arange(16, dtype=f32) + 1
+    assert c.truncate_last(int(g["trunc_drop"]), imp) == int(g["trunc_left"]) == c.seq_len
+    assert c.head_rows.tolist() == [3, 3] and c.k[0, 2, 0] == 2.0
+    assert imp[:3].tolist() == [1, 2, 3] and imp[3:5].tolist() == [0, 0] and imp[5] == 6
+    c.append(np.full((2, 4), 9.0, f32), np.full((2, 4), 9.0, f32))
+    assert c.seq_len == 4 and c.k[1, 3, 0] == 9.0
+    out = c.attend_group(np.zeros((1, 4), f32), 0, f32(1.0))
+    assert np.allclose(out[0], (0 + 1 + 2 + 9) / 4.0)  # the dropped rows are gone
+    assert c.truncate_last(10, imp) == 0 and c.head_rows.tolist() == [0, 0]
