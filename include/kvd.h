@@ -138,6 +138,14 @@ KVD_API kvd_status kv_append(kvd_layer *L, const float *k, const float *v, const
  * operation, then requantise every stored row against col.  Idempotent. */
 KVD_API kvd_status kv_freeze_colfield(kvd_layer *L, void *stream);
 
+/* cortiq LayerKvCache::truncate_last (speculative-decode reject), batched:
+ * sequence b drops its last min(n_drop[b], length) rows in every storage
+ * (n_drop host [n_seq], NULL = one row each).  Only the lengths change;
+ * with imp (device f32, the decode_attention buffer, or NULL) the dropped
+ * rows' entries are cleared so that rows appended later start from zero
+ * mass.  Frozen fields are kept.  KVD_EINVAL for a negative count. */
+KVD_API kvd_status kv_truncate_last(kvd_layer *L, const int32_t *n_drop, float *imp, void *stream);
+
 /* Workspace bytes kv_evict_born needs for a given keep_last. */
 KVD_API kvd_status kv_evict_workspace_bytes(const kvd_layer *L, int64_t keep_last, int64_t *bytes_out);
 
@@ -148,8 +156,9 @@ KVD_API kvd_status kv_evict_workspace_bytes(const kvd_layer *L, int64_t keep_las
  * the middle rows of highest accumulated mass imp (equal mass: the lower
  * row first); the kept rows move, in row order, to rows 0 .. keep_last - 1
  * of every storage of every live head independently (f32 K / V, int8 codes
- * and their scales), imp moves with them, and the sequence's length
- * becomes keep_last.  Frozen fields are kept.  cortiq KvCache::evict under
+ * and their scales), imp moves with them (the dropped rows' entries are
+ * cleared, so rows appended later start from zero mass), and the sequence's
+ * length becomes keep_last.  Frozen fields are kept.  cortiq KvCache::evict under
  * EvictionPolicy::Born { sink } passes recent = max(keep_last / 2, 1).
  *   imp        device f32, the buffer decode_attention accumulates
  *              (imp_off(b) + p); masses must be finite;
@@ -235,27 +244,66 @@ KVD_API kvd_status kvd_layer_device_error(const kvd_layer *L, int32_t clear, uin
  * Per stream s and head h the reference block is ref[s][h][0..ref_cap) and
  * the ring ring[s][h][0..W), rows of head_dim f32 (head-major, as rswa
  * RingCache keeps them).  Cursors live on the host, one int32 per stream:
- * prefill_len (< 0 = no prefill recorded), ring_len, ring_pos. */
+ * prefill_len (< 0 = no prefill recorded), ring_len, ring_pos.  The
+ * writers also keep, when given a host rswa_history array [B], each
+ * stream's decode-write count and branch lineage (rswa RingCache's
+ * decode_writes and lineage_epoch), which rswa_checkpoint_take and
+ * rswa_rollback_to use; NULL = not kept. */
+typedef struct {
+    int64_t decode_writes;   /* ring writes since the stream's prefill */
+    uint64_t lineage_epoch;  /* +1 at every prefill and every rollback that discards writes */
+} rswa_history;
 
 /* rswa RingCache::record_prefill for stream `s`: copy k, v (device f32
  * [H][seq][head_dim]) into the reference block and reset the stream's ring
- * (ring_len = ring_pos = 0).  KVD_ECAPACITY if seq > ref_cap. */
+ * (ring_len = ring_pos = 0; with hist: decode_writes = 0 and a new
+ * lineage).  KVD_ECAPACITY if seq > ref_cap; KVD_ESTATE if the lineage
+ * counter is exhausted. */
 KVD_API kvd_status rswa_record_prefill(float *ref_k, float *ref_v, const float *k, const float *v,
                                int32_t s, int32_t seq, int32_t B, int32_t H, int32_t head_dim,
                                int64_t ref_cap, int32_t W, int32_t *prefill_len,
-                               int32_t *ring_len, int32_t *ring_pos, void *stream);
+                               int32_t *ring_len, int32_t *ring_pos, rswa_history *hist,
+                               void *stream);
 
 /* rswa RingCache::write_decode_step for every stream at once: stream s
  * writes its token (k, v device f32 [B][H][head_dim], already rotated at
  * the true absolute position by the caller) into slot ring_len[s] while
  * ring_len < W (then ring_len += 1, ring_pos = ring_len % W) and into slot
  * ring_pos[s] afterwards (then ring_pos = (ring_pos + 1) % W).  Cursors are
- * host arrays updated in place; slot_out (host [B] or NULL) gets each
- * stream's slot.  KVD_ESTATE if any stream has no prefill (nothing written). */
+ * host arrays updated in place (with hist: decode_writes += 1); slot_out
+ * (host [B] or NULL) gets each stream's slot.  KVD_ESTATE if any stream
+ * has no prefill (nothing written). */
 KVD_API kvd_status rswa_ring_write(float *ring_k, float *ring_v, const float *k, const float *v,
                            const int32_t *prefill_len, int32_t *ring_len, int32_t *ring_pos,
-                           int32_t B, int32_t H, int32_t head_dim, int32_t W,
+                           rswa_history *hist, int32_t B, int32_t H, int32_t head_dim, int32_t W,
                            int32_t *slot_out, void *stream);
+
+/* rswa RingCheckpoint of one stream: the issuing cache's identity (a
+ * caller-chosen number), the prefill boundary, the ring cursors, the
+ * decode-write count and the lineage at the time it was taken. */
+typedef struct {
+    uint64_t cache_id;
+    uint64_t lineage_epoch;
+    int64_t decode_writes;
+    int32_t prefill_len, ring_len, ring_pos, pad;
+} rswa_checkpoint;
+
+/* rswa RingCache::checkpoint of stream s (host only, O(1), no K/V copy). */
+KVD_API kvd_status rswa_checkpoint_take(uint64_t cache_id, const int32_t *prefill_len,
+                                        const int32_t *ring_len, const int32_t *ring_pos,
+                                        const rswa_history *hist, int32_t s, rswa_checkpoint *out);
+
+/* rswa RingCache::rollback_to for stream s (host only): restore ring_len,
+ * ring_pos and decode_writes from cp, discarding the ring writes made since
+ * (the stale slots >= ring_len are never read).  Refused with KVD_ESTATE,
+ * nothing changed, when cp comes from another cache, another prefill
+ * boundary or another lineage, is from the future, or when the discarded
+ * writes wrapped the ring over a row live at the checkpoint (cp.ring_len +
+ * discarded > W: an overwritten row cannot be restored from cursors).  A
+ * rollback that discards writes starts a new lineage. */
+KVD_API kvd_status rswa_rollback_to(uint64_t cache_id, const int32_t *prefill_len, int32_t *ring_len,
+                                    int32_t *ring_pos, rswa_history *hist, int32_t s, int32_t W,
+                                    const rswa_checkpoint *cp);
 
 /* Workspace bytes rswa_decode needs. */
 KVD_API kvd_status rswa_decode_workspace_bytes(int32_t B, int32_t H, int32_t head_dim,
@@ -299,7 +347,7 @@ KVD_API kvd_status rswa_record_prefill_i8(float *ref_k, float *ref_v, const rswa
                                           const float *k, const float *v, int32_t s, int32_t seq,
                                           int32_t B, int32_t H, int32_t head_dim, int64_t ref_cap,
                                           int32_t W, int32_t *prefill_len, int32_t *ring_len,
-                                          int32_t *ring_pos, void *stream);
+                                          int32_t *ring_pos, rswa_history *hist, void *stream);
 
 /* rswa_ring_write plus the int8 mirror of each freshly written ring row at the
  * same slot (rswa write_decode_step with the int8 lever on).  head_dim 64 or
@@ -307,9 +355,9 @@ KVD_API kvd_status rswa_record_prefill_i8(float *ref_k, float *ref_v, const rswa
  * and errors as rswa_ring_write. */
 KVD_API kvd_status rswa_ring_write_i8(float *ring_k, float *ring_v, const rswa_i8_mirror *m,
                                       const float *k, const float *v, const int32_t *prefill_len,
-                                      int32_t *ring_len, int32_t *ring_pos, int32_t B, int32_t H,
-                                      int32_t head_dim, int32_t W, int32_t *slot_out,
-                                      void *stream);
+                                      int32_t *ring_len, int32_t *ring_pos, rswa_history *hist,
+                                      int32_t B, int32_t H, int32_t head_dim, int32_t W,
+                                      int32_t *slot_out, void *stream);
 
 /* rswa decode_attention_int8 for every stream, reading the int8 mirror only:
  * per (stream, head) the query row is quantised like a cache row (codes and

@@ -15,6 +15,7 @@ from .api import (  # noqa: F401
     kv_append,
     kv_evict_born,
     kv_freeze_colfield,
+    kv_truncate_last,
     rswa_attention,
     rswa_decode,
     rswa_decode_i8,

@@ -31,6 +31,16 @@ class rswa_i8_mirror(C.Structure):
                 ("ring_ks", C.c_void_p), ("ring_vs", C.c_void_p)]
 
 
+class rswa_history(C.Structure):
+    _fields_ = [("decode_writes", C.c_int64), ("lineage_epoch", C.c_uint64)]
+
+
+class rswa_checkpoint(C.Structure):
+    _fields_ = [("cache_id", C.c_uint64), ("lineage_epoch", C.c_uint64), ("decode_writes", C.c_int64),
+                ("prefill_len", C.c_int32), ("ring_len", C.c_int32), ("ring_pos", C.c_int32),
+                ("pad", C.c_int32)]
+
+
 class KvdError(RuntimeError):
     def __init__(self, fn: str, status: int, msg: str):
         super().__init__("%s failed: %s (%d)" % (fn, msg, status))
@@ -48,6 +58,7 @@ _SIGS = {
     "kvd_layer_memory_bytes": [_P(kvd_layer), _P(_i64)],
     "kv_append": [_P(kvd_layer), _vp, _vp, _vp, _vp],
     "kv_freeze_colfield": [_P(kvd_layer), _vp],
+    "kv_truncate_last": [_P(kvd_layer), _vp, _vp, _vp],
     "kv_evict_workspace_bytes": [_P(kvd_layer), _i64, _P(_i64)],
     "kv_evict_born": [_P(kvd_layer), _vp, _i64, _i32, _i32, _vp, _i64, _vp],
     "kvd_decode_workspace_bytes": [_P(kvd_layer), _i32, _i32, _P(_i64)],
@@ -56,14 +67,16 @@ _SIGS = {
     "decode_attention_static": [_vp, _P(kvd_layer), _i32, _f32, _vp, _vp],
     "kvd_layer_device_error": [_P(kvd_layer), _i32, _P(C.c_uint32)],
     "rswa_record_prefill": [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i64, _i32,
-                            _vp, _vp, _vp, _vp],
-    "rswa_ring_write": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp],
+                            _vp, _vp, _vp, _vp, _vp],
+    "rswa_ring_write": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp],
+    "rswa_checkpoint_take": [C.c_uint64, _vp, _vp, _vp, _vp, _i32, _P(rswa_checkpoint)],
+    "rswa_rollback_to": [C.c_uint64, _vp, _vp, _vp, _vp, _i32, _i32, _P(rswa_checkpoint)],
     "rswa_decode_workspace_bytes": [_i32, _i32, _i32, _i64, _i32, _P(_i64)],
     "rswa_decode": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, _i32, _f32,
                     _vp, _vp, _i64, _vp],
     "rswa_record_prefill_i8": [_vp, _vp, _P(rswa_i8_mirror), _vp, _vp, _i32, _i32, _i32, _i32, _i32,
-                               _i64, _i32, _vp, _vp, _vp, _vp],
-    "rswa_ring_write_i8": [_vp, _vp, _P(rswa_i8_mirror), _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
+                               _i64, _i32, _vp, _vp, _vp, _vp, _vp],
+    "rswa_ring_write_i8": [_vp, _vp, _P(rswa_i8_mirror), _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
                            _i32, _vp, _vp],
     "rswa_decode_i8": [_vp, _P(rswa_i8_mirror), _vp, _vp, _vp, _i32, _i32, _i32, _i64, _i32, _f32, _vp,
                        _vp, _i64, _vp],

@@ -169,6 +169,18 @@ def kv_freeze_colfield(layer: LayerKvCache, stream=None):
     _abi.call("kv_freeze_colfield", C.byref(layer.L), _stream(stream))
 
 
+def kv_truncate_last(layer: LayerKvCache, n_drop=1, imp: torch.Tensor | None = None, stream=None):
+    """cortiq truncate_last: drop the last n_drop rows of every sequence (an int for
+    all, or one count per sequence); with imp, the dropped rows' masses are cleared."""
+    counts = np.broadcast_to(np.asarray(n_drop, np.int32), (layer.n_seq,)).copy()
+    if imp is not None:
+        _f32_cuda(imp, "imp")
+        if imp.numel() < layer.imp_len:
+            raise ValueError("imp must hold %d floats" % layer.imp_len)
+    _abi.call("kv_truncate_last", C.byref(layer.L), _np_ptr(counts), _ptr(imp) if imp is not None else None,
+              _stream(stream))
+
+
 def kv_evict_born(layer: LayerKvCache, imp: torch.Tensor, keep_last: int, sink: int = 4,
                   recent: int | None = None, workspace: torch.Tensor | None = None, stream=None):
     """cortiq evict_born on every sequence holding more than keep_last rows: keep the
@@ -254,6 +266,8 @@ class RingCache:
     int8 mirror (rswa Int8Kv: codes of the same shapes, one f32 scale per row)
     is kept beside the f32 regions and written by the same calls."""
 
+    _next_id = 0
+
     def __init__(self, B: int, ref_cap: int, H: int = 10, head_dim: int = 128, W: int = 128,
                  device="cuda", int8: bool = False):
         self.B, self.H, self.head_dim, self.W, self.ref_cap = B, H, head_dim, W, ref_cap
@@ -279,9 +293,26 @@ class RingCache:
         self.prefill_len = np.full(B, -1, np.int32)
         self.ring_len = np.zeros(B, np.int32)
         self.ring_pos = np.zeros(B, np.int32)
+        # decode-write counts and branch lineages (checkpoint / rollback)
+        self.history = (_abi.rswa_history * B)()
+        RingCache._next_id += 1
+        self.cache_id = RingCache._next_id
         n = C.c_int64(0)
         _abi.call("rswa_decode_workspace_bytes", B, H, head_dim, ref_cap, W, C.byref(n))
         self.workspace = torch.zeros(int(n.value), dtype=torch.uint8, device=dev)
+
+    def checkpoint(self, s: int):
+        """rswa RingCache::checkpoint of stream s (cursors only, no K/V copy)."""
+        cp = _abi.rswa_checkpoint()
+        _abi.call("rswa_checkpoint_take", self.cache_id, _np_ptr(self.prefill_len), _np_ptr(self.ring_len),
+                  _np_ptr(self.ring_pos), self.history, int(s), C.byref(cp))
+        return cp
+
+    def rollback_to(self, s: int, cp) -> None:
+        """rswa RingCache::rollback_to: discard stream s's ring writes since cp
+        (KvdError with status -3, nothing changed, when the page refuses it)."""
+        _abi.call("rswa_rollback_to", self.cache_id, _np_ptr(self.prefill_len), _np_ptr(self.ring_len),
+                  _np_ptr(self.ring_pos), self.history, int(s), self.W, C.byref(cp))
 
     def device_error(self, clear: bool = True) -> int:
         w = C.c_uint32(0)
@@ -300,7 +331,7 @@ def rswa_record_prefill(cache: RingCache, s: int, k: torch.Tensor, v: torch.Tens
         raise ValueError("prefill k/v must be [H, seq, head_dim]")
     args = (int(s), int(seq), cache.B, cache.H, cache.head_dim, cache.ref_cap, cache.W,
             _np_ptr(cache.prefill_len), _np_ptr(cache.ring_len), _np_ptr(cache.ring_pos),
-            _stream(stream))
+            cache.history, _stream(stream))
     if cache.mirror is not None:
         _abi.call("rswa_record_prefill_i8", _ptr(cache.ref_k), _ptr(cache.ref_v), C.byref(cache.mirror),
                   _ptr(k), _ptr(v), *args)
@@ -316,8 +347,8 @@ def rswa_ring_write(cache: RingCache, k: torch.Tensor, v: torch.Tensor, stream=N
         raise ValueError("k/v must be [B, H, head_dim]")
     slots = np.zeros(cache.B, np.int32)
     args = (_ptr(k), _ptr(v), _np_ptr(cache.prefill_len), _np_ptr(cache.ring_len),
-            _np_ptr(cache.ring_pos), cache.B, cache.H, cache.head_dim, cache.W, _np_ptr(slots),
-            _stream(stream))
+            _np_ptr(cache.ring_pos), cache.history, cache.B, cache.H, cache.head_dim, cache.W,
+            _np_ptr(slots), _stream(stream))
     if cache.mirror is not None:
         _abi.call("rswa_ring_write_i8", _ptr(cache.ring_k), _ptr(cache.ring_v), C.byref(cache.mirror),
                   *args)

@@ -625,7 +625,7 @@ static bool mirror_ok(const rswa_i8_mirror *m) {
 static kvd_status record_prefill(float *ref_k, float *ref_v, const rswa_i8_mirror *m, const float *k,
                           const float *v, int32_t s, int32_t seq, int32_t B, int32_t H,
                           int32_t head_dim, int64_t ref_cap, int32_t W, int32_t *prefill_len,
-                          int32_t *ring_len, int32_t *ring_pos, void *stream) {
+                          int32_t *ring_len, int32_t *ring_pos, rswa_history *hist, void *stream) {
     if (ref_k == nullptr || ref_v == nullptr || prefill_len == nullptr || ring_len == nullptr ||
         ring_pos == nullptr)
         return KVD_EINVAL;
@@ -633,6 +633,8 @@ static kvd_status record_prefill(float *ref_k, float *ref_v, const rswa_i8_mirro
         return KVD_EINVAL;
     if (seq > ref_cap) return KVD_ECAPACITY;
     if (seq > 0 && (k == nullptr || v == nullptr)) return KVD_EINVAL;
+    // the new lineage is reserved before anything changes
+    if (hist != nullptr && hist[s].lineage_epoch == UINT64_MAX) return KVD_ESTATE;
     if (m != nullptr) {
         if (!mirror_ok(m) || (head_dim != 64 && head_dim != 128) || !aligned16(ref_k) ||
             !aligned16(ref_v) || (seq > 0 && (!aligned16(k) || !aligned16(v))))
@@ -658,6 +660,10 @@ static kvd_status record_prefill(float *ref_k, float *ref_v, const rswa_i8_mirro
     prefill_len[s] = seq;
     ring_len[s] = 0;
     ring_pos[s] = 0;
+    if (hist != nullptr) {
+        hist[s].decode_writes = 0;
+        hist[s].lineage_epoch += 1;
+    }
     return KVD_OK;
 }
 
@@ -665,25 +671,25 @@ extern "C" kvd_status rswa_record_prefill(float *ref_k, float *ref_v, const floa
                                           const float *v, int32_t s, int32_t seq, int32_t B,
                                           int32_t H, int32_t head_dim, int64_t ref_cap, int32_t W,
                                           int32_t *prefill_len, int32_t *ring_len,
-                                          int32_t *ring_pos, void *stream) {
+                                          int32_t *ring_pos, rswa_history *hist, void *stream) {
     return record_prefill(ref_k, ref_v, nullptr, k, v, s, seq, B, H, head_dim, ref_cap, W,
-                          prefill_len, ring_len, ring_pos, stream);
+                          prefill_len, ring_len, ring_pos, hist, stream);
 }
 
 extern "C" kvd_status rswa_record_prefill_i8(float *ref_k, float *ref_v, const rswa_i8_mirror *m,
                                              const float *k, const float *v, int32_t s, int32_t seq,
                                              int32_t B, int32_t H, int32_t head_dim, int64_t ref_cap,
                                              int32_t W, int32_t *prefill_len, int32_t *ring_len,
-                                             int32_t *ring_pos, void *stream) {
+                                             int32_t *ring_pos, rswa_history *hist, void *stream) {
     if (m == nullptr) return KVD_EINVAL;
     return record_prefill(ref_k, ref_v, m, k, v, s, seq, B, H, head_dim, ref_cap, W, prefill_len,
-                          ring_len, ring_pos, stream);
+                          ring_len, ring_pos, hist, stream);
 }
 
 static kvd_status ring_write(float *ring_k, float *ring_v, const rswa_i8_mirror *m, const float *k,
                       const float *v, const int32_t *prefill_len, int32_t *ring_len,
-                      int32_t *ring_pos, int32_t B, int32_t H, int32_t head_dim, int32_t W,
-                      int32_t *slot_out, void *stream) {
+                      int32_t *ring_pos, rswa_history *hist, int32_t B, int32_t H, int32_t head_dim,
+                      int32_t W, int32_t *slot_out, void *stream) {
     if (ring_k == nullptr || ring_v == nullptr || k == nullptr || v == nullptr ||
         prefill_len == nullptr || ring_len == nullptr || ring_pos == nullptr)
         return KVD_EINVAL;
@@ -695,6 +701,8 @@ static kvd_status ring_write(float *ring_k, float *ring_v, const rswa_i8_mirror 
         if (prefill_len[s] < 0) return KVD_ESTATE;
         if (ring_len[s] < 0 || ring_len[s] > W || ring_pos[s] < 0 || ring_pos[s] >= W)
             return KVD_EINVAL;
+        if (hist != nullptr && (hist[s].decode_writes < 0 || hist[s].decode_writes == INT64_MAX))
+            return KVD_ESTATE;
     }
     std::vector<int32_t> slot(B);
     for (int s = 0; s < B; ++s) slot[s] = ring_len[s] < W ? ring_len[s] : ring_pos[s];
@@ -727,26 +735,66 @@ static kvd_status ring_write(float *ring_k, float *ring_v, const rswa_i8_mirror 
             ring_pos[s] = (ring_pos[s] + 1) % W;
         }
         if (slot_out) slot_out[s] = slot[s];
+        if (hist) hist[s].decode_writes += 1;
     }
     return KVD_OK;
 }
 
 extern "C" kvd_status rswa_ring_write(float *ring_k, float *ring_v, const float *k, const float *v,
                                       const int32_t *prefill_len, int32_t *ring_len,
-                                      int32_t *ring_pos, int32_t B, int32_t H, int32_t head_dim,
-                                      int32_t W, int32_t *slot_out, void *stream) {
-    return ring_write(ring_k, ring_v, nullptr, k, v, prefill_len, ring_len, ring_pos, B, H, head_dim,
-                      W, slot_out, stream);
+                                      int32_t *ring_pos, rswa_history *hist, int32_t B, int32_t H,
+                                      int32_t head_dim, int32_t W, int32_t *slot_out, void *stream) {
+    return ring_write(ring_k, ring_v, nullptr, k, v, prefill_len, ring_len, ring_pos, hist, B, H,
+                      head_dim, W, slot_out, stream);
 }
 
 extern "C" kvd_status rswa_ring_write_i8(float *ring_k, float *ring_v, const rswa_i8_mirror *m,
                                          const float *k, const float *v, const int32_t *prefill_len,
-                                         int32_t *ring_len, int32_t *ring_pos, int32_t B, int32_t H,
-                                         int32_t head_dim, int32_t W, int32_t *slot_out,
-                                         void *stream) {
+                                         int32_t *ring_len, int32_t *ring_pos, rswa_history *hist,
+                                         int32_t B, int32_t H, int32_t head_dim, int32_t W,
+                                         int32_t *slot_out, void *stream) {
     if (m == nullptr) return KVD_EINVAL;
-    return ring_write(ring_k, ring_v, m, k, v, prefill_len, ring_len, ring_pos, B, H, head_dim, W,
-                      slot_out, stream);
+    return ring_write(ring_k, ring_v, m, k, v, prefill_len, ring_len, ring_pos, hist, B, H, head_dim,
+                      W, slot_out, stream);
+}
+
+extern "C" kvd_status rswa_checkpoint_take(uint64_t cache_id, const int32_t *prefill_len,
+                                           const int32_t *ring_len, const int32_t *ring_pos,
+                                           const rswa_history *hist, int32_t s, rswa_checkpoint *out) {
+    if (prefill_len == nullptr || ring_len == nullptr || ring_pos == nullptr || hist == nullptr ||
+        out == nullptr || s < 0)
+        return KVD_EINVAL;
+    rswa_checkpoint cp{};
+    cp.cache_id = cache_id;
+    cp.lineage_epoch = hist[s].lineage_epoch;
+    cp.decode_writes = hist[s].decode_writes;
+    cp.prefill_len = prefill_len[s];
+    cp.ring_len = ring_len[s];
+    cp.ring_pos = ring_pos[s];
+    *out = cp;
+    return KVD_OK;
+}
+
+extern "C" kvd_status rswa_rollback_to(uint64_t cache_id, const int32_t *prefill_len, int32_t *ring_len,
+                                       int32_t *ring_pos, rswa_history *hist, int32_t s, int32_t W,
+                                       const rswa_checkpoint *cp) {
+    if (prefill_len == nullptr || ring_len == nullptr || ring_pos == nullptr || hist == nullptr ||
+        cp == nullptr || s < 0 || W < 1)
+        return KVD_EINVAL;
+    // the page's order of refusals; nothing changes on any of them
+    if (cp->cache_id != cache_id) return KVD_ESTATE;
+    if (cp->prefill_len != prefill_len[s]) return KVD_ESTATE;
+    if (cp->lineage_epoch != hist[s].lineage_epoch) return KVD_ESTATE;
+    if (cp->decode_writes > hist[s].decode_writes) return KVD_ESTATE;
+    const int64_t discarded = hist[s].decode_writes - cp->decode_writes;
+    if (cp->ring_len < 0 || cp->ring_len > W || discarded > int64_t(W) - cp->ring_len) return KVD_ESTATE;
+    if (cp->ring_pos < 0 || cp->ring_pos >= W) return KVD_EINVAL;
+    if (discarded > 0 && hist[s].lineage_epoch == UINT64_MAX) return KVD_ESTATE;
+    ring_len[s] = cp->ring_len;
+    ring_pos[s] = cp->ring_pos;
+    hist[s].decode_writes = cp->decode_writes;
+    if (discarded > 0) hist[s].lineage_epoch += 1;
+    return KVD_OK;
 }
 
 extern "C" kvd_status rswa_decode_workspace_bytes(int32_t B, int32_t H, int32_t head_dim,

@@ -10,7 +10,7 @@
 //           kept and, of the rows equal to T, the lowest positions (the
 //           order of the page's stable sort).  Two ordered block scans turn
 //           the keep flags into the ascending list of kept rows, and the
-//           CTA gathers imp along it.
+//           CTA gathers imp along it (clearing the dropped rows' entries).
 //   gather  one CTA per (live head, storage): the kept rows move down to
 //           positions 0 .. keep_last - 1 of every storage independently (f32
 //           K / V, int8 codes, their scales).  Kept positions ascend and
@@ -19,6 +19,9 @@
 //           overwrote: the move is in place, with no staging copy.
 // The device length becomes keep_last in the select kernel; the host mirror
 // is updated by the entry point.
+//
+// Also here: cortiq LayerKvCache::truncate_last (the speculative-decode
+// reject), which only shortens the lengths and clears the dropped rows' imp.
 
 #include <algorithm>
 #include <vector>
@@ -152,7 +155,9 @@ __global__ void __launch_bounds__(kSelectThreads) born_select_kernel(BornArgs a,
         return;
     }
 
-    // ---- imp follows its rows (in place, tiles in order)
+    // ---- imp follows its rows (in place, tiles in order); the entries of the
+    // dropped rows are cleared: a row appended there later starts from zero
+    // mass, as each appended row does on the page
     for (int j0 = sink_n; j0 < keep_last; j0 += kSelectThreads) {
         const int j = j0 + tid;
         float v = 0.0f;
@@ -161,6 +166,7 @@ __global__ void __launch_bounds__(kSelectThreads) born_select_kernel(BornArgs a,
         if (j < keep_last) imp[j] = v;
         __syncthreads();
     }
+    for (int j = keep_last + tid; j < stored; j += kSelectThreads) imp[j] = 0.0f;
     if (tid == 0) a.seq_len[b] = keep_last;
 }
 
@@ -227,6 +233,24 @@ __global__ void __launch_bounds__(kGatherThreads) born_gather_kernel(GatherArgs 
     else
         gather_region(reinterpret_cast<uint32_t *>(region), g.row_bytes / 4, kept, a.sink_n, a.keep_last, cap,
                       a.err);
+}
+
+struct TruncTable {
+    int32_t n;
+    int32_t seq[kSlice];
+    int32_t new_len[kSlice];
+    int32_t old_len[kSlice];
+    int64_t imp_base[kSlice];
+};
+
+__global__ void truncate_kernel(int32_t *seq_len, float *imp, TruncTable t) {
+    const int i = blockIdx.x;
+    if (i >= t.n) return;
+    if (imp != nullptr) {
+        float *m = imp + t.imp_base[i];
+        for (int p = t.new_len[i] + int(threadIdx.x); p < t.old_len[i]; p += blockDim.x) m[p] = 0.0f;
+    }
+    if (threadIdx.x == 0) seq_len[t.seq[i]] = t.new_len[i];
 }
 
 int64_t evict_ws_bytes(const Layer *l, int64_t keep_last) {
@@ -311,5 +335,32 @@ extern "C" kvd_status kv_evict_born(kvd_layer *L, float *imp, int64_t keep_last,
         }
     }
     for (int b : todo) l->h_seq_len[b] = keep_last;
+    return KVD_OK;
+}
+
+extern "C" kvd_status kv_truncate_last(kvd_layer *L, const int32_t *n_drop, float *imp, void *stream) {
+    Layer *l = checked_layer(L);
+    if (l == nullptr || (reinterpret_cast<uintptr_t>(imp) & 3)) return KVD_EINVAL;
+    for (int b = 0; b < l->n_seq; ++b)
+        if (n_drop != nullptr && n_drop[b] < 0) return KVD_EINVAL;
+    std::vector<int32_t> todo;
+    for (int b = 0; b < l->n_seq; ++b)
+        if ((n_drop ? n_drop[b] : 1) > 0 && l->h_seq_len[b] > 0) todo.push_back(b);
+    cudaStream_t st = as_stream(stream);
+    for (size_t s0 = 0; s0 < todo.size(); s0 += kSlice) {
+        TruncTable t;
+        t.n = int32_t(std::min<size_t>(kSlice, todo.size() - s0));
+        for (int i = 0; i < t.n; ++i) {
+            const int b = todo[s0 + i];
+            const int64_t d = std::min<int64_t>(n_drop ? n_drop[b] : 1, l->h_seq_len[b]);
+            t.seq[i] = b;
+            t.old_len[i] = int32_t(l->h_seq_len[b]);
+            t.new_len[i] = int32_t(l->h_seq_len[b] - d);
+            t.imp_base[i] = l->h_imp_base[b];
+        }
+        truncate_kernel<<<unsigned(t.n), 256, 0, st>>>(l->d_seq_len, imp, t);
+        if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
+        for (int i = 0; i < t.n; ++i) l->h_seq_len[t.seq[i]] = t.new_len[i];
+    }
     return KVD_OK;
 }

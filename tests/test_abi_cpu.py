@@ -86,7 +86,7 @@ def test_rswa_host_validation_before_any_launch(abi):
     fake = C.c_void_p(1 << 20)  # never dereferenced: validation fails first
     p = lambda a: C.c_void_p(a.ctypes.data)
     # a stream without prefill: ESTATE and the cursors stay untouched
-    st = L.rswa_ring_write(fake, fake, fake, fake, p(pl), p(rl), p(rp), B, H, hd, W, None, None)
+    st = L.rswa_ring_write(fake, fake, fake, fake, p(pl), p(rl), p(rp), None, B, H, hd, W, None, None)
     assert st == abi.ESTATE and rl.tolist() == [0, 0] and rp.tolist() == [0, 0]
     n = C.c_int64(0)
     assert L.rswa_decode_workspace_bytes(B, H, hd, 32640, W, C.byref(n)) == abi.OK and n.value > 0
@@ -100,7 +100,7 @@ def test_rswa_host_validation_before_any_launch(abi):
     assert st == abi.EEMPTY  # stream 0: no keys
     # capacity: a prefill longer than the reference block
     st = L.rswa_record_prefill(fake, fake, fake, fake, 0, 33000, B, H, hd, 32640, W, p(pl), p(rl),
-                               p(rp), None)
+                               p(rp), None, None)
     assert st == abi.ECAPACITY and pl.tolist() == [0, 5]
     # ragged region sizes are refused (bulk copies move 16-row groups)
     pl[:] = [3, 5]
@@ -126,3 +126,64 @@ def test_api_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(_abi, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
         _abi.lib()
+
+
+def test_rswa_checkpoint_rollback_contract(abi):
+    """rswa RingCache::checkpoint / rollback_to (host cursors only): a rollback
+    restores ring_len, ring_pos and the write count and starts a new lineage;
+    a checkpoint from another cache, another prefill boundary, an abandoned
+    lineage or the future, or one whose discarded writes wrapped over a row
+    live at the checkpoint, is refused with nothing changed."""
+    L = abi.lib()
+    B, W, cid = 2, 128, 77
+    pl = np.array([10, 40], np.int32)
+    rl = np.array([5, 128], np.int32)
+    rp = np.array([5, 9], np.int32)
+    hist = (abi.rswa_history * B)()
+    hist[0].decode_writes, hist[0].lineage_epoch = 5, 1
+    hist[1].decode_writes, hist[1].lineage_epoch = 300, 1
+    p = lambda a: C.c_void_p(a.ctypes.data)
+    cp = abi.rswa_checkpoint()
+    assert L.rswa_checkpoint_take(cid, p(pl), p(rl), p(rp), hist, 0, C.byref(cp)) == abi.OK
+    assert (cp.prefill_len, cp.ring_len, cp.ring_pos, cp.decode_writes, cp.lineage_epoch) == (10, 5, 5, 5, 1)
+
+    def state():
+        return (rl.tolist(), rp.tolist(), hist[0].decode_writes, hist[0].lineage_epoch)
+
+    # three speculative writes into the warm ring, as rswa_ring_write applies them
+    rl[0], rp[0], hist[0].decode_writes = 8, 8, 8
+    before = state()
+    for bad_id, bad in ((cid + 1, None), (cid, "prefill"), (cid, "future")):
+        c2 = abi.rswa_checkpoint.from_buffer_copy(cp)
+        if bad == "prefill":
+            c2.prefill_len = 11
+        if bad == "future":
+            c2.decode_writes = 9
+        assert L.rswa_rollback_to(bad_id, p(pl), p(rl), p(rp), hist, 0, W, C.byref(c2)) == abi.ESTATE
+        assert state() == before
+    assert L.rswa_rollback_to(cid, p(pl), p(rl), p(rp), hist, 0, W, C.byref(cp)) == abi.OK
+    assert state() == ([5, 128], [5, 9], 5, 2)
+    # the same checkpoint now belongs to an abandoned lineage
+    assert L.rswa_rollback_to(cid, p(pl), p(rl), p(rp), hist, 0, W, C.byref(cp)) == abi.ESTATE
+    # a rollback that discards nothing keeps the lineage
+    cp2 = abi.rswa_checkpoint()
+    assert L.rswa_checkpoint_take(cid, p(pl), p(rl), p(rp), hist, 0, C.byref(cp2)) == abi.OK
+    assert L.rswa_rollback_to(cid, p(pl), p(rl), p(rp), hist, 0, W, C.byref(cp2)) == abi.OK
+    assert hist[0].lineage_epoch == 2
+    # steady state (ring full): any discarded write overwrote a live row
+    cp3 = abi.rswa_checkpoint()
+    assert L.rswa_checkpoint_take(cid, p(pl), p(rl), p(rp), hist, 1, C.byref(cp3)) == abi.OK
+    rp[1], hist[1].decode_writes = 10, 301
+    assert L.rswa_rollback_to(cid, p(pl), p(rl), p(rp), hist, 1, W, C.byref(cp3)) == abi.ESTATE
+    assert (rl[1], rp[1], hist[1].decode_writes, hist[1].lineage_epoch) == (128, 10, 301, 1)
+    # warm ring: exactly W - ring_len discarded writes are still lossless, one more is not
+    rl[0], rp[0], hist[0].decode_writes = 100, 100, 40
+    cp4 = abi.rswa_checkpoint()
+    assert L.rswa_checkpoint_take(cid, p(pl), p(rl), p(rp), hist, 0, C.byref(cp4)) == abi.OK
+    rl[0], rp[0], hist[0].decode_writes = 128, 0, 68
+    assert L.rswa_rollback_to(cid, p(pl), p(rl), p(rp), hist, 0, W, C.byref(cp4)) == abi.OK
+    assert (rl[0], rp[0], hist[0].decode_writes) == (100, 100, 40)
+    cp5 = abi.rswa_checkpoint()
+    assert L.rswa_checkpoint_take(cid, p(pl), p(rl), p(rp), hist, 0, C.byref(cp5)) == abi.OK
+    rl[0], rp[0], hist[0].decode_writes = 128, 1, 69
+    assert L.rswa_rollback_to(cid, p(pl), p(rl), p(rp), hist, 0, W, C.byref(cp5)) == abi.ESTATE

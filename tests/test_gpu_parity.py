@@ -462,7 +462,8 @@ def test_rswa_i8_errors(torch, kvd):
     x = torch.ones(10, 4, 96, device="cuda")
     pl, rl, rp = (np.array(a, np.int32) for a in (cache.prefill_len, cache.ring_len, cache.ring_pos))
     args = (C.c_void_p(x.data_ptr()), C.c_void_p(x.data_ptr()), 0, 4, 2, 10, 96, 32, 128,
-            pl.ctypes.data_as(C.c_void_p), rl.ctypes.data_as(C.c_void_p), rp.ctypes.data_as(C.c_void_p), None)
+            pl.ctypes.data_as(C.c_void_p), rl.ctypes.data_as(C.c_void_p), rp.ctypes.data_as(C.c_void_p), None,
+            None)
     ref = (C.c_void_p(cache.ref_k.data_ptr()), C.c_void_p(cache.ref_v.data_ptr()))
     assert lib.rswa_record_prefill_i8(*ref, C.byref(cache.mirror), *args) == -1
     assert lib.rswa_record_prefill_i8(*ref, None, *args) == -1
@@ -504,22 +505,25 @@ def test_born_eviction_parity(torch, kvd, mode, hd):
     imp = torch.from_numpy(full.copy()).cuda()
     kvd.kv_evict_born(layer, imp, keep, sink, recent)
     got_imp = imp.cpu().numpy()
+    o_imps = []
     for b, oc in enumerate(ocs):
         o_imp = np.zeros(oc.cap, np.float32)
         o_imp[:lengths[b]] = per[b]
         assert oc.evict_born(keep, sink, recent, o_imp) == min(lengths[b], keep)
-        n = oc.seq_len
-        assert np.array_equal(got_imp[layer.imp_base[b]:layer.imp_base[b] + n].view(np.uint32),
-                              o_imp[:n].view(np.uint32)), b
+        n_old = lengths[b]
+        # kept masses gathered, the dropped rows' entries cleared
+        assert np.array_equal(got_imp[layer.imp_base[b]:layer.imp_base[b] + n_old].view(np.uint32),
+                              o_imp[:n_old].view(np.uint32)), b
+        o_imps.append(o_imp.astype(np.float64))
     assert_storage_bitexact(layer, ocs, torch)
     assert layer.device_error() == 0
     n_q = n_kv * 2
     scale = np.float32(1.0 / math.sqrt(hd))
     for step in range(2):
         q = synthetic.normal((len(lengths), n_q, hd), 63 + step)
-        out = kvd.decode_attention(torch.from_numpy(q).cuda(), layer, scale=float(scale)).cpu().numpy()
+        out = kvd.decode_attention(torch.from_numpy(q).cuda(), layer, imp=imp, scale=float(scale)).cpu().numpy()
         for b, oc in enumerate(ocs):
-            ref = oc.decode(q[b], n_q, scale)
+            ref = oc.decode(q[b], n_q, scale, o_imps[b])
             live = np.repeat(np.array(alive, bool), 2)
             assert out_error(out[b], ref, live) <= OUT_TOL, (step, b)
         # rows appended after the eviction land behind the kept rows
@@ -530,6 +534,9 @@ def test_born_eviction_parity(torch, kvd, mode, hd):
             oc.append(k_new[b], v_new[b])
             oc.freeze_if_due()
     assert_storage_bitexact(layer, ocs, torch)
+    got_imp = imp.cpu().numpy()
+    for b, oc in enumerate(ocs):  # masses accumulated after the eviction, on the kept and new rows
+        assert_imp_close(got_imp[layer.imp_base[b]:layer.imp_base[b] + oc.seq_len], o_imps[b][:oc.seq_len])
 
 
 def test_born_page_example_on_gpu(torch, kvd):
@@ -575,3 +582,91 @@ def test_born_edges_and_errors(torch, kvd):
     kvd.kv_evict_born(layer, imp, 0, 4, 8)
     assert layer.seq_len(0) == 0 and layer.seq_len(1) == 0 and layer.frozen(0)
     assert layer.device_error() == 0
+
+
+# ------------------------------- truncate_last and ring rollback (NEXT-4)
+
+@pytest.mark.parametrize("mode", list(MODES))
+def test_truncate_last_parity(torch, kvd, mode):
+    """cortiq truncate_last per sequence (0, 3, more than stored, 70 rows: below
+    the freeze point of a frozen sequence): lengths and storages match the
+    oracle, imp of the dropped rows is cleared, and rows appended afterwards
+    (quantised against the kept fields) decode like the oracle's."""
+    lengths = [90, 200, 30, 150]
+    n_kv, hd = 2, 128
+    ks, vs = seq_rows(lengths, n_kv, hd, seed=81)
+    layer = _layer(kvd, MODES[mode], lengths, n_kv, hd, None, cap_extra=8)
+    gpu_append_bulk(layer, ks, vs, torch)
+    ocs = oracle_caches(MODES[mode], lengths, n_kv, hd, None, ks, vs, cap=max(lengths) + 8)
+    for oc in ocs:
+        oc.freeze_if_due()
+    rng = np.random.default_rng(82)
+    full = rng.random(layer.imp_len).astype(np.float32)
+    imp = torch.from_numpy(full.copy()).cuda()
+    drop = np.array([0, 3, 100, 70], np.int32)
+    kvd.kv_truncate_last(layer, drop, imp)
+    got = imp.cpu().numpy()
+    o_imps = []
+    for b, oc in enumerate(ocs):
+        o_imp = full[layer.imp_base[b]:layer.imp_base[b] + oc.cap].copy()
+        oc.truncate_last(int(drop[b]), o_imp)
+        n_old = lengths[b]
+        assert np.array_equal(got[layer.imp_base[b]:layer.imp_base[b] + n_old], o_imp[:n_old]), b
+        o_imps.append(o_imp.astype(np.float64))
+    assert [layer.seq_len(b) for b in range(4)] == [90, 197, 0, 80]
+    assert_storage_bitexact(layer, ocs, torch)
+    k_new = synthetic.normal((4, n_kv, hd), 83)
+    v_new = synthetic.normal((4, n_kv, hd), 84)
+    kvd.kv_append(layer, torch.from_numpy(k_new).cuda(), torch.from_numpy(v_new).cuda())
+    for b, oc in enumerate(ocs):
+        oc.append(k_new[b], v_new[b])
+        oc.freeze_if_due()
+    assert_storage_bitexact(layer, ocs, torch)
+    n_q = 4
+    q = synthetic.normal((4, n_q, hd), 85)
+    scale = np.float32(1.0 / math.sqrt(hd))
+    out = kvd.decode_attention(torch.from_numpy(q).cuda(), layer, imp=imp, scale=float(scale)).cpu().numpy()
+    got = imp.cpu().numpy()
+    for b, oc in enumerate(ocs):
+        ref = oc.decode(q[b], n_q, scale, o_imps[b])
+        assert out_error(out[b], ref) <= OUT_TOL, b
+        assert_imp_close(got[layer.imp_base[b]:layer.imp_base[b] + oc.seq_len], o_imps[b][:oc.seq_len])
+    assert layer.device_error() == 0
+
+
+@pytest.mark.parametrize("int8", [False, True])
+def test_rswa_rollback_erases_speculative_steps(torch, kvd, int8):
+    """rswa checkpoint -> three draft writes -> rollback: the decode after the
+    rollback is bit-identical to the decode before the drafts, and the steps
+    written afterwards match a cache that never saw the drafts."""
+    B, H, hd, W, ref_cap = 2, 10, 128, 128, 64
+    mk = lambda: kvd.RingCache(B, ref_cap, H, hd, W, int8=int8)
+    spec, plain = mk(), mk()
+    dec = kvd.rswa_decode_i8 if int8 else kvd.rswa_decode
+    for c in (spec, plain):
+        for s in range(B):
+            k = synthetic.normal((H, 40, hd), 90 + s)
+            kvd.rswa_record_prefill(c, s, torch.from_numpy(k).cuda(), torch.from_numpy(k * 0.5).cuda())
+    steps = [(synthetic.normal((B, H, hd), 100 + t), synthetic.normal((B, H, hd), 200 + t)) for t in range(6)]
+    q = torch.from_numpy(synthetic.normal((B, H, hd), 300)).cuda()
+    for t in range(2):
+        for c in (spec, plain):
+            kvd.rswa_ring_write(c, torch.from_numpy(steps[t][0]).cuda(), torch.from_numpy(steps[t][1]).cuda())
+    before = dec(q, spec).cpu().numpy()
+    cps = [spec.checkpoint(s) for s in range(B)]
+    for t in range(3):  # drafts
+        d = synthetic.normal((B, H, hd), 400 + t)
+        kvd.rswa_ring_write(spec, torch.from_numpy(d).cuda(), torch.from_numpy(d).cuda())
+    assert not np.array_equal(dec(q, spec).cpu().numpy(), before)
+    for s in range(B):
+        spec.rollback_to(s, cps[s])
+    assert spec.ring_len.tolist() == [2, 2] and spec.ring_pos.tolist() == [2, 2]
+    assert np.array_equal(dec(q, spec).cpu().numpy(), before)
+    with pytest.raises(kvd.KvdError) as e:  # the abandoned branch cannot be replayed
+        spec.rollback_to(0, cps[0])
+    assert e.value.status == -3
+    for t in range(2, 6):
+        for c in (spec, plain):
+            kvd.rswa_ring_write(c, torch.from_numpy(steps[t][0]).cuda(), torch.from_numpy(steps[t][1]).cuda())
+    assert np.array_equal(dec(q, spec).cpu().numpy(), dec(q, plain).cpu().numpy())
+    assert spec.device_error() == 0
