@@ -359,8 +359,9 @@ int kvo_attend_group(const kvo_cache *c, const float *q_group, int kv_head, int 
     return n;
 }
 
-/* cortiq attend_group_upto with its three options, for every stored row
- * (upto = all), in f64:
+/* cortiq attend_group_upto with its four options, in f64:
+ *   - upto >= 0 limits the stored rows to min(stored, upto) (the page's causal
+ *     limit: a query at position upto - 1 sees rows [0, upto)); upto < 0 = all;
  *   - only rows [first, stored) are scored, first clamped to stored - 1 (the
  *     earliest visible position; sliding-window layers pass stored - window);
  *     earlier rows have probability 0 and their imp entries are untouched;
@@ -374,10 +375,13 @@ int kvo_attend_group(const kvo_cache *c, const float *q_group, int kv_head, int 
  * [exp(z - m)]), m = max(max_p s_p, [z]); imp[p] += w_p over the heads.  A
  * dead or empty group yields zeros and leaves imp untouched. */
 int kvo_attend_group_ex(const kvo_cache *c, const float *q_group, int kv_head, int nheads,
-                        float scale, int first, float softcap, const float *sinks,
-                        double *out, double *imp)
+                        float scale, int first, float softcap, long long upto,
+                        const float *sinks, double *out, double *imp)
 {
     int hd = c->hd, stored = c->head_rows[kv_head];
+    /* upto: attend the first min(stored, upto) rows only (the page's causal
+     * limit; a negative value means none) */
+    if (upto >= 0 && upto < stored) stored = (int)upto;
     if (stored == 0) {
         for (int i = 0; i < nheads * hd; ++i) out[i] = 0.0;
         return 0;

@@ -66,7 +66,8 @@ def lib():
             L.kvo_row.restype = None
             L.kvo_attend_head.argtypes = [C.POINTER(_Cache), vp, i32, f32, vp, vp]
             L.kvo_attend_group.argtypes = [C.POINTER(_Cache), vp, i32, i32, f32, vp, vp]
-            L.kvo_attend_group_ex.argtypes = [C.POINTER(_Cache), vp, i32, i32, f32, i32, f32, vp, vp,
+            L.kvo_attend_group_ex.argtypes = [C.POINTER(_Cache), vp, i32, i32, f32, i32, f32, C.c_longlong,
+                                              vp, vp,
                                               vp]
             L.kvo_evict_born.argtypes = [C.POINTER(_Cache), vp, i32, i32, i32]
             L.kvo_truncate_last.argtypes = [C.POINTER(_Cache), vp, i32]
@@ -206,9 +207,10 @@ class OracleSeqCache:
         return out
 
     def attend_group_ex(self, q_group, kv_head: int, scale: float, first: int = 0,
-                        softcap: float = 0.0, sinks=None, imp=None):
-        """attend_group with a first visible row, logit soft-capping and learned
-        sink logits (one per head of the group, or None)."""
+                        softcap: float = 0.0, sinks=None, imp=None, upto: int = -1):
+        """attend_group with a first visible row, logit soft-capping, learned
+        sink logits (one per head of the group, or None) and the causal limit
+        upto (rows [0, upto) only; -1 = all rows)."""
         q_group = np.ascontiguousarray(q_group, dtype=np.float32)
         nheads = q_group.size // self.hd
         out = np.zeros((nheads, self.hd), np.float64)
@@ -217,7 +219,7 @@ class OracleSeqCache:
         sk = None if sinks is None else np.ascontiguousarray(sinks, dtype=np.float32)
         assert sk is None or sk.size == nheads
         lib().kvo_attend_group_ex(C.byref(self._s), _p(q_group), kv_head, nheads, scale, int(first),
-                                  float(softcap), _p(sk), _p(out), _p(imp))
+                                  float(softcap), int(upto), _p(sk), _p(out), _p(imp))
         return out
 
     def decode_ex(self, q, n_q: int, scale: float, window: int = 0, softcap: float = 0.0,
@@ -233,6 +235,25 @@ class OracleSeqCache:
             sk = None if sinks is None else np.asarray(sinks, np.float32)[g * hpk:(g + 1) * hpk]
             out[g * hpk:(g + 1) * hpk] = self.attend_group_ex(q[g * hpk:(g + 1) * hpk], g, scale, first,
                                                               softcap, sk, imp)
+        return out
+
+    def decode_verify(self, q, n_q: int, K: int, scale: float, window: int = 0, softcap: float = 0.0,
+                      sinks=None):
+        """Query-batched verify of K draft rows already appended: query k ([K, n_q,
+        hd]) attends with upto = stored - (K - 1 - k), i.e. the rows up to and
+        including draft k (causal among the drafts), and a sliding window counted
+        back from its own position.  Returns [K, n_q, hd] (f64)."""
+        hpk = n_q // self.n_kv
+        q = np.ascontiguousarray(q, dtype=np.float32).reshape(K, n_q, self.hd)
+        out = np.zeros((K, n_q, self.hd), np.float64)
+        for k in range(K):
+            for g in range(self.n_kv):
+                stored = int(self.head_rows[g])
+                upto = max(stored - (K - 1 - k), 0)
+                first = upto - window if window > 0 and upto > window else 0
+                sk = None if sinks is None else np.asarray(sinks, np.float32)[g * hpk:(g + 1) * hpk]
+                out[k, g * hpk:(g + 1) * hpk] = self.attend_group_ex(q[k, g * hpk:(g + 1) * hpk], g, scale, first,
+                                                                     softcap, sk, None, upto)
         return out
 
     def decode(self, q, n_q: int, scale: float, imp=None):

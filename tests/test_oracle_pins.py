@@ -922,3 +922,51 @@ def test_truncate_last_page_example_and_resume():
     out = c.attend_group(np.zeros((1, 4), f32), 0, f32(1.0))
     assert np.allclose(out[0], (0 + 1 + 2 + 9) / 4.0)  # the dropped rows are gone
     assert c.truncate_last(10, imp) == 0 and c.head_rows.tolist() == [0, 0]
+
+
+# ------------------------------------------------ verify / upto (NEXT-4)
+
+def test_upto_equals_a_truncated_cache_and_limits():
+    """[cortiq] attend_group_upto's upto: attending rows [0, upto) equals attending
+    a copy truncated to upto rows (truncate_last is pinned on its own); upto at
+    or above the stored rows changes nothing; upto 0 gives zeros; upto 1 returns
+    the first row's dequantised value."""
+    c = _ramp_cache(oracle.Q8, 2, 64, 120, seed=5)
+    t = _ramp_cache(oracle.Q8, 2, 64, 120, seed=5)
+    q = synthetic.normal((3, 64), 6)
+    sc = f32(0.125)
+    for u in (119, 90, 64, 2):
+        t.truncate_last(t.seq_len - u)
+        for first, cap_, sk in ((0, 0.0, None), (u // 2, 1.5, np.array([0.3, -1.0, 2.0], f32))):
+            got = c.attend_group_ex(q, 1, sc, first, cap_, sk, None, u)
+            ref = t.attend_group_ex(q, 1, sc, first, cap_, sk, None)
+            assert np.array_equal(got, ref), (u, first)
+    base = c.attend_group_ex(q, 0, sc)
+    assert np.array_equal(c.attend_group_ex(q, 0, sc, upto=120), base)
+    assert np.array_equal(c.attend_group_ex(q, 0, sc, upto=10 ** 6), base)
+    assert not c.attend_group_ex(q, 0, sc, upto=0).any()
+    one = c.attend_group_ex(q, 0, sc, upto=1)
+    assert np.allclose(one, np.tile(c.row(0, 0, True), (3, 1)), rtol=1e-14, atol=0)
+
+
+def test_verify_equals_sequential_decodes():
+    """Query-batched verify of K = 4 drafts (causal among them) equals decoding
+    after each draft's append in turn, with a window counted back from each
+    query's position, soft-capping and sinks."""
+    n_kv, hd, n_q, K = 2, 64, 6, 4
+    c_seq = _ramp_cache(oracle.F32, n_kv, hd, 70, seed=7)
+    c_bat = _ramp_cache(oracle.F32, n_kv, hd, 70, seed=7)
+    drafts = [(synthetic.normal((n_kv, hd), 20 + i), synthetic.normal((n_kv, hd), 30 + i)) for i in range(K)]
+    q = synthetic.normal((K, n_q, hd), 40)
+    sinks = synthetic.normal((n_q,), 41)
+    sc = f32(0.125)
+    seq = []
+    for k in range(K):
+        c_seq.append(*drafts[k])
+        seq.append(c_seq.decode_ex(q[k], n_q, sc, window=33, softcap=2.0, sinks=sinks))
+    for d in drafts:
+        c_bat.append(*d)
+    bat = c_bat.decode_verify(q, n_q, K, sc, window=33, softcap=2.0, sinks=sinks)
+    assert np.allclose(bat, np.stack(seq), rtol=1e-13, atol=1e-15)
+    # K = 1 is the plain decode
+    assert np.array_equal(c_bat.decode_verify(q[3:], n_q, 1, sc)[0], c_bat.decode(q[3], n_q, sc))
