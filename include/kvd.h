@@ -138,6 +138,26 @@ KVD_API kvd_status kv_append(kvd_layer *L, const float *k, const float *v, const
  * operation, then requantise every stored row against col.  Idempotent. */
 KVD_API kvd_status kv_freeze_colfield(kvd_layer *L, void *stream);
 
+/* Workspace bytes decode_attention_verify needs for n_q query heads and K drafts. */
+KVD_API kvd_status kvd_verify_workspace_bytes(const kvd_layer *L, int32_t n_q, int32_t K,
+                                              int64_t *bytes_out);
+
+/* Query-batched verify of K draft rows (speculative decode), read as cortiq
+ * attend_group_upto's causal limit: the K drafts have been appended
+ * (kv_append), so sequence b holds L_b rows ending with them; query k
+ * (q device f32 [n_seq][K][n_q][head_dim]) attends rows [first_k, upto_k)
+ * with upto_k = L_b - (K - 1 - k) -- everything before draft k and draft k
+ * itself, causal among the drafts -- first_k = upto_k - window when
+ * upto_k > window (else 0), softcap and sinks as decode_attention_ex.  Every
+ * K/V row is read once for the K * n_q queries (n_q / n_kv * K <= 16).
+ * out device f32 [n_seq][K][n_q][head_dim]; a query whose upto_k <= 0 gets
+ * zeros.  No imp (rejected drafts are dropped by kv_truncate_last).  With
+ * K = 1 it is decode_attention_ex without imp. */
+KVD_API kvd_status decode_attention_verify(const float *q, const kvd_layer *L, int32_t n_q, int32_t K,
+                                           float scale, int64_t window, float softcap,
+                                           const float *sinks, float *out, void *workspace,
+                                           int64_t workspace_bytes, void *stream);
+
 /* cortiq LayerKvCache::truncate_last (speculative-decode reject), batched:
  * sequence b drops its last min(n_drop[b], length) rows in every storage
  * (n_drop host [n_seq], NULL = one row each).  Only the lengths change;

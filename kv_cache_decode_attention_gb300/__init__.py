@@ -12,6 +12,7 @@ from .api import (  # noqa: F401
     RingCache,
     decode_attention,
     decode_attention_static,
+    decode_attention_verify,
     kv_append,
     kv_evict_born,
     kv_freeze_colfield,

@@ -59,6 +59,8 @@ _SIGS = {
     "kv_append": [_P(kvd_layer), _vp, _vp, _vp, _vp],
     "kv_freeze_colfield": [_P(kvd_layer), _vp],
     "kv_truncate_last": [_P(kvd_layer), _vp, _vp, _vp],
+    "kvd_verify_workspace_bytes": [_P(kvd_layer), _i32, _i32, _P(_i64)],
+    "decode_attention_verify": [_vp, _P(kvd_layer), _i32, _i32, _f32, _i64, _f32, _vp, _vp, _vp, _i64, _vp],
     "kv_evict_workspace_bytes": [_P(kvd_layer), _i64, _P(_i64)],
     "kv_evict_born": [_P(kvd_layer), _vp, _i64, _i32, _i32, _vp, _i64, _vp],
     "kvd_decode_workspace_bytes": [_P(kvd_layer), _i32, _i32, _P(_i64)],

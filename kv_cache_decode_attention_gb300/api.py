@@ -169,6 +169,35 @@ def kv_freeze_colfield(layer: LayerKvCache, stream=None):
     _abi.call("kv_freeze_colfield", C.byref(layer.L), _stream(stream))
 
 
+def decode_attention_verify(q: torch.Tensor, cache: LayerKvCache, K: int, out: torch.Tensor | None = None,
+                            scale: float | None = None, window: int = 0, softcap: float = 0.0,
+                            sinks: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                            stream=None) -> torch.Tensor:
+    """Query-batched verify of the last K rows (drafts already appended): q and out
+    [n_seq, K, n_q, hd]; query k attends up to and including draft k."""
+    _f32_cuda(q, "q")
+    n_q = q.numel() // (cache.n_seq * K * cache.head_dim)
+    if n_q * cache.n_seq * K * cache.head_dim != q.numel():
+        raise ValueError("q must be [n_seq, K, n_q, head_dim]")
+    if out is None:
+        out = torch.empty(cache.n_seq, K, n_q, cache.head_dim, device=q.device)
+    _f32_cuda(out, "out")
+    if scale is None:
+        scale = 1.0 / math.sqrt(cache.head_dim)
+    if sinks is not None:
+        _f32_cuda(sinks, "sinks")
+        if sinks.numel() != n_q:
+            raise ValueError("sinks must hold one logit per query head (%d)" % n_q)
+    if workspace is None:
+        n = C.c_int64(0)
+        _abi.call("kvd_verify_workspace_bytes", C.byref(cache.L), int(n_q), int(K), C.byref(n))
+        workspace = torch.empty(max(int(n.value), 256), dtype=torch.uint8, device=q.device)
+    _abi.call("decode_attention_verify", _ptr(q), C.byref(cache.L), int(n_q), int(K), C.c_float(scale),
+              int(window), C.c_float(softcap), _ptr(sinks), _ptr(out), _ptr(workspace),
+              int(workspace.numel()), _stream(stream))
+    return out
+
+
 def kv_truncate_last(layer: LayerKvCache, n_drop=1, imp: torch.Tensor | None = None, stream=None):
     """cortiq truncate_last: drop the last n_drop rows of every sequence (an int for
     all, or one count per sequence); with imp, the dropped rows' masses are cleared."""

@@ -612,6 +612,112 @@ extern "C" kvd_status decode_attention_ex(const float *q, const kvd_layer *L, in
     return KVD_OK;
 }
 
+// ------------------------------------------------------------ verify
+
+extern "C" kvd_status kvd_verify_workspace_bytes(const kvd_layer *L, int32_t n_q, int32_t K,
+                                                 int64_t *bytes_out) {
+    const Layer *l = checked_layer(L);
+    if (l == nullptr || bytes_out == nullptr || K < 1) return KVD_EINVAL;
+    if (n_q < l->n_kv || n_q % l->n_kv != 0 || int64_t(n_q / l->n_kv) * K > kMaxHpk) return KVD_EINVAL;
+    const DecodeWs w = decode_ws(l, n_q * K, false);
+    if (w.total < 0) return KVD_ECUDA;
+    *bytes_out = w.total;
+    return KVD_OK;
+}
+
+extern "C" kvd_status decode_attention_verify(const float *q, const kvd_layer *L, int32_t n_q, int32_t K,
+                                              float scale, int64_t window, float softcap, const float *sinks,
+                                              float *out, void *workspace, int64_t workspace_bytes,
+                                              void *stream) {
+    const Layer *l = checked_layer(L);
+    if (l == nullptr || q == nullptr || out == nullptr || K < 1) return KVD_EINVAL;
+    if (n_q < l->n_kv || n_q % l->n_kv != 0 || int64_t(n_q / l->n_kv) * K > kMaxHpk) return KVD_EINVAL;
+    if (!std::isfinite(scale)) return KVD_EINVAL;
+    if (window < 0 || !std::isfinite(softcap) || softcap < 0.0f) return KVD_EINVAL;
+    if (!aligned16(q) || !aligned16(out) || (sinks && (reinterpret_cast<uintptr_t>(sinks) & 3)))
+        return KVD_EINVAL;
+    const int hg = n_q / l->n_kv, hpk = hg * K;
+    const DecodeWs w = decode_ws(l, n_q * K, false);
+    if (w.total < 0) return KVD_ECUDA;
+    if (workspace == nullptr || workspace_bytes < w.total ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255))
+        return KVD_EINVAL;
+    cudaStream_t st = as_stream(stream);
+    char *ws = static_cast<char *>(workspace);
+    int64_t work = 0, max_len = 0;
+    for (int b = 0; b < l->n_seq; ++b) {
+        const int64_t Lb = l->h_seq_len[b];
+        const int64_t vis = Lb - first_visible(verify_len(Lb, K), window) / kRowAlign * kRowAlign;
+        work += vis * int64_t(l->n_live);
+        max_len = std::max(max_len, vis);
+    }
+    const int32_t chunk = pick_chunk(work);
+    SplitArgs a;
+    a.q = q;
+    a.n_q = n_q;
+    a.hpk = hpk;
+    a.qscale = scale * kLog2e;
+    a.chunk = chunk;
+    a.nc_max = w.nc_max;
+    a.n_grp = std::max(1, l->n_live);
+    a.pm = reinterpret_cast<float *>(ws + w.pm);
+    a.pl = reinterpret_cast<float *>(ws + w.pl);
+    a.pacc = reinterpret_cast<float *>(ws + w.pacc);
+    a.scores = nullptr;
+    a.err = l->d_err;
+    a.window = window;
+    a.softcap2 = softcap * kLog2e;
+    a.K = K;
+    a.hg = hg;
+    LayerSrc s;
+    s.kf = static_cast<const float *>(l->buf[KVD_BUF_K]);
+    s.vf = static_cast<const float *>(l->buf[KVD_BUF_V]);
+    s.kq = static_cast<const int8_t *>(l->buf[KVD_BUF_KQ]);
+    s.vq = static_cast<const int8_t *>(l->buf[KVD_BUF_VQ]);
+    s.ks = static_cast<const float *>(l->buf[KVD_BUF_KS]);
+    s.vs = static_cast<const float *>(l->buf[KVD_BUF_VS]);
+    s.kcol = static_cast<const float *>(l->buf[KVD_BUF_KCOL]);
+    s.row_base = l->d_row_base;
+    s.cap = l->d_cap;
+    s.seq_len = l->d_seq_len;
+    s.live = l->d_live;
+    s.n_live = l->n_live;
+    if (max_len > 0 && l->n_live > 0) {
+        dim3 grid(unsigned(ceil_div(max_len, chunk)), unsigned(l->n_live), unsigned(l->n_seq));
+        const int hb = hpk_bucket(hpk);
+        cudaError_t e;
+        switch (l->mode) {
+            case KVD_F32: e = split_layer_f32(l->hd, hb, a, s, grid, st); break;
+            case KVD_Q8: e = split_layer_q8(l->hd, hb, a, s, grid, st); break;
+            case KVD_Q8K: e = split_layer_q8k(l->hd, hb, a, s, grid, st); break;
+            default: e = split_layer_q8v(l->hd, hb, a, s, grid, st); break;
+        }
+        if (e != cudaSuccess) return KVD_ECUDA;
+    }
+    MergeArgs m;
+    m.pm = a.pm;
+    m.pl = a.pl;
+    m.pacc = a.pacc;
+    m.out = out;
+    m.ml = nullptr;
+    m.n_q = n_q;
+    m.hpk = hpk;
+    m.n_grp = a.n_grp;
+    m.nc_max = w.nc_max;
+    m.chunk = chunk;
+    m.sinks = sinks;
+    m.window = window;
+    MergeLayerSrc ms;
+    ms.seq_len = l->d_seq_len;
+    ms.slot = l->d_slot;
+    ms.vcol = static_cast<const float *>(l->buf[KVD_BUF_VCOL]);
+    ms.n_live = l->n_live;
+    dim3 mgrid(unsigned(n_q), unsigned(l->n_seq), unsigned(K));
+    if (l->hd == 128) merge_verify_kernel<128><<<mgrid, 128, 0, st>>>(m, ms, K, hg);
+    else merge_verify_kernel<64><<<mgrid, 64, 0, st>>>(m, ms, K, hg);
+    return cudaGetLastError() == cudaSuccess ? KVD_OK : KVD_ECUDA;
+}
+
 // ------------------------------------------------------------------ R-SWA
 
 // The eight mirror pointers are present and 16-byte aligned.

@@ -93,13 +93,25 @@ struct SplitArgs {
     uint32_t *err;
     int64_t window = 0;      // sliding window in rows (0 = none)
     float softcap2 = 0.0f;   // softcap * log2(e) (0 = none)
+    // Query-batched verify of K draft rows (K = 1: a plain decode): the group's
+    // hpk = K * hg query rows are e = k * hg + h (draft k, head h of the hg
+    // heads per KV group), query k sees rows [first_k, upto_k) with upto_k =
+    // L - (K - 1 - k) and first_k the window's start counted back from upto_k.
+    int32_t K = 1;
+    int32_t hg = 0;
 };
+
+// Rows the earliest query of a verify sees at most: L - (K - 1), at least 0.
+__host__ __device__ __forceinline__ int64_t verify_len(int64_t L, int32_t K) {
+    return L - (K - 1) > 0 ? L - (K - 1) : 0;
+}
 
 // Where one CTA's chunk lives.
 struct ChunkInfo {
     const char *k, *v, *ks, *vs;  // global address of the chunk's first row
     int n;                        // rows in the chunk (>= 1)
     int lo;                       // rows of the chunk before the first visible one
+    int L, r0;                    // the sequence's rows and the chunk's first row (verify)
     int64_t pidx0;                // partial index of the group's head 0
     const float *q;               // query of the group's head 0
     const float *kcol;            // K field of the group, or null
@@ -253,11 +265,13 @@ __device__ void split_body(const ChunkInfo &ci, const SplitArgs &a, char *smem) 
     }
 #pragma unroll
     for (int h = 0; h < HPK; ++h) {
+        // query row h: draft h / hg, head h % hg (h itself for a plain decode)
+        const int64_t qo = a.K > 1 ? int64_t(h / a.hg) * a.n_q * HD + int64_t(h % a.hg) * HD : int64_t(h) * HD;
 #pragma unroll
         for (int j = 0; j < CPL; ++j) {
             float x = 0.0f;
             if (!KI8 && h < a.hpk) {
-                x = ci.q[h * HD + lane * CPL + j];
+                x = ci.q[qo + lane * CPL + j];
                 if (KQ) x *= ci.kcol[lane * CPL + j];
                 x *= a.qscale;
             }
@@ -319,7 +333,13 @@ __device__ void split_body(const ChunkInfo &ci, const SplitArgs &a, char *smem) 
                 const int e = lane >> (5 - C::LOGE);
                 const int r = rbase + e / HPK, h = e % HPK;
                 if (KI8) s = s * reinterpret_cast<const float *>(kseg + C::KS_OFF)[r] * qfac;
-                const bool vis = r < nt && (!OPT || row0 + r >= ci.lo);
+                bool vis = r < nt && (!OPT || row0 + r >= ci.lo);
+                if (OPT && a.K > 1 && vis) {
+                    // verify: this query row's own causal limit and window
+                    const int64_t upto = int64_t(ci.L) - (a.K - 1 - h / a.hg);
+                    const int64_t row = int64_t(ci.r0) + row0 + r;
+                    vis = row < upto && row >= first_visible(upto, a.window);
+                }
                 const float sv =
                     vis ? (OPT && a.softcap2 > 0.0f ? softcap_log2(s, a.softcap2) : s) : -INFINITY;
                 sc[r * HPK + h] = sv;
@@ -355,7 +375,8 @@ __device__ void split_body(const ChunkInfo &ci, const SplitArgs &a, char *smem) 
             lsum *= alpha[h];
             const float *vsr = reinterpret_cast<const float *>(kseg + C::VS_OFF);
             for (int r = tid / HPK; r < nt; r += kThreads / HPK) {
-                const float e = exp2f(sc[r * HPK + h] - mn);
+                // a head that has seen no visible row yet (verify) keeps weight 0
+                const float e = mn == -INFINITY ? 0.0f : exp2f(sc[r * HPK + h] - mn);
                 lsum += e;
                 sc[r * HPK + h] = VQ ? e * vsr[r] : e;
             }
@@ -466,9 +487,10 @@ __global__ void __launch_bounds__(kThreads, 2) split_layer_kernel(SplitArgs a, L
     extern __shared__ __align__(128) char smem[];
     const int b = blockIdx.z, gl = blockIdx.y, c = blockIdx.x;
     const int L = src.seq_len[b];
-    // chunks start at the first visible row rounded down to kRowAlign (the
-    // bulk copies' alignment); the rows before it are masked in chunk 0
-    const int64_t first = first_visible(L, a.window);
+    // chunks start at the first visible row (of the earliest query, for a
+    // verify) rounded down to kRowAlign (the bulk copies' alignment); the rows
+    // before it are masked in chunk 0
+    const int64_t first = first_visible(verify_len(L, a.K), a.window);
     const int64_t f0 = first / kRowAlign * kRowAlign;
     const int64_t r0 = f0 + int64_t(c) * a.chunk;
     if (r0 >= L) return;
@@ -480,6 +502,8 @@ __global__ void __launch_bounds__(kThreads, 2) split_layer_kernel(SplitArgs a, L
     const int64_t row = src.row_base[b] + int64_t(gl) * cap + r0;
     ChunkInfo ci;
     ci.lo = int(first - r0 > 0 ? first - r0 : 0);
+    ci.L = L;
+    ci.r0 = int(r0);
     ci.k = KQ ? reinterpret_cast<const char *>(src.kq + row * HD)
               : reinterpret_cast<const char *>(src.kf + row * HD);
     ci.v = VQ ? reinterpret_cast<const char *>(src.vq + row * HD)
@@ -489,7 +513,8 @@ __global__ void __launch_bounds__(kThreads, 2) split_layer_kernel(SplitArgs a, L
     ci.n = int(a.chunk < L - r0 ? int64_t(a.chunk) : L - r0);
     ci.pidx0 = ((int64_t(b) * a.n_grp + gl) * a.nc_max + c) * a.hpk;
     const int g = src.live[gl];
-    ci.q = a.q + (int64_t(b) * a.n_q + int64_t(g) * a.hpk) * HD;
+    const int hg = a.K > 1 ? a.hg : a.hpk;  // query heads per KV group
+    ci.q = a.q + (int64_t(b) * a.K * a.n_q + int64_t(g) * hg) * HD;
     ci.kcol = KQ ? src.kcol + (int64_t(b) * src.n_live + gl) * HD : nullptr;
     // scores region of (b, gl): [hpk][cap] starting at its first storage row * hpk
     ci.score0 = (src.row_base[b] + int64_t(gl) * cap) * a.hpk + r0;
@@ -578,24 +603,28 @@ struct MergeArgs {
 
 // Log-sum-exp merge of the chunk partials of one (sequence, query head):
 // out[d] = field[d] * sum_c acc_c[d] 2^(m_c - M) / sum_c l_c 2^(m_c - M).
+// orow: output row (sequence-major); hh: the query row within its group's
+// partials; h: the query head (for its sink).  A query that saw no row at all
+// (a verify query whose limit precedes every row) outputs zeros.
 template <int HD>
-__device__ void merge_body(const MergeArgs &a, int b, int h, int grp, int nc, const float *vcol) {
+__device__ void merge_body(const MergeArgs &a, int b, int64_t orow, int hh, int h, int grp, int nc,
+                           const float *vcol) {
     const int d = threadIdx.x;
-    float *o = a.out + (int64_t(b) * a.n_q + h) * HD;
-    if (grp < 0 || nc == 0) {
+    float *o = a.out + orow * HD;
+    const int64_t p0 = (int64_t(b) * a.n_grp + grp) * a.nc_max * a.hpk + hh;
+    float Mr = -INFINITY;
+    for (int c = 0; grp >= 0 && c < nc; ++c) Mr = fmaxf(Mr, a.pm[p0 + int64_t(c) * a.hpk]);
+    if (grp < 0 || nc == 0 || Mr == -INFINITY) {
         o[d] = 0.0f;
         if (a.ml && d == 0) {
-            a.ml[(int64_t(b) * a.n_q + h) * 2] = -INFINITY;
-            a.ml[(int64_t(b) * a.n_q + h) * 2 + 1] = 0.0f;
+            a.ml[orow * 2] = -INFINITY;
+            a.ml[orow * 2 + 1] = 0.0f;
         }
         return;
     }
-    const int hh = h % a.hpk;
-    const int64_t p0 = (int64_t(b) * a.n_grp + grp) * a.nc_max * a.hpk + hh;
     // a learned sink joins the maximum and the sum; it has no value row
     const float z = a.sinks ? a.sinks[h] * kLog2e : -INFINITY;
-    float M = z;
-    for (int c = 0; c < nc; ++c) M = fmaxf(M, a.pm[p0 + int64_t(c) * a.hpk]);
+    const float M = fmaxf(Mr, z);
     float Ls = a.sinks ? exp2f(z - M) : 0.0f, s = 0.0f;
     for (int c = 0; c < nc; ++c) {
         const int64_t p = p0 + int64_t(c) * a.hpk;
@@ -607,8 +636,8 @@ __device__ void merge_body(const MergeArgs &a, int b, int h, int grp, int nc, co
     if (vcol) r *= vcol[d];
     o[d] = r;
     if (a.ml && d == 0) {
-        a.ml[(int64_t(b) * a.n_q + h) * 2] = M;
-        a.ml[(int64_t(b) * a.n_q + h) * 2 + 1] = Ls;
+        a.ml[orow * 2] = M;
+        a.ml[orow * 2 + 1] = Ls;
     }
 }
 
@@ -627,7 +656,20 @@ __global__ void __launch_bounds__(HD) merge_layer_kernel(MergeArgs a, MergeLayer
     const int f0 = int(first_visible(L, a.window) / kRowAlign * kRowAlign);
     const int nc = (L - f0 + a.chunk - 1) / a.chunk;
     const float *vcol = (src.vcol && grp >= 0) ? src.vcol + (int64_t(b) * src.n_live + grp) * HD : nullptr;
-    merge_body<HD>(a, b, h, grp, nc, vcol);
+    merge_body<HD>(a, b, int64_t(b) * a.n_q + h, h % a.hpk, h, grp, nc, vcol);
+}
+
+// Verify merge: grid (n_q, n_seq, K); a.hpk = K * hg partial rows per group,
+// output [n_seq][K][n_q][HD].
+template <int HD>
+__global__ void __launch_bounds__(HD) merge_verify_kernel(MergeArgs a, MergeLayerSrc src, int32_t K, int32_t hg) {
+    const int h = blockIdx.x, b = blockIdx.y, k = blockIdx.z;
+    const int L = src.seq_len[b];
+    const int grp = src.slot[h / hg];
+    const int f0 = int(first_visible(verify_len(L, K), a.window) / kRowAlign * kRowAlign);
+    const int nc = (L - f0 + a.chunk - 1) / a.chunk;
+    const float *vcol = (src.vcol && grp >= 0) ? src.vcol + (int64_t(b) * src.n_live + grp) * HD : nullptr;
+    merge_body<HD>(a, b, (int64_t(b) * K + k) * a.n_q + h, k * hg + h % hg, h, grp, nc, vcol);
 }
 
 template <int HD>
@@ -637,7 +679,7 @@ __global__ void __launch_bounds__(HD) merge_rswa_kernel(MergeArgs a, RswaTable t
     const int s = tb.s0 + si;
     const int nc = (tb.prefill_len[si] + a.chunk - 1) / a.chunk +
                    (tb.ring_len[si] + a.chunk - 1) / a.chunk;
-    merge_body<HD>(a, s, h, h, nc, nullptr);
+    merge_body<HD>(a, s, int64_t(s) * a.n_q + h, 0, h, h, nc, nullptr);
 }
 
 // Host launcher for one instance (instantiated per storage mode in its own unit).
@@ -645,8 +687,8 @@ template <int HD, int HPK, bool KQ, bool VQ>
 cudaError_t launch_split_layer_impl(const SplitArgs &a, const LayerSrc &s, dim3 grid,
                                     cudaStream_t st) {
     using C = SplitCfg<HD, HPK, KQ, VQ>;
-    auto kern = (a.window > 0 || a.softcap2 > 0.0f) ? split_layer_kernel<HD, HPK, KQ, VQ, true>
-                                                     : split_layer_kernel<HD, HPK, KQ, VQ, false>;
+    auto kern = (a.window > 0 || a.softcap2 > 0.0f || a.K > 1) ? split_layer_kernel<HD, HPK, KQ, VQ, true>
+                                                                : split_layer_kernel<HD, HPK, KQ, VQ, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, C::SMEM, st>>>(a, s);

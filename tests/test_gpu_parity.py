@@ -670,3 +670,76 @@ def test_rswa_rollback_erases_speculative_steps(torch, kvd, int8):
             kvd.rswa_ring_write(c, torch.from_numpy(steps[t][0]).cuda(), torch.from_numpy(steps[t][1]).cuda())
     assert np.array_equal(dec(q, spec).cpu().numpy(), dec(q, plain).cpu().numpy())
     assert spec.device_error() == 0
+
+
+@pytest.mark.parametrize("mode", list(MODES))
+@pytest.mark.parametrize("hd,hg,K", [(128, 4, 4), (64, 2, 3), (128, 16, 1), (128, 1, 8)])
+def test_verify_parity(torch, kvd, mode, hd, hg, K):
+    """Query-batched verify of K drafts (appended by kv_append, then verified in
+    one call; causal among them) against the oracle, plain and with window +
+    softcap + sinks, over sequences shorter than K, around a tile edge and long
+    enough for several chunks; a dead group gives zeros.  Rejecting the last
+    drafts with kv_truncate_last then leaves a cache that decodes like the
+    oracle's."""
+    n_kv = 3
+    n_q = hg * n_kv
+    lengths = [2, 40, 1200, 3000]
+    alive = [1, 0, 1]
+    ks, vs = seq_rows([L - K if L >= K else 0 for L in lengths], n_kv, hd, seed=91)
+    layer = _layer(kvd, MODES[mode], lengths, n_kv, hd, alive, cap_extra=8)
+    pre = [k.shape[0] for k in ks]
+    if max(pre) > 0:
+        gpu_append_bulk(layer, ks, vs, torch)
+    ocs = oracle_caches(MODES[mode], pre, n_kv, hd, alive, ks, vs, cap=max(lengths) + 8)
+    for oc in ocs:
+        oc.freeze_if_due()
+    dk, dv = seq_rows([L - p for L, p in zip(lengths, pre)], n_kv, hd, seed=92)
+    nn = np.array([d.shape[0] for d in dk], np.int32)
+    kvd.kv_append(layer, torch.from_numpy(np.concatenate(dk)).cuda(), torch.from_numpy(np.concatenate(dv)).cuda(), nn)
+    for b, oc in enumerate(ocs):
+        for i in range(nn[b]):  # the oracle appends one row at a time
+            oc.append(dk[b][i], dv[b][i])
+            oc.freeze_if_due()
+    assert_storage_bitexact(layer, ocs, torch)
+    q = synthetic.normal((len(lengths), K, n_q, hd), 93)
+    sinks = synthetic.normal((n_q,), 94)
+    scale = np.float32(1.0 / math.sqrt(hd))
+    live = np.repeat(np.array(alive, bool), hg)
+    for opts in ({}, {"window": 700, "softcap": 3.0, "sinks": sinks}):
+        kw = dict(opts)
+        if "sinks" in kw:
+            kw["sinks"] = torch.from_numpy(kw["sinks"]).cuda()
+        out = kvd.decode_attention_verify(torch.from_numpy(q).cuda(), layer, K, scale=float(scale), **kw)
+        out = out.cpu().numpy()
+        for b, oc in enumerate(ocs):
+            ref = oc.decode_verify(q[b], n_q, K, scale, opts.get("window", 0), opts.get("softcap", 0.0),
+                                   opts.get("sinks"))
+            for k in range(K):
+                if not np.any(ref[k][live]):  # no visible row: zeros
+                    assert not out[b, k].any(), (b, k)
+                    continue
+                assert out_error(out[b, k], ref[k], live) <= OUT_TOL, (opts.keys(), b, k)
+            assert not out[b][:, ~live].any()
+    assert layer.device_error() == 0
+    # reject the last two drafts everywhere
+    drop = min(2, K)
+    kvd.kv_truncate_last(layer, drop)
+    for oc in ocs:
+        oc.truncate_last(drop)
+    q1 = synthetic.normal((len(lengths), n_q, hd), 95)
+    out = kvd.decode_attention(torch.from_numpy(q1).cuda(), layer, scale=float(scale)).cpu().numpy()
+    for b, oc in enumerate(ocs):
+        if oc.seq_len:
+            assert out_error(out[b], oc.decode(q1[b], n_q, scale), live) <= OUT_TOL, b
+
+
+def test_verify_errors(torch, kvd):
+    layer = _layer(kvd, MODES["q8"], [100], 2, 128, None)
+    q = torch.zeros(1, 4, 8, 128, device="cuda")  # hg 4 x K 4 = 16 query rows per group
+    kvd.decode_attention_verify(q, layer, 4)
+    with pytest.raises(kvd.KvdError) as e:  # 4 heads per group x 5 drafts > 16
+        kvd.decode_attention_verify(torch.zeros(1, 5, 8, 128, device="cuda"), layer, 5)
+    assert e.value.status == -1
+    with pytest.raises(kvd.KvdError) as e:
+        kvd.decode_attention_verify(q, layer, 4, window=-1)
+    assert e.value.status == -1
