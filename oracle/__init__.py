@@ -25,6 +25,7 @@ from .oracle import (  # noqa: F401
     rswa_decode,
     rswa_decode_i8,
     rswa_mirror,
+    rswa_verify,
     rswa_write,
     online_head,
 )

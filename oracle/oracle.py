@@ -358,6 +358,31 @@ def rswa_decode_i8(q, ref_k8, ref_ks, ref_v8, ref_vs, prefill_len, ring_k8, ring
     return out
 
 
+def rswa_verify(q, draft_k, draft_v, ref_k, ref_v, prefill_len, ring_k, ring_v, cursors, scale,
+                int8: bool = False):
+    """rswa verify_attention for one stream: K draft tokens (q, draft_k, draft_v
+    [K, H, hd]) against a PRIVATE copy of the ring: draft i is written
+    (write_decode_step) before query i decodes (decode_attention, or
+    decode_attention_int8 over the mirror of the copy when int8), so query i
+    sees the reference rows and the ring after drafts 0..i.  The caller's
+    arrays and cursors are left untouched.  Returns [K, H, hd] f64."""
+    K = q.shape[0]
+    gk, gv, cur = ring_k.copy(), ring_v.copy(), np.array(cursors, np.int32).copy()
+    out = []
+    if int8:
+        rk8, rks = rswa_mirror(ref_k)
+        rv8, rvs = rswa_mirror(ref_v)
+    for i in range(K):
+        rswa_write(gk, gv, draft_k[i], draft_v[i], prefill_len is not None, cur)
+        if int8:
+            gk8, gks = rswa_mirror(gk)
+            gv8, gvs = rswa_mirror(gv)
+            out.append(rswa_decode_i8(q[i], rk8, rks, rv8, rvs, prefill_len, gk8, gks, gv8, gvs, cur[0], scale))
+        else:
+            out.append(rswa_decode(q[i], ref_k, ref_v, prefill_len, gk, gv, cur[0], scale))
+    return np.stack(out)
+
+
 def online_head(q, keys, vals, scale):
     """rswa fold recurrence (f32) for one head over keys/vals [n, hd]."""
     q = np.ascontiguousarray(q, dtype=np.float32)

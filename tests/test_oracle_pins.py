@@ -970,3 +970,56 @@ def test_verify_equals_sequential_decodes():
     assert np.allclose(bat, np.stack(seq), rtol=1e-13, atol=1e-15)
     # K = 1 is the plain decode
     assert np.array_equal(c_bat.decode_verify(q[3:], n_q, 1, sc)[0], c_bat.decode(q[3], n_q, sc))
+
+
+def test_rswa_verify_is_brute_force_over_the_last_w_rows():
+    """[rswa] verify_attention: query i sees the reference rows and the last W
+    rows of (live ring in logical order ++ drafts 0..i), in a warm ring (no
+    overwrite), a ring that fills during the drafts, and a full ring (each
+    draft evicts the oldest row); the caller's ring and cursors stay untouched.
+    Brute force: scipy softmax over the explicit key list."""
+    from scipy.special import softmax
+
+    m, K = 11, 5
+    scale = f32(1.0) / f32(math.sqrt(HD))
+    for n_gen in (40, 125, 300):
+        rk, rv, gk, gv, cur = _rswa_state(16)
+        rk[:, :m] = synthetic.normal((H, m, HD), 110)
+        rv[:, :m] = synthetic.normal((H, m, HD), 111)
+        gen_k = synthetic.normal((n_gen, H, HD), 112)
+        gen_v = synthetic.normal((n_gen, H, HD), 113)
+        for t in range(n_gen):
+            oracle.rswa_write(gk, gv, gen_k[t], gen_v[t], True, cur)
+        dq = synthetic.normal((K, H, HD), 114)
+        dk = synthetic.normal((K, H, HD), 115)
+        dv = synthetic.normal((K, H, HD), 116)
+        snap = (gk.copy(), gv.copy(), cur.copy())
+        got = oracle.rswa_verify(dq, dk, dv, rk, rv, m, gk, gv, cur, scale)
+        assert np.array_equal(gk, snap[0]) and np.array_equal(gv, snap[1]) and np.array_equal(cur, snap[2])
+        for i in range(K):
+            keys_k = np.concatenate([gen_k, dk[:i + 1]])[-W:]
+            keys_v = np.concatenate([gen_v, dv[:i + 1]])[-W:]
+            for h in range(H):
+                Kh = np.concatenate([rk[h, :m], keys_k[:, h]]).astype(np.float64)
+                Vh = np.concatenate([rv[h, :m], keys_v[:, h]]).astype(np.float64)
+                w = softmax(np.float64(scale) * (Kh @ dq[i, h].astype(np.float64)))
+                assert np.allclose(got[i, h], w @ Vh, rtol=1e-11, atol=1e-13), (n_gen, i, h)
+
+
+def test_rswa_verify_int8_on_lossless_rows_equals_f32():
+    """The int8 verify (drafts mirrored as write_decode_step mirrors them) equals
+    the f32 verify on rows that quantise losslessly (absmax 127, small integers)."""
+    rng = np.random.default_rng(12)
+
+    def rows(shape):
+        x = rng.integers(-3, 4, size=shape).astype(f32)
+        x[..., 0] = 127.0
+        return x
+
+    rk, rv, gk, gv, cur = _rswa_state(16)
+    rk[:, :6], rv[:, :6] = rows((H, 6, HD)), rows((H, 6, HD))
+    for _ in range(126):
+        oracle.rswa_write(gk, gv, rows((H, HD)), rows((H, HD)), True, cur)
+    dq, dk, dv = rows((4, H, HD)), rows((4, H, HD)), rows((4, H, HD))
+    args = (dq, dk, dv, rk, rv, 6, gk, gv, cur, f32(1e-3))
+    assert np.allclose(oracle.rswa_verify(*args, int8=True), oracle.rswa_verify(*args), rtol=1e-12, atol=1e-12)
