@@ -393,6 +393,35 @@ KVD_API kvd_status rswa_decode_i8(const float *q, const rswa_i8_mirror *m,
                                   int64_t ref_cap, int32_t W, float scale, float *out,
                                   void *workspace, int64_t workspace_bytes, void *stream);
 
+/* Workspace bytes rswa_verify / rswa_verify_i8 need for K drafts. */
+KVD_API kvd_status rswa_verify_workspace_bytes(int32_t B, int32_t H, int32_t head_dim, int64_t ref_cap,
+                                               int32_t W, int32_t K, int64_t *bytes_out);
+
+/* rswa verify_attention for every stream, query-batched: K draft tokens
+ * (q, draft_k, draft_v device f32 [B][K][H][head_dim], already rotated) are
+ * attended as K sequential write_decode_step + decode_attention calls would
+ * -- query i sees the reference rows and the last W rows of (the live ring
+ * in logical order, then drafts 0..i): drafts that a full ring makes evict
+ * its oldest rows -- WITHOUT writing the cache (it is read-only here; the
+ * caller then writes the accepted drafts with rswa_ring_write).  The
+ * reference rows are read once for all K queries of a head.  out device f32
+ * [B][K][H * head_dim].  1 <= K <= 16; errors as rswa_decode (KVD_ESTATE for
+ * a stream without prefill). */
+KVD_API kvd_status rswa_verify(const float *q, const float *draft_k, const float *draft_v, int32_t K,
+                               const float *ref_k, const float *ref_v, const float *ring_k,
+                               const float *ring_v, const int32_t *prefill_len, const int32_t *ring_len,
+                               const int32_t *ring_pos, int32_t B, int32_t H, int32_t head_dim,
+                               int64_t ref_cap, int32_t W, float scale, float *out, void *workspace,
+                               int64_t workspace_bytes, void *stream);
+
+/* rswa_verify over the int8 mirror (decode_attention_int8): the drafts are
+ * quantised per row as write_decode_step would mirror them. */
+KVD_API kvd_status rswa_verify_i8(const float *q, const float *draft_k, const float *draft_v, int32_t K,
+                                  const rswa_i8_mirror *m, const int32_t *prefill_len,
+                                  const int32_t *ring_len, const int32_t *ring_pos, int32_t B, int32_t H,
+                                  int32_t head_dim, int64_t ref_cap, int32_t W, float scale, float *out,
+                                  void *workspace, int64_t workspace_bytes, void *stream);
+
 /* Device error word kept in an R-SWA workspace (see kvd_layer_device_error). */
 KVD_API kvd_status rswa_device_error(const void *workspace, int32_t clear, uint32_t *word_out);
 

@@ -22,4 +22,5 @@ from .api import (  # noqa: F401
     rswa_decode_i8,
     rswa_record_prefill,
     rswa_ring_write,
+    rswa_verify,
 )

@@ -82,6 +82,11 @@ _SIGS = {
                            _i32, _vp, _vp],
     "rswa_decode_i8": [_vp, _P(rswa_i8_mirror), _vp, _vp, _vp, _i32, _i32, _i32, _i64, _i32, _f32, _vp,
                        _vp, _i64, _vp],
+    "rswa_verify_workspace_bytes": [_i32, _i32, _i32, _i64, _i32, _i32, _P(_i64)],
+    "rswa_verify": [_vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, _i32,
+                    _f32, _vp, _vp, _i64, _vp],
+    "rswa_verify_i8": [_vp, _vp, _vp, _i32, _P(rswa_i8_mirror), _vp, _vp, _vp, _i32, _i32, _i32, _i64, _i32,
+                       _f32, _vp, _vp, _i64, _vp],
     "rswa_device_error": [_vp, _i32, _P(C.c_uint32)],
     "kvd_status_string": [_i32],
 }

@@ -426,6 +426,40 @@ def rswa_decode_i8(q: torch.Tensor, cache: RingCache, out: torch.Tensor | None =
     return out
 
 
+def rswa_verify(q: torch.Tensor, draft_k: torch.Tensor, draft_v: torch.Tensor, cache: RingCache,
+                int8: bool = False, out: torch.Tensor | None = None, scale: float | None = None,
+                stream=None) -> torch.Tensor:
+    """rswa verify_attention: K draft tokens q, draft_k, draft_v [B, K, H, hd] ->
+    out [B, K, H * hd], query i as after writing drafts 0..i -- the cache is not
+    written.  int8=True reads the int8 mirror (decode_attention_int8)."""
+    for t, name in ((q, "q"), (draft_k, "draft_k"), (draft_v, "draft_v")):
+        _f32_cuda(t, name)
+    K = q.numel() // (cache.B * cache.H * cache.head_dim)
+    if K * cache.B * cache.H * cache.head_dim != q.numel() or draft_k.numel() != q.numel() or \
+            draft_v.numel() != q.numel():
+        raise ValueError("q, draft_k, draft_v must be [B, K, H, head_dim]")
+    if int8 and cache.mirror is None:
+        raise ValueError("int8 verify needs a RingCache built with int8=True")
+    if out is None:
+        out = torch.empty(cache.B, K, cache.H * cache.head_dim, device=q.device)
+    _f32_cuda(out, "out")
+    if scale is None:
+        scale = 1.0 / math.sqrt(cache.head_dim)
+    n = C.c_int64(0)
+    _abi.call("rswa_verify_workspace_bytes", cache.B, cache.H, cache.head_dim, cache.ref_cap, cache.W, int(K),
+              C.byref(n))
+    ws = torch.empty(int(n.value), dtype=torch.uint8, device=q.device)
+    tail = (_np_ptr(cache.prefill_len), _np_ptr(cache.ring_len), _np_ptr(cache.ring_pos), cache.B, cache.H,
+            cache.head_dim, cache.ref_cap, cache.W, C.c_float(scale), _ptr(out), _ptr(ws), int(ws.numel()),
+            _stream(stream))
+    if int8:
+        _abi.call("rswa_verify_i8", _ptr(q), _ptr(draft_k), _ptr(draft_v), int(K), C.byref(cache.mirror), *tail)
+    else:
+        _abi.call("rswa_verify", _ptr(q), _ptr(draft_k), _ptr(draft_v), int(K), _ptr(cache.ref_k),
+                  _ptr(cache.ref_v), _ptr(cache.ring_k), _ptr(cache.ring_v), *tail)
+    return out
+
+
 def rswa_attention(cache: RingCache, q, k, v, stream=None) -> torch.Tensor:
     """rswa attention(): write this step's K/V into every ring, then attend (the
     query sees itself as the newest ring row)."""

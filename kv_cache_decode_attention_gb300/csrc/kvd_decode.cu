@@ -103,10 +103,12 @@ struct RswaWs {
     int32_t nc_max;
 };
 
-RswaWs rswa_ws(int32_t B, int32_t H, int32_t hd, int64_t ref_cap, int32_t W) {
+// K > 1: a verify of K drafts (K partial rows per chunk; the ring's chunk
+// slots hold the one tail partial).
+RswaWs rswa_ws(int32_t B, int32_t H, int32_t hd, int64_t ref_cap, int32_t W, int32_t K = 1) {
     RswaWs w;
     w.nc_max = int32_t(ceil_div(ref_cap, kMinChunk) + ceil_div(W, kMinChunk));
-    const int64_t P = int64_t(B) * H * w.nc_max;
+    const int64_t P = int64_t(B) * H * w.nc_max * K;
     int64_t o = 0;
     auto take = [&](int64_t bytes) {
         const int64_t at = o;
@@ -419,15 +421,189 @@ __global__ void ring_write_i8_kernel(float *ring_k, float *ring_v, rswa_i8_mirro
     }
 }
 
-template <int HD, bool I8>
+template <int HD, bool I8, int HPK = 1>
 cudaError_t launch_split_rswa(const SplitArgs &a, const RswaSrc &s, const RswaTable &t, dim3 grid,
                               cudaStream_t st) {
-    using C = SplitCfg<HD, 1, I8, I8, I8>;
-    auto kern = split_rswa_kernel<HD, I8>;
+    using C = SplitCfg<HD, HPK, I8, I8, I8>;
+    auto kern = split_rswa_kernel<HD, I8, HPK>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, C::SMEM, st>>>(a, s, t);
     return cudaGetLastError();
+}
+
+template <int HD, bool I8>
+cudaError_t launch_split_rswa_k(int hb, const SplitArgs &a, const RswaSrc &s, const RswaTable &t, dim3 grid,
+                                cudaStream_t st) {
+    switch (hb) {
+        case 1: return launch_split_rswa<HD, I8, 1>(a, s, t, grid, st);
+        case 2: return launch_split_rswa<HD, I8, 2>(a, s, t, grid, st);
+        case 4: return launch_split_rswa<HD, I8, 4>(a, s, t, grid, st);
+        case 8: return launch_split_rswa<HD, I8, 8>(a, s, t, grid, st);
+        case 16: return launch_split_rswa<HD, I8, 16>(a, s, t, grid, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+// rswa verify_attention, the ring-and-drafts part: query i of a head sees the
+// live ring rows and drafts 0..i that survive in the last W written rows --
+// the ring in logical order (oldest at slot rp0) followed by the drafts; the
+// reference rows are the split kernel's.  One CTA per (query, head, stream),
+// four warps over the candidate rows, each warp an online softmax with the
+// score of a row complete in every lane, then combined; the result is written
+// as one more chunk partial (slot nc_ref) for the merge.
+struct TailTable {
+    int32_t s0, n;
+    int32_t ring_len[kSlice];
+    int32_t rp0[kSlice];     // slot of the oldest live ring row
+    int32_t nc_ref[kSlice];  // chunk partials of the reference rows
+};
+
+struct TailArgs {
+    const float *q, *dk, *dv;         // [B][K][H][HD]
+    const float *ring_k, *ring_v;     // f32 ring (I8 false)
+    const int8_t *ring_k8, *ring_v8;  // mirror codes (I8)
+    const float *ring_ks, *ring_vs;   // mirror scales (I8)
+    float *pm, *pl, *pacc;
+    int32_t K, H, W, nc_max;
+    float qscale;  // softmax scale * log2(e)
+};
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    return x;
+}
+
+// quantize_row_i8 of a row held CPL values per lane: codes packed per lane, scale returned
+template <int CPL>
+__device__ __forceinline__ uint32_t quant_lane_i8(const float (&x)[CPL], float &scale) {
+    float mx = 0.0f;
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) mx = fmaxf(mx, fabsf(x[j]));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    scale = mx > 0.0f ? __fdiv_rn(mx, 127.0f) : 1.0f;
+    uint32_t w = 0;
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) w |= (uint32_t(quant_code_i8(x[j], scale)) & 0xffu) << (8 * j);
+    return w;
+}
+
+template <int CPL>
+__device__ __forceinline__ void load_f32_lane(const float *row, int lane, float (&x)[CPL]) {
+    if (CPL == 4) {
+        const float4 f = reinterpret_cast<const float4 *>(row)[lane];
+        x[0] = f.x, x[1] = f.y, x[2] = f.z, x[3] = f.w;
+    } else {
+        const float2 f = reinterpret_cast<const float2 *>(row)[lane];
+        x[0] = f.x, x[1] = f.y;
+    }
+}
+
+template <int HD, bool I8>
+__global__ void __launch_bounds__(128) rswa_verify_tail_kernel(TailArgs a, TailTable t) {
+    constexpr int CPL = HD / 32;
+    __shared__ float sm_m[4], sm_l[4];
+    __shared__ float sm_acc[4][HD];
+    const int i = blockIdx.x, h = blockIdx.y, si = blockIdx.z;
+    if (si >= t.n) return;
+    const int s = t.s0 + si;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int rl = t.ring_len[si], rp0 = t.rp0[si];
+    const int drop = max(0, rl + i + 1 - a.W);  // oldest rows pushed out by drafts 0..i
+    float qv[CPL];
+    load_f32_lane<CPL>(a.q + ((int64_t(s) * a.K + i) * a.H + h) * HD, lane, qv);
+    uint32_t qi = 0;
+    float qfac = 0.0f;
+    if (I8) {
+        float sq;
+        qi = quant_lane_i8<CPL>(qv, sq);
+        qfac = sq * a.qscale;
+    } else {
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) qv[j] *= a.qscale;
+    }
+    float m = -INFINITY, l = 0.0f, acc[CPL];
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) acc[j] = 0.0f;
+    const int64_t ring0 = (int64_t(s) * a.H + h) * a.W;  // row of slot 0 of this head's ring
+    for (int r = warp; r < rl + i + 1; r += 4) {
+        const bool ring = r < rl;
+        const int j = r - rl;  // draft index
+        const bool vis = ring ? ((r - rp0 + a.W) % a.W) >= drop : rl + j >= drop;
+        if (!vis) continue;  // the same for the whole warp
+        const float *drow_k = a.dk + ((int64_t(s) * a.K + j) * a.H + h) * HD;
+        const float *drow_v = a.dv + ((int64_t(s) * a.K + j) * a.H + h) * HD;
+        float score, w_scale = 1.0f, x[CPL];
+        if (I8) {
+            uint32_t kw;
+            float ks;
+            if (ring) {
+                const int8_t *kr = a.ring_k8 + (ring0 + r) * HD;
+                kw = CPL == 4 ? reinterpret_cast<const uint32_t *>(kr)[lane]
+                              : uint32_t(reinterpret_cast<const uint16_t *>(kr)[lane]);
+                ks = a.ring_ks[ring0 + r];
+            } else {
+                float kx[CPL];
+                load_f32_lane<CPL>(drow_k, lane, kx);
+                kw = quant_lane_i8<CPL>(kx, ks);
+            }
+            // exact integer dot (every partial sum an integer below 2^24)
+            score = warp_sum(float(__dp4a(int(qi), int(kw), 0))) * ks * qfac;
+            uint32_t vw;
+            if (ring) {
+                const int8_t *vr = a.ring_v8 + (ring0 + r) * HD;
+                vw = CPL == 4 ? reinterpret_cast<const uint32_t *>(vr)[lane]
+                              : uint32_t(reinterpret_cast<const uint16_t *>(vr)[lane]);
+                w_scale = a.ring_vs[ring0 + r];
+            } else {
+                float vx[CPL];
+                load_f32_lane<CPL>(drow_v, lane, vx);
+                vw = quant_lane_i8<CPL>(vx, w_scale);
+            }
+#pragma unroll
+            for (int jj = 0; jj < CPL; ++jj) x[jj] = float(int8_t((vw >> (8 * jj)) & 0xffu));
+        } else {
+            float kx[CPL];
+            load_f32_lane<CPL>(ring ? a.ring_k + (ring0 + r) * HD : drow_k, lane, kx);
+            float p = 0.0f;
+#pragma unroll
+            for (int jj = 0; jj < CPL; ++jj) p = fmaf(qv[jj], kx[jj], p);
+            score = warp_sum(p);
+            load_f32_lane<CPL>(ring ? a.ring_v + (ring0 + r) * HD : drow_v, lane, x);
+        }
+        const float mn = fmaxf(m, score);
+        const float al = m == -INFINITY ? 0.0f : exp2f(m - mn);
+        const float e = exp2f(score - mn);
+        l = l * al + e;
+        const float w = e * w_scale;
+#pragma unroll
+        for (int jj = 0; jj < CPL; ++jj) acc[jj] = fmaf(acc[jj], al, w * x[jj]);
+        m = mn;
+    }
+    if (lane == 0) {
+        sm_m[warp] = m;
+        sm_l[warp] = l;
+    }
+#pragma unroll
+    for (int jj = 0; jj < CPL; ++jj) sm_acc[warp][lane * CPL + jj] = acc[jj];
+    __syncthreads();
+    float M = fmaxf(fmaxf(sm_m[0], sm_m[1]), fmaxf(sm_m[2], sm_m[3]));
+    const int64_t p = ((int64_t(s) * a.H + h) * a.nc_max + t.nc_ref[si]) * a.K + i;
+    for (int d = threadIdx.x; d < HD; d += blockDim.x) {
+        float L = 0.0f, A = 0.0f;
+        for (int w2 = 0; w2 < 4; ++w2) {
+            const float f = sm_m[w2] == -INFINITY ? 0.0f : exp2f(sm_m[w2] - M);
+            L += sm_l[w2] * f;
+            A += sm_acc[w2][d] * f;
+        }
+        a.pacc[p * HD + d] = A;
+        if (d == 0) {
+            a.pm[p] = M;
+            a.pl[p] = L;
+        }
+    }
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
@@ -1028,6 +1204,163 @@ extern "C" kvd_status rswa_decode_i8(const float *q, const rswa_i8_mirror *m,
     src.ring_vs = m->ring_vs;
     return rswa_decode_impl<true>(q, src, prefill_len, ring_len, ring_pos, B, H, head_dim, ref_cap, W,
                                   scale, out, workspace, workspace_bytes, stream);
+}
+
+// rswa verify_attention over the f32 regions (I8 false) or the int8 mirror.
+template <bool I8>
+static kvd_status rswa_verify_impl(const float *q, const float *dk, const float *dv, int32_t K,
+                                   const RswaSrc &src_in, const int32_t *prefill_len, const int32_t *ring_len,
+                                   const int32_t *ring_pos, int32_t B, int32_t H, int32_t head_dim,
+                                   int64_t ref_cap, int32_t W, float scale, float *out, void *workspace,
+                                   int64_t workspace_bytes, void *stream) {
+    if (q == nullptr || dk == nullptr || dv == nullptr || prefill_len == nullptr || ring_len == nullptr ||
+        ring_pos == nullptr || out == nullptr)
+        return KVD_EINVAL;
+    if (K < 1 || K > kMaxHpk || B < 1 || H < 1 || (head_dim != 64 && head_dim != 128) || ref_cap < 0 || W < 1)
+        return KVD_EINVAL;
+    if (ref_cap % kRowAlign != 0 || W % kRowAlign != 0) return KVD_EINVAL;
+    if (!std::isfinite(scale)) return KVD_EINVAL;
+    if (!aligned16(q) || !aligned16(out) || !aligned16(dk) || !aligned16(dv)) return KVD_EINVAL;
+    const RswaWs w = rswa_ws(B, H, head_dim, ref_cap, W, K);
+    if (workspace == nullptr || workspace_bytes < w.total || (reinterpret_cast<uintptr_t>(workspace) & 255))
+        return KVD_EINVAL;
+    int64_t work = 0;
+    for (int s = 0; s < B; ++s) {
+        if (prefill_len[s] < 0) return KVD_ESTATE;  // write_decode_step refuses a stream without prefill
+        if (prefill_len[s] > ref_cap || ring_len[s] < 0 || ring_len[s] > W || ring_pos[s] < 0 ||
+            ring_pos[s] >= W)
+            return KVD_EINVAL;
+        work += int64_t(prefill_len[s]) * H;
+    }
+    const int32_t chunk = pick_chunk(std::max<int64_t>(work, 1));
+    char *ws = static_cast<char *>(workspace);
+    cudaStream_t st = as_stream(stream);
+    SplitArgs a;
+    a.q = q;
+    a.n_q = H;
+    a.hpk = K;
+    a.K = K;
+    a.hg = 1;
+    a.qscale = scale * kLog2e;
+    a.chunk = chunk;
+    a.nc_max = w.nc_max;
+    a.n_grp = H;
+    a.pm = reinterpret_cast<float *>(ws + w.pm);
+    a.pl = reinterpret_cast<float *>(ws + w.pl);
+    a.pacc = reinterpret_cast<float *>(ws + w.pacc);
+    a.scores = nullptr;
+    a.err = reinterpret_cast<uint32_t *>(ws + w.err);
+    RswaSrc src = src_in;
+    src.ref_cap = ref_cap;
+    src.W = W;
+    src.H = H;
+    TailArgs ta;
+    ta.q = q;
+    ta.dk = dk;
+    ta.dv = dv;
+    ta.ring_k = src.ring_k;
+    ta.ring_v = src.ring_v;
+    ta.ring_k8 = src.ring_k8;
+    ta.ring_v8 = src.ring_v8;
+    ta.ring_ks = src.ring_ks;
+    ta.ring_vs = src.ring_vs;
+    ta.pm = a.pm;
+    ta.pl = a.pl;
+    ta.pacc = a.pacc;
+    ta.K = K;
+    ta.H = H;
+    ta.W = W;
+    ta.nc_max = w.nc_max;
+    ta.qscale = a.qscale;
+    MergeArgs m;
+    m.pm = a.pm;
+    m.pl = a.pl;
+    m.pacc = a.pacc;
+    m.out = out;
+    m.ml = nullptr;
+    m.n_q = H;
+    m.hpk = K;
+    m.n_grp = H;
+    m.nc_max = w.nc_max;
+    m.chunk = chunk;
+    const int hb = hpk_bucket(K);
+    for (int32_t s0 = 0; s0 < B; s0 += kSlice) {
+        RswaTable t;  // the split kernel reads the reference rows only
+        TailTable tt;
+        t.s0 = tt.s0 = s0;
+        t.n = tt.n = std::min(kSlice, B - s0);
+        int32_t max_nc = 0;
+        for (int i = 0; i < t.n; ++i) {
+            const int s = s0 + i;
+            t.prefill_len[i] = prefill_len[s];
+            t.ring_len[i] = 0;
+            tt.ring_len[i] = ring_len[s];
+            tt.rp0[i] = ring_len[s] == W ? ring_pos[s] : 0;
+            tt.nc_ref[i] = int32_t(ceil_div(prefill_len[s], chunk));
+            max_nc = std::max(max_nc, tt.nc_ref[i]);
+        }
+        if (max_nc > 0) {
+            dim3 grid(unsigned(max_nc), unsigned(H), unsigned(t.n));
+            cudaError_t e = head_dim == 128 ? launch_split_rswa_k<128, I8>(hb, a, src, t, grid, st)
+                                            : launch_split_rswa_k<64, I8>(hb, a, src, t, grid, st);
+            if (e != cudaSuccess) return KVD_ECUDA;
+        }
+        dim3 tgrid(unsigned(K), unsigned(H), unsigned(t.n));
+        if (head_dim == 128) rswa_verify_tail_kernel<128, I8><<<tgrid, 128, 0, st>>>(ta, tt);
+        else rswa_verify_tail_kernel<64, I8><<<tgrid, 128, 0, st>>>(ta, tt);
+        if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
+        dim3 mgrid(unsigned(H), unsigned(t.n), unsigned(K));
+        if (head_dim == 128) merge_rswa_verify_kernel<128><<<mgrid, 128, 0, st>>>(m, t, K);
+        else merge_rswa_verify_kernel<64><<<mgrid, 64, 0, st>>>(m, t, K);
+        if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
+    }
+    return KVD_OK;
+}
+
+extern "C" kvd_status rswa_verify_workspace_bytes(int32_t B, int32_t H, int32_t head_dim, int64_t ref_cap,
+                                                  int32_t W, int32_t K, int64_t *bytes_out) {
+    if (bytes_out == nullptr || B < 1 || H < 1 || (head_dim != 64 && head_dim != 128) || ref_cap < 0 || W < 1 ||
+        K < 1 || K > kMaxHpk)
+        return KVD_EINVAL;
+    *bytes_out = rswa_ws(B, H, head_dim, ref_cap, W, K).total;
+    return KVD_OK;
+}
+
+extern "C" kvd_status rswa_verify(const float *q, const float *draft_k, const float *draft_v, int32_t K,
+                                  const float *ref_k, const float *ref_v, const float *ring_k,
+                                  const float *ring_v, const int32_t *prefill_len, const int32_t *ring_len,
+                                  const int32_t *ring_pos, int32_t B, int32_t H, int32_t head_dim,
+                                  int64_t ref_cap, int32_t W, float scale, float *out, void *workspace,
+                                  int64_t workspace_bytes, void *stream) {
+    if (ref_k == nullptr || ref_v == nullptr || ring_k == nullptr || ring_v == nullptr ||
+        !aligned16(ref_k) || !aligned16(ref_v) || !aligned16(ring_k) || !aligned16(ring_v))
+        return KVD_EINVAL;
+    RswaSrc src{};
+    src.ref_k = ref_k;
+    src.ref_v = ref_v;
+    src.ring_k = ring_k;
+    src.ring_v = ring_v;
+    return rswa_verify_impl<false>(q, draft_k, draft_v, K, src, prefill_len, ring_len, ring_pos, B, H, head_dim,
+                                   ref_cap, W, scale, out, workspace, workspace_bytes, stream);
+}
+
+extern "C" kvd_status rswa_verify_i8(const float *q, const float *draft_k, const float *draft_v, int32_t K,
+                                     const rswa_i8_mirror *m, const int32_t *prefill_len,
+                                     const int32_t *ring_len, const int32_t *ring_pos, int32_t B, int32_t H,
+                                     int32_t head_dim, int64_t ref_cap, int32_t W, float scale, float *out,
+                                     void *workspace, int64_t workspace_bytes, void *stream) {
+    if (!mirror_ok(m)) return KVD_EINVAL;
+    RswaSrc src{};
+    src.ref_k8 = m->ref_k;
+    src.ref_v8 = m->ref_v;
+    src.ring_k8 = m->ring_k;
+    src.ring_v8 = m->ring_v;
+    src.ref_ks = m->ref_ks;
+    src.ref_vs = m->ref_vs;
+    src.ring_ks = m->ring_ks;
+    src.ring_vs = m->ring_vs;
+    return rswa_verify_impl<true>(q, draft_k, draft_v, K, src, prefill_len, ring_len, ring_pos, B, H, head_dim,
+                                  ref_cap, W, scale, out, workspace, workspace_bytes, stream);
 }
 
 extern "C" kvd_status rswa_device_error(const void *workspace, int32_t clear, uint32_t *word_out) {

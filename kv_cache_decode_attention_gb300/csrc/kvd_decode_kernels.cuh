@@ -216,13 +216,14 @@ __device__ __forceinline__ int quant_code_i8(float x, float sc) {
 }
 
 // OPT: the call has a window or a softcap (compiled out of the common path).
-// KI8: the R-SWA int8 mirror (one query head, int8 K with one scale per row):
-// the query is quantised per head like a cache row and the QK dot is the
-// exact integer dot of the codes, scaled by qscale * kscale[row] after.
+// KI8: the R-SWA int8 mirror (int8 K with one scale per row; several query
+// rows only for a verify): each query row is quantised like a cache row and
+// the QK dot is the exact integer dot of the codes, scaled by qscale *
+// kscale[row] after.
 template <int HD, int HPK, bool KQ, bool VQ, bool OPT, bool KI8 = false>
 __device__ void split_body(const ChunkInfo &ci, const SplitArgs &a, char *smem) {
     using C = SplitCfg<HD, HPK, KQ, VQ, KI8>;
-    static_assert(!KI8 || (KQ && HPK == 1), "the int8 mirror has int8 K and one head per group");
+    static_assert(!KI8 || KQ, "the int8 mirror has int8 K");
     constexpr int CPL = C::CPL, TR = C::TR;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     float *sc = reinterpret_cast<float *>(smem + C::SC_OFF);
@@ -247,21 +248,27 @@ __device__ void split_body(const ChunkInfo &ci, const SplitArgs &a, char *smem) 
     // Query of every head of the group for this lane's channels, with the
     // K field and the softmax scale (in log2 units) folded in.
     float qr[HPK][CPL];
-    uint32_t qi = 0;     // KI8: this lane's query codes, packed bytes
-    float qfac = 0.0f;   // KI8: qscale * softmax scale * log2(e)
-    if (KI8) {
-        float x[CPL], mx = 0.0f;
+    uint32_t qi[HPK];    // KI8: this lane's query codes per query row, packed bytes
+    float qfac[HPK];     // KI8: qscale * softmax scale * log2(e) per query row
 #pragma unroll
-        for (int j = 0; j < CPL; ++j) {
-            x[j] = ci.q[lane * CPL + j];
-            mx = fmaxf(mx, fabsf(x[j]));
+    for (int h = 0; h < HPK; ++h) {
+        qi[h] = 0;
+        qfac[h] = 0.0f;
+        if (KI8 && h < a.hpk) {
+            const int64_t qo = a.K > 1 ? int64_t(h / a.hg) * a.n_q * HD + int64_t(h % a.hg) * HD : int64_t(h) * HD;
+            float x[CPL], mx = 0.0f;
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) {
+                x[j] = ci.q[qo + lane * CPL + j];
+                mx = fmaxf(mx, fabsf(x[j]));
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            const float sq = mx > 0.0f ? __fdiv_rn(mx, 127.0f) : 1.0f;
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) qi[h] |= (uint32_t(quant_code_i8(x[j], sq)) & 0xffu) << (8 * j);
+            qfac[h] = sq * a.qscale;
         }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        const float sq = mx > 0.0f ? __fdiv_rn(mx, 127.0f) : 1.0f;
-#pragma unroll
-        for (int j = 0; j < CPL; ++j) qi |= (uint32_t(quant_code_i8(x[j], sq)) & 0xffu) << (8 * j);
-        qfac = sq * a.qscale;
     }
 #pragma unroll
     for (int h = 0; h < HPK; ++h) {
@@ -311,7 +318,8 @@ __device__ void split_body(const ChunkInfo &ci, const SplitArgs &a, char *smem) 
                     const char *kr = kseg + (rbase + r) * C::KROW;
                     const uint32_t kw = CPL == 4 ? reinterpret_cast<const uint32_t *>(kr)[lane]
                                                  : uint32_t(reinterpret_cast<const uint16_t *>(kr)[lane]);
-                    v[r] = float(__dp4a(int(qi), int(kw), 0));
+#pragma unroll
+                    for (int h = 0; h < HPK; ++h) v[r * HPK + h] = float(__dp4a(int(qi[h]), int(kw), 0));
                     continue;
                 }
                 float x[CPL];
@@ -332,7 +340,13 @@ __device__ void split_body(const ChunkInfo &ci, const SplitArgs &a, char *smem) 
             if ((lane & ((32 >> C::LOGE) - 1)) == 0) {
                 const int e = lane >> (5 - C::LOGE);
                 const int r = rbase + e / HPK, h = e % HPK;
-                if (KI8) s = s * reinterpret_cast<const float *>(kseg + C::KS_OFF)[r] * qfac;
+                if (KI8) {
+                    float qf = qfac[0];
+#pragma unroll
+                    for (int hh = 1; hh < HPK; ++hh)
+                        if (h == hh) qf = qfac[hh];
+                    s = s * reinterpret_cast<const float *>(kseg + C::KS_OFF)[r] * qf;
+                }
                 bool vis = r < nt && (!OPT || row0 + r >= ci.lo);
                 if (OPT && a.K > 1 && vis) {
                     // verify: this query row's own causal limit and window
@@ -539,8 +553,9 @@ struct RswaSrc {
 };
 
 // I8: read the int8 mirror (rswa decode_attention_int8) instead of the f32
-// regions (decode_attention_scalar_head).
-template <int HD, bool I8>
+// regions (decode_attention_scalar_head).  HPK > 1 only for a verify: the
+// a.K = a.hpk draft queries of a head share every row (q [B][K][H][HD]).
+template <int HD, bool I8, int HPK = 1>
 __global__ void __launch_bounds__(kThreads, 2) split_rswa_kernel(SplitArgs a, RswaSrc src,
                                                                  RswaTable tb) {
     extern __shared__ __align__(128) char smem[];
@@ -582,12 +597,12 @@ __global__ void __launch_bounds__(kThreads, 2) split_rswa_kernel(SplitArgs a, Rs
         return;
     }
     ci.lo = 0;
-    ci.pidx0 = (head * a.nc_max + c) * 1;
-    ci.q = a.q + head * HD;
+    ci.pidx0 = (head * a.nc_max + c) * a.hpk;
+    ci.q = a.q + (int64_t(s) * a.K * src.H + h) * HD;
     ci.kcol = nullptr;
     ci.score0 = -1;
     ci.score_ld = 0;
-    split_body<HD, 1, I8, I8, false, I8>(ci, a, smem);
+    split_body<HD, HPK, I8, I8, false, I8>(ci, a, smem);
 }
 
 // ---------------------------------------------------------------- merge
@@ -680,6 +695,17 @@ __global__ void __launch_bounds__(HD) merge_rswa_kernel(MergeArgs a, RswaTable t
     const int nc = (tb.prefill_len[si] + a.chunk - 1) / a.chunk +
                    (tb.ring_len[si] + a.chunk - 1) / a.chunk;
     merge_body<HD>(a, s, int64_t(s) * a.n_q + h, 0, h, h, nc, nullptr);
+}
+
+// R-SWA verify merge: grid (H, streams of the launch, K); chunk partials of
+// the reference rows then one tail partial (ring + drafts) per query.
+template <int HD>
+__global__ void __launch_bounds__(HD) merge_rswa_verify_kernel(MergeArgs a, RswaTable tb, int32_t K) {
+    const int h = blockIdx.x, si = blockIdx.y, i = blockIdx.z;
+    if (si >= tb.n) return;
+    const int s = tb.s0 + si;
+    const int nc = (tb.prefill_len[si] + a.chunk - 1) / a.chunk + 1;
+    merge_body<HD>(a, s, (int64_t(s) * K + i) * a.n_q + h, i, h, h, nc, nullptr);
 }
 
 // Host launcher for one instance (instantiated per storage mode in its own unit).

@@ -743,3 +743,82 @@ def test_verify_errors(torch, kvd):
     with pytest.raises(kvd.KvdError) as e:
         kvd.decode_attention_verify(q, layer, 4, window=-1)
     assert e.value.status == -1
+
+
+@pytest.mark.parametrize("int8", [False, True])
+@pytest.mark.parametrize("hd,H", [(128, 10), (64, 3)])
+def test_rswa_verify_parity(torch, kvd, int8, hd, H):
+    """rswa verify_attention, query-batched over K = 5, 16 and 1 drafts, against the
+    oracle's write-then-decode on a private ring copy: streams with a long, a
+    short and no reference block, full rings (each draft evicts the oldest
+    row); the device cache and cursors stay as they were."""
+    B, W, ref_cap = 3, 128, 1024
+    prefill = [700, 30, 0]
+    cache = kvd.RingCache(B, ref_cap, H, hd, W, int8=int8)
+    o_ref_k = np.zeros((B, H, ref_cap, hd), np.float32)
+    o_ref_v = np.zeros_like(o_ref_k)
+    o_ring_k = np.zeros((B, H, W, hd), np.float32)
+    o_ring_v = np.zeros_like(o_ring_k)
+    cursors = [np.zeros(2, np.int32) for _ in range(B)]
+    for s in range(B):
+        m = prefill[s]
+        k = synthetic.normal((H, m, hd), 500 + s)
+        v = synthetic.normal((H, m, hd), 510 + s)
+        kvd.rswa_record_prefill(cache, s, torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda())
+        o_ref_k[s, :, :m], o_ref_v[s, :, :m] = k, v
+    for t in range(140):
+        kt = synthetic.normal((B, H, hd), 600 + t)
+        vt = synthetic.normal((B, H, hd), 700 + t)
+        kvd.rswa_ring_write(cache, torch.from_numpy(kt).cuda(), torch.from_numpy(vt).cuda())
+        for s in range(B):
+            oracle.rswa_write(o_ring_k[s], o_ring_v[s], kt[s], vt[s], True, cursors[s])
+    scale = np.float32(1.0 / math.sqrt(hd))
+    for K in (5, 16, 1):
+        q = synthetic.normal((B, K, H, hd), 800 + K)
+        dk = synthetic.normal((B, K, H, hd), 810 + K)
+        dv = synthetic.normal((B, K, H, hd), 820 + K)
+        snap = (cache.ring_len.copy(), cache.ring_pos.copy(), cache.ring_k.clone())
+        out = kvd.rswa_verify(torch.from_numpy(q).cuda(), torch.from_numpy(dk).cuda(), torch.from_numpy(dv).cuda(),
+                              cache, int8=int8).cpu().numpy()
+        assert np.array_equal(cache.ring_len, snap[0]) and np.array_equal(cache.ring_pos, snap[1])
+        assert torch.equal(cache.ring_k, snap[2])
+        for s in range(B):
+            ref = oracle.rswa_verify(q[s], dk[s], dv[s], o_ref_k[s], o_ref_v[s], prefill[s], o_ring_k[s],
+                                     o_ring_v[s], cursors[s], scale, int8=int8)
+            for i in range(K):
+                err = out_error(out[s, i].reshape(H, hd), ref[i])
+                assert err <= OUT_TOL, (K, s, i, err)
+    assert cache.device_error() == 0
+
+
+@pytest.mark.parametrize("int8", [False, True])
+def test_rswa_verify_steady_ring_and_fill(torch, kvd, int8):
+    """One stream per ring state (warm with room for the drafts, filling during
+    them, full: each draft evicts the oldest row) with a reference block; K = 6."""
+    H, hd, W, ref_cap, K = 4, 128, 128, 64, 6
+    scale = np.float32(1.0 / math.sqrt(hd))
+    for n_gen in (10, 124, 333):
+        cache = kvd.RingCache(1, ref_cap, H, hd, W, int8=int8)
+        k = synthetic.normal((H, 50, hd), 900)
+        v = synthetic.normal((H, 50, hd), 901)
+        kvd.rswa_record_prefill(cache, 0, torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda())
+        rk = np.zeros((H, ref_cap, hd), np.float32)
+        rv = np.zeros_like(rk)
+        rk[:, :50], rv[:, :50] = k, v
+        gk = np.zeros((H, W, hd), np.float32)
+        gv = np.zeros_like(gk)
+        cur = np.zeros(2, np.int32)
+        for t in range(n_gen):
+            kt = synthetic.normal((1, H, hd), 1000 + t)
+            vt = synthetic.normal((1, H, hd), 2000 + t)
+            kvd.rswa_ring_write(cache, torch.from_numpy(kt).cuda(), torch.from_numpy(vt).cuda())
+            oracle.rswa_write(gk, gv, kt[0], vt[0], True, cur)
+        q = synthetic.normal((1, K, H, hd), 3000 + n_gen)
+        dk = synthetic.normal((1, K, H, hd), 3100 + n_gen)
+        dv = synthetic.normal((1, K, H, hd), 3200 + n_gen)
+        out = kvd.rswa_verify(torch.from_numpy(q).cuda(), torch.from_numpy(dk).cuda(), torch.from_numpy(dv).cuda(),
+                              cache, int8=int8).cpu().numpy()
+        ref = oracle.rswa_verify(q[0], dk[0], dv[0], rk, rv, 50, gk, gv, cur, scale, int8=int8)
+        for i in range(K):
+            assert out_error(out[0, i].reshape(H, hd), ref[i]) <= OUT_TOL, (n_gen, i)
+        assert cache.ring_len[0] == cur[0] and cache.ring_pos[0] == cur[1]
