@@ -132,6 +132,7 @@ struct RunMergeArgs {
     float *ml;                    // (max, sum) per (sequence, query head) for imp, or null
     const float *sinks;           // learned sink logit per query head [n_q], or null
     int32_t n_q, hpk;
+    int32_t K = 1, hg = 0;        // verify: K drafts, hg heads per group (hpk = K * hg)
 };
 
 // Log-sum-exp merge of the run partials of one (sequence, query head) written
@@ -149,11 +150,12 @@ constexpr int kMergeBatch = 4;
 __global__ void __launch_bounds__(32 * kMergeWarps) merge_runs_kernel(RunMergeArgs a, MergeLayerSrc src) {
     __shared__ float wmax[kMergeWarps], wsum[kMergeWarps];
     __shared__ __align__(16) float wacc[kMergeWarps][128];
-    const int h = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
+    const int h = blockIdx.x, b = blockIdx.y, k = blockIdx.z, t = threadIdx.x;
     const int warp = t >> 5, lane = t & 31;
     const int L = src.seq_len[b];
-    const int grp = src.slot[h / a.hpk];
-    float *o = a.out + (int64_t(b) * a.n_q + h) * 128;
+    const int hg = a.K > 1 ? a.hg : a.hpk;
+    const int grp = src.slot[h / hg];
+    float *o = a.out + ((int64_t(b) * a.K + k) * a.n_q + h) * 128;
     float *mlp = a.ml ? a.ml + (int64_t(b) * a.n_q + h) * 2 : nullptr;
     if (grp < 0 || L <= 0) {
         if (t < 128) o[t] = 0.0f;
@@ -165,7 +167,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_runs_kernel(RunMergeAr
     }
     const int64_t unit = int64_t(b) * src.n_live + grp;
     const int64_t first = a.unit_slots[2 * unit], last = a.unit_slots[2 * unit + 1];
-    const int hh = h % a.hpk;
+    const int hh = a.K > 1 ? k * hg + h % hg : h % a.hpk;  // the query's row in the partials
     const float *pmh = a.pm + hh, *plh = a.pl + hh, *pah = a.pacc + int64_t(hh) * 128 + 4 * lane;
     float M = -INFINITY, Ls = 0.0f;
     float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
@@ -206,7 +208,15 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_runs_kernel(RunMergeAr
     __syncthreads();
     float Mall = wmax[0];
 #pragma unroll
-    for (int w = 1; w < kMergeWarps; ++w) Mall = fmaxf(Mall, wmax[w]);  // finite: L >= 1
+    for (int w = 1; w < kMergeWarps; ++w) Mall = fmaxf(Mall, wmax[w]);
+    if (Mall == -INFINITY) {  // no visible row (a verify query before every row)
+        if (t < 128) o[t] = 0.0f;
+        if (mlp && t == 0) {
+            mlp[0] = -INFINITY;
+            mlp[1] = 0.0f;
+        }
+        return;
+    }
     const float fw = exp2f(M - Mall);  // 0 for a warp that saw no run
     acc.x *= fw;
     acc.y *= fw;
@@ -858,6 +868,45 @@ extern "C" kvd_status decode_attention_verify(const float *q, const kvd_layer *L
     s.seq_len = l->d_seq_len;
     s.live = l->d_live;
     s.n_live = l->n_live;
+    MergeLayerSrc ms;
+    ms.seq_len = l->d_seq_len;
+    ms.slot = l->d_slot;
+    ms.vcol = static_cast<const float *>(l->buf[KVD_BUF_VCOL]);
+    ms.n_live = l->n_live;
+    if (warp_path(l)) {
+        // q8_2f at head_dim 128: the K * hg query rows of a group are the M rows
+        // of the tensor-core kernel (heads in M), one read of every tile
+        int64_t T = 0;
+        for (int b = 0; b < l->n_seq; ++b) T += int64_t(l->n_live) * tiles_of(l->h_seq_len[b], window, K);
+        const int64_t workers = split_q8_tc_workers(2);
+        if (workers <= 0) return KVD_ECUDA;
+        WarpArgs wa;
+        wa.a = a;
+        wa.T = T;
+        wa.G = int32_t(std::min(T, workers));
+        wa.n_seq = l->n_seq;
+        wa.unit_slots = reinterpret_cast<int64_t *>(ws + w.units);
+        if (T > 0) {
+            MmaMaps maps;
+            std::memcpy(&maps.kq, l->tmap_kq, sizeof(maps.kq));
+            std::memcpy(&maps.vq, l->tmap_vq, sizeof(maps.vq));
+            if (split_layer_q8_tc(2, wa, s, maps, st) != cudaSuccess) return KVD_ECUDA;
+        }
+        RunMergeArgs rm;
+        rm.pm = a.pm;
+        rm.pl = a.pl;
+        rm.pacc = a.pacc;
+        rm.out = out;
+        rm.ml = nullptr;
+        rm.n_q = n_q;
+        rm.hpk = hpk;
+        rm.K = K;
+        rm.hg = hg;
+        rm.unit_slots = wa.unit_slots;
+        rm.sinks = sinks;
+        merge_runs_kernel<<<dim3(unsigned(n_q), unsigned(l->n_seq), unsigned(K)), 32 * kMergeWarps, 0, st>>>(rm, ms);
+        return cudaGetLastError() == cudaSuccess ? KVD_OK : KVD_ECUDA;
+    }
     if (max_len > 0 && l->n_live > 0) {
         dim3 grid(unsigned(ceil_div(max_len, chunk)), unsigned(l->n_live), unsigned(l->n_seq));
         const int hb = hpk_bucket(hpk);
@@ -883,11 +932,6 @@ extern "C" kvd_status decode_attention_verify(const float *q, const kvd_layer *L
     m.chunk = chunk;
     m.sinks = sinks;
     m.window = window;
-    MergeLayerSrc ms;
-    ms.seq_len = l->d_seq_len;
-    ms.slot = l->d_slot;
-    ms.vcol = static_cast<const float *>(l->buf[KVD_BUF_VCOL]);
-    ms.n_live = l->n_live;
     dim3 mgrid(unsigned(n_q), unsigned(l->n_seq), unsigned(K));
     if (l->hd == 128) merge_verify_kernel<128><<<mgrid, 128, 0, st>>>(m, ms, K, hg);
     else merge_verify_kernel<64><<<mgrid, 64, 0, st>>>(m, ms, K, hg);

@@ -50,7 +50,7 @@ __global__ void __launch_bounds__(32, 8) split_h16_kernel(WarpArgs wa, LayerSrc 
     if (x_begin >= x_end) return;
 
     TileCursor cur;
-    if (!cursor_locate(cur, x_begin, src, wa.n_seq, a.window, lane, a.err)) return;
+    if (!cursor_locate(cur, x_begin, src, wa.n_seq, a.window, a.K, lane, a.err)) return;
     TileCursor prod = cur;
     if (cur.tl % kBlockTiles == 0) {
         // the slot just below this worker's first run belongs to no run
@@ -73,7 +73,7 @@ __global__ void __launch_bounds__(32, 8) split_h16_kernel(WarpArgs wa, LayerSrc 
             if (lane == 0) issue_tile(prod, &maps.kq, &maps.vq, src, sm + (i % kStages) * kStageBytes,
                                       &bar[i % kStages]);
             ++issued;
-            if (x_begin + issued < x_end) prod_ok = cursor_next(prod, src, wa.n_seq, a.window, a.err);
+            if (x_begin + issued < x_end) prod_ok = cursor_next(prod, src, wa.n_seq, a.window, a.K, a.err);
         }
     }
 
@@ -106,7 +106,12 @@ __global__ void __launch_bounds__(32, 8) split_h16_kernel(WarpArgs wa, LayerSrc 
             q_b = cur.b;
             q_gl = cur.gl;
             const int g = src.live[cur.gl];
-            const float *qg = a.q + (int64_t(cur.b) * a.n_q + int64_t(g) * a.hpk) * 128;
+            // M row e: query head e of the group, or for a verify of K drafts
+            // draft e / hg, head e % hg ([n_seq][K][n_q][128])
+            const int hg = a.K > 1 ? a.hg : a.hpk;
+            const float *qg = a.q + (int64_t(cur.b) * a.K * a.n_q + int64_t(g) * hg) * 128;
+            const float *qa_row = qg + (int64_t(ha / hg) * a.n_q + ha % hg) * 128;
+            const float *qb_row = qg + (int64_t(hb / hg) * a.n_q + hb % hg) * 128;
             const float *kc = src.kcol + (int64_t(cur.b) * src.n_live + cur.gl) * 128;
             // two passes over the (cached) query rows: the heads' maxima
             // first, then the scaled terms, so no copy of q stays live
@@ -114,8 +119,8 @@ __global__ void __launch_bounds__(32, 8) split_h16_kernel(WarpArgs wa, LayerSrc 
                 const int d = 16 * ch + 4 * t4;
                 const float4 kv = *reinterpret_cast<const float4 *>(kc + d);
                 float4 qv = make_float4(0.0f, 0.0f, 0.0f, 0.0f), qw = qv;
-                if (ha < a.hpk) qv = *reinterpret_cast<const float4 *>(qg + ha * 128 + d);
-                if (hb < a.hpk) qw = *reinterpret_cast<const float4 *>(qg + hb * 128 + d);
+                if (ha < a.hpk) qv = *reinterpret_cast<const float4 *>(qa_row + d);
+                if (hb < a.hpk) qw = *reinterpret_cast<const float4 *>(qb_row + d);
                 xa[0] = qv.x * kv.x * a.qscale;
                 xa[1] = qv.y * kv.y * a.qscale;
                 xa[2] = qv.z * kv.z * a.qscale;
@@ -246,15 +251,28 @@ __global__ void __launch_bounds__(32, 8) split_h16_kernel(WarpArgs wa, LayerSrc 
                 }
             }
             // rows outside [r_lo, n_valid) (a partial last tile, or rows before
-            // the window in the first one) drop out; full tiles skip the masks
-            const bool full = (!OPT || r_lo <= 0) && n_valid == kWR;
+            // the window in the first one) drop out; full tiles skip the masks.
+            // A verify bounds each M row by its own query's limit and window:
+            // rows [lo_a, hi_a) for ha, [lo_b, hi_b) for hb (tile rows).
+            bool full = (!OPT || r_lo <= 0) && n_valid == kWR;
+            int lo_a = r_lo, hi_a = n_valid, lo_b = r_lo, hi_b = n_valid;
+            if (OPT && a.K > 1) {
+                const int hg = a.hg;
+                const int upto_a = cur.Lb - (a.K - 1 - ha / hg), upto_b = cur.Lb - (a.K - 1 - hb / hg);
+                lo_a = int(first_visible(upto_a, a.window)) - row0;
+                lo_b = int(first_visible(upto_b, a.window)) - row0;
+                hi_a = min(upto_a - row0, n_valid);
+                hi_b = min(upto_b - row0, n_valid);
+                full = full && __all_sync(0xffffffffu, lo_a <= 0 && lo_b <= 0 && hi_a >= kWR && hi_b >= kWR);
+            }
             if (!full) {
 #pragma unroll
                 for (int nt = 0; nt < 4; ++nt) {
                     const int r0 = nt * 8 + 2 * t4;
-                    const bool v0 = r0 >= r_lo && r0 < n_valid, v1 = r0 + 1 >= r_lo && r0 + 1 < n_valid;
-                    if (!v0) sreg[nt][0] = sreg[nt][2] = -INFINITY;
-                    if (!v1) sreg[nt][1] = sreg[nt][3] = -INFINITY;
+                    if (!(r0 >= lo_a && r0 < hi_a)) sreg[nt][0] = -INFINITY;
+                    if (!(r0 + 1 >= lo_a && r0 + 1 < hi_a)) sreg[nt][1] = -INFINITY;
+                    if (!(r0 >= lo_b && r0 < hi_b)) sreg[nt][2] = -INFINITY;
+                    if (!(r0 + 1 >= lo_b && r0 + 1 < hi_b)) sreg[nt][3] = -INFINITY;
                 }
             }
             if (IMP) {
@@ -321,11 +339,13 @@ __global__ void __launch_bounds__(32, 8) split_h16_kernel(WarpArgs wa, LayerSrc 
             mb = mnb;
             // weights -> f16 terms in the A layout of the value MMA: k16 step
             // kk covers score tiles 2kk (a0, a1) and 2kk + 1 (a2, a3)
+            // a verify row that has seen no visible row yet keeps weight 0
+            const float mza = OPT && ma == -INFINITY ? 0.0f : ma, mzb = OPT && mb == -INFINITY ? 0.0f : mb;
             uint32_t pa[2][2][4];  // [kk][term][reg]
 #pragma unroll
             for (int nt = 0; nt < 4; ++nt) {
-                const float e0 = fast_exp2(sreg[nt][0] - ma), e1 = fast_exp2(sreg[nt][1] - ma);
-                const float e2 = fast_exp2(sreg[nt][2] - mb), e3 = fast_exp2(sreg[nt][3] - mb);
+                const float e0 = fast_exp2(sreg[nt][0] - mza), e1 = fast_exp2(sreg[nt][1] - mza);
+                const float e2 = fast_exp2(sreg[nt][2] - mzb), e3 = fast_exp2(sreg[nt][3] - mzb);
                 la += e0 + e1;
                 lb += e2 + e3;
                 const float v0 = vsr[nt][0] * wsc, v1 = vsr[nt][1] * wsc;
@@ -380,9 +400,9 @@ __global__ void __launch_bounds__(32, 8) split_h16_kernel(WarpArgs wa, LayerSrc 
                     issue_tile(prod, &maps.kq, &maps.vq, src, st, &bar[stg]);
                 }
                 ++issued;
-                if (x_begin + issued < x_end) prod_ok = cursor_next(prod, src, wa.n_seq, a.window, a.err);
+                if (x_begin + issued < x_end) prod_ok = cursor_next(prod, src, wa.n_seq, a.window, a.K, a.err);
             }
-            if (x + 1 < x_end && !cursor_next(cur, src, wa.n_seq, a.window, a.err)) {
+            if (x + 1 < x_end && !cursor_next(cur, src, wa.n_seq, a.window, a.K, a.err)) {
                 ok = false;
                 ++i;
                 break;
@@ -427,7 +447,7 @@ __global__ void __launch_bounds__(32, 8) split_h16_kernel(WarpArgs wa, LayerSrc 
 
 inline cudaError_t launch_split_h16(const WarpArgs &wa, const LayerSrc &s, const MmaMaps &maps,
                                     cudaStream_t st) {
-    const bool opt = wa.a.window > 0 || wa.a.softcap2 > 0.0f, imp = wa.a.scores != nullptr;
+    const bool opt = wa.a.window > 0 || wa.a.softcap2 > 0.0f || wa.a.K > 1, imp = wa.a.scores != nullptr;
     auto kern = opt ? (imp ? split_h16_kernel<true, true> : split_h16_kernel<true, false>)
                     : (imp ? split_h16_kernel<false, true> : split_h16_kernel<false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, H16Cfg::SMEM_ALLOC);

@@ -191,19 +191,20 @@ struct TileCursor {
 
 __device__ __forceinline__ int blocks_of(int tiles) { return (tiles + kBlockTiles - 1) / kBlockTiles; }
 
-// Tiles of a sequence of L rows under a sliding window (0 = none).
-__host__ __device__ __forceinline__ int64_t tiles_of(int64_t L, int64_t window) {
-    const int64_t f0 = first_visible(L, window) / kWR * kWR;
+// Tiles of a sequence of L rows under a sliding window (0 = none); for a
+// verify of K drafts they start at the earliest query's first row.
+__host__ __device__ __forceinline__ int64_t tiles_of(int64_t L, int64_t window, int32_t K = 1) {
+    const int64_t f0 = first_visible(verify_len(L, K), window) / kWR * kWR;
     return (L - f0 + kWR - 1) / kWR;
 }
 
 // Load sequence b's shape into the cursor; false (and an error bit) if its
 // length exceeds its capacity.
-__device__ __forceinline__ bool cursor_seq(TileCursor &c, const LayerSrc &src, int64_t window,
+__device__ __forceinline__ bool cursor_seq(TileCursor &c, const LayerSrc &src, int64_t window, int32_t K,
                                            uint32_t *err) {
     c.cap = src.cap[c.b];
     c.rbase = src.row_base[c.b];
-    c.lo = int(first_visible(c.Lb, window));
+    c.lo = int(first_visible(verify_len(c.Lb, K), window));
     c.f0 = c.lo / kWR * kWR;
     if (int64_t(c.Lb) > c.cap) {
         set_error(err, kErrBounds);
@@ -214,7 +215,7 @@ __device__ __forceinline__ bool cursor_seq(TileCursor &c, const LayerSrc &src, i
 
 // Advance to the next tile in the global order; false past the last sequence.
 __device__ __forceinline__ bool cursor_next(TileCursor &c, const LayerSrc &src, int n_seq, int64_t window,
-                                            uint32_t *err) {
+                                            int32_t K, uint32_t *err) {
     if (++c.tl < c.Tb) return true;
     c.tl = 0;
     if (++c.gl < src.n_live) {
@@ -226,20 +227,20 @@ __device__ __forceinline__ bool cursor_next(TileCursor &c, const LayerSrc &src, 
     for (;;) {
         if (++c.b >= n_seq) return false;
         c.Lb = src.seq_len[c.b];
-        c.Tb = int(tiles_of(c.Lb, window));
+        c.Tb = int(tiles_of(c.Lb, window, K));
         if (c.Tb > 0) break;
     }
-    return cursor_seq(c, src, window, err);
+    return cursor_seq(c, src, window, K, err);
 }
 
 // Find global tile x: a warp-wide scan of the sequences' tile counts.
 __device__ inline bool cursor_locate(TileCursor &c, int64_t x, const LayerSrc &src, int n_seq, int64_t window,
-                                     int lane, uint32_t *err) {
+                                     int32_t K, int lane, uint32_t *err) {
     int64_t tp = 0, bq = 0;  // tiles and blocks of the sequences before `base`
     for (int base = 0; base < n_seq; base += 32) {
         const int i = base + lane;
         const int L = i < n_seq ? src.seq_len[i] : 0;
-        const int Tb = int(tiles_of(L, window));
+        const int Tb = int(tiles_of(L, window, K));
         int64_t ut = int64_t(src.n_live) * Tb, ub = int64_t(src.n_live) * blocks_of(Tb);
         // inclusive prefix over the lanes
 #pragma unroll
@@ -265,7 +266,7 @@ __device__ inline bool cursor_locate(TileCursor &c, int64_t x, const LayerSrc &s
             const int64_t r = x - (tp + ex_t);
             c.gl = int(r / c.Tb);
             c.tl = int(r % c.Tb);
-            if (!cursor_seq(c, src, window, err)) return false;
+            if (!cursor_seq(c, src, window, K, err)) return false;
             c.rbase += int64_t(c.gl) * c.cap;
             return true;
         }
@@ -307,7 +308,7 @@ __global__ void __launch_bounds__(32, 12) split_warp_kernel(WarpArgs wa, LayerSr
     if (x_begin >= x_end) return;
 
     TileCursor cur;
-    if (!cursor_locate(cur, x_begin, src, wa.n_seq, a.window, lane, a.err)) return;
+    if (!cursor_locate(cur, x_begin, src, wa.n_seq, a.window, a.K, lane, a.err)) return;
     TileCursor prod = cur;
     if (cur.tl % kBlockTiles == 0) {
         // This worker starts on a block start: the slot just below its first
@@ -333,7 +334,7 @@ __global__ void __launch_bounds__(32, 12) split_warp_kernel(WarpArgs wa, LayerSr
             if (lane == 0) issue_tile(prod, &maps.kq, &maps.vq, src, sm + (i % kStages) * kStageBytes,
                                       &bar[i % kStages]);
             ++issued;
-            if (x_begin + issued < x_end) prod_ok = cursor_next(prod, src, wa.n_seq, a.window, a.err);
+            if (x_begin + issued < x_end) prod_ok = cursor_next(prod, src, wa.n_seq, a.window, a.K, a.err);
         }
     }
 
@@ -620,9 +621,9 @@ __global__ void __launch_bounds__(32, 12) split_warp_kernel(WarpArgs wa, LayerSr
                     issue_tile(prod, &maps.kq, &maps.vq, src, st, &bar[stg]);
                 }
                 ++issued;
-                if (x_begin + issued < x_end) prod_ok = cursor_next(prod, src, wa.n_seq, a.window, a.err);
+                if (x_begin + issued < x_end) prod_ok = cursor_next(prod, src, wa.n_seq, a.window, a.K, a.err);
             }
-            if (x + 1 < x_end && !cursor_next(cur, src, wa.n_seq, a.window, a.err)) {
+            if (x + 1 < x_end && !cursor_next(cur, src, wa.n_seq, a.window, a.K, a.err)) {
                 ok = false;
                 ++i;
                 break;
