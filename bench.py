@@ -281,6 +281,20 @@ def run_reference(args, rank):
 RSWA_WORKLOADS = ("rswa", "rswa_i8")
 
 
+def packed_inputs(torch, parts_per_step):
+    """Each step's input tensors packed into one pinned host buffer, and one device
+    staging buffer with views of the same shapes: one host-to-device copy per step."""
+    shapes = [t.shape for t in parts_per_step[0]]
+    sizes = [t.numel() for t in parts_per_step[0]]
+    pinned = [torch.cat([t.reshape(-1).cpu() for t in parts]).pin_memory() for parts in parts_per_step]
+    stage = torch.empty(sum(sizes), device=parts_per_step[0][0].device)
+    views, o = [], 0
+    for shp, n in zip(shapes, sizes):
+        views.append(stage[o:o + n].view(shp))
+        o += n
+    return pinned, stage, views
+
+
 def run_gpu_rswa(args, rank, world):
     """The R-SWA workloads: 16 streams in steady state (reference 32640 rows +
     a full ring), one step = rswa ring write of one token per stream + decode
@@ -356,17 +370,12 @@ def run_gpu_rswa(args, rank, world):
     peak, peak_kind = peaks()
     achieved = dec_bytes / (k_ms * 1e-3) / 1e9
 
-    pin_q = [qs[i].cpu().pin_memory() for i in range(8)]
-    pin_k = [news[i][0].cpu().pin_memory() for i in range(8)]
-    pin_v = [news[i][1].cpu().pin_memory() for i in range(8)]
+    pinned, stage, (dq, dk, dv) = packed_inputs(torch, [(qs[i], news[i][0], news[i][1]) for i in range(8)])
     pin_out = torch.empty(B, H * hd).pin_memory()
-    dq, dk, dv = torch.empty_like(qs[0]), torch.empty_like(news[0][0]), torch.empty_like(news[0][1])
     torch.cuda.synchronize()
     a0 = time.perf_counter()
     for j in range(args.steps):
-        dq.copy_(pin_q[j % 8], non_blocking=True)
-        dk.copy_(pin_k[j % 8], non_blocking=True)
-        dv.copy_(pin_v[j % 8], non_blocking=True)
+        stage.copy_(pinned[j % 8], non_blocking=True)
         kvd.rswa_ring_write(c, dk, dv)
         decode(dq, c, out=out)
         pin_out.copy_(out, non_blocking=True)
@@ -527,12 +536,8 @@ def run_gpu(args, rank, world):
     achieved = kbytes / (k_ms * 1e-3) / 1e9
 
     # ---- end to end through the public API with host buffers
-    pin_q = [qs[i].cpu().pin_memory() for i in range(8)]
-    pin_k = [news[i][0].cpu().pin_memory() for i in range(8)]
-    pin_v = [news[i][1].cpu().pin_memory() for i in range(8)]
+    pinned, stage, (dq, dk, dv) = packed_inputs(torch, [(qs[i], news[i][0], news[i][1]) for i in range(8)])
     pin_out = torch.empty(wl0.n_seq, wl0.n_q, wl0.hd).pin_memory()
-    dq = torch.empty_like(qs[0])
-    dk, dv = torch.empty_like(news[0][0]), torch.empty_like(news[0][1])
     e2e_steps = args.steps
     if math.ceil(2 * (n_steps + e2e_steps) / R) > extra:
         e2e_steps = 0
@@ -544,9 +549,7 @@ def run_gpu(args, rank, world):
         for j in range(e2e_steps):
             i = n_steps + j
             w = wls[i % R]
-            dq.copy_(pin_q[i % 8], non_blocking=True)
-            dk.copy_(pin_k[i % 8], non_blocking=True)
-            dv.copy_(pin_v[i % 8], non_blocking=True)
+            stage.copy_(pinned[i % 8], non_blocking=True)
             kvd.kv_append(w.layer, dk, dv)
             kvd.decode_attention(dq, w.layer, out=outs[i % R], imp=imps[i % R], scale=w.scale, workspace=ws)
             pin_out.copy_(outs[i % R], non_blocking=True)

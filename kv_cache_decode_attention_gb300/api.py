@@ -25,9 +25,17 @@ from ._abi import F32, Q8, Q8K, Q8V  # noqa: F401
 MODE_NAMES = {"f32": F32, "q8": Q8, "q8_2f": Q8, "q8k": Q8K, "q8v": Q8V}
 
 
+# The current stream's raw handle without building a Stream object (the
+# public torch.cuda.current_stream() costs microseconds per call).
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream=None) -> C.c_void_p:
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return C.c_void_p(s.cuda_stream)
+    if stream is not None:
+        return C.c_void_p(stream.cuda_stream)
+    if _raw_stream is not None:
+        return C.c_void_p(_raw_stream(torch.cuda.current_device()))
+    return C.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
 def _ptr(t: torch.Tensor | None) -> C.c_void_p | None:

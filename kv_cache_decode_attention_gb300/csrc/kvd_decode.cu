@@ -436,7 +436,7 @@ cudaError_t launch_split_rswa(const SplitArgs &a, const RswaSrc &s, const RswaTa
                               cudaStream_t st) {
     using C = SplitCfg<HD, HPK, I8, I8, I8>;
     auto kern = split_rswa_kernel<HD, I8, HPK>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), C::SMEM);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, C::SMEM, st>>>(a, s, t);
     return cudaGetLastError();
@@ -789,8 +789,7 @@ extern "C" kvd_status decode_attention_ex(const float *q, const kvd_layer *L, in
         dim3 igrid(unsigned(ceil_div(max_len, kImpRows)), unsigned(l->n_seq));
         const size_t ml_bytes = size_t(std::max(1, l->n_live * hpk)) * 2 * sizeof(float);
         if (ml_bytes > 40 * 1024 &&
-            cudaFuncSetAttribute(imp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(ml_bytes)) != cudaSuccess)
+            set_smem_once(reinterpret_cast<const void *>(imp_kernel), int(ml_bytes)) != cudaSuccess)
             return KVD_ECUDA;
         imp_kernel<<<igrid, kImpThreads, ml_bytes, st>>>(ia);
         if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;

@@ -715,7 +715,7 @@ cudaError_t launch_split_layer_impl(const SplitArgs &a, const LayerSrc &s, dim3 
     using C = SplitCfg<HD, HPK, KQ, VQ>;
     auto kern = (a.window > 0 || a.softcap2 > 0.0f || a.K > 1) ? split_layer_kernel<HD, HPK, KQ, VQ, true>
                                                                 : split_layer_kernel<HD, HPK, KQ, VQ, false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), C::SMEM);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, C::SMEM, st>>>(a, s);
     return cudaGetLastError();

@@ -8,6 +8,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+#include <vector>
+
 #include "../../include/kvd.h"
 
 namespace kvd {
@@ -135,6 +138,27 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
             smem_addr(dst)),
         "l"(src), "r"(bytes), "r"(smem_addr(bar))
         : "memory");
+}
+
+// Raise a kernel's dynamic shared-memory limit once per (kernel, device):
+// the attribute belongs to the function in a device's context, and setting
+// it on every launch costs a driver call per launch.
+inline cudaError_t set_smem_once(const void *kern, int bytes) {
+    struct Done {
+        const void *kern;
+        int dev, bytes;
+    };
+    static std::mutex mu;
+    static std::vector<Done> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Done &d : done)
+        if (d.kern == kern && d.dev == dev && d.bytes >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.push_back(Done{kern, dev, bytes});
+    return e;
 }
 
 __device__ __forceinline__ void set_error(uint32_t *err, uint32_t bit) {

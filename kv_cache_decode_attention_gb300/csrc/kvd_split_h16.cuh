@@ -450,7 +450,7 @@ inline cudaError_t launch_split_h16(const WarpArgs &wa, const LayerSrc &s, const
     const bool opt = wa.a.window > 0 || wa.a.softcap2 > 0.0f || wa.a.K > 1, imp = wa.a.scores != nullptr;
     auto kern = opt ? (imp ? split_h16_kernel<true, true> : split_h16_kernel<true, false>)
                     : (imp ? split_h16_kernel<false, true> : split_h16_kernel<false, false>);
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, H16Cfg::SMEM_ALLOC);
+    cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), H16Cfg::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     kern<<<unsigned(wa.G), 32, H16Cfg::SMEM_ALLOC, st>>>(wa, s, maps);
     return cudaGetLastError();

@@ -682,7 +682,7 @@ cudaError_t launch_split_warp(const WarpArgs &wa, const LayerSrc &s, const MmaMa
     const bool opt = wa.a.window > 0 || wa.a.softcap2 > 0.0f, imp = wa.a.scores != nullptr;
     auto kern = opt ? (imp ? split_warp_kernel<PACK, true, true> : split_warp_kernel<PACK, true, false>)
                     : (imp ? split_warp_kernel<PACK, false, true> : split_warp_kernel<PACK, false, false>);
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+    cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     kern<<<unsigned(wa.G), 32, C::SMEM_ALLOC, st>>>(wa, s, maps);
     return cudaGetLastError();
