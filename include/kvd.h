@@ -4,7 +4,8 @@
  * One process, one GPU (sm_103a).  Every device buffer is allocated by the
  * caller (by any CUDA allocator) and passed in as a plain pointer;
  * the library computes the sizes, never allocates device memory and keeps
- * no global state.  Every call is asynchronous on the caller's CUDA stream
+ * no global state beyond caches of per-device kernel attributes and
+ * occupancy (and the scratch array of decode_attention_static).  Every call is asynchronous on the caller's CUDA stream
  * (`stream` is a cudaStream_t passed as void*, NULL = legacy default
  * stream) unless its comment says otherwise.
  *
