@@ -11,12 +11,15 @@
 //           order of the page's stable sort).  Two ordered block scans turn
 //           the keep flags into the ascending list of kept rows, and the
 //           CTA gathers imp along it (clearing the dropped rows' entries).
-//   gather  one CTA per (live head, storage): the kept rows move down to
-//           positions 0 .. keep_last - 1 of every storage independently (f32
-//           K / V, int8 codes, their scales).  Kept positions ascend and
-//           kept[j] >= j, so walking tiles of j in order, loading a whole
-//           tile before storing it, never reads a row an earlier store
-//           overwrote: the move is in place, with no staging copy.
+//   gather  the kept rows move down to positions 0 .. keep_last - 1 of every
+//           storage independently (f32 K / V, int8 codes, their scales).
+//           Kept positions ascend and kept[j] >= j, so a pass over j in
+//           order that reads a stretch of rows before writing it never reads
+//           a row an earlier write overwrote.  With many regions (sequence x
+//           live head x storage) one CTA walks each region's tiles in order,
+//           in place; with few, the rows go in batches of j through a
+//           workspace copy (one kernel reads a batch, the next writes it), so
+//           every batch spreads over the whole GPU.
 // The device length becomes keep_last in the select kernel; the host mirror
 // is updated by the entry point.
 //
@@ -58,30 +61,36 @@ __device__ __forceinline__ uint32_t mass_key(float x) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Exclusive prefix count of `flag` over the block in thread order, and the
-// block total.  `warp_sums` holds kSelectThreads / 32 ints of shared memory.
-__device__ __forceinline__ int block_excl_count(bool flag, int *warp_sums, int &total) {
+// Exclusive prefix sum of `v` over the block in thread order, and the total.
+__device__ __forceinline__ int block_excl_sum(int v, int *warp_sums, int &total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const unsigned m = __ballot_sync(0xffffffffu, flag);
-    const int in_warp = __popc(m & ((1u << lane) - 1u));
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += t;
+    }
     __syncthreads();  // warp_sums free (a previous call has read it)
-    if (lane == 0) warp_sums[warp] = __popc(m);
+    if (lane == 31) warp_sums[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        const int v = lane < kSelectThreads / 32 ? warp_sums[lane] : 0;
-        int incl = v;
+        const int w = lane < kSelectThreads / 32 ? warp_sums[lane] : 0;
+        int wi = w;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            const int t = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += t;
+            const int t = __shfl_up_sync(0xffffffffu, wi, off);
+            if (lane >= off) wi += t;
         }
-        if (lane < kSelectThreads / 32) warp_sums[lane] = incl - v;  // exclusive
-        if (lane == 31) warp_sums[kSelectThreads / 32] = incl;
+        if (lane < kSelectThreads / 32) warp_sums[lane] = wi - w;  // exclusive
+        if (lane == 31) warp_sums[kSelectThreads / 32] = wi;
     }
     __syncthreads();
     total = warp_sums[kSelectThreads / 32];
-    return warp_sums[warp] + in_warp;
+    return warp_sums[warp] + incl - v;
 }
+
+constexpr int kSelectRows = 8;   // consecutive rows per thread in the ordered scans
+constexpr int kSelectLoads = 8;  // strided loads in flight per thread in the histogram passes
 
 __global__ void __launch_bounds__(kSelectThreads) born_select_kernel(BornArgs a, BornTable t) {
     __shared__ uint32_t hist[256];
@@ -105,9 +114,20 @@ __global__ void __launch_bounds__(kSelectThreads) born_select_kernel(BornArgs a,
         for (int shift = 24; shift >= 0; shift -= 8) {
             for (int d = tid; d < 256; d += kSelectThreads) hist[d] = 0;
             __syncthreads();
-            for (int p = sink_n + tid; p < hi; p += kSelectThreads) {
-                const uint32_t k = mass_key(imp[p]);
-                if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1u);
+            // kSelectLoads loads in flight per thread before any is used
+            for (int p0 = sink_n; p0 < hi; p0 += kSelectThreads * kSelectLoads) {
+                float m[kSelectLoads];
+#pragma unroll
+                for (int u = 0; u < kSelectLoads; ++u) {
+                    const int p = p0 + u * kSelectThreads + tid;
+                    m[u] = p < hi ? imp[p] : 0.0f;
+                }
+#pragma unroll
+                for (int u = 0; u < kSelectLoads; ++u) {
+                    const uint32_t k = mass_key(m[u]);
+                    if (p0 + u * kSelectThreads + tid < hi && (k & mask) == prefix)
+                        atomicAdd(&hist[(k >> shift) & 255u], 1u);
+                }
             }
             __syncthreads();
             if (tid == 0) {
@@ -127,24 +147,50 @@ __global__ void __launch_bounds__(kSelectThreads) born_select_kernel(BornArgs a,
     }
     // prefix = the threshold key; `need` rows equal to it are kept, lowest first
 
-    // ---- keep flags -> ascending list of kept rows
+    // ---- keep flags -> ascending list of kept rows (kSelectRows consecutive
+    // rows per thread, in thread order)
     int eq_carry = 0, out_carry = 0;
-    for (int p0 = 0; p0 < stored; p0 += kSelectThreads) {
-        const int p = p0 + tid;
-        bool mid_gt = false, mid_eq = false;
-        if (budget > 0 && p >= sink_n && p < hi) {
-            const uint32_t k = mass_key(imp[p]);
-            mid_gt = k > prefix;
-            mid_eq = k == prefix;
+    for (int p0 = 0; p0 < stored; p0 += kSelectThreads * kSelectRows) {
+        const int pb = p0 + tid * kSelectRows;
+        bool mid_gt[kSelectRows], mid_eq[kSelectRows];
+        float mv[kSelectRows];
+#pragma unroll
+        for (int u = 0; u < kSelectRows; ++u) {
+            const int p = pb + u;
+            mv[u] = (budget > 0 && p >= sink_n && p < hi) ? imp[p] : 0.0f;
+        }
+        int n_eq = 0;
+#pragma unroll
+        for (int u = 0; u < kSelectRows; ++u) {
+            const int p = pb + u;
+            mid_gt[u] = mid_eq[u] = false;
+            if (budget > 0 && p >= sink_n && p < hi) {
+                const uint32_t k = mass_key(mv[u]);
+                mid_gt[u] = k > prefix;
+                mid_eq[u] = k == prefix;
+            }
+            n_eq += mid_eq[u];
         }
         int eq_total;
-        const int eq_rank = eq_carry + block_excl_count(mid_eq, warp_sums, eq_total);
+        int eq_rank = eq_carry + block_excl_sum(n_eq, warp_sums, eq_total);
         eq_carry += eq_total;
-        const bool keep = p < stored && (p < sink_n || p >= hi || mid_gt || (mid_eq && eq_rank < need));
+        bool keep[kSelectRows];
+        int n_keep = 0;
+#pragma unroll
+        for (int u = 0; u < kSelectRows; ++u) {
+            const int p = pb + u;
+            keep[u] = p < stored && (p < sink_n || p >= hi || mid_gt[u] || (mid_eq[u] && eq_rank < need));
+            eq_rank += mid_eq[u];
+            n_keep += keep[u];
+        }
         int out_total;
-        const int pos = out_carry + block_excl_count(keep, warp_sums, out_total);
+        int pos = out_carry + block_excl_sum(n_keep, warp_sums, out_total);
         out_carry += out_total;
-        if (keep && pos < keep_last) idx[pos] = p;
+#pragma unroll
+        for (int u = 0; u < kSelectRows; ++u) {
+            if (keep[u] && pos < keep_last) idx[pos] = pb + u;
+            pos += keep[u];
+        }
     }
     __syncthreads();
     if (out_carry != keep_last) {
@@ -158,16 +204,30 @@ __global__ void __launch_bounds__(kSelectThreads) born_select_kernel(BornArgs a,
     // ---- imp follows its rows (in place, tiles in order); the entries of the
     // dropped rows are cleared: a row appended there later starts from zero
     // mass, as each appended row does on the page
-    for (int j0 = sink_n; j0 < keep_last; j0 += kSelectThreads) {
-        const int j = j0 + tid;
-        float v = 0.0f;
-        if (j < keep_last) v = imp[idx[j]];
+    for (int j0 = sink_n; j0 < keep_last; j0 += kSelectThreads * kSelectLoads) {
+        float v[kSelectLoads];
+#pragma unroll
+        for (int u = 0; u < kSelectLoads; ++u) {
+            const int j = j0 + u * kSelectThreads + tid;
+            v[u] = j < keep_last ? imp[idx[j]] : 0.0f;
+        }
         __syncthreads();
-        if (j < keep_last) imp[j] = v;
+#pragma unroll
+        for (int u = 0; u < kSelectLoads; ++u) {
+            const int j = j0 + u * kSelectThreads + tid;
+            if (j < keep_last) imp[j] = v[u];
+        }
         __syncthreads();
     }
     for (int j = keep_last + tid; j < stored; j += kSelectThreads) imp[j] = 0.0f;
     if (tid == 0) a.seq_len[b] = keep_last;
+}
+
+// log2 of a power of two.
+__host__ __device__ __forceinline__ int log2_exact(int x) {
+    int l = 0;
+    while ((1 << l) < x) ++l;
+    return l;
 }
 
 struct GatherStorage {
@@ -190,6 +250,7 @@ struct GatherArgs {
 template <typename U>
 __device__ void gather_region(U *region, int upr, const int32_t *kept, int sink_n, int keep_last,
                               int64_t cap, uint32_t *err) {
+    const int lu = log2_exact(upr);  // upr is a power of two
     const int tile_rows = max(1, kGatherThreads * kGatherUnits / upr);
     for (int j0 = sink_n; j0 < keep_last; j0 += tile_rows) {
         const int rows = min(tile_rows, keep_last - j0);
@@ -201,8 +262,8 @@ __device__ void gather_region(U *region, int upr, const int32_t *kept, int sink_
         for (int k = 0; k < kGatherUnits; ++k) {
             const int e = threadIdx.x + k * kGatherThreads;
             if (e < units) {
-                const int32_t src = kept[j0 + e / upr];
-                if (src >= 0 && src < cap) r[k] = region[int64_t(src) * upr + e % upr];
+                const int32_t src = kept[j0 + (e >> lu)];
+                if (src >= 0 && src < cap) r[k] = region[(int64_t(src) << lu) + (e & (upr - 1))];
                 else set_error(err, kErrBounds);
             }
         }
@@ -210,10 +271,60 @@ __device__ void gather_region(U *region, int upr, const int32_t *kept, int sink_
 #pragma unroll
         for (int k = 0; k < kGatherUnits; ++k) {
             const int e = threadIdx.x + k * kGatherThreads;
-            if (e < units) region[int64_t(j0 + e / upr) * upr + e % upr] = r[k];
+            if (e < units) region[(int64_t(j0 + (e >> lu)) << lu) + (e & (upr - 1))] = r[k];
         }
         __syncthreads();
     }
+}
+
+// Batched gather: rows j in [j0, j1) of every region (blockIdx.y = live head
+// x storage, blockIdx.z = table entry), through the workspace copy `stage`
+// laid out [entry][live head][storage block of (j1 - j0) rows, padded to 16
+// bytes].  to_stage: read the kept sources into it; else write it to rows j.
+struct BatchArgs {
+    GatherArgs g;
+    char *stage;
+    int64_t stage_group;   // bytes of one (entry, live head) block, a multiple of 16
+    int64_t st_off[4];     // byte offset of each storage's block in it, multiples of 16
+    int32_t n_live, j0, j1;
+};
+
+// Rows are a power-of-two number of units U (16-byte units where the row
+// holds whole ones, else 4-byte words), so row and unit come from shifts.
+template <bool TO_STAGE, typename U>
+__device__ __forceinline__ void batch_copy(U *region, U *stage, int lu, const int32_t *kept, int j0, int rows,
+                                           int64_t cap, uint32_t *err) {
+    const int n = rows << lu;
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < n; e += gridDim.x * blockDim.x) {
+        const int j = j0 + (e >> lu), w = e & ((1 << lu) - 1);
+        if (TO_STAGE) {
+            const int32_t src = kept[j];
+            if (src >= 0 && src < cap) stage[e] = region[(int64_t(src) << lu) + w];
+            else set_error(err, kErrBounds);
+        } else {
+            region[(int64_t(j) << lu) + w] = stage[e];
+        }
+    }
+}
+
+template <bool TO_STAGE>
+__global__ void __launch_bounds__(kGatherThreads) born_batch_kernel(BatchArgs a, BornTable t) {
+    const int i = blockIdx.z;
+    if (i >= t.n) return;
+    const int s = blockIdx.y % a.g.n_st, gl = blockIdx.y / a.g.n_st;
+    const int b = t.seq[i];
+    const GatherStorage g = a.g.st[s];
+    const int64_t cap = a.g.cap[b];
+    char *region = g.base + (a.g.row_base[b] + int64_t(gl) * cap) * g.row_bytes;
+    char *stage = a.stage + (int64_t(i) * a.n_live + gl) * a.stage_group + a.st_off[s];
+    const int32_t *kept = a.g.idx + int64_t(i) * a.g.keep_last;
+    const int rows = a.j1 - a.j0;
+    if (g.row_bytes % 16 == 0)
+        batch_copy<TO_STAGE>(reinterpret_cast<uint4 *>(region), reinterpret_cast<uint4 *>(stage),
+                             log2_exact(g.row_bytes / 16), kept, a.j0, rows, cap, a.g.err);
+    else
+        batch_copy<TO_STAGE>(reinterpret_cast<uint32_t *>(region), reinterpret_cast<uint32_t *>(stage),
+                             log2_exact(g.row_bytes / 4), kept, a.j0, rows, cap, a.g.err);
 }
 
 __global__ void __launch_bounds__(kGatherThreads) born_gather_kernel(GatherArgs a, BornTable t) {
@@ -253,8 +364,26 @@ __global__ void truncate_kernel(int32_t *seq_len, float *imp, TruncTable t) {
     if (threadIdx.x == 0) seq_len[t.seq[i]] = t.new_len[i];
 }
 
-int64_t evict_ws_bytes(const Layer *l, int64_t keep_last) {
+constexpr int64_t kEvictStage = int64_t(64) << 20;  // most bytes of the batched gather's copy
+constexpr int kSerialRegions = 2 * 152;               // enough regions to walk each in one CTA
+
+// Bytes per row summed over the layer's storages.
+int64_t row_bytes_all(const Layer *l) {
+    const bool qk = l->mode == KVD_Q8 || l->mode == KVD_Q8K;
+    const bool qv = l->mode == KVD_Q8 || l->mode == KVD_Q8V;
+    return (qk ? l->hd + (l->hd / 32) * 4 : l->hd * 4) + (qv ? l->hd + 4 : l->hd * 4);
+}
+
+int64_t ceil_div_ev(int64_t x, int64_t y) { return (x + y - 1) / y; }
+
+int64_t evict_idx_bytes(const Layer *l, int64_t keep_last) {
     return (int64_t(std::min(kSlice, l->n_seq)) * keep_last * 4 + 255) / 256 * 256;
+}
+
+int64_t evict_ws_bytes(const Layer *l, int64_t keep_last) {
+    const int64_t stage = std::min(kEvictStage, int64_t(std::min(kSlice, l->n_seq)) * std::max(1, l->n_live) *
+                                                    keep_last * row_bytes_all(l));
+    return evict_idx_bytes(l, keep_last) + (stage + 255) / 256 * 256;
 }
 
 }  // namespace
@@ -286,7 +415,7 @@ extern "C" kvd_status kv_evict_born(kvd_layer *L, float *imp, int64_t keep_last,
     cudaStream_t st = as_stream(stream);
     BornArgs a;
     a.imp = imp;
-    a.idx = static_cast<int32_t *>(workspace);
+    a.idx = static_cast<int32_t *>(workspace);  // the stage of the batched gather follows the lists
     a.seq_len = l->d_seq_len;
     a.err = l->d_err;
     a.keep_last = int32_t(keep_last);
@@ -328,9 +457,36 @@ extern "C" kvd_status kv_evict_born(kvd_layer *L, float *imp, int64_t keep_last,
         }
         born_select_kernel<<<unsigned(t.n), kSelectThreads, 0, st>>>(a, t);
         if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
-        if (l->n_live > 0 && g.n_st > 0 && keep_last > a.sink_n) {
+        if (l->n_live <= 0 || g.n_st <= 0 || keep_last <= a.sink_n) continue;
+        const int64_t regions = int64_t(t.n) * l->n_live * g.n_st;
+        const int64_t stage_bytes = workspace_bytes - evict_idx_bytes(l, keep_last);
+        const int64_t per_row = int64_t(t.n) * l->n_live * row_bytes_all(l);  // one j across the batch
+        const int64_t pad = int64_t(t.n) * l->n_live * g.n_st * 16;            // blocks padded to 16 bytes
+        const int64_t batch = (stage_bytes - pad) / per_row;
+        if (regions >= kSerialRegions || batch < 1) {
             dim3 grid(unsigned(l->n_live * g.n_st), unsigned(t.n));
             born_gather_kernel<<<grid, kGatherThreads, 0, st>>>(g, t);
+            if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
+            continue;
+        }
+        BatchArgs ba;
+        ba.g = g;
+        ba.stage = static_cast<char *>(workspace) + evict_idx_bytes(l, keep_last);
+        ba.n_live = l->n_live;
+        for (int64_t j0 = a.sink_n; j0 < keep_last; j0 += batch) {
+            ba.j0 = int32_t(j0);
+            ba.j1 = int32_t(std::min<int64_t>(keep_last, j0 + batch));
+            int64_t off = 0;
+            for (int k = 0; k < g.n_st; ++k) {
+                ba.st_off[k] = off;
+                off += (int64_t(ba.j1 - ba.j0) * g.st[k].row_bytes + 15) / 16 * 16;
+            }
+            ba.stage_group = off;
+            const int64_t units = int64_t(ba.j1 - ba.j0) * 8;  // a code region's 16-byte units, for the grid
+            dim3 grid(unsigned(std::max<int64_t>(1, std::min<int64_t>(ceil_div_ev(units, kGatherThreads), 1024))),
+                      unsigned(l->n_live * g.n_st), unsigned(t.n));
+            born_batch_kernel<true><<<grid, kGatherThreads, 0, st>>>(ba, t);
+            born_batch_kernel<false><<<grid, kGatherThreads, 0, st>>>(ba, t);
             if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
         }
     }

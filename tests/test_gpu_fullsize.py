@@ -227,3 +227,47 @@ def test_rswa_i8_steady_full_size(env):
         assert err <= OUT_TOL, (s, err)
     del wl, c
     torch.cuda.empty_cache()
+
+
+def test_born_eviction_long_full_size(env):
+    """Born eviction at full size: 4 seq x 131072 rows (q8_2f, 16 heads per group)
+    cut to 65536 rows with seeded masses full of ties; one sampled group's codes,
+    scales and imp bit-exact against the oracle's evict_born, then its decode."""
+    torch, kvd, W = env
+    wl = W.long_q8(extra_cap=64)
+    rng = np.random.default_rng(4242)
+    masses = (rng.integers(0, 64, size=wl.layer.imp_len) / 16.0).astype(np.float32)
+    imp = torch.from_numpy(masses.copy()).cuda()
+    keep, sink, recent = 65536, 4, 8192
+    ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev[0].record()
+    kvd.kv_evict_born(wl.layer, imp, keep, sink, recent)
+    ev[1].record()
+    torch.cuda.synchronize()
+    print("kv_evict_born 4 x 131072 -> 65536 rows: %.1f us" % (ev[0].elapsed_time(ev[1]) * 1e3))
+    assert wl.layer.device_error() == 0
+    b, h = 2, 1
+    oc, _ = _oracle_seq(wl, b, [h])
+    L = int(wl.lengths[b])
+    ib = int(wl.layer.imp_base[b])
+    o_imp = np.zeros(oc.cap, np.float32)
+    o_imp[:L] = masses[ib:ib + L]
+    assert oc.evict_born(keep, sink, recent, o_imp) == keep
+    got = imp.cpu().numpy()
+    assert np.array_equal(got[ib:ib + L].view(np.uint32), o_imp[:L].view(np.uint32))
+    assert all(wl.layer.seq_len(s) == keep for s in range(wl.n_seq))
+    from kv_cache_decode_attention_gb300 import _abi
+
+    r0, _ = wl.layer.region(b, h)
+    for slot, arr in ((_abi.BUF_KQ, oc.kq), (_abi.BUF_VQ, oc.vq)):
+        assert np.array_equal(wl.layer.component(slot)[r0:r0 + keep].cpu().numpy(), arr[0, :keep])
+    for slot, arr in ((_abi.BUF_KS, oc.ks), (_abi.BUF_VS, oc.vs)):
+        assert np.array_equal(wl.layer.component(slot)[r0:r0 + keep].cpu().numpy().view(np.uint32),
+                              arr[0, :keep].view(np.uint32))
+    q = wl.query(0)
+    out = kvd.decode_attention(q, wl.layer, scale=wl.scale).cpu().numpy()
+    qg = q.cpu().numpy()[b, h * wl.hpk:(h + 1) * wl.hpk]
+    ref = oc.decode(qg, wl.hpk, np.float32(wl.scale))
+    assert out_error(out[b, h * wl.hpk:(h + 1) * wl.hpk], ref) <= OUT_TOL
+    del wl
+    torch.cuda.empty_cache()
