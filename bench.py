@@ -185,11 +185,11 @@ class RswaOracleSample:
     generators (its reference rows and the ring rows of its 500 writes), ready
     for the CPU oracle's decode (f32 regions, or their int8 mirror)."""
 
-    def __init__(self, wl, int8: bool, s: int = 0):
+    def __init__(self, wl, int8: bool, s: int = 0, verify_k: int = 0):
         import oracle
 
         c = wl.cache
-        self.int8, self.H, self.hd = int8, c.H, c.head_dim
+        self.int8, self.H, self.hd, self.verify_k = int8, c.H, c.head_dim, verify_k
         pk, pv = wl.prefill_rows(s)
         self.ref_k, self.ref_v = pk.cpu().numpy(), pv.cpu().numpy()
         self.ring_k = np.zeros((c.H, c.W, c.head_dim), np.float32)
@@ -199,18 +199,29 @@ class RswaOracleSample:
             k, v = wl.step_rows(t)
             oracle.rswa_write(self.ring_k, self.ring_v, k[s].cpu().numpy(), v[s].cpu().numpy(), True, cur)
         self.prefill, self.ring_len = wl.prefill, int(cur[0])
+        self.cursors = cur
         self.q = wl.query(10_000)[s].cpu().numpy()
+        if verify_k:
+            import synthetic
+
+            shp = (verify_k, c.H, c.head_dim)
+            self.vq, self.vk, self.vv = (synthetic.normal(shp, 90_000 + i) for i in range(3))
         if int8:
             self.mir = [oracle.rswa_mirror(x) for x in (self.ref_k, self.ref_v, self.ring_k, self.ring_v)]
         self.rows = self.prefill + self.ring_len
         from kv_cache_decode_attention_gb300 import workloads as W
 
         self.bytes = (W.rswa_i8_bytes if int8 else W.rswa_bytes)(1, c.H, c.head_dim, [self.rows])
+        if verify_k:
+            self.bytes += 2 * verify_k * c.H * c.head_dim * 4 + 2 * (verify_k - 1) * c.H * c.head_dim * 4
 
     def decode(self):
         import oracle
 
         scale = np.float32(1.0 / math.sqrt(self.hd))
+        if self.verify_k:
+            return oracle.rswa_verify(self.vq, self.vk, self.vv, self.ref_k, self.ref_v, self.prefill, self.ring_k,
+                                      self.ring_v, self.cursors, scale, int8=self.int8)
         if self.int8:
             (rk, rks), (rv, rvs), (gk, gks), (gv, gvs) = self.mir
             return oracle.rswa_decode_i8(self.q, rk, rks, rv, rvs, self.prefill, gk, gks, gv, gvs,
@@ -230,8 +241,9 @@ class RswaOracleSample:
         return self.bytes / per / 1e9, per
 
     def describe(self, wl):
-        return "1 of %d streams (all %d heads, %d rows), %s, f64 softmax" % (
-            wl.cache.B, self.H, self.rows, "int8 mirror" if self.int8 else "f32 regions")
+        return "1 of %d streams (all %d heads, %d rows%s), %s, f64 softmax" % (
+            wl.cache.B, self.H, self.rows, ", %d draft queries" % self.verify_k if self.verify_k else "",
+            "int8 mirror" if self.int8 else "f32 regions")
 
 
 def run_reference(args, rank):
@@ -248,11 +260,34 @@ def run_reference(args, rank):
         print(json.dumps({"impl": "reference", "unavailable": "needs the GPU box to build the workload"}))
         return
     if args.workload in RSWA_WORKLOADS:
-        wl = W.rswa_steady(B=args.rswa_streams, int8=args.workload == "rswa_i8")
-        smp = RswaOracleSample(wl, args.workload == "rswa_i8")
+        int8, verify = args.workload.startswith("rswa_i8"), args.workload.endswith("_verify")
+        wl = W.rswa_steady(B=args.rswa_streams, int8=int8)
+        smp = RswaOracleSample(wl, int8, verify_k=VERIFY_DRAFTS if verify else 0)
         smp.gbs(0.0, max_reps=max(1, args.warmup))
         gbs, per = smp.gbs(0.0, max_reps=args.steps)
         sample, name = smp.describe(wl), args.workload + "_steady"
+    elif args.workload == "verify_q8":
+        import oracle
+        import synthetic
+
+        K = VERIFY_DRAFTS
+        wl = W.q8_gqa(extra_cap=64)
+        k, v = wl.rows(0)
+        oc = oracle.OracleSeqCache(wl.mode, wl.n_kv, wl.hd, int(wl.lengths[0]) + K, alive=wl.alive)
+        oc.append_rows(k.cpu().numpy(), v.cpu().numpy())
+        oc.append_rows(synthetic.normal((K, wl.n_kv, wl.hd), 91_000), synthetic.normal((K, wl.n_kv, wl.hd), 91_001))
+        q0 = synthetic.normal((K, wl.n_q, wl.hd), 91_002)
+        one = W.decode_bytes(wl.mode, int(wl.alive.sum()), wl.hd, wl.n_q, wl.lengths[:1] + K, False, 1)
+        for _ in range(max(1, args.warmup)):
+            oc.decode_verify(q0, wl.n_q, K, np.float32(wl.scale))
+        a0 = time.perf_counter()
+        for _ in range(args.steps):
+            oc.decode_verify(q0, wl.n_q, K, np.float32(wl.scale))
+        per = (time.perf_counter() - a0) / args.steps
+        gbs = one / per / 1e9
+        sample = "1 of %d sequences (%d drafts x %d query heads x %d rows), f64" % (
+            wl.n_seq, K, wl.n_q, int(wl.lengths[0]) + K)
+        name = "verify_q8_gqa"
     else:
         wl = build_workload(args.workload, replicas=1)[0]
         # warm-up and timed steps: one oracle decode of the sampled sequence each
@@ -278,7 +313,8 @@ def run_reference(args, rank):
 
 # ------------------------------------------------------------------ GPU arm
 
-RSWA_WORKLOADS = ("rswa", "rswa_i8")
+RSWA_WORKLOADS = ("rswa", "rswa_i8", "rswa_verify", "rswa_i8_verify")
+VERIFY_DRAFTS = 4  # draft tokens per speculative step in the verify workloads
 
 
 def packed_inputs(torch, parts_per_step):
@@ -305,30 +341,53 @@ def run_gpu_rswa(args, rank, world):
     from kv_cache_decode_attention_gb300 import replicas
     from kv_cache_decode_attention_gb300 import workloads as W
 
-    int8 = args.workload == "rswa_i8"
+    int8 = args.workload.startswith("rswa_i8")
+    verify = args.workload.endswith("_verify")
+    K = VERIFY_DRAFTS
     dev = torch.device("cuda", replicas.rank_info().local_rank)
     torch.cuda.set_device(dev)
     wl = W.rswa_steady(B=args.rswa_streams, int8=int8)
     c = wl.cache
-    decode = kvd.rswa_decode_i8 if int8 else kvd.rswa_decode
+    if verify:
+        # speculative step: verify K drafts per stream (read-only), then write the
+        # accepted token; qs hold the drafts' queries, news their K / V rows
+        def decode(q, cache, out=None):
+            return kvd.rswa_verify(q, dks[cur_i[0] % 8], dvs[cur_i[0] % 8], cache, int8=int8, out=out)
+    else:
+        decode = kvd.rswa_decode_i8 if int8 else kvd.rswa_decode
     B, H, hd = c.B, c.H, c.head_dim
     lengths = c.prefill_len + c.ring_len  # steady state: constant over the steps
     dec_bytes = (W.rswa_i8_bytes if int8 else W.rswa_bytes)(B, H, hd, lengths)
     # ring write: read k, v; write the f32 rows (+ codes and scales with the mirror)
     wr_bytes = B * H * hd * 4 * 4 + (B * H * (2 * hd + 8) if int8 else 0)
-    qs = [wl.query(i, dev) for i in range(8)]
+    if verify:
+        import synthetic
+
+        qs = [synthetic.torch_normal((B, K, H, hd), 70_000 + i, dev) for i in range(8)]
+        dks = [synthetic.torch_normal((B, K, H, hd), 71_000 + i, dev) for i in range(8)]
+        dvs = [synthetic.torch_normal((B, K, H, hd), 72_000 + i, dev) for i in range(8)]
+        out = torch.empty(B, K, H * hd, device=dev)
+        # the drafts are read once per step; the verify writes K outputs per stream
+        dec_bytes += 2 * B * K * H * hd * 4 + 2 * B * (K - 1) * H * hd * 4
+    else:
+        qs = [wl.query(i, dev) for i in range(8)]
+        out = torch.empty(B, H * hd, device=dev)
     news = [wl.step_rows(wl.steps + i, dev) for i in range(8)]
-    out = torch.empty(B, H * hd, device=dev)
     stream = torch.cuda.current_stream()
+    cur_i = [0]
 
     def step(i, with_events=None):
         k, v = news[i % 8]
-        kvd.rswa_ring_write(c, k, v)
+        cur_i[0] = i
+        if not verify:
+            kvd.rswa_ring_write(c, k, v)
         if with_events is not None:
             with_events[0].record(stream)
         decode(qs[i % 8], c, out=out)
         if with_events is not None:
             with_events[1].record(stream)
+        if verify:
+            kvd.rswa_ring_write(c, k, v)  # the accepted token
 
     for i in range(args.warmup):
         step(i)
@@ -361,6 +420,7 @@ def run_gpu_rswa(args, rank, world):
     dev_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nrep)]
     torch.cuda.profiler.start()
     for j in range(nrep):
+        cur_i[0] = j
         dev_ev[j][0].record(stream)
         decode(qs[j % 8], c, out=out)
         dev_ev[j][1].record(stream)
@@ -371,13 +431,17 @@ def run_gpu_rswa(args, rank, world):
     achieved = dec_bytes / (k_ms * 1e-3) / 1e9
 
     pinned, stage, (dq, dk, dv) = packed_inputs(torch, [(qs[i], news[i][0], news[i][1]) for i in range(8)])
-    pin_out = torch.empty(B, H * hd).pin_memory()
+    pin_out = torch.empty(out.shape).pin_memory()
     torch.cuda.synchronize()
     a0 = time.perf_counter()
     for j in range(args.steps):
         stage.copy_(pinned[j % 8], non_blocking=True)
-        kvd.rswa_ring_write(c, dk, dv)
+        cur_i[0] = j
+        if not verify:
+            kvd.rswa_ring_write(c, dk, dv)
         decode(dq, c, out=out)
+        if verify:
+            kvd.rswa_ring_write(c, dk, dv)
         pin_out.copy_(out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
     a1 = time.perf_counter()
@@ -390,7 +454,7 @@ def run_gpu_rswa(args, rank, world):
         return
     cpu = None
     if not args.no_cpu_baseline:
-        smp = RswaOracleSample(wl, int8)
+        smp = RswaOracleSample(wl, int8, verify_k=K if verify else 0)
         v, per = smp.gbs(args.cpu_seconds)
         cpu = {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                "sample": smp.describe(wl) + ", %.1f s" % args.cpu_seconds}
@@ -401,12 +465,14 @@ def run_gpu_rswa(args, rank, world):
         "dtype": "i8" if int8 else "f32", "data": "synthetic",
         "config": {"workload": args.workload + "_steady", "streams": B, "heads": H, "head_dim": hd,
                    "reference_rows": int(wl.prefill), "ring_rows": int(c.W),
-                   "step": "rswa ring write 1 token/stream + decode of every stream",
+                   "step": ("rswa verify of %d drafts/stream (read-only) + ring write of the accepted token" % K
+                            if verify else "rswa ring write 1 token/stream + decode of every stream"),
                    "l2": "inputs larger than L2 (%.2f GB read per decode)" % (dec_bytes / 1e9),
                    "parallelism": "replicas" if world > 1 else "single"},
         "fraction_of_peak": round(gbs / world / peak, 4),
         "queries_per_s": round(B * world / (ms_per_step * 1e-3), 1),
-        "roofline": {"bound": "hbm", "kernel": "rswa decode (split + merge)",
+        "roofline": {"bound": "hbm", "kernel": "rswa verify (split + tail + merge)" if verify
+                     else "rswa decode (split + merge)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": measured_traffic(args.workload),
                      "peak_kind": peak_kind, "ms_per_launch": round(k_ms, 5),
@@ -414,7 +480,150 @@ def run_gpu_rswa(args, rank, world):
         "decode_ms_in_step": round(statistics.mean(dec_ms), 5),
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps * 3,
+        "gpu_launches": args.steps * (4 if verify else 3),
+        "clocks": sampler.summary(c0, c1),
+    }
+    if verify:
+        line["queries_per_s"] = round(B * K * world / (ms_per_step * 1e-3), 1)
+    print(json.dumps(line), flush=True)
+
+
+def run_gpu_verify(args, rank, world):
+    """q8_gqa speculative step: append VERIFY_DRAFTS draft rows per sequence, verify
+    them in one query-batched call (causal among the drafts), reject them all
+    (kv_truncate_last) so the cache length stays steady."""
+    import torch
+
+    import kv_cache_decode_attention_gb300 as kvd
+    from kv_cache_decode_attention_gb300 import replicas
+    from kv_cache_decode_attention_gb300 import workloads as W
+    import synthetic
+
+    K = VERIFY_DRAFTS
+    dev = torch.device("cuda", replicas.rank_info().local_rank)
+    torch.cuda.set_device(dev)
+    probe = W.q8_gqa(extra_cap=64)
+    n_live = int(probe.alive.sum())
+    bytes_each = W.decode_bytes(probe.mode, n_live, probe.hd, probe.n_q, probe.lengths + K, False, probe.n_seq)
+    R = max(1, min(8, math.ceil(4 * L2_BYTES / bytes_each)))
+    wls = [probe] + [W.q8_gqa(extra_cap=64) for _ in range(R - 1)]
+    n_seq, n_q, n_kv, hd = probe.n_seq, probe.n_q, probe.n_kv, probe.hd
+    qs = [synthetic.torch_normal((n_seq, K, n_q, hd), 80_000 + i, dev) for i in range(8)]
+    drafts = [(synthetic.torch_normal((n_seq * K, n_kv, hd), 81_000 + i, dev),
+               synthetic.torch_normal((n_seq * K, n_kv, hd), 82_000 + i, dev)) for i in range(8)]
+    nn = np.full(n_seq, K, np.int32)
+    out = torch.empty(n_seq, K, n_q, hd, device=dev)
+    import ctypes as C
+
+    from kv_cache_decode_attention_gb300 import _abi
+
+    nb = C.c_int64(0)
+    _abi.call("kvd_verify_workspace_bytes", C.byref(probe.layer.L), n_q, K, C.byref(nb))
+    ws = torch.empty(int(nb.value), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i, with_events=None):
+        w = wls[i % R]
+        kvd.kv_append(w.layer, drafts[i % 8][0], drafts[i % 8][1], nn)
+        if with_events is not None:
+            with_events[0].record(stream)
+        kvd.decode_attention_verify(qs[i % 8], w.layer, K, out=out, scale=w.scale, workspace=ws)
+        if with_events is not None:
+            with_events[1].record(stream)
+        kvd.kv_truncate_last(w.layer, K)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sampler = ClockSampler(dev.index)
+    with sampler:
+        time.sleep(0.3)
+        replicas.barrier()
+        torch.cuda.synchronize()
+        c0 = time.time()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.profiler.start()
+        t0.record(stream)
+        for j in range(args.steps):
+            step(args.warmup + j, ev[j])
+        t1.record(stream)
+        torch.cuda.synchronize()
+        torch.cuda.profiler.stop()
+        replicas.barrier()
+        c1 = time.time()
+        time.sleep(0.1)
+    elapsed_ms = replicas.max_over_ranks(t0.elapsed_time(t1))
+    ms_per_step = elapsed_ms / args.steps
+    # per step: K appended rows per sequence, the verify's read of every cached row
+    # (the drafts included), its K queries and outputs
+    step_bytes = K * W.append_bytes(probe.mode, n_live, hd, n_seq) + bytes_each + 2 * n_seq * (K - 1) * n_q * hd * 4
+    gbs = replicas.whole_job_rate(step_bytes * args.steps, elapsed_ms * 1e-3, world) / 1e9
+    ver_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    achieved = (bytes_each + 2 * n_seq * (K - 1) * n_q * hd * 4) / (ver_ms * 1e-3) / 1e9
+    peak, peak_kind = peaks()
+    # end to end: the step's queries and drafts copied in (one pinned buffer),
+    # the K outputs copied out, every step
+    pinned, stage, (dq, ddk, ddv) = packed_inputs(torch, [(qs[i], drafts[i][0], drafts[i][1]) for i in range(8)])
+    pin_out = torch.empty(out.shape).pin_memory()
+    torch.cuda.synchronize()
+    a0 = time.perf_counter()
+    for j in range(args.steps):
+        w = wls[j % R]
+        stage.copy_(pinned[j % 8], non_blocking=True)
+        kvd.kv_append(w.layer, ddk, ddv, nn)
+        kvd.decode_attention_verify(dq, w.layer, K, out=out, scale=w.scale, workspace=ws)
+        kvd.kv_truncate_last(w.layer, K)
+        pin_out.copy_(out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    a1 = time.perf_counter()
+    e2e = {"value": round(step_bytes * args.steps / (a1 - a0) / 1e9 * world, 2), "unit": "GB/s",
+           "h2d_bytes_per_step": int(stage.numel() * 4), "d2h_bytes_per_step": int(pin_out.numel() * 4)}
+    for w in wls:
+        if w.layer.device_error():
+            raise SystemExit("device error word set")
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+
+        k, v = probe.rows(0)
+        oc = oracle.OracleSeqCache(probe.mode, n_kv, hd, int(probe.lengths[0]) + K, alive=probe.alive)
+        oc.append_rows(k.cpu().numpy(), v.cpu().numpy())
+        dk = drafts[0][0].cpu().numpy().reshape(n_seq, K, n_kv, hd)[0]
+        dv = drafts[0][1].cpu().numpy().reshape(n_seq, K, n_kv, hd)[0]
+        oc.append_rows(dk, dv)
+        q0 = qs[0][0].cpu().numpy()
+        reps, a0 = 0, time.perf_counter()
+        while time.perf_counter() - a0 < args.cpu_seconds:
+            oc.decode_verify(q0, n_q, K, np.float32(probe.scale))
+            reps += 1
+        per = (time.perf_counter() - a0) / reps
+        one = W.decode_bytes(probe.mode, n_live, hd, n_q, probe.lengths[:1] + K, False, 1)
+        cpu = {"value": round(one / per / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": "1 of %d sequences (%d drafts x %d query heads x %d rows), f64, %.1f s" % (
+                   n_seq, K, n_q, int(probe.lengths[0]) + K, args.cpu_seconds)}
+    line = {
+        "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": "verify_q8_gqa", "mode": "q8_2f", "n_seq": n_seq,
+                   "cached_rows": int(probe.lengths[0]), "drafts": K, "n_q": n_q, "n_kv": n_kv, "head_dim": hd,
+                   "step": "kv_append %d drafts/seq + decode_attention_verify + kv_truncate_last %d" % (K, K),
+                   "replicas": R, "l2": "inputs larger than L2 (%d rotated cache replicas)" % R,
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "fraction_of_peak": round(gbs / world / peak, 4),
+        "queries_per_s": round(n_seq * K * world / (ms_per_step * 1e-3), 1),
+        "roofline": {"bound": "hbm", "kernel": "decode_attention_verify (split + merge)",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None, "peak_kind": peak_kind,
+                     "ms_per_launch": round(ver_ms, 5), "bytes_per_launch": int(bytes_each)},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps * 4,
         "clocks": sampler.summary(c0, c1),
     }
     print(json.dumps(line), flush=True)
@@ -613,7 +822,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="q8_gqa",
-                    choices=["q8_gqa", "long_q8", "tiny_f32", *RSWA_WORKLOADS])
+                    choices=["q8_gqa", "long_q8", "tiny_f32", "verify_q8", *RSWA_WORKLOADS])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--rswa-streams", type=int, default=16,
                     help="streams of the R-SWA workloads (16 = the measured configuration)")
@@ -641,6 +850,8 @@ def main():
     build()
     if args.workload in RSWA_WORKLOADS:
         run_gpu_rswa(args, rank, world)
+    elif args.workload == "verify_q8":
+        run_gpu_verify(args, rank, world)
     else:
         run_gpu(args, rank, world)
 
