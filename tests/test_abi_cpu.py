@@ -187,3 +187,43 @@ def test_rswa_checkpoint_rollback_contract(abi):
     assert L.rswa_checkpoint_take(cid, p(pl), p(rl), p(rp), hist, 0, C.byref(cp5)) == abi.OK
     rl[0], rp[0], hist[0].decode_writes = 128, 1, 69
     assert L.rswa_rollback_to(cid, p(pl), p(rl), p(rp), hist, 0, W, C.byref(cp5)) == abi.ESTATE
+
+
+def test_rswa_verify_and_mirror_host_validation(abi):
+    """rswa_verify(_i8), the mirrored writers and the workspace sizes refuse bad
+    arguments on the host (nothing is launched or changed)."""
+    L = abi.lib()
+    B, H, hd, W, ref_cap = 2, 10, 128, 128, 64
+    p = lambda a: C.c_void_p(a.ctypes.data)
+    fake = C.c_void_p(1 << 20)  # never dereferenced
+    n = C.c_int64(0)
+    assert L.rswa_verify_workspace_bytes(B, H, hd, ref_cap, W, 4, C.byref(n)) == abi.OK and n.value > 0
+    n1 = C.c_int64(0)
+    assert L.rswa_verify_workspace_bytes(B, H, hd, ref_cap, W, 1, C.byref(n1)) == abi.OK and n1.value < n.value
+    for K in (0, 17):
+        assert L.rswa_verify_workspace_bytes(B, H, hd, ref_cap, W, K, C.byref(n1)) == abi.EINVAL
+    assert L.rswa_verify_workspace_bytes(B, H, 96, ref_cap, W, 4, C.byref(n1)) == abi.EINVAL
+    pl = np.array([-1, 5], np.int32)
+    rl = np.zeros(B, np.int32)
+    rp = np.zeros(B, np.int32)
+    ws = C.c_void_p(1 << 21)
+    args = (p(pl), p(rl), p(rp), B, H, hd, ref_cap, W, C.c_float(0.088), fake, ws, n.value, None)
+    # a stream without prefill: the verify would have to write into it
+    assert L.rswa_verify(fake, fake, fake, 4, fake, fake, fake, fake, *args) == abi.ESTATE
+    pl[0] = 3
+    assert L.rswa_verify(fake, fake, fake, 17, fake, fake, fake, fake, *args) == abi.EINVAL
+    assert L.rswa_verify(fake, None, fake, 4, fake, fake, fake, fake, *args) == abi.EINVAL
+    small = (p(pl), p(rl), p(rp), B, H, hd, ref_cap, W, C.c_float(0.088), fake, ws, 256, None)
+    assert L.rswa_verify(fake, fake, fake, 4, fake, fake, fake, fake, *small) == abi.EINVAL
+    # the int8 entry points need a complete, aligned mirror
+    assert L.rswa_verify_i8(fake, fake, fake, 4, None, *args) == abi.EINVAL
+    m = abi.rswa_i8_mirror(fake.value, fake.value, fake.value, fake.value, fake.value, fake.value, fake.value, None)
+    assert L.rswa_verify_i8(fake, fake, fake, 4, C.byref(m), *args) == abi.EINVAL
+    assert L.rswa_decode_i8(fake, C.byref(m), *args) == abi.EINVAL
+    hist = (abi.rswa_history * B)()
+    assert L.rswa_ring_write_i8(fake, fake, C.byref(m), fake, fake, p(pl), p(rl), p(rp), hist, B, H, hd, W,
+                                None, None) == abi.EINVAL
+    assert rl.tolist() == [0, 0] and hist[0].decode_writes == 0
+    assert L.rswa_record_prefill_i8(fake, fake, None, fake, fake, 0, 4, B, H, hd, ref_cap, W, p(pl), p(rl), p(rp),
+                                    hist, None) == abi.EINVAL
+    assert pl.tolist() == [3, 5] and hist[0].lineage_epoch == 0
