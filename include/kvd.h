@@ -167,7 +167,9 @@ KVD_API kvd_status decode_attention_verify(const float *q, const kvd_layer *L, i
  * mass.  Frozen fields are kept.  KVD_EINVAL for a negative count. */
 KVD_API kvd_status kv_truncate_last(kvd_layer *L, const int32_t *n_drop, float *imp, void *stream);
 
-/* Workspace bytes kv_evict_born needs for a given keep_last. */
+/* Workspace bytes kv_evict_born needs for a given keep_last: the kept-row
+ * lists plus, for layers with few (sequence, live head, storage) regions,
+ * up to 64 MiB of staging for the batched gather. */
 KVD_API kvd_status kv_evict_workspace_bytes(const kvd_layer *L, int64_t keep_last, int64_t *bytes_out);
 
 /* cortiq LayerKvCache::evict_born for every sequence of the layer holding
