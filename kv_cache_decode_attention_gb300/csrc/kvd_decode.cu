@@ -249,6 +249,121 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_runs_kernel(RunMergeAr
     }
 }
 
+// The same merge with one warp per (sequence, draft, query head), for units
+// with few runs: the warp loads the (max, sum, accumulator) of kHeadBatch
+// slots at once -- every lane the same maxima and sums, its own four channels
+// -- so a unit of up to kHeadBatch slots merges in one round of loads; longer
+// ranges go batch by batch under a running maximum.  Slots are taken in
+// order, so the result does not depend on timing.
+constexpr int kHeadWarps = 4;
+constexpr int kHeadBatch = 16;
+
+__global__ void __launch_bounds__(32 * kHeadWarps) merge_heads_kernel(RunMergeArgs a, MergeLayerSrc src) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = blockIdx.x * kHeadWarps + warp, b = blockIdx.y, k = blockIdx.z;
+    if (h >= a.n_q) return;
+    const int L = src.seq_len[b];
+    const int hg = a.K > 1 ? a.hg : a.hpk;
+    const int grp = src.slot[h / hg];
+    float4 res = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    float Mall = -INFINITY, sum = 0.0f;
+    if (grp >= 0 && L > 0) {
+        const int64_t unit = int64_t(b) * src.n_live + grp;
+        const int64_t first = a.unit_slots[2 * unit], last = a.unit_slots[2 * unit + 1];
+        const int hh = a.K > 1 ? k * hg + h % hg : h % a.hpk;  // the query's row in the partials
+        const float *pmh = a.pm + hh, *plh = a.pl + hh, *pah = a.pacc + int64_t(hh) * 128 + 4 * lane;
+        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        for (int64_t s0 = first; s0 <= last; s0 += kHeadBatch) {
+            float m[kHeadBatch], pl[kHeadBatch];
+            float4 v[kHeadBatch];
+#pragma unroll
+            for (int j = 0; j < kHeadBatch; ++j) {
+                const int64_t sl = s0 + j;
+                m[j] = -INFINITY;
+                if (sl <= last) {
+                    m[j] = pmh[sl * a.hpk];
+                    pl[j] = plh[sl * a.hpk];
+                    v[j] = *reinterpret_cast<const float4 *>(pah + sl * a.hpk * 128);
+                }
+            }
+            float bm = Mall;
+#pragma unroll
+            for (int j = 0; j < kHeadBatch; ++j) bm = fmaxf(bm, m[j]);
+            if (bm == -INFINITY) continue;  // only empty markers so far
+            const float r = exp2f(Mall - bm);  // 0 while Mall is -inf
+            sum *= r;
+            acc.x *= r;
+            acc.y *= r;
+            acc.z *= r;
+            acc.w *= r;
+            Mall = bm;
+#pragma unroll
+            for (int j = 0; j < kHeadBatch; ++j) {
+                if (m[j] == -INFINITY) continue;  // past the range, or an empty marker
+                const float f = exp2f(m[j] - Mall);
+                sum = fmaf(pl[j], f, sum);
+                acc.x = fmaf(v[j].x, f, acc.x);
+                acc.y = fmaf(v[j].y, f, acc.y);
+                acc.z = fmaf(v[j].z, f, acc.z);
+                acc.w = fmaf(v[j].w, f, acc.w);
+            }
+        }
+        if (Mall != -INFINITY) {  // else no visible row (a verify query before every row)
+            if (a.sinks) {
+                // a learned sink joins the maximum and the sum; it has no value row
+                const float z = a.sinks[h] * kLog2e;
+                const float Mf = fmaxf(Mall, z), f = exp2f(Mall - Mf);
+                sum = fmaf(sum, f, exp2f(z - Mf));
+                acc.x *= f;
+                acc.y *= f;
+                acc.z *= f;
+                acc.w *= f;
+                Mall = Mf;
+            }
+            const float4 vc = src.vcol ? reinterpret_cast<const float4 *>(src.vcol + unit * 128)[lane]
+                                       : make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+            res = make_float4(acc.x / sum * vc.x, acc.y / sum * vc.y, acc.z / sum * vc.z, acc.w / sum * vc.w);
+        }
+    }
+    reinterpret_cast<float4 *>(a.out + ((int64_t(b) * a.K + k) * a.n_q + h) * 128)[lane] = res;
+    if (a.ml && lane == 0) {
+        float *mlp = a.ml + (int64_t(b) * a.n_q + h) * 2;
+        mlp[0] = Mall;
+        mlp[1] = sum;
+    }
+}
+
+// Largest slot range of one unit under the tensor-core work split:
+// blocks(u) + c(last tile of u) - c(first tile of u), with c(x) the worker
+// holding global tile x (units in sequence-major, live-group order).
+int64_t max_unit_slots(const Layer *l, int64_t window, int32_t K, int64_t T, int64_t G) {
+    if (T <= 0 || G <= 0) return 0;
+    auto worker = [&](int64_t x) { return std::min(((x + 1) * G + T - 1) / T, G) - 1; };
+    int64_t t = 0, most = 0;
+    for (int b = 0; b < l->n_seq; ++b) {
+        const int64_t Tb = tiles_of(l->h_seq_len[b], window, K);
+        if (Tb <= 0) continue;
+        for (int gl = 0; gl < l->n_live; ++gl) {
+            most = std::max(most, ceil_div(Tb, kBlockTiles) + worker(t + Tb - 1) - worker(t));
+            t += Tb;
+        }
+    }
+    return most;
+}
+
+// Merge of the run partials: a warp per query head while every unit has at
+// most two batches of slots, else a CTA per query head.
+cudaError_t launch_run_merge(const RunMergeArgs &rm, const MergeLayerSrc &ms, int n_seq, int K,
+                             int64_t most_slots, cudaStream_t st) {
+    if (most_slots <= 2 * kHeadBatch)
+        merge_heads_kernel<<<dim3(unsigned(ceil_div(rm.n_q, kHeadWarps)), unsigned(n_seq), unsigned(K)),
+                             32 * kHeadWarps, 0, st>>>(rm, ms);
+    else
+        merge_runs_kernel<<<dim3(unsigned(rm.n_q), unsigned(n_seq), unsigned(K)), 32 * kMergeWarps, 0, st>>>(rm,
+                                                                                                         ms);
+    return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ imp
 
 struct ImpArgs {
@@ -737,8 +852,8 @@ extern "C" kvd_status decode_attention_ex(const float *q, const kvd_layer *L, in
         rm.hpk = hpk;
         rm.unit_slots = wa.unit_slots;
         rm.sinks = sinks;
-        merge_runs_kernel<<<dim3(unsigned(n_q), unsigned(l->n_seq)), 32 * kMergeWarps, 0, st>>>(rm, ms);
-        if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
+        if (launch_run_merge(rm, ms, l->n_seq, 1, max_unit_slots(l, window, 1, T, wa.G), st) != cudaSuccess)
+            return KVD_ECUDA;
     } else {
         if (max_len > 0 && l->n_live > 0) {
             dim3 grid(unsigned(ceil_div(max_len, chunk)), unsigned(l->n_live), unsigned(l->n_seq));
@@ -903,8 +1018,9 @@ extern "C" kvd_status decode_attention_verify(const float *q, const kvd_layer *L
         rm.hg = hg;
         rm.unit_slots = wa.unit_slots;
         rm.sinks = sinks;
-        merge_runs_kernel<<<dim3(unsigned(n_q), unsigned(l->n_seq), unsigned(K)), 32 * kMergeWarps, 0, st>>>(rm, ms);
-        return cudaGetLastError() == cudaSuccess ? KVD_OK : KVD_ECUDA;
+        return launch_run_merge(rm, ms, l->n_seq, K, max_unit_slots(l, window, K, T, wa.G), st) == cudaSuccess
+                   ? KVD_OK
+                   : KVD_ECUDA;
     }
     if (max_len > 0 && l->n_live > 0) {
         dim3 grid(unsigned(ceil_div(max_len, chunk)), unsigned(l->n_live), unsigned(l->n_seq));
