@@ -53,8 +53,8 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
 # profiles/decode_q8_gqa_traffic.md), valid while the kernel sources hash to
 # the captured version; reported as null otherwise.
 TRAFFIC = {
-    "q8_gqa": {"sources_sha256": "ec5e95fb70eaf1f8ac318c279c2d92b8beda026b6691b6b27e9fe7943df9c82b",
-               "bytes": 300567936},
+    "q8_gqa": {"sources_sha256": "1ff8e6b9c8b563d0a84bc70e33a31a4c697f9f8e239588541841af29f6a3689d",
+               "bytes": 300577792},
 }
 
 
