@@ -333,29 +333,30 @@ __global__ void __launch_bounds__(32 * kHeadWarps) merge_heads_kernel(RunMergeAr
     }
 }
 
-// Largest slot range of one unit under the tensor-core work split:
+// Whether every unit's slot range under the tensor-core work split --
 // blocks(u) + c(last tile of u) - c(first tile of u), with c(x) the worker
-// holding global tile x (units in sequence-major, live-group order).
-int64_t max_unit_slots(const Layer *l, int64_t window, int32_t K, int64_t T, int64_t G) {
-    if (T <= 0 || G <= 0) return 0;
+// holding global tile x (units in sequence-major, live-group order) -- has
+// at most `limit` slots.
+bool unit_slots_within(const Layer *l, int64_t window, int32_t K, int64_t T, int64_t G, int64_t limit) {
+    if (T <= 0 || G <= 0) return true;
     auto worker = [&](int64_t x) { return std::min(((x + 1) * G + T - 1) / T, G) - 1; };
-    int64_t t = 0, most = 0;
+    int64_t t = 0;
     for (int b = 0; b < l->n_seq; ++b) {
         const int64_t Tb = tiles_of(l->h_seq_len[b], window, K);
         if (Tb <= 0) continue;
         for (int gl = 0; gl < l->n_live; ++gl) {
-            most = std::max(most, ceil_div(Tb, kBlockTiles) + worker(t + Tb - 1) - worker(t));
+            if (ceil_div(Tb, kBlockTiles) + worker(t + Tb - 1) - worker(t) > limit) return false;
             t += Tb;
         }
     }
-    return most;
+    return true;
 }
 
 // Merge of the run partials: a warp per query head while every unit has at
 // most two batches of slots, else a CTA per query head.
 cudaError_t launch_run_merge(const RunMergeArgs &rm, const MergeLayerSrc &ms, int n_seq, int K,
-                             int64_t most_slots, cudaStream_t st) {
-    if (most_slots <= 2 * kHeadBatch)
+                             bool few_slots, cudaStream_t st) {
+    if (few_slots)
         merge_heads_kernel<<<dim3(unsigned(ceil_div(rm.n_q, kHeadWarps)), unsigned(n_seq), unsigned(K)),
                              32 * kHeadWarps, 0, st>>>(rm, ms);
     else
@@ -852,8 +853,8 @@ extern "C" kvd_status decode_attention_ex(const float *q, const kvd_layer *L, in
         rm.hpk = hpk;
         rm.unit_slots = wa.unit_slots;
         rm.sinks = sinks;
-        if (launch_run_merge(rm, ms, l->n_seq, 1, max_unit_slots(l, window, 1, T, wa.G), st) != cudaSuccess)
-            return KVD_ECUDA;
+        const bool few = unit_slots_within(l, window, 1, T, wa.G, 2 * kHeadBatch);
+        if (launch_run_merge(rm, ms, l->n_seq, 1, few, st) != cudaSuccess) return KVD_ECUDA;
     } else {
         if (max_len > 0 && l->n_live > 0) {
             dim3 grid(unsigned(ceil_div(max_len, chunk)), unsigned(l->n_live), unsigned(l->n_seq));
@@ -1018,9 +1019,8 @@ extern "C" kvd_status decode_attention_verify(const float *q, const kvd_layer *L
         rm.hg = hg;
         rm.unit_slots = wa.unit_slots;
         rm.sinks = sinks;
-        return launch_run_merge(rm, ms, l->n_seq, K, max_unit_slots(l, window, K, T, wa.G), st) == cudaSuccess
-                   ? KVD_OK
-                   : KVD_ECUDA;
+        const bool few = unit_slots_within(l, window, K, T, wa.G, 2 * kHeadBatch);
+        return launch_run_merge(rm, ms, l->n_seq, K, few, st) == cudaSuccess ? KVD_OK : KVD_ECUDA;
     }
     if (max_len > 0 && l->n_live > 0) {
         dim3 grid(unsigned(ceil_div(max_len, chunk)), unsigned(l->n_live), unsigned(l->n_seq));

@@ -147,6 +147,19 @@ def test_decode_parity_hd128(torch, kvd, mode, hpk):
                  np.array([1, 1, 0, 1], np.uint8), seed=11 + hpk)
 
 
+# q8_2f at head_dim 128 runs on the tensor-core kernels, whose run partials are
+# merged by one warp per query head (up to 16 slots per unit in one batch of
+# loads, up to 32 in two) or by one CTA per query head beyond that.  With fewer
+# tiles than resident workers every tile is its own run, so the longest
+# sequence sets the slot count: 16 tiles (500 rows), 29 tiles (900 rows); the
+# hd128 case above (1030 rows, 33 tiles) takes the CTA merge.
+@pytest.mark.parametrize("hpk", [1, 3, 4, 8, 12, 16])
+@pytest.mark.parametrize("longest", [500, 900])
+def test_decode_q8_merge_paths(torch, kvd, hpk, longest):
+    _decode_case(torch, kvd, oracle.Q8, 128, hpk, [0, 1, 64, 300, longest, 33],
+                 np.array([1, 0, 1, 1], np.uint8), seed=31 + hpk + longest)
+
+
 @pytest.mark.parametrize("mode", list(MODES))
 @pytest.mark.parametrize("hpk", [2, 8])
 def test_decode_parity_hd64(torch, kvd, mode, hpk):
