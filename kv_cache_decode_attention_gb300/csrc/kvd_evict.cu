@@ -19,7 +19,8 @@
 //           live head x storage) one CTA walks each region's tiles in order,
 //           in place; with few, the rows go in batches of j through a
 //           workspace copy (one kernel reads a batch, the next writes it), so
-//           every batch spreads over the whole GPU.
+//           every batch spreads over the whole GPU -- or straight from their
+//           sources when the batch's first source lies past its last row.
 // The device length becomes keep_last in the select kernel; the host mirror
 // is updated by the entry point.
 //
@@ -307,6 +308,24 @@ __device__ __forceinline__ void batch_copy(U *region, U *stage, int lu, const in
     }
 }
 
+// The batch's rows straight from their sources, for a batch whose every source
+// lies at or past its end (kept[j0] >= j1, kept ascending): no row the batch
+// writes is a source of it or of a later batch.
+template <typename U>
+__device__ __forceinline__ void direct_copy(U *region, int lu, const int32_t *kept, int j0, int rows, int64_t cap,
+                                            uint32_t *err) {
+    const int n = rows << lu;
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < n; e += gridDim.x * blockDim.x) {
+        const int j = j0 + (e >> lu), w = e & ((1 << lu) - 1);
+        const int32_t src = kept[j];
+        if (src >= 0 && src < cap) region[(int64_t(j) << lu) + w] = region[(int64_t(src) << lu) + w];
+        else set_error(err, kErrBounds);
+    }
+}
+
+// to_stage: read the batch's sources into the stage (or, for a batch whose
+// sources all lie past it, copy it directly); else write the stage to its rows
+// (nothing for a direct batch).
 template <bool TO_STAGE>
 __global__ void __launch_bounds__(kGatherThreads) born_batch_kernel(BatchArgs a, BornTable t) {
     const int i = blockIdx.z;
@@ -319,6 +338,15 @@ __global__ void __launch_bounds__(kGatherThreads) born_batch_kernel(BatchArgs a,
     char *stage = a.stage + (int64_t(i) * a.n_live + gl) * a.stage_group + a.st_off[s];
     const int32_t *kept = a.g.idx + int64_t(i) * a.g.keep_last;
     const int rows = a.j1 - a.j0;
+    if (kept[a.j0] >= a.j1) {
+        if (!TO_STAGE) return;
+        if (g.row_bytes % 16 == 0)
+            direct_copy(reinterpret_cast<uint4 *>(region), log2_exact(g.row_bytes / 16), kept, a.j0, rows, cap, a.g.err);
+        else
+            direct_copy(reinterpret_cast<uint32_t *>(region), log2_exact(g.row_bytes / 4), kept, a.j0, rows, cap,
+                        a.g.err);
+        return;
+    }
     if (g.row_bytes % 16 == 0)
         batch_copy<TO_STAGE>(reinterpret_cast<uint4 *>(region), reinterpret_cast<uint4 *>(stage),
                              log2_exact(g.row_bytes / 16), kept, a.j0, rows, cap, a.g.err);

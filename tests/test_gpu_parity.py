@@ -500,14 +500,18 @@ def _mass(lengths, imp_base, imp_len, seed):
 
 @pytest.mark.parametrize("mode", list(MODES))
 @pytest.mark.parametrize("hd", [128, 64])
-def test_born_eviction_parity(torch, kvd, mode, hd):
+@pytest.mark.parametrize("recent", [60, 146])
+def test_born_eviction_parity(torch, kvd, mode, hd, recent):
     """Sequences above, at and below the budget, a dead head, many tied masses:
     after kv_evict_born every storage, imp and the lengths equal the oracle's
     evict_born bit for bit; decode over the evicted cache and over rows appended
-    afterwards matches the oracle."""
+    afterwards matches the oracle.  recent 146 leaves no middle budget: the long
+    sequences keep their sinks and last rows, whose sources all lie past the
+    kept range (the gather copies them directly), while the 151-row one moves
+    through the workspace copy."""
     lengths = [700, 150, 151, 40, 2300]
     n_kv, alive, extra = 4, [1, 1, 0, 1], 40
-    keep, sink, recent = 150, 4, 60
+    keep, sink = 150, 4
     ks, vs = seq_rows(lengths, n_kv, hd, seed=61)
     layer = _layer(kvd, MODES[mode], lengths, n_kv, hd, alive, cap_extra=extra)
     gpu_append_bulk(layer, ks, vs, torch, pieces=(0.5, 1.0))
