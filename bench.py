@@ -331,6 +331,62 @@ def packed_inputs(torch, parts_per_step):
     return pinned, stage, views
 
 
+def e2e_pipelined(torch, pinned, stages, steps, launch):
+    """End-to-end steps through the public API with host buffers, pipelined: step j's
+    inputs go host -> device on a copy stream into staging buffer j % 2 while step
+    j - 1 computes, its kernels wait for that copy, its output goes device -> host on
+    a second copy stream once they finish, and the host waits once, at the end.
+    stages: two (buffer, views) pairs; launch(j, views) enqueues step j on the
+    current stream and returns (output tensor, pinned host tensor to copy it to).
+    Events keep a staging buffer from being refilled before the step reading it has
+    run, and an output from being rewritten before its copy out has.  Returns the
+    seconds from the first copy to the last result on the host."""
+    comp = torch.cuda.current_stream()
+    cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
+    Event = torch.cuda.Event
+    freed = [None, None]   # staging buffer b no longer read (its step's kernels done)
+    copied = {}            # output tensor -> its last copy out
+    torch.cuda.synchronize()
+    a0 = time.perf_counter()
+    for j in range(steps):
+        buf, views = stages[j % 2]
+        ev_in = Event()
+        with torch.cuda.stream(cin):
+            if freed[j % 2] is not None:
+                cin.wait_event(freed[j % 2])
+            buf.copy_(pinned[j % len(pinned)], non_blocking=True)
+            ev_in.record(cin)
+        comp.wait_event(ev_in)
+        out, host = launch(j, views, lambda t: copied.get(t.data_ptr()))
+        done = Event()
+        done.record(comp)
+        freed[j % 2] = done
+        ev_out = Event()
+        with torch.cuda.stream(cout):
+            cout.wait_event(done)
+            host.copy_(out, non_blocking=True)
+            ev_out.record(cout)
+        copied[out.data_ptr()] = ev_out
+    torch.cuda.synchronize()
+    return time.perf_counter() - a0
+
+
+def restage(torch, stage, views):
+    """A second device staging buffer with views of the same shapes."""
+    buf = torch.empty_like(stage)
+    out, o = [], 0
+    for v in views:
+        out.append(buf[o:o + v.numel()].view(v.shape))
+        o += v.numel()
+    return buf, out
+
+
+def wait_copied(torch, ev):
+    """Make the current stream wait for an output's last copy out (None: none yet)."""
+    if ev is not None:
+        torch.cuda.current_stream().wait_event(ev)
+
+
 def run_gpu_rswa(args, rank, world):
     """The R-SWA workloads: 16 streams in steady state (reference 32640 rows +
     a full ring), one step = rswa ring write of one token per stream + decode
@@ -404,7 +460,7 @@ def run_gpu_rswa(args, rank, world):
         torch.cuda.profiler.start()
         t0.record(stream)
         for j in range(args.steps):
-            step(args.warmup + j, ev[j])
+            step(args.warmup + j)
         t1.record(stream)
         torch.cuda.synchronize()
         torch.cuda.profiler.stop()
@@ -414,6 +470,11 @@ def run_gpu_rswa(args, rank, world):
     elapsed_ms = replicas.max_over_ranks(t0.elapsed_time(t1))
     ms_per_step = elapsed_ms / args.steps
     gbs = replicas.whole_job_rate((dec_bytes + wr_bytes) * args.steps, elapsed_ms * 1e-3, world) / 1e9
+    # the decode's share of a step: the same steps again with events around it
+    # (kept out of the timed steps above)
+    for j in range(len(ev)):
+        step(args.warmup + args.steps + j, ev[j])
+    torch.cuda.synchronize()
     dec_ms = [a.elapsed_time(b) for a, b in ev]
 
     nrep = max(20, args.steps)
@@ -430,8 +491,27 @@ def run_gpu_rswa(args, rank, world):
     peak, peak_kind = peaks()
     achieved = dec_bytes / (k_ms * 1e-3) / 1e9
 
+    # end to end: pipelined (the headline), then synchronising on every step
     pinned, stage, (dq, dk, dv) = packed_inputs(torch, [(qs[i], news[i][0], news[i][1]) for i in range(8)])
-    pin_out = torch.empty(out.shape).pin_memory()
+    stages = [(stage, (dq, dk, dv)), restage(torch, stage, (dq, dk, dv))]
+    pin_outs = [torch.empty(out.shape).pin_memory() for _ in range(2)]
+
+    def e2e_step(j, views, last_copy):
+        wait_copied(torch, last_copy(out))
+        cur_i[0] = j
+        if not verify:
+            kvd.rswa_ring_write(c, views[1], views[2])
+        decode(views[0], c, out=out)
+        if verify:
+            kvd.rswa_ring_write(c, views[1], views[2])
+        return out, pin_outs[j % 2]
+
+    secs = e2e_pipelined(torch, pinned, stages, args.steps, e2e_step)
+    e2e = {"value": round((dec_bytes + wr_bytes) * args.steps / secs / 1e9 * world, 2), "unit": "GB/s",
+           "h2d_bytes_per_step": int((dq.numel() + dk.numel() + dv.numel()) * 4),
+           "d2h_bytes_per_step": int(pin_outs[0].numel() * 4),
+           "mode": "pipelined: inputs copied in on a copy stream while the previous step computes, "
+                   "outputs copied out on another, one host synchronisation at the end"}
     torch.cuda.synchronize()
     a0 = time.perf_counter()
     for j in range(args.steps):
@@ -442,12 +522,11 @@ def run_gpu_rswa(args, rank, world):
         decode(dq, c, out=out)
         if verify:
             kvd.rswa_ring_write(c, dk, dv)
-        pin_out.copy_(out, non_blocking=True)
+        pin_outs[0].copy_(out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
     a1 = time.perf_counter()
-    e2e = {"value": round((dec_bytes + wr_bytes) * args.steps / (a1 - a0) / 1e9 * world, 2), "unit": "GB/s",
-           "h2d_bytes_per_step": int((dq.numel() + dk.numel() + dv.numel()) * 4),
-           "d2h_bytes_per_step": int(pin_out.numel() * 4)}
+    e2e_sync = {"value": round((dec_bytes + wr_bytes) * args.steps / (a1 - a0) / 1e9 * world, 2),
+                "unit": "GB/s", "mode": "the host waits for every step's result before the next step"}
     if c.device_error():
         raise SystemExit("device error word set")
     if rank != 0:
@@ -480,6 +559,7 @@ def run_gpu_rswa(args, rank, world):
         "decode_ms_in_step": round(statistics.mean(dec_ms), 5),
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "e2e_sync": e2e_sync,
         "gpu_launches": args.steps * (4 if verify else 3),
         "clocks": sampler.summary(c0, c1),
     }
@@ -547,7 +627,7 @@ def run_gpu_verify(args, rank, world):
         torch.cuda.profiler.start()
         t0.record(stream)
         for j in range(args.steps):
-            step(args.warmup + j, ev[j])
+            step(args.warmup + j)
         t1.record(stream)
         torch.cuda.synchronize()
         torch.cuda.profiler.stop()
@@ -560,13 +640,33 @@ def run_gpu_verify(args, rank, world):
     # (the drafts included), its K queries and outputs
     step_bytes = K * W.append_bytes(probe.mode, n_live, hd, n_seq) + bytes_each + 2 * n_seq * (K - 1) * n_q * hd * 4
     gbs = replicas.whole_job_rate(step_bytes * args.steps, elapsed_ms * 1e-3, world) / 1e9
+    # the verify call timed inside the same steps run again with events around
+    # it (kept out of the timed steps above)
+    for j in range(len(ev)):
+        step(args.warmup + args.steps + j, ev[j])
+    torch.cuda.synchronize()
     ver_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     achieved = (bytes_each + 2 * n_seq * (K - 1) * n_q * hd * 4) / (ver_ms * 1e-3) / 1e9
     peak, peak_kind = peaks()
     # end to end: the step's queries and drafts copied in (one pinned buffer),
     # the K outputs copied out, every step
     pinned, stage, (dq, ddk, ddv) = packed_inputs(torch, [(qs[i], drafts[i][0], drafts[i][1]) for i in range(8)])
-    pin_out = torch.empty(out.shape).pin_memory()
+    stages = [(stage, (dq, ddk, ddv)), restage(torch, stage, (dq, ddk, ddv))]
+    pin_outs = [torch.empty(out.shape).pin_memory() for _ in range(2)]
+
+    def e2e_step(j, views, last_copy):
+        w = wls[j % R]
+        wait_copied(torch, last_copy(out))
+        kvd.kv_append(w.layer, views[1], views[2], nn)
+        kvd.decode_attention_verify(views[0], w.layer, K, out=out, scale=w.scale, workspace=ws)
+        kvd.kv_truncate_last(w.layer, K)
+        return out, pin_outs[j % 2]
+
+    secs = e2e_pipelined(torch, pinned, stages, args.steps, e2e_step)
+    e2e = {"value": round(step_bytes * args.steps / secs / 1e9 * world, 2), "unit": "GB/s",
+           "h2d_bytes_per_step": int(stage.numel() * 4), "d2h_bytes_per_step": int(pin_outs[0].numel() * 4),
+           "mode": "pipelined: inputs copied in on a copy stream while the previous step computes, "
+                   "outputs copied out on another, one host synchronisation at the end"}
     torch.cuda.synchronize()
     a0 = time.perf_counter()
     for j in range(args.steps):
@@ -575,11 +675,11 @@ def run_gpu_verify(args, rank, world):
         kvd.kv_append(w.layer, ddk, ddv, nn)
         kvd.decode_attention_verify(dq, w.layer, K, out=out, scale=w.scale, workspace=ws)
         kvd.kv_truncate_last(w.layer, K)
-        pin_out.copy_(out, non_blocking=True)
+        pin_outs[0].copy_(out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
     a1 = time.perf_counter()
-    e2e = {"value": round(step_bytes * args.steps / (a1 - a0) / 1e9 * world, 2), "unit": "GB/s",
-           "h2d_bytes_per_step": int(stage.numel() * 4), "d2h_bytes_per_step": int(pin_out.numel() * 4)}
+    e2e_sync = {"value": round(step_bytes * args.steps / (a1 - a0) / 1e9 * world, 2), "unit": "GB/s",
+                "mode": "the host waits for every step's result before the next step"}
     for w in wls:
         if w.layer.device_error():
             raise SystemExit("device error word set")
@@ -623,6 +723,7 @@ def run_gpu_verify(args, rank, world):
                      "ms_per_launch": round(ver_ms, 5), "bytes_per_launch": int(bytes_each)},
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "e2e_sync": e2e_sync,
         "gpu_launches": args.steps * 4,
         "clocks": sampler.summary(c0, c1),
     }
@@ -689,8 +790,9 @@ def run_gpu(args, rank, world):
 
     # ---- timed region
     bytes_total = 0
+    n_ev = min(args.steps, 10)  # steps run again with events around the decode, after the timing
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+          for _ in range(n_ev)]
     lens_before = lengths_now()
     sampler = ClockSampler(dev.index)
     with sampler:
@@ -703,7 +805,7 @@ def run_gpu(args, rank, world):
         torch.cuda.profiler.start()  # profilers started with capture off record only this range
         t0.record(stream)
         for j in range(args.steps):
-            step(args.warmup + j, ev[j])
+            step(args.warmup + j)
         t1.record(stream)
         torch.cuda.synchronize()
         torch.cuda.profiler.stop()
@@ -719,7 +821,13 @@ def run_gpu(args, rank, world):
         bytes_total += W.append_bytes(w.mode, n_live, w.hd, w.n_seq)
         lens[r] += 1
         bytes_total += W.decode_bytes(w.mode, n_live, w.hd, w.n_q, lens[r], True, w.n_seq)
+    # the decode's share of a step, from steps run again with events around it
+    # (kept out of the timed steps above)
+    for j in range(n_ev):
+        step(n_steps + j, ev[j])
+    torch.cuda.synchronize()
     dec_ms = [a.elapsed_time(b) for a, b in ev]
+    n_steps += n_ev
     elapsed_ms = replicas.max_over_ranks(elapsed_ms)  # every rank ran its own replica
     ms_per_step = elapsed_ms / args.steps
     gbs = replicas.whole_job_rate(bytes_total, elapsed_ms * 1e-3, world) / 1e9
@@ -744,37 +852,59 @@ def run_gpu(args, rank, world):
     peak, peak_kind = peaks()
     achieved = kbytes / (k_ms * 1e-3) / 1e9
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the public API with host buffers: pipelined (the
+    #      headline), then the same steps synchronising on every step's result
     pinned, stage, (dq, dk, dv) = packed_inputs(torch, [(qs[i], news[i][0], news[i][1]) for i in range(8)])
-    pin_out = torch.empty(wl0.n_seq, wl0.n_q, wl0.hd).pin_memory()
+    stages = [(stage, (dq, dk, dv)), restage(torch, stage, (dq, dk, dv))]
+    pin_outs = [torch.empty(wl0.n_seq, wl0.n_q, wl0.hd).pin_memory() for _ in range(2)]
     e2e_steps = args.steps
-    if math.ceil(2 * (n_steps + e2e_steps) / R) > extra:
-        e2e_steps = 0
-    e2e = None
-    if e2e_steps:
-        torch.cuda.synchronize()
-        lens_b = lengths_now()
-        a0 = time.perf_counter()
-        for j in range(e2e_steps):
-            i = n_steps + j
-            w = wls[i % R]
-            stage.copy_(pinned[i % 8], non_blocking=True)
-            kvd.kv_append(w.layer, dk, dv)
-            kvd.decode_attention(dq, w.layer, out=outs[i % R], imp=imps[i % R], scale=w.scale, workspace=ws)
-            pin_out.copy_(outs[i % R], non_blocking=True)
-            torch.cuda.current_stream().synchronize()
-        a1 = time.perf_counter()
+    sync_steps = min(e2e_steps, 50)  # the synchronised leg: a shorter sample of the same steps
+    if math.ceil(2 * (n_steps + e2e_steps + sync_steps) / R) > extra:
+        e2e_steps = sync_steps = 0
+    e2e = e2e_sync = None
+
+    def e2e_bytes(first, count, lens_b):
         eb = 0
         lens_e = [l.copy() for l in lens_b]
-        for j in range(e2e_steps):
-            r = (n_steps + j) % R
+        for j in range(count):
+            r = (first + j) % R
             w = wls[r]
             lens_e[r] += 1
             eb += W.append_bytes(w.mode, n_live, w.hd, w.n_seq)
             eb += W.decode_bytes(w.mode, n_live, w.hd, w.n_q, lens_e[r], True, w.n_seq)
-        e2e = {"value": round(eb / (a1 - a0) / 1e9 * world, 2), "unit": "GB/s",
+        return eb
+
+    def e2e_step(j, views, last_copy):
+        i = n_steps + j
+        w, o = wls[i % R], outs[i % R]
+        wait_copied(torch, last_copy(o))  # o's previous copy out has left before it is rewritten
+        kvd.kv_append(w.layer, views[1], views[2])
+        kvd.decode_attention(views[0], w.layer, out=o, imp=imps[i % R], scale=w.scale, workspace=ws)
+        return o, pin_outs[j % 2]
+
+    if e2e_steps:
+        lens_b = lengths_now()
+        secs = e2e_pipelined(torch, pinned, stages, e2e_steps, e2e_step)
+        e2e = {"value": round(e2e_bytes(n_steps, e2e_steps, lens_b) / secs / 1e9 * world, 2), "unit": "GB/s",
                "h2d_bytes_per_step": int(dq.numel() * 4 + dk.numel() * 4 + dv.numel() * 4),
-               "d2h_bytes_per_step": int(pin_out.numel() * 4)}
+               "d2h_bytes_per_step": int(pin_outs[0].numel() * 4),
+               "mode": "pipelined: inputs copied in on a copy stream while the previous step computes, "
+                       "outputs copied out on another, one host synchronisation at the end"}
+        first = n_steps + e2e_steps
+        torch.cuda.synchronize()
+        lens_b = lengths_now()
+        a0 = time.perf_counter()
+        for j in range(sync_steps):
+            i = first + j
+            w = wls[i % R]
+            stage.copy_(pinned[i % 8], non_blocking=True)
+            kvd.kv_append(w.layer, dk, dv)
+            kvd.decode_attention(dq, w.layer, out=outs[i % R], imp=imps[i % R], scale=w.scale, workspace=ws)
+            pin_outs[0].copy_(outs[i % R], non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+        a1 = time.perf_counter()
+        e2e_sync = {"value": round(e2e_bytes(first, sync_steps, lens_b) / (a1 - a0) / 1e9 * world, 2),
+                    "unit": "GB/s", "mode": "the host waits for every step's result before the next step"}
     for w in wls:
         err = w.layer.device_error()
         if err:
@@ -809,6 +939,7 @@ def run_gpu(args, rank, world):
         "decode_ms_in_step": round(statistics.mean(dec_ms), 5),
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "e2e_sync": e2e_sync,
         "gpu_launches": args.steps * 4,
         "clocks": clocks,
     }
