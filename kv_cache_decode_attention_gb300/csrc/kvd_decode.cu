@@ -166,6 +166,8 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_runs_kernel(RunMergeAr
         return;
     }
     const int64_t unit = int64_t(b) * src.n_live + grp;
+    pdl_wait();     // the split kernel's partials are complete
+    pdl_trigger();  // the imp pass may start (it reads the split's scores first)
     const int64_t first = a.unit_slots[2 * unit], last = a.unit_slots[2 * unit + 1];
     const int hh = a.K > 1 ? k * hg + h % hg : h % a.hpk;  // the query's row in the partials
     const float *pmh = a.pm + hh, *plh = a.pl + hh, *pah = a.pacc + int64_t(hh) * 128 + 4 * lane;
@@ -269,6 +271,8 @@ __global__ void __launch_bounds__(32 * kHeadWarps) merge_heads_kernel(RunMergeAr
     float Mall = -INFINITY, sum = 0.0f;
     if (grp >= 0 && L > 0) {
         const int64_t unit = int64_t(b) * src.n_live + grp;
+        pdl_wait();     // the split kernel's partials are complete
+        pdl_trigger();  // the imp pass may start (it reads the split's scores first)
         const int64_t first = a.unit_slots[2 * unit], last = a.unit_slots[2 * unit + 1];
         const int hh = a.K > 1 ? k * hg + h % hg : h % a.hpk;  // the query's row in the partials
         const float *pmh = a.pm + hh, *plh = a.pl + hh, *pah = a.pacc + int64_t(hh) * 128 + 4 * lane;
@@ -356,13 +360,12 @@ bool unit_slots_within(const Layer *l, int64_t window, int32_t K, int64_t T, int
 // most two batches of slots, else a CTA per query head.
 cudaError_t launch_run_merge(const RunMergeArgs &rm, const MergeLayerSrc &ms, int n_seq, int K,
                              bool few_slots, cudaStream_t st) {
+    // launched as dependents of the split kernel: their set-up overlaps its tail
     if (few_slots)
-        merge_heads_kernel<<<dim3(unsigned(ceil_div(rm.n_q, kHeadWarps)), unsigned(n_seq), unsigned(K)),
-                             32 * kHeadWarps, 0, st>>>(rm, ms);
-    else
-        merge_runs_kernel<<<dim3(unsigned(rm.n_q), unsigned(n_seq), unsigned(K)), 32 * kMergeWarps, 0, st>>>(rm,
-                                                                                                         ms);
-    return cudaGetLastError();
+        return launch_pdl(merge_heads_kernel, dim3(unsigned(ceil_div(rm.n_q, kHeadWarps)), unsigned(n_seq), unsigned(K)),
+                          dim3(32 * kHeadWarps), 0, st, rm, ms);
+    return launch_pdl(merge_runs_kernel, dim3(unsigned(rm.n_q), unsigned(n_seq), unsigned(K)), dim3(32 * kMergeWarps),
+                      0, st, rm, ms);
 }
 
 // ------------------------------------------------------------------ imp
@@ -401,13 +404,6 @@ __global__ void __launch_bounds__(kImpThreads) imp_kernel(ImpArgs a) {
     if (p0 >= L) return;
     const int nh = a.n_live * a.hpk;
     const int64_t cap = a.cap[b];
-    for (int i = t; i < nh; i += kImpThreads) {
-        const int h = a.live[i / a.hpk] * a.hpk + i % a.hpk;
-        const float M = a.ml[(int64_t(b) * a.n_q + h) * 2];
-        const float Ls = a.ml[(int64_t(b) * a.n_q + h) * 2 + 1];
-        mlinv[2 * i] = M;
-        mlinv[2 * i + 1] = Ls > 0.0f ? 1.0f / Ls : 0.0f;
-    }
     const int quad = t % (kImpRows / 4), cls = t / (kImpRows / 4);
     const int p = p0 + 4 * quad;
     const int r = p0 + t;
@@ -425,7 +421,15 @@ __global__ void __launch_bounds__(kImpThreads) imp_kernel(ImpArgs a) {
             if (p < L && i < nh) sv[k] = *reinterpret_cast<const float4 *>(sb + int64_t(i) * cap);
         }
     };
-    load(cls);        // the first batch is in flight across the barrier
+    load(cls);  // the first batch (scores of the finished split kernel) is in flight across the wait
+    pdl_wait();  // the merge's maxima and sums are complete
+    for (int i = t; i < nh; i += kImpThreads) {
+        const int h = a.live[i / a.hpk] * a.hpk + i % a.hpk;
+        const float M = a.ml[(int64_t(b) * a.n_q + h) * 2];
+        const float Ls = a.ml[(int64_t(b) * a.n_q + h) * 2 + 1];
+        mlinv[2 * i] = M;
+        mlinv[2 * i + 1] = Ls > 0.0f ? 1.0f / Ls : 0.0f;
+    }
     __syncthreads();  // the staged maxima and sums are visible
     for (int i0 = cls; i0 < nh; i0 += kImpClasses * kImpBatch) {
         if (i0 != cls) load(i0);
@@ -907,8 +911,8 @@ extern "C" kvd_status decode_attention_ex(const float *q, const kvd_layer *L, in
         if (ml_bytes > 40 * 1024 &&
             set_smem_once(reinterpret_cast<const void *>(imp_kernel), int(ml_bytes)) != cudaSuccess)
             return KVD_ECUDA;
-        imp_kernel<<<igrid, kImpThreads, ml_bytes, st>>>(ia);
-        if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
+        // a dependent of the merge: its score loads overlap the merge
+        if (launch_pdl(imp_kernel, igrid, dim3(kImpThreads), ml_bytes, st, ia) != cudaSuccess) return KVD_ECUDA;
     }
     return KVD_OK;
 }

@@ -664,6 +664,7 @@ struct MergeLayerSrc {
 
 template <int HD>
 __global__ void __launch_bounds__(HD) merge_layer_kernel(MergeArgs a, MergeLayerSrc src) {
+    pdl_trigger();  // launched after the split kernel finished: the imp pass may start
     const int h = blockIdx.x, b = blockIdx.y;
     const int L = src.seq_len[b];
     const int grp = src.slot[h / a.hpk];

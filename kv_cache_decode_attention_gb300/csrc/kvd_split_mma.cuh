@@ -305,6 +305,7 @@ __global__ void __launch_bounds__(32, 12) split_warp_kernel(WarpArgs wa, LayerSr
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + C::BAR_OFF);
     const int64_t T = wa.T, G = wa.G, c = blockIdx.x;
     const int64_t x_begin = c * T / G, x_end = (c + 1) * T / G;
+    pdl_trigger();  // the run merge (launched as a dependent) may be scheduled; it waits for this grid
     if (x_begin >= x_end) return;
 
     TileCursor cur;
