@@ -77,6 +77,7 @@ __device__ __forceinline__ void quantise_row_warp(const float (&x)[CPL], const f
 
 template <int HD>
 __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(AppendArgs a, AppendTable t) {
+    pdl_trigger();  // a decode launched as a dependent may be scheduled; it waits for this grid
     constexpr int CPL = HD / 32;
     constexpr int NG = HD / kKGroup;
     const int i = blockIdx.y;

@@ -47,7 +47,10 @@ __global__ void __launch_bounds__(32, 8) split_h16_kernel(WarpArgs wa, LayerSrc 
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + C::BAR_OFF);
     const int64_t T = wa.T, G = wa.G, c = blockIdx.x;
     const int64_t x_begin = c * T / G, x_end = (c + 1) * T / G;
-    pdl_trigger();  // the run merge (launched as a dependent) may be scheduled; it waits for this grid
+    // launched as a dependent of the kernel before (the append of a decode
+    // step): wait for it, then let the run merge be scheduled
+    pdl_wait();
+    pdl_trigger();
     if (x_begin >= x_end) return;
 
     TileCursor cur;
@@ -453,8 +456,7 @@ inline cudaError_t launch_split_h16(const WarpArgs &wa, const LayerSrc &s, const
                     : (imp ? split_h16_kernel<false, true> : split_h16_kernel<false, false>);
     cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), H16Cfg::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    kern<<<unsigned(wa.G), 32, H16Cfg::SMEM_ALLOC, st>>>(wa, s, maps);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(unsigned(wa.G)), dim3(32), H16Cfg::SMEM_ALLOC, st, wa, s, maps);
 }
 
 inline int64_t split_h16_workers() {

@@ -305,7 +305,10 @@ __global__ void __launch_bounds__(32, 12) split_warp_kernel(WarpArgs wa, LayerSr
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + C::BAR_OFF);
     const int64_t T = wa.T, G = wa.G, c = blockIdx.x;
     const int64_t x_begin = c * T / G, x_end = (c + 1) * T / G;
-    pdl_trigger();  // the run merge (launched as a dependent) may be scheduled; it waits for this grid
+    // launched as a dependent of the kernel before (the append of a decode
+    // step): wait for it, then let the run merge be scheduled
+    pdl_wait();
+    pdl_trigger();
     if (x_begin >= x_end) return;
 
     TileCursor cur;
@@ -685,8 +688,7 @@ cudaError_t launch_split_warp(const WarpArgs &wa, const LayerSrc &s, const MmaMa
                     : (imp ? split_warp_kernel<PACK, false, true> : split_warp_kernel<PACK, false, false>);
     cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    kern<<<unsigned(wa.G), 32, C::SMEM_ALLOC, st>>>(wa, s, maps);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(unsigned(wa.G)), dim3(32), C::SMEM_ALLOC, st, wa, s, maps);
 }
 
 // Workers of one launch on the current device: SMs x resident CTAs per SM.
