@@ -77,7 +77,11 @@ __device__ __forceinline__ void quantise_row_warp(const float (&x)[CPL], const f
 
 template <int HD>
 __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(AppendArgs a, AppendTable t) {
-    pdl_trigger();  // a decode launched as a dependent may be scheduled; it waits for this grid
+    // launched as a dependent of the kernel before (the previous step's imp
+    // pass reads the lengths this kernel advances): wait for it, then let a
+    // decode launched as a dependent be scheduled
+    pdl_wait();
+    pdl_trigger();
     constexpr int CPL = HD / 32;
     constexpr int NG = HD / kKGroup;
     const int i = blockIdx.y;
@@ -239,9 +243,9 @@ kvd_status launch_append(const Layer *l, const float *k, const float *v, const A
     const int64_t items = std::max<int64_t>(1, max_count * l->n_live);
     const int64_t per_block = kAppendWarps * kItemsPerWarp;
     dim3 grid(unsigned((items + per_block - 1) / per_block), unsigned(t.n));
-    if (l->hd == 128) append_kernel<128><<<grid, kAppendWarps * 32, 0, s>>>(a, t);
-    else append_kernel<64><<<grid, kAppendWarps * 32, 0, s>>>(a, t);
-    return cudaGetLastError() == cudaSuccess ? KVD_OK : KVD_ECUDA;
+    const cudaError_t e = l->hd == 128 ? launch_pdl(append_kernel<128>, grid, dim3(kAppendWarps * 32), 0, s, a, t)
+                                       : launch_pdl(append_kernel<64>, grid, dim3(kAppendWarps * 32), 0, s, a, t);
+    return e == cudaSuccess ? KVD_OK : KVD_ECUDA;
 }
 
 // Freeze the sequences flagged in `todo` (host view); updates the host mirror.

@@ -422,7 +422,8 @@ __global__ void __launch_bounds__(kImpThreads) imp_kernel(ImpArgs a) {
         }
     };
     load(cls);  // the first batch (scores of the finished split kernel) is in flight across the wait
-    pdl_wait();  // the merge's maxima and sums are complete
+    pdl_wait();     // the merge's maxima and sums are complete
+    pdl_trigger();  // the next append may be scheduled (it waits for this grid)
     for (int i = t; i < nh; i += kImpThreads) {
         const int h = a.live[i / a.hpk] * a.hpk + i % a.hpk;
         const float M = a.ml[(int64_t(b) * a.n_q + h) * 2];
