@@ -3,14 +3,16 @@
 // EvictionPolicy::Born), batched over the sequences of a layer.
 //
 // Per sequence holding more than keep_last rows:
-//   select  one CTA: the middle rows [sinks, stored - recents) compete for
-//           the budget keep_last - sinks - recents by accumulated mass.  An
+//   select  the middle rows [sinks, stored - recents) compete for the
+//           budget keep_last - sinks - recents by accumulated mass.  An
 //           exact radix select over order-preserving 32-bit keys of the
 //           masses finds the budget-th largest key T; every row above T is
 //           kept and, of the rows equal to T, the lowest positions (the
-//           order of the page's stable sort).  Two ordered block scans turn
-//           the keep flags into the ascending list of kept rows, and the
-//           CTA gathers imp along it (clearing the dropped rows' entries).
+//           order of the page's stable sort).  Ordered sums of per-chunk
+//           counts turn the keep flags into the ascending list of kept rows,
+//           and imp follows it (the dropped rows' entries cleared).  A chain
+//           of short kernels, each spreading every sequence over CTAs of
+//           4096 rows (see the select section below).
 //   gather  the kept rows move down to positions 0 .. keep_last - 1 of every
 //           storage independently (f32 K / V, int8 codes, their scales).
 //           Kept positions ascend and kept[j] >= j, so a pass over j in
@@ -21,8 +23,8 @@
 //           workspace copy (one kernel reads a batch, the next writes it), so
 //           every batch spreads over the whole GPU -- or straight from their
 //           sources when the batch's first source lies past its last row.
-// The device length becomes keep_last in the select kernel; the host mirror
-// is updated by the entry point.
+// The device length becomes keep_last in the select's last kernel; the host
+// mirror is updated by the entry point.
 //
 // Also here: cortiq LayerKvCache::truncate_last (the speculative-decode
 // reject), which only shortens the lengths and clears the dropped rows' imp.
@@ -35,7 +37,6 @@
 namespace kvd {
 namespace {
 
-constexpr int kSelectThreads = 1024;
 constexpr int kGatherThreads = 256;
 constexpr int kGatherUnits = 8;  // 16-byte (or smaller) units per thread per tile
 
@@ -62,8 +63,151 @@ __device__ __forceinline__ uint32_t mass_key(float x) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Exclusive prefix sum of `v` over the block in thread order, and the total.
-__device__ __forceinline__ int block_excl_sum(int v, int *warp_sums, int &total) {
+// ---------------------------------------------------------------------------
+// The select over many CTAs.  The same result as one CTA per sequence, in a
+// chain of short kernels that each spread every sequence's rows over CTAs of
+// kChunkRows rows:
+//   sel_init   per entry: the radix state (prefix 0, need = budget), zeroed
+//              histogram;
+//   sel_hist   (x4, digits from the top byte down) each CTA histograms the
+//              digit of its chunk's middle keys that match the prefix so far
+//              and adds its bins into the entry's histogram;
+//   sel_pick   (x4) one warp per entry finds the digit holding the need-th
+//              largest key, extends the prefix and zeroes the histogram;
+//   sel_count  each CTA counts its chunk's rows kept for sure (sinks, recents,
+//              middle keys above the threshold) and its threshold-equal ones;
+//   sel_scan   per entry, exclusive sums of those counts over the chunks in
+//              order, and the check that exactly keep_last rows are kept;
+//   sel_write  each CTA keeps the threshold-equal rows whose rank over the
+//              whole sequence is below `need` (lowest positions first), and
+//              writes its kept rows' positions to the ascending list;
+//   sel_imp    the kept rows' imp entries into a copy, then (sel_imp_put) back
+//              to positions 0 .. keep_last - 1, the dropped rows' entries
+//              cleared, and the device length set.
+// Each kernel is launched as a dependent of the one before (it waits first).
+constexpr int kChunkRows = 4096;          // rows per CTA
+constexpr int kChunkThreads = 256;
+constexpr int kRowsPerThread = kChunkRows / kChunkThreads;  // consecutive rows per thread
+
+struct SelState {
+    uint32_t prefix, mask;
+    int32_t need;         // threshold-equal rows still to keep (after the passes: of the threshold key)
+    int32_t identity;     // 1: the kept count came out wrong; the list is the identity
+};
+
+struct SelArgs {
+    float *imp;
+    int32_t *idx;         // [kSlice][keep_last]
+    float *imp_copy;      // [kSlice][keep_last]
+    SelState *state;      // [kSlice]
+    uint32_t *hist;       // [kSlice][256]
+    int32_t *counts;      // [kSlice][chunks][2]: sure kept, threshold-equal
+    int32_t *offsets;     // [kSlice][chunks][2]: exclusive sums of them
+    int32_t *seq_len;
+    uint32_t *err;
+    int32_t keep_last, sink_n, recent, chunks;
+};
+
+struct SelRange {
+    int stored, hi, budget, recent_n;
+};
+
+__device__ __forceinline__ SelRange sel_range(const SelArgs &a, const BornTable &t, int i) {
+    SelRange r;
+    r.stored = t.stored[i];
+    r.recent_n = min(a.recent, a.keep_last - a.sink_n);
+    r.hi = r.stored - r.recent_n;  // middle rows: [sink_n, hi)
+    r.budget = a.keep_last - a.sink_n - r.recent_n;
+    return r;
+}
+
+__global__ void sel_init_kernel(SelArgs a, BornTable t) {
+    pdl_wait();
+    pdl_trigger();
+    const int i = blockIdx.x;
+    if (i >= t.n) return;
+    a.hist[i * 256 + threadIdx.x] = 0u;
+    if (threadIdx.x == 0) {
+        const SelRange r = sel_range(a, t, i);
+        a.state[i] = SelState{0u, 0u, r.budget > 0 ? r.budget : 0, 0};
+    }
+}
+
+__global__ void __launch_bounds__(kChunkThreads) sel_hist_kernel(SelArgs a, BornTable t, int shift) {
+    __shared__ uint32_t h[256];
+    pdl_wait();
+    pdl_trigger();
+    const int i = blockIdx.y, tid = threadIdx.x;
+    if (i >= t.n) return;
+    const SelRange r = sel_range(a, t, i);
+    const SelState s = a.state[i];
+    const int p0 = a.sink_n + blockIdx.x * kChunkRows, p1 = min(r.hi, p0 + kChunkRows);
+    if (s.need <= 0 || p0 >= p1) return;
+    h[tid] = 0u;
+    __syncthreads();
+    const float *imp = a.imp + t.imp_base[i];
+    float m[kRowsPerThread];
+#pragma unroll
+    for (int u = 0; u < kRowsPerThread; ++u) {
+        const int p = p0 + u * kChunkThreads + tid;
+        m[u] = p < p1 ? imp[p] : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < kRowsPerThread; ++u) {
+        const uint32_t k = mass_key(m[u]);
+        if (p0 + u * kChunkThreads + tid < p1 && (k & s.mask) == s.prefix) atomicAdd(&h[(k >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (h[tid] != 0u) atomicAdd(&a.hist[i * 256 + tid], h[tid]);
+}
+
+// One warp per entry: lane l holds bins 8l .. 8l + 7; the digit holding the
+// need-th largest key is the highest d with (keys of digits >= d) >= need.
+__global__ void sel_pick_kernel(SelArgs a, BornTable t, int shift) {
+    pdl_wait();
+    pdl_trigger();
+    const int i = blockIdx.x, lane = threadIdx.x;
+    if (i >= t.n) return;
+    SelState s = a.state[i];
+    uint32_t *hist = a.hist + i * 256;
+    uint32_t c[8];
+    uint32_t tot = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        c[k] = hist[8 * lane + k];
+        tot += c[k];
+    }
+    // keys in the bins above this lane's: the totals of the higher lanes
+    uint32_t above = 0;
+#pragma unroll
+    for (int L = 31; L > 0; --L) {
+        const uint32_t v = __shfl_sync(0xffffffffu, tot, L);
+        if (L > lane) above += v;
+    }
+    const uint32_t need = uint32_t(s.need);
+    // the lane whose bins hold the need-th key: above < need <= above + tot
+    const bool mine = s.need > 0 && above < need && need <= above + tot;
+    const unsigned who = __ballot_sync(0xffffffffu, mine);
+    if (s.need > 0 && who != 0u && lane == __ffs(who) - 1) {
+        uint32_t cum = above;
+        int d = 8 * lane + 7;
+        for (; d > 8 * lane; --d) {
+            if (cum + c[d - 8 * lane] >= need) break;
+            cum += c[d - 8 * lane];
+        }
+        s.prefix |= uint32_t(d) << shift;
+        s.mask |= 255u << shift;
+        s.need = int32_t(need - cum);
+        a.state[i] = s;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) hist[8 * lane + k] = 0u;
+}
+
+// Exclusive prefix sum of `v` over a kChunkThreads block in thread order, and
+// the total.  `ws` holds kChunkThreads / 32 + 1 ints.
+__device__ __forceinline__ int chunk_excl_sum(int v, int *ws, int &total) {
+    constexpr int W = kChunkThreads / 32;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int incl = v;
 #pragma unroll
@@ -71,157 +215,177 @@ __device__ __forceinline__ int block_excl_sum(int v, int *warp_sums, int &total)
         const int t = __shfl_up_sync(0xffffffffu, incl, off);
         if (lane >= off) incl += t;
     }
-    __syncthreads();  // warp_sums free (a previous call has read it)
-    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();  // ws free (a previous call has read it)
+    if (lane == 31) ws[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        const int w = lane < kSelectThreads / 32 ? warp_sums[lane] : 0;
+        const int w = lane < W ? ws[lane] : 0;
         int wi = w;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             const int t = __shfl_up_sync(0xffffffffu, wi, off);
             if (lane >= off) wi += t;
         }
-        if (lane < kSelectThreads / 32) warp_sums[lane] = wi - w;  // exclusive
-        if (lane == 31) warp_sums[kSelectThreads / 32] = wi;
+        if (lane < W) ws[lane] = wi - w;
+        if (lane == 31) ws[W] = wi;
     }
     __syncthreads();
-    total = warp_sums[kSelectThreads / 32];
-    return warp_sums[warp] + incl - v;
+    total = ws[W];
+    return ws[warp] + incl - v;
 }
 
-constexpr int kSelectRows = 8;   // consecutive rows per thread in the ordered scans
-constexpr int kSelectLoads = 8;  // strided loads in flight per thread in the histogram passes
+// Keep flags of a thread's kRowsPerThread consecutive rows from pb: sure =
+// sinks, recents, middle keys above the threshold; eq = middle keys equal to it.
+__device__ __forceinline__ void sel_flags(const float *imp, const SelRange &r, int sink_n, uint32_t thr, int pb,
+                                          bool (&sure)[kRowsPerThread], bool (&eq)[kRowsPerThread]) {
+    float m[kRowsPerThread];
+#pragma unroll
+    for (int u = 0; u < kRowsPerThread; ++u) {
+        const int p = pb + u;
+        m[u] = (r.budget > 0 && p >= sink_n && p < r.hi) ? imp[p] : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < kRowsPerThread; ++u) {
+        const int p = pb + u;
+        const bool mid = r.budget > 0 && p >= sink_n && p < r.hi;
+        const uint32_t k = mass_key(m[u]);
+        sure[u] = p < r.stored && (p < sink_n || p >= r.hi || (mid && k > thr));
+        eq[u] = mid && k == thr;
+    }
+}
 
-__global__ void __launch_bounds__(kSelectThreads) born_select_kernel(BornArgs a, BornTable t) {
-    __shared__ uint32_t hist[256];
-    __shared__ int warp_sums[kSelectThreads / 32 + 1];
-    __shared__ uint32_t sel_digit;
-    __shared__ int sel_need;
-    const int i = blockIdx.x, tid = threadIdx.x;
+__global__ void __launch_bounds__(kChunkThreads) sel_count_kernel(SelArgs a, BornTable t) {
+    __shared__ int ws[kChunkThreads / 32 + 1];
+    pdl_wait();
+    pdl_trigger();
+    const int i = blockIdx.y, c = blockIdx.x;
     if (i >= t.n) return;
-    const int b = t.seq[i], stored = t.stored[i];
-    const int keep_last = a.keep_last, sink_n = a.sink_n;
-    const int recent_n = min(a.recent, keep_last - sink_n);
-    const int hi = stored - recent_n;  // middle rows: [sink_n, hi)
-    const int budget = keep_last - sink_n - recent_n;
-    float *imp = a.imp + t.imp_base[i];
-    int32_t *idx = a.idx + int64_t(i) * keep_last;
+    const SelRange r = sel_range(a, t, i);
+    if (c * kChunkRows >= r.stored) return;
+    const uint32_t thr = a.state[i].prefix;
+    bool sure[kRowsPerThread], eq[kRowsPerThread];
+    sel_flags(a.imp + t.imp_base[i], r, a.sink_n, thr, c * kChunkRows + threadIdx.x * kRowsPerThread, sure, eq);
+    int ns = 0, ne = 0;
+#pragma unroll
+    for (int u = 0; u < kRowsPerThread; ++u) {
+        ns += sure[u];
+        ne += eq[u];
+    }
+    int tot_s, tot_e;
+    chunk_excl_sum(ns, ws, tot_s);
+    chunk_excl_sum(ne, ws, tot_e);
+    if (threadIdx.x == 0) {
+        a.counts[(int64_t(i) * a.chunks + c) * 2] = tot_s;
+        a.counts[(int64_t(i) * a.chunks + c) * 2 + 1] = tot_e;
+    }
+}
 
-    // ---- radix select of the budget-th largest key among the middle rows
-    uint32_t prefix = 0, mask = 0;
-    int need = budget;
-    if (budget > 0) {
-        for (int shift = 24; shift >= 0; shift -= 8) {
-            for (int d = tid; d < 256; d += kSelectThreads) hist[d] = 0;
-            __syncthreads();
-            // kSelectLoads loads in flight per thread before any is used
-            for (int p0 = sink_n; p0 < hi; p0 += kSelectThreads * kSelectLoads) {
-                float m[kSelectLoads];
+// One warp per entry: exclusive sums of the chunk counts in chunk order.
+__global__ void sel_scan_kernel(SelArgs a, BornTable t) {
+    pdl_wait();
+    pdl_trigger();
+    const int i = blockIdx.x, lane = threadIdx.x;
+    if (i >= t.n) return;
+    const SelRange r = sel_range(a, t, i);
+    const int nc = (r.stored + kChunkRows - 1) / kChunkRows;
+    int carry_s = 0, carry_e = 0;
+    for (int c0 = 0; c0 < nc; c0 += 32) {
+        const int c = c0 + lane;
+        const int64_t o = (int64_t(i) * a.chunks + c) * 2;
+        const int vs = c < nc ? a.counts[o] : 0, ve = c < nc ? a.counts[o + 1] : 0;
+        int is = vs, ie = ve;
 #pragma unroll
-                for (int u = 0; u < kSelectLoads; ++u) {
-                    const int p = p0 + u * kSelectThreads + tid;
-                    m[u] = p < hi ? imp[p] : 0.0f;
-                }
-#pragma unroll
-                for (int u = 0; u < kSelectLoads; ++u) {
-                    const uint32_t k = mass_key(m[u]);
-                    if (p0 + u * kSelectThreads + tid < hi && (k & mask) == prefix)
-                        atomicAdd(&hist[(k >> shift) & 255u], 1u);
-                }
-            }
-            __syncthreads();
-            if (tid == 0) {
-                int cum = 0, d = 255;
-                for (; d > 0; --d) {
-                    if (cum + int(hist[d]) >= need) break;
-                    cum += int(hist[d]);
-                }
-                sel_digit = uint32_t(d);
-                sel_need = need - cum;
-            }
-            __syncthreads();
-            prefix |= sel_digit << shift;
-            mask |= 255u << shift;
-            need = sel_need;
+        for (int off = 1; off < 32; off <<= 1) {
+            const int ts = __shfl_up_sync(0xffffffffu, is, off), te = __shfl_up_sync(0xffffffffu, ie, off);
+            if (lane >= off) is += ts, ie += te;
+        }
+        if (c < nc) {
+            a.offsets[o] = carry_s + is - vs;
+            a.offsets[o + 1] = carry_e + ie - ve;
+        }
+        carry_s += __shfl_sync(0xffffffffu, is, 31);
+        carry_e += __shfl_sync(0xffffffffu, ie, 31);
+    }
+    if (lane == 0) {
+        const int need = a.state[i].need;
+        if (carry_s + min(carry_e, need) != a.keep_last) {
+            // cannot happen for finite masses: report it, and make the list
+            // the identity so that the gather leaves every row where it is
+            set_error(a.err, kErrBounds);
+            a.state[i].identity = 1;
         }
     }
-    // prefix = the threshold key; `need` rows equal to it are kept, lowest first
+}
 
-    // ---- keep flags -> ascending list of kept rows (kSelectRows consecutive
-    // rows per thread, in thread order)
-    int eq_carry = 0, out_carry = 0;
-    for (int p0 = 0; p0 < stored; p0 += kSelectThreads * kSelectRows) {
-        const int pb = p0 + tid * kSelectRows;
-        bool mid_gt[kSelectRows], mid_eq[kSelectRows];
-        float mv[kSelectRows];
-#pragma unroll
-        for (int u = 0; u < kSelectRows; ++u) {
-            const int p = pb + u;
-            mv[u] = (budget > 0 && p >= sink_n && p < hi) ? imp[p] : 0.0f;
-        }
-        int n_eq = 0;
-#pragma unroll
-        for (int u = 0; u < kSelectRows; ++u) {
-            const int p = pb + u;
-            mid_gt[u] = mid_eq[u] = false;
-            if (budget > 0 && p >= sink_n && p < hi) {
-                const uint32_t k = mass_key(mv[u]);
-                mid_gt[u] = k > prefix;
-                mid_eq[u] = k == prefix;
-            }
-            n_eq += mid_eq[u];
-        }
-        int eq_total;
-        int eq_rank = eq_carry + block_excl_sum(n_eq, warp_sums, eq_total);
-        eq_carry += eq_total;
-        bool keep[kSelectRows];
-        int n_keep = 0;
-#pragma unroll
-        for (int u = 0; u < kSelectRows; ++u) {
-            const int p = pb + u;
-            keep[u] = p < stored && (p < sink_n || p >= hi || mid_gt[u] || (mid_eq[u] && eq_rank < need));
-            eq_rank += mid_eq[u];
-            n_keep += keep[u];
-        }
-        int out_total;
-        int pos = out_carry + block_excl_sum(n_keep, warp_sums, out_total);
-        out_carry += out_total;
-#pragma unroll
-        for (int u = 0; u < kSelectRows; ++u) {
-            if (keep[u] && pos < keep_last) idx[pos] = pb + u;
-            pos += keep[u];
-        }
-    }
-    __syncthreads();
-    if (out_carry != keep_last) {
-        // cannot happen for finite masses: report it, and make the list the
-        // identity so that the gather leaves every row where it is
-        if (tid == 0) set_error(a.err, kErrBounds);
-        for (int j = tid; j < keep_last; j += kSelectThreads) idx[j] = j;
+__global__ void __launch_bounds__(kChunkThreads) sel_write_kernel(SelArgs a, BornTable t) {
+    __shared__ int ws[kChunkThreads / 32 + 1];
+    pdl_wait();
+    pdl_trigger();
+    const int i = blockIdx.y, c = blockIdx.x;
+    if (i >= t.n) return;
+    const SelRange r = sel_range(a, t, i);
+    if (c * kChunkRows >= r.stored) return;
+    int32_t *idx = a.idx + int64_t(i) * a.keep_last;
+    const SelState s = a.state[i];
+    if (s.identity) {
+        for (int j = c * kChunkRows + threadIdx.x; j < min(a.keep_last, (c + 1) * kChunkRows); j += kChunkThreads)
+            idx[j] = j;
         return;
     }
-
-    // ---- imp follows its rows (in place, tiles in order); the entries of the
-    // dropped rows are cleared: a row appended there later starts from zero
-    // mass, as each appended row does on the page
-    for (int j0 = sink_n; j0 < keep_last; j0 += kSelectThreads * kSelectLoads) {
-        float v[kSelectLoads];
+    const int pb = c * kChunkRows + threadIdx.x * kRowsPerThread;
+    bool sure[kRowsPerThread], eq[kRowsPerThread];
+    sel_flags(a.imp + t.imp_base[i], r, a.sink_n, s.prefix, pb, sure, eq);
+    const int64_t o = (int64_t(i) * a.chunks + c) * 2;
+    const int sure_before = a.offsets[o], eq_before = a.offsets[o + 1];
+    int ne = 0;
 #pragma unroll
-        for (int u = 0; u < kSelectLoads; ++u) {
-            const int j = j0 + u * kSelectThreads + tid;
-            v[u] = j < keep_last ? imp[idx[j]] : 0.0f;
-        }
-        __syncthreads();
+    for (int u = 0; u < kRowsPerThread; ++u) ne += eq[u];
+    int tot;
+    int eq_rank = eq_before + chunk_excl_sum(ne, ws, tot);
+    bool keep[kRowsPerThread];
+    int nk = 0;
 #pragma unroll
-        for (int u = 0; u < kSelectLoads; ++u) {
-            const int j = j0 + u * kSelectThreads + tid;
-            if (j < keep_last) imp[j] = v[u];
-        }
-        __syncthreads();
+    for (int u = 0; u < kRowsPerThread; ++u) {
+        keep[u] = sure[u] || (eq[u] && eq_rank < s.need);  // equal keys: the lowest positions first
+        eq_rank += eq[u];
+        nk += keep[u];
     }
-    for (int j = keep_last + tid; j < stored; j += kSelectThreads) imp[j] = 0.0f;
-    if (tid == 0) a.seq_len[b] = keep_last;
+    int pos = sure_before + min(eq_before, s.need) + chunk_excl_sum(nk, ws, tot);
+#pragma unroll
+    for (int u = 0; u < kRowsPerThread; ++u) {
+        if (keep[u] && pos < a.keep_last) idx[pos] = pb + u;
+        pos += keep[u];
+    }
+}
+
+// The kept rows' masses into the copy (rows below sink_n stay where they are).
+__global__ void sel_imp_get_kernel(SelArgs a, BornTable t) {
+    pdl_wait();
+    pdl_trigger();
+    const int i = blockIdx.y;
+    if (i >= t.n || a.state[i].identity) return;
+    const float *imp = a.imp + t.imp_base[i];
+    const int32_t *idx = a.idx + int64_t(i) * a.keep_last;
+    float *cp = a.imp_copy + int64_t(i) * a.keep_last;
+    const int j0 = a.sink_n + blockIdx.x * kChunkRows;
+    for (int j = j0 + threadIdx.x; j < min(a.keep_last, j0 + kChunkRows); j += blockDim.x) cp[j] = imp[idx[j]];
+}
+
+// The copy back to rows sink_n .. keep_last - 1, the dropped rows' entries
+// cleared (a row appended there later starts from zero mass, as each appended
+// row does on the page), and the device length.
+__global__ void sel_imp_put_kernel(SelArgs a, BornTable t) {
+    pdl_wait();
+    pdl_trigger();
+    const int i = blockIdx.y;
+    if (i >= t.n || a.state[i].identity) return;
+    const int stored = t.stored[i];
+    float *imp = a.imp + t.imp_base[i];
+    const float *cp = a.imp_copy + int64_t(i) * a.keep_last;
+    const int j0 = a.sink_n + blockIdx.x * kChunkRows;
+    for (int j = j0 + threadIdx.x; j < min(stored, j0 + kChunkRows); j += blockDim.x)
+        imp[j] = j < a.keep_last ? cp[j] : 0.0f;
+    if (blockIdx.x == 0 && threadIdx.x == 0) a.seq_len[t.seq[i]] = a.keep_last;
 }
 
 // log2 of a power of two.
@@ -404,14 +568,38 @@ int64_t row_bytes_all(const Layer *l) {
 
 int64_t ceil_div_ev(int64_t x, int64_t y) { return (x + y - 1) / y; }
 
+int64_t round256(int64_t x) { return (x + 255) / 256 * 256; }
+
 int64_t evict_idx_bytes(const Layer *l, int64_t keep_last) {
-    return (int64_t(std::min(kSlice, l->n_seq)) * keep_last * 4 + 255) / 256 * 256;
+    return round256(int64_t(std::min(kSlice, l->n_seq)) * keep_last * 4);
+}
+
+// Chunks of kChunkRows rows of the longest sequence the layer can hold.
+int32_t sel_chunks(const Layer *l) { return int32_t(std::max<int64_t>(1, ceil_div_ev(l->max_cap, kChunkRows))); }
+
+// The workspace before the batched gather's copy: the kept lists, the masses'
+// copy, then the select's state, histograms, chunk counts and their sums.
+struct SelLayout {
+    int64_t idx, imp_copy, state, hist, counts, offsets, end;
+};
+
+SelLayout sel_layout(const Layer *l, int64_t keep_last) {
+    const int64_t n = std::min(kSlice, l->n_seq);
+    SelLayout w;
+    w.idx = 0;
+    w.imp_copy = evict_idx_bytes(l, keep_last);
+    w.state = w.imp_copy + evict_idx_bytes(l, keep_last);
+    w.hist = w.state + round256(n * int64_t(sizeof(SelState)));
+    w.counts = w.hist + round256(n * 256 * 4);
+    w.offsets = w.counts + round256(n * sel_chunks(l) * 8);
+    w.end = w.offsets + round256(n * sel_chunks(l) * 8);
+    return w;
 }
 
 int64_t evict_ws_bytes(const Layer *l, int64_t keep_last) {
     const int64_t stage = std::min(kEvictStage, int64_t(std::min(kSlice, l->n_seq)) * std::max(1, l->n_live) *
                                                     keep_last * row_bytes_all(l));
-    return evict_idx_bytes(l, keep_last) + (stage + 255) / 256 * 256;
+    return sel_layout(l, keep_last).end + round256(stage);
 }
 
 }  // namespace
@@ -441,9 +629,11 @@ extern "C" kvd_status kv_evict_born(kvd_layer *L, float *imp, int64_t keep_last,
         if (l->h_seq_len[b] > keep_last) todo.push_back(b);
     if (todo.empty()) return KVD_OK;
     cudaStream_t st = as_stream(stream);
+    const SelLayout wl = sel_layout(l, keep_last);
+    char *wsb = static_cast<char *>(workspace);
     BornArgs a;
     a.imp = imp;
-    a.idx = static_cast<int32_t *>(workspace);  // the stage of the batched gather follows the lists
+    a.idx = reinterpret_cast<int32_t *>(wsb + wl.idx);  // the stage of the batched gather follows the select's data
     a.seq_len = l->d_seq_len;
     a.err = l->d_err;
     a.keep_last = int32_t(keep_last);
@@ -474,6 +664,20 @@ extern "C" kvd_status kv_evict_born(kvd_layer *L, float *imp, int64_t keep_last,
     g.cap = l->d_cap;
     g.keep_last = a.keep_last;
     g.sink_n = a.sink_n;
+    SelArgs sa;
+    sa.imp = imp;
+    sa.idx = a.idx;
+    sa.imp_copy = reinterpret_cast<float *>(wsb + wl.imp_copy);
+    sa.state = reinterpret_cast<SelState *>(wsb + wl.state);
+    sa.hist = reinterpret_cast<uint32_t *>(wsb + wl.hist);
+    sa.counts = reinterpret_cast<int32_t *>(wsb + wl.counts);
+    sa.offsets = reinterpret_cast<int32_t *>(wsb + wl.offsets);
+    sa.seq_len = l->d_seq_len;
+    sa.err = l->d_err;
+    sa.keep_last = a.keep_last;
+    sa.sink_n = a.sink_n;
+    sa.recent = a.recent;
+    sa.chunks = sel_chunks(l);
     for (size_t s0 = 0; s0 < todo.size(); s0 += kSlice) {
         BornTable t;
         t.n = int32_t(std::min<size_t>(kSlice, todo.size() - s0));
@@ -483,11 +687,24 @@ extern "C" kvd_status kv_evict_born(kvd_layer *L, float *imp, int64_t keep_last,
             t.stored[i] = int32_t(l->h_seq_len[b]);
             t.imp_base[i] = l->h_imp_base[b];
         }
-        born_select_kernel<<<unsigned(t.n), kSelectThreads, 0, st>>>(a, t);
-        if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
+        int64_t most = 0;
+        for (int i = 0; i < t.n; ++i) most = std::max<int64_t>(most, t.stored[i]);
+        const unsigned chunks = unsigned(ceil_div_ev(most, kChunkRows));
+        const dim3 cgrid(chunks, unsigned(t.n)), eg(unsigned(t.n));
+        cudaError_t e = launch_pdl(sel_init_kernel, eg, dim3(256), 0, st, sa, t);
+        for (int shift = 24; shift >= 0 && e == cudaSuccess; shift -= 8) {
+            e = launch_pdl(sel_hist_kernel, cgrid, dim3(kChunkThreads), 0, st, sa, t, shift);
+            if (e == cudaSuccess) e = launch_pdl(sel_pick_kernel, eg, dim3(32), 0, st, sa, t, shift);
+        }
+        if (e == cudaSuccess) e = launch_pdl(sel_count_kernel, cgrid, dim3(kChunkThreads), 0, st, sa, t);
+        if (e == cudaSuccess) e = launch_pdl(sel_scan_kernel, eg, dim3(32), 0, st, sa, t);
+        if (e == cudaSuccess) e = launch_pdl(sel_write_kernel, cgrid, dim3(kChunkThreads), 0, st, sa, t);
+        if (e == cudaSuccess) e = launch_pdl(sel_imp_get_kernel, cgrid, dim3(kChunkThreads), 0, st, sa, t);
+        if (e == cudaSuccess) e = launch_pdl(sel_imp_put_kernel, cgrid, dim3(kChunkThreads), 0, st, sa, t);
+        if (e != cudaSuccess) return KVD_ECUDA;
         if (l->n_live <= 0 || g.n_st <= 0 || keep_last <= a.sink_n) continue;
         const int64_t regions = int64_t(t.n) * l->n_live * g.n_st;
-        const int64_t stage_bytes = workspace_bytes - evict_idx_bytes(l, keep_last);
+        const int64_t stage_bytes = workspace_bytes - wl.end;
         const int64_t per_row = int64_t(t.n) * l->n_live * row_bytes_all(l);  // one j across the batch
         const int64_t pad = int64_t(t.n) * l->n_live * g.n_st * 16;            // blocks padded to 16 bytes
         const int64_t batch = (stage_bytes - pad) / per_row;
@@ -499,7 +716,7 @@ extern "C" kvd_status kv_evict_born(kvd_layer *L, float *imp, int64_t keep_last,
         }
         BatchArgs ba;
         ba.g = g;
-        ba.stage = static_cast<char *>(workspace) + evict_idx_bytes(l, keep_last);
+        ba.stage = wsb + wl.end;
         ba.n_live = l->n_live;
         for (int64_t j0 = a.sink_n; j0 < keep_last; j0 += batch) {
             ba.j0 = int32_t(j0);
