@@ -168,8 +168,11 @@ KVD_API kvd_status decode_attention_verify(const float *q, const kvd_layer *L, i
 KVD_API kvd_status kv_truncate_last(kvd_layer *L, const int32_t *n_drop, float *imp, void *stream);
 
 /* Workspace bytes kv_evict_born needs for a given keep_last: the kept-row
- * lists plus, for layers with few (sequence, live head, storage) regions,
- * up to 64 MiB of staging for the batched gather. */
+ * lists and a copy of their masses (keep_last entries each for up to 256
+ * sequences), the select's per-sequence state, digit histograms and
+ * per-4096-row chunk counts, plus, for layers with few (sequence, live head,
+ * storage) regions, up to 64 MiB of staging for the batched gather.  No
+ * initialisation needed. */
 KVD_API kvd_status kv_evict_workspace_bytes(const kvd_layer *L, int64_t keep_last, int64_t *bytes_out);
 
 /* cortiq LayerKvCache::evict_born for every sequence of the layer holding
