@@ -21,8 +21,9 @@
 //           live head x storage) one CTA walks each region's tiles in order,
 //           in place; with few, the rows go in batches of j through a
 //           workspace copy (one kernel reads a batch, the next writes it), so
-//           every batch spreads over the whole GPU -- or straight from their
-//           sources when the batch's first source lies past its last row.
+//           every batch spreads over the whole GPU; only rows whose source
+//           lies inside the batch's own rows take the copy, the others are
+//           copied straight across by the second kernel.
 // The device length becomes keep_last in the select's last kernel; the host
 // mirror is updated by the entry point.
 //
@@ -443,9 +444,9 @@ __device__ void gather_region(U *region, int upr, const int32_t *kept, int sink_
 }
 
 // Batched gather: rows j in [j0, j1) of every region (blockIdx.y = live head
-// x storage, blockIdx.z = table entry), through the workspace copy `stage`
-// laid out [entry][live head][storage block of (j1 - j0) rows, padded to 16
-// bytes].  to_stage: read the kept sources into it; else write it to rows j.
+// x storage, blockIdx.z = table entry), the rows whose sources lie inside the
+// batch through the workspace copy `stage` laid out [entry][live head][storage
+// block of (j1 - j0) rows, padded to 16 bytes].
 struct BatchArgs {
     GatherArgs g;
     char *stage;
@@ -456,40 +457,55 @@ struct BatchArgs {
 
 // Rows are a power-of-two number of units U (16-byte units where the row
 // holds whole ones, else 4-byte words), so row and unit come from shifts.
+// Rows j0 .. j0 + rows - 1 of one region.  A row whose source lies at or past
+// the batch's end (kept[j] >= j1) is copied straight across by the second
+// kernel: neither kernel writes there, and later batches write there only
+// after this one.  A row whose source lies inside the batch's own rows goes
+// through the stage: the first kernel reads all of those before the second
+// writes any row.  Rows are a power-of-two number of units U (16-byte units
+// where the row holds whole ones, else 4-byte words), so row and unit come
+// from shifts.
 template <bool TO_STAGE, typename U>
 __device__ __forceinline__ void batch_copy(U *region, U *stage, int lu, const int32_t *kept, int j0, int rows,
                                            int64_t cap, uint32_t *err) {
-    const int n = rows << lu;
-    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < n; e += gridDim.x * blockDim.x) {
-        const int j = j0 + (e >> lu), w = e & ((1 << lu) - 1);
-        if (TO_STAGE) {
-            const int32_t src = kept[j];
-            if (src >= 0 && src < cap) stage[e] = region[(int64_t(src) << lu) + w];
-            else set_error(err, kErrBounds);
-        } else {
-            region[(int64_t(j) << lu) + w] = stage[e];
+    constexpr int kIn = 4;  // units per thread in flight
+    const int n = rows << lu, j1 = j0 + rows;
+    const int stride = gridDim.x * blockDim.x;
+    for (int e0 = blockIdx.x * blockDim.x + threadIdx.x; e0 < n; e0 += kIn * stride) {
+        int32_t src[kIn];
+        U v[kIn];
+#pragma unroll
+        for (int k = 0; k < kIn; ++k) {
+            const int e = e0 + k * stride;
+            src[k] = -1;
+            if (e < n) {
+                const int j = j0 + (e >> lu), w = e & ((1 << lu) - 1);
+                src[k] = kept[j];
+                if (src[k] < 0 || src[k] >= cap) {
+                    if (TO_STAGE) set_error(err, kErrBounds);
+                    src[k] = -1;
+                } else if (TO_STAGE ? src[k] < j1 : src[k] >= j1) {
+                    v[k] = region[(int64_t(src[k]) << lu) + w];
+                } else if (!TO_STAGE) {
+                    v[k] = stage[e];
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kIn; ++k) {
+            const int e = e0 + k * stride;
+            if (src[k] < 0) continue;
+            if (TO_STAGE) {
+                if (src[k] < j1) stage[e] = v[k];
+            } else {
+                region[(int64_t(j0 + (e >> lu)) << lu) + (e & ((1 << lu) - 1))] = v[k];
+            }
         }
     }
 }
 
-// The batch's rows straight from their sources, for a batch whose every source
-// lies at or past its end (kept[j0] >= j1, kept ascending): no row the batch
-// writes is a source of it or of a later batch.
-template <typename U>
-__device__ __forceinline__ void direct_copy(U *region, int lu, const int32_t *kept, int j0, int rows, int64_t cap,
-                                            uint32_t *err) {
-    const int n = rows << lu;
-    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < n; e += gridDim.x * blockDim.x) {
-        const int j = j0 + (e >> lu), w = e & ((1 << lu) - 1);
-        const int32_t src = kept[j];
-        if (src >= 0 && src < cap) region[(int64_t(j) << lu) + w] = region[(int64_t(src) << lu) + w];
-        else set_error(err, kErrBounds);
-    }
-}
-
-// to_stage: read the batch's sources into the stage (or, for a batch whose
-// sources all lie past it, copy it directly); else write the stage to its rows
-// (nothing for a direct batch).
+// to_stage: read the batch's rows whose sources lie inside it into the stage;
+// else write every row of the batch (from the stage, or from its source).
 template <bool TO_STAGE>
 __global__ void __launch_bounds__(kGatherThreads) born_batch_kernel(BatchArgs a, BornTable t) {
     const int i = blockIdx.z;
@@ -502,15 +518,7 @@ __global__ void __launch_bounds__(kGatherThreads) born_batch_kernel(BatchArgs a,
     char *stage = a.stage + (int64_t(i) * a.n_live + gl) * a.stage_group + a.st_off[s];
     const int32_t *kept = a.g.idx + int64_t(i) * a.g.keep_last;
     const int rows = a.j1 - a.j0;
-    if (kept[a.j0] >= a.j1) {
-        if (!TO_STAGE) return;
-        if (g.row_bytes % 16 == 0)
-            direct_copy(reinterpret_cast<uint4 *>(region), log2_exact(g.row_bytes / 16), kept, a.j0, rows, cap, a.g.err);
-        else
-            direct_copy(reinterpret_cast<uint32_t *>(region), log2_exact(g.row_bytes / 4), kept, a.j0, rows, cap,
-                        a.g.err);
-        return;
-    }
+    if (TO_STAGE && kept[a.j0] >= a.j1) return;  // every source lies past the batch
     if (g.row_bytes % 16 == 0)
         batch_copy<TO_STAGE>(reinterpret_cast<uint4 *>(region), reinterpret_cast<uint4 *>(stage),
                              log2_exact(g.row_bytes / 16), kept, a.j0, rows, cap, a.g.err);
@@ -727,8 +735,9 @@ extern "C" kvd_status kv_evict_born(kvd_layer *L, float *imp, int64_t keep_last,
                 off += (int64_t(ba.j1 - ba.j0) * g.st[k].row_bytes + 15) / 16 * 16;
             }
             ba.stage_group = off;
-            const int64_t units = int64_t(ba.j1 - ba.j0) * 8;  // a code region's 16-byte units, for the grid
-            dim3 grid(unsigned(std::max<int64_t>(1, std::min<int64_t>(ceil_div_ev(units, kGatherThreads), 1024))),
+            // a code region's 16-byte units, four per thread in flight
+            const int64_t units = int64_t(ba.j1 - ba.j0) * 8;
+            dim3 grid(unsigned(std::max<int64_t>(1, std::min<int64_t>(ceil_div_ev(units, 4 * kGatherThreads), 256))),
                       unsigned(l->n_live * g.n_st), unsigned(t.n));
             born_batch_kernel<true><<<grid, kGatherThreads, 0, st>>>(ba, t);
             born_batch_kernel<false><<<grid, kGatherThreads, 0, st>>>(ba, t);
