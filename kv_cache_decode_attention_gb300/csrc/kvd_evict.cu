@@ -65,9 +65,8 @@ __device__ __forceinline__ uint32_t mass_key(float x) {
 }
 
 // ---------------------------------------------------------------------------
-// The select over many CTAs.  The same result as one CTA per sequence, in a
-// chain of short kernels that each spread every sequence's rows over CTAs of
-// kChunkRows rows:
+// The select over many CTAs: a chain of short kernels that each spread every
+// sequence's rows over CTAs of kChunkRows rows:
 //   sel_init   per entry: the radix state (prefix 0, need = budget), zeroed
 //              histogram;
 //   sel_hist   (x4, digits from the top byte down) each CTA histograms the
