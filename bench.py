@@ -53,8 +53,8 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
 # profiles/decode_q8_gqa_traffic.md), valid while the kernel sources hash to
 # the captured version; reported as null otherwise.
 TRAFFIC = {
-    "q8_gqa": {"sources_sha256": "1334e125e5a573f20352046e1a66ed1e37f14ba4c688b16c8cbf3e2eb3eb3d27",
-               "bytes": 300557184},
+    "q8_gqa": {"sources_sha256": "5c4581bf16aea7fbf8f30bf0ec7c2414260f513d409977118e070810a01f44ba",
+               "bytes": 300744320},
 }
 
 
