@@ -120,9 +120,10 @@ struct ChunkInfo {
 };
 
 // Butterfly reduce-scatter of E partial sums held by every lane: after it,
-// lane l holds in v[0] the full warp sum of entry l >> (5 - LOGE).
-template <int E, int LOGE>
-__device__ __forceinline__ float reduce_scatter(float (&v)[E], int lane) {
+// lane l holds in v[0] the full warp sum of entry l >> (5 - LOGE).  T: float,
+// or int for exact integer partials.
+template <int E, int LOGE, typename T>
+__device__ __forceinline__ T reduce_scatter(T (&v)[E], int lane) {
 #pragma unroll
     for (int s = 0; s < LOGE; ++s) {
         const int off = 16 >> s;
@@ -130,8 +131,8 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[E], int lane) {
         const bool upper = (lane & off) != 0;
 #pragma unroll
         for (int i = 0; i < half; ++i) {
-            const float send = upper ? v[i] : v[i + half];
-            const float keep = upper ? v[i + half] : v[i];
+            const T send = upper ? v[i] : v[i + half];
+            const T keep = upper ? v[i + half] : v[i];
             v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
         }
     }
@@ -310,16 +311,16 @@ __device__ void split_body(const ChunkInfo &ci, const SplitArgs &a, char *smem) 
         for (int bt = 0; bt < C::RPW / C::RB; ++bt) {
             const int rbase = warp * C::RPW + bt * C::RB;
             float v[C::E];
+            int vi[C::E];  // KI8: the codes' dot products, exact integers
 #pragma unroll
             for (int r = 0; r < C::RB; ++r) {
                 if (KI8) {
-                    // exact: |partial| <= 4 * 127 * 127 and every sum of the
-                    // reduction stays an integer below 2^24
+                    // exact: |partial| <= 4 * 127 * 127, the warp sum <= 128 * 127 * 127
                     const char *kr = kseg + (rbase + r) * C::KROW;
                     const uint32_t kw = CPL == 4 ? reinterpret_cast<const uint32_t *>(kr)[lane]
                                                  : uint32_t(reinterpret_cast<const uint16_t *>(kr)[lane]);
 #pragma unroll
-                    for (int h = 0; h < HPK; ++h) v[r * HPK + h] = float(__dp4a(int(qi[h]), int(kw), 0));
+                    for (int h = 0; h < HPK; ++h) vi[r * HPK + h] = __dp4a(int(qi[h]), int(kw), 0);
                     continue;
                 }
                 float x[CPL];
@@ -336,7 +337,9 @@ __device__ void split_body(const ChunkInfo &ci, const SplitArgs &a, char *smem) 
                     v[r * HPK + h] = KQ ? p * gs : p;
                 }
             }
-            float s = reduce_scatter<C::E, C::LOGE>(v, lane);
+            // KI8: reduced in integers, one conversion per row and query
+            // (an integer below 2^24, so the float is the same either way)
+            float s = KI8 ? float(reduce_scatter<C::E, C::LOGE>(vi, lane)) : reduce_scatter<C::E, C::LOGE>(v, lane);
             if ((lane & ((32 >> C::LOGE) - 1)) == 0) {
                 const int e = lane >> (5 - C::LOGE);
                 const int r = rbase + e / HPK, h = e % HPK;
