@@ -53,8 +53,8 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
 # profiles/decode_q8_gqa_traffic.md), valid while the kernel sources hash to
 # the captured version; reported as null otherwise.
 TRAFFIC = {
-    "q8_gqa": {"sources_sha256": "5c4581bf16aea7fbf8f30bf0ec7c2414260f513d409977118e070810a01f44ba",
-               "bytes": 300744320},
+    "q8_gqa": {"sources_sha256": "8ffb72feb5a3ab60f7e55e32a105cda6a2518abe06885004b8c6fb9c077a52e3",
+               "bytes": 300547328},
 }
 
 
