@@ -53,8 +53,8 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
 # profiles/decode_q8_gqa_traffic.md), valid while the kernel sources hash to
 # the captured version; reported as null otherwise.
 TRAFFIC = {
-    "q8_gqa": {"sources_sha256": "8ffb72feb5a3ab60f7e55e32a105cda6a2518abe06885004b8c6fb9c077a52e3",
-               "bytes": 300547328},
+    "q8_gqa": {"sources_sha256": "28371b22867eb403006a3b64ac36869082a6b968888e1803a6d9a0fe77fe9406",
+               "bytes": 300610560},
 }
 
 

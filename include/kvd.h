@@ -266,6 +266,15 @@ KVD_API kvd_status decode_attention_static(const float *q, const kvd_layer *L, i
  * found metadata out of range and skipped the access. */
 KVD_API kvd_status kvd_layer_device_error(const kvd_layer *L, int32_t clear, uint32_t *word_out);
 
+/* The bounded-wait path, run on purpose (a diagnostic: the pages have no
+ * counterpart).  One warp waits for an mbarrier phase that nothing
+ * completes, gives up after limit_ns nanoseconds and sets bit 0 of the
+ * layer's device error word, as a decode kernel whose copies never landed
+ * would; the kernel exits normally and the context stays usable.  Read the
+ * word with kvd_layer_device_error after synchronising the stream.
+ * KVD_EINVAL for limit_ns outside 1 .. 10^9. */
+KVD_API kvd_status kvd_wait_timeout_selftest(const kvd_layer *L, int64_t limit_ns, void *stream);
+
 /* ---- R-SWA (rswa module): retained prefix + W-slot ring, per stream ----
  * Per stream s and head h the reference block is ref[s][h][0..ref_cap) and
  * the ring ring[s][h][0..W), rows of head_dim f32 (head-major, as rswa

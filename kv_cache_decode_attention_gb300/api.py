@@ -116,6 +116,12 @@ class LayerKvCache:
             _abi.check("kvd_layer_device_error", st)
         return int(w.value)
 
+    def wait_timeout_selftest(self, limit_ns: int = 2_000_000, stream=None):
+        """Run the bounded-wait path on purpose: one warp waits for a barrier
+        phase nothing completes, gives up after limit_ns and sets bit 0 of the
+        device error word (read it with device_error() after synchronising)."""
+        _abi.call("kvd_wait_timeout_selftest", C.byref(self.L), int(limit_ns), _stream(stream))
+
     def reset(self, seq: int = -1, stream=None):
         _abi.call("kvd_layer_reset", C.byref(self.L), int(seq), _stream(stream))
 

@@ -340,6 +340,32 @@ extern "C" kvd_status kvd_layer_device_error(const kvd_layer *L, int32_t clear,
     return w ? KVD_EDEVICE : KVD_OK;
 }
 
+namespace kvd {
+namespace {
+
+// One warp waits for a phase of an mbarrier that nothing completes, as a
+// kernel whose copies never land would, gives up after limit_ns and records
+// it the way every kernel here does: no trap, the error bit, a normal exit.
+__global__ void wait_selftest_kernel(uint32_t *err, uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    if (threadIdx.x == 0 && !mbar_wait_bounded(&bar, 0u, limit_ns)) set_error(err, kErrTimeout);
+}
+
+}  // namespace
+}  // namespace kvd
+
+extern "C" kvd_status kvd_wait_timeout_selftest(const kvd_layer *L, int64_t limit_ns, void *stream) {
+    const Layer *l = checked_layer(L);
+    if (l == nullptr || limit_ns < 1 || limit_ns > 1000000000) return KVD_EINVAL;
+    wait_selftest_kernel<<<1, 32, 0, as_stream(stream)>>>(l->d_err, uint64_t(limit_ns));
+    return cudaGetLastError() == cudaSuccess ? KVD_OK : KVD_ECUDA;
+}
+
 extern "C" const char *kvd_status_string(int32_t status) {
     switch (status) {
         case KVD_OK: return "ok";

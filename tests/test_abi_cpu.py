@@ -116,6 +116,7 @@ def test_layer_calls_reject_uninitialised_descriptor(abi):
     assert L.kvd_decode_workspace_bytes(C.byref(lay), 8, 0, C.byref(n)) == abi.EINVAL
     assert L.kv_append(C.byref(lay), C.c_void_p(16), C.c_void_p(16), None, None) == abi.EINVAL
     assert L.kv_freeze_colfield(C.byref(lay), None) == abi.EINVAL
+    assert L.kvd_wait_timeout_selftest(C.byref(lay), 1000, None) == abi.EINVAL
     assert L.kvd_status_string(abi.ECAPACITY) == b"capacity exceeded"
 
 

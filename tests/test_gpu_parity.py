@@ -222,6 +222,25 @@ def test_tiny_f32_gqa_config(torch, kvd):
     assert abs(got.sum() - n_kv * hpk) < 1e-3  # every head's weights sum to one
 
 
+def test_bounded_wait_times_out_and_context_stays_usable(torch, kvd):
+    """A wait that nothing satisfies gives up after its limit and reports it
+    through the device error word (bit 0) -- no trap, no hang -- and the same
+    context then decodes correctly with a clean word."""
+    lengths = [300, 77]
+    alive = np.array([1, 1], np.uint8)
+    layer = _layer(kvd, MODES["q8"], lengths, 2, 128, alive, cap_extra=3)
+    ks, vs = seq_rows(lengths, 2, 128, seed=5)
+    gpu_append_bulk(layer, ks, vs, torch)
+    assert layer.device_error() == 0
+    layer.wait_timeout_selftest(2_000_000)  # 2 ms
+    torch.cuda.synchronize()
+    assert layer.device_error(clear=True) == 1  # bit 0: a bounded wait timed out
+    assert layer.device_error() == 0
+    with pytest.raises(kvd.KvdError):
+        layer.wait_timeout_selftest(0)  # refused on the host, nothing launched
+    _decode_case(torch, kvd, MODES["q8"], 128, 4, lengths, alive, seed=5)
+
+
 def test_all_groups_dead_and_capacity_errors(torch, kvd):
     layer = kvd.LayerKvCache(2, 2, 128, "q8", [8, 8], alive=[0, 0])
     k = torch.randn(2, 2, 128, device="cuda")
