@@ -176,7 +176,7 @@ _OPTS = {
 
 
 @pytest.mark.parametrize("mode", list(MODES))
-@pytest.mark.parametrize("hpk", [4, 16])
+@pytest.mark.parametrize("hpk", [4, 8, 16])
 @pytest.mark.parametrize("opt", list(_OPTS))
 def test_decode_options_parity(torch, kvd, mode, hpk, opt):
     """[cortiq] attend_group_upto's window (first = stored - window), logit
