@@ -147,6 +147,15 @@ def test_decode_parity_hd128(torch, kvd, mode, hpk):
                  np.array([1, 1, 0, 1], np.uint8), seed=11 + hpk)
 
 
+# The tensor-core kernels compile the imp score stores out when the call has no
+# imp: each of those variants (heads in N with packed or chained query terms,
+# heads in M), the benchmark's roofline kernel among them.
+@pytest.mark.parametrize("hpk", [1, 4, 8, 16])
+def test_decode_q8_without_imp(torch, kvd, hpk):
+    _decode_case(torch, kvd, oracle.Q8, 128, hpk, [0, 1, 64, 300, 777, 1030, 2100],
+                 np.array([1, 1, 0, 1], np.uint8), seed=41 + hpk, with_imp=False)
+
+
 # q8_2f at head_dim 128 runs on the tensor-core kernels, whose run partials are
 # merged by one warp per query head (up to 16 slots per unit in one batch of
 # loads, up to 32 in two) or by one CTA per query head beyond that.  With fewer
