@@ -141,7 +141,7 @@ def _decode_case(torch, kvd, mode, hd, hpk, lengths, alive, seed, with_imp=True,
 
 
 @pytest.mark.parametrize("mode", list(MODES))
-@pytest.mark.parametrize("hpk", [1, 3, 4, 8, 12, 16])
+@pytest.mark.parametrize("hpk", [1, 2, 3, 4, 8, 12, 16])
 def test_decode_parity_hd128(torch, kvd, mode, hpk):
     _decode_case(torch, kvd, MODES[mode], 128, hpk, [0, 1, 64, 300, 777, 1030],
                  np.array([1, 1, 0, 1], np.uint8), seed=11 + hpk)
