@@ -550,7 +550,9 @@ def run_gpu_rswa(args, rank, world):
                    "parallelism": "replicas" if world > 1 else "single"},
         "fraction_of_peak": round(gbs / world / peak, 4),
         "queries_per_s": round(B * world / (ms_per_step * 1e-3), 1),
-        "roofline": {"bound": "hbm", "kernel": "rswa verify (split + tail + merge)" if verify
+        "roofline": {"bound": "hbm",
+                     "kernel": ("rswa verify (stream tables + tensor-core split + tail + run merge)" if int8
+                                else "rswa verify (split + tail + merge)") if verify
                      else "rswa decode (split + merge)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": measured_traffic(args.workload),
@@ -560,7 +562,7 @@ def run_gpu_rswa(args, rank, world):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "e2e_sync": e2e_sync,
-        "gpu_launches": args.steps * (4 if verify else 3),
+        "gpu_launches": args.steps * ((5 if int8 else 4) if verify else 3),
         "clocks": sampler.summary(c0, c1),
     }
     if verify:

@@ -98,14 +98,33 @@ DecodeWs decode_ws(const Layer *l, int32_t n_q, bool imp) {
     return w;
 }
 
+// Most workers the tensor-core verify of the R-SWA int8 mirror launches (a
+// bound on resident one-warp CTAs, so its workspace size needs no device).
+constexpr int64_t kRswaTcWorkers = 2048;
+
 struct RswaWs {
     int64_t err, pm, pl, pacc, total;
     int32_t nc_max;
+    // tensor-core verify of the int8 mirror (tc): run partials [slot][K],
+    // tail partials [B][H][K], per-launch unit slot ranges and the stream
+    // tables the kernel reads (lengths, capacities, row bases, head map)
+    bool tc = false;
+    int64_t slots = 0, tc_pm = -1, tc_pl = -1, tc_pacc = -1, tail_pm = -1, tail_pl = -1, tail_pacc = -1;
+    int64_t units = -1, t_len = -1, t_cap = -1, t_base = -1, t_live = -1;
 };
 
+// The int8 mirror's verify runs on the tensor-core kernel at head_dim 128 with
+// up to 8 drafts, when every head's block is a whole number of 32-row tiles
+// (the tiles' scale copies stay inside it) and its rows fit the TMA's int32
+// coordinates.
+bool rswa_tc_shape(int32_t B, int32_t H, int32_t hd, int64_t ref_cap, int32_t K) {
+    return hd == 128 && K <= 8 && ref_cap > 0 && ref_cap % kWR == 0 && int64_t(B) * H * ref_cap < (int64_t(1) << 31);
+}
+
 // K > 1: a verify of K drafts (K partial rows per chunk; the ring's chunk
-// slots hold the one tail partial).
-RswaWs rswa_ws(int32_t B, int32_t H, int32_t hd, int64_t ref_cap, int32_t W, int32_t K = 1) {
+// slots hold the one tail partial).  tc: also lay out the tensor-core verify's
+// regions (they alias the chunk partials: a call uses one or the other).
+RswaWs rswa_ws(int32_t B, int32_t H, int32_t hd, int64_t ref_cap, int32_t W, int32_t K = 1, bool tc = false) {
     RswaWs w;
     w.nc_max = int32_t(ceil_div(ref_cap, kMinChunk) + ceil_div(W, kMinChunk));
     const int64_t P = int64_t(B) * H * w.nc_max * K;
@@ -116,10 +135,30 @@ RswaWs rswa_ws(int32_t B, int32_t H, int32_t hd, int64_t ref_cap, int32_t W, int
         return at;
     };
     w.err = take(16);
+    const int64_t base = o;
     w.pm = take(P * 4);
     w.pl = take(P * 4);
     w.pacc = take(P * hd * 4);
-    w.total = o;
+    const int64_t end_chunks = o;
+    if (tc && rswa_tc_shape(B, H, hd, ref_cap, K)) {
+        w.tc = true;
+        o = base;
+        const int64_t n = std::min<int32_t>(B, kSlice);
+        w.slots = n * H * ceil_div(ceil_div(ref_cap, kWR), kBlockTiles) + kRswaTcWorkers;
+        const int64_t tails = int64_t(B) * H * K;
+        w.tc_pm = take(w.slots * K * 4);
+        w.tc_pl = take(w.slots * K * 4);
+        w.tc_pacc = take(w.slots * K * hd * 4);
+        w.tail_pm = take(tails * 4);
+        w.tail_pl = take(tails * 4);
+        w.tail_pacc = take(tails * hd * 4);
+        w.units = take(n * H * 2 * 8);
+        w.t_len = take(n * 4);
+        w.t_cap = take(n * 8);
+        w.t_base = take(n * 8);
+        w.t_live = take(int64_t(H) * 4);
+    }
+    w.total = std::max(o, end_chunks);
     return w;
 }
 
@@ -658,52 +697,9 @@ __global__ void __launch_bounds__(128) rswa_verify_tail_kernel(TailArgs a, TailT
     float m = -INFINITY, l = 0.0f, acc[CPL];
 #pragma unroll
     for (int j = 0; j < CPL; ++j) acc[j] = 0.0f;
-    const int64_t ring0 = (int64_t(s) * a.H + h) * a.W;  // row of slot 0 of this head's ring
-    for (int r = warp; r < rl + i + 1; r += 4) {
-        const bool ring = r < rl;
-        const int j = r - rl;  // draft index
-        const bool vis = ring ? ((r - rp0 + a.W) % a.W) >= drop : rl + j >= drop;
-        if (!vis) continue;  // the same for the whole warp
-        const float *drow_k = a.dk + ((int64_t(s) * a.K + j) * a.H + h) * HD;
-        const float *drow_v = a.dv + ((int64_t(s) * a.K + j) * a.H + h) * HD;
-        float score, w_scale = 1.0f, x[CPL];
-        if (I8) {
-            uint32_t kw;
-            float ks;
-            if (ring) {
-                const int8_t *kr = a.ring_k8 + (ring0 + r) * HD;
-                kw = CPL == 4 ? reinterpret_cast<const uint32_t *>(kr)[lane]
-                              : uint32_t(reinterpret_cast<const uint16_t *>(kr)[lane]);
-                ks = a.ring_ks[ring0 + r];
-            } else {
-                float kx[CPL];
-                load_f32_lane<CPL>(drow_k, lane, kx);
-                kw = quant_lane_i8<CPL>(kx, ks);
-            }
-            // exact integer dot (every partial sum an integer below 2^24)
-            score = warp_sum(float(__dp4a(int(qi), int(kw), 0))) * ks * qfac;
-            uint32_t vw;
-            if (ring) {
-                const int8_t *vr = a.ring_v8 + (ring0 + r) * HD;
-                vw = CPL == 4 ? reinterpret_cast<const uint32_t *>(vr)[lane]
-                              : uint32_t(reinterpret_cast<const uint16_t *>(vr)[lane]);
-                w_scale = a.ring_vs[ring0 + r];
-            } else {
-                float vx[CPL];
-                load_f32_lane<CPL>(drow_v, lane, vx);
-                vw = quant_lane_i8<CPL>(vx, w_scale);
-            }
-#pragma unroll
-            for (int jj = 0; jj < CPL; ++jj) x[jj] = float(int8_t((vw >> (8 * jj)) & 0xffu));
-        } else {
-            float kx[CPL];
-            load_f32_lane<CPL>(ring ? a.ring_k + (ring0 + r) * HD : drow_k, lane, kx);
-            float p = 0.0f;
-#pragma unroll
-            for (int jj = 0; jj < CPL; ++jj) p = fmaf(qv[jj], kx[jj], p);
-            score = warp_sum(p);
-            load_f32_lane<CPL>(ring ? a.ring_v + (ring0 + r) * HD : drow_v, lane, x);
-        }
+    // one row into the warp's online softmax (score and weight scale uniform
+    // over the warp, x this lane's CPL values)
+    auto add_row = [&](float score, float w_scale, const float (&x)[CPL]) {
         const float mn = fmaxf(m, score);
         const float al = m == -INFINITY ? 0.0f : exp2f(m - mn);
         const float e = exp2f(score - mn);
@@ -712,6 +708,77 @@ __global__ void __launch_bounds__(128) rswa_verify_tail_kernel(TailArgs a, TailT
 #pragma unroll
         for (int jj = 0; jj < CPL; ++jj) acc[jj] = fmaf(acc[jj], al, w * x[jj]);
         m = mn;
+    };
+    const int64_t ring0 = (int64_t(s) * a.H + h) * a.W;  // row of slot 0 of this head's ring
+    // Ring rows, warp-strided, kTB rows per batch: every load of a batch is
+    // issued before its first row is used, so the rows' latencies overlap.
+    constexpr int kTB = 8;
+    for (int r0 = warp; r0 < rl; r0 += 4 * kTB) {
+        bool vis[kTB];
+        uint32_t kw[kTB], vw[kTB];
+        float ksr[kTB], vsr[kTB];
+        float kx[I8 ? 1 : kTB][CPL], vx[I8 ? 1 : kTB][CPL];
+#pragma unroll
+        for (int u = 0; u < kTB; ++u) {
+            const int r = r0 + 4 * u;
+            vis[u] = r < rl && ((r - rp0 + a.W) % a.W) >= drop;  // the same for the whole warp
+            if (!vis[u]) continue;
+            if constexpr (I8) {
+                const int8_t *kr = a.ring_k8 + (ring0 + r) * HD;
+                const int8_t *vr = a.ring_v8 + (ring0 + r) * HD;
+                kw[u] = CPL == 4 ? reinterpret_cast<const uint32_t *>(kr)[lane]
+                                 : uint32_t(reinterpret_cast<const uint16_t *>(kr)[lane]);
+                vw[u] = CPL == 4 ? reinterpret_cast<const uint32_t *>(vr)[lane]
+                                 : uint32_t(reinterpret_cast<const uint16_t *>(vr)[lane]);
+                ksr[u] = a.ring_ks[ring0 + r];
+                vsr[u] = a.ring_vs[ring0 + r];
+            } else {
+                load_f32_lane<CPL>(a.ring_k + (ring0 + r) * HD, lane, kx[u]);
+                load_f32_lane<CPL>(a.ring_v + (ring0 + r) * HD, lane, vx[u]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kTB; ++u) {
+            if (!vis[u]) continue;
+            float x[CPL];
+            if constexpr (I8) {
+                // exact integer dot (every partial sum an integer below 2^24)
+                const float score = warp_sum(float(__dp4a(int(qi), int(kw[u]), 0))) * ksr[u] * qfac;
+#pragma unroll
+                for (int jj = 0; jj < CPL; ++jj) x[jj] = float(int8_t((vw[u] >> (8 * jj)) & 0xffu));
+                add_row(score, vsr[u], x);
+            } else {
+                float p = 0.0f;
+#pragma unroll
+                for (int jj = 0; jj < CPL; ++jj) p = fmaf(qv[jj], kx[u][jj], p);
+#pragma unroll
+                for (int jj = 0; jj < CPL; ++jj) x[jj] = vx[u][jj];
+                add_row(warp_sum(p), 1.0f, x);
+            }
+        }
+    }
+    // drafts 0..i (the int8 path quantises each like a cache row first)
+    for (int j = warp; j <= i; j += 4) {
+        if (rl + j < drop) continue;  // pushed out of the window (the same for the whole warp)
+        const float *drow_k = a.dk + ((int64_t(s) * a.K + j) * a.H + h) * HD;
+        const float *drow_v = a.dv + ((int64_t(s) * a.K + j) * a.H + h) * HD;
+        float kx[CPL], x[CPL];
+        load_f32_lane<CPL>(drow_k, lane, kx);
+        load_f32_lane<CPL>(drow_v, lane, x);
+        if constexpr (I8) {
+            float ks, w_scale;
+            const uint32_t kw = quant_lane_i8<CPL>(kx, ks);
+            const float score = warp_sum(float(__dp4a(int(qi), int(kw), 0))) * ks * qfac;
+            const uint32_t vw = quant_lane_i8<CPL>(x, w_scale);
+#pragma unroll
+            for (int jj = 0; jj < CPL; ++jj) x[jj] = float(int8_t((vw >> (8 * jj)) & 0xffu));
+            add_row(score, w_scale, x);
+        } else {
+            float p = 0.0f;
+#pragma unroll
+            for (int jj = 0; jj < CPL; ++jj) p = fmaf(qv[jj], kx[jj], p);
+            add_row(warp_sum(p), 1.0f, x);
+        }
     }
     if (lane == 0) {
         sm_m[warp] = m;
@@ -735,6 +802,80 @@ __global__ void __launch_bounds__(128) rswa_verify_tail_kernel(TailArgs a, TailT
             a.pl[p] = L;
         }
     }
+}
+
+// The stream tables the tensor-core kernel walks, for the streams of one
+// launch: stream si is "sequence" si with prefill_len rows per head, its
+// H heads the live groups (identity map), head h's block at row
+// ((s0 + si) H + h) ref_cap of the mirror.
+struct RswaTcTables {
+    int32_t *seq_len, *live;
+    int64_t *cap, *row_base;
+    int32_t H;
+    int64_t ref_cap;
+};
+
+__global__ void rswa_tc_tables_kernel(RswaTable tb, RswaTcTables t) {
+    for (int i = threadIdx.x; i < tb.n || i < t.H; i += blockDim.x) {
+        if (i < tb.n) {
+            t.seq_len[i] = tb.prefill_len[i];
+            t.cap[i] = t.ref_cap;
+            t.row_base[i] = (int64_t(tb.s0) + i) * t.H * t.ref_cap;
+        }
+        if (i < t.H) t.live[i] = i;
+    }
+}
+
+struct RswaRunMerge {
+    const float *pm, *pl, *pacc;     // run partials [slot][K] (+ [128])
+    const float *tpm, *tpl, *tpacc;  // tail partials [B][H][K] (+ [128])
+    const int64_t *unit_slots;       // [stream of the launch][H][2]
+    float *out;                      // [B][K][H][128]
+    int32_t H, K;
+};
+
+// Verify merge of the tensor-core path: query i of head h of stream s is the
+// log-sum-exp merge of the reference block's run partials (the slot range its
+// workers recorded; empty markers carry max -inf) and the ring-and-drafts
+// tail partial, which always holds at least draft i itself.
+__global__ void __launch_bounds__(128) merge_rswa_runs_kernel(RswaRunMerge a, RswaTable tb) {
+    const int h = blockIdx.x, si = blockIdx.y, i = blockIdx.z, d = threadIdx.x;
+    if (si >= tb.n) return;
+    const int s = tb.s0 + si;
+    const int64_t tp = (int64_t(s) * a.H + h) * a.K + i;
+    float M = a.tpm[tp], Ls = a.tpl[tp], acc = a.tpacc[tp * 128 + d];
+    if (tb.prefill_len[si] > 0) {
+        const int64_t unit = int64_t(si) * a.H + h;
+        const int64_t first = a.unit_slots[2 * unit], last = a.unit_slots[2 * unit + 1];
+        constexpr int kBatch = 4;  // slots whose loads are in flight together
+        for (int64_t s0 = first; s0 <= last; s0 += kBatch) {
+            float m[kBatch], l[kBatch], v[kBatch];
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                const int64_t p = (s0 + k) * a.K + i;
+                m[k] = -INFINITY;
+                if (s0 + k <= last) {
+                    m[k] = a.pm[p];
+                    l[k] = a.pl[p];
+                    v[k] = a.pacc[p * 128 + d];
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                if (m[k] == -INFINITY) continue;  // past the range, or an empty marker
+                if (m[k] > M) {
+                    const float r = exp2f(M - m[k]);
+                    Ls *= r;
+                    acc *= r;
+                    M = m[k];
+                }
+                const float f = exp2f(m[k] - M);
+                Ls = fmaf(l[k], f, Ls);
+                acc = fmaf(v[k], f, acc);
+            }
+        }
+    }
+    a.out[((int64_t(s) * a.K + i) * a.H + h) * 128 + d] = acc / Ls;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
@@ -1385,7 +1526,7 @@ static kvd_status rswa_verify_impl(const float *q, const float *dk, const float 
     if (ref_cap % kRowAlign != 0 || W % kRowAlign != 0) return KVD_EINVAL;
     if (!std::isfinite(scale)) return KVD_EINVAL;
     if (!aligned16(q) || !aligned16(out) || !aligned16(dk) || !aligned16(dv)) return KVD_EINVAL;
-    const RswaWs w = rswa_ws(B, H, head_dim, ref_cap, W, K);
+    const RswaWs w = rswa_ws(B, H, head_dim, ref_cap, W, K, true);
     if (workspace == nullptr || workspace_bytes < w.total || (reinterpret_cast<uintptr_t>(workspace) & 255))
         return KVD_EINVAL;
     int64_t work = 0;
@@ -1447,6 +1588,27 @@ static kvd_status rswa_verify_impl(const float *q, const float *dk, const float 
     m.n_grp = H;
     m.nc_max = w.nc_max;
     m.chunk = chunk;
+    // The int8 mirror's reference block on the tensor-core kernel (the draft
+    // rows of a head as the group's query rows), else the CUDA-core kernel.
+    const int variant = K <= 4 ? 3 : 4;
+    MmaMaps maps;
+    int64_t workers = 0;
+    bool tc = false;
+    if (I8 && w.tc) {
+        const int64_t rows = int64_t(B) * H * ref_cap;
+        tc = encode_code_map(const_cast<int8_t *>(src_in.ref_k8), rows, head_dim,
+                             reinterpret_cast<unsigned char *>(&maps.kq)) &&
+             encode_code_map(const_cast<int8_t *>(src_in.ref_v8), rows, head_dim,
+                             reinterpret_cast<unsigned char *>(&maps.vq));
+        workers = tc ? std::min(split_q8_tc_workers(variant), kRswaTcWorkers) : 0;
+        tc = workers > 0;
+    }
+    if (tc) {
+        ta.pm = reinterpret_cast<float *>(ws + w.tail_pm);
+        ta.pl = reinterpret_cast<float *>(ws + w.tail_pl);
+        ta.pacc = reinterpret_cast<float *>(ws + w.tail_pacc);
+        ta.nc_max = 1;
+    }
     const int hb = hpk_bucket(K);
     for (int32_t s0 = 0; s0 < B; s0 += kSlice) {
         RswaTable t;  // the split kernel reads the reference rows only
@@ -1460,8 +1622,58 @@ static kvd_status rswa_verify_impl(const float *q, const float *dk, const float 
             t.ring_len[i] = 0;
             tt.ring_len[i] = ring_len[s];
             tt.rp0[i] = ring_len[s] == W ? ring_pos[s] : 0;
-            tt.nc_ref[i] = int32_t(ceil_div(prefill_len[s], chunk));
+            tt.nc_ref[i] = tc ? 0 : int32_t(ceil_div(prefill_len[s], chunk));
             max_nc = std::max(max_nc, tt.nc_ref[i]);
+        }
+        if (tc) {
+            RswaTcTables tabs;
+            tabs.seq_len = reinterpret_cast<int32_t *>(ws + w.t_len);
+            tabs.live = reinterpret_cast<int32_t *>(ws + w.t_live);
+            tabs.cap = reinterpret_cast<int64_t *>(ws + w.t_cap);
+            tabs.row_base = reinterpret_cast<int64_t *>(ws + w.t_base);
+            tabs.H = H;
+            tabs.ref_cap = ref_cap;
+            rswa_tc_tables_kernel<<<1, 256, 0, st>>>(t, tabs);
+            if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
+            int64_t T = 0;
+            for (int i = 0; i < t.n; ++i) T += int64_t(H) * ceil_div(t.prefill_len[i], kWR);
+            WarpArgs wa;
+            wa.a = a;
+            wa.a.q = q + int64_t(s0) * K * H * head_dim;
+            wa.a.K = 1;  // every draft sees the whole block
+            wa.a.hg = 0;
+            wa.a.pm = reinterpret_cast<float *>(ws + w.tc_pm);
+            wa.a.pl = reinterpret_cast<float *>(ws + w.tc_pl);
+            wa.a.pacc = reinterpret_cast<float *>(ws + w.tc_pacc);
+            wa.T = T;
+            wa.G = int32_t(std::min(T, workers));
+            wa.n_seq = t.n;
+            wa.unit_slots = reinterpret_cast<int64_t *>(ws + w.units);
+            LayerSrc ls{};
+            ls.ks = src.ref_ks;
+            ls.vs = src.ref_vs;
+            ls.row_base = tabs.row_base;
+            ls.cap = tabs.cap;
+            ls.seq_len = tabs.seq_len;
+            ls.live = tabs.live;
+            ls.n_live = H;
+            if (T > 0 && split_layer_q8_tc(variant, wa, ls, maps, st) != cudaSuccess) return KVD_ECUDA;
+            rswa_verify_tail_kernel<128, true><<<dim3(unsigned(K), unsigned(H), unsigned(t.n)), 128, 0, st>>>(ta, tt);
+            if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
+            RswaRunMerge rm;
+            rm.pm = wa.a.pm;
+            rm.pl = wa.a.pl;
+            rm.pacc = wa.a.pacc;
+            rm.tpm = ta.pm;
+            rm.tpl = ta.pl;
+            rm.tpacc = ta.pacc;
+            rm.unit_slots = wa.unit_slots;
+            rm.out = out;
+            rm.H = H;
+            rm.K = K;
+            merge_rswa_runs_kernel<<<dim3(unsigned(H), unsigned(t.n), unsigned(K)), 128, 0, st>>>(rm, t);
+            if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
+            continue;
         }
         if (max_nc > 0) {
             dim3 grid(unsigned(max_nc), unsigned(H), unsigned(t.n));
@@ -1486,7 +1698,7 @@ extern "C" kvd_status rswa_verify_workspace_bytes(int32_t B, int32_t H, int32_t 
     if (bytes_out == nullptr || B < 1 || H < 1 || (head_dim != 64 && head_dim != 128) || ref_cap < 0 || W < 1 ||
         K < 1 || K > kMaxHpk)
         return KVD_EINVAL;
-    *bytes_out = rswa_ws(B, H, head_dim, ref_cap, W, K).total;
+    *bytes_out = rswa_ws(B, H, head_dim, ref_cap, W, K, true).total;
     return KVD_OK;
 }
 

@@ -187,6 +187,11 @@ inline cudaError_t set_smem_once(const void *kern, int bytes) {
     return e;
 }
 
+// TMA descriptor (128 bytes, written to out) of an int8 code buffer
+// [rows][hd]: boxes of 32 rows x 128 bytes, 128-byte swizzle, rows past the
+// end read as zeros.  head_dim 128 only; false if the driver refuses it.
+bool encode_code_map(void *base, int64_t rows, int hd, unsigned char *out);
+
 __device__ __forceinline__ void set_error(uint32_t *err, uint32_t bit) {
     if (err) atomicOr(err, bit);
 }

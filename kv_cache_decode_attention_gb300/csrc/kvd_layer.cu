@@ -104,6 +104,8 @@ int64_t host_block_bytes(int32_t n_seq, int32_t n_kv) {
     return 8 * 4 * int64_t(n_seq) + 4 * int64_t(n_seq) + 8 * int64_t(n_kv) + round_up(n_kv, 8);
 }
 
+}  // namespace
+
 // TMA descriptor of an int8 code buffer: 2-D [rows][hd] bytes, row pitch hd,
 // boxes of 32 rows x 128 bytes landing in shared memory with the 128-byte
 // swizzle (16-byte chunk c of row r stored at chunk c ^ (r % 8)); rows past
@@ -134,6 +136,8 @@ bool encode_code_map(void *base, int64_t rows, int hd, unsigned char *out) {
     std::memcpy(out, &m, sizeof(m));
     return true;
 }
+
+namespace {
 
 __global__ void fill_f32_kernel(float *p, int64_t n, float v) {
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n;

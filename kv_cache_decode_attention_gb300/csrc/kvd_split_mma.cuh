@@ -66,6 +66,7 @@ constexpr int kStKs = 8192;         // K scales [32][4] f32
 constexpr int kStVs = 8704;         // V scales [32] f32
 constexpr int kStageBytes = 9216;   // multiple of 1024 (swizzle atom)
 constexpr uint32_t kStageTx = 4096 + 4096 + 512 + 128;
+constexpr uint32_t kStageTxRow = 4096 + 4096 + 128 + 128;  // one K scale per row
 
 // PACK: groups of at most 4 query heads put both query terms (and both
 // weight terms) side by side in the 8 columns of one n8 tile; larger groups
@@ -277,20 +278,31 @@ __device__ inline bool cursor_locate(TileCursor &c, int64_t x, const LayerSrc &s
     return false;
 }
 
+// ROWK: one K scale per row ([rows] f32) instead of one per 32 channels.
+template <bool ROWK = false>
 __device__ __forceinline__ void issue_tile(const TileCursor &c, const CUtensorMap *kmap,
                                            const CUtensorMap *vmap, const LayerSrc &src, char *stage,
                                            uint64_t *bar) {
     const int64_t row = c.rbase + c.f0 + int64_t(c.tl) * kWR;
-    mbar_arrive_expect_tx(bar, kStageTx);
+    mbar_arrive_expect_tx(bar, ROWK ? kStageTxRow : kStageTx);
     tma_load_2d(stage + kStK, kmap, 0, int(row), bar);
     tma_load_2d(stage + kStV, vmap, 0, int(row), bar);
-    bulk_g2s(stage + kStKs, src.ks + row * 4, 512, bar);
+    if (ROWK) bulk_g2s(stage + kStKs, src.ks + row, 128, bar);
+    else bulk_g2s(stage + kStKs, src.ks + row * 4, 512, bar);
     bulk_g2s(stage + kStVs, src.vs + row, 128, bar);
 }
 
 // OPT: the call has a window or a softcap; IMP: the call accumulates imp
 // (per-row scores are stored).  Both are compiled out of the common path.
-template <bool PACK, bool OPT, bool IMP>
+// ROWK: the R-SWA int8 mirror's reference block (rswa decode_attention_int8,
+// query-batched for verify_attention): one K scale per row, no column field,
+// and each query row quantised like a cache row, so the B operand is the
+// query's int8 codes (exact in f16, one term) and the score is the exact
+// integer dot times the row's K scale times qscale * softmax scale * log2(e).
+// The group's a.hpk query rows are the K drafts of one head, read from
+// q [stream][draft][head][128] (a.n_q heads); a.K stays 1 (every draft sees
+// the whole block).
+template <bool PACK, bool OPT, bool IMP, bool ROWK = false>
 __global__ void __launch_bounds__(32, 12) split_warp_kernel(WarpArgs wa, LayerSrc src,
                                                         const __grid_constant__ MmaMaps maps) {
     using C = WarpCfg<PACK>;
@@ -335,8 +347,8 @@ __global__ void __launch_bounds__(32, 12) split_warp_kernel(WarpArgs wa, LayerSr
     {
         const int64_t first = x_end - x_begin < kStages ? x_end - x_begin : int64_t(kStages);
         for (int64_t i = 0; i < first && prod_ok; ++i) {
-            if (lane == 0) issue_tile(prod, &maps.kq, &maps.vq, src, sm + (i % kStages) * kStageBytes,
-                                      &bar[i % kStages]);
+            if (lane == 0) issue_tile<ROWK>(prod, &maps.kq, &maps.vq, src, sm + (i % kStages) * kStageBytes,
+                                            &bar[i % kStages]);
             ++issued;
             if (x_begin + issued < x_end) prod_ok = cursor_next(prod, src, wa.n_seq, a.window, a.K, a.err);
         }
@@ -363,7 +375,7 @@ __global__ void __launch_bounds__(32, 12) split_warp_kernel(WarpArgs wa, LayerSr
     const bool owner = !PACK || t4 < 2;  // writes scores and partials of its heads
     // B fragments of the query [chunk][term or -][reg]: the column this lane
     // feeds is gl4 (PACK: term gl4 / 4 of head gl4 % 4; else head gl4)
-    uint32_t bq[8][PACK ? 1 : 2][2];
+    uint32_t bq[8][(PACK || ROWK) ? 1 : 2][2];
     float qexp[2];
     int q_b = -1, q_gl = -1;
 
@@ -384,6 +396,39 @@ __global__ void __launch_bounds__(32, 12) split_warp_kernel(WarpArgs wa, LayerSr
             q_b = cur.b;
             q_gl = cur.gl;
             const int g = src.live[cur.gl];
+            if constexpr (ROWK) {
+                // draft hb of head g, quantised like a cache row (scale max|x| / 127,
+                // 1 for a zero row; IEEE division, round half to even, clamp to
+                // +-127): the codes are exact f16 values, the scale joins qexp
+                const int hb = PACK ? gl4 & 3 : gl4;
+                const float *qr = a.q + ((int64_t(cur.b) * a.hpk + hb) * a.n_q + g) * 128;
+                float xq[8][4];
+                float mx = 0.0f;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    float4 qv = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    if (hb < a.hpk) qv = *reinterpret_cast<const float4 *>(qr + 16 * ch + 4 * t4);
+                    xq[ch][0] = qv.x, xq[ch][1] = qv.y, xq[ch][2] = qv.z, xq[ch][3] = qv.w;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) mx = fmaxf(mx, fabsf(xq[ch][j]));
+                }
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                const float qs = mx > 0.0f ? __fdiv_rn(mx, 127.0f) : 1.0f;
+                const bool empty = PACK && gl4 >= 4;  // the second term's columns stay zero
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    float cd[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) cd[j] = float(quant_code_i8(xq[ch][j], qs));
+                    bq[ch][0][0] = empty ? 0u : pack_half2(cd[0], cd[1]);
+                    bq[ch][0][1] = empty ? 0u : pack_half2(cd[2], cd[3]);
+                }
+                const float qf = qs * a.qscale;
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) qexp[cc] = __shfl_sync(0xffffffffu, qf, (hc0 + cc) * 4);
+                __syncwarp();
+            } else {
             const float *qg = a.q + (int64_t(cur.b) * a.n_q + int64_t(g) * a.hpk) * 128;
             const float *kc = src.kcol + (int64_t(cur.b) * src.n_live + cur.gl) * 128;
             const int hb = PACK ? gl4 & 3 : gl4;
@@ -421,8 +466,8 @@ __global__ void __launch_bounds__(32, 12) split_warp_kernel(WarpArgs wa, LayerSr
                 } else {
                     bq[ch][0][0] = pack_half2(hi[0], hi[1]);
                     bq[ch][0][1] = pack_half2(hi[2], hi[3]);
-                    bq[ch][PACK ? 0 : 1][0] = pack_half2(lo[0], lo[1]);
-                    bq[ch][PACK ? 0 : 1][1] = pack_half2(lo[2], lo[3]);
+                    bq[ch][(PACK || ROWK) ? 0 : 1][0] = pack_half2(lo[0], lo[1]);
+                    bq[ch][(PACK || ROWK) ? 0 : 1][1] = pack_half2(lo[2], lo[3]);
                 }
             }
             // 2^-E of the heads of this lane's score columns, held by the
@@ -430,6 +475,7 @@ __global__ void __launch_bounds__(32, 12) split_warp_kernel(WarpArgs wa, LayerSr
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) qexp[cc] = pow2i(-__shfl_sync(0xffffffffu, E, (hc0 + cc) * 4));
             __syncwarp();
+            }
         }
         float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.0f, 0.0f};
         float acc[8][4];
@@ -458,10 +504,17 @@ __global__ void __launch_bounds__(32, 12) split_warp_kernel(WarpArgs wa, LayerSr
 #pragma unroll
             for (int mb = 0; mb < 2; ++mb) {
                 float sacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                const float4 ksA = *reinterpret_cast<const float4 *>(&ks_s[(mb * 16 + gl4) * 4]);
-                const float4 ksB = *reinterpret_cast<const float4 *>(&ks_s[(mb * 16 + gl4 + 8) * 4]);
-                const float kA[4] = {ksA.x, ksA.y, ksA.z, ksA.w};
-                const float kB[4] = {ksB.x, ksB.y, ksB.z, ksB.w};
+                float kA[4], kB[4];
+                if constexpr (ROWK) {
+                    kA[0] = ks_s[mb * 16 + gl4];
+                    kB[0] = ks_s[mb * 16 + gl4 + 8];
+                } else {
+                    const float4 ksA = *reinterpret_cast<const float4 *>(&ks_s[(mb * 16 + gl4) * 4]);
+                    const float4 ksB = *reinterpret_cast<const float4 *>(&ks_s[(mb * 16 + gl4 + 8) * 4]);
+                    kA[0] = ksA.x, kA[1] = ksA.y, kA[2] = ksA.z, kA[3] = ksA.w;
+                    kB[0] = ksB.x, kB[1] = ksB.y, kB[2] = ksB.z, kB[3] = ksB.w;
+                }
+                float di[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // ROWK: the integer dot over all channels
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
                     uint32_t w[4];
@@ -472,16 +525,28 @@ __global__ void __launch_bounds__(32, 12) split_warp_kernel(WarpArgs wa, LayerSr
                     const uint32_t a01 = codes_f16x2<0x4140>(u1), a03 = codes_f16x2<0x4342>(u1);
                     const uint32_t a10 = codes_f16x2<0x4140>(u2), a12 = codes_f16x2<0x4342>(u2);
                     const uint32_t a11 = codes_f16x2<0x4140>(u3), a13 = codes_f16x2<0x4342>(u3);
-                    float dg[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                    if constexpr (ROWK) {
+                        mma_f16(di, a00, a01, a02, a03, bq[2 * g][0][0], bq[2 * g][0][1]);
+                        mma_f16(di, a10, a11, a12, a13, bq[2 * g + 1][0][0], bq[2 * g + 1][0][1]);
+                    } else {
+                        float dg[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-                    for (int tm = 0; tm < (PACK ? 1 : 2); ++tm) {
-                        mma_f16(dg, a00, a01, a02, a03, bq[2 * g][tm][0], bq[2 * g][tm][1]);
-                        mma_f16(dg, a10, a11, a12, a13, bq[2 * g + 1][tm][0], bq[2 * g + 1][tm][1]);
+                        for (int tm = 0; tm < (PACK ? 1 : 2); ++tm) {
+                            mma_f16(dg, a00, a01, a02, a03, bq[2 * g][tm][0], bq[2 * g][tm][1]);
+                            mma_f16(dg, a10, a11, a12, a13, bq[2 * g + 1][tm][0], bq[2 * g + 1][tm][1]);
+                        }
+                        sacc[0] = fmaf(kA[g], dg[0], sacc[0]);
+                        sacc[1] = fmaf(kA[g], dg[1], sacc[1]);
+                        sacc[2] = fmaf(kB[g], dg[2], sacc[2]);
+                        sacc[3] = fmaf(kB[g], dg[3], sacc[3]);
                     }
-                    sacc[0] = fmaf(kA[g], dg[0], sacc[0]);
-                    sacc[1] = fmaf(kA[g], dg[1], sacc[1]);
-                    sacc[2] = fmaf(kB[g], dg[2], sacc[2]);
-                    sacc[3] = fmaf(kB[g], dg[3], sacc[3]);
+                }
+                if constexpr (ROWK) {
+                    // every partial sum is an integer below 2^24: exact in f32
+                    sacc[0] = di[0] * kA[0];
+                    sacc[1] = di[1] * kA[0];
+                    sacc[2] = di[2] * kB[0];
+                    sacc[3] = di[3] * kB[0];
                 }
                 if constexpr (PACK) {
                     // add the other term's part (columns 2*t4 ^ 4)
@@ -622,7 +687,7 @@ __global__ void __launch_bounds__(32, 12) split_warp_kernel(WarpArgs wa, LayerSr
             if (x_begin + issued < x_end && prod_ok) {
                 if (lane == 0) {
                     fence_proxy_async();
-                    issue_tile(prod, &maps.kq, &maps.vq, src, st, &bar[stg]);
+                    issue_tile<ROWK>(prod, &maps.kq, &maps.vq, src, st, &bar[stg]);
                 }
                 ++issued;
                 if (x_begin + issued < x_end) prod_ok = cursor_next(prod, src, wa.n_seq, a.window, a.K, a.err);
@@ -691,14 +756,25 @@ cudaError_t launch_split_warp(const WarpArgs &wa, const LayerSrc &s, const MmaMa
     return launch_pdl(kern, dim3(unsigned(wa.G)), dim3(32), C::SMEM_ALLOC, st, wa, s, maps);
 }
 
-// Workers of one launch on the current device: SMs x resident CTAs per SM.
+// The R-SWA int8 mirror's reference block (no window, softcap or imp there).
 template <bool PACK>
+cudaError_t launch_split_warp_rowk(const WarpArgs &wa, const LayerSrc &s, const MmaMaps &maps,
+                                   cudaStream_t st) {
+    using C = WarpCfg<PACK>;
+    auto kern = split_warp_kernel<PACK, false, false, true>;
+    cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), C::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(kern, dim3(unsigned(wa.G)), dim3(32), C::SMEM_ALLOC, st, wa, s, maps);
+}
+
+// Workers of one launch on the current device: SMs x resident CTAs per SM.
+template <bool PACK, bool ROWK = false>
 int64_t split_warp_workers() {
     int dev = 0, sms = 0, occ = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return 0;
-    auto kern = split_warp_kernel<PACK, false, false>;
+    auto kern = split_warp_kernel<PACK, false, false, ROWK>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              WarpCfg<PACK>::SMEM_ALLOC) != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 32, WarpCfg<PACK>::SMEM_ALLOC) !=

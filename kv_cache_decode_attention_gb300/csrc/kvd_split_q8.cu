@@ -21,7 +21,8 @@ cudaError_t split_layer_q8(int hd, int hpk_bucket, const SplitArgs &a, const Lay
 
 // Tensor-core kernels for the q8_2f cache by query heads per group:
 // variant 0 = up to 4 (terms packed in the columns), 1 = up to 8 (heads in
-// the columns), 2 = up to 16 (heads in the MMA rows).
+// the columns), 2 = up to 16 (heads in the MMA rows); 3 and 4 are 0 and 1
+// over the R-SWA int8 mirror (one K scale per row, int8 query codes).
 int q8_tc_variant(int hpk) { return hpk <= 4 ? 0 : hpk <= 8 ? 1 : 2; }
 
 cudaError_t split_layer_q8_tc(int variant, const WarpArgs &wa, const LayerSrc &s, const MmaMaps &maps,
@@ -30,6 +31,8 @@ cudaError_t split_layer_q8_tc(int variant, const WarpArgs &wa, const LayerSrc &s
         case 0: return launch_split_warp<true>(wa, s, maps, st);
         case 1: return launch_split_warp<false>(wa, s, maps, st);
         case 2: return launch_split_h16(wa, s, maps, st);
+        case 3: return launch_split_warp_rowk<true>(wa, s, maps, st);
+        case 4: return launch_split_warp_rowk<false>(wa, s, maps, st);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -39,14 +42,19 @@ cudaError_t split_layer_q8_tc(int variant, const WarpArgs &wa, const LayerSrc &s
 int64_t split_q8_tc_workers(int variant) {
     constexpr int kMaxDev = 64;
     static std::mutex mu;
-    static int64_t cache[kMaxDev][3] = {};
+    static int64_t cache[kMaxDev][5] = {};
     int dev = 0;
-    if (variant < 0 || variant > 2 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+    if (variant < 0 || variant > 4 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
     std::lock_guard<std::mutex> lock(mu);
     int64_t &w = cache[dev][variant];
     if (w == 0) {
-        w = variant == 0 ? split_warp_workers<true>() : variant == 1 ? split_warp_workers<false>()
-                                                                     : split_h16_workers();
+        switch (variant) {
+            case 0: w = split_warp_workers<true>(); break;
+            case 1: w = split_warp_workers<false>(); break;
+            case 2: w = split_h16_workers(); break;
+            case 3: w = split_warp_workers<true, true>(); break;
+            default: w = split_warp_workers<false, true>(); break;
+        }
     }
     return w;
 }

@@ -225,6 +225,25 @@ def test_rswa_i8_steady_full_size(env):
                                     cursors[s][0], scale)
         err = out_error(out[s].reshape(c.H, c.head_dim), ref)
         assert err <= OUT_TOL, (s, err)
+    # the benchmark's speculative step: 4 drafts verified over the same mirror
+    # (the reference block on the tensor-core kernel), two sampled streams
+    import synthetic
+
+    K = 4
+    vq = synthetic.normal((c.B, K, c.H, c.head_dim), 5900)
+    vk = synthetic.normal((c.B, K, c.H, c.head_dim), 5901)
+    vv = synthetic.normal((c.B, K, c.H, c.head_dim), 5902)
+    dev = torch.device("cuda")
+    vout = kvd.rswa_verify(torch.from_numpy(vq).to(dev), torch.from_numpy(vk).to(dev),
+                           torch.from_numpy(vv).to(dev), c, int8=True).cpu().numpy()
+    assert c.device_error() == 0
+    for s in (0, 11):
+        pk, pv = wl.prefill_rows(s)
+        ref = oracle.rswa_verify(vq[s], vk[s], vv[s], pk.cpu().numpy(), pv.cpu().numpy(), wl.prefill, ring_k[s],
+                                 ring_v[s], cursors[s], scale, int8=True)
+        for i in range(K):
+            err = out_error(vout[s, i].reshape(c.H, c.head_dim), ref[i])
+            assert err <= OUT_TOL, (s, i, err)
     del wl, c
     torch.cuda.empty_cache()
 

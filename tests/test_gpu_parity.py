@@ -836,6 +836,49 @@ def test_rswa_verify_parity(torch, kvd, int8, hd, H):
     assert cache.device_error() == 0
 
 
+@pytest.mark.parametrize("K,ref_cap", [(4, 6144), (8, 6144), (2, 6144), (3, 2096)])
+def test_rswa_i8_verify_reference_runs(torch, kvd, K, ref_cap):
+    """The int8 mirror's verify with long reference blocks: at head_dim 128 with
+    up to 8 drafts and a block of whole 32-row tiles the block runs on the
+    tensor-core kernel (many tiles per head, several workers and partial runs
+    per head, a ragged last tile, a stream without a block); ref_cap 2096 (not
+    a whole number of tiles) keeps the CUDA-core kernel.  Against the oracle's
+    write-then-decode over the mirror."""
+    B, H, hd, W = 3, 3, 128, 128
+    prefill = [ref_cap - 144, 2077, 0]
+    cache = kvd.RingCache(B, ref_cap, H, hd, W, int8=True)
+    o_ref_k = np.zeros((B, H, ref_cap, hd), np.float32)
+    o_ref_v = np.zeros_like(o_ref_k)
+    o_ring_k = np.zeros((B, H, W, hd), np.float32)
+    o_ring_v = np.zeros_like(o_ring_k)
+    cursors = [np.zeros(2, np.int32) for _ in range(B)]
+    for s in range(B):
+        m = prefill[s]
+        k = synthetic.normal((H, m, hd), 5500 + s)
+        v = synthetic.normal((H, m, hd), 5510 + s)
+        kvd.rswa_record_prefill(cache, s, torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda())
+        o_ref_k[s, :, :m], o_ref_v[s, :, :m] = k, v
+    for t in range(90):
+        kt = synthetic.normal((B, H, hd), 5600 + t)
+        vt = synthetic.normal((B, H, hd), 5700 + t)
+        kvd.rswa_ring_write(cache, torch.from_numpy(kt).cuda(), torch.from_numpy(vt).cuda())
+        for s in range(B):
+            oracle.rswa_write(o_ring_k[s], o_ring_v[s], kt[s], vt[s], True, cursors[s])
+    scale = np.float32(1.0 / math.sqrt(hd))
+    q = synthetic.normal((B, K, H, hd), 5800 + K)
+    dk = synthetic.normal((B, K, H, hd), 5810 + K)
+    dv = synthetic.normal((B, K, H, hd), 5820 + K)
+    out = kvd.rswa_verify(torch.from_numpy(q).cuda(), torch.from_numpy(dk).cuda(), torch.from_numpy(dv).cuda(),
+                          cache, int8=True).cpu().numpy()
+    assert cache.device_error() == 0
+    for s in range(B):
+        ref = oracle.rswa_verify(q[s], dk[s], dv[s], o_ref_k[s], o_ref_v[s], prefill[s], o_ring_k[s],
+                                 o_ring_v[s], cursors[s], scale, int8=True)
+        for i in range(K):
+            err = out_error(out[s, i].reshape(H, hd), ref[i])
+            assert err <= OUT_TOL, (s, i, err)
+
+
 @pytest.mark.parametrize("int8", [False, True])
 def test_rswa_verify_steady_ring_and_fill(torch, kvd, int8):
     """One stream per ring state (warm with room for the drafts, filling during
