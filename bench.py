@@ -51,10 +51,13 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
 # without imp -- the split kernel plus the run merge -- from one ncu capture of
 # this benchmark's roofline loop (command and figures in
 # profiles/decode_q8_gqa_traffic.md), valid while the kernel sources hash to
-# the captured version; reported as null otherwise.
+# the captured version; reported as null otherwise.  The capture ran 25 steps
+# (cache rows 4096 + 25); a run of another length reports it scaled by its
+# algorithmic bytes over the capture's (both are rows x bytes per row plus a
+# small fixed part).
 TRAFFIC = {
-    "q8_gqa": {"sources_sha256": "28371b22867eb403006a3b64ac36869082a6b968888e1803a6d9a0fe77fe9406",
-               "bytes": 300610560},
+    "q8_gqa": {"sources_sha256": "d095e6c876260a9dc49f6fb94eca909cb7f0d06bd2e8033020dfeeadfd9fc1ee",
+               "bytes": 300596480, "algorithmic_bytes": 291600896},
 }
 
 
@@ -70,11 +73,13 @@ def kernel_sources_sha256() -> str:
     return h.hexdigest()
 
 
-def measured_traffic(workload: str):
+def measured_traffic(workload: str, bytes_per_launch=None):
     t = TRAFFIC.get(workload)
     if not t or t["bytes"] is None or t["sources_sha256"] != kernel_sources_sha256():
         return None
-    return t["bytes"]
+    if bytes_per_launch is None:
+        return t["bytes"]
+    return int(round(t["bytes"] * bytes_per_launch / t["algorithmic_bytes"]))
 
 
 def peaks():
@@ -935,7 +940,7 @@ def run_gpu(args, rank, world):
         "queries_per_s": round(wl0.n_seq * world / (ms_per_step * 1e-3), 1),
         "roofline": {"bound": "hbm", "kernel": "decode_attention (split + merge, imp off)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": measured_traffic(wl0.name),
+                     "frac": round(achieved / peak, 4), "traffic": measured_traffic(wl0.name, kbytes),
                      "peak_kind": peak_kind, "ms_per_launch": round(k_ms, 5),
                      "bytes_per_launch": int(kbytes)},
         "decode_ms_in_step": round(statistics.mean(dec_ms), 5),

@@ -847,7 +847,7 @@ __global__ void __launch_bounds__(128) merge_rswa_runs_kernel(RswaRunMerge a, Rs
     if (tb.prefill_len[si] > 0) {
         const int64_t unit = int64_t(si) * a.H + h;
         const int64_t first = a.unit_slots[2 * unit], last = a.unit_slots[2 * unit + 1];
-        constexpr int kBatch = 4;  // slots whose loads are in flight together
+        constexpr int kBatch = 8;  // slots whose loads are in flight together
         for (int64_t s0 = first; s0 <= last; s0 += kBatch) {
             float m[kBatch], l[kBatch], v[kBatch];
 #pragma unroll
