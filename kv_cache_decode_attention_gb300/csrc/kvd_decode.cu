@@ -106,10 +106,10 @@ struct RswaWs {
     int64_t err, pm, pl, pacc, total;
     int32_t nc_max;
     // tensor-core verify of the int8 mirror (tc): run partials [slot][K],
-    // tail partials [B][H][K], per-launch unit slot ranges and the stream
-    // tables the kernel reads (lengths, capacities, row bases, head map)
+    // per-launch unit slot ranges and the stream tables the kernel reads
+    // (lengths, capacities, row bases, head map)
     bool tc = false;
-    int64_t slots = 0, tc_pm = -1, tc_pl = -1, tc_pacc = -1, tail_pm = -1, tail_pl = -1, tail_pacc = -1;
+    int64_t slots = 0, tc_pm = -1, tc_pl = -1, tc_pacc = -1;
     int64_t units = -1, t_len = -1, t_cap = -1, t_base = -1, t_live = -1;
 };
 
@@ -145,13 +145,9 @@ RswaWs rswa_ws(int32_t B, int32_t H, int32_t hd, int64_t ref_cap, int32_t W, int
         o = base;
         const int64_t n = std::min<int32_t>(B, kSlice);
         w.slots = n * H * ceil_div(ceil_div(ref_cap, kWR), kBlockTiles) + kRswaTcWorkers;
-        const int64_t tails = int64_t(B) * H * K;
         w.tc_pm = take(w.slots * K * 4);
         w.tc_pl = take(w.slots * K * 4);
         w.tc_pacc = take(w.slots * K * hd * 4);
-        w.tail_pm = take(tails * 4);
-        w.tail_pl = take(tails * 4);
-        w.tail_pacc = take(tails * hd * 4);
         w.units = take(n * H * 2 * 8);
         w.t_len = take(n * 4);
         w.t_cap = take(n * 8);
@@ -671,8 +667,19 @@ __device__ __forceinline__ void load_f32_lane(const float *row, int lane, float 
     }
 }
 
-template <int HD, bool I8>
-__global__ void __launch_bounds__(128) rswa_verify_tail_kernel(TailArgs a, TailTable t) {
+struct RswaRunMerge {
+    const float *pm, *pl, *pacc;     // run partials [slot][K] (+ [128])
+    const int64_t *unit_slots;       // [stream of the launch][H][2]
+    float *out;                      // [B][K][H][128]
+    int32_t H, K;
+};
+
+// FUSED (the tensor-core path, head_dim 128): the kernel is the split kernel's
+// programmatic dependent, computes the ring-and-drafts partial while the split
+// drains, then waits for it and merges the partial with the head's run
+// partials (t.nc_ref[si] = 1 if stream si has a reference block), writing out.
+template <int HD, bool I8, bool FUSED = false>
+__global__ void __launch_bounds__(128) rswa_verify_tail_kernel(TailArgs a, TailTable t, RswaRunMerge rm) {
     constexpr int CPL = HD / 32;
     __shared__ float sm_m[4], sm_l[4];
     __shared__ float sm_acc[4][HD];
@@ -788,6 +795,50 @@ __global__ void __launch_bounds__(128) rswa_verify_tail_kernel(TailArgs a, TailT
     for (int jj = 0; jj < CPL; ++jj) sm_acc[warp][lane * CPL + jj] = acc[jj];
     __syncthreads();
     float M = fmaxf(fmaxf(sm_m[0], sm_m[1]), fmaxf(sm_m[2], sm_m[3]));
+    if constexpr (FUSED) {
+        static_assert(HD == 128, "one thread per channel");
+        const int d = threadIdx.x;
+        float Ls = 0.0f, A = 0.0f;
+        for (int w2 = 0; w2 < 4; ++w2) {
+            const float f = sm_m[w2] == -INFINITY ? 0.0f : exp2f(sm_m[w2] - M);
+            Ls += sm_l[w2] * f;
+            A += sm_acc[w2][d] * f;
+        }
+        pdl_wait();  // the split kernel's run partials are complete and visible
+        if (t.nc_ref[si] > 0) {
+            const int64_t unit = int64_t(si) * rm.H + h;
+            const int64_t first = rm.unit_slots[2 * unit], last = rm.unit_slots[2 * unit + 1];
+            constexpr int kBatch = 8;  // slots whose loads are in flight together
+            for (int64_t s0 = first; s0 <= last; s0 += kBatch) {
+                float mk[kBatch], lk[kBatch], vk[kBatch];
+#pragma unroll
+                for (int k = 0; k < kBatch; ++k) {
+                    const int64_t p = (s0 + k) * rm.K + i;
+                    mk[k] = -INFINITY;
+                    if (s0 + k <= last) {
+                        mk[k] = rm.pm[p];
+                        lk[k] = rm.pl[p];
+                        vk[k] = rm.pacc[p * 128 + d];
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < kBatch; ++k) {
+                    if (mk[k] == -INFINITY) continue;  // past the range, or an empty marker
+                    if (mk[k] > M) {
+                        const float r = exp2f(M - mk[k]);
+                        Ls *= r;
+                        A *= r;
+                        M = mk[k];
+                    }
+                    const float f = exp2f(mk[k] - M);
+                    Ls = fmaf(lk[k], f, Ls);
+                    A = fmaf(vk[k], f, A);
+                }
+            }
+        }
+        rm.out[((int64_t(s) * rm.K + i) * rm.H + h) * 128 + d] = A / Ls;
+        return;
+    }
     const int64_t p = ((int64_t(s) * a.H + h) * a.nc_max + t.nc_ref[si]) * a.K + i;
     for (int d = threadIdx.x; d < HD; d += blockDim.x) {
         float L = 0.0f, A = 0.0f;
@@ -826,57 +877,6 @@ __global__ void rswa_tc_tables_kernel(RswaTable tb, RswaTcTables t) {
     }
 }
 
-struct RswaRunMerge {
-    const float *pm, *pl, *pacc;     // run partials [slot][K] (+ [128])
-    const float *tpm, *tpl, *tpacc;  // tail partials [B][H][K] (+ [128])
-    const int64_t *unit_slots;       // [stream of the launch][H][2]
-    float *out;                      // [B][K][H][128]
-    int32_t H, K;
-};
-
-// Verify merge of the tensor-core path: query i of head h of stream s is the
-// log-sum-exp merge of the reference block's run partials (the slot range its
-// workers recorded; empty markers carry max -inf) and the ring-and-drafts
-// tail partial, which always holds at least draft i itself.
-__global__ void __launch_bounds__(128) merge_rswa_runs_kernel(RswaRunMerge a, RswaTable tb) {
-    const int h = blockIdx.x, si = blockIdx.y, i = blockIdx.z, d = threadIdx.x;
-    if (si >= tb.n) return;
-    const int s = tb.s0 + si;
-    const int64_t tp = (int64_t(s) * a.H + h) * a.K + i;
-    float M = a.tpm[tp], Ls = a.tpl[tp], acc = a.tpacc[tp * 128 + d];
-    if (tb.prefill_len[si] > 0) {
-        const int64_t unit = int64_t(si) * a.H + h;
-        const int64_t first = a.unit_slots[2 * unit], last = a.unit_slots[2 * unit + 1];
-        constexpr int kBatch = 8;  // slots whose loads are in flight together
-        for (int64_t s0 = first; s0 <= last; s0 += kBatch) {
-            float m[kBatch], l[kBatch], v[kBatch];
-#pragma unroll
-            for (int k = 0; k < kBatch; ++k) {
-                const int64_t p = (s0 + k) * a.K + i;
-                m[k] = -INFINITY;
-                if (s0 + k <= last) {
-                    m[k] = a.pm[p];
-                    l[k] = a.pl[p];
-                    v[k] = a.pacc[p * 128 + d];
-                }
-            }
-#pragma unroll
-            for (int k = 0; k < kBatch; ++k) {
-                if (m[k] == -INFINITY) continue;  // past the range, or an empty marker
-                if (m[k] > M) {
-                    const float r = exp2f(M - m[k]);
-                    Ls *= r;
-                    acc *= r;
-                    M = m[k];
-                }
-                const float f = exp2f(m[k] - M);
-                Ls = fmaf(l[k], f, Ls);
-                acc = fmaf(v[k], f, acc);
-            }
-        }
-    }
-    a.out[((int64_t(s) * a.K + i) * a.H + h) * 128 + d] = acc / Ls;
-}
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
@@ -1603,12 +1603,6 @@ static kvd_status rswa_verify_impl(const float *q, const float *dk, const float 
         workers = tc ? std::min(split_q8_tc_workers(variant), kRswaTcWorkers) : 0;
         tc = workers > 0;
     }
-    if (tc) {
-        ta.pm = reinterpret_cast<float *>(ws + w.tail_pm);
-        ta.pl = reinterpret_cast<float *>(ws + w.tail_pl);
-        ta.pacc = reinterpret_cast<float *>(ws + w.tail_pacc);
-        ta.nc_max = 1;
-    }
     const int hb = hpk_bucket(K);
     for (int32_t s0 = 0; s0 < B; s0 += kSlice) {
         RswaTable t;  // the split kernel reads the reference rows only
@@ -1622,7 +1616,8 @@ static kvd_status rswa_verify_impl(const float *q, const float *dk, const float 
             t.ring_len[i] = 0;
             tt.ring_len[i] = ring_len[s];
             tt.rp0[i] = ring_len[s] == W ? ring_pos[s] : 0;
-            tt.nc_ref[i] = tc ? 0 : int32_t(ceil_div(prefill_len[s], chunk));
+            // tensor-core path: nc_ref only flags a reference block for the fused merge
+            tt.nc_ref[i] = tc ? (prefill_len[s] > 0 ? 1 : 0) : int32_t(ceil_div(prefill_len[s], chunk));
             max_nc = std::max(max_nc, tt.nc_ref[i]);
         }
         if (tc) {
@@ -1658,21 +1653,18 @@ static kvd_status rswa_verify_impl(const float *q, const float *dk, const float 
             ls.live = tabs.live;
             ls.n_live = H;
             if (T > 0 && split_layer_q8_tc(variant, wa, ls, maps, st) != cudaSuccess) return KVD_ECUDA;
-            rswa_verify_tail_kernel<128, true><<<dim3(unsigned(K), unsigned(H), unsigned(t.n)), 128, 0, st>>>(ta, tt);
-            if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
             RswaRunMerge rm;
             rm.pm = wa.a.pm;
             rm.pl = wa.a.pl;
             rm.pacc = wa.a.pacc;
-            rm.tpm = ta.pm;
-            rm.tpl = ta.pl;
-            rm.tpacc = ta.pacc;
             rm.unit_slots = wa.unit_slots;
             rm.out = out;
             rm.H = H;
             rm.K = K;
-            merge_rswa_runs_kernel<<<dim3(unsigned(H), unsigned(t.n), unsigned(K)), 128, 0, st>>>(rm, t);
-            if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
+            // the ring-and-drafts partials and the merge, as the split's dependent
+            if (launch_pdl(rswa_verify_tail_kernel<128, true, true>, dim3(unsigned(K), unsigned(H), unsigned(t.n)),
+                           dim3(128), 0, st, ta, tt, rm) != cudaSuccess)
+                return KVD_ECUDA;
             continue;
         }
         if (max_nc > 0) {
@@ -1682,8 +1674,8 @@ static kvd_status rswa_verify_impl(const float *q, const float *dk, const float 
             if (e != cudaSuccess) return KVD_ECUDA;
         }
         dim3 tgrid(unsigned(K), unsigned(H), unsigned(t.n));
-        if (head_dim == 128) rswa_verify_tail_kernel<128, I8><<<tgrid, 128, 0, st>>>(ta, tt);
-        else rswa_verify_tail_kernel<64, I8><<<tgrid, 128, 0, st>>>(ta, tt);
+        if (head_dim == 128) rswa_verify_tail_kernel<128, I8><<<tgrid, 128, 0, st>>>(ta, tt, RswaRunMerge{});
+        else rswa_verify_tail_kernel<64, I8><<<tgrid, 128, 0, st>>>(ta, tt, RswaRunMerge{});
         if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
         dim3 mgrid(unsigned(H), unsigned(t.n), unsigned(K));
         if (head_dim == 128) merge_rswa_verify_kernel<128><<<mgrid, 128, 0, st>>>(m, t, K);
