@@ -430,7 +430,14 @@ KVD_API kvd_status rswa_verify(const float *q, const float *draft_k, const float
                                int64_t workspace_bytes, void *stream);
 
 /* rswa_verify over the int8 mirror (decode_attention_int8): the drafts are
- * quantised per row as write_decode_step would mirror them. */
+ * quantised per row as write_decode_step would mirror them, and each draft
+ * query as decode_attention_int8 quantises a query.  At head_dim 128 with
+ * K <= 8, ref_cap a multiple of 32 and B * H * ref_cap < 2^31 the reference
+ * rows are read by the tensor-core kernel (TMA over the mirror's codes: their
+ * base pointers must then also suit a TMA descriptor, which the 16-byte rule
+ * above does; if the driver refuses one, the CUDA-core kernel runs); otherwise
+ * by the CUDA-core kernel.  Same results within the output tolerance either
+ * way; same workspace (rswa_verify_workspace_bytes covers both). */
 KVD_API kvd_status rswa_verify_i8(const float *q, const float *draft_k, const float *draft_v, int32_t K,
                                   const rswa_i8_mirror *m, const int32_t *prefill_len,
                                   const int32_t *ring_len, const int32_t *ring_pos, int32_t B, int32_t H,

@@ -1,5 +1,8 @@
 // kvd_split_mma.cuh -- split-KV decode over the q8_2f cache (int8 K and V,
 // head_dim 128) on the tensor cores (warp-level mma.sync, f16 in, f32 out).
+// The same kernel, in its row-scale mode (ROWK), reads the reference block of
+// the R-SWA int8 mirror for a query-batched verify (rswa verify_attention over
+// decode_attention_int8): one K scale per row, int8 query codes.
 //
 // Why tensor cores: with int8 rows a CUDA-core kernel spends ~84 instructions
 // per cached row (int8->f32 conversions, hpk x 128 FMAs per pass, warp
