@@ -879,6 +879,47 @@ def test_rswa_i8_verify_reference_runs(torch, kvd, K, ref_cap):
             assert err <= OUT_TOL, (s, i, err)
 
 
+def test_rswa_i8_verify_more_streams_than_one_launch(torch, kvd):
+    """260 streams: the tensor-core route of the int8 verify runs in two launch
+    slices (256 + 4 streams) that reuse the workspace's stream tables, unit
+    slot ranges and run partials; blocks of 0..96 rows (ragged tiles, empty
+    blocks), rings filling and full."""
+    B, H, hd, W, ref_cap, K = 260, 2, 128, 16, 96, 3
+    prefill = [(37 * s) % (ref_cap + 1) for s in range(B)]
+    cache = kvd.RingCache(B, ref_cap, H, hd, W, int8=True)
+    o_ref_k = np.zeros((B, H, ref_cap, hd), np.float32)
+    o_ref_v = np.zeros_like(o_ref_k)
+    k = synthetic.normal((B, H, ref_cap, hd), 6100)
+    v = synthetic.normal((B, H, ref_cap, hd), 6101)
+    for s in range(B):
+        m = prefill[s]
+        kvd.rswa_record_prefill(cache, s, torch.from_numpy(np.ascontiguousarray(k[s, :, :m])).cuda(),
+                                torch.from_numpy(np.ascontiguousarray(v[s, :, :m])).cuda())
+        o_ref_k[s, :, :m], o_ref_v[s, :, :m] = k[s, :, :m], v[s, :, :m]
+    o_ring_k = np.zeros((B, H, W, hd), np.float32)
+    o_ring_v = np.zeros_like(o_ring_k)
+    cursors = [np.zeros(2, np.int32) for _ in range(B)]
+    for t in range(20):
+        kt = synthetic.normal((B, H, hd), 6200 + t)
+        vt = synthetic.normal((B, H, hd), 6300 + t)
+        kvd.rswa_ring_write(cache, torch.from_numpy(kt).cuda(), torch.from_numpy(vt).cuda())
+        for s in range(B):
+            oracle.rswa_write(o_ring_k[s], o_ring_v[s], kt[s], vt[s], True, cursors[s])
+    scale = np.float32(1.0 / math.sqrt(hd))
+    q = synthetic.normal((B, K, H, hd), 6400)
+    dk = synthetic.normal((B, K, H, hd), 6401)
+    dv = synthetic.normal((B, K, H, hd), 6402)
+    out = kvd.rswa_verify(torch.from_numpy(q).cuda(), torch.from_numpy(dk).cuda(), torch.from_numpy(dv).cuda(),
+                          cache, int8=True).cpu().numpy()
+    assert cache.device_error() == 0
+    for s in list(range(0, B, 7)) + [255, 256, 257, 258, 259]:
+        ref = oracle.rswa_verify(q[s], dk[s], dv[s], o_ref_k[s], o_ref_v[s], prefill[s], o_ring_k[s],
+                                 o_ring_v[s], cursors[s], scale, int8=True)
+        for i in range(K):
+            err = out_error(out[s, i].reshape(H, hd), ref[i])
+            assert err <= OUT_TOL, (s, i, err)
+
+
 @pytest.mark.parametrize("int8", [False, True])
 def test_rswa_verify_steady_ring_and_fill(torch, kvd, int8):
     """One stream per ring state (warm with room for the drafts, filling during
