@@ -2,21 +2,27 @@
 """Decode-attention benchmark on GB300: KV GB/s (fraction of the HBM roofline)
 and decode queries/s.
 
-Default workload: q8_2f GQA decode, 32 sequences x 4096 cached rows, 32 query
-/ 8 KV heads, head_dim 128, the cache built one row at a time through
-kv_append (freeze and requantisation at row 64).  One step = the whole hot
-path for one decode token: kv_append of one new K/V row per sequence
-(quantised against the frozen fields) + decode_attention over every cached
-row with the attention-mass (imp) accumulation.  The timed region holds
-exactly --steps steps between a barrier + device synchronisation on each side;
---warmup steps run untimed first.  Two cache replicas alternate step by step
-so that every step streams HBM, not L2 (2 x 289 MB > 129 MB of L2).
+Default workload: the ragged serving batch -- 256 sequences with lengths
+U{1..16384} (seed 7), 32 query / 8 KV heads, head_dim 128, one layer per
+storage mode (f32, q8_2f, q8k, q8v), 2 of 8 KV heads dead per layer, outlier
+channels.  One step = the whole hot path for one decode token through the
+four layers: kv_append of one new K/V row per sequence (quantised against
+the frozen fields) + decode_attention over every cached row with the
+attention-mass (imp) accumulation.  The timed region holds exactly --steps
+steps between a barrier + device synchronisation on each side; --warmup
+steps run untimed first.  The layers hold ~34 GB, far above L2.  The line
+reports the step's KV GB/s, each mode's decode (without imp, timed alone)
+against the HBM roofline, the same with imp, the end-to-end rate through the
+public API with host buffers, and the CPU oracle on one and on all host cores.
 
-Other workloads (--workload): long_q8 (4 sequences x 131072 rows, 64 query /
-4 KV heads), tiny_f32, and the R-SWA decode of franken_ocr's rswa module
-(16 streams x 10 heads, a 32640-row reference block + a full 128-slot ring):
-rswa reads the f32 regions, rswa_i8 the int8 mirror; one step = the ring
-write of one token per stream (mirror included) + the decode of every stream.
+Other workloads (--workload): q8_gqa (32 sequences x 4096 rows, the cache
+built one row at a time, two or more cache replicas rotated so each step
+streams HBM), long_q8 (4 sequences x 131072 rows, 64 query / 4 KV heads),
+tiny_f32, verify_q8 (4 drafts verified per step), and the R-SWA decode of
+franken_ocr's rswa module (16 streams x 10 heads, a 32640-row reference block
++ a full 128-slot ring): rswa reads the f32 regions, rswa_i8 the int8 mirror;
+one step = the ring write of one token per stream (mirror included) + the
+decode of every stream; rswa_verify / rswa_i8_verify verify 4 drafts.
 
 Under torchrun each rank times its own replica on its own GPU (independent
 sequences: weak scaling, no data-path collective); rank 0 prints one JSON line
@@ -90,6 +96,200 @@ def peaks():
     return 6800.0, "fallback"
 
 
+# ------------------------------------------------------------ byte counts
+# The metric's algorithmic bytes: what a decode must move at least, whatever
+# the kernel (scratch partials are implementation cost and not counted).
+
+F32_MODE, Q8_MODE, Q8K_MODE, Q8V_MODE = 0, 1, 2, 3
+MODE_NAMES = ("f32", "q8", "q8k", "q8v")
+
+
+def kv_bytes_per_row(mode: int, hd: int) -> int:
+    """Stored bytes per cached row per live KV head (K and V with their scales)."""
+    qk = mode in (Q8_MODE, Q8K_MODE)
+    qv = mode in (Q8_MODE, Q8V_MODE)
+    kb = hd + 4 * (hd // 32) if qk else 4 * hd
+    vb = hd + 4 if qv else 4 * hd
+    return kb + vb
+
+
+def n_fields(mode: int) -> int:
+    return (1 if mode in (Q8_MODE, Q8K_MODE) else 0) + (1 if mode in (Q8_MODE, Q8V_MODE) else 0)
+
+
+def decode_bytes(mode, n_live, hd, n_q, lengths, with_imp, n_seq) -> int:
+    """One decode call: every live row's K/V (+ scales) once, the query and
+    output, the fields of the quantised components, and imp read + write when
+    it is requested."""
+    rows = int(np.sum(lengths)) * n_live
+    b = rows * kv_bytes_per_row(mode, hd)
+    b += 2 * n_seq * n_q * hd * 4
+    b += n_fields(mode) * n_seq * n_live * hd * 4
+    if with_imp:
+        b += 8 * int(np.sum(lengths))
+    return b
+
+
+def append_bytes(mode, n_live, hd, n_seq) -> int:
+    """Appending one row per sequence: f32 K, V in for the live heads, stored
+    codes/scales (or f32 rows) out, fields read."""
+    b = n_seq * n_live * (8 * hd + kv_bytes_per_row(mode, hd))
+    return b + n_fields(mode) * n_seq * n_live * hd * 4
+
+
+def rswa_bytes(B, H, hd, lengths) -> int:
+    return int(np.sum(lengths)) * H * hd * 8 + 2 * B * H * hd * 4
+
+
+def rswa_i8_bytes(B, H, hd, lengths) -> int:
+    """One int8-mirror decode: every row's K and V codes and their two row
+    scales, plus the f32 query and output."""
+    return int(np.sum(lengths)) * H * (2 * hd + 8) + 2 * B * H * hd * 4
+
+
+def host_cpu() -> dict:
+    """The host's core count and CPU model (lscpu, else /proc/cpuinfo)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith(("model name", "cpu part")):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except OSError:
+            pass
+    return {"nproc": os.cpu_count(), "cpu_model": model}
+
+
+class GqaOracleSample:
+    """Sampled sequences of one GQA layer rebuilt in the CPU oracle from the
+    workload's seeded recipe -- rows drawn on the host (the device's draws come
+    from another generator: same distribution, other numbers) and appended one
+    row at a time -- with one decode query per sequence.  run() decodes every
+    sampled sequence (all query heads, every row, imp on) through the oracle's
+    multi-sequence driver."""
+
+    def __init__(self, mode, n_q, n_kv, hd, lengths, alive, seed, outliers, picks):
+        import oracle
+        import synthetic
+
+        self.mode, self.n_q, self.picks = mode, n_q, list(picks)
+        q_all = synthetic.gqa_query(seed, 0, len(lengths), n_q, hd, "cpu").numpy()
+        self.caches, self.qs = [], []
+        for b in self.picks:
+            L = int(lengths[b])
+            k, v = synthetic.gqa_seq_rows(seed, b, L, n_kv, hd, outliers, "cpu")
+            oc = oracle.OracleSeqCache(mode, n_kv, hd, max(L, 1), alive=alive)
+            oc.append_rows(k.numpy(), v.numpy())
+            self.caches.append(oc)
+            self.qs.append(q_all[b])
+        self.scale = np.float32(1.0 / math.sqrt(hd))
+        self.rows = [int(lengths[b]) for b in self.picks]
+        self.bytes = decode_bytes(mode, int(np.sum(alive)), hd, n_q, self.rows, True, len(self.picks))
+
+    def run(self, threads: int) -> int:
+        import oracle
+
+        imps = [np.zeros(c.cap) for c in self.caches]
+        _, used = oracle.decode_many(self.caches, self.qs, self.n_q, self.scale, imps, threads)
+        return used
+
+
+def time_oracle(samples, threads: int, min_seconds: float = 0.0, reps: int | None = None):
+    """Decode every sample (one call per sample per repetition) until
+    min_seconds have passed or `reps` repetitions ran: (GB/s, seconds per
+    repetition, threads used)."""
+    nbytes = sum(s.bytes for s in samples)
+    n, used, t0 = 0, 1, time.perf_counter()
+    while True:
+        for smp in samples:
+            used = max(used, smp.run(threads))
+        n += 1
+        el = time.perf_counter() - t0
+        if (reps is not None and n >= reps) or (reps is None and el >= min_seconds):
+            break
+    return nbytes / (el / n) / 1e9, el / n, used
+
+
+def time_threaded(samples, threads: int, min_seconds: float):
+    """Run every sample's decode() once per repetition, the samples shared among
+    `threads` Python threads (each decode is one call into the C oracle, which
+    releases the interpreter lock), until min_seconds have passed: (GB/s,
+    seconds per repetition, threads)."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    nbytes = sum(s.bytes for s in samples)
+    n, t0 = 0, time.perf_counter()
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        while True:
+            list(ex.map(lambda smp: smp.decode(), samples))
+            n += 1
+            el = time.perf_counter() - t0
+            if el >= min_seconds:
+                break
+    return nbytes / (el / n) / 1e9, el / n, min(threads, len(samples))
+
+
+def cpu_baseline_gqa(single, multi, seconds: float, what_single: str, what_multi: str) -> dict:
+    """The oracle on one host core (the `single` samples) and on every core
+    (the `multi` samples, its (sequence, head) pairs shared among threads)."""
+    v1, _, _ = time_oracle(single, 1, seconds / 2)
+    vn, _, used = time_oracle(multi, 0, seconds / 2)
+    info = host_cpu()
+    return {"value": round(vn, 4), "unit": "GB/s", "cores": used, "kind": "oracle",
+            "sample": "%s, %.1f s" % (what_multi, seconds / 2),
+            "single_core": {"value": round(v1, 4), "unit": "GB/s", "cores": 1,
+                            "sample": "%s, %.1f s" % (what_single, seconds / 2)},
+            "nproc": info["nproc"], "cpu_model": info["cpu_model"]}
+
+
+def gqa_samples(name: str, n_multi: int):
+    """(single-core samples, all-core samples, descriptions) of a fixed-length
+    GQA workload: one sequence, and the first n_multi sequences."""
+    import synthetic
+
+    w = synthetic.GQA_WORKLOADS[name]
+    mode = MODE_NAMES.index(w["mode"])
+    lengths = [w["rows"]] * w["n_seq"]
+    alive = np.ones(w["n_kv"], np.uint8)
+    n_multi = min(n_multi, w["n_seq"])
+    multi = GqaOracleSample(mode, w["n_q"], w["n_kv"], w["hd"], lengths, alive, w["seed"], w["outliers"],
+                            range(n_multi))
+    single = GqaOracleSample(mode, w["n_q"], w["n_kv"], w["hd"], lengths, alive, w["seed"], w["outliers"],
+                             [0])
+    what = "%%d of %d sequences (all %d query heads x %d rows, imp on), f64" % (w["n_seq"], w["n_q"], w["rows"])
+    return [single], [multi], what % 1, what % n_multi
+
+
+def ragged_samples(n_multi: int, n_seq: int = 256):
+    """(single-core samples, all-core samples, descriptions) of the ragged
+    batch: per layer (f32, q8, q8k, q8v) the sequence nearest the mean length,
+    and n_multi sequences spaced evenly through the batch."""
+    import synthetic
+
+    lengths, specs = synthetic.ragged_batch(n_seq)
+    step = max(1, len(lengths) // n_multi)
+    picks = list(range(0, len(lengths), step))[:n_multi]
+    one = int(np.argmin(np.abs(lengths - lengths.mean())))
+    single, multi = [], []
+    for mode, (_, alive, seed) in enumerate(specs):
+        multi.append(GqaOracleSample(mode, 32, 8, 128, lengths, alive, seed, True, picks))
+        single.append(GqaOracleSample(mode, 32, 8, 128, lengths, alive, seed, True, [one]))
+    rows = int(np.sum(lengths[picks]))
+    return (single, multi,
+            "1 sequence (%d rows) of each of the 4 layers, all 32 query heads, imp on, f64" % lengths[one],
+            "%d of %d sequences (%d rows) of each of the 4 layers, all 32 query heads, imp on, f64"
+            % (len(picks), len(lengths), rows))
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons while the GPU works."""
 
@@ -150,59 +350,42 @@ class ClockSampler:
 
 # --------------------------------------------------------------- reference
 
-def oracle_sample_gbs(wl, n_seq_sample: int, min_seconds: float, max_reps: int | None = None):
-    """Time the CPU oracle (single thread) decoding `n_seq_sample` sequences of
-    the workload (every query head, every cached row, f64 two-pass softmax)."""
-    import oracle
-    import torch
-
-    from kv_cache_decode_attention_gb300 import workloads as W
-
-    caches, qs = [], []
-    q_all = wl.query(10_000).cpu().numpy()
-    for b in range(n_seq_sample):
-        k, v = wl.rows(b)
-        k, v = k.cpu().numpy(), v.cpu().numpy()
-        oc = oracle.OracleSeqCache(wl.mode, wl.n_kv, wl.hd, int(wl.lengths[b]), alive=wl.alive)
-        oc.append_rows(k, v)
-        caches.append(oc)
-        qs.append(q_all[b])
-        del k, v
-        torch.cuda.empty_cache()
-    n_live = int(wl.alive.sum())
-    bytes_per = W.decode_bytes(wl.mode, n_live, wl.hd, wl.n_q, wl.lengths[:n_seq_sample], True,
-                               n_seq_sample)
-    reps, t0 = 0, time.perf_counter()
-    while True:
-        for b, oc in enumerate(caches):
-            imp = np.zeros(oc.cap)
-            oc.decode(qs[b], wl.n_q, np.float32(wl.scale), imp)
-        reps += 1
-        el = time.perf_counter() - t0
-        if el >= min_seconds or (max_reps is not None and reps >= max_reps):
-            break
-    per_rep = el / reps
-    return bytes_per / per_rep / 1e9, per_rep, bytes_per
-
-
 class RswaOracleSample:
     """One stream of an R-SWA workload rebuilt on the host from the workload's
     generators (its reference rows and the ring rows of its 500 writes), ready
     for the CPU oracle's decode (f32 regions, or their int8 mirror)."""
 
-    def __init__(self, wl, int8: bool, s: int = 0, verify_k: int = 0):
+    @classmethod
+    def many(cls, wl, int8: bool, streams, verify_k: int = 0):
+        """Samples of several streams, their ring writes replayed together."""
+        import oracle
+
+        c = wl.cache
+        rings = {s: (np.zeros((c.H, c.W, c.head_dim), np.float32), np.zeros((c.H, c.W, c.head_dim), np.float32),
+                     np.zeros(2, np.int32)) for s in streams}
+        for t in range(wl.steps):
+            k, v = wl.step_rows(t)
+            k, v = k.cpu().numpy(), v.cpu().numpy()
+            for s, (rk, rv, cur) in rings.items():
+                oracle.rswa_write(rk, rv, k[s], v[s], True, cur)
+        return [cls(wl, int8, s, verify_k, rings[s]) for s in streams]
+
+    def __init__(self, wl, int8: bool, s: int = 0, verify_k: int = 0, ring=None):
         import oracle
 
         c = wl.cache
         self.int8, self.H, self.hd, self.verify_k = int8, c.H, c.head_dim, verify_k
         pk, pv = wl.prefill_rows(s)
         self.ref_k, self.ref_v = pk.cpu().numpy(), pv.cpu().numpy()
-        self.ring_k = np.zeros((c.H, c.W, c.head_dim), np.float32)
-        self.ring_v = np.zeros_like(self.ring_k)
-        cur = np.zeros(2, np.int32)
-        for t in range(wl.steps):
-            k, v = wl.step_rows(t)
-            oracle.rswa_write(self.ring_k, self.ring_v, k[s].cpu().numpy(), v[s].cpu().numpy(), True, cur)
+        if ring is None:
+            self.ring_k = np.zeros((c.H, c.W, c.head_dim), np.float32)
+            self.ring_v = np.zeros_like(self.ring_k)
+            cur = np.zeros(2, np.int32)
+            for t in range(wl.steps):
+                k, v = wl.step_rows(t)
+                oracle.rswa_write(self.ring_k, self.ring_v, k[s].cpu().numpy(), v[s].cpu().numpy(), True, cur)
+        else:
+            self.ring_k, self.ring_v, cur = ring
         self.prefill, self.ring_len = wl.prefill, int(cur[0])
         self.cursors = cur
         self.q = wl.query(10_000)[s].cpu().numpy()
@@ -214,9 +397,7 @@ class RswaOracleSample:
         if int8:
             self.mir = [oracle.rswa_mirror(x) for x in (self.ref_k, self.ref_v, self.ring_k, self.ring_v)]
         self.rows = self.prefill + self.ring_len
-        from kv_cache_decode_attention_gb300 import workloads as W
-
-        self.bytes = (W.rswa_i8_bytes if int8 else W.rswa_bytes)(1, c.H, c.head_dim, [self.rows])
+        self.bytes = (rswa_i8_bytes if int8 else rswa_bytes)(1, c.H, c.head_dim, [self.rows])
         if verify_k:
             self.bytes += 2 * verify_k * c.H * c.head_dim * 4 + 2 * (verify_k - 1) * c.H * c.head_dim * 4
 
@@ -251,67 +432,85 @@ class RswaOracleSample:
             "int8 mirror" if self.int8 else "f32 regions")
 
 
+class VerifyOracleSample:
+    """Sequence 0 of q8_gqa rebuilt in the oracle from its seeded recipe on the
+    host, with K draft rows appended; run() verifies the K draft queries
+    (oracle decode_verify, causal among the drafts)."""
+
+    def __init__(self, K: int, b: int = 0):
+        import oracle
+        import synthetic
+
+        w = synthetic.GQA_WORKLOADS["q8_gqa"]
+        self.K, self.n_q, self.picks = K, w["n_q"], [b]
+        k, v = synthetic.gqa_seq_rows(w["seed"], b, w["rows"], w["n_kv"], w["hd"], True, "cpu")
+        self.oc = oracle.OracleSeqCache(Q8_MODE, w["n_kv"], w["hd"], w["rows"] + K)
+        self.oc.append_rows(k.numpy(), v.numpy())
+        self.oc.append_rows(synthetic.normal((K, w["n_kv"], w["hd"]), 91_000),
+                            synthetic.normal((K, w["n_kv"], w["hd"]), 91_001))
+        self.q = synthetic.normal((K, w["n_q"], w["hd"]), 91_002)
+        self.scale = np.float32(1.0 / math.sqrt(w["hd"]))
+        self.bytes = decode_bytes(Q8_MODE, w["n_kv"], w["hd"], w["n_q"], [w["rows"] + K], False, 1)
+        self.what = "1 of %d sequences (%d drafts x %d query heads x %d rows), f64" % (
+            w["n_seq"], K, w["n_q"], w["rows"] + K)
+
+    def decode(self):
+        return self.oc.decode_verify(self.q, self.n_q, self.K, self.scale)
+
+    def run(self, threads: int) -> int:
+        self.decode()
+        return 1
+
+
 def run_reference(args, rank):
     """--impl reference: the CPU oracle as it stands, on the host cores, each
-    step a bounded sample (one sequence, every head and cached row) of the
-    workload; rank 0 only."""
+    step a bounded sample of the workload decoded through the oracle's
+    multi-sequence driver on every core; rank 0 only.  The GQA workloads are
+    rebuilt from their seeded recipes on the host (the library under test is
+    neither loaded nor built); the R-SWA ones read their rows from the device
+    workload."""
     if rank != 0:
         return
-    import torch
+    if args.workload in ("ragged", "q8_gqa", "long_q8", "tiny_f32", "verify_q8"):
+        if args.workload == "ragged":
+            _, multi, _, what = ragged_samples(args.cpu_sample_seqs)
+            name = "ragged"
+        elif args.workload == "verify_q8":
+            multi = [VerifyOracleSample(VERIFY_DRAFTS)]
+            what, name = multi[0].what, "verify_q8_gqa"
+        else:
+            _, multi, _, what = gqa_samples(args.workload, args.cpu_sample_seqs)
+            name = args.workload
+        time_oracle(multi, 0, reps=max(1, args.warmup))
+        gbs, per, used = time_oracle(multi, 0, reps=args.steps)
+        sample = what
+        queries = sum(len(m.picks) for m in multi)
+    else:
+        import torch
 
-    from kv_cache_decode_attention_gb300 import workloads as W
+        from kv_cache_decode_attention_gb300 import workloads as W
 
-    if not torch.cuda.is_available():
-        print(json.dumps({"impl": "reference", "unavailable": "needs the GPU box to build the workload"}))
-        return
-    if args.workload in RSWA_WORKLOADS:
+        if not torch.cuda.is_available():
+            print(json.dumps({"impl": "reference", "unavailable": "needs the GPU box to build the workload"}))
+            return
         int8, verify = args.workload.startswith("rswa_i8"), args.workload.endswith("_verify")
         wl = W.rswa_steady(B=args.rswa_streams, int8=int8)
         smp = RswaOracleSample(wl, int8, verify_k=VERIFY_DRAFTS if verify else 0)
         smp.gbs(0.0, max_reps=max(1, args.warmup))
         gbs, per = smp.gbs(0.0, max_reps=args.steps)
-        sample, name = smp.describe(wl), args.workload + "_steady"
-    elif args.workload == "verify_q8":
-        import oracle
-        import synthetic
-
-        K = VERIFY_DRAFTS
-        wl = W.q8_gqa(extra_cap=64)
-        k, v = wl.rows(0)
-        oc = oracle.OracleSeqCache(wl.mode, wl.n_kv, wl.hd, int(wl.lengths[0]) + K, alive=wl.alive)
-        oc.append_rows(k.cpu().numpy(), v.cpu().numpy())
-        oc.append_rows(synthetic.normal((K, wl.n_kv, wl.hd), 91_000), synthetic.normal((K, wl.n_kv, wl.hd), 91_001))
-        q0 = synthetic.normal((K, wl.n_q, wl.hd), 91_002)
-        one = W.decode_bytes(wl.mode, int(wl.alive.sum()), wl.hd, wl.n_q, wl.lengths[:1] + K, False, 1)
-        for _ in range(max(1, args.warmup)):
-            oc.decode_verify(q0, wl.n_q, K, np.float32(wl.scale))
-        a0 = time.perf_counter()
-        for _ in range(args.steps):
-            oc.decode_verify(q0, wl.n_q, K, np.float32(wl.scale))
-        per = (time.perf_counter() - a0) / args.steps
-        gbs = one / per / 1e9
-        sample = "1 of %d sequences (%d drafts x %d query heads x %d rows), f64" % (
-            wl.n_seq, K, wl.n_q, int(wl.lengths[0]) + K)
-        name = "verify_q8_gqa"
-    else:
-        wl = build_workload(args.workload, replicas=1)[0]
-        # warm-up and timed steps: one oracle decode of the sampled sequence each
-        gbs_w, _, _ = oracle_sample_gbs(wl, 1, 0.0, max_reps=max(1, args.warmup))
-        gbs, per, nbytes = oracle_sample_gbs(wl, 1, 0.0, max_reps=args.steps)
-        sample = "1 of %d sequences (all %d query heads, %d rows), f64 two-pass softmax" % (
-            wl.n_seq, wl.n_q, int(wl.lengths[0]))
-        name = wl.name
+        sample, name, used, queries = smp.describe(wl), args.workload + "_steady", 1, 1
+    info = host_cpu()
     line = {
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(per * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": name, "sample": sample},
-        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": sample},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": used, "kind": "oracle",
+                         "sample": sample, "nproc": info["nproc"], "cpu_model": info["cpu_model"]},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
-        "queries_per_s": round(1.0 / per, 4),
+        "queries_per_s": round(queries / per, 4),
     }
     print(json.dumps(line), flush=True)
 
@@ -418,7 +617,7 @@ def run_gpu_rswa(args, rank, world):
         decode = kvd.rswa_decode_i8 if int8 else kvd.rswa_decode
     B, H, hd = c.B, c.H, c.head_dim
     lengths = c.prefill_len + c.ring_len  # steady state: constant over the steps
-    dec_bytes = (W.rswa_i8_bytes if int8 else W.rswa_bytes)(B, H, hd, lengths)
+    dec_bytes = (rswa_i8_bytes if int8 else rswa_bytes)(B, H, hd, lengths)
     # ring write: read k, v; write the f32 rows (+ codes and scales with the mirror)
     wr_bytes = B * H * hd * 4 * 4 + (B * H * (2 * hd + 8) if int8 else 0)
     if verify:
@@ -538,10 +737,17 @@ def run_gpu_rswa(args, rank, world):
         return
     cpu = None
     if not args.no_cpu_baseline:
-        smp = RswaOracleSample(wl, int8, verify_k=K if verify else 0)
-        v, per = smp.gbs(args.cpu_seconds)
-        cpu = {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": smp.describe(wl) + ", %.1f s" % args.cpu_seconds}
+        info = host_cpu()
+        n_par = max(1, min(B, info["nproc"] or 1, args.cpu_sample_seqs))
+        smps = RswaOracleSample.many(wl, int8, list(range(n_par)), verify_k=K if verify else 0)
+        v1, _ = smps[0].gbs(args.cpu_seconds / 2)
+        vn, _, used = time_threaded(smps, n_par, args.cpu_seconds / 2)
+        cpu = {"value": round(vn, 4), "unit": "GB/s", "cores": used, "kind": "oracle",
+               "sample": "%d streams at once, one per thread: %s, %.1f s" % (
+                   n_par, smps[0].describe(wl), args.cpu_seconds / 2),
+               "single_core": {"value": round(v1, 4), "unit": "GB/s", "cores": 1,
+                               "sample": smps[0].describe(wl) + ", %.1f s" % (args.cpu_seconds / 2)},
+               "nproc": info["nproc"], "cpu_model": info["cpu_model"]}
     line = {
         "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
@@ -592,7 +798,7 @@ def run_gpu_verify(args, rank, world):
     torch.cuda.set_device(dev)
     probe = W.q8_gqa(extra_cap=64)
     n_live = int(probe.alive.sum())
-    bytes_each = W.decode_bytes(probe.mode, n_live, probe.hd, probe.n_q, probe.lengths + K, False, probe.n_seq)
+    bytes_each = decode_bytes(probe.mode, n_live, probe.hd, probe.n_q, probe.lengths + K, False, probe.n_seq)
     R = max(1, min(8, math.ceil(4 * L2_BYTES / bytes_each)))
     wls = [probe] + [W.q8_gqa(extra_cap=64) for _ in range(R - 1)]
     n_seq, n_q, n_kv, hd = probe.n_seq, probe.n_q, probe.n_kv, probe.hd
@@ -646,7 +852,7 @@ def run_gpu_verify(args, rank, world):
     ms_per_step = elapsed_ms / args.steps
     # per step: K appended rows per sequence, the verify's read of every cached row
     # (the drafts included), its K queries and outputs
-    step_bytes = K * W.append_bytes(probe.mode, n_live, hd, n_seq) + bytes_each + 2 * n_seq * (K - 1) * n_q * hd * 4
+    step_bytes = K * append_bytes(probe.mode, n_live, hd, n_seq) + bytes_each + 2 * n_seq * (K - 1) * n_q * hd * 4
     gbs = replicas.whole_job_rate(step_bytes * args.steps, elapsed_ms * 1e-3, world) / 1e9
     # the verify call timed inside the same steps run again with events around
     # it (kept out of the timed steps above)
@@ -695,24 +901,17 @@ def run_gpu_verify(args, rank, world):
         return
     cpu = None
     if not args.no_cpu_baseline:
-        import oracle
-
-        k, v = probe.rows(0)
-        oc = oracle.OracleSeqCache(probe.mode, n_kv, hd, int(probe.lengths[0]) + K, alive=probe.alive)
-        oc.append_rows(k.cpu().numpy(), v.cpu().numpy())
-        dk = drafts[0][0].cpu().numpy().reshape(n_seq, K, n_kv, hd)[0]
-        dv = drafts[0][1].cpu().numpy().reshape(n_seq, K, n_kv, hd)[0]
-        oc.append_rows(dk, dv)
-        q0 = qs[0][0].cpu().numpy()
-        reps, a0 = 0, time.perf_counter()
-        while time.perf_counter() - a0 < args.cpu_seconds:
-            oc.decode_verify(q0, n_q, K, np.float32(probe.scale))
-            reps += 1
-        per = (time.perf_counter() - a0) / reps
-        one = W.decode_bytes(probe.mode, n_live, hd, n_q, probe.lengths[:1] + K, False, 1)
-        cpu = {"value": round(one / per / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": "1 of %d sequences (%d drafts x %d query heads x %d rows), f64, %.1f s" % (
-                   n_seq, K, n_q, int(probe.lengths[0]) + K, args.cpu_seconds)}
+        info = host_cpu()
+        n_par = max(1, min(n_seq, info["nproc"] or 1, args.cpu_sample_seqs))
+        smps = [VerifyOracleSample(K, b) for b in range(n_par)]
+        v1, _, _ = time_oracle(smps[:1], 1, args.cpu_seconds / 2)
+        vn, _, used = time_threaded(smps, n_par, args.cpu_seconds / 2)
+        cpu = {"value": round(vn, 4), "unit": "GB/s", "cores": used, "kind": "oracle",
+               "sample": "%d sequences at once, one per thread: %s, %.1f s" % (
+                   n_par, smps[0].what, args.cpu_seconds / 2),
+               "single_core": {"value": round(v1, 4), "unit": "GB/s", "cores": 1,
+                               "sample": smps[0].what + ", %.1f s" % (args.cpu_seconds / 2)},
+               "nproc": info["nproc"], "cpu_model": info["cpu_model"]}
     line = {
         "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
@@ -738,6 +937,230 @@ def run_gpu_verify(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_gpu_ragged(args, rank, world):
+    """The ragged serving batch: 256 sequences, lengths U{1..16384}, one layer
+    per storage mode (f32, q8, q8k, q8v), 2 of 8 KV heads dead per layer.  One
+    step = for every layer, kv_append of one row per sequence + decode_attention
+    with imp (a decode token through the four layers).  The layers together hold
+    ~34 GB, far above L2, so every step streams HBM."""
+    import torch
+
+    import kv_cache_decode_attention_gb300 as kvd
+    from kv_cache_decode_attention_gb300 import replicas
+    from kv_cache_decode_attention_gb300 import workloads as W
+
+    dev = torch.device("cuda", replicas.rank_info().local_rank)
+    torch.cuda.set_device(dev)
+    n_ev = min(args.steps, 10)
+    sync_steps = min(args.steps, 20)
+    spare = args.warmup + 2 * args.steps + n_ev + sync_steps + 16
+    layers = W.ragged(extra_cap=spare, n_seq=args.ragged_seqs, device=dev)
+    w0 = layers[0]
+    n_seq, n_q, n_kv, hd = w0.n_seq, w0.n_q, w0.n_kv, w0.hd
+    n_live = [int(w.alive.sum()) for w in layers]
+    imps = [torch.zeros(w.layer.imp_len, device=dev) for w in layers]
+    out_all = torch.empty(len(layers), n_seq, n_q, hd, device=dev)
+    outs = [out_all[i] for i in range(len(layers))]
+    ws = torch.empty(max(w.layer.workspace_bytes(n_q, True) for w in layers), dtype=torch.uint8, device=dev)
+    qs = [[w.query(i, dev) for i in range(8)] for w in layers]
+    news = [[w.new_rows(i, dev) for i in range(8)] for w in layers]
+    stream = torch.cuda.current_stream()
+    lens = np.array([w0.layer.seq_len(b) for b in range(n_seq)], np.int64)  # the same in every layer
+
+    def step(i, ev=None):
+        for li, w in enumerate(layers):
+            k, v = news[li][i % 8]
+            kvd.kv_append(w.layer, k, v)
+            if ev is not None:
+                ev[li][0].record(stream)
+            kvd.decode_attention(qs[li][i % 8], w.layer, out=outs[li], imp=imps[li], scale=w.scale,
+                                 workspace=ws)
+            if ev is not None:
+                ev[li][1].record(stream)
+
+    def step_bytes(lens_after):
+        return sum(append_bytes(w.mode, n_live[li], hd, n_seq) +
+                   decode_bytes(w.mode, n_live[li], hd, n_q, lens_after, True, n_seq)
+                   for li, w in enumerate(layers))
+
+    for i in range(args.warmup):
+        step(i)
+    lens += args.warmup
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev.index)
+    with sampler:
+        time.sleep(0.3)
+        replicas.barrier()
+        torch.cuda.synchronize()
+        c0 = time.time()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.profiler.start()
+        t0.record(stream)
+        for j in range(args.steps):
+            step(args.warmup + j)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        torch.cuda.profiler.stop()
+        replicas.barrier()
+        c1 = time.time()
+        time.sleep(0.1)
+    bytes_total = 0
+    for j in range(args.steps):
+        lens += 1
+        bytes_total += step_bytes(lens)
+    n_done = args.warmup + args.steps
+    elapsed_ms = replicas.max_over_ranks(t0.elapsed_time(t1))
+    ms_per_step = elapsed_ms / args.steps
+    gbs = replicas.whole_job_rate(bytes_total, elapsed_ms * 1e-3, world) / 1e9
+
+    # each layer's decode with imp, timed inside steps run again with events
+    # around it (kept out of the timed steps above)
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in layers]
+           for _ in range(n_ev)]
+    imp_bytes = [0] * len(layers)
+    for j in range(n_ev):
+        step(n_done + j, evs[j])
+        lens += 1
+        for li, w in enumerate(layers):
+            imp_bytes[li] += decode_bytes(w.mode, n_live[li], hd, n_q, lens, True, n_seq)
+    n_done += n_ev
+    torch.cuda.synchronize()
+    imp_ms = [statistics.mean(evs[j][li][0].elapsed_time(evs[j][li][1]) for j in range(n_ev))
+              for li in range(len(layers))]
+    imp_bytes = [b / n_ev for b in imp_bytes]
+
+    # ---- per mode: the decode call without imp timed alone (CUDA events on the
+    #      launching stream), each layer's calls back to back
+    peak, peak_kind = peaks()
+    nrep = max(10, min(args.steps, 40))
+    per_mode = {}
+    k_bytes, k_ms = [], []
+    kernels = {F32_MODE: "split_layer_kernel<128,4,f32> + merge_layer_kernel",
+               Q8_MODE: "split_warp_kernel (mma.sync) + merge_heads_kernel",
+               Q8K_MODE: "split_layer_kernel<128,4,q8k> + merge_layer_kernel",
+               Q8V_MODE: "split_layer_kernel<128,4,q8v> + merge_layer_kernel"}
+    torch.cuda.profiler.start()  # second profiled range: the per-mode decode calls
+    for li, w in enumerate(layers):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nrep)]
+        for j in range(nrep):
+            ev[j][0].record(stream)
+            kvd.decode_attention(qs[li][j % 8], w.layer, out=outs[li], imp=None, scale=w.scale, workspace=ws)
+            ev[j][1].record(stream)
+        torch.cuda.synchronize()
+        ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        nb = decode_bytes(w.mode, n_live[li], hd, n_q, lens, False, n_seq)
+        k_bytes.append(nb)
+        k_ms.append(ms)
+        name = MODE_NAMES[w.mode]
+        achieved = nb / (ms * 1e-3) / 1e9
+        per_mode[name] = {
+            "bound": "hbm", "kernel": kernels[w.mode], "achieved": round(achieved, 1), "peak": peak,
+            "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "traffic": measured_traffic("ragged_" + name, nb), "peak_kind": peak_kind,
+            "ms_per_launch": round(ms, 5), "bytes_per_launch": int(nb),
+            "imp_on": {"ms_per_launch": round(imp_ms[li], 5), "bytes_per_launch": int(imp_bytes[li]),
+                       "achieved": round(imp_bytes[li] / (imp_ms[li] * 1e-3) / 1e9, 1),
+                       "frac": round(imp_bytes[li] / (imp_ms[li] * 1e-3) / 1e9 / peak, 4)},
+        }
+    torch.cuda.profiler.stop()
+    achieved = sum(k_bytes) / (sum(k_ms) * 1e-3) / 1e9
+    tr = [per_mode[MODE_NAMES[w.mode]]["traffic"] for w in layers]
+
+    # ---- end to end through the public API with host buffers: every step's 4
+    #      queries and 4 x (k, v) new rows copied in from one pinned buffer, the
+    #      4 layers' outputs copied out (pipelined; then synchronising per step)
+    parts = [tuple(t for li in range(len(layers)) for t in (qs[li][i], news[li][i][0], news[li][i][1]))
+             for i in range(8)]
+    pinned, stage, views = packed_inputs(torch, parts)
+    stages = [(stage, views), restage(torch, stage, views)]
+    pin_outs = [torch.empty(out_all.shape).pin_memory() for _ in range(2)]
+
+    def e2e_step(j, vw, last_copy):
+        wait_copied(torch, last_copy(out_all))
+        for li, w in enumerate(layers):
+            kvd.kv_append(w.layer, vw[3 * li + 1], vw[3 * li + 2])
+            kvd.decode_attention(vw[3 * li], w.layer, out=outs[li], imp=imps[li], scale=w.scale, workspace=ws)
+        return out_all, pin_outs[j % 2]
+
+    lens_b = lens.copy()
+    secs = e2e_pipelined(torch, pinned, stages, args.steps, e2e_step)
+    eb = 0
+    for j in range(args.steps):
+        lens += 1
+        eb += step_bytes(lens)
+    e2e = {"value": round(eb / secs / 1e9 * world, 2), "unit": "GB/s",
+           "h2d_bytes_per_step": int(stage.numel() * 4), "d2h_bytes_per_step": int(out_all.numel() * 4),
+           "mode": "pipelined: inputs copied in on a copy stream while the previous step computes, "
+                   "outputs copied out on another, one host synchronisation at the end"}
+    torch.cuda.synchronize()
+    eb = 0
+    a0 = time.perf_counter()
+    for j in range(sync_steps):
+        stage.copy_(pinned[j % 8], non_blocking=True)
+        for li, w in enumerate(layers):
+            kvd.kv_append(w.layer, views[3 * li + 1], views[3 * li + 2])
+            kvd.decode_attention(views[3 * li], w.layer, out=outs[li], imp=imps[li], scale=w.scale,
+                                 workspace=ws)
+        pin_outs[0].copy_(out_all, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    a1 = time.perf_counter()
+    for j in range(sync_steps):
+        lens += 1
+        eb += step_bytes(lens)
+    e2e_sync = {"value": round(eb / (a1 - a0) / 1e9 * world, 2), "unit": "GB/s",
+                "mode": "the host waits for every step's result before the next step"}
+    del lens_b
+    for w in layers:
+        err = w.layer.device_error()
+        if err:
+            raise SystemExit("device error word set: %d" % err)
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline:
+        del layers, qs, news, imps, out_all, outs, ws, pinned, stage, views, stages
+        torch.cuda.empty_cache()
+        single, multi, w1, wn = ragged_samples(args.cpu_sample_seqs, args.ragged_seqs)
+        cpu = cpu_baseline_gqa(single, multi, args.cpu_seconds, w1, wn)
+    line = {
+        "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": "ragged", "n_seq": n_seq, "lengths": "U{1..16384}, seed 7 (mean %.0f at the start)"
+                   % float(np.mean(synthetic_lengths(n_seq))),
+                   "n_q": n_q, "n_kv": n_kv, "head_dim": hd,
+                   "layers": "f32, q8 (q8_2f), q8k, q8v; 2 of 8 KV heads dead per layer",
+                   "step": "per layer: kv_append 1 row/seq + decode_attention with imp",
+                   "arithmetic": "f32 CUDA-core dots (f32, q8k, q8v layers); q8 layer: int8 codes exact in f16, "
+                                 "query and weights split into two f16 terms each, mma.sync, f32 accumulate",
+                   "l2": "inputs larger than L2 (%.1f GB read per step)" % (bytes_total / args.steps / 1e9),
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "fraction_of_peak": round(gbs / world / peak, 4),
+        "queries_per_s": round(n_seq * world / (ms_per_step * 1e-3), 1),
+        "roofline": {"bound": "hbm", "kernel": "decode_attention over the four layers (imp off; per mode below)",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4),
+                     "traffic": int(sum(tr)) if all(t is not None for t in tr) else None,
+                     "peak_kind": peak_kind, "ms_per_launch": round(sum(k_ms), 5),
+                     "bytes_per_launch": int(sum(k_bytes))},
+        "per_mode": per_mode,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "e2e_sync": e2e_sync,
+        "gpu_launches": args.steps * 16,
+        "clocks": sampler.summary(c0, c1),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def synthetic_lengths(n_seq):
+    import synthetic
+
+    return synthetic.ragged_batch(n_seq)[0]
+
+
 def build_workload(name: str, replicas: int):
     from kv_cache_decode_attention_gb300 import workloads as W
 
@@ -761,7 +1184,7 @@ def run_gpu(args, rank, world):
     probe = build_workload(args.workload, 1)
     wl0 = probe[0]
     n_live = int(wl0.alive.sum())
-    ws_bytes_each = W.decode_bytes(wl0.mode, n_live, wl0.hd, wl0.n_q, wl0.lengths, True, wl0.n_seq)
+    ws_bytes_each = decode_bytes(wl0.mode, n_live, wl0.hd, wl0.n_q, wl0.lengths, True, wl0.n_seq)
     R = max(1, min(8, math.ceil(4 * L2_BYTES / ws_bytes_each)))
     wls = probe + build_workload(args.workload, R - 1)
     n_steps = args.warmup + args.steps
@@ -826,9 +1249,9 @@ def run_gpu(args, rank, world):
     for j in range(args.steps):
         r = (args.warmup + j) % R
         w = wls[r]
-        bytes_total += W.append_bytes(w.mode, n_live, w.hd, w.n_seq)
+        bytes_total += append_bytes(w.mode, n_live, w.hd, w.n_seq)
         lens[r] += 1
-        bytes_total += W.decode_bytes(w.mode, n_live, w.hd, w.n_q, lens[r], True, w.n_seq)
+        bytes_total += decode_bytes(w.mode, n_live, w.hd, w.n_q, lens[r], True, w.n_seq)
     # the decode's share of a step, from steps run again with events around it
     # (kept out of the timed steps above)
     for j in range(n_ev):
@@ -855,7 +1278,7 @@ def run_gpu(args, rank, world):
     k_ms = statistics.mean(a.elapsed_time(b) for a, b in dev_ev)
     lens_now = lengths_now()
     kbytes = statistics.mean(
-        W.decode_bytes(wls[j % R].mode, n_live, wl0.hd, wl0.n_q, lens_now[j % R], False, wl0.n_seq)
+        decode_bytes(wls[j % R].mode, n_live, wl0.hd, wl0.n_q, lens_now[j % R], False, wl0.n_seq)
         for j in range(nrep))
     peak, peak_kind = peaks()
     achieved = kbytes / (k_ms * 1e-3) / 1e9
@@ -878,8 +1301,8 @@ def run_gpu(args, rank, world):
             r = (first + j) % R
             w = wls[r]
             lens_e[r] += 1
-            eb += W.append_bytes(w.mode, n_live, w.hd, w.n_seq)
-            eb += W.decode_bytes(w.mode, n_live, w.hd, w.n_q, lens_e[r], True, w.n_seq)
+            eb += append_bytes(w.mode, n_live, w.hd, w.n_seq)
+            eb += decode_bytes(w.mode, n_live, w.hd, w.n_q, lens_e[r], True, w.n_seq)
         return eb
 
     def e2e_step(j, views, last_copy):
@@ -921,11 +1344,9 @@ def run_gpu(args, rank, world):
     if rank != 0:
         return
     cpu = None
-    if not args.no_cpu_baseline and world >= 1:
-        v, per, nb = oracle_sample_gbs(wl0, 1, args.cpu_seconds)
-        cpu = {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": "1 of %d sequences (all %d query heads x %d rows) decoded in f64, "
-                         "%.1f s" % (wl0.n_seq, wl0.n_q, int(wl0.lengths[0]), args.cpu_seconds)}
+    if not args.no_cpu_baseline:
+        single, multi, w1, wn = gqa_samples(wl0.name, args.cpu_sample_seqs)
+        cpu = cpu_baseline_gqa(single, multi, args.cpu_seconds, w1, wn)
     clocks = sampler.summary(c0, c1)
     line = {
         "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world,
@@ -960,9 +1381,15 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", default="q8_gqa",
-                    choices=["q8_gqa", "long_q8", "tiny_f32", "verify_q8", *RSWA_WORKLOADS])
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--workload", default="ragged",
+                    choices=["ragged", "q8_gqa", "long_q8", "tiny_f32", "verify_q8", *RSWA_WORKLOADS])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="seconds of oracle decoding for the CPU baseline (half on one core, half on all)")
+    ap.add_argument("--cpu-sample-seqs", type=int, default=16,
+                    help="sequences (streams) in the all-core CPU baseline sample")
+    ap.add_argument("--ragged-seqs", type=int, default=256,
+                    help="sequences of the ragged batch (256 = the measured configuration; fewer keeps "
+                         "the first ones, for small profiler captures)")
     ap.add_argument("--rswa-streams", type=int, default=16,
                     help="streams of the R-SWA workloads (16 = the measured configuration)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -983,11 +1410,17 @@ def main():
 
     if args.impl == "reference":
         if rank == 0:
-            build()
+            from oracle.oracle import build_oracle
+
+            build_oracle()
+            if args.workload in RSWA_WORKLOADS:
+                build()
         run_reference(args, rank)
         return
     build()
-    if args.workload in RSWA_WORKLOADS:
+    if args.workload == "ragged":
+        run_gpu_ragged(args, rank, world)
+    elif args.workload in RSWA_WORKLOADS:
         run_gpu_rswa(args, rank, world)
     elif args.workload == "verify_q8":
         run_gpu_verify(args, rank, world)

@@ -31,7 +31,6 @@ import synthetic
 
 from . import api
 
-SEED_OFFSETS = {"k": 101, "v": 202, "sk": 303, "sv": 404, "q": 505}
 
 
 @dataclass
@@ -59,8 +58,7 @@ class GqaWorkload:
         return seq_rows(self.seed, b, int(self.lengths[b]), self.n_kv, self.hd, self.outliers, device)
 
     def query(self, step: int, device="cuda"):
-        return synthetic.torch_normal((self.n_seq, self.n_q, self.hd),
-                                      self.seed * 7919 + SEED_OFFSETS["q"] + step, device)
+        return synthetic.gqa_query(self.seed, step, self.n_seq, self.n_q, self.hd, device)
 
     def new_rows(self, step: int, device="cuda"):
         """One appended row per sequence for decode step `step`: [n_seq, n_kv, hd]."""
@@ -71,13 +69,7 @@ class GqaWorkload:
 
 
 def seq_rows(seed: int, b: int, L: int, n_kv: int, hd: int, outliers: bool, device="cuda"):
-    base = seed * 1_000_003 + b * 9973
-    k = synthetic.torch_normal((L, n_kv, hd), base + SEED_OFFSETS["k"], device)
-    v = synthetic.torch_normal((L, n_kv, hd), base + SEED_OFFSETS["v"], device)
-    if outliers:
-        k *= synthetic.torch_channel_sigma((n_kv, hd), base + SEED_OFFSETS["sk"], device)
-        v *= synthetic.torch_channel_sigma((n_kv, hd), base + SEED_OFFSETS["sv"], device)
-    return k, v
+    return synthetic.gqa_seq_rows(seed, b, L, n_kv, hd, outliers, device)
 
 
 def _build_gqa(name, mode, n_seq, n_q, n_kv, hd, lengths, alive, seed, outliers, stepwise,
@@ -116,31 +108,38 @@ def _build_gqa(name, mode, n_seq, n_q, n_kv, hd, lengths, alive, seed, outliers,
     return wl
 
 
-def tiny_f32(device="cuda"):
-    return _build_gqa("tiny_f32", api.F32, 1, 4, 2, 64, [256], np.ones(2, np.uint8), 0,
-                      outliers=False, stepwise=False, extra_cap=64, device=device)
+def _fixed(name, device, extra_cap):
+    w = synthetic.GQA_WORKLOADS[name]
+    return _build_gqa(name, api.MODE_NAMES[w["mode"]], w["n_seq"], w["n_q"], w["n_kv"], w["hd"],
+                      [w["rows"]] * w["n_seq"], np.ones(w["n_kv"], np.uint8), w["seed"],
+                      outliers=w["outliers"], stepwise=w["stepwise"], extra_cap=extra_cap, device=device)
+
+
+def tiny_f32(device="cuda", extra_cap=64):
+    return _fixed("tiny_f32", device, extra_cap)
 
 
 def q8_gqa(device="cuda", extra_cap=512):
-    return _build_gqa("q8_gqa", api.Q8, 32, 32, 8, 128, [4096] * 32, np.ones(8, np.uint8), 2,
-                      outliers=True, stepwise=True, extra_cap=extra_cap, device=device)
+    return _fixed("q8_gqa", device, extra_cap)
 
 
 def long_q8(device="cuda", extra_cap=512):
-    return _build_gqa("long_q8", api.Q8, 4, 64, 4, 128, [131072] * 4, np.ones(4, np.uint8), 4,
-                      outliers=True, stepwise=False, extra_cap=extra_cap, device=device)
+    return _fixed("long_q8", device, extra_cap)
 
 
 RAGGED_MODES = (api.F32, api.Q8, api.Q8K, api.Q8V)
 
 
-def ragged(device="cuda", extra_cap=64, modes=RAGGED_MODES):
-    lengths = synthetic.ragged_lengths(256, 1, 16384, 7)
+def ragged(device="cuda", extra_cap=64, modes=RAGGED_MODES, n_seq=256):
+    """The ragged serving batch: one layer per storage mode over the same 256
+    sequence lengths (n_seq < 256 keeps the first n_seq of them, a smaller
+    batch of the same length mix)."""
+    lengths, specs = synthetic.ragged_batch(n_seq)
     out = []
-    for li, mode in enumerate(modes):
-        alive = synthetic.dead_mask(8, 2, 7 * 100 + li)
-        out.append(_build_gqa("ragged_%s" % ["f32", "q8", "q8k", "q8v"][mode], mode, 256, 32, 8, 128,
-                              lengths, alive, 70 + li, outliers=True, stepwise=False,
+    for mode in modes:
+        name, alive, seed = specs[mode]
+        out.append(_build_gqa("ragged_%s" % name, mode, n_seq, 32, 8, 128,
+                              lengths, alive, seed, outliers=True, stepwise=False,
                               extra_cap=extra_cap, device=device))
     return out
 
@@ -183,46 +182,3 @@ def rswa_steady(device="cuda", B=16, prefill=32640, steps=500, seed=3, int8=Fals
         api.rswa_ring_write(cache, k, v)
     torch.cuda.synchronize()
     return wl
-
-
-# ---------------------------------------------------------------- byte counts
-
-def kv_bytes_per_row(mode: int, hd: int) -> int:
-    """Stored bytes per cached row per live KV head (K and V with their scales)."""
-    qk = mode in (api.Q8, api.Q8K)
-    qv = mode in (api.Q8, api.Q8V)
-    kb = hd + 4 * (hd // 32) if qk else 4 * hd
-    vb = hd + 4 if qv else 4 * hd
-    return kb + vb
-
-
-def decode_bytes(mode, n_live, hd, n_q, lengths, with_imp, n_seq) -> int:
-    """Algorithmic bytes of one decode call: every live row's K/V (+ scales) once,
-    the query and output, the fields of the quantised components, and imp
-    read + write when it is requested."""
-    rows = int(np.sum(lengths)) * n_live
-    b = rows * kv_bytes_per_row(mode, hd)
-    b += 2 * n_seq * n_q * hd * 4
-    nf = (1 if mode in (api.Q8, api.Q8K) else 0) + (1 if mode in (api.Q8, api.Q8V) else 0)
-    b += nf * n_seq * n_live * hd * 4
-    if with_imp:
-        b += 8 * int(np.sum(lengths))
-    return b
-
-
-def append_bytes(mode, n_live, hd, n_seq) -> int:
-    """Algorithmic bytes of appending one row per sequence: f32 K, V in for the
-    live heads, stored codes/scales (or f32 rows) out, fields read."""
-    b = n_seq * n_live * (8 * hd + kv_bytes_per_row(mode, hd))
-    nf = (1 if mode in (api.Q8, api.Q8K) else 0) + (1 if mode in (api.Q8, api.Q8V) else 0)
-    return b + nf * n_seq * n_live * hd * 4
-
-
-def rswa_bytes(B, H, hd, lengths) -> int:
-    return int(np.sum(lengths)) * H * hd * 8 + 2 * B * H * hd * 4
-
-
-def rswa_i8_bytes(B, H, hd, lengths) -> int:
-    """Algorithmic bytes of one int8-mirror decode: every row's K and V codes and
-    their two row scales, plus the f32 query and output."""
-    return int(np.sum(lengths)) * H * (2 * hd + 8) + 2 * B * H * hd * 4

@@ -19,6 +19,7 @@ from .oracle import (  # noqa: F401
     K_GROUP,
     OracleSeqCache,
     build_oracle,
+    decode_many,
     lib,
     quant_row,
     quantize_row_i8,

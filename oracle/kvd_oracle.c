@@ -40,6 +40,9 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #define KVO_COL_WARMUP 64 /* cortiq KV_COL_WARMUP */
 #define KVO_K_GROUP 32    /* cortiq KV_K_GROUP */
@@ -357,6 +360,62 @@ int kvo_attend_group(const kvo_cache *c, const float *q_group, int kv_head, int 
     }
     free(probs);
     return n;
+}
+
+/* The decode of many sequences at once, for timing the oracle on every host
+ * core: the (sequence, query head) pairs are independent, so they are shared
+ * among `threads` OpenMP threads (0 = the runtime's default).  Each pair runs
+ * exactly the serial code above -- kvo_attend_group for one head -- with its
+ * probabilities kept in a buffer of its own; the per-row masses are then
+ * added into imp[i] sequence by sequence in ascending head order, the order
+ * the serial group loop adds them, so the result is bitwise the serial one
+ * whatever the thread count.  caches[i], qs[i] ([n_q][hd] f32) and outs[i]
+ * ([n_q][hd] f64) describe sequence i; imps (NULL, or NULL entries) skips imp.
+ * Returns the number of threads that ran, or -1 if a buffer could not be
+ * allocated (nothing is written then). */
+int kvo_decode_many(const kvo_cache *const *caches, int n_seq, const float *const *qs, int n_q,
+                    float scale, double *const *outs, double *const *imps, int threads)
+{
+    long long n_pairs = (long long)n_seq * n_q;
+    double **probs = (double **)calloc((size_t)(n_pairs > 0 ? n_pairs : 1), sizeof(double *));
+    if (!probs) return -1;
+    int fail = 0;
+    for (long long t = 0; t < n_pairs && !fail; ++t) {
+        int i = (int)(t / n_q);
+        if (imps && imps[i]) {
+            probs[t] = (double *)calloc((size_t)(caches[i]->cap > 0 ? caches[i]->cap : 1), sizeof(double));
+            if (!probs[t]) fail = 1;
+        }
+    }
+    int used = 1;
+    if (!fail) {
+#ifdef _OPENMP
+        if (threads <= 0) threads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(threads)
+#endif
+        for (long long t = 0; t < n_pairs; ++t) {
+            int i = (int)(t / n_q), h = (int)(t % n_q);
+            const kvo_cache *c = caches[i];
+            int hpk = n_q / c->n_kv;
+            kvo_attend_group(c, qs[i] + (size_t)h * c->hd, h / hpk, 1, scale,
+                             outs[i] + (size_t)h * c->hd, probs[t]);
+#ifdef _OPENMP
+            if (t == 0) used = omp_get_num_threads();
+#endif
+        }
+        for (int i = 0; i < n_seq && imps; ++i) {
+            if (!imps[i]) continue;
+            for (int h = 0; h < n_q; ++h) {
+                const kvo_cache *c = caches[i];
+                int n = c->head_rows[h / (n_q / c->n_kv)];
+                const double *pr = probs[(long long)i * n_q + h];
+                for (int p = 0; p < n; ++p) imps[i][p] += pr[p];
+            }
+        }
+    }
+    for (long long t = 0; t < n_pairs; ++t) free(probs[t]);
+    free(probs);
+    return fail ? -1 : used;
 }
 
 /* cortiq attend_group_upto with its four options, in f64:

@@ -31,7 +31,10 @@ def build_oracle(force: bool = False) -> str:
             "gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
             "-fPIC", "-shared", "-o", tmp, _SRC, "-lm",
         ]
-        subprocess.run(cmd, check=True)
+        # OpenMP only shares the multi-sequence decode's (sequence, head) pairs
+        # among threads; without it the same code runs on one thread
+        if subprocess.run(cmd[:1] + ["-fopenmp"] + cmd[1:], capture_output=True).returncode != 0:
+            subprocess.run(cmd, check=True)
         os.replace(tmp, _SO)
     return _SO
 
@@ -78,6 +81,7 @@ def lib():
                                           i32, i32, f32, vp]
             L.kvo_rswa_decode_i8.argtypes = [i32, i32, vp, vp, vp, vp, vp, C.c_longlong, i32, vp, vp,
                                              vp, vp, i32, i32, f32, vp]
+            L.kvo_decode_many.argtypes = [vp, i32, vp, i32, f32, vp, vp, i32]
             L.kvo_online_head.argtypes = [i32, i32, vp, vp, vp, f32, vp]
             L.kvo_online_head.restype = None
             _lib = L
@@ -287,6 +291,30 @@ class OracleSeqCache:
         if n < 0:
             raise ValueError("evict_born: negative argument")
         return n
+
+
+def decode_many(caches, qs, n_q: int, scale, imps=None, threads: int = 0):
+    """Decode of several sequences at once (kvo_decode_many): the (sequence,
+    query head) pairs shared among `threads` OpenMP threads (0 = every core the
+    runtime sees), bitwise equal to calling OracleSeqCache.decode on each.
+    caches: OracleSeqCache list; qs: [n_q, hd] f32 each; imps: None or an f64
+    array per sequence (accumulated).  Returns (outputs [n_q, hd] f64 list,
+    threads used)."""
+    n = len(caches)
+    qs = [np.ascontiguousarray(q, dtype=np.float32).reshape(n_q, c.hd) for q, c in zip(qs, caches)]
+    outs = [np.zeros((n_q, c.hd), np.float64) for c in caches]
+    cp = (C.c_void_p * n)(*[C.addressof(c._s) for c in caches])
+    qp = (C.c_void_p * n)(*[q.ctypes.data for q in qs])
+    op = (C.c_void_p * n)(*[o.ctypes.data for o in outs])
+    ip = None
+    if imps is not None:
+        for a in imps:
+            assert a is None or (a.dtype == np.float64 and a.flags.c_contiguous)
+        ip = (C.c_void_p * n)(*[None if a is None else a.ctypes.data for a in imps])
+    used = lib().kvo_decode_many(cp, n, qp, int(n_q), float(scale), op, ip, int(threads))
+    if used < 0:
+        raise MemoryError("oracle decode_many: allocation failed")
+    return outs, int(used)
 
 
 def rswa_write(ring_k, ring_v, k, v, prefill_recorded: bool, cursors):

@@ -77,3 +77,55 @@ def torch_channel_sigma(shape, seed: int, device):
     u = torch.rand(shape, generator=g, device=device, dtype=torch.float64)
     lo, hi = np.log(SIGMA_LO), np.log(SIGMA_HI)
     return torch.exp(lo + (hi - lo) * u).to(torch.float32)
+
+
+# ---- the benchmark workloads' per-sequence recipes -----------------------
+# (seeds and shapes only; the library's workload builders and the oracle's
+# CPU baseline both draw a workload's rows from these, on the device or on
+# the host: torch's CPU and CUDA generators give different draws of the same
+# distribution)
+
+SEED_OFFSETS = {"k": 101, "v": 202, "sk": 303, "sv": 404, "q": 505}
+
+
+def gqa_seq_rows(seed: int, b: int, L: int, n_kv: int, hd: int, outliers: bool, device="cuda"):
+    """(K, V) rows [L, n_kv, hd] f32 of sequence b of a GQA workload: N(0,1),
+    times the per-(head, channel) log-uniform sigma with outlier channels."""
+    base = seed * 1_000_003 + b * 9973
+    k = torch_normal((L, n_kv, hd), base + SEED_OFFSETS["k"], device)
+    v = torch_normal((L, n_kv, hd), base + SEED_OFFSETS["v"], device)
+    if outliers:
+        k *= torch_channel_sigma((n_kv, hd), base + SEED_OFFSETS["sk"], device)
+        v *= torch_channel_sigma((n_kv, hd), base + SEED_OFFSETS["sv"], device)
+    return k, v
+
+
+def gqa_query(seed: int, step: int, n_seq: int, n_q: int, hd: int, device="cuda"):
+    """The queries [n_seq, n_q, hd] of decode step `step` of a GQA workload."""
+    return torch_normal((n_seq, n_q, hd), seed * 7919 + SEED_OFFSETS["q"] + step, device)
+
+
+RAGGED_MODE_NAMES = ("f32", "q8", "q8k", "q8v")
+
+
+def ragged_batch(n_seq: int = 256):
+    """The ragged serving batch: 256 lengths U{1..16384} (seed 7; n_seq < 256
+    keeps the first n_seq), 32 query / 8 KV heads, head_dim 128, and one layer
+    per storage mode (f32, q8, q8k, q8v) with 2 of its 8 KV heads dead and its
+    own row seed.  Returns (lengths, [(mode name, alive mask, row seed)])."""
+    lengths = ragged_lengths(256, 1, 16384, 7)[:n_seq]
+    layers = [(name, dead_mask(8, 2, 7 * 100 + li), 70 + li) for li, name in enumerate(RAGGED_MODE_NAMES)]
+    return lengths, layers
+
+
+# The fixed-length GQA workloads: storage mode, sequences, query / KV heads,
+# head_dim, rows per sequence, row seed, outlier channels, and whether the
+# benchmark builds the cache one row at a time (else in bulk appends).
+GQA_WORKLOADS = {
+    "tiny_f32": dict(mode="f32", n_seq=1, n_q=4, n_kv=2, hd=64, rows=256, seed=0, outliers=False,
+                     stepwise=False),
+    "q8_gqa": dict(mode="q8", n_seq=32, n_q=32, n_kv=8, hd=128, rows=4096, seed=2, outliers=True,
+                   stepwise=True),
+    "long_q8": dict(mode="q8", n_seq=4, n_q=64, n_kv=4, hd=128, rows=131072, seed=4, outliers=True,
+                    stepwise=False),
+}

@@ -128,10 +128,71 @@ def test_q8_gqa_full_size(env):
 
 
 def test_long_q8_full_size(env):
-    """4 seq x 131072 rows, 64 Q / 4 KV heads (16 per group): one sampled group."""
+    """4 seq x 131072 rows, 64 Q / 4 KV heads (16 per group), the benchmark's
+    decode with imp (split_h16_kernel with the score stores + imp_kernel):
+    sequences 1 and 2 in full (every group, imp per element over all 131072
+    rows), sequences 0 and 3 on one group each."""
     torch, kvd, W = env
     wl = W.long_q8(extra_cap=64)
-    _decode_and_check(torch, kvd, wl, samples=[2], heads_per_sample=[1], with_imp=False)
+    q = wl.query(0)
+    imp = torch.zeros(wl.layer.imp_len, device="cuda")
+    ws = torch.empty(wl.layer.workspace_bytes(wl.n_q, True), dtype=torch.uint8, device="cuda")
+    out = kvd.decode_attention(q, wl.layer, imp=imp, scale=wl.scale, workspace=ws)
+    torch.cuda.synchronize()
+    assert wl.layer.device_error() == 0
+    out, qh, got_imp = out.cpu().numpy(), q.cpu().numpy(), imp.cpu().numpy()
+    full = [_oracle_seq(wl, b)[0] for b in (1, 2)]
+    imps = [np.zeros(oc.cap) for oc in full]
+    refs, _ = oracle.decode_many(full, [qh[1], qh[2]], wl.n_q, np.float32(wl.scale), imps)
+    L = int(wl.lengths[0])
+    for b, ref, imp_ref, oc in zip((1, 2), refs, imps, full):
+        _check_storage(kvd, wl, b, oc, None)
+        err = out_error(out[b], ref)
+        assert err <= OUT_TOL, (b, err)
+        ib = int(wl.layer.imp_base[b])
+        assert_imp_close(got_imp[ib:ib + L], imp_ref[:L])
+        assert abs(imp_ref[:L].sum() - wl.n_q) < 1e-6 * wl.n_q
+    for b, g in ((0, 3), (3, 0)):
+        oc, hs = _oracle_seq(wl, b, [g])
+        ref = oc.decode(qh[b, g * wl.hpk:(g + 1) * wl.hpk], wl.hpk, np.float32(wl.scale))
+        err = out_error(out[b, g * wl.hpk:(g + 1) * wl.hpk], ref)
+        assert err <= OUT_TOL, (b, g, err)
+    del wl
+    torch.cuda.empty_cache()
+
+
+def test_verify_q8_full_size(env):
+    """The benchmark's speculative step on q8_gqa (32 seq x 4096 rows): 4 draft
+    rows appended per sequence, one query-batched verify (16 query rows per
+    group on split_h16_kernel), three sampled sequences against the oracle's
+    decode_verify, then kv_truncate_last of the 4 drafts and a plain decode
+    that matches the cache without them."""
+    torch, kvd, W = env
+    import synthetic
+
+    K = 4
+    wl = W.q8_gqa(extra_cap=64)
+    n_seq, n_q, n_kv, hd = wl.n_seq, wl.n_q, wl.n_kv, wl.hd
+    dk = synthetic.normal((n_seq, K, n_kv, hd), 81_000)
+    dv = synthetic.normal((n_seq, K, n_kv, hd), 82_000)
+    vq = synthetic.normal((n_seq, K, n_q, hd), 80_000)
+    kvd.kv_append(wl.layer, torch.from_numpy(dk.reshape(-1, n_kv, hd)).cuda(),
+                  torch.from_numpy(dv.reshape(-1, n_kv, hd)).cuda(), np.full(n_seq, K, np.int32))
+    out = kvd.decode_attention_verify(torch.from_numpy(vq).cuda(), wl.layer, K, scale=wl.scale).cpu().numpy()
+    assert wl.layer.device_error() == 0
+    samples = (0, 13, 31)
+    for b in samples:
+        oc_full = oracle.OracleSeqCache(wl.mode, n_kv, hd, int(wl.lengths[b]) + K, alive=wl.alive)
+        k, v = wl.rows(b)
+        oc_full.append_rows(k.cpu().numpy(), v.cpu().numpy())
+        oc_full.append_rows(dk[b], dv[b])
+        ref = oc_full.decode_verify(vq[b], n_q, K, np.float32(wl.scale))
+        for i in range(K):
+            err = out_error(out[b, i], ref[i])
+            assert err <= OUT_TOL, (b, i, err)
+    kvd.kv_truncate_last(wl.layer, K)
+    assert all(wl.layer.seq_len(b) == int(wl.lengths[b]) for b in range(n_seq))
+    _decode_and_check(torch, kvd, wl, samples=[13], with_imp=True)
     del wl
     torch.cuda.empty_cache()
 

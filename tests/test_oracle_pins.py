@@ -359,6 +359,37 @@ def test_grouped_equals_per_head_bitwise():
             assert np.array_equal(imp, imp_ref)
 
 
+def test_parallel_decode_is_bitwise_the_serial_decode():
+    """[rswa] test parallel_heads_are_bit_identical_to_serial, for the oracle's
+    multi-sequence driver: the (sequence, head) pairs shared among threads give
+    the serial decode's outputs and imp bit for bit, with dead groups, an empty
+    sequence and every storage mode, at 1 and several threads."""
+    hd, n_kv, hpk = 32, 4, 3
+    lengths = [70, 0, 1, 130]
+    alive = [1, 0, 1, 1]
+    for mode in (oracle.F32, oracle.Q8, oracle.Q8K, oracle.Q8V):
+        caches = []
+        for b, L in enumerate(lengths):
+            c = oracle.OracleSeqCache(mode, n_kv, hd, max(L, 1), alive=alive)
+            c.append_rows(synthetic.normal((L, n_kv, hd), 80 + b), synthetic.normal((L, n_kv, hd), 90 + b))
+            caches.append(c)
+        qs = [synthetic.normal((n_kv * hpk, hd), 100 + b) for b in range(len(lengths))]
+        ref_out, ref_imp = [], []
+        for c, q in zip(caches, qs):
+            imp = np.full(c.cap, 0.5)
+            ref_out.append(c.decode(q, n_kv * hpk, f32(0.2), imp))
+            ref_imp.append(imp)
+        for threads in (1, 3, 0):
+            imps = [np.full(c.cap, 0.5) for c in caches]
+            outs, used = oracle.decode_many(caches, qs, n_kv * hpk, f32(0.2), imps, threads)
+            assert used >= 1
+            for b in range(len(lengths)):
+                assert np.array_equal(outs[b], ref_out[b]), (mode, threads, b)
+                assert np.array_equal(imps[b], ref_imp[b]), (mode, threads, b)
+            outs, _ = oracle.decode_many(caches, qs, n_kv * hpk, f32(0.2), None, threads)
+            assert all(np.array_equal(o, r) for o, r in zip(outs, ref_out))
+
+
 def test_closed_forms_single_key_and_equal_scores():
     """1 key -> its V; equal scores -> the mean of the V rows (for any query)."""
     c = oracle.OracleSeqCache(oracle.F32, 1, 16, 4)
