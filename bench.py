@@ -54,34 +54,52 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
 
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one decode call
-# without imp -- the split kernel plus the run merge -- from one ncu capture of
-# this benchmark's roofline loop (command and figures in
-# profiles/decode_q8_gqa_traffic.md), valid while the kernel sources hash to
-# the captured version; reported as null otherwise.  The capture ran 25 steps
-# (cache rows 4096 + 25); a run of another length reports it scaled by its
-# algorithmic bytes over the capture's (both are rows x bytes per row plus a
-# small fixed part).
+# without imp -- the split kernel plus its merge -- from one ncu capture of
+# this benchmark's own decode calls (the capture's command and figures are
+# kept with the profiles), valid while the sources the call compiles from hash
+# to the captured version, null otherwise.  The capture may run a smaller case
+# of the same workload (fewer steps, or the first sequences of the ragged
+# batch); a run reports it scaled by its algorithmic bytes over the capture's
+# (both are rows x bytes per row plus a small fixed part).
+CSRC_COMMON = ("kvd_internal.cuh", "kvd_decode.cu")
+CSRC_CUDA_CORE = CSRC_COMMON + ("kvd_decode_kernels.cuh", "kvd_split_f32.cu", "kvd_split_q8k.cu",
+                                "kvd_split_q8v.cu")
+CSRC_TC = CSRC_COMMON + ("kvd_split_mma.cuh", "kvd_split_h16.cuh", "kvd_split_q8.cu")
 TRAFFIC = {
-    "q8_gqa": {"sources_sha256": "813bda5fa871babc27a6d8f99409a7ac294be15c3a90ad55523a3c5f51eb5034",
+    "q8_gqa": {"files": None, "sources_sha256": "813bda5fa871babc27a6d8f99409a7ac294be15c3a90ad55523a3c5f51eb5034",
                "bytes": 300582016, "algorithmic_bytes": 291600896},
+    # the first 16 sequences of the ragged batch, 3 + 3 steps in, mean of 10 calls
+    "ragged_f32": {"files": CSRC_CUDA_CORE,
+                   "sources_sha256": "b99d56bbae086aa8c688ef9de3b003900223726775ca6005098e62e525aa5a1c",
+                   "bytes": 944687436, "algorithmic_bytes": 939376640},
+    "ragged_q8": {"files": CSRC_TC,
+                  "sources_sha256": "e9cb89721ca7cdcccbe7a46cc4c54596019ef1596f8a7ac25c48dfbf64398b9e",
+                  "bytes": 259252633, "algorithmic_bytes": 253672640},
+    "ragged_q8k": {"files": CSRC_CUDA_CORE,
+                   "sources_sha256": "b99d56bbae086aa8c688ef9de3b003900223726775ca6005098e62e525aa5a1c",
+                   "bytes": 606965145, "algorithmic_bytes": 602025728},
+    "ragged_q8v": {"files": CSRC_CUDA_CORE,
+                   "sources_sha256": "b99d56bbae086aa8c688ef9de3b003900223726775ca6005098e62e525aa5a1c",
+                   "bytes": 596030105, "algorithmic_bytes": 591023552},
 }
 
 
-def kernel_sources_sha256() -> str:
+def kernel_sources_sha256(files=None) -> str:
+    """sha256 over the named csrc files (every .cu / .cuh when None)."""
     import hashlib
 
     csrc = os.path.join(ROOT, "kv_cache_decode_attention_gb300", "csrc")
+    names = sorted(files) if files else sorted(n for n in os.listdir(csrc) if n.endswith((".cu", ".cuh")))
     h = hashlib.sha256()
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in names:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()
 
 
 def measured_traffic(workload: str, bytes_per_launch=None):
     t = TRAFFIC.get(workload)
-    if not t or t["bytes"] is None or t["sources_sha256"] != kernel_sources_sha256():
+    if not t or t["bytes"] is None or t["sources_sha256"] != kernel_sources_sha256(t["files"]):
         return None
     if bytes_per_launch is None:
         return t["bytes"]
