@@ -1135,13 +1135,11 @@ extern "C" kvd_status decode_attention_verify(const float *q, const kvd_layer *L
     ms.vcol = static_cast<const float *>(l->buf[KVD_BUF_VCOL]);
     ms.n_live = l->n_live;
     if (warp_path(l)) {
-        // q8_2f at head_dim 128: the K * hg query rows of a group are the rows
-        // of the tcgen05 kernel's weight matrices (or the M rows of the 16-head
-        // mma.sync kernel without the 128-row tensor maps), one read of every tile
-        const int vv = l->have_tmap128 ? 5 : 2;
+        // q8_2f at head_dim 128: the K * hg query rows of a group are the M rows
+        // of the tensor-core kernel (heads in M), one read of every tile
         int64_t T = 0;
         for (int b = 0; b < l->n_seq; ++b) T += int64_t(l->n_live) * tiles_of(l->h_seq_len[b], window, K);
-        const int64_t workers = split_q8_tc_workers(vv);
+        const int64_t workers = split_q8_tc_workers(2);
         if (workers <= 0) return KVD_ECUDA;
         WarpArgs wa;
         wa.a = a;
@@ -1151,9 +1149,9 @@ extern "C" kvd_status decode_attention_verify(const float *q, const kvd_layer *L
         wa.unit_slots = reinterpret_cast<int64_t *>(ws + w.units);
         if (T > 0) {
             MmaMaps maps;
-            std::memcpy(&maps.kq, vv == 5 ? l->tmap_kq128 : l->tmap_kq, sizeof(maps.kq));
-            std::memcpy(&maps.vq, vv == 5 ? l->tmap_vq128 : l->tmap_vq, sizeof(maps.vq));
-            if (split_layer_q8_tc(vv, wa, s, maps, st) != cudaSuccess) return KVD_ECUDA;
+            std::memcpy(&maps.kq, l->tmap_kq, sizeof(maps.kq));
+            std::memcpy(&maps.vq, l->tmap_vq, sizeof(maps.vq));
+            if (split_layer_q8_tc(2, wa, s, maps, st) != cudaSuccess) return KVD_ECUDA;
         }
         RunMergeArgs rm;
         rm.pm = a.pm;

@@ -61,13 +61,10 @@ struct Layer {
     int32_t *d_seq_len, *d_frozen, *d_live, *d_slot;
     uint32_t *d_err;
     // TMA tensor maps (CUtensorMap, 128 bytes each) of the int8 K and V code
-    // buffers, 2-D [rows][head_dim] with 128-byte swizzled [32 x 128] boxes, and
-    // the same with [128 x 128] boxes (one per 128-row chunk of the 16-head
-    // kernel); have_tmap = 0 when they are not built (head_dim 64 or no int8
-    // buffer).
-    int32_t have_tmap_kq, have_tmap_vq, have_tmap128, pad1;
+    // buffers, 2-D [rows][head_dim] with 128-byte swizzled [32 x 128] boxes;
+    // have_tmap = 0 when they are not built (head_dim 64 or no int8 buffer).
+    int32_t have_tmap_kq, have_tmap_vq;
     unsigned char tmap_kq[128], tmap_vq[128];
-    unsigned char tmap_kq128[128], tmap_vq128[128];
 };
 static_assert(sizeof(Layer) <= sizeof(kvd_layer), "kvd_layer too small");
 constexpr int32_t kLayerMagic = 0x4b564431;  // "KVD1"
@@ -191,9 +188,9 @@ inline cudaError_t set_smem_once(const void *kern, int bytes) {
 }
 
 // TMA descriptor (128 bytes, written to out) of an int8 code buffer
-// [rows][hd]: boxes of box_rows rows x 128 bytes, 128-byte swizzle, rows past
-// the end read as zeros.  head_dim 128 only; false if the driver refuses it.
-bool encode_code_map(void *base, int64_t rows, int hd, unsigned char *out, uint32_t box_rows = 32);
+// [rows][hd]: boxes of 32 rows x 128 bytes, 128-byte swizzle, rows past the
+// end read as zeros.  head_dim 128 only; false if the driver refuses it.
+bool encode_code_map(void *base, int64_t rows, int hd, unsigned char *out);
 
 __device__ __forceinline__ void set_error(uint32_t *err, uint32_t bit) {
     if (err) atomicOr(err, bit);

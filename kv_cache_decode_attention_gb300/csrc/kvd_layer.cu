@@ -111,7 +111,7 @@ int64_t host_block_bytes(int32_t n_seq, int32_t n_kv) {
 // swizzle (16-byte chunk c of row r stored at chunk c ^ (r % 8)); rows past
 // the end read as zeros.  Returns false if the driver entry point is missing
 // or refuses the descriptor (the caller then uses the plain bulk-copy kernel).
-bool encode_code_map(void *base, int64_t rows, int hd, unsigned char *out, uint32_t box_rows) {
+bool encode_code_map(void *base, int64_t rows, int hd, unsigned char *out) {
     static std::once_flag once;
     static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     std::call_once(once, [] {
@@ -126,7 +126,7 @@ bool encode_code_map(void *base, int64_t rows, int hd, unsigned char *out, uint3
     alignas(64) CUtensorMap m;
     const cuuint64_t dims[2] = {cuuint64_t(hd), cuuint64_t(rows)};
     const cuuint64_t strides[1] = {cuuint64_t(hd)};
-    const cuuint32_t box[2] = {128u, box_rows};
+    const cuuint32_t box[2] = {128u, 32u};
     const cuuint32_t estr[2] = {1u, 1u};
     if (encode(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -285,10 +285,6 @@ extern "C" kvd_status kvd_layer_init(kvd_layer *L, int32_t n_seq, int32_t n_kv, 
         l.have_tmap_kq = encode_code_map(l.buf[KVD_BUF_KQ], code_rows, head_dim, l.tmap_kq) ? 1 : 0;
     if (l.buf[KVD_BUF_VQ])
         l.have_tmap_vq = encode_code_map(l.buf[KVD_BUF_VQ], code_rows, head_dim, l.tmap_vq) ? 1 : 0;
-    // 128-row boxes for the 16-head kernel's chunks
-    l.have_tmap128 = l.have_tmap_kq && l.have_tmap_vq &&
-                     encode_code_map(l.buf[KVD_BUF_KQ], code_rows, head_dim, l.tmap_kq128, 128) &&
-                     encode_code_map(l.buf[KVD_BUF_VQ], code_rows, head_dim, l.tmap_vq128, 128);
     std::memcpy(L, &l, sizeof(l));
     return KVD_OK;
 }

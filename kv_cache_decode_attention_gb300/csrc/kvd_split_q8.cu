@@ -5,7 +5,6 @@
 #include <mutex>
 
 #include "kvd_split_h16.cuh"
-#include "kvd_split_h16_tc.cuh"
 
 namespace kvd {
 
@@ -23,8 +22,7 @@ cudaError_t split_layer_q8(int hd, int hpk_bucket, const SplitArgs &a, const Lay
 // Tensor-core kernels for the q8_2f cache by query heads per group:
 // variant 0 = up to 4 (terms packed in the columns), 1 = up to 8 (heads in
 // the columns), 2 = up to 16 (heads in the MMA rows); 3 and 4 are 0 and 1
-// over the R-SWA int8 mirror (one K scale per row, int8 query codes); 5 = up
-// to 16 query rows on tcgen05 (accumulators in TMEM, 128-row chunks).
+// over the R-SWA int8 mirror (one K scale per row, int8 query codes).
 int q8_tc_variant(int hpk) { return hpk <= 4 ? 0 : hpk <= 8 ? 1 : 2; }
 
 cudaError_t split_layer_q8_tc(int variant, const WarpArgs &wa, const LayerSrc &s, const MmaMaps &maps,
@@ -35,7 +33,6 @@ cudaError_t split_layer_q8_tc(int variant, const WarpArgs &wa, const LayerSrc &s
         case 2: return launch_split_h16(wa, s, maps, st);
         case 3: return launch_split_warp_rowk<true>(wa, s, maps, st);
         case 4: return launch_split_warp_rowk<false>(wa, s, maps, st);
-        case 5: return launch_split_h16_tc(wa, s, maps, st);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -45,9 +42,9 @@ cudaError_t split_layer_q8_tc(int variant, const WarpArgs &wa, const LayerSrc &s
 int64_t split_q8_tc_workers(int variant) {
     constexpr int kMaxDev = 64;
     static std::mutex mu;
-    static int64_t cache[kMaxDev][6] = {};
+    static int64_t cache[kMaxDev][5] = {};
     int dev = 0;
-    if (variant < 0 || variant > 5 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+    if (variant < 0 || variant > 4 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
     std::lock_guard<std::mutex> lock(mu);
     int64_t &w = cache[dev][variant];
     if (w == 0) {
@@ -56,8 +53,7 @@ int64_t split_q8_tc_workers(int variant) {
             case 1: w = split_warp_workers<false>(); break;
             case 2: w = split_h16_workers(); break;
             case 3: w = split_warp_workers<true, true>(); break;
-            case 4: w = split_warp_workers<false, true>(); break;
-            default: w = split_h16_tc_workers(); break;
+            default: w = split_warp_workers<false, true>(); break;
         }
     }
     return w;
