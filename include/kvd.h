@@ -255,9 +255,12 @@ KVD_API kvd_status decode_attention_ex(const float *q, const kvd_layer *L, int32
  *   longest sequence divided by the rows per chunk the call picks (>= 256);
  *   a larger call returns KVD_ECAPACITY and launches nothing.
  *   The first call on each device looks up the array's device address (with
- *   that device current); make it before any stream capture.  Calls share
- *   the array: two calls whose kernels overlap on the GPU race and must be
- *   serialised by the caller. */
+ *   that device current) and keeps it with the id of the current context; a
+ *   call under another context (after a device reset, which unloads the
+ *   module and the array with it) looks it up again.  Make the first call on
+ *   a device, and the first after a reset, before any stream capture.  Calls
+ *   share the array and it keeps the last call's partials: two calls whose
+ *   kernels overlap on the GPU race and must be serialised by the caller. */
 KVD_API kvd_status decode_attention_static(const float *q, const kvd_layer *L, int32_t n_q,
                                            float scale, float *out, void *stream);
 

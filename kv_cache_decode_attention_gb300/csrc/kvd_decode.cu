@@ -23,28 +23,6 @@ int64_t split_q8_tc_workers(int);
 
 namespace {
 
-constexpr int kMinChunk = 256;           // rows; multiple of every tile height
-constexpr int kMaxChunk = 2048;          // rows; bounds one CTA's f32 accumulation chain
-constexpr int64_t kTargetCtas = 152 * 8; // about four waves of two CTAs per SM
-
-int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
-int64_t ceil_div(int64_t x, int64_t a) { return (x + a - 1) / a; }
-
-int hpk_bucket(int hpk) {
-    int b = 1;
-    while (b < hpk) b <<= 1;
-    return b;
-}
-
-// Rows per chunk: a multiple of kMinChunk, large enough that the grid holds
-// about kTargetCtas chunks, but at most kMaxChunk.  The cap keeps each CTA's
-// sequential f32 accumulation short (its rounding grows like the square root
-// of the rows summed, and long diffuse softmaxes shrink the output), at the
-// cost of more partials, which are ~0.2% of the bytes.
-int32_t pick_chunk(int64_t work_rows) {
-    const int64_t c = std::max<int64_t>(kMinChunk, ceil_div(work_rows, kTargetCtas));
-    return int32_t(std::min<int64_t>(kMaxChunk, round_up(c, kMinChunk)));
-}
 
 struct DecodeWs {
     int64_t pm, pl, pacc, ml, scores, units, total;  // byte offsets; total < 0 if unknown

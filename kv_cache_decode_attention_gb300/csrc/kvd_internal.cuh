@@ -27,6 +27,33 @@ constexpr uint32_t kErrTimeout = 1u;
 constexpr uint32_t kErrBounds = 2u;
 
 inline bool quant_k(int mode) { return mode == KVD_Q8 || mode == KVD_Q8K; }
+
+// ---- chunking of the CUDA-core split pass (shared by every entry point
+// that launches it, so their grids and partial layouts agree)
+constexpr int kMinChunk = 256;           // rows; multiple of every tile height
+constexpr int kMaxChunk = 2048;          // rows; bounds one CTA's f32 accumulation chain
+constexpr int64_t kTargetCtas = 152 * 8; // about four waves of two CTAs per SM
+
+inline int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+inline int64_t ceil_div(int64_t x, int64_t a) { return (x + a - 1) / a; }
+
+// Query heads per group rounded up to the instantiated kernels' bucket (1, 2, 4, 8, 16).
+inline int hpk_bucket(int hpk) {
+    int b = 1;
+    while (b < hpk) b <<= 1;
+    return b;
+}
+
+// Rows per chunk: a multiple of kMinChunk, large enough that the grid holds
+// about kTargetCtas chunks, but at most kMaxChunk.  The cap keeps each CTA's
+// sequential f32 accumulation short (its rounding grows like the square root
+// of the rows summed, and long diffuse softmaxes shrink the output), at the
+// cost of more partials, which are ~0.2% of the bytes.
+inline int32_t pick_chunk(int64_t work_rows) {
+    const int64_t c = ceil_div(work_rows, kTargetCtas);
+    const int64_t r = round_up(c > kMinChunk ? c : kMinChunk, kMinChunk);
+    return int32_t(r < kMaxChunk ? r : kMaxChunk);
+}
 inline bool quant_v(int mode) { return mode == KVD_Q8 || mode == KVD_Q8V; }
 
 // Device metadata block (KVD_BUF_META), laid out by layer_meta_layout().

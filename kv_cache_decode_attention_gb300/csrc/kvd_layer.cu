@@ -19,8 +19,6 @@ namespace kvd {
 
 namespace {
 
-int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
-
 struct Shape {
     int32_t n_seq, n_kv, hd, mode, n_live, ng;
     std::vector<int64_t> cap;  // rounded

@@ -14,8 +14,11 @@
 // library holds it until the process exits.  Host code may not use the
 // array's name as a device address (on the host it is only a stand-in), so
 // the first call on each device looks its device address up with
-// cudaGetSymbolAddress, with that device current, and keeps it.  Because that
-// first call does this set-up, it should come before any stream capture.
+// cudaGetSymbolAddress, with that device current, and keeps it together with
+// the id of the device's current context; a later call under another context
+// (the device was reset, which unloads the module) looks the address up
+// again.  Because the first call on a device (and the first after a reset)
+// does this set-up, it should come before any stream capture.
 // Every call shares the one array per device and leaves its contents behind;
 // the partials are fully rewritten before they are read, so nothing in it
 // must start at zero.  Two calls whose kernels overlap on the GPU (different
@@ -25,6 +28,8 @@
 #include <algorithm>
 #include <cmath>
 #include <mutex>
+
+#include <cuda.h>
 
 #include "kvd_decode_kernels.cuh"
 
@@ -45,27 +50,49 @@ __device__ __align__(256) char g_static_scratch[kStaticScratchBytes];
 
 std::mutex g_static_mu;
 void *g_static_ptr[kMaxDevices] = {};
+unsigned long long g_static_ctx[kMaxDevices] = {};
+
+// Id of the calling thread's current context (0 if the driver cannot tell).
+unsigned long long current_context_id() {
+    using GetCurrent = CUresult (*)(CUcontext *);
+    using GetId = CUresult (*)(CUcontext, unsigned long long *);
+    static std::once_flag once;
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    std::call_once(once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrent>(fn);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetId>(fn);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+        get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
 
 // Device address of the scratch array on the current device (looked up once
-// per device), or null if the lookup fails.
+// per device and context), or null if the lookup fails.
 void *static_scratch() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
     std::lock_guard<std::mutex> lock(g_static_mu);
-    if (g_static_ptr[dev] == nullptr) {
+    // (before the first lookup no context may be current yet: the lookup
+    // makes the device's primary context current, then its id is taken)
+    if (g_static_ptr[dev] == nullptr || g_static_ctx[dev] != current_context_id()) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) return nullptr;
         g_static_ptr[dev] = p;
+        g_static_ctx[dev] = current_context_id();
     }
     return g_static_ptr[dev];
 }
-
-constexpr int kMinChunkRows = 256;
-constexpr int kMaxChunkRows = 2048;
-constexpr int64_t kCtaTarget = 152 * 8;
-
-int64_t up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
-int64_t cdiv(int64_t x, int64_t a) { return (x + a - 1) / a; }
 
 }  // namespace
 }  // namespace kvd
@@ -86,15 +113,14 @@ extern "C" kvd_status decode_attention_static(const float *q, const kvd_layer *L
         work += l->h_seq_len[b] * int64_t(l->n_live);
         max_len = std::max(max_len, l->h_seq_len[b]);
     }
-    // the same chunking as decode_attention
-    const int32_t chunk = int32_t(std::min<int64_t>(
-        kMaxChunkRows, up(std::max<int64_t>(kMinChunkRows, cdiv(work, kCtaTarget)), kMinChunkRows)));
-    const int32_t nc = int32_t(std::max<int64_t>(1, cdiv(max_len, chunk)));
+    // the same chunking as decode_attention (one definition, kvd_internal.cuh)
+    const int32_t chunk = pick_chunk(work);
+    const int32_t nc = int32_t(std::max<int64_t>(1, ceil_div(max_len, chunk)));
     const int32_t n_grp = std::max(1, l->n_live);
     // Partials of this call: (max, sum, accumulator[hd]) per head per chunk.
     const int64_t P = int64_t(l->n_seq) * n_grp * nc * hpk;
-    const int64_t off_pl = up(P * 4, 256), off_pacc = off_pl + up(P * 4, 256);
-    const int64_t need = off_pacc + up(P * l->hd * 4, 256);
+    const int64_t off_pl = round_up(P * 4, 256), off_pacc = off_pl + round_up(P * 4, 256);
+    const int64_t need = off_pacc + round_up(P * l->hd * 4, 256);
     if (need > kStaticScratchBytes) return KVD_ECAPACITY;
     char *ws = static_cast<char *>(static_scratch());
     if (ws == nullptr) return KVD_ECUDA;
@@ -127,9 +153,8 @@ extern "C" kvd_status decode_attention_static(const float *q, const kvd_layer *L
         s.seq_len = l->d_seq_len;
         s.live = l->d_live;
         s.n_live = l->n_live;
-        dim3 grid(unsigned(cdiv(max_len, chunk)), unsigned(l->n_live), unsigned(l->n_seq));
-        int hb = 1;
-        while (hb < hpk) hb <<= 1;
+        dim3 grid(unsigned(ceil_div(max_len, chunk)), unsigned(l->n_live), unsigned(l->n_seq));
+        const int hb = hpk_bucket(hpk);
         cudaError_t e;
         switch (l->mode) {
             case KVD_F32: e = split_layer_f32(l->hd, hb, a, s, grid, st); break;
