@@ -269,6 +269,19 @@ KVD_API kvd_status decode_attention_static(const float *q, const kvd_layer *L, i
  * found metadata out of range and skipped the access. */
 KVD_API kvd_status kvd_layer_device_error(const kvd_layer *L, int32_t clear, uint32_t *word_out);
 
+/* Failure injection for tests (the pages have no counterpart; host-only, the
+ * device never sees it).  n >= 0 arms a process-wide counter: the (n+1)-th
+ * kernel launch or host/device copy that the library issues from then on
+ * reports failure, the entry point that issued it returns KVD_ECUDA, and the
+ * counter disarms itself; n < 0 disarms it.  Entry points that change
+ * host-mirrored state (lengths, frozen flags, ring cursors, histories) change
+ * it only after every launch of the call has gone in, so a call that fails
+ * this way leaves that state as it was; kernels it launched before the
+ * failure may have run, so the caller resets the layer or stream state it
+ * cannot vouch for (kvd_layer_reset).  Calls from several threads at once
+ * share the counter. */
+KVD_API kvd_status kvd_test_fail_after(int64_t n);
+
 /* The bounded-wait path, run on purpose (a diagnostic: the pages have no
  * counterpart).  One warp waits for an mbarrier phase that nothing
  * completes, gives up after limit_ns nanoseconds and sets bit 0 of the

@@ -278,9 +278,7 @@ kvd_status launch_freeze(Layer *l, const std::vector<uint8_t> &todo, cudaStream_
         dim3 grid(unsigned(l->n_live), unsigned(a.n));
         if (l->hd == 128) freeze_kernel<128><<<grid, 128, 0, s>>>(a);
         else freeze_kernel<64><<<grid, 64, 0, s>>>(a);
-        if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
-        for (int i = 0; i < a.n; ++i)
-            if (a.todo[i]) l->h_frozen[s0 + i] = 1;
+        if (launch_status() != cudaSuccess) return KVD_ECUDA;
     }
     return KVD_OK;
 }
@@ -346,12 +344,15 @@ extern "C" kvd_status kv_append(kvd_layer *L, const float *k, const float *v, co
         kvd_status st = launch_append(l, k, v, t, mx, s);
         if (st != KVD_OK) return st;
     }
+    // The host mirror changes only once every launch of the call has gone in
+    // (a failed launch leaves it as it was; the device state is then the
+    // caller's to reset).
     bool any_freeze = false;
-    for (int b = 0; b < ns; ++b) {
-        l->h_seq_len[b] += pre[b];
-        any_freeze = any_freeze || freeze[b];
+    for (int b = 0; b < ns; ++b) any_freeze = any_freeze || freeze[b];
+    if (!any_freeze) {
+        for (int b = 0; b < ns; ++b) l->h_seq_len[b] += cnt[b];
+        return KVD_OK;
     }
-    if (!any_freeze) return KVD_OK;
     // Phase B: freeze; phase C: the remaining rows against the new fields.
     kvd_status st = launch_freeze(l, freeze, s);
     if (st != KVD_OK) return st;
@@ -365,7 +366,7 @@ extern "C" kvd_status kv_append(kvd_layer *L, const float *k, const float *v, co
             const int b = s0 + i;
             const int64_t rest = cnt[b] - pre[b];
             t.in_row[i] = int32_t(in_row[b] + pre[b]);
-            t.start[i] = int32_t(l->h_seq_len[b]);
+            t.start[i] = int32_t(l->h_seq_len[b] + pre[b]);
             t.count[i] = int32_t(rest);
             mx = std::max(mx, rest);
             any = any || rest > 0;
@@ -374,7 +375,10 @@ extern "C" kvd_status kv_append(kvd_layer *L, const float *k, const float *v, co
         st = launch_append(l, k, v, t, mx, s);
         if (st != KVD_OK) return st;
     }
-    for (int b = 0; b < ns; ++b) l->h_seq_len[b] += cnt[b] - pre[b];
+    for (int b = 0; b < ns; ++b) {
+        l->h_seq_len[b] += cnt[b];
+        if (freeze[b]) l->h_frozen[b] = 1;
+    }
     return KVD_OK;
 }
 
@@ -388,5 +392,9 @@ extern "C" kvd_status kv_freeze_colfield(kvd_layer *L, void *stream) {
         any = any || todo[b];
     }
     if (!any) return KVD_OK;
-    return launch_freeze(l, todo, as_stream(stream));
+    const kvd_status st = launch_freeze(l, todo, as_stream(stream));
+    if (st != KVD_OK) return st;
+    for (int b = 0; b < l->n_seq; ++b)
+        if (todo[b]) l->h_frozen[b] = 1;
+    return KVD_OK;
 }

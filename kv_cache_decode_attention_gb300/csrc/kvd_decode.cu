@@ -573,7 +573,7 @@ cudaError_t launch_split_rswa(const SplitArgs &a, const RswaSrc &s, const RswaTa
     cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), C::SMEM);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, C::SMEM, st>>>(a, s, t);
-    return cudaGetLastError();
+    return launch_status();
 }
 
 template <int HD, bool I8>
@@ -1008,7 +1008,7 @@ extern "C" kvd_status decode_attention_ex(const float *q, const kvd_layer *L, in
         dim3 mgrid(unsigned(n_q), unsigned(l->n_seq));
         if (l->hd == 128) merge_layer_kernel<128><<<mgrid, 128, 0, st>>>(m, ms);
         else merge_layer_kernel<64><<<mgrid, 64, 0, st>>>(m, ms);
-        if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
+        if (launch_status() != cudaSuccess) return KVD_ECUDA;
     }
 
     if (imp && max_len > 0 && l->n_live > 0) {
@@ -1174,7 +1174,7 @@ extern "C" kvd_status decode_attention_verify(const float *q, const kvd_layer *L
     dim3 mgrid(unsigned(n_q), unsigned(l->n_seq), unsigned(K));
     if (l->hd == 128) merge_verify_kernel<128><<<mgrid, 128, 0, st>>>(m, ms, K, hg);
     else merge_verify_kernel<64><<<mgrid, 64, 0, st>>>(m, ms, K, hg);
-    return cudaGetLastError() == cudaSuccess ? KVD_OK : KVD_ECUDA;
+    return launch_status() == cudaSuccess ? KVD_OK : KVD_ECUDA;
 }
 
 // ------------------------------------------------------------------ R-SWA
@@ -1220,7 +1220,7 @@ static kvd_status record_prefill(float *ref_k, float *ref_v, const rswa_i8_mirro
             prefill_copy_kernel<<<blocks, 256, 0, st>>>(ref_k, ref_v, k, v, s, seq, H, head_dim,
                                                         ref_cap);
         }
-        if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
+        if (launch_status() != cudaSuccess) return KVD_ECUDA;
     }
     prefill_len[s] = seq;
     ring_len[s] = 0;
@@ -1290,7 +1290,7 @@ static kvd_status ring_write(float *ring_k, float *ring_v, const rswa_i8_mirror 
             ring_write_kernel<<<grid, 256, 0, as_stream(stream)>>>(ring_k, ring_v, k, v, H, head_dim,
                                                                   W, t);
         }
-        if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
+        if (launch_status() != cudaSuccess) return KVD_ECUDA;
     }
     for (int s = 0; s < B; ++s) {
         if (ring_len[s] < W) {
@@ -1447,7 +1447,7 @@ static kvd_status rswa_decode_impl(const float *q, const RswaSrc &src_in, const 
         dim3 mgrid(unsigned(H), unsigned(t.n));
         if (head_dim == 128) merge_rswa_kernel<128><<<mgrid, 128, 0, st>>>(m, t);
         else merge_rswa_kernel<64><<<mgrid, 64, 0, st>>>(m, t);
-        if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
+        if (launch_status() != cudaSuccess) return KVD_ECUDA;
     }
     return KVD_OK;
 }
@@ -1607,7 +1607,7 @@ static kvd_status rswa_verify_impl(const float *q, const float *dk, const float 
             tabs.H = H;
             tabs.ref_cap = ref_cap;
             rswa_tc_tables_kernel<<<1, 256, 0, st>>>(t, tabs);
-            if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
+            if (launch_status() != cudaSuccess) return KVD_ECUDA;
             int64_t T = 0;
             for (int i = 0; i < t.n; ++i) T += int64_t(H) * ceil_div(t.prefill_len[i], kWR);
             WarpArgs wa;
@@ -1654,11 +1654,11 @@ static kvd_status rswa_verify_impl(const float *q, const float *dk, const float 
         dim3 tgrid(unsigned(K), unsigned(H), unsigned(t.n));
         if (head_dim == 128) rswa_verify_tail_kernel<128, I8><<<tgrid, 128, 0, st>>>(ta, tt, RswaRunMerge{});
         else rswa_verify_tail_kernel<64, I8><<<tgrid, 128, 0, st>>>(ta, tt, RswaRunMerge{});
-        if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
+        if (launch_status() != cudaSuccess) return KVD_ECUDA;
         dim3 mgrid(unsigned(H), unsigned(t.n), unsigned(K));
         if (head_dim == 128) merge_rswa_verify_kernel<128><<<mgrid, 128, 0, st>>>(m, t, K);
         else merge_rswa_verify_kernel<64><<<mgrid, 64, 0, st>>>(m, t, K);
-        if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
+        if (launch_status() != cudaSuccess) return KVD_ECUDA;
     }
     return KVD_OK;
 }

@@ -722,7 +722,7 @@ cudaError_t launch_split_layer_impl(const SplitArgs &a, const LayerSrc &s, dim3 
     cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), C::SMEM);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, C::SMEM, st>>>(a, s);
-    return cudaGetLastError();
+    return launch_status();
 }
 
 }  // namespace kvd

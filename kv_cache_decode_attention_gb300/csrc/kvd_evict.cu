@@ -718,7 +718,7 @@ extern "C" kvd_status kv_evict_born(kvd_layer *L, float *imp, int64_t keep_last,
         if (regions >= kSerialRegions || batch < 1) {
             dim3 grid(unsigned(l->n_live * g.n_st), unsigned(t.n));
             born_gather_kernel<<<grid, kGatherThreads, 0, st>>>(g, t);
-            if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
+            if (launch_status() != cudaSuccess) return KVD_ECUDA;
             continue;
         }
         BatchArgs ba;
@@ -740,7 +740,7 @@ extern "C" kvd_status kv_evict_born(kvd_layer *L, float *imp, int64_t keep_last,
                       unsigned(l->n_live * g.n_st), unsigned(t.n));
             born_batch_kernel<true><<<grid, kGatherThreads, 0, st>>>(ba, t);
             born_batch_kernel<false><<<grid, kGatherThreads, 0, st>>>(ba, t);
-            if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
+            if (launch_status() != cudaSuccess) return KVD_ECUDA;
         }
     }
     for (int b : todo) l->h_seq_len[b] = keep_last;
@@ -768,8 +768,9 @@ extern "C" kvd_status kv_truncate_last(kvd_layer *L, const int32_t *n_drop, floa
             t.imp_base[i] = l->h_imp_base[b];
         }
         truncate_kernel<<<unsigned(t.n), 256, 0, st>>>(l->d_seq_len, imp, t);
-        if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
-        for (int i = 0; i < t.n; ++i) l->h_seq_len[t.seq[i]] = t.new_len[i];
+        if (launch_status() != cudaSuccess) return KVD_ECUDA;
     }
+    // the host mirror changes once every launch has gone in
+    for (int b : todo) l->h_seq_len[b] -= std::min<int64_t>(n_drop ? n_drop[b] : 1, l->h_seq_len[b]);
     return KVD_OK;
 }

@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 #include <utility>
 #include <vector>
@@ -137,6 +138,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Failure injection for tests (kvd_test_fail_after): while armed with n >= 0,
+// the (n+1)-th kernel launch or host/device copy that the library issues from
+// then on reports failure (cudaErrorLaunchFailure) to its entry point, which
+// returns KVD_ECUDA; the counter then disarms itself.  Host-only: the device
+// never sees it.
+extern std::atomic<int64_t> g_fault_countdown;
+inline bool fault_fires() {
+    int64_t c = g_fault_countdown.load(std::memory_order_relaxed);
+    while (c >= 0 && !g_fault_countdown.compare_exchange_weak(c, c - 1, std::memory_order_relaxed)) {
+    }
+    return c == 0;
+}
+
+// Status of the launches since the last call (cudaGetLastError), or the
+// injected failure.
+inline cudaError_t launch_status() {
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess && fault_fires() ? cudaErrorLaunchFailure : e;
+}
+
 // Programmatic dependent launch.  A kernel that produces data calls
 // pdl_trigger() to let the next kernel on the stream (launched with
 // launch_pdl) start early; that kernel does the work that does not read the
@@ -159,7 +180,8 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+    return e == cudaSuccess && fault_fires() ? cudaErrorLaunchFailure : e;
 }
 
 __device__ __forceinline__ uint64_t global_ns() {

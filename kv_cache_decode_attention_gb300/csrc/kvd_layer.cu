@@ -263,8 +263,8 @@ extern "C" kvd_status kvd_layer_init(kvd_layer *L, int32_t n_seq, int32_t n_kv, 
     std::memcpy(stage.data() + l.ml.slot, l.h_slot, 4 * size_t(n_kv));
     cudaStream_t cs = as_stream(stream);
     // Pageable source: the copy is staged before cudaMemcpyAsync returns.
-    if (cudaMemcpyAsync(meta, stage.data(), stage.size(), cudaMemcpyHostToDevice, cs) !=
-        cudaSuccess)
+    if (cudaMemcpyAsync(meta, stage.data(), stage.size(), cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+        fault_fires())
         return KVD_ECUDA;
     const int64_t fe = int64_t(n_seq) * s.n_live * head_dim;
     if (fe > 0) {
@@ -276,7 +276,7 @@ extern "C" kvd_status kvd_layer_init(kvd_layer *L, int32_t n_seq, int32_t n_kv, 
             fill_f32_kernel<<<608, 256, 0, cs>>>(static_cast<float *>(l.buf[KVD_BUF_VCOL]), fe,
                                                      1.0f);
         }
-        if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
+        if (launch_status() != cudaSuccess) return KVD_ECUDA;
     }
     const int64_t code_rows = s.total_rows + kRowAlign;
     if (l.buf[KVD_BUF_KQ])
@@ -299,7 +299,7 @@ extern "C" kvd_status kvd_layer_reset(kvd_layer *L, int32_t seq, void *stream) {
             l->d_seq_len, l->d_frozen, static_cast<float *>(l->buf[KVD_BUF_KCOL]),
             static_cast<float *>(l->buf[KVD_BUF_VCOL]), s0, cnt, fe);
     }
-    if (cudaGetLastError() != cudaSuccess) return KVD_ECUDA;
+    if (launch_status() != cudaSuccess) return KVD_ECUDA;
     for (int32_t b = seq0; b < seq0 + n; ++b) {
         l->h_seq_len[b] = 0;
         l->h_frozen[b] = 0;
@@ -365,7 +365,16 @@ extern "C" kvd_status kvd_wait_timeout_selftest(const kvd_layer *L, int64_t limi
     const Layer *l = checked_layer(L);
     if (l == nullptr || limit_ns < 1 || limit_ns > 1000000000) return KVD_EINVAL;
     wait_selftest_kernel<<<1, 32, 0, as_stream(stream)>>>(l->d_err, uint64_t(limit_ns));
-    return cudaGetLastError() == cudaSuccess ? KVD_OK : KVD_ECUDA;
+    return launch_status() == cudaSuccess ? KVD_OK : KVD_ECUDA;
+}
+
+namespace kvd {
+std::atomic<int64_t> g_fault_countdown{-1};
+}  // namespace kvd
+
+extern "C" kvd_status kvd_test_fail_after(int64_t n) {
+    kvd::g_fault_countdown.store(n < 0 ? -1 : n);
+    return KVD_OK;
 }
 
 extern "C" const char *kvd_status_string(int32_t status) {

@@ -183,5 +183,5 @@ extern "C" kvd_status decode_attention_static(const float *q, const kvd_layer *L
     dim3 mgrid(unsigned(n_q), unsigned(l->n_seq));
     if (l->hd == 128) merge_layer_kernel<128><<<mgrid, 128, 0, st>>>(m, ms);
     else merge_layer_kernel<64><<<mgrid, 64, 0, st>>>(m, ms);
-    return cudaGetLastError() == cudaSuccess ? KVD_OK : KVD_ECUDA;
+    return launch_status() == cudaSuccess ? KVD_OK : KVD_ECUDA;
 }

@@ -228,3 +228,11 @@ def test_rswa_verify_and_mirror_host_validation(abi):
     assert L.rswa_record_prefill_i8(fake, fake, None, fake, fake, 0, 4, B, H, hd, ref_cap, W, p(pl), p(rl), p(rp),
                                     hist, None) == abi.EINVAL
     assert pl.tolist() == [3, 5] and hist[0].lineage_epoch == 0
+
+
+def test_failure_injection_hook_arms_and_disarms(abi):
+    """kvd_test_fail_after is host-only: arming and disarming it needs no
+    device (the GPU tests make calls fail with it)."""
+    lib = abi.lib()
+    assert lib.kvd_test_fail_after(3) == abi.OK
+    assert lib.kvd_test_fail_after(-1) == abi.OK
