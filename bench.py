@@ -47,6 +47,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "decode-attention KV GB/s (fraction of GB300 HBM peak) and queries/sec, 1 GPU"
+# the q8_2f decode's contraction: int8 codes are exact in f16; the query and the
+# softmax weights are each split into two f16 terms (hi + lo), so the products
+# keep ~22 bits of the f32 operand; mma.sync m16n8k16, f32 accumulate
+Q8_ARITHMETIC = ("int8 codes exact in f16, query and weights split into two f16 terms each, "
+                 "mma.sync, f32 accumulate")
 L2_BYTES = 129 * 1024 * 1024
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -775,6 +780,11 @@ def run_gpu_rswa(args, rank, world):
                    "reference_rows": int(wl.prefill), "ring_rows": int(c.W),
                    "step": ("rswa verify of %d drafts/stream (read-only) + ring write of the accepted token" % K
                             if verify else "rswa ring write 1 token/stream + decode of every stream"),
+                   "arithmetic": ("int8 query and K codes exact in f16, mma.sync, f32 accumulate, per-row "
+                                  "K scales applied to the scores (reference block); f32 CUDA-core dots "
+                                  "elsewhere" if int8 and verify else
+                                  "int8 codes widened to f32, CUDA-core dots" if int8 else
+                                  "f32 CUDA-core dots"),
                    "l2": "inputs larger than L2 (%.2f GB read per decode)" % (dec_bytes / 1e9),
                    "parallelism": "replicas" if world > 1 else "single"},
         "fraction_of_peak": round(gbs / world / peak, 4),
@@ -938,6 +948,7 @@ def run_gpu_verify(args, rank, world):
         "config": {"workload": "verify_q8_gqa", "mode": "q8_2f", "n_seq": n_seq,
                    "cached_rows": int(probe.lengths[0]), "drafts": K, "n_q": n_q, "n_kv": n_kv, "head_dim": hd,
                    "step": "kv_append %d drafts/seq + decode_attention_verify + kv_truncate_last %d" % (K, K),
+                   "arithmetic": Q8_ARITHMETIC,
                    "replicas": R, "l2": "inputs larger than L2 (%d rotated cache replicas)" % R,
                    "parallelism": "replicas" if world > 1 else "single"},
         "fraction_of_peak": round(gbs / world / peak, 4),
@@ -1151,8 +1162,7 @@ def run_gpu_ragged(args, rank, world):
                    "n_q": n_q, "n_kv": n_kv, "head_dim": hd,
                    "layers": "f32, q8 (q8_2f), q8k, q8v; 2 of 8 KV heads dead per layer",
                    "step": "per layer: kv_append 1 row/seq + decode_attention with imp",
-                   "arithmetic": "f32 CUDA-core dots (f32, q8k, q8v layers); q8 layer: int8 codes exact in f16, "
-                                 "query and weights split into two f16 terms each, mma.sync, f32 accumulate",
+                   "arithmetic": "f32 CUDA-core dots (f32, q8k, q8v layers); q8 layer: " + Q8_ARITHMETIC,
                    "l2": "inputs larger than L2 (%.1f GB read per step)" % (bytes_total / args.steps / 1e9),
                    "parallelism": "replicas" if world > 1 else "single"},
         "fraction_of_peak": round(gbs / world / peak, 4),
@@ -1298,6 +1308,17 @@ def run_gpu(args, rank, world):
     kbytes = statistics.mean(
         decode_bytes(wls[j % R].mode, n_live, wl0.hd, wl0.n_q, lens_now[j % R], False, wl0.n_seq)
         for j in range(nrep))
+    # the same calls with imp on (the score round trip and the imp pass), timed alone
+    for j in range(nrep):
+        w = wls[j % R]
+        dev_ev[j][0].record(stream)
+        kvd.decode_attention(qs[j % 8], w.layer, out=outs[j % R], imp=imps[j % R], scale=w.scale, workspace=ws)
+        dev_ev[j][1].record(stream)
+    torch.cuda.synchronize()
+    imp_ms = statistics.mean(a.elapsed_time(b) for a, b in dev_ev)
+    imp_bytes = statistics.mean(
+        decode_bytes(wls[j % R].mode, n_live, wl0.hd, wl0.n_q, lens_now[j % R], True, wl0.n_seq)
+        for j in range(nrep))
     peak, peak_kind = peaks()
     achieved = kbytes / (k_ms * 1e-3) / 1e9
 
@@ -1374,6 +1395,7 @@ def run_gpu(args, rank, world):
         "config": {"workload": wl0.name, "mode": "q8_2f", "n_seq": wl0.n_seq,
                    "cached_rows": int(wl0.lengths[0]), "n_q": wl0.n_q, "n_kv": wl0.n_kv,
                    "head_dim": wl0.hd, "step": "kv_append 1 row/seq + decode_attention with imp",
+                   "arithmetic": Q8_ARITHMETIC,
                    "replicas": R, "l2": "inputs larger than L2 (%d rotated cache replicas)" % R,
                    "parallelism": "replicas" if world > 1 else "single"},
         "fraction_of_peak": round(gbs / world / peak, 4),
@@ -1382,7 +1404,10 @@ def run_gpu(args, rank, world):
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": measured_traffic(wl0.name, kbytes),
                      "peak_kind": peak_kind, "ms_per_launch": round(k_ms, 5),
-                     "bytes_per_launch": int(kbytes)},
+                     "bytes_per_launch": int(kbytes),
+                     "imp_on": {"ms_per_launch": round(imp_ms, 5), "bytes_per_launch": int(imp_bytes),
+                                "achieved": round(imp_bytes / (imp_ms * 1e-3) / 1e9, 1),
+                                "frac": round(imp_bytes / (imp_ms * 1e-3) / 1e9 / peak, 4)}},
         "decode_ms_in_step": round(statistics.mean(dec_ms), 5),
         "cpu_baseline": cpu,
         "e2e": e2e,
