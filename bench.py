@@ -69,9 +69,9 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
 CSRC_COMMON = ("kvd_internal.cuh", "kvd_decode.cu")
 CSRC_CUDA_CORE = CSRC_COMMON + ("kvd_decode_kernels.cuh", "kvd_split_f32.cu", "kvd_split_q8k.cu",
                                 "kvd_split_q8v.cu")
-CSRC_TC = CSRC_COMMON + ("kvd_split_mma.cuh", "kvd_split_h16.cuh", "kvd_split_q8.cu")
+CSRC_TC = CSRC_COMMON + ("kvd_decode_kernels.cuh", "kvd_split_mma.cuh", "kvd_split_h16.cuh", "kvd_split_q8.cu")
 TRAFFIC = {
-    "q8_gqa": {"files": None, "sources_sha256": "813bda5fa871babc27a6d8f99409a7ac294be15c3a90ad55523a3c5f51eb5034",
+    "q8_gqa": {"files": CSRC_TC, "sources_sha256": "813bda5fa871babc27a6d8f99409a7ac294be15c3a90ad55523a3c5f51eb5034",
                "bytes": 300582016, "algorithmic_bytes": 291600896},
     # the first 16 sequences of the ragged batch, 3 + 3 steps in, mean of 10 calls
     "ragged_f32": {"files": CSRC_CUDA_CORE,
