@@ -51,7 +51,14 @@ struct TileCfg {
     static constexpr int VS_OFF = KS_OFF + (KQ ? TR * NKS * 4 : 0);
     static constexpr int KSEG = VS_OFF + (VQ ? TR * 4 : 0);
     static constexpr int VSEG = TR * VROW;
-    static constexpr int SLOT = ce_round(ce_max(KSEG, VSEG), 128);
+    // Ring slots alternate K segments (even slots) and V segments (odd slots),
+    // each sized for its own segment: with one int8 component (q8k, q8v) the
+    // ring is ~40 KB instead of 64 KB, so four CTAs fit an SM instead of three.
+    static constexpr int KSLOT = ce_round(KSEG, 128);
+    static constexpr int VSLOT = ce_round(VSEG, 128);
+    static constexpr int RING = 2 * (KSLOT + VSLOT);
+    static_assert(kNSeg == 4, "segment j goes to slot j % 4: K in slots 0 and 2, V in 1 and 3");
+    static __host__ __device__ constexpr int slot_off(int slot) { return (slot >> 1) * (KSLOT + VSLOT) + (slot & 1) * KSLOT; }
 };
 
 template <int HD, int HPK, bool KQ, bool VQ, bool KI8 = false>
@@ -61,11 +68,11 @@ struct SplitCfg : TileCfg<HD, KQ, VQ, KI8> {
     static constexpr int RB = ce_min(32 / HPK, RPW);       // rows per reduce batch
     static constexpr int E = RB * HPK;                     // entries per reduce (<= 32)
     static constexpr int LOGE = ce_log2(E);
-    static constexpr int SC_OFF = kNSeg * T::SLOT;         // scores/weights [TR][HPK]
+    static constexpr int SC_OFF = T::RING;                 // scores/weights [TR][HPK]
     static constexpr int MISC_OFF = SC_OFF + T::TR * HPK * 4;
     // misc: kNSeg mbarriers, red[kWarps][HPK], mrun[HPK], alpha[HPK], flag
     static constexpr int SMEM = MISC_OFF + kNSeg * 8 + (kWarps + 2) * HPK * 4 + 16;
-    static_assert(kWarps * HPK * HD * 4 <= kNSeg * T::SLOT, "accumulator reduction must fit");
+    static_assert(kWarps * HPK * HD * 4 <= T::RING, "accumulator reduction must fit");
     static_assert((1 << LOGE) == E, "reduce entries must be a power of two");
 };
 
@@ -190,7 +197,7 @@ __device__ __forceinline__ void issue_segment(const ChunkInfo &ci, char *smem, u
     const int row0 = t * C::TR;
     const int nt = min(C::TR, ci.n - row0);
     const int rows = (nt + kRowAlign - 1) / kRowAlign * kRowAlign;
-    char *dst = smem + slot * C::SLOT;
+    char *dst = smem + C::slot_off(slot);
     if ((j & 1) == 0) {
         uint32_t bytes = uint32_t(rows) * C::KROW;
         if (KQ) bytes += uint32_t(rows) * C::NKS * 4;
@@ -306,7 +313,7 @@ __device__ void split_body(const ChunkInfo &ci, const SplitArgs &a, char *smem) 
             ok = false;
             break;
         }
-        const char *kseg = smem + slot * C::SLOT;
+        const char *kseg = smem + C::slot_off(slot);
 #pragma unroll 1
         for (int bt = 0; bt < C::RPW / C::RB; ++bt) {
             const int rbase = warp * C::RPW + bt * C::RB;
@@ -407,7 +414,7 @@ __device__ void split_body(const ChunkInfo &ci, const SplitArgs &a, char *smem) 
             ok = false;
             break;
         }
-        const char *vseg = smem + slot * C::SLOT;
+        const char *vseg = smem + C::slot_off(slot);
         // this tile's rows accumulate into fresh registers, folded into the
         // running (rescaled) sum once per tile: short rounding chains
         float tacc[HPK][CPL];
