@@ -506,8 +506,11 @@ struct LayerSrc {
     int32_t n_live;
 };
 
+// Up to 4 heads per group the kernel fits 102 registers without spilling, so
+// five CTAs share an SM where shared memory allows (the q8k and q8v rings);
+// more heads per group need the larger register budget of two.
 template <int HD, int HPK, bool KQ, bool VQ, bool OPT>
-__global__ void __launch_bounds__(kThreads, 2) split_layer_kernel(SplitArgs a, LayerSrc src) {
+__global__ void __launch_bounds__(kThreads, HPK <= 4 ? 5 : 2) split_layer_kernel(SplitArgs a, LayerSrc src) {
     extern __shared__ __align__(128) char smem[];
     const int b = blockIdx.z, gl = blockIdx.y, c = blockIdx.x;
     const int L = src.seq_len[b];
