@@ -78,14 +78,14 @@ TRAFFIC = {
     "long_q8": {"files": CSRC_TC, "sources_sha256": "9f6c5a583b51a725b503a174feee22625e7526babc31d3ee0c3054a075afcd3c",
                 "bytes": 609700352, "algorithmic_bytes": 579149888},
     # the first 16 sequences of the ragged batch, 3 + 3 steps in, mean of 10 calls
-    "ragged_f32": {"files": CSRC_CUDA_CORE, "sources_sha256": "a3e3dfe2f61a7a40ef7cb5ea8050bed6daf6e7fa1ef442d7c58ab324ae947509",
-                   "bytes": 944681830, "algorithmic_bytes": 939376640},
-    "ragged_q8": {"files": CSRC_TC, "sources_sha256": "9f6c5a583b51a725b503a174feee22625e7526babc31d3ee0c3054a075afcd3c",
-                  "bytes": 259254144, "algorithmic_bytes": 253672640},
-    "ragged_q8k": {"files": CSRC_CUDA_CORE, "sources_sha256": "a3e3dfe2f61a7a40ef7cb5ea8050bed6daf6e7fa1ef442d7c58ab324ae947509",
-                   "bytes": 606989926, "algorithmic_bytes": 602025728},
-    "ragged_q8v": {"files": CSRC_CUDA_CORE, "sources_sha256": "a3e3dfe2f61a7a40ef7cb5ea8050bed6daf6e7fa1ef442d7c58ab324ae947509",
-                   "bytes": 595987072, "algorithmic_bytes": 591023552},
+    "ragged_f32": {"files": CSRC_CUDA_CORE, "sources_sha256": "ed4ede5c7b63d3c498d8e0d06eeeac3b8a6eab582212b3643da829b521611cfc",
+                   "bytes": 944696576, "algorithmic_bytes": 939376640},
+    "ragged_q8": {"files": CSRC_TC, "sources_sha256": "ac5f99cf2411775dfd376fa02c024d5e04929e7bd3f75f28c7a6c10568d8662b",
+                  "bytes": 259220429, "algorithmic_bytes": 253672640},
+    "ragged_q8k": {"files": CSRC_CUDA_CORE, "sources_sha256": "ed4ede5c7b63d3c498d8e0d06eeeac3b8a6eab582212b3643da829b521611cfc",
+                   "bytes": 606740762, "algorithmic_bytes": 602025728},
+    "ragged_q8v": {"files": CSRC_CUDA_CORE, "sources_sha256": "ed4ede5c7b63d3c498d8e0d06eeeac3b8a6eab582212b3643da829b521611cfc",
+                   "bytes": 595761024, "algorithmic_bytes": 591023552},
 }
 
 
