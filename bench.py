@@ -119,6 +119,22 @@ def peaks():
     return 6800.0, "fallback"
 
 
+def tensor_peak():
+    """Dense 16-bit tensor peak in TFLOP/s (the measured bf16 burst figure; f16
+    runs at the same rate), else the fallback."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        return float(json.load(open(p))["bf16_tflops"]), "measured (bf16 burst; f16 at the same rate)"
+    return 1900.0, "fallback"
+
+
+def decode_flops(n_live, hd, hpk, lengths, n_seq) -> int:
+    """The decode's algorithmic floating-point work: two contractions (q.K and
+    P.V) of 2 flops per multiply-add, hpk heads x hd channels per cached row
+    per live group."""
+    return int(4 * hpk * hd * n_live * int(np.sum(np.asarray(lengths[:n_seq], dtype=np.int64))))
+
+
 # ------------------------------------------------------------ byte counts
 # The metric's algorithmic bytes: what a decode must move at least, whatever
 # the kernel (scratch partials are implementation cost and not counted).
@@ -1324,6 +1340,10 @@ def run_gpu(args, rank, world):
         for j in range(nrep))
     peak, peak_kind = peaks()
     achieved = kbytes / (k_ms * 1e-3) / 1e9
+    tpeak, tpeak_kind = tensor_peak()
+    kflops = statistics.mean(
+        decode_flops(n_live, wl0.hd, wl0.n_q // wl0.n_kv, lens_now[j % R], wl0.n_seq) for j in range(nrep))
+    kflops = int(kflops)
 
     # ---- end to end through the public API with host buffers: pipelined (the
     #      headline), then the same steps synchronising on every step's result
@@ -1411,6 +1431,13 @@ def run_gpu(args, rank, world):
                      "imp_on": {"ms_per_launch": round(imp_ms, 5), "bytes_per_launch": int(imp_bytes),
                                 "achieved": round(imp_bytes / (imp_ms * 1e-3) / 1e9, 1),
                                 "frac": round(imp_bytes / (imp_ms * 1e-3) / 1e9 / peak, 4)}},
+        # the second roof: the same decode call against the tensor peak (the
+        # q8_2f kernels run each contraction twice, one f16 term each)
+        "roofline_tensor": {"bound": "tensor", "achieved": round(kflops / (k_ms * 1e-3) / 1e12, 2),
+                            "peak": tpeak, "unit": "TFLOP/s",
+                            "frac": round(kflops / (k_ms * 1e-3) / 1e12 / tpeak, 4), "peak_kind": tpeak_kind,
+                            "flops_per_launch": kflops, "executed_flops_per_launch": 2 * kflops}
+        if wl0.mode == Q8_MODE else None,
         "decode_ms_in_step": round(statistics.mean(dec_ms), 5),
         "cpu_baseline": cpu,
         "e2e": e2e,
