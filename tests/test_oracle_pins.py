@@ -129,8 +129,9 @@ def test_quantiser_floor_and_zero_group():
 
 
 def test_quantiser_col_division_and_half_scale_bound():
-    """The benchmark spec pin: dequantised rows reproduce the originals within scale/2 per
-    element; with a per-channel field the residual x/col is what is quantised."""
+    """Round-to-nearest bound: dequantised rows reproduce the originals within
+    scale/2 per element; with a per-channel field the residual x/col is what is
+    quantised."""
     x = synthetic.normal((50, 128), 11) * synthetic.channel_sigma((128,), 12)
     col = synthetic.channel_sigma((128,), 13)
     for r in x:
