@@ -291,6 +291,25 @@ KVD_API kvd_status kvd_test_fail_after(int64_t n);
  * KVD_EINVAL for limit_ns outside 1 .. 10^9. */
 KVD_API kvd_status kvd_wait_timeout_selftest(const kvd_layer *L, int64_t limit_ns, void *stream);
 
+/* The kernels' metadata guards, run on purpose (a diagnostic: the pages have
+ * no counterpart; it exercises bit 1 of the device error word, which no
+ * sequence of ordinary calls sets).  Launches, on `stream`: the append kernel
+ * asked for storage row cap[0] of sequence 0 (one past its capacity); for a
+ * quantised mode the freeze kernel on lengths that put sequence 0 at
+ * cap[0] + 1 rows; and the decode's split kernel on the same lengths (one CTA
+ * on the CUDA-core path, one worker over one tile on the q8_2f tensor-core
+ * path).  The fake lengths, and every length, flag, partial or slot record
+ * those kernels are given to write, live in `scratch` (device, caller-owned,
+ * 256-byte aligned, at least kvd_bounds_selftest_bytes bytes; its contents on
+ * return are unspecified), never in the layer.  Each kernel's guard sets
+ * bit 1 and returns before it reads or writes the cache, so the layer's
+ * storage, lengths and frozen flags are unchanged.  Read the word with
+ * kvd_layer_device_error after synchronising the stream.  KVD_EINVAL for a
+ * layer without live groups, a null or unaligned scratch, or cap[0] >= 2^31 - 1;
+ * KVD_ECAPACITY if scratch_bytes is too small (nothing launched). */
+KVD_API kvd_status kvd_bounds_selftest_bytes(const kvd_layer *L, int64_t *bytes_out);
+KVD_API kvd_status kvd_bounds_selftest(const kvd_layer *L, void *scratch, int64_t scratch_bytes, void *stream);
+
 /* ---- R-SWA (rswa module): retained prefix + W-slot ring, per stream ----
  * Per stream s and head h the reference block is ref[s][h][0..ref_cap) and
  * the ring ring[s][h][0..W), rows of head_dim f32 (head-major, as rswa

@@ -69,6 +69,8 @@ _SIGS = {
     "decode_attention_static": [_vp, _P(kvd_layer), _i32, _f32, _vp, _vp],
     "kvd_layer_device_error": [_P(kvd_layer), _i32, _P(C.c_uint32)],
     "kvd_wait_timeout_selftest": [_P(kvd_layer), _i64, _vp],
+    "kvd_bounds_selftest_bytes": [_P(kvd_layer), _P(_i64)],
+    "kvd_bounds_selftest": [_P(kvd_layer), _vp, _i64, _vp],
     "kvd_test_fail_after": [_i64],
     "rswa_record_prefill": [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i64, _i32,
                             _vp, _vp, _vp, _vp, _vp],

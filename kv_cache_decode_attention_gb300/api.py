@@ -122,6 +122,19 @@ class LayerKvCache:
         device error word (read it with device_error() after synchronising)."""
         _abi.call("kvd_wait_timeout_selftest", C.byref(self.L), int(limit_ns), _stream(stream))
 
+    def bounds_selftest(self, stream=None):
+        """Run the kernels' metadata guards on purpose: the append, freeze and
+        decode split kernels are launched on lengths that put sequence 0 one
+        row past its capacity (held in a scratch buffer, not the layer's
+        metadata); each guard sets bit 1 of the device error word and returns
+        before touching the cache (read it with device_error() after
+        synchronising)."""
+        n = C.c_int64(0)
+        _abi.call("kvd_bounds_selftest_bytes", C.byref(self.L), C.byref(n))
+        scratch = torch.empty(int(n.value), dtype=torch.uint8, device=self.device)
+        _abi.call("kvd_bounds_selftest", C.byref(self.L), _ptr(scratch), int(scratch.numel()), _stream(stream))
+        return scratch  # keep it alive until the launches have run
+
     def reset(self, seq: int = -1, stream=None):
         _abi.call("kvd_layer_reset", C.byref(self.L), int(seq), _stream(stream))
 

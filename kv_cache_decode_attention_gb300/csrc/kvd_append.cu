@@ -217,9 +217,7 @@ __global__ void __launch_bounds__(HD) freeze_kernel(FreezeArgs a) {
     if (threadIdx.x == 0) a.frozen[b] = 1;  // same value from every head's block
 }
 
-kvd_status launch_append(const Layer *l, const float *k, const float *v, const AppendTable &t,
-                         int64_t max_count, cudaStream_t s) {
-    if (t.n == 0) return KVD_OK;
+AppendArgs append_args(const Layer *l, const float *k, const float *v) {
     AppendArgs a;
     a.k = k;
     a.v = v;
@@ -240,6 +238,13 @@ kvd_status launch_append(const Layer *l, const float *k, const float *v, const A
     a.n_live = l->n_live;
     a.qk = quant_k(l->mode);
     a.qv = quant_v(l->mode);
+    return a;
+}
+
+kvd_status launch_append(const Layer *l, const float *k, const float *v, const AppendTable &t,
+                         int64_t max_count, cudaStream_t s) {
+    if (t.n == 0) return KVD_OK;
+    const AppendArgs a = append_args(l, k, v);
     const int64_t items = std::max<int64_t>(1, max_count * l->n_live);
     const int64_t per_block = kAppendWarps * kItemsPerWarp;
     dim3 grid(unsigned((items + per_block - 1) / per_block), unsigned(t.n));
@@ -248,25 +253,30 @@ kvd_status launch_append(const Layer *l, const float *k, const float *v, const A
     return e == cudaSuccess ? KVD_OK : KVD_ECUDA;
 }
 
+FreezeArgs freeze_args(const Layer *l) {
+    FreezeArgs a;
+    a.kq = static_cast<int8_t *>(l->buf[KVD_BUF_KQ]);
+    a.vq = static_cast<int8_t *>(l->buf[KVD_BUF_VQ]);
+    a.ks = static_cast<float *>(l->buf[KVD_BUF_KS]);
+    a.vs = static_cast<float *>(l->buf[KVD_BUF_VS]);
+    a.kcol = static_cast<float *>(l->buf[KVD_BUF_KCOL]);
+    a.vcol = static_cast<float *>(l->buf[KVD_BUF_VCOL]);
+    a.row_base = l->d_row_base;
+    a.cap = l->d_cap;
+    a.seq_len = l->d_seq_len;
+    a.frozen = l->d_frozen;
+    a.err = l->d_err;
+    a.n_live = l->n_live;
+    a.qk = quant_k(l->mode);
+    a.qv = quant_v(l->mode);
+    return a;
+}
+
 // Freeze the sequences flagged in `todo` (host view); updates the host mirror.
 kvd_status launch_freeze(Layer *l, const std::vector<uint8_t> &todo, cudaStream_t s) {
     if (l->mode == KVD_F32 || l->n_live == 0) return KVD_OK;
     for (int32_t s0 = 0; s0 < l->n_seq; s0 += kSlice) {
-        FreezeArgs a;
-        a.kq = static_cast<int8_t *>(l->buf[KVD_BUF_KQ]);
-        a.vq = static_cast<int8_t *>(l->buf[KVD_BUF_VQ]);
-        a.ks = static_cast<float *>(l->buf[KVD_BUF_KS]);
-        a.vs = static_cast<float *>(l->buf[KVD_BUF_VS]);
-        a.kcol = static_cast<float *>(l->buf[KVD_BUF_KCOL]);
-        a.vcol = static_cast<float *>(l->buf[KVD_BUF_VCOL]);
-        a.row_base = l->d_row_base;
-        a.cap = l->d_cap;
-        a.seq_len = l->d_seq_len;
-        a.frozen = l->d_frozen;
-        a.err = l->d_err;
-        a.n_live = l->n_live;
-        a.qk = quant_k(l->mode);
-        a.qv = quant_v(l->mode);
+        FreezeArgs a = freeze_args(l);
         a.seq0 = s0;
         a.n = std::min(kSlice, l->n_seq - s0);
         bool any = false;
@@ -288,6 +298,38 @@ bool freeze_due(const Layer *l, int b) {
 }
 
 }  // namespace
+
+// Bounds self-test of the append and freeze kernels (kvd_bounds_selftest):
+// launches whose metadata put sequence 0 one row past its capacity.  The
+// append is asked for storage row cap[0]; the freeze reads lengths from
+// `seq_len` (scratch holding cap[0] + 1 for sequence 0).  Each kernel's guard
+// must set bit 1 of the error word and return before touching storage; the
+// lengths and frozen flags they could write point at scratch too.
+cudaError_t append_bounds_selftest(const Layer *l, const float *zeros, int32_t *seq_len, int32_t *frozen,
+                                   cudaStream_t s) {
+    AppendArgs a = append_args(l, zeros, zeros);
+    a.seq_len = seq_len + l->n_seq;  // a second scratch copy: the append may only write past the first
+    AppendTable t{};
+    t.seq0 = 0;
+    t.n = 1;
+    t.in_row[0] = 0;
+    t.start[0] = int32_t(l->h_cap[0]);
+    t.count[0] = 1;
+    if (l->hd == 128) append_kernel<128><<<dim3(1, 1), kAppendWarps * 32, 0, s>>>(a, t);
+    else append_kernel<64><<<dim3(1, 1), kAppendWarps * 32, 0, s>>>(a, t);
+    cudaError_t e = launch_status();
+    if (e != cudaSuccess || l->mode == KVD_F32) return e;
+    FreezeArgs f = freeze_args(l);
+    f.seq_len = seq_len;
+    f.frozen = frozen;
+    f.seq0 = 0;
+    f.n = 1;
+    f.todo[0] = 1;
+    if (l->hd == 128) freeze_kernel<128><<<dim3(unsigned(l->n_live), 1), 128, 0, s>>>(f);
+    else freeze_kernel<64><<<dim3(unsigned(l->n_live), 1), 64, 0, s>>>(f);
+    return launch_status();
+}
+
 }  // namespace kvd
 
 using namespace kvd;

@@ -1037,6 +1037,122 @@ extern "C" kvd_status decode_attention_ex(const float *q, const kvd_layer *L, in
     return KVD_OK;
 }
 
+// ------------------------------------------------------------ bounds self-test
+
+namespace kvd {
+namespace {
+
+// Scratch of kvd_bounds_selftest: two copies of fake lengths, fake frozen
+// flags, zero input rows for the append, and room for the partials and slot
+// records the split launches are given (they write none: their guards return
+// first).
+struct BoundsWs {
+    int64_t len, frozen, zeros, part, total;
+};
+
+BoundsWs bounds_ws(const Layer *l) {
+    BoundsWs w;
+    int64_t o = 0;
+    auto take = [&](int64_t bytes) {
+        const int64_t at = o;
+        o = round_up(o + bytes, 256);
+        return at;
+    };
+    w.len = take(int64_t(l->n_seq) * 2 * 4);
+    w.frozen = take(int64_t(l->n_seq) * 4);
+    w.zeros = take(int64_t(l->n_kv) * l->hd * 4);
+    w.part = take(int64_t(kMaxHpk) * (2 + l->hd) * 4 + 256);
+    w.total = o;
+    return w;
+}
+
+}  // namespace
+}  // namespace kvd
+
+extern "C" kvd_status kvd_bounds_selftest_bytes(const kvd_layer *L, int64_t *bytes_out) {
+    const Layer *l = checked_layer(L);
+    if (l == nullptr || bytes_out == nullptr) return KVD_EINVAL;
+    *bytes_out = bounds_ws(l).total;
+    return KVD_OK;
+}
+
+extern "C" kvd_status kvd_bounds_selftest(const kvd_layer *L, void *scratch, int64_t scratch_bytes,
+                                          void *stream) {
+    const Layer *l = checked_layer(L);
+    if (l == nullptr || scratch == nullptr || l->n_seq < 1 || l->n_live < 1) return KVD_EINVAL;
+    if (l->h_cap[0] >= (int64_t(1) << 31) - 1) return KVD_EINVAL;
+    if (reinterpret_cast<uintptr_t>(scratch) & 255) return KVD_EINVAL;
+    const BoundsWs w = bounds_ws(l);
+    if (scratch_bytes < w.total) return KVD_ECAPACITY;
+    char *ws = static_cast<char *>(scratch);
+    cudaStream_t st = as_stream(stream);
+    // fake lengths: sequence 0 one row past its capacity, the others as stored
+    std::vector<int32_t> len(size_t(l->n_seq) * 2);
+    for (int b = 0; b < l->n_seq; ++b) len[b] = len[l->n_seq + b] = int32_t(l->h_seq_len[b]);
+    len[0] = int32_t(l->h_cap[0] + 1);
+    if (cudaMemcpyAsync(ws + w.len, len.data(), len.size() * 4, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemsetAsync(ws + w.frozen, 0, size_t(l->n_seq) * 4, st) != cudaSuccess ||
+        cudaMemsetAsync(ws + w.zeros, 0, size_t(l->n_kv) * l->hd * 4, st) != cudaSuccess || fault_fires())
+        return KVD_ECUDA;
+    int32_t *fake_len = reinterpret_cast<int32_t *>(ws + w.len);
+    const float *zeros = reinterpret_cast<const float *>(ws + w.zeros);
+    if (append_bounds_selftest(l, zeros, fake_len, reinterpret_cast<int32_t *>(ws + w.frozen), st) != cudaSuccess)
+        return KVD_ECUDA;
+
+    // the decode's split kernel over the fake lengths: one CTA (CUDA-core
+    // path) or one worker over one tile (tensor-core path), both on
+    // sequence 0, whose guard returns before any read of the cache
+    SplitArgs a;
+    a.q = zeros;
+    a.n_q = l->n_kv;
+    a.hpk = 1;
+    a.qscale = kLog2e;
+    a.chunk = kMinChunk;
+    a.nc_max = 1;
+    a.n_grp = l->n_live;
+    a.pm = reinterpret_cast<float *>(ws + w.part);
+    a.pl = a.pm + kMaxHpk;
+    a.pacc = a.pl + kMaxHpk;
+    a.scores = nullptr;
+    a.err = l->d_err;
+    LayerSrc s;
+    s.kf = static_cast<const float *>(l->buf[KVD_BUF_K]);
+    s.vf = static_cast<const float *>(l->buf[KVD_BUF_V]);
+    s.kq = static_cast<const int8_t *>(l->buf[KVD_BUF_KQ]);
+    s.vq = static_cast<const int8_t *>(l->buf[KVD_BUF_VQ]);
+    s.ks = static_cast<const float *>(l->buf[KVD_BUF_KS]);
+    s.vs = static_cast<const float *>(l->buf[KVD_BUF_VS]);
+    s.kcol = static_cast<const float *>(l->buf[KVD_BUF_KCOL]);
+    s.row_base = l->d_row_base;
+    s.cap = l->d_cap;
+    s.seq_len = fake_len;
+    s.live = l->d_live;
+    s.n_live = l->n_live;
+    if (warp_path(l)) {
+        WarpArgs wa;
+        wa.a = a;
+        wa.T = 1;
+        wa.G = 1;
+        wa.n_seq = l->n_seq;
+        wa.unit_slots = reinterpret_cast<int64_t *>(a.pacc + kMaxHpk * l->hd);
+        MmaMaps maps;
+        std::memcpy(&maps.kq, l->tmap_kq, sizeof(maps.kq));
+        std::memcpy(&maps.vq, l->tmap_vq, sizeof(maps.vq));
+        if (split_layer_q8_tc(q8_tc_variant(1), wa, s, maps, st) != cudaSuccess) return KVD_ECUDA;
+    } else {
+        const dim3 grid(1, 1, 1);
+        cudaError_t e;
+        switch (l->mode) {
+            case KVD_F32: e = split_layer_f32(l->hd, 1, a, s, grid, st); break;
+            case KVD_Q8: e = split_layer_q8(l->hd, 1, a, s, grid, st); break;
+            case KVD_Q8K: e = split_layer_q8k(l->hd, 1, a, s, grid, st); break;
+            default: e = split_layer_q8v(l->hd, 1, a, s, grid, st); break;
+        }
+        if (e != cudaSuccess) return KVD_ECUDA;
+    }
+    return KVD_OK;
+}
+
 // ------------------------------------------------------------ verify
 
 extern "C" kvd_status kvd_verify_workspace_bytes(const kvd_layer *L, int32_t n_q, int32_t K,

@@ -102,6 +102,10 @@ inline const Layer *as_layer(const kvd_layer *L) { return reinterpret_cast<const
 const Layer *checked_layer(const kvd_layer *L);
 Layer *checked_layer(kvd_layer *L);
 
+// The append and freeze halves of kvd_bounds_selftest (kvd_append.cu).
+cudaError_t append_bounds_selftest(const Layer *l, const float *zeros, int32_t *seq_len, int32_t *frozen,
+                                   cudaStream_t s);
+
 inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
 
 // ---------------------------------------------------------------- PTX helpers

@@ -117,6 +117,8 @@ def test_layer_calls_reject_uninitialised_descriptor(abi):
     assert L.kv_append(C.byref(lay), C.c_void_p(16), C.c_void_p(16), None, None) == abi.EINVAL
     assert L.kv_freeze_colfield(C.byref(lay), None) == abi.EINVAL
     assert L.kvd_wait_timeout_selftest(C.byref(lay), 1000, None) == abi.EINVAL
+    assert L.kvd_bounds_selftest_bytes(C.byref(lay), C.byref(n)) == abi.EINVAL
+    assert L.kvd_bounds_selftest(C.byref(lay), C.c_void_p(256), 1 << 20, None) == abi.EINVAL
     assert L.kvd_status_string(abi.ECAPACITY) == b"capacity exceeded"
 
 

@@ -250,6 +250,33 @@ def test_bounded_wait_times_out_and_context_stays_usable(torch, kvd):
     _decode_case(torch, kvd, MODES["q8"], 128, 4, lengths, alive, seed=5)
 
 
+@pytest.mark.parametrize("mode,hd", [("q8", 128), ("q8k", 128), ("q8v", 64), ("f32", 64)])
+def test_metadata_guards_set_bit1_and_touch_nothing(torch, kvd, mode, hd):
+    """The append, freeze and decode-split guards run on lengths one row past
+    a capacity (kvd_bounds_selftest; q8 at head_dim 128 takes the tensor-core
+    split, the others the CUDA-core one): the device error word reads bit 1
+    alone, every storage byte and every length is unchanged, and the same
+    context then decodes at parity with a clean word."""
+    lengths = [100, 37]
+    alive = np.array([1, 1], np.uint8)
+    layer = _layer(kvd, MODES[mode], lengths, 2, hd, alive, cap_extra=3)
+    ks, vs = seq_rows(lengths, 2, hd, seed=8)
+    gpu_append_bulk(layer, ks, vs, torch)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    before = [b.clone() if b is not None else None for b in layer.bufs]
+    scratch = layer.bounds_selftest()
+    torch.cuda.synchronize()
+    del scratch
+    assert layer.device_error(clear=True) == 2  # bit 1 only: metadata out of range
+    for a, b in zip(before, layer.bufs):
+        if a is not None:
+            assert torch.equal(a, b)
+    assert [layer.seq_len(b) for b in range(2)] == lengths
+    _decode_case(torch, kvd, MODES[mode], hd, 4, lengths, alive, seed=8)
+    assert layer.device_error() == 0
+
+
 def test_all_groups_dead_and_capacity_errors(torch, kvd):
     layer = kvd.LayerKvCache(2, 2, 128, "q8", [8, 8], alive=[0, 0])
     k = torch.randn(2, 2, 128, device="cuda")
