@@ -336,6 +336,7 @@ using namespace kvd;
 
 extern "C" kvd_status kv_append(kvd_layer *L, const float *k, const float *v, const int32_t *n_new,
                                 void *stream) {
+    KVD_NVTX_RANGE("kv_append");
     Layer *l = checked_layer(L);
     if (l == nullptr || k == nullptr || v == nullptr) return KVD_EINVAL;
     if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15) return KVD_EINVAL;
@@ -425,6 +426,7 @@ extern "C" kvd_status kv_append(kvd_layer *L, const float *k, const float *v, co
 }
 
 extern "C" kvd_status kv_freeze_colfield(kvd_layer *L, void *stream) {
+    KVD_NVTX_RANGE("kv_freeze_colfield");
     Layer *l = checked_layer(L);
     if (l == nullptr) return KVD_EINVAL;
     std::vector<uint8_t> todo(l->n_seq, 0);

@@ -877,6 +877,7 @@ extern "C" kvd_status kvd_decode_workspace_bytes(const kvd_layer *L, int32_t n_q
 extern "C" kvd_status decode_attention(const float *q, const kvd_layer *L, int32_t n_q, float scale,
                                        float *out, float *imp, void *workspace,
                                        int64_t workspace_bytes, void *stream) {
+    KVD_NVTX_RANGE("decode_attention");
     return decode_attention_ex(q, L, n_q, scale, 0, 0.0f, nullptr, out, imp, workspace, workspace_bytes,
                                stream);
 }
@@ -885,6 +886,7 @@ extern "C" kvd_status decode_attention_ex(const float *q, const kvd_layer *L, in
                                           int64_t window, float softcap, const float *sinks, float *out,
                                           float *imp, void *workspace, int64_t workspace_bytes,
                                           void *stream) {
+    KVD_NVTX_RANGE("decode_attention_ex");
     const Layer *l = checked_layer(L);
     if (l == nullptr || q == nullptr || out == nullptr) return KVD_EINVAL;
     if (n_q < l->n_kv || n_q % l->n_kv != 0 || n_q / l->n_kv > kMaxHpk) return KVD_EINVAL;
@@ -1078,6 +1080,7 @@ extern "C" kvd_status kvd_bounds_selftest_bytes(const kvd_layer *L, int64_t *byt
 
 extern "C" kvd_status kvd_bounds_selftest(const kvd_layer *L, void *scratch, int64_t scratch_bytes,
                                           void *stream) {
+    KVD_NVTX_RANGE("kvd_bounds_selftest");
     const Layer *l = checked_layer(L);
     if (l == nullptr || scratch == nullptr || l->n_seq < 1 || l->n_live < 1) return KVD_EINVAL;
     if (l->h_cap[0] >= (int64_t(1) << 31) - 1) return KVD_EINVAL;
@@ -1170,6 +1173,7 @@ extern "C" kvd_status decode_attention_verify(const float *q, const kvd_layer *L
                                               float scale, int64_t window, float softcap, const float *sinks,
                                               float *out, void *workspace, int64_t workspace_bytes,
                                               void *stream) {
+    KVD_NVTX_RANGE("decode_attention_verify");
     const Layer *l = checked_layer(L);
     if (l == nullptr || q == nullptr || out == nullptr || K < 1) return KVD_EINVAL;
     if (n_q < l->n_kv || n_q % l->n_kv != 0 || int64_t(n_q / l->n_kv) * K > kMaxHpk) return KVD_EINVAL;
@@ -1353,6 +1357,7 @@ extern "C" kvd_status rswa_record_prefill(float *ref_k, float *ref_v, const floa
                                           int32_t H, int32_t head_dim, int64_t ref_cap, int32_t W,
                                           int32_t *prefill_len, int32_t *ring_len,
                                           int32_t *ring_pos, rswa_history *hist, void *stream) {
+    KVD_NVTX_RANGE("rswa_record_prefill");
     return record_prefill(ref_k, ref_v, nullptr, k, v, s, seq, B, H, head_dim, ref_cap, W,
                           prefill_len, ring_len, ring_pos, hist, stream);
 }
@@ -1362,6 +1367,7 @@ extern "C" kvd_status rswa_record_prefill_i8(float *ref_k, float *ref_v, const r
                                              int32_t B, int32_t H, int32_t head_dim, int64_t ref_cap,
                                              int32_t W, int32_t *prefill_len, int32_t *ring_len,
                                              int32_t *ring_pos, rswa_history *hist, void *stream) {
+    KVD_NVTX_RANGE("rswa_record_prefill_i8");
     if (m == nullptr) return KVD_EINVAL;
     return record_prefill(ref_k, ref_v, m, k, v, s, seq, B, H, head_dim, ref_cap, W, prefill_len,
                           ring_len, ring_pos, hist, stream);
@@ -1425,6 +1431,7 @@ extern "C" kvd_status rswa_ring_write(float *ring_k, float *ring_v, const float 
                                       const int32_t *prefill_len, int32_t *ring_len,
                                       int32_t *ring_pos, rswa_history *hist, int32_t B, int32_t H,
                                       int32_t head_dim, int32_t W, int32_t *slot_out, void *stream) {
+    KVD_NVTX_RANGE("rswa_ring_write");
     return ring_write(ring_k, ring_v, nullptr, k, v, prefill_len, ring_len, ring_pos, hist, B, H,
                       head_dim, W, slot_out, stream);
 }
@@ -1434,6 +1441,7 @@ extern "C" kvd_status rswa_ring_write_i8(float *ring_k, float *ring_v, const rsw
                                          int32_t *ring_len, int32_t *ring_pos, rswa_history *hist,
                                          int32_t B, int32_t H, int32_t head_dim, int32_t W,
                                          int32_t *slot_out, void *stream) {
+    KVD_NVTX_RANGE("rswa_ring_write_i8");
     if (m == nullptr) return KVD_EINVAL;
     return ring_write(ring_k, ring_v, m, k, v, prefill_len, ring_len, ring_pos, hist, B, H, head_dim,
                       W, slot_out, stream);
@@ -1574,6 +1582,7 @@ extern "C" kvd_status rswa_decode(const float *q, const float *ref_k, const floa
                                   const int32_t *ring_pos, int32_t B, int32_t H, int32_t head_dim,
                                   int64_t ref_cap, int32_t W, float scale, float *out,
                                   void *workspace, int64_t workspace_bytes, void *stream) {
+    KVD_NVTX_RANGE("rswa_decode");
     if (ref_k == nullptr || ref_v == nullptr || ring_k == nullptr || ring_v == nullptr ||
         !aligned16(ref_k) || !aligned16(ref_v) || !aligned16(ring_k) || !aligned16(ring_v))
         return KVD_EINVAL;
@@ -1591,6 +1600,7 @@ extern "C" kvd_status rswa_decode_i8(const float *q, const rswa_i8_mirror *m,
                                      const int32_t *ring_pos, int32_t B, int32_t H, int32_t head_dim,
                                      int64_t ref_cap, int32_t W, float scale, float *out,
                                      void *workspace, int64_t workspace_bytes, void *stream) {
+    KVD_NVTX_RANGE("rswa_decode_i8");
     if (!mirror_ok(m)) return KVD_EINVAL;
     RswaSrc src{};
     src.ref_k8 = m->ref_k;
@@ -1794,6 +1804,7 @@ extern "C" kvd_status rswa_verify(const float *q, const float *draft_k, const fl
                                   const int32_t *ring_pos, int32_t B, int32_t H, int32_t head_dim,
                                   int64_t ref_cap, int32_t W, float scale, float *out, void *workspace,
                                   int64_t workspace_bytes, void *stream) {
+    KVD_NVTX_RANGE("rswa_verify");
     if (ref_k == nullptr || ref_v == nullptr || ring_k == nullptr || ring_v == nullptr ||
         !aligned16(ref_k) || !aligned16(ref_v) || !aligned16(ring_k) || !aligned16(ring_v))
         return KVD_EINVAL;
@@ -1811,6 +1822,7 @@ extern "C" kvd_status rswa_verify_i8(const float *q, const float *draft_k, const
                                      const int32_t *ring_len, const int32_t *ring_pos, int32_t B, int32_t H,
                                      int32_t head_dim, int64_t ref_cap, int32_t W, float scale, float *out,
                                      void *workspace, int64_t workspace_bytes, void *stream) {
+    KVD_NVTX_RANGE("rswa_verify_i8");
     if (!mirror_ok(m)) return KVD_EINVAL;
     RswaSrc src{};
     src.ref_k8 = m->ref_k;

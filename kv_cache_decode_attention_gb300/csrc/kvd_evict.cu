@@ -625,6 +625,7 @@ extern "C" kvd_status kv_evict_workspace_bytes(const kvd_layer *L, int64_t keep_
 extern "C" kvd_status kv_evict_born(kvd_layer *L, float *imp, int64_t keep_last, int32_t sink,
                                     int32_t recent, void *workspace, int64_t workspace_bytes,
                                     void *stream) {
+    KVD_NVTX_RANGE("kv_evict_born");
     Layer *l = checked_layer(L);
     if (l == nullptr || imp == nullptr || (reinterpret_cast<uintptr_t>(imp) & 3)) return KVD_EINVAL;
     if (keep_last < 0 || keep_last > (int64_t(1) << 31) - 1 || sink < 0 || recent < 0) return KVD_EINVAL;
@@ -748,6 +749,7 @@ extern "C" kvd_status kv_evict_born(kvd_layer *L, float *imp, int64_t keep_last,
 }
 
 extern "C" kvd_status kv_truncate_last(kvd_layer *L, const int32_t *n_drop, float *imp, void *stream) {
+    KVD_NVTX_RANGE("kv_truncate_last");
     Layer *l = checked_layer(L);
     if (l == nullptr || (reinterpret_cast<uintptr_t>(imp) & 3)) return KVD_EINVAL;
     for (int b = 0; b < l->n_seq; ++b)

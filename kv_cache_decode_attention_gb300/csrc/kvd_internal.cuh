@@ -9,6 +9,8 @@
 #include <stdint.h>
 
 #include <atomic>
+
+#include <nvtx3/nvToolsExt.h>
 #include <mutex>
 #include <utility>
 #include <vector>
@@ -99,6 +101,17 @@ constexpr int32_t kLayerMagic = 0x4b564431;  // "KVD1"
 
 inline Layer *as_layer(kvd_layer *L) { return reinterpret_cast<Layer *>(L); }
 inline const Layer *as_layer(const kvd_layer *L) { return reinterpret_cast<const Layer *>(L); }
+// An NVTX range named for the entry point around each call that launches work,
+// so profilers can attribute kernels to calls (header-only NVTX: a pointer
+// check when no tool is attached).
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
+#define KVD_NVTX_RANGE(name) const ::kvd::NvtxRange kvd_nvtx_range_(name)
+
 const Layer *checked_layer(const kvd_layer *L);
 Layer *checked_layer(kvd_layer *L);
 

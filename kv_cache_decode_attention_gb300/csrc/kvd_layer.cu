@@ -288,6 +288,7 @@ extern "C" kvd_status kvd_layer_init(kvd_layer *L, int32_t n_seq, int32_t n_kv, 
 }
 
 extern "C" kvd_status kvd_layer_reset(kvd_layer *L, int32_t seq, void *stream) {
+    KVD_NVTX_RANGE("kvd_layer_reset");
     Layer *l = checked_layer(L);
     if (l == nullptr || seq < -1 || seq >= l->n_seq) return KVD_EINVAL;
     const int32_t seq0 = seq < 0 ? 0 : seq, n = seq < 0 ? l->n_seq : 1;

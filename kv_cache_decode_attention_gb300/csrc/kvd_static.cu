@@ -101,6 +101,7 @@ using namespace kvd;
 
 extern "C" kvd_status decode_attention_static(const float *q, const kvd_layer *L, int32_t n_q,
                                               float scale, float *out, void *stream) {
+    KVD_NVTX_RANGE("decode_attention_static");
     const Layer *l = checked_layer(L);
     if (l == nullptr || q == nullptr || out == nullptr) return KVD_EINVAL;
     if (n_q < l->n_kv || n_q % l->n_kv != 0 || n_q / l->n_kv > kMaxHpk) return KVD_EINVAL;
