@@ -72,20 +72,20 @@ CSRC_CUDA_CORE = CSRC_COMMON + ("kvd_decode_kernels.cuh", "kvd_split_f32.cu", "k
 CSRC_TC = CSRC_COMMON + ("kvd_decode_kernels.cuh", "kvd_split_mma.cuh", "kvd_split_h16.cuh", "kvd_split_q8.cu")
 TRAFFIC = {
     # q8_gqa (--steps 20 --warmup 5): the first two calls of the roofline loop
-    "q8_gqa": {"files": CSRC_TC, "sources_sha256": "ac5f99cf2411775dfd376fa02c024d5e04929e7bd3f75f28c7a6c10568d8662b",
-               "bytes": 300940288, "algorithmic_bytes": 291954176},
+    "q8_gqa": {"files": CSRC_TC, "sources_sha256": "9af7d0aafcc69837b27d6875bd2f3de87a29105e02b53d479939617aa50d907e",
+               "bytes": 300552576, "algorithmic_bytes": 291954176},
     # long_q8 (--steps 5 --warmup 3): the first two calls of the roofline loop
-    "long_q8": {"files": CSRC_TC, "sources_sha256": "ac5f99cf2411775dfd376fa02c024d5e04929e7bd3f75f28c7a6c10568d8662b",
-                "bytes": 609331968, "algorithmic_bytes": 579149888},
+    "long_q8": {"files": CSRC_TC, "sources_sha256": "9af7d0aafcc69837b27d6875bd2f3de87a29105e02b53d479939617aa50d907e",
+                "bytes": 609561088, "algorithmic_bytes": 579149888},
     # the first 16 sequences of the ragged batch, 3 + 3 steps in, mean of 10 calls
-    "ragged_f32": {"files": CSRC_CUDA_CORE, "sources_sha256": "ed4ede5c7b63d3c498d8e0d06eeeac3b8a6eab582212b3643da829b521611cfc",
-                   "bytes": 944696576, "algorithmic_bytes": 939376640},
-    "ragged_q8": {"files": CSRC_TC, "sources_sha256": "ac5f99cf2411775dfd376fa02c024d5e04929e7bd3f75f28c7a6c10568d8662b",
-                  "bytes": 259220429, "algorithmic_bytes": 253672640},
-    "ragged_q8k": {"files": CSRC_CUDA_CORE, "sources_sha256": "ed4ede5c7b63d3c498d8e0d06eeeac3b8a6eab582212b3643da829b521611cfc",
-                   "bytes": 606740762, "algorithmic_bytes": 602025728},
-    "ragged_q8v": {"files": CSRC_CUDA_CORE, "sources_sha256": "ed4ede5c7b63d3c498d8e0d06eeeac3b8a6eab582212b3643da829b521611cfc",
-                   "bytes": 595761024, "algorithmic_bytes": 591023552},
+    "ragged_f32": {"files": CSRC_CUDA_CORE, "sources_sha256": "f4a882943a7a7c529c7b9734d27e061751fe904afe4ad531d73855d01ab93e16",
+                   "bytes": 944721178, "algorithmic_bytes": 939376640},
+    "ragged_q8": {"files": CSRC_TC, "sources_sha256": "9af7d0aafcc69837b27d6875bd2f3de87a29105e02b53d479939617aa50d907e",
+                  "bytes": 259236506, "algorithmic_bytes": 253672640},
+    "ragged_q8k": {"files": CSRC_CUDA_CORE, "sources_sha256": "f4a882943a7a7c529c7b9734d27e061751fe904afe4ad531d73855d01ab93e16",
+                   "bytes": 606727347, "algorithmic_bytes": 602025728},
+    "ragged_q8v": {"files": CSRC_CUDA_CORE, "sources_sha256": "f4a882943a7a7c529c7b9734d27e061751fe904afe4ad531d73855d01ab93e16",
+                   "bytes": 595746355, "algorithmic_bytes": 591023552},
 }
 
 
