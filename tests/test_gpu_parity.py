@@ -141,7 +141,7 @@ def _decode_case(torch, kvd, mode, hd, hpk, lengths, alive, seed, with_imp=True,
 
 
 @pytest.mark.parametrize("mode", list(MODES))
-@pytest.mark.parametrize("hpk", [1, 2, 3, 4, 8, 12, 16])
+@pytest.mark.parametrize("hpk", [1, 2, 3, 4, 5, 6, 7, 8, 9, 12, 13, 16])
 def test_decode_parity_hd128(torch, kvd, mode, hpk):
     _decode_case(torch, kvd, MODES[mode], 128, hpk, [0, 1, 64, 300, 777, 1030],
                  np.array([1, 1, 0, 1], np.uint8), seed=11 + hpk)
@@ -170,7 +170,7 @@ def test_decode_q8_merge_paths(torch, kvd, hpk, longest):
 
 
 @pytest.mark.parametrize("mode", list(MODES))
-@pytest.mark.parametrize("hpk", [2, 8])
+@pytest.mark.parametrize("hpk", [2, 5, 8, 16])
 def test_decode_parity_hd64(torch, kvd, mode, hpk):
     _decode_case(torch, kvd, MODES[mode], 64, hpk, [5, 257, 600], np.array([0, 1, 1], np.uint8),
                  seed=21 + hpk)
