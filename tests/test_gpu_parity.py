@@ -147,6 +147,15 @@ def test_decode_parity_hd128(torch, kvd, mode, hpk):
                  np.array([1, 1, 0, 1], np.uint8), seed=11 + hpk)
 
 
+# More sequences than one launch describes (appends, freezes and the
+# tensor-core tables go in slices of 256): every sequence against the oracle,
+# storage bit-exact, on the tensor-core path (q8) and the CUDA-core one (q8k).
+@pytest.mark.parametrize("mode", ["q8", "q8k"])
+def test_decode_parity_over_two_launch_slices(torch, kvd, mode):
+    lengths = [int(x) for x in synthetic.rng(97).integers(0, 180, 300)]
+    _decode_case(torch, kvd, MODES[mode], 128, 4, lengths, np.array([1, 0, 1], np.uint8), seed=97)
+
+
 # The tensor-core kernels compile the imp score stores out when the call has no
 # imp: each of those variants (heads in N with packed or chained query terms,
 # heads in M), the benchmark's roofline kernel among them.
