@@ -22,7 +22,9 @@ tiny_f32, verify_q8 (4 drafts verified per step), and the R-SWA decode of
 franken_ocr's rswa module (16 streams x 10 heads, a 32640-row reference block
 + a full 128-slot ring): rswa reads the f32 regions, rswa_i8 the int8 mirror;
 one step = the ring write of one token per stream (mirror included) + the
-decode of every stream; rswa_verify / rswa_i8_verify verify 4 drafts.
+decode of every stream; rswa_verify / rswa_i8_verify verify 4 drafts.  The
+q8_2f GQA lines also carry the decode against the tensor-core peak
+(roofline_tensor), the second roof at 16 heads per group.
 
 Under torchrun each rank times its own replica on its own GPU (independent
 sequences: weak scaling, no data-path collective); rank 0 prints one JSON line
