@@ -1340,6 +1340,19 @@ def run_gpu(args, rank, world):
     imp_bytes = statistics.mean(
         decode_bytes(wls[j % R].mode, n_live, wl0.hd, wl0.n_q, lens_now[j % R], True, wl0.n_seq)
         for j in range(nrep))
+    # decode_attention_static (no workspace: the library's scratch array, the
+    # CUDA-core split kernel) on the same calls, where its partials fit
+    static_ms = None
+    try:
+        for j in range(nrep):
+            w = wls[j % R]
+            dev_ev[j][0].record(stream)
+            kvd.decode_attention_static(qs[j % 8], w.layer, out=outs[j % R], scale=w.scale)
+            dev_ev[j][1].record(stream)
+        torch.cuda.synchronize()
+        static_ms = statistics.mean(a.elapsed_time(b) for a, b in dev_ev)
+    except kvd.KvdError:
+        torch.cuda.synchronize()
     peak, peak_kind = peaks()
     achieved = kbytes / (k_ms * 1e-3) / 1e9
     tpeak, tpeak_kind = tensor_peak()
@@ -1432,7 +1445,12 @@ def run_gpu(args, rank, world):
                      "bytes_per_launch": int(kbytes),
                      "imp_on": {"ms_per_launch": round(imp_ms, 5), "bytes_per_launch": int(imp_bytes),
                                 "achieved": round(imp_bytes / (imp_ms * 1e-3) / 1e9, 1),
-                                "frac": round(imp_bytes / (imp_ms * 1e-3) / 1e9 / peak, 4)}},
+                                "frac": round(imp_bytes / (imp_ms * 1e-3) / 1e9 / peak, 4)},
+                     "static": None if static_ms is None else
+                     {"kernel": "decode_attention_static (CUDA-core split + merge, no workspace)",
+                      "ms_per_launch": round(static_ms, 5), "bytes_per_launch": int(kbytes),
+                      "achieved": round(kbytes / (static_ms * 1e-3) / 1e9, 1),
+                      "frac": round(kbytes / (static_ms * 1e-3) / 1e9 / peak, 4)}},
         # the second roof: the same decode call against the tensor peak (the
         # q8_2f kernels run each contraction twice, one f16 term each)
         "roofline_tensor": {"bound": "tensor", "achieved": round(kflops / (k_ms * 1e-3) / 1e12, 2),
